@@ -1,0 +1,129 @@
+"""Seeded synthetic inputs for the two products, shared by the tests, the
+smoke check and the benchmark.
+
+This module only draws numbers: it holds none of the products' arithmetic and
+imports neither the CUDA library nor the oracle.  Every tensor is produced on
+the CPU from a ``torch.Generator`` seeded explicitly, so the oracle and the
+GPU path always consume the very same host arrays.
+
+The five named workloads follow the pages' own test and benchmark shapes:
+
+* SGEMM 256³ with A from seed 1 and B from seed 2, values uniform in [-1, 1]
+  (the correctness size of the host harness in "异步拷贝与 Hopper/Blackwell
+  新特性", section "cp.async 与多级流水 sm_80+"), 1024³, and the 4096³
+  benchmark size of the same harness, here with alpha = 1, beta = 0.5 and a
+  C drawn from seed 3.
+* fp16 NT 5376 × 5376 × 2048, uniform [-1, 1] rounded to half (the problem of
+  "从零开始的 AI Infra: 算子基础与GPU架构", section "背景与分析").
+* fp16 NT 5000 × 5376 × 2040, normal(0, 1) rounded to half, seeds 4 and 5:
+  the same problem with M and K off the tile grid, to exercise the tails.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    form: str            # "sgemm" or "f16_nt"
+    M: int
+    N: int
+    K: int
+    dist: str            # "uniform" (in [-1, 1]) or "normal" (mean 0, sd 1)
+    seed_a: int
+    seed_b: int
+    seed_c: Optional[int] = None
+    alpha: float = 1.0
+    beta: float = 0.0
+
+    @property
+    def flop(self) -> int:
+        """2·M·N·K, the operation count both pages use for throughput."""
+        return 2 * self.M * self.N * self.K
+
+
+WORKLOADS = {
+    w.name: w
+    for w in [
+        Workload("sgemm_256", "sgemm", 256, 256, 256, "uniform", 1, 2),
+        Workload("sgemm_1024", "sgemm", 1024, 1024, 1024, "uniform", 1, 2),
+        Workload("sgemm_4096", "sgemm", 4096, 4096, 4096, "uniform", 1, 2, 3, 1.0, 0.5),
+        Workload("f16_nt_5376x5376x2048", "f16_nt", 5376, 5376, 2048, "uniform", 1, 2),
+        Workload("f16_nt_5000x5376x2040", "f16_nt", 5000, 5376, 2040, "normal", 4, 5),
+    ]
+}
+
+# The throughput workload: the fp16 NT problem the pages tune.
+HEADLINE = "f16_nt_5376x5376x2048"
+
+
+def _gen(seed: int) -> torch.Generator:
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    return g
+
+
+def draw_f32(shape, seed: int, dist: str = "uniform") -> torch.Tensor:
+    """A float32 CPU tensor: uniform in [-1, 1] or standard normal."""
+    g = _gen(seed)
+    if dist == "uniform":
+        return torch.rand(tuple(shape), generator=g, dtype=torch.float32) * 2.0 - 1.0
+    if dist == "normal":
+        return torch.randn(tuple(shape), generator=g, dtype=torch.float32)
+    raise ValueError(f"unknown distribution {dist!r}")
+
+
+def draw_f16(shape, seed: int, dist: str = "uniform") -> torch.Tensor:
+    """A half CPU tensor: the float32 draw rounded to nearest half."""
+    return draw_f32(shape, seed, dist).to(torch.float16)
+
+
+def draw_int(shape, seed: int, lo: int, hi: int, dtype=torch.float32) -> torch.Tensor:
+    """Integer values in [lo, hi] stored in a float dtype (exact products)."""
+    g = _gen(seed)
+    return torch.randint(lo, hi + 1, tuple(shape), generator=g, dtype=torch.int64).to(dtype)
+
+
+def make_inputs(w: Workload):
+    """Host tensors (A, B, C0) of a workload; C0 is None when beta == 0."""
+    if w.form == "f16_nt":
+        A = draw_f16((w.M, w.K), w.seed_a, w.dist)
+        B = draw_f16((w.N, w.K), w.seed_b, w.dist)
+        return A, B, None
+    if w.form == "sgemm":
+        A = draw_f32((w.M, w.K), w.seed_a, w.dist)
+        B = draw_f32((w.K, w.N), w.seed_b, w.dist)
+        C0 = None
+        if w.seed_c is not None:
+            C0 = draw_f32((w.M, w.N), w.seed_c, w.dist)
+        return A, B, C0
+    raise ValueError(f"unknown form {w.form!r}")
+
+
+def sample_positions(M: int, N: int, count: int, seed: int, tail_rows=None):
+    """Seeded output positions for a sampled comparison.
+
+    ``count`` distinct (row, col) pairs drawn without replacement from M×N,
+    plus forced coverage: the four corners, every element of the last row and
+    of the last column, and every column of each row in ``tail_rows``.
+    Returns two int64 numpy arrays (rows, cols) without duplicates."""
+    import numpy as np
+
+    total = M * N
+    rng = np.random.default_rng(seed)
+    count = min(count, total)
+    flat = rng.choice(total, size=count, replace=False) if count else np.zeros(0, np.int64)
+    extra = []
+    if M and N:
+        extra += [0, N - 1, (M - 1) * N, (M - 1) * N + N - 1]
+        extra += list((M - 1) * N + np.arange(N))          # last row
+        extra += list(np.arange(M) * N + (N - 1))          # last column
+        for r in tail_rows or []:
+            if 0 <= r < M:
+                extra += list(r * N + np.arange(N))
+    flat = np.unique(np.concatenate([flat.astype(np.int64), np.asarray(extra, dtype=np.int64)]))
+    return (flat // N).astype(np.int64), (flat % N).astype(np.int64)

@@ -1,0 +1,266 @@
+/*
+ * gemm_oracle.c -- the parity oracle for the two dense matrix products.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path (the CUDA library
+ * and its Python binding) may include, link, load or call this file.  Only
+ * the test suite, the smoke check and the benchmark's CPU-baseline leg use it.
+ * It shares no code, header, table or helper with the CUDA path.
+ *
+ * What it computes is the plain definition of each product, written out as
+ * nested loops with one float64 accumulator per output element, summed in
+ * ascending k.  There is no blocking, no reordering of the sum and no fusion;
+ * the only preparation steps are exact conversions of the inputs to double
+ * (half -> double and float -> double are both exact) and, for the SGEMM,
+ * a copy of B into k-contiguous order so that each dot product walks memory
+ * linearly.  Neither step changes a single rounding.
+ *
+ * Sources (the pages the method is taken from):
+ *  - fp16 NT product: "从零开始的 AI Infra: 算子基础与GPU架构"
+ *    (qi-zhan.github.io/blog/2026/cuda-gemm), section "0. Naive
+ *    Implementation": C[m][n] = sum_k float(A[m*K+k]) * float(B[n*K+k]),
+ *    stored as half(acc); and section "19. 去掉转置" for the reading of
+ *    B[N,K] row-major as the transposed right operand.
+ *  - fp32 SGEMM: "异步拷贝与 Hopper/Blackwell 新特性"
+ *    (anrans.github.io/ai-infra-handbooks/cuda/advanced/async-hopper),
+ *    section "cp.async 与多级流水 sm_80+", the gemm_cp_async listing's
+ *    epilogue c = alpha*acc + beta*c over row-major A[M,K], B[K,N], C[M,N],
+ *    and the CPU reference loop of its host harness.
+ *
+ * Precision: the pages accumulate in float; this oracle accumulates in
+ * float64 and keeps the result unrounded, so that the GPU result can be
+ * judged against the exact-ish value with a tolerance scaled by
+ * S[i][j] = |alpha| * sum_k |A[i][k] * B'[k][j]|, which is also returned.
+ *
+ * Build: plain C99 + OpenMP, no fast-math, no FP contraction:
+ *   gcc -O2 -std=c99 -fopenmp -ffp-contract=off -fPIC -shared
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ---------------------------------------------------------------------- */
+/* IEEE 754 binary16, from its definition: 1 sign bit, 5 exponent bits     */
+/* with bias 15, 10 fraction bits; exponent 0 = zero/subnormal, 31 = inf or */
+/* NaN.                                                                     */
+/* ---------------------------------------------------------------------- */
+
+double oracle_half_to_f64(uint16_t h)
+{
+    const int sign = (h >> 15) & 1;
+    const int expo = (h >> 10) & 0x1f;
+    const int frac = h & 0x3ff;
+    double v;
+    if (expo == 0) {
+        v = ldexp((double)frac, -24);              /* 2^-14 * frac/2^10 */
+    } else if (expo == 31) {
+        v = frac ? NAN : INFINITY;
+    } else {
+        v = ldexp((double)(1024 + frac), expo - 25); /* 2^(e-15) * (1024+f)/2^10 */
+    }
+    return sign ? -v : v;
+}
+
+/* Round-to-nearest-even of a double to binary16, returned as its bits.
+ * Values at or beyond 65520 (the midpoint between the largest finite half,
+ * 65504, and 2^16) round to infinity. */
+uint16_t oracle_f64_to_half_rn(double x)
+{
+    if (isnan(x)) return (uint16_t)0x7e00;
+    const uint16_t sign = signbit(x) ? 0x8000 : 0;
+    const double a = fabs(x);
+    if (a >= 65520.0) return (uint16_t)(sign | 0x7c00);
+    if (a < ldexp(1.0, -14)) {
+        /* subnormal range: multiples of 2^-24; 1024 * 2^-24 is the smallest
+         * normal, whose encoding 0x0400 is also the integer 1024. */
+        const double n = nearbyint(ldexp(a, 24));   /* ties to even */
+        return (uint16_t)(sign | (uint16_t)n);
+    }
+    int ex;
+    (void)frexp(a, &ex);             /* a = m * 2^ex, m in [0.5, 1) */
+    int E = ex - 1;                  /* a in [2^E, 2^(E+1)) */
+    double r = nearbyint(ldexp(a, 10 - E));   /* in [1024, 2048] */
+    if (r >= 2048.0) { r = 1024.0; E += 1; }
+    if (E + 15 >= 31) return (uint16_t)(sign | 0x7c00);
+    return (uint16_t)(sign | (uint16_t)((E + 15) << 10) | (uint16_t)(r - 1024.0));
+}
+
+void oracle_half_to_f64_array(int64_t n, const uint16_t *h, double *out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_half_to_f64(h[i]);
+}
+
+void oracle_f64_to_half_rn_array(int64_t n, const double *x, uint16_t *out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_f64_to_half_rn(x[i]);
+}
+
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* ---------------------------------------------------------------------- */
+/* fp16 NT: C[i][j] = sum_{k<K} A[i][k] * B[j][k]                           */
+/*   A: half [M,K] row-major, B: half [N,K] row-major (= B^T [K,N]          */
+/*   column-major), C, S: double [M,N] row-major.  S may be NULL.           */
+/* ---------------------------------------------------------------------- */
+
+static double *decode_half_matrix(int64_t rows, int64_t cols, const uint16_t *h)
+{
+    const int64_t n = rows * cols;
+    double *d = (double *)malloc((size_t)(n > 0 ? n : 1) * sizeof(double));
+    if (!d) return NULL;
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) d[i] = oracle_half_to_f64(h[i]);
+    return d;
+}
+
+static void dot_nt(const double *a_row, const double *b_row, int64_t K,
+                   double *acc_out, double *mag_out)
+{
+    double acc = 0.0, mag = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+        const double p = a_row[k] * b_row[k];  /* exact: 11 x 11 bit significands */
+        acc += p;
+        mag += fabs(p);
+    }
+    *acc_out = acc;
+    *mag_out = mag;
+}
+
+int oracle_gemm_f16_nt(int64_t M, int64_t N, int64_t K,
+                       const uint16_t *A, const uint16_t *B,
+                       double *C, double *S)
+{
+    if (M < 0 || N < 0 || K < 0) return -1;
+    if (M == 0 || N == 0) return 0;
+    double *a = decode_half_matrix(M, K, A);
+    double *b = decode_half_matrix(N, K, B);
+    if (!a || !b) { free(a); free(b); return -2; }
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < M; ++i) {
+        for (int64_t j = 0; j < N; ++j) {
+            double acc, mag;
+            dot_nt(a + i * K, b + j * K, K, &acc, &mag);
+            C[i * N + j] = acc;
+            if (S) S[i * N + j] = mag;
+        }
+    }
+    free(a);
+    free(b);
+    return 0;
+}
+
+/* The same product at n listed positions (rows[t], cols[t]) only. */
+int oracle_gemm_f16_nt_sampled(int64_t M, int64_t N, int64_t K,
+                               const uint16_t *A, const uint16_t *B,
+                               int64_t n, const int64_t *rows, const int64_t *cols,
+                               double *C, double *S)
+{
+    if (M < 0 || N < 0 || K < 0 || n < 0) return -1;
+    for (int64_t t = 0; t < n; ++t)
+        if (rows[t] < 0 || rows[t] >= M || cols[t] < 0 || cols[t] >= N) return -1;
+#pragma omp parallel
+    {
+        double *a = (double *)malloc((size_t)(K > 0 ? K : 1) * sizeof(double));
+        double *b = (double *)malloc((size_t)(K > 0 ? K : 1) * sizeof(double));
+#pragma omp for schedule(static)
+        for (int64_t t = 0; t < n; ++t) {
+            for (int64_t k = 0; k < K; ++k) {
+                a[k] = oracle_half_to_f64(A[rows[t] * K + k]);
+                b[k] = oracle_half_to_f64(B[cols[t] * K + k]);
+            }
+            double acc, mag;
+            dot_nt(a, b, K, &acc, &mag);
+            C[t] = acc;
+            if (S) S[t] = mag;
+        }
+        free(a);
+        free(b);
+    }
+    return 0;
+}
+
+/* ---------------------------------------------------------------------- */
+/* fp32 SGEMM: C[i][j] = alpha * sum_{k<K} A[i][k] * B[k][j] + beta * C0[i][j] */
+/*   A: float [M,K], B: float [K,N], C0: float [M,N], all row-major.        */
+/*   beta == 0 follows the BLAS convention: C0 is not read (may be NULL).   */
+/*   C, S: double [M,N].  S = |alpha| * sum_k |A[i][k] * B[k][j]|.          */
+/* ---------------------------------------------------------------------- */
+
+static void dot_sgemm(const float *a_row, const double *b_col, int64_t K,
+                      double *acc_out, double *mag_out)
+{
+    double acc = 0.0, mag = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+        const double p = (double)a_row[k] * b_col[k];  /* exact: 24 x 24 bits */
+        acc += p;
+        mag += fabs(p);
+    }
+    *acc_out = acc;
+    *mag_out = mag;
+}
+
+int oracle_sgemm(int64_t M, int64_t N, int64_t K, double alpha,
+                 const float *A, const float *B, double beta, const float *C0,
+                 double *C, double *S)
+{
+    if (M < 0 || N < 0 || K < 0) return -1;
+    if (M == 0 || N == 0) return 0;
+    if (beta != 0.0 && !C0) return -1;
+    /* B gathered column by column (bt[j*K + k] = B[k][j]); values unchanged. */
+    double *bt = (double *)malloc((size_t)(N * K > 0 ? N * K : 1) * sizeof(double));
+    if (!bt) return -2;
+#pragma omp parallel for schedule(static)
+    for (int64_t j = 0; j < N; ++j)
+        for (int64_t k = 0; k < K; ++k) bt[j * K + k] = (double)B[k * N + j];
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < M; ++i) {
+        for (int64_t j = 0; j < N; ++j) {
+            double acc, mag;
+            dot_sgemm(A + i * K, bt + j * K, K, &acc, &mag);
+            double c = alpha * acc;
+            if (beta != 0.0) c += beta * (double)C0[i * N + j];
+            C[i * N + j] = c;
+            if (S) S[i * N + j] = fabs(alpha) * mag;
+        }
+    }
+    free(bt);
+    return 0;
+}
+
+int oracle_sgemm_sampled(int64_t M, int64_t N, int64_t K, double alpha,
+                         const float *A, const float *B, double beta, const float *C0,
+                         int64_t n, const int64_t *rows, const int64_t *cols,
+                         double *C, double *S)
+{
+    if (M < 0 || N < 0 || K < 0 || n < 0) return -1;
+    if (beta != 0.0 && !C0) return -1;
+    for (int64_t t = 0; t < n; ++t)
+        if (rows[t] < 0 || rows[t] >= M || cols[t] < 0 || cols[t] >= N) return -1;
+#pragma omp parallel
+    {
+        double *b = (double *)malloc((size_t)(K > 0 ? K : 1) * sizeof(double));
+#pragma omp for schedule(static)
+        for (int64_t t = 0; t < n; ++t) {
+            const int64_t i = rows[t], j = cols[t];
+            for (int64_t k = 0; k < K; ++k) b[k] = (double)B[k * N + j];
+            double acc, mag;
+            dot_sgemm(A + i * K, b, K, &acc, &mag);
+            double c = alpha * acc;
+            if (beta != 0.0) c += beta * (double)C0[i * N + j];
+            C[t] = c;
+            if (S) S[t] = fabs(alpha) * mag;
+        }
+        free(b);
+    }
+    return 0;
+}
