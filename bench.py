@@ -1,0 +1,451 @@
+#!/usr/bin/env python3
+"""Throughput of the fp16 NT GEMM C = A·Bᵀ at 5376 × 5376 × 2048 on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step is one call of ``gemm_f16_nt`` (the whole path: host validation and
+tile selection, tensor-map encoding, the persistent tcgen05 kernel) on one
+batch of synthetic input.  W untimed warm-up steps, then exactly K timed steps
+bracketed by a barrier and ``torch.cuda.synchronize()``; the maximum over
+ranks is taken and rank 0 prints one JSON line.
+
+* ``value``: TFLOP/s = 2·M·N·K per step, summed over ranks, ÷ the timed region.
+  Inputs and outputs rotate over 4 resident copies (≈407 MB, more than the
+  126 MB L2), so no step finds its operands in L2 from the previous use.
+* ``roofline``: the GEMM kernel's average launch duration from CUDA events on
+  its own stream, against the measured dense bf16/fp16 tensor peak.
+* ``e2e``: the same metric through the C ABI with host buffers: each step
+  copies A and B from pinned host memory, runs the GEMM and copies C back.
+* ``cpu_baseline``: the float64 oracle on the host cores, on a bounded row
+  sample of the same product.
+* ``cublas``: torch.matmul(A, Bᵀ) (cuBLAS, fp32 accumulation) timed the same
+  way, as a reference line only.
+* ``sgemm``: the fp32 SGEMM at 4096³ (alpha 1, beta 0.5), a second line
+  against the FP32 FFMA peak.
+
+N > 1 runs N independent replicas (one per GPU; the product has no exchange
+step), ``scaling: weak``.  ``--impl reference`` times the float64 oracle on
+the host cores instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "TFLOP/s (2MNK/t) fp16 NT GEMM 5376x5376x2048 on 1 GB300; % of dense FP16 peak"
+ROTATE = 4
+FALLBACK_TENSOR_TFLOPS = 1900.0
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["dense_gemm_fp16_gb300/csrc/gemm_f16_nt.cu",
+                  "dense_gemm_fp16_gb300/csrc/sm103_ptx.cuh"]
+TRAFFIC_FILE = "profiles/gemm_f16_nt_5376x5376x2048_traffic.txt"
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas only)
+# ---------------------------------------------------------------------------
+
+def dist_setup(n_gpus):
+    import torch
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return rank, local, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# peaks, clocks, profile-derived traffic
+# ---------------------------------------------------------------------------
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return {"bf16_tflops": FALLBACK_TENSOR_TFLOPS, "hbm_gbs": FALLBACK_HBM_GBS,
+                "sm_max_mhz": 2070.0}, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the kernel as it stands (same source hash); else None."""
+    path = os.path.join(ROOT, TRAFFIC_FILE)
+    try:
+        vals = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    vals[k.strip()] = v.strip()
+        if vals.get("kernel_source_sha256_16") != kernel_source_hash():
+            return None
+        return float(vals["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of this GPU's clocks and throttle reasons."""
+
+    FIELDS = ("pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        import torch
+
+        props = torch.cuda.get_device_properties(device_index)
+        dom = getattr(props, "pci_domain_id", 0)
+        bus = getattr(props, "pci_bus_id", None)
+        dev = getattr(props, "pci_device_id", 0)
+        self.bus_id = None if bus is None else f"{dom:08X}:{bus:02X}:{dev:02X}.0"
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        allrows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    allrows.append(parts)
+        # nvidia-smi prints the bus id as DDDDDDDD:BB:DD.F; match bus and device
+        want = self.bus_id.upper()[-7:] if self.bus_id else None
+        rows = [r for r in allrows if want and r[0].upper().endswith(want)]
+        if not rows and len({r[0] for r in allrows}) == 1:
+            rows = allrows
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        loaded = [s for s in sm if mx and s >= 0.3 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host cores (cpu_baseline and --impl reference)
+# ---------------------------------------------------------------------------
+
+def oracle_rows_timing(A, B, rows):
+    import oracle
+
+    t0 = time.perf_counter()
+    oracle.gemm_f16_nt(A[:rows], B)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(w, A, B, budget_s=10.0):
+    import oracle
+
+    cores = oracle.num_threads()
+    probe = 32
+    t = oracle_rows_timing(A, B, probe)
+    rows = int(min(w.M, max(probe, probe * budget_s / max(t, 1e-6))))
+    t = oracle_rows_timing(A, B, rows)
+    flop = 2.0 * rows * w.N * w.K
+    return {"value": flop / t / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"rows 0..{rows - 1} of A against all of B ({rows}x{w.N} outputs, K={w.K}), "
+                      f"float64 triple loop, {t:.1f} s"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from dense_gemm_fp16_gb300 import workloads as wl
+    import oracle
+
+    w = wl.WORKLOADS[wl.HEADLINE]
+    A, B, _ = wl.make_inputs(w)
+    rows = 96  # one bounded sample per step: 96 x 5376 outputs, full K
+    for _ in range(args.warmup):
+        oracle_rows_timing(A, B, rows)
+    times = [oracle_rows_timing(A, B, rows) for _ in range(args.steps)]
+    total = sum(times)
+    value = 2.0 * rows * w.N * w.K * args.steps / total / 1e12
+    cores = oracle.num_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K,
+                   "inputs": "A,B uniform[-1,1] seeds 1,2 rounded to fp16"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"each step: rows 0..{rows - 1} of A against all of B "
+                                   f"({rows}x{w.N} outputs, K={w.K}), float64 triple loop"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def time_launches(fn, stream, n):
+    """Average device time of n launches of fn, CUDA events on `stream`."""
+    import torch
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n)]
+    for i in range(n):
+        ev[i][0].record(stream)
+        fn(i)
+        ev[i][1].record(stream)
+    stream.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def run_ours(args):
+    import torch
+
+    import dense_gemm_fp16_gb300 as g
+    from dense_gemm_fp16_gb300 import build, workloads as wl
+
+    rank, local, world = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    build.build()
+    g.load_library()
+
+    w = wl.WORKLOADS[wl.HEADLINE]
+    M, N, K = w.M, w.N, w.K
+    A, B, _ = wl.make_inputs(w)
+    stream = torch.cuda.Stream()
+    sh = stream.cuda_stream
+    with torch.cuda.stream(stream):
+        sets = [(A.cuda(), B.cuda(), torch.empty((M, N), dtype=torch.float16, device="cuda"))
+                for _ in range(ROTATE)]
+    stream.synchronize()
+
+    def step(i):
+        a, b, c = sets[i % ROTATE]
+        g.gemm_f16_nt(M, N, K, a.data_ptr(), b.data_ptr(), c.data_ptr(), sh)
+
+    for i in range(args.warmup):
+        step(i)
+    g.gemm_check_device_status(sh)
+
+    # ---- timed region: exactly K steps, barrier + synchronize on both sides.
+    # nvidia-smi samples every 100 ms, so the sampler also covers a short soak
+    # of the same launches right before and right after the timed region.
+    ev_start = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev_end = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    soak = max(1, int(args.soak_s / max(1e-4, 1e-3 * statistics.mean(
+        time_launches(step, stream, 5)))))
+    with ClockSampler(local) as clocks:
+        time_launches(step, stream, soak)
+        barrier(world)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            ev_start[i].record(stream)
+            step(i)
+            ev_end[i].record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        wall = time.perf_counter() - t0
+        time_launches(step, stream, soak)
+    g.gemm_check_device_status(sh)
+    launch_ms = [a.elapsed_time(b) for a, b in zip(ev_start, ev_end)]
+    region_ms = ev_start[0].elapsed_time(ev_end[-1])
+    region_ms = max_over_ranks(region_ms, world)
+    ms_per_step = region_ms / args.steps
+    value = world * w.flop * args.steps / (region_ms * 1e-3) / 1e12
+    avg_launch_ms = statistics.mean(launch_ms)
+
+    peaks, peak_kind = measured_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_TENSOR_TFLOPS))
+    achieved = w.flop / (avg_launch_ms * 1e-3) / 1e12
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "M": M, "N": N, "K": K,
+                   "inputs": "A,B uniform[-1,1] seeds 1,2 rounded to fp16; fp32 accumulate; "
+                             "fp16 out",
+                   "l2": f"inputs larger than L2: {ROTATE} rotating A/B/C sets "
+                         f"({ROTATE * (2 * M * K + 2 * N * K + 2 * M * N) / 1e6:.0f} MB)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "percent_of_peak": 100.0 * value / world / peak,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": profiled_traffic(),
+                     "peak_source": f"{peak_kind} bf16 dense burst (fp16 runs at the bf16 rate)",
+                     "kernel": "gemm_f16_nt_tc_kernel<256,4>",
+                     "avg_launch_us": 1e3 * avg_launch_ms},
+        "gpu_launches": args.steps,
+        "clocks": clocks.summary(),
+        "wall_s_timed_region": wall,
+    }
+
+    # ---- end to end through the C ABI with pinned host buffers
+    hA, hB = A.pin_memory(), B.pin_memory()
+    hC = torch.empty((M, N), dtype=torch.float16).pin_memory()
+    a, b, c = sets[0]
+
+    def e2e_step(_):
+        a.copy_(hA, non_blocking=True)
+        b.copy_(hB, non_blocking=True)
+        g.gemm_f16_nt(M, N, K, a.data_ptr(), b.data_ptr(), c.data_ptr(), sh)
+        hC.copy_(c, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            e2e_step(i)
+        stream.synchronize()
+        barrier(world)
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            e2e_step(i)
+        stream.synchronize()
+        e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    line["e2e"] = {"value": world * w.flop * args.steps / e2e_s / 1e12, "unit": "TFLOP/s",
+                   "h2d_bytes_per_step": hA.numel() * 2 + hB.numel() * 2,
+                   "d2h_bytes_per_step": hC.numel() * 2,
+                   "gpu_launches": args.steps}
+
+    # ---- cuBLAS reference line (context only, never on the product path)
+    torch.backends.cuda.matmul.allow_fp16_reduced_precision_reduction = False
+    with torch.cuda.stream(stream):
+        def cublas_step(i):
+            x, y, z = sets[i % ROTATE]
+            torch.matmul(x, y.t(), out=z)
+        time_launches(cublas_step, stream, args.warmup + 2)
+        cb = time_launches(cublas_step, stream, args.steps)
+    line["cublas"] = {"value": w.flop / (statistics.mean(cb) * 1e-3) / 1e12, "unit": "TFLOP/s",
+                      "what": "torch.matmul(A, B.t()) fp16, fp32 accumulation; reference only"}
+
+    # ---- fp32 SGEMM 4096^3 (alpha 1, beta 0.5) against the FP32 FFMA peak
+    if not args.skip_sgemm:
+        sw = wl.WORKLOADS["sgemm_4096"]
+        sA, sB, sC0 = wl.make_inputs(sw)
+        with torch.cuda.stream(stream):
+            dsa, dsb, dsc = sA.cuda(), sB.cuda(), sC0.cuda()
+        stream.synchronize()
+
+        def sg(_):
+            g.sgemm(sw.M, sw.N, sw.K, sw.alpha, dsa.data_ptr(), dsb.data_ptr(), sw.beta,
+                    dsc.data_ptr(), sh)
+        time_launches(sg, stream, 3)
+        st = time_launches(sg, stream, max(5, min(args.steps, 20)))
+        sm_count = torch.cuda.get_device_properties(local).multi_processor_count
+        fp32_peak = sm_count * 128 * 2 * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6 / 1e12
+        sval = sw.flop / (statistics.mean(st) * 1e-3) / 1e12
+        line["sgemm"] = {"workload": sw.name, "value": sval, "unit": "TFLOP/s",
+                         "roofline": {"bound": "alu", "achieved": sval, "peak": fp32_peak,
+                                      "unit": "TFLOP/s", "frac": sval / fp32_peak,
+                                      "peak_source": f"{sm_count} SMs x 128 FFMA/clk x 2 FLOP x "
+                                                     f"{peaks.get('sm_max_mhz', 2070.0)} MHz"}}
+
+    if rank == 0 and not args.skip_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, A, B, budget_s=args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--soak-s", type=float, default=0.6,
+                    help="seconds of launches before and after the timed region while clocks "
+                         "are sampled")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-budget", type=float, default=10.0,
+                    help="seconds of oracle work for the cpu_baseline sample")
+    ap.add_argument("--skip-cpu-baseline", action="store_true")
+    ap.add_argument("--skip-sgemm", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)   # timing rule: at least 3 warm-up steps
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,1 +1,42 @@
-"""GB300-native dense matrix multiplication (placeholder; binding follows)."""
+"""GB300-native (sm_103a) dense matrix multiplication.
+
+Two products behind the C ABI of ``include/gemm.h`` (``libgemm.so``):
+
+* ``gemm_f16_nt(M, N, K, A, B, C, stream)``: C = A·Bᵀ, half in, fp32
+  accumulation on the tcgen05 tensor cores, half out.
+* ``sgemm(M, N, K, alpha, A, B, beta, C, stream)``: C = alpha·A·B + beta·C in
+  fp32 on the CUDA cores.
+
+This package is the thin Python binding (same names, pointers as ints) plus
+tensor conveniences ``f16_nt`` and ``sgemm_``; ``workloads`` holds the seeded
+synthetic inputs.  The library is built in-tree by
+``python -m dense_gemm_fp16_gb300.build``; without it every call raises.
+"""
+from ._binding import (  # noqa: F401
+    GEMM_ERR_CUDA,
+    GEMM_ERR_DEVICE_TIMEOUT,
+    GEMM_ERR_INVALID_ARG,
+    GEMM_ERR_MISALIGNED,
+    GEMM_ERR_UNSUPPORTED,
+    GEMM_F16_128x128,
+    GEMM_F16_128x256,
+    GEMM_F16_AUTO,
+    GEMM_OK,
+    GEMM_SGEMM_64x64,
+    GEMM_SGEMM_128x128,
+    GEMM_SGEMM_AUTO,
+    LIB_PATH,
+    GemmError,
+    f16_nt,
+    gemm_check_device_status,
+    gemm_debug_f16_nt_skip_load,
+    gemm_f16_nt,
+    gemm_f16_nt_ex,
+    gemm_f16_select,
+    gemm_last_error,
+    gemm_sgemm_select,
+    load_library,
+    sgemm,
+    sgemm_,
+    sgemm_ex,
+)

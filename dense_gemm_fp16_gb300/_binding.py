@@ -1,0 +1,189 @@
+"""ctypes binding of libgemm.so: the C ABI of include/gemm.h under the same
+names, plus tensor conveniences.  Argument marshalling only: every step of
+both products runs in the library's CUDA kernels.  There is no fallback; if
+the library is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libgemm.so")
+
+GEMM_OK = 0
+GEMM_ERR_INVALID_ARG = -1
+GEMM_ERR_MISALIGNED = -2
+GEMM_ERR_UNSUPPORTED = -3
+GEMM_ERR_CUDA = -4
+GEMM_ERR_DEVICE_TIMEOUT = -5
+
+GEMM_F16_AUTO, GEMM_F16_128x256, GEMM_F16_128x128 = 0, 1, 2
+GEMM_SGEMM_AUTO, GEMM_SGEMM_128x128, GEMM_SGEMM_64x64 = 0, 1, 2
+
+STATUS_NAMES = {
+    GEMM_OK: "GEMM_OK",
+    GEMM_ERR_INVALID_ARG: "GEMM_ERR_INVALID_ARG",
+    GEMM_ERR_MISALIGNED: "GEMM_ERR_MISALIGNED",
+    GEMM_ERR_UNSUPPORTED: "GEMM_ERR_UNSUPPORTED",
+    GEMM_ERR_CUDA: "GEMM_ERR_CUDA",
+    GEMM_ERR_DEVICE_TIMEOUT: "GEMM_ERR_DEVICE_TIMEOUT",
+}
+
+
+class GemmError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+class _F16Config(ctypes.Structure):
+    _fields_ = [("variant", ctypes.c_int), ("grid", ctypes.c_int)]
+
+
+class _SgemmConfig(ctypes.Structure):
+    _fields_ = [("variant", ctypes.c_int)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libgemm.so (once).  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: build it with `python -m dense_gemm_fp16_gb300.build` "
+                "(there is no CPU fallback)")
+        lib = ctypes.CDLL(path)
+        i, vp, f = ctypes.c_int, ctypes.c_void_p, ctypes.c_float
+        lib.gemm_f16_nt.argtypes = [i, i, i, vp, vp, vp, vp]
+        lib.gemm_f16_nt.restype = i
+        lib.gemm_f16_nt_ex.argtypes = [i, i, i, vp, vp, vp, vp, ctypes.POINTER(_F16Config)]
+        lib.gemm_f16_nt_ex.restype = i
+        lib.sgemm.argtypes = [i, i, i, f, vp, vp, f, vp, vp]
+        lib.sgemm.restype = i
+        lib.sgemm_ex.argtypes = [i, i, i, f, vp, vp, f, vp, vp, ctypes.POINTER(_SgemmConfig)]
+        lib.sgemm_ex.restype = i
+        lib.gemm_last_error.argtypes = []
+        lib.gemm_last_error.restype = ctypes.c_char_p
+        lib.gemm_check_device_status.argtypes = [vp]
+        lib.gemm_check_device_status.restype = i
+        lib.gemm_f16_select.argtypes = [i, i, i, i, ctypes.POINTER(_F16Config)]
+        lib.gemm_f16_select.restype = i
+        lib.gemm_sgemm_select.argtypes = [i, i, i, i, ctypes.POINTER(_SgemmConfig)]
+        lib.gemm_sgemm_select.restype = i
+        lib.gemm_debug_f16_nt_skip_load.argtypes = [i, i, i, vp, vp, vp, vp, i, ctypes.c_ulonglong]
+        lib.gemm_debug_f16_nt_skip_load.restype = i
+        _lib = lib
+        return lib
+
+
+def gemm_last_error() -> str:
+    return load_library().gemm_last_error().decode("utf-8", "replace")
+
+
+def _check(status: int) -> int:
+    if status != GEMM_OK:
+        raise GemmError(status, gemm_last_error())
+    return status
+
+
+# ---------------------------------------------------------------------------
+# The C ABI, same names and argument order (pointers and streams as ints).
+# ---------------------------------------------------------------------------
+
+def gemm_f16_nt(M: int, N: int, K: int, A: int, B: int, C: int, stream: int | None = 0) -> int:
+    return _check(load_library().gemm_f16_nt(M, N, K, A, B, C, stream or None))
+
+
+def gemm_f16_nt_ex(M, N, K, A, B, C, stream=0, variant=GEMM_F16_AUTO, grid=0) -> int:
+    cfg = _F16Config(variant, grid)
+    return _check(load_library().gemm_f16_nt_ex(M, N, K, A, B, C, stream or None, ctypes.byref(cfg)))
+
+
+def sgemm(M: int, N: int, K: int, alpha: float, A: int, B: int, beta: float, C: int,
+          stream: int | None = 0) -> int:
+    return _check(load_library().sgemm(M, N, K, alpha, A, B, beta, C, stream or None))
+
+
+def sgemm_ex(M, N, K, alpha, A, B, beta, C, stream=0, variant=GEMM_SGEMM_AUTO) -> int:
+    cfg = _SgemmConfig(variant)
+    return _check(load_library().sgemm_ex(M, N, K, alpha, A, B, beta, C, stream or None,
+                                          ctypes.byref(cfg)))
+
+
+def gemm_check_device_status(stream: int | None = 0) -> int:
+    return _check(load_library().gemm_check_device_status(stream or None))
+
+
+def gemm_f16_select(M: int, N: int, K: int, sm_count: int) -> tuple[int, int]:
+    cfg = _F16Config(0, 0)
+    _check(load_library().gemm_f16_select(M, N, K, sm_count, ctypes.byref(cfg)))
+    return cfg.variant, cfg.grid
+
+
+def gemm_sgemm_select(M: int, N: int, K: int, sm_count: int) -> int:
+    cfg = _SgemmConfig(0)
+    _check(load_library().gemm_sgemm_select(M, N, K, sm_count, ctypes.byref(cfg)))
+    return cfg.variant
+
+
+def gemm_debug_f16_nt_skip_load(M, N, K, A, B, C, stream, skip_kblock, timeout_ns) -> int:
+    """Raw status of the fault-injection hook of include/gemm_testing.h."""
+    return load_library().gemm_debug_f16_nt_skip_load(M, N, K, A, B, C, stream or None,
+                                                      skip_kblock, timeout_ns)
+
+
+# ---------------------------------------------------------------------------
+# Tensor conveniences (torch supplies device memory and the stream).
+# ---------------------------------------------------------------------------
+
+def _stream_handle(stream) -> int:
+    import torch
+
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def f16_nt(A, B, C=None, stream=None, variant: int = GEMM_F16_AUTO, grid: int = 0):
+    """C = A·Bᵀ for contiguous half CUDA tensors A [M,K], B [N,K]; returns C [M,N]."""
+    import torch
+
+    if A.dtype != torch.float16 or B.dtype != torch.float16:
+        raise TypeError("f16_nt expects float16 tensors")
+    if not (A.is_cuda and B.is_cuda and A.is_contiguous() and B.is_contiguous()):
+        raise ValueError("f16_nt expects contiguous CUDA tensors")
+    if A.dim() != 2 or B.dim() != 2 or A.shape[1] != B.shape[1]:
+        raise ValueError(f"shape mismatch {tuple(A.shape)} x {tuple(B.shape)}^T")
+    M, K = A.shape
+    N = B.shape[0]
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.float16, device=A.device)
+    elif C.shape != (M, N) or C.dtype != torch.float16 or not C.is_contiguous():
+        raise ValueError("C must be a contiguous float16 [M, N] tensor")
+    gemm_f16_nt_ex(M, N, K, A.data_ptr(), B.data_ptr(), C.data_ptr(), _stream_handle(stream),
+                   variant, grid)
+    return C
+
+
+def sgemm_(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None,
+           variant: int = GEMM_SGEMM_AUTO):
+    """In place: C = alpha·A·B + beta·C for contiguous float32 CUDA tensors."""
+    import torch
+
+    for t in (A, B, C):
+        if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("sgemm_ expects contiguous float32 CUDA tensors")
+    if A.dim() != 2 or B.dim() != 2 or A.shape[1] != B.shape[0] or C.shape != (A.shape[0], B.shape[1]):
+        raise ValueError(f"shape mismatch {tuple(A.shape)} x {tuple(B.shape)} -> {tuple(C.shape)}")
+    M, K = A.shape
+    N = B.shape[1]
+    sgemm_ex(M, N, K, float(alpha), A.data_ptr(), B.data_ptr(), float(beta), C.data_ptr(),
+             _stream_handle(stream), variant)
+    return C

@@ -1,0 +1,239 @@
+// gemm_api.cu -- the C ABI of libgemm.so: argument validation, shape-keyed
+// selection of the kernel configuration, per-thread error messages, and the
+// device-status query.  Declarations and the contract of each entry point are
+// in include/gemm.h.
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+#include "gemm.h"
+#include "gemm_internal.h"
+#include "gemm_testing.h"
+
+namespace {
+
+thread_local std::string t_last_error;
+
+int fail(int status, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    std::vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    t_last_error = buf;
+    return status;
+}
+
+int fail_str(int status, const std::string &msg) {
+    t_last_error = msg;
+    return status;
+}
+
+// Bounded-wait budget inside the fp16 kernel: long enough for any legitimate
+// stall (preemption by another context included), short enough that a broken
+// handshake ends the kernel instead of holding the GPU.
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s
+
+int sm_count_of_current_device(int *out) {
+    static std::mutex mu;
+    static int cache[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev >= 0 && dev < 64 && cache[dev] > 0) {
+        *out = cache[dev];
+        return GEMM_OK;
+    }
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess || n <= 0)
+        return fail(GEMM_ERR_CUDA, "cudaDeviceGetAttribute(SM count): %s", cudaGetErrorString(e));
+    if (dev >= 0 && dev < 64) cache[dev] = n;
+    *out = n;
+    return GEMM_OK;
+}
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
+
+}  // namespace
+
+extern "C" {
+
+const char *gemm_last_error(void) { return t_last_error.c_str(); }
+
+// ---------------------------------------------------------------------------
+// Selection (host logic only; no device call)
+// ---------------------------------------------------------------------------
+
+int gemm_f16_select(int M, int N, int K, int sm_count, gemm_f16_config *cfg) {
+    if (!cfg) return fail(GEMM_ERR_INVALID_ARG, "gemm_f16_select: cfg is NULL");
+    if (M < 0 || N < 0 || K < 0 || sm_count <= 0)
+        return fail(GEMM_ERR_INVALID_ARG, "gemm_f16_select: bad M=%d N=%d K=%d sm_count=%d", M, N,
+                    K, sm_count);
+    // 128 x 256 tiles halve the shared-memory bytes read per MMA compared to
+    // 128 x 128 and are the default.  When the wide tiles would leave SMs idle
+    // (fewer tiles than SMs) the narrow tile doubles the parallelism.
+    const long long wide = ceil_div(M, 128) * ceil_div(N, 256);
+    int variant = GEMM_F16_128x256;
+    if (wide < sm_count || N <= 128) variant = GEMM_F16_128x128;
+    const long long tiles =
+        ceil_div(M, 128) * ceil_div(N, variant == GEMM_F16_128x256 ? 256 : 128);
+    cfg->variant = variant;
+    cfg->grid = static_cast<int>(tiles < sm_count ? (tiles > 0 ? tiles : 1) : sm_count);
+    return GEMM_OK;
+}
+
+int gemm_sgemm_select(int M, int N, int K, int sm_count, gemm_sgemm_config *cfg) {
+    if (!cfg) return fail(GEMM_ERR_INVALID_ARG, "gemm_sgemm_select: cfg is NULL");
+    if (M < 0 || N < 0 || K < 0 || sm_count <= 0)
+        return fail(GEMM_ERR_INVALID_ARG, "gemm_sgemm_select: bad M=%d N=%d K=%d sm_count=%d", M,
+                    N, K, sm_count);
+    // The 128 x 128 tile does 16 FFMA per shared-memory load; use it whenever
+    // it still gives every SM at least one CTA, else the 64 x 64 tile (4x the
+    // CTAs) so small problems do not run on a handful of SMs.
+    const long long big = ceil_div(M, 128) * ceil_div(N, 128);
+    cfg->variant = (big >= sm_count) ? GEMM_SGEMM_128x128 : GEMM_SGEMM_64x64;
+    return GEMM_OK;
+}
+
+// ---------------------------------------------------------------------------
+// fp16 NT
+// ---------------------------------------------------------------------------
+
+static int f16_nt_impl(int M, int N, int K, const void *A, const void *B, void *C,
+                       gemm_stream_t stream, const gemm_f16_config *cfg, uint64_t timeout_ns,
+                       int debug_skip_kblock) {
+    if (M < 0 || N < 0 || K < 0)
+        return fail(GEMM_ERR_INVALID_ARG, "gemm_f16_nt: negative size M=%d N=%d K=%d", M, N, K);
+    if (M == 0 || N == 0) return GEMM_OK;
+    if (!C) return fail(GEMM_ERR_INVALID_ARG, "gemm_f16_nt: C is NULL");
+    if (K > 0 && (!A || !B)) return fail(GEMM_ERR_INVALID_ARG, "gemm_f16_nt: A or B is NULL");
+    if (K > 0 && (!aligned16(A) || !aligned16(B)))
+        return fail(GEMM_ERR_MISALIGNED, "gemm_f16_nt: A and B must be 16-byte aligned");
+    if (K % 8 != 0)
+        return fail(GEMM_ERR_UNSUPPORTED,
+                    "gemm_f16_nt: K=%d; K*2 bytes must be a multiple of 16 (K %% 8 == 0)", K);
+    if (cfg && (cfg->variant < 0 || cfg->variant >= GEMM_F16_NUM_VARIANTS || cfg->grid < 0))
+        return fail(GEMM_ERR_INVALID_ARG, "gemm_f16_nt_ex: bad config variant=%d grid=%d",
+                    cfg->variant, cfg->grid);
+    int sms = 0;
+    int st = sm_count_of_current_device(&sms);
+    if (st != GEMM_OK) return st;
+    gemm_f16_config sel;
+    st = gemm_f16_select(M, N, K, sms, &sel);
+    if (st != GEMM_OK) return st;
+    if (cfg && cfg->variant != GEMM_F16_AUTO) {
+        sel.variant = cfg->variant;
+        const long long tiles =
+            ceil_div(M, 128) * ceil_div(N, sel.variant == GEMM_F16_128x256 ? 256 : 128);
+        sel.grid = static_cast<int>(tiles < sms ? tiles : sms);
+    }
+    if (cfg && cfg->grid > 0) sel.grid = cfg->grid;
+
+    gb300::F16Launch L;
+    L.M = M;
+    L.N = N;
+    L.K = K;
+    L.A = A;
+    L.B = B;
+    L.C = C;
+    L.stream = reinterpret_cast<cudaStream_t>(stream);
+    L.variant = sel.variant;
+    L.grid = sel.grid;
+    L.timeout_ns = timeout_ns;
+    L.debug_skip_kblock = debug_skip_kblock;
+    std::string err;
+    st = gb300::f16_launch(L, err);
+    if (st != GEMM_OK) return fail_str(st, err);
+    return GEMM_OK;
+}
+
+int gemm_f16_nt(int M, int N, int K, const void *A, const void *B, void *C, gemm_stream_t stream) {
+    return f16_nt_impl(M, N, K, A, B, C, stream, nullptr, kDefaultTimeoutNs, -1);
+}
+
+int gemm_f16_nt_ex(int M, int N, int K, const void *A, const void *B, void *C,
+                   gemm_stream_t stream, const gemm_f16_config *cfg) {
+    return f16_nt_impl(M, N, K, A, B, C, stream, cfg, kDefaultTimeoutNs, -1);
+}
+
+// Test hook declared in gemm_testing.h: one TMA load left out so that the
+// kernel's bounded waits run out (`timeout_ns` each) and the status path runs.
+int gemm_debug_f16_nt_skip_load(int M, int N, int K, const void *A, const void *B, void *C,
+                                gemm_stream_t stream, int skip_kblock, unsigned long long timeout_ns) {
+    return f16_nt_impl(M, N, K, A, B, C, stream, nullptr, timeout_ns, skip_kblock);
+}
+
+// ---------------------------------------------------------------------------
+// SGEMM
+// ---------------------------------------------------------------------------
+
+int sgemm_ex(int M, int N, int K, float alpha, const float *A, const float *B, float beta,
+             float *C, gemm_stream_t stream, const gemm_sgemm_config *cfg) {
+    if (M < 0 || N < 0 || K < 0)
+        return fail(GEMM_ERR_INVALID_ARG, "sgemm: negative size M=%d N=%d K=%d", M, N, K);
+    if (M == 0 || N == 0) return GEMM_OK;
+    if (!C) return fail(GEMM_ERR_INVALID_ARG, "sgemm: C is NULL");
+    if (K > 0 && (!A || !B)) return fail(GEMM_ERR_INVALID_ARG, "sgemm: A or B is NULL");
+    if (cfg && (cfg->variant < 0 || cfg->variant >= GEMM_SGEMM_NUM_VARIANTS))
+        return fail(GEMM_ERR_INVALID_ARG, "sgemm_ex: bad config variant=%d", cfg->variant);
+    int variant = cfg ? cfg->variant : GEMM_SGEMM_AUTO;
+    if (variant == GEMM_SGEMM_AUTO) {
+        int sms = 0;
+        int st = sm_count_of_current_device(&sms);
+        if (st != GEMM_OK) return st;
+        gemm_sgemm_config sel;
+        st = gemm_sgemm_select(M, N, K, sms, &sel);
+        if (st != GEMM_OK) return st;
+        variant = sel.variant;
+    }
+    gb300::SgemmLaunch L;
+    L.M = M;
+    L.N = N;
+    L.K = K;
+    L.alpha = alpha;
+    L.beta = beta;
+    L.A = A;
+    L.B = B;
+    L.C = C;
+    L.stream = reinterpret_cast<cudaStream_t>(stream);
+    L.variant = variant;
+    std::string err;
+    int st = gb300::sgemm_launch(L, err);
+    if (st != GEMM_OK) return fail_str(st, err);
+    return GEMM_OK;
+}
+
+int sgemm(int M, int N, int K, float alpha, const float *A, const float *B, float beta, float *C,
+          gemm_stream_t stream) {
+    return sgemm_ex(M, N, K, alpha, A, B, beta, C, stream, nullptr);
+}
+
+// ---------------------------------------------------------------------------
+// Device status
+// ---------------------------------------------------------------------------
+
+int gemm_check_device_status(gemm_stream_t stream) {
+    int code = 0;
+    std::string err;
+    int st = gb300::f16_status_read_clear(reinterpret_cast<cudaStream_t>(stream), &code, err);
+    if (st != GEMM_OK) return fail_str(st, err);
+    if (code != 0) {
+        static const char *role[] = {"?", "TMA producer (free-slot wait)",
+                                     "MMA issuer (data or accumulator wait)",
+                                     "epilogue (accumulator-ready wait)"};
+        return fail(GEMM_ERR_DEVICE_TIMEOUT,
+                    "gemm_f16_nt: a bounded pipeline wait expired in the %s",
+                    role[(code >= 1 && code <= 3) ? code : 0]);
+    }
+    return GEMM_OK;
+}
+
+}  // extern "C"

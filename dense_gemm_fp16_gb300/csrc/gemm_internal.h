@@ -1,0 +1,43 @@
+// gemm_internal.h -- declarations shared by the translation units of
+// libgemm.so (never installed, never part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <string>
+
+namespace gb300 {
+
+// One fp16 NT launch, after argument validation and selection.
+struct F16Launch {
+    int M, N, K;
+    const void *A;
+    const void *B;
+    void *C;
+    cudaStream_t stream;
+    int variant;            // GEMM_F16_128x256 or GEMM_F16_128x128
+    int grid;               // persistent CTAs (> 0)
+    uint64_t timeout_ns;    // budget of every bounded wait in the kernel
+    int debug_skip_kblock;  // test hook: producer skips this k-block of its first tile (-1: none)
+};
+
+int f16_launch(const F16Launch &L, std::string &err);
+
+// Read-and-clear the fp16 kernel's device status word (0 = no fault).
+int f16_status_read_clear(cudaStream_t stream, int *code, std::string &err);
+
+// One SGEMM launch, after validation and selection.
+struct SgemmLaunch {
+    int M, N, K;
+    float alpha, beta;
+    const float *A;
+    const float *B;
+    float *C;
+    cudaStream_t stream;
+    int variant;  // GEMM_SGEMM_128x128 or GEMM_SGEMM_64x64
+};
+
+int sgemm_launch(const SgemmLaunch &L, std::string &err);
+
+}  // namespace gb300

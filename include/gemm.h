@@ -1,0 +1,157 @@
+/*
+ * gemm.h -- C ABI of libgemm.so, the GB300 (sm_103a) dense matrix products.
+ *
+ * Two products, both on row-major, densely packed matrices in device memory:
+ *
+ *  gemm_f16_nt  C = A * B^T, A half [M,K], B half [N,K], fp32 accumulation,
+ *               C half [M,N] (each output rounded to nearest-even once).
+ *               Defined by "从零开始的 AI Infra: 算子基础与GPU架构"
+ *               (qi-zhan.github.io/blog/2026/cuda-gemm), section "0. Naive
+ *               Implementation" (C[m][n] = half(sum_k A[m][k] * B[n][k]) with
+ *               a float accumulator) and section "19. 去掉转置" (B stored as
+ *               [N,K] row-major is the right operand B^T [K,N] column-major).
+ *               Runs on the 5th-generation tensor cores (tcgen05.mma, TMEM
+ *               accumulators, TMA-fed 128-byte-swizzled shared-memory tiles).
+ *
+ *  sgemm        C = alpha * A * B + beta * C, A float [M,K], B float [K,N],
+ *               C float [M,N], fp32 arithmetic on the CUDA cores (FFMA; no
+ *               TF32).  Defined by "异步拷贝与 Hopper/Blackwell 新特性"
+ *               (anrans.github.io/ai-infra-handbooks/cuda/advanced/
+ *               async-hopper), section "cp.async 与多级流水 sm_80+": the
+ *               gemm_cp_async kernel's epilogue c = alpha*acc + beta*c.
+ *
+ * Common rules for every entry point below:
+ *  - Ownership: all matrix pointers are device memory owned by the caller;
+ *    the library keeps no reference after the call returns and allocates no
+ *    device memory per call.  C must not overlap A or B.
+ *  - Asynchrony: work is enqueued on `stream` (a cudaStream_t; NULL means
+ *    the legacy default stream) on the calling thread's current device.  The
+ *    call returns once the work is enqueued; it does not synchronise.
+ *  - Errors: the return value is a gemm_status.  On any non-OK status nothing
+ *    was enqueued, and gemm_last_error() gives a message.  Faults found on
+ *    the device (a bounded wait inside a kernel that ran out) are reported by
+ *    gemm_check_device_status().
+ *  - Empty problems: M == 0 or N == 0 is a no-op returning GEMM_OK.
+ */
+#ifndef DENSE_GEMM_FP16_GB300_GEMM_H
+#define DENSE_GEMM_FP16_GB300_GEMM_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t, spelled without including the CUDA headers. */
+typedef struct CUstream_st *gemm_stream_t;
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_ARG = -1,     /* negative size, NULL pointer with work to do, bad config */
+    GEMM_ERR_MISALIGNED = -2,      /* a pointer the fast path needs 16-byte aligned is not   */
+    GEMM_ERR_UNSUPPORTED = -3,     /* a shape the path cannot express (see each entry point) */
+    GEMM_ERR_CUDA = -4,            /* a CUDA runtime/driver call failed (message has detail) */
+    GEMM_ERR_DEVICE_TIMEOUT = -5   /* a kernel's bounded wait expired (device-side status)   */
+} gemm_status;
+
+/*
+ * C = A * B^T in fp16 with fp32 accumulation.
+ *   M, N, K  sizes, each >= 0.  A is [M,K], B is [N,K], C is [M,N]; row
+ *            strides are K, K and N elements (packed).
+ *   A, B     const half*, 16-byte aligned (they are read by TMA).
+ *   C        half*, written; never read.
+ * Constraints: K * 2 bytes must be a multiple of 16 (K % 8 == 0), the row
+ * stride rule of the tensor-memory-accelerator descriptors; otherwise
+ * GEMM_ERR_UNSUPPORTED.  M and N are arbitrary: partial tiles are masked.
+ * K == 0 writes C = 0.  When N % 8 == 0 and C is 16-byte aligned the
+ * epilogue stores 16-byte vectors, else single halves.
+ * Returns GEMM_ERR_INVALID_ARG (negative size, NULL with M*N > 0),
+ * GEMM_ERR_MISALIGNED (A or B not 16-byte aligned), GEMM_ERR_UNSUPPORTED,
+ * GEMM_ERR_CUDA, or GEMM_OK.
+ */
+int gemm_f16_nt(int M, int N, int K, const void *A, const void *B, void *C,
+                gemm_stream_t stream);
+
+/*
+ * C = alpha * A * B + beta * C in fp32 (FFMA only, no TF32).
+ *   M, N, K  sizes, each >= 0.  A is [M,K], B is [K,N], C is [M,N], all
+ *            row-major and packed.
+ *   alpha, beta  scalars.  beta == 0 follows the BLAS convention: C is not
+ *            read, so its prior contents (even NaN) do not matter.
+ *   A, B     const float*; C float*, read (when beta != 0) and written.
+ * Any alignment is accepted: 16-byte vector loads/stores are used where the
+ * pointers and row strides allow, scalar ones elsewhere.  K == 0 gives
+ * C = beta * C.
+ * Returns GEMM_ERR_INVALID_ARG, GEMM_ERR_CUDA, or GEMM_OK.
+ */
+int sgemm(int M, int N, int K, float alpha, const float *A, const float *B, float beta,
+          float *C, gemm_stream_t stream);
+
+/* Message for the last non-OK status returned on this host thread ("" if none).
+ * The pointer stays valid until the next call into the library on this thread. */
+const char *gemm_last_error(void);
+
+/*
+ * Synchronises `stream`, then reads and clears the device-side status word
+ * that kernels set when a bounded wait runs out (a pipeline handshake that
+ * never completed).  Returns GEMM_OK, GEMM_ERR_DEVICE_TIMEOUT, or
+ * GEMM_ERR_CUDA (for an error raised by the synchronisation itself).
+ */
+int gemm_check_device_status(gemm_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Tile and cluster selection.                                               */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * One kernel configuration of the fp16 path.  `variant` names a compiled
+ * instance (GEMM_F16_* below); grid is the persistent CTA count
+ * (0 = choose from the device's SM count).
+ */
+typedef struct {
+    int variant;
+    int grid;
+} gemm_f16_config;
+
+enum {
+    GEMM_F16_AUTO = 0,          /* let gemm_f16_select decide                     */
+    GEMM_F16_128x256 = 1,       /* one CTA per 128 x 256 output tile, 4 stages    */
+    GEMM_F16_128x128 = 2,       /* one CTA per 128 x 128 output tile, 6 stages    */
+    GEMM_F16_NUM_VARIANTS = 3
+};
+
+/*
+ * Shape-keyed choice of the fp16 configuration: pure host logic, no device
+ * call.  sm_count is the number of SMs to plan for (> 0).  Fills *cfg and
+ * returns GEMM_OK, or GEMM_ERR_INVALID_ARG.
+ */
+int gemm_f16_select(int M, int N, int K, int sm_count, gemm_f16_config *cfg);
+
+/* gemm_f16_nt with an explicit configuration (cfg == NULL or variant AUTO
+ * means the selector's choice).  Same argument rules and errors as
+ * gemm_f16_nt, plus GEMM_ERR_INVALID_ARG for an unknown variant. */
+int gemm_f16_nt_ex(int M, int N, int K, const void *A, const void *B, void *C,
+                   gemm_stream_t stream, const gemm_f16_config *cfg);
+
+/* One kernel configuration of the SGEMM path. */
+typedef struct {
+    int variant;
+} gemm_sgemm_config;
+
+enum {
+    GEMM_SGEMM_AUTO = 0,
+    GEMM_SGEMM_128x128 = 1,     /* 128 x 128 CTA tile, BK 8, 8 x 8 per thread */
+    GEMM_SGEMM_64x64 = 2,       /* 64 x 64 CTA tile, BK 8, 4 x 4 per thread   */
+    GEMM_SGEMM_NUM_VARIANTS = 3
+};
+
+/* Shape-keyed choice of the SGEMM tile (host logic only). */
+int gemm_sgemm_select(int M, int N, int K, int sm_count, gemm_sgemm_config *cfg);
+
+/* sgemm with an explicit configuration (NULL or AUTO = selector's choice). */
+int sgemm_ex(int M, int N, int K, float alpha, const float *A, const float *B, float beta,
+             float *C, gemm_stream_t stream, const gemm_sgemm_config *cfg);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DENSE_GEMM_FP16_GB300_GEMM_H */

@@ -1,0 +1,115 @@
+"""CPU-only checks of the C ABI: the library loads, exports every function
+the headers declare, validates arguments on the host before touching a
+device, and selects tiles by shape."""
+import glob
+import os
+import re
+
+import pytest
+
+import dense_gemm_fp16_gb300 as g
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from dense_gemm_fp16_gb300 import build
+
+    build.build()
+    return g.load_library()
+
+
+def _declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h, encoding="utf-8").read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+def test_headers_declare_the_boundary():
+    names = _declared_functions()
+    for n in ["gemm_f16_nt", "sgemm", "gemm_last_error", "gemm_check_device_status",
+              "gemm_f16_select", "gemm_sgemm_select", "gemm_f16_nt_ex", "sgemm_ex",
+              "gemm_debug_f16_nt_skip_load"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), f"libgemm.so does not export {name}"
+
+
+def test_negative_sizes_are_rejected_on_the_host(lib):
+    with pytest.raises(g.GemmError) as e:
+        g.gemm_f16_nt(-1, 4, 8, 16, 16, 16)
+    assert e.value.status == g.GEMM_ERR_INVALID_ARG
+    assert "negative" in g.gemm_last_error()
+    with pytest.raises(g.GemmError) as e:
+        g.sgemm(4, -4, 4, 1.0, 16, 16, 0.0, 16)
+    assert e.value.status == g.GEMM_ERR_INVALID_ARG
+
+
+def test_empty_problems_are_no_ops(lib):
+    assert g.gemm_f16_nt(0, 10, 64, 0, 0, 0) == g.GEMM_OK
+    assert g.gemm_f16_nt(10, 0, 64, 0, 0, 0) == g.GEMM_OK
+    assert g.sgemm(0, 5, 5, 1.0, 0, 0, 0.0, 0) == g.GEMM_OK
+
+
+def test_null_and_misaligned_pointers(lib):
+    with pytest.raises(g.GemmError) as e:
+        g.gemm_f16_nt(4, 4, 8, 0, 0x1000, 0x1000)
+    assert e.value.status == g.GEMM_ERR_INVALID_ARG
+    with pytest.raises(g.GemmError) as e:
+        g.gemm_f16_nt(4, 4, 8, 0x1002, 0x1000, 0x1000)
+    assert e.value.status == g.GEMM_ERR_MISALIGNED
+    with pytest.raises(g.GemmError) as e:
+        g.sgemm(4, 4, 4, 1.0, 0x1000, 0x1000, 0.0, 0)
+    assert e.value.status == g.GEMM_ERR_INVALID_ARG
+
+
+def test_k_not_multiple_of_8_is_unsupported_for_f16(lib):
+    with pytest.raises(g.GemmError) as e:
+        g.gemm_f16_nt(16, 16, 12, 0x1000, 0x1000, 0x1000)
+    assert e.value.status == g.GEMM_ERR_UNSUPPORTED
+    assert "K=12" in str(e.value)
+
+
+def test_bad_config_is_rejected(lib):
+    with pytest.raises(g.GemmError) as e:
+        g.gemm_f16_nt_ex(16, 16, 16, 0x1000, 0x1000, 0x1000, variant=99)
+    assert e.value.status == g.GEMM_ERR_INVALID_ARG
+    with pytest.raises(g.GemmError) as e:
+        g.sgemm_ex(16, 16, 16, 1.0, 0x1000, 0x1000, 0.0, 0x1000, variant=7)
+    assert e.value.status == g.GEMM_ERR_INVALID_ARG
+
+
+def test_f16_selector(lib):
+    # the two fp16 workloads: wide tiles, one persistent CTA per SM
+    assert g.gemm_f16_select(5376, 5376, 2048, 152) == (g.GEMM_F16_128x256, 152)
+    assert g.gemm_f16_select(5000, 5376, 2040, 152) == (g.GEMM_F16_128x256, 152)
+    # too few wide tiles to fill the SMs: narrow tiles, grid = tile count
+    assert g.gemm_f16_select(1024, 1024, 1024, 152) == (g.GEMM_F16_128x128, 64)
+    assert g.gemm_f16_select(100, 100, 64, 152) == (g.GEMM_F16_128x128, 1)
+    assert g.gemm_f16_select(128, 8192, 64, 148)[0] == g.GEMM_F16_128x128
+    with pytest.raises(g.GemmError):
+        g.gemm_f16_select(1, 1, 1, 0)
+
+
+def test_sgemm_selector(lib):
+    assert g.gemm_sgemm_select(4096, 4096, 4096, 152) == g.GEMM_SGEMM_128x128
+    assert g.gemm_sgemm_select(1024, 1024, 1024, 152) == g.GEMM_SGEMM_64x64
+    assert g.gemm_sgemm_select(256, 256, 256, 152) == g.GEMM_SGEMM_64x64
+
+
+def test_product_path_never_imports_the_oracle():
+    pkg = os.path.join(ROOT, "dense_gemm_fp16_gb300")
+    for path in glob.glob(os.path.join(pkg, "**", "*"), recursive=True):
+        if not path.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+            continue
+        text = open(path, encoding="utf-8").read()
+        assert not re.search(r"^\s*(import|from)\s+oracle\b", text, flags=re.M), path
+        assert "gemm_oracle" not in text and "liboracle" not in text, path

@@ -1,0 +1,165 @@
+"""GPU parity of gemm_f16_nt (C = A·Bᵀ, fp16 in, fp32 accumulate, fp16 out)
+against the float64 oracle, called through the C ABI.
+
+Small shapes are compared element by element (several tiles, ragged M/N/K
+tails, every compiled tile variant, persistent loops forced through many
+tiles per CTA); the two full-size workloads are compared on a seeded sample
+of 65,536 outputs plus the last row, last column and the partial M tile.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import dense_gemm_fp16_gb300 as g
+from dense_gemm_fp16_gb300 import workloads as wl
+from parity import check_f16
+
+pytestmark = pytest.mark.gpu
+
+SENTINEL = 0x7E5A  # a NaN payload nothing in the product writes
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from dense_gemm_fp16_gb300 import build
+
+    build.build()
+    g.load_library()
+    torch.cuda.init()
+
+
+def _run(A, B, variant=g.GEMM_F16_AUTO, grid=0, pad=64):
+    """Run on the GPU with a sentinel guard of `pad` halves around C."""
+    M, K = A.shape
+    N = B.shape[0]
+    dA, dB = A.cuda(), B.cuda()
+    buf = torch.full((M * N + 2 * pad,), 0, dtype=torch.int16, device="cuda")
+    buf.fill_(SENTINEL - (1 << 16) if SENTINEL >= (1 << 15) else SENTINEL)
+    buf = buf.view(torch.float16)
+    C = buf[pad:pad + M * N].view(M, N)
+    g.gemm_f16_nt_ex(M, N, K, dA.data_ptr(), dB.data_ptr(), C.data_ptr(),
+                     torch.cuda.current_stream().cuda_stream, variant, grid)
+    g.gemm_check_device_status(torch.cuda.current_stream().cuda_stream)
+    host = buf.cpu()
+    guard = torch.cat([host[:pad], host[pad + M * N:]]).view(torch.int16).numpy().view(np.uint16)
+    assert np.all(guard == SENTINEL), "kernel wrote outside C"
+    return host[pad:pad + M * N].view(M, N).numpy()
+
+
+SHAPES = [
+    (128, 256, 64),      # exactly one wide tile, one k-block
+    (256, 512, 128),     # 2 x 2 wide tiles
+    (300, 520, 136),     # ragged M, N and a partial k-block (136 = 2*64 + 8)
+    (129, 257, 72),      # one row / column past the tile edge
+    (1, 1, 8),           # smallest legal problem
+    (7, 1000, 2048),     # thin M, long K
+    (1000, 24, 520),     # thin N
+    (640, 768, 1024),    # several tiles per CTA under the selector's grid
+]
+
+
+@pytest.mark.parametrize("variant", [g.GEMM_F16_128x256, g.GEMM_F16_128x128])
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_f16_nt_full_compare(M, N, K, variant):
+    A = wl.draw_f16((M, K), seed=M + 1)
+    B = wl.draw_f16((N, K), seed=N + 2)
+    C = _run(A, B, variant)
+    Cref, S = oracle.gemm_f16_nt(A, B)
+    check_f16(C, Cref, S, what=f"{M}x{N}x{K} v{variant}")
+
+
+@pytest.mark.parametrize("variant,grid", [(g.GEMM_F16_128x256, 1), (g.GEMM_F16_128x256, 3),
+                                          (g.GEMM_F16_128x128, 1), (g.GEMM_F16_128x128, 5)])
+def test_f16_nt_persistent_many_tiles_per_cta(variant, grid):
+    # 5 x 3 (wide) or 5 x 6 (narrow) tiles on 1..5 CTAs: every stage and
+    # accumulator barrier goes through several phases.
+    M, N, K = 600, 700, 392
+    A = wl.draw_f16((M, K), seed=31, dist="normal")
+    B = wl.draw_f16((N, K), seed=32, dist="normal")
+    C = _run(A, B, variant, grid)
+    Cref, S = oracle.gemm_f16_nt(A, B)
+    check_f16(C, Cref, S, what=f"grid={grid} v{variant}")
+
+
+def test_f16_nt_small_integers_bit_exact():
+    # entries in {-1, 0, 1}, K = 1024: every partial sum is an integer below
+    # 2^11, exact in fp32 and in half, so the output must match bit for bit.
+    M, N, K = 384, 640, 1024
+    A = wl.draw_int((M, K), 41, -1, 1, torch.float16)
+    B = wl.draw_int((N, K), 42, -1, 1, torch.float16)
+    C = _run(A, B)
+    Cref, _ = oracle.gemm_f16_nt(A, B)
+    assert np.array_equal(C.astype(np.float64), Cref)
+
+
+def test_f16_nt_identity_and_permutation():
+    M, K = 256, 256
+    A = wl.draw_f16((M, K), seed=5)
+    perm = torch.randperm(K, generator=torch.Generator().manual_seed(6))
+    B = torch.eye(K, dtype=torch.float16)[perm]
+    C = _run(A, B)
+    assert np.array_equal(C, A.numpy()[:, perm.numpy()])
+
+
+def test_f16_nt_scalar_store_paths():
+    # N % 8 != 0 forces the per-element epilogue; a C offset by one element
+    # (2-byte aligned) does too.
+    for (M, N, K), pad in [((200, 250, 64), 64), ((130, 136, 128), 1)]:
+        A = wl.draw_f16((M, K), seed=7)
+        B = wl.draw_f16((N, K), seed=8)
+        C = _run(A, B, pad=pad)
+        Cref, S = oracle.gemm_f16_nt(A, B)
+        check_f16(C, Cref, S, what=f"scalar {M}x{N}x{K} pad={pad}")
+
+
+def test_f16_nt_k0_writes_zeros():
+    A = torch.zeros((0,), dtype=torch.float16).reshape(33, 0)
+    B = torch.zeros((0,), dtype=torch.float16).reshape(17, 0)
+    dA = torch.zeros(8, dtype=torch.float16, device="cuda")
+    C = torch.full((33, 17), 3.0, dtype=torch.float16, device="cuda")
+    g.gemm_f16_nt(33, 17, 0, dA.data_ptr(), dA.data_ptr(), C.data_ptr(),
+                  torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert A.shape[1] == 0 and B.shape[1] == 0
+    assert (C == 0).all()
+
+
+def test_f16_nt_unsupported_k_leaves_c_untouched():
+    A = torch.zeros((16, 12), dtype=torch.float16, device="cuda")
+    C = torch.full((16, 16), 5.0, dtype=torch.float16, device="cuda")
+    with pytest.raises(g.GemmError) as e:
+        g.gemm_f16_nt(16, 16, 12, A.data_ptr(), A.data_ptr(), C.data_ptr(), 0)
+    assert e.value.status == g.GEMM_ERR_UNSUPPORTED
+    torch.cuda.synchronize()
+    assert (C == 5.0).all()
+
+
+def test_f16_nt_on_a_side_stream_and_tensor_wrapper():
+    A = wl.draw_f16((512, 256), seed=9)
+    B = wl.draw_f16((384, 256), seed=10)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        dA, dB = A.cuda(), B.cuda()
+        C = g.f16_nt(dA, dB)
+    s.synchronize()
+    Cref, S = oracle.gemm_f16_nt(A, B)
+    check_f16(C.cpu().numpy(), Cref, S, what="side stream")
+
+
+@pytest.mark.parametrize("name", ["f16_nt_5376x5376x2048", "f16_nt_5000x5376x2040"])
+def test_f16_nt_full_size_sampled(name):
+    # The launch configuration the benchmark times (selector default).
+    w = wl.WORKLOADS[name]
+    A, B, _ = wl.make_inputs(w)
+    dA, dB = A.cuda(), B.cuda()
+    C = torch.empty((w.M, w.N), dtype=torch.float16, device="cuda")
+    g.gemm_f16_nt(w.M, w.N, w.K, dA.data_ptr(), dB.data_ptr(), C.data_ptr(),
+                  torch.cuda.current_stream().cuda_stream)
+    g.gemm_check_device_status(torch.cuda.current_stream().cuda_stream)
+    Ch = C.cpu().numpy()
+    assert np.all(np.isfinite(Ch.astype(np.float32)))
+    tail = list(range((w.M // 128) * 128, w.M))[:8] if w.M % 128 else []
+    rows, cols = wl.sample_positions(w.M, w.N, 65536, seed=2024, tail_rows=tail)
+    Cref, S = oracle.gemm_f16_nt_sampled(A, B, rows, cols)
+    check_f16(Ch[rows, cols], Cref, S, what=name)

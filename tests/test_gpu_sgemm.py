@@ -1,0 +1,129 @@
+"""GPU parity of sgemm (C = alpha·A·B + beta·C, fp32 FFMA) against the
+float64 oracle, called through the C ABI: the three SGEMM workloads, ragged
+shapes on both tile variants and both load paths, and the BLAS conventions
+(beta == 0 never reads C; K == 0 gives beta·C)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import dense_gemm_fp16_gb300 as g
+from dense_gemm_fp16_gb300 import workloads as wl
+from parity import check_sgemm
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from dense_gemm_fp16_gb300 import build
+
+    build.build()
+    g.load_library()
+    torch.cuda.init()
+
+
+def _run(A, B, C0, alpha, beta, variant=g.GEMM_SGEMM_AUTO, pad=64):
+    M, K = A.shape
+    N = B.shape[1]
+    dA, dB = A.cuda(), B.cuda()
+    buf = torch.full((M * N + 2 * pad,), -7.25, dtype=torch.float32, device="cuda")
+    C = buf[pad:pad + M * N].view(M, N)
+    if C0 is not None:
+        C.copy_(C0.cuda())
+    g.sgemm_ex(M, N, K, alpha, dA.data_ptr(), dB.data_ptr(), beta, C.data_ptr(),
+               torch.cuda.current_stream().cuda_stream, variant)
+    torch.cuda.synchronize()
+    host = buf.cpu().numpy()
+    assert np.all(host[:pad] == -7.25) and np.all(host[pad + M * N:] == -7.25), "wrote outside C"
+    return host[pad:pad + M * N].reshape(M, N)
+
+
+@pytest.mark.parametrize("name", ["sgemm_256", "sgemm_1024"])
+def test_sgemm_workloads_full_compare(name):
+    w = wl.WORKLOADS[name]
+    A, B, C0 = wl.make_inputs(w)
+    C = _run(A, B, torch.zeros(w.M, w.N), w.alpha, w.beta)
+    Cref, S = oracle.sgemm(A, B, w.alpha, w.beta, C0)
+    check_sgemm(C, Cref, S, what=name)
+
+
+def test_sgemm_4096_alpha_beta_sampled():
+    w = wl.WORKLOADS["sgemm_4096"]
+    A, B, C0 = wl.make_inputs(w)
+    C = _run(A, B, C0, w.alpha, w.beta, pad=4)
+    rows, cols = wl.sample_positions(w.M, w.N, 65536, seed=77)
+    Cref, S = oracle.sgemm_sampled(A, B, rows, cols, w.alpha, w.beta, C0)
+    c0 = C0.numpy()[rows, cols].astype(np.float64)
+    check_sgemm(C[rows, cols], Cref, S, beta_c0=w.beta * c0, what="sgemm_4096")
+
+
+@pytest.mark.parametrize("variant", [g.GEMM_SGEMM_128x128, g.GEMM_SGEMM_64x64])
+@pytest.mark.parametrize("M,N,K,alpha,beta", [
+    (100, 70, 33, 1.0, 0.0),       # ragged everything, scalar loads (K, N odd-ish)
+    (257, 129, 17, -1.5, 0.25),    # one past the tile edges
+    (1, 1, 1, 2.0, 0.0),
+    (300, 260, 64, 1.0, -1.0),     # vector loads, ragged M/N
+    (128, 128, 8, 0.5, 2.0),       # exactly one tile and one k-slice
+    (513, 384, 200, 1.0, 0.5),
+])
+def test_sgemm_ragged(M, N, K, alpha, beta, variant):
+    A = wl.draw_f32((M, K), seed=M)
+    B = wl.draw_f32((K, N), seed=N + 1)
+    C0 = wl.draw_f32((M, N), seed=K + 2)
+    C = _run(A, B, C0, alpha, beta, variant)
+    Cref, S = oracle.sgemm(A, B, alpha, beta, C0)
+    check_sgemm(C, Cref, S, beta_c0=beta * C0.numpy().astype(np.float64),
+                what=f"{M}x{N}x{K} v{variant}")
+
+
+def test_sgemm_misaligned_pointers_use_scalar_path():
+    M, N, K = 96, 80, 48
+    A = wl.draw_f32((M, K), seed=1)
+    B = wl.draw_f32((K, N), seed=2)
+    C = _run(A, B, None, 1.0, 0.0, pad=1)      # C offset by 4 bytes
+    Cref, S = oracle.sgemm(A, B)
+    check_sgemm(C, Cref, S, what="misaligned C")
+
+
+def test_sgemm_small_integers_exact():
+    M, N, K = 200, 150, 96
+    A = wl.draw_int((M, K), 3, -4, 4)
+    B = wl.draw_int((K, N), 4, -4, 4)
+    C0 = wl.draw_int((M, N), 5, -4, 4)
+    C = _run(A, B, C0, 2.0, -3.0)
+    Cref, _ = oracle.sgemm(A, B, 2.0, -3.0, C0)
+    assert np.array_equal(C.astype(np.float64), Cref)
+
+
+def test_sgemm_beta_zero_ignores_nan_c():
+    M, N, K = 130, 140, 40
+    A = wl.draw_f32((M, K), seed=11)
+    B = wl.draw_f32((K, N), seed=12)
+    C = _run(A, B, torch.full((M, N), float("nan")), 1.0, 0.0)
+    Cref, S = oracle.sgemm(A, B)
+    check_sgemm(C, Cref, S, what="beta=0 NaN C")
+
+
+def test_sgemm_k0_is_beta_c():
+    M, N = 65, 33
+    C0 = wl.draw_f32((M, N), seed=13)
+    dummy = torch.zeros(4, device="cuda")
+    C = C0.cuda()
+    g.sgemm(M, N, 0, 1.0, dummy.data_ptr(), dummy.data_ptr(), 0.5, C.data_ptr(),
+            torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert np.array_equal(C.cpu().numpy(), (0.5 * C0).numpy())
+    g.sgemm(M, N, 0, 1.0, dummy.data_ptr(), dummy.data_ptr(), 0.0, C.data_ptr(),
+            torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert (C == 0).all()
+
+
+def test_sgemm_tensor_wrapper():
+    A = wl.draw_f32((64, 32), seed=20).cuda()
+    B = wl.draw_f32((32, 48), seed=21).cuda()
+    C = torch.zeros(64, 48, device="cuda")
+    g.sgemm_(A, B, C)
+    Cref, S = oracle.sgemm(A.cpu(), B.cpu())
+    check_sgemm(C.cpu().numpy(), Cref, S, what="wrapper")
