@@ -20,6 +20,7 @@ from ._binding import (  # noqa: F401
     GEMM_ERR_UNSUPPORTED,
     GEMM_F16_128x128,
     GEMM_F16_128x256,
+    GEMM_F16_256x256_PAIR,
     GEMM_F16_AUTO,
     GEMM_OK,
     GEMM_SGEMM_64x64,

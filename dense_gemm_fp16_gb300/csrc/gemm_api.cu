@@ -62,6 +62,21 @@ inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 inline long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 
+// Persistent CTA count of an fp16 variant: one CTA (or CTA pair) per tile up
+// to one per SM.
+int f16_default_grid(int variant, int M, int N, int sm_count) {
+    long long tiles;
+    switch (variant) {
+        case GEMM_F16_128x256: tiles = ceil_div(M, 128) * ceil_div(N, 256); break;
+        case GEMM_F16_256x256_PAIR: tiles = 2 * ceil_div(M, 256) * ceil_div(N, 256); break;
+        default: tiles = ceil_div(M, 128) * ceil_div(N, 128); break;
+    }
+    long long cap = sm_count;
+    if (variant == GEMM_F16_256x256_PAIR) cap = sm_count & ~1;
+    long long g = tiles < cap ? tiles : cap;
+    return static_cast<int>(g > 0 ? g : 1);
+}
+
 }  // namespace
 
 extern "C" {
@@ -77,16 +92,18 @@ int gemm_f16_select(int M, int N, int K, int sm_count, gemm_f16_config *cfg) {
     if (M < 0 || N < 0 || K < 0 || sm_count <= 0)
         return fail(GEMM_ERR_INVALID_ARG, "gemm_f16_select: bad M=%d N=%d K=%d sm_count=%d", M, N,
                     K, sm_count);
-    // 128 x 256 tiles halve the shared-memory bytes read per MMA compared to
-    // 128 x 128 and are the default.  When the wide tiles would leave SMs idle
-    // (fewer tiles than SMs) the narrow tile doubles the parallelism.
-    const long long wide = ceil_div(M, 128) * ceil_div(N, 256);
-    int variant = GEMM_F16_128x256;
-    if (wide < sm_count || N <= 128) variant = GEMM_F16_128x128;
-    const long long tiles =
-        ceil_div(M, 128) * ceil_div(N, variant == GEMM_F16_128x256 ? 256 : 128);
+    // The CTA-pair 256 x 256 tile brings the fewest bytes into each SM per
+    // MMA (A and half of B: 32 KB per 64-deep k-block for 4 M FMA per SM) and
+    // is the default whenever its tiles keep every SM pair busy.  Otherwise
+    // the 128 x 128 tile gives 4x the tiles so small problems still spread
+    // over the SMs.  (The 1-CTA 128 x 256 tile has no shape range of its own
+    // between the two: it fills the SMs exactly when the pair tile fills the
+    // pairs; it stays available through gemm_f16_nt_ex.)
+    const long long pair_tiles = ceil_div(M, 256) * ceil_div(N, 256);
+    const int variant = (pair_tiles >= sm_count / 2 && N > 128) ? GEMM_F16_256x256_PAIR
+                                                                : GEMM_F16_128x128;
     cfg->variant = variant;
-    cfg->grid = static_cast<int>(tiles < sm_count ? (tiles > 0 ? tiles : 1) : sm_count);
+    cfg->grid = f16_default_grid(variant, M, N, sm_count);
     return GEMM_OK;
 }
 
@@ -131,9 +148,7 @@ static int f16_nt_impl(int M, int N, int K, const void *A, const void *B, void *
     if (st != GEMM_OK) return st;
     if (cfg && cfg->variant != GEMM_F16_AUTO) {
         sel.variant = cfg->variant;
-        const long long tiles =
-            ceil_div(M, 128) * ceil_div(N, sel.variant == GEMM_F16_128x256 ? 256 : 128);
-        sel.grid = static_cast<int>(tiles < sms ? tiles : sms);
+        sel.grid = f16_default_grid(sel.variant, M, N, sms);
     }
     if (cfg && cfg->grid > 0) sel.grid = cfg->grid;
 

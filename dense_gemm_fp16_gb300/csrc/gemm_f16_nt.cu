@@ -75,6 +75,34 @@ struct TileCfg {
 
 __device__ __forceinline__ void record_timeout(int code) { atomicCAS(&g_f16_status, 0, code); }
 
+// Round 32 consecutive fp32 accumulators of one output row to half and store
+// the columns n0 .. n0+31 that lie below N (16-byte vectors when allowed).
+__device__ __forceinline__ void store_row_chunk(__half *crow, bool row_ok, int n0, int N, int vec,
+                                                const uint32_t (&r)[32]) {
+    if (!row_ok) return;
+    if (vec) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            if (n0 + q * 8 < N) {
+                uint4 v;
+                __half2 h0 = __floats2half2_rn(__uint_as_float(r[q * 8 + 0]), __uint_as_float(r[q * 8 + 1]));
+                __half2 h1 = __floats2half2_rn(__uint_as_float(r[q * 8 + 2]), __uint_as_float(r[q * 8 + 3]));
+                __half2 h2 = __floats2half2_rn(__uint_as_float(r[q * 8 + 4]), __uint_as_float(r[q * 8 + 5]));
+                __half2 h3 = __floats2half2_rn(__uint_as_float(r[q * 8 + 6]), __uint_as_float(r[q * 8 + 7]));
+                v.x = *reinterpret_cast<uint32_t *>(&h0);
+                v.y = *reinterpret_cast<uint32_t *>(&h1);
+                v.z = *reinterpret_cast<uint32_t *>(&h2);
+                v.w = *reinterpret_cast<uint32_t *>(&h3);
+                *reinterpret_cast<uint4 *>(crow + n0 + q * 8) = v;
+            }
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (n0 + j < N) crow[n0 + j] = __float2half_rn(__uint_as_float(r[j]));
+    }
+}
+
 template <int BN, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_f16_nt_tc_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -244,30 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < BN / 32; ++c) {
                 uint32_t r[32];
                 tmem_load_32cols(tmem_base + lane_field + static_cast<uint32_t>(b * BN + c * 32), r);
-                const int n0 = nt * BN + c * 32;
-                if (m < args.M) {
-                    if (args.vec_store) {
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            if (n0 + q * 8 < args.N) {
-                                uint4 v;
-                                __half2 h0 = __floats2half2_rn(__uint_as_float(r[q * 8 + 0]), __uint_as_float(r[q * 8 + 1]));
-                                __half2 h1 = __floats2half2_rn(__uint_as_float(r[q * 8 + 2]), __uint_as_float(r[q * 8 + 3]));
-                                __half2 h2 = __floats2half2_rn(__uint_as_float(r[q * 8 + 4]), __uint_as_float(r[q * 8 + 5]));
-                                __half2 h3 = __floats2half2_rn(__uint_as_float(r[q * 8 + 6]), __uint_as_float(r[q * 8 + 7]));
-                                v.x = *reinterpret_cast<uint32_t *>(&h0);
-                                v.y = *reinterpret_cast<uint32_t *>(&h1);
-                                v.z = *reinterpret_cast<uint32_t *>(&h2);
-                                v.w = *reinterpret_cast<uint32_t *>(&h3);
-                                *reinterpret_cast<uint4 *>(crow + n0 + q * 8) = v;
-                            }
-                        }
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            if (n0 + j < args.N) crow[n0 + j] = __float2half_rn(__uint_as_float(r[j]));
-                    }
-                }
+                store_row_chunk(crow, m < args.M, nt * BN + c * 32, args.N, args.vec_store, r);
             }
             tc_fence_before_sync();
             __syncwarp();
@@ -300,6 +305,244 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc(tmem_base, T::kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// CTA-pair variant: a cluster of two CTAs computes a 256 x 256 output tile
+// with tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16).  CTA r of the pair
+// loads rows 128r .. 128r+127 of the tile's A block and rows 128r .. 128r+127
+// of its B block (the B half it contributes), so each SM brings in 32 KB per
+// 64-deep k-block instead of 48 KB, and each CTA's TMEM receives its own 128
+// output rows x 256 columns.  The even CTA's single MMA thread drives both
+// SMs' tensor cores:
+//   full[s]   (even CTA)  one arrive.expect_tx for both CTAs' bytes; the odd
+//                         CTA's TMA loads complete on it across the pair,
+//   empty[s]  (both CTAs) freed by a commit multicast to the pair,
+//   accf[b]   (both CTAs) accumulator ready, commit multicast to the pair,
+//   acce[b]   (even CTA)  accumulator drained: 4 epilogue warps x 2 CTAs.
+// ---------------------------------------------------------------------------
+
+template <int STAGES>
+struct PairCfg {
+    static constexpr int kBN = 256;                 // pair tile N (= MMA N)
+    static constexpr int kABytes = kBM * kBK * 2;   // this CTA's 128 rows of A
+    static constexpr int kBBytes = 128 * kBK * 2;   // this CTA's half of B
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kTmemCols = 512;           // two 256-column accumulators
+    static constexpr int kNumBars = 2 * STAGES + 5;
+    static constexpr int kBarOffset = STAGES * kStageBytes;
+    static constexpr int kSmemBytes = 1024 + kBarOffset + kNumBars * 8 + 16;
+    static_assert(kSmemBytes <= 232448, "fits the 227 KB opt-in limit");
+};
+
+template <int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_f16_nt_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                            const __grid_constant__ CUtensorMap tmB, const F16Args args) {
+    using T = PairCfg<STAGES>;
+    constexpr int BN = T::kBN;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+    const uint32_t sbase = smem_addr(smem);
+
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + T::kBarOffset);
+    const uint32_t bar0 = smem_addr(bars);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto accf_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+    auto acce_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + T::kNumBars);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    __shared__ int never_abort;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();  // 0 (leader) or 1
+    const bool leader = rank == 0;
+    const int pair = blockIdx.x >> 1;
+    const int num_pairs = gridDim.x >> 1;
+
+    if (threadIdx.x == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf_bar(b), 1);
+            mbar_init(acce_bar(b), 8);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        never_abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_addr(tmem_slot), T::kTmemCols);
+        tmem_relinquish_alloc_permit_pair();
+    }
+    tc_fence_before_sync();
+    cluster_sync();  // barriers of both CTAs initialised, TMEM allocated in both
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int total_tiles = args.m_tiles * args.n_tiles;  // pair tiles
+    const int num_kb = args.num_kb;
+    uint32_t armed = 0, arm_parity = 0;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer (both CTAs)
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            bool first_tile = true;
+            for (int tile = pair; tile < total_tiles && ok; tile += num_pairs) {
+                const int mt = tile % args.m_tiles;
+                const int nt = tile / args.m_tiles;
+                const int a_row = mt * 256 + static_cast<int>(rank) * 128;
+                const int b_row = nt * BN + static_cast<int>(rank) * 128;
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait_cluster(empty_bar(stage), phase ^ 1u, args.timeout_ns, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const bool skip = first_tile && kb == args.debug_skip_kblock && leader;
+                    if (!skip) {
+                        const uint32_t sa = sbase + stage * T::kStageBytes;
+                        const uint32_t full_leader = mapa_shared(full_bar(stage), 0);
+                        if (leader) {
+                            mbar_arrive_expect_tx(full_bar(stage), 2 * T::kStageBytes);
+                            armed |= 1u << stage;
+                            arm_parity ^= 1u << stage;
+                        }
+                        tma_load_2d_pair(sa, &tmA, full_leader, kb * kBK, a_row);
+                        tma_load_2d_pair(sa + T::kABytes, &tmB, full_leader, kb * kBK, b_row);
+                    }
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                first_tile = false;
+            }
+            if (!ok) {
+                if (!*abort_flag) record_timeout(1);
+                *abort_flag = 1;
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer (leader only)
+        if (lane == 0 && leader) {
+            constexpr uint32_t idesc = idesc_f16_f32acc(256, BN);
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            int i = 0;
+            for (int tile = pair; tile < total_tiles; tile += num_pairs, ++i) {
+                const int b = i & 1;
+                const uint32_t ap = (i >> 1) & 1;
+                if (!mbar_wait_cluster(acce_bar(b), ap ^ 1u, args.timeout_ns, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait_cluster(full_bar(stage), phase, args.timeout_ns, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t sa = sbase + stage * T::kStageBytes;
+                    const uint64_t adesc = sw128_kmajor_desc(sa);
+                    const uint64_t bdesc = sw128_kmajor_desc(sa + T::kABytes);
+#pragma unroll
+                    for (int k = 0; k < kBK / kUmmaK; ++k)
+                        mma_f16_ss_pair(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc,
+                                        (kb > 0 || k > 0) ? 1u : 0u);
+                    mma_commit_pair_multicast(empty_bar(stage), 0x3);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                mma_commit_pair_multicast(accf_bar(b), 0x3);
+            }
+            if (!ok) {
+                if (!*abort_flag) record_timeout(2);
+                *abort_flag = 1;
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue (both CTAs)
+        const int quarter = warp & 3;
+        const uint32_t lane_field = static_cast<uint32_t>(quarter * 32) << 16;
+        int i = 0;
+        for (int tile = pair; tile < total_tiles; tile += num_pairs, ++i) {
+            const int b = i & 1;
+            const uint32_t ap = (i >> 1) & 1;
+            int ok = 1;
+            if (lane == 0)
+                ok = mbar_wait_cluster(accf_bar(b), ap, args.timeout_ns, abort_flag) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) {
+                if (lane == 0) {
+                    if (!*abort_flag) record_timeout(3);
+                    *abort_flag = 1;
+                }
+                break;
+            }
+            tc_fence_after_sync();
+            const int mt = tile % args.m_tiles;
+            const int nt = tile / args.m_tiles;
+            const int m = mt * 256 + static_cast<int>(rank) * 128 + quarter * 32 + lane;
+            __half *crow = args.C + static_cast<size_t>(m) * args.N;
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t r[32];
+                tmem_load_32cols(tmem_base + lane_field + static_cast<uint32_t>(b * BN + c * 32), r);
+                store_row_chunk(crow, m < args.M, nt * BN + c * 32, args.N, args.vec_store, r);
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(mapa_shared(acce_bar(b), 0));
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (*abort_flag) {
+        // The even CTA waits for the last phase armed on each stage (it counts
+        // both CTAs' bytes) and for every MMA it issued; the odd CTA's copies
+        // complete on those same barriers.
+        if (leader && warp == 0 && lane == 0) {
+            for (int s = 0; s < STAGES; ++s)
+                if (armed & (1u << s))
+                    (void)mbar_wait_cluster(full_bar(s), ((arm_parity >> s) & 1u) ^ 1u,
+                                            args.timeout_ns, &never_abort);
+        }
+        if (leader && warp == 1 && lane == 0) {
+            mma_commit_pair(drain_bar);
+            (void)mbar_wait_cluster(drain_bar, 0, args.timeout_ns, &never_abort);
+        }
+        __syncwarp();
+        tc_fence_before_sync();
+        __syncthreads();
+    }
+    // Neither CTA may leave while the other can still touch its shared memory
+    // (remote arrivals, pair TMA completions, pair MMA operand reads).
+    cluster_sync();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc_pair(tmem_base, T::kTmemCols);
     }
 }
 
@@ -408,6 +651,76 @@ int launch_variant(const F16Launch &L, std::string &err) {
     return GEMM_OK;
 }
 
+template <int STAGES>
+int launch_pair(const F16Launch &L, std::string &err) {
+    using T = PairCfg<STAGES>;
+    auto kernel = gemm_f16_nt_pair_kernel<STAGES>;
+    static int max_clusters[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        err = std::string("cudaGetDevice: ") + cudaGetErrorString(e);
+        return GEMM_ERR_CUDA;
+    }
+    const bool cached = dev >= 0 && dev < 64 && max_clusters[dev] > 0;
+    if (!cached) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, T::kSmemBytes);
+        if (e != cudaSuccess) {
+            err = std::string("cudaFuncSetAttribute(max dynamic smem): ") + cudaGetErrorString(e);
+            return GEMM_ERR_CUDA;
+        }
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = T::kSmemBytes;
+    cfg.stream = L.stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = cached ? max_clusters[dev] : 0;
+    if (!cached) {
+        // How many CTA pairs can be resident at once: the persistent grid size.
+        cfg.gridDim = dim3(2);
+        e = cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg);
+        if (e != cudaSuccess || clusters <= 0) {
+            err = std::string("cudaOccupancyMaxActiveClusters: ") + cudaGetErrorString(e);
+            return GEMM_ERR_CUDA;
+        }
+        if (dev >= 0 && dev < 64) max_clusters[dev] = clusters;
+    }
+    CUtensorMap tmA, tmB;
+    if (!encode_operand_map(&tmA, L.A, L.M, L.K, kBM, err)) return GEMM_ERR_CUDA;
+    if (!encode_operand_map(&tmB, L.B, L.N, L.K, 128, err)) return GEMM_ERR_CUDA;
+
+    F16Args args;
+    args.C = static_cast<__half *>(L.C);
+    args.M = L.M;
+    args.N = L.N;
+    args.K = L.K;
+    args.m_tiles = (L.M + 255) / 256;
+    args.n_tiles = (L.N + 255) / 256;
+    args.num_kb = (L.K + kBK - 1) / kBK;
+    args.vec_store = (L.N % 8 == 0) && ((reinterpret_cast<uintptr_t>(L.C) & 15u) == 0);
+    args.timeout_ns = L.timeout_ns;
+    args.debug_skip_kblock = L.debug_skip_kblock;
+    const int tiles = args.m_tiles * args.n_tiles;
+    int pairs = L.grid / 2;
+    if (pairs < 1) pairs = 1;
+    if (pairs > clusters) pairs = clusters;
+    if (pairs > tiles) pairs = tiles;
+    cfg.gridDim = dim3(2 * pairs);
+    e = cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, args);
+    if (e != cudaSuccess) {
+        err = std::string("gemm_f16_nt pair kernel launch: ") + cudaGetErrorString(e);
+        return GEMM_ERR_CUDA;
+    }
+    return GEMM_OK;
+}
+
 }  // namespace
 
 int f16_launch(const F16Launch &L, std::string &err) {
@@ -425,6 +738,7 @@ int f16_launch(const F16Launch &L, std::string &err) {
     switch (L.variant) {
         case GEMM_F16_128x256: return launch_variant<256, 4>(L, err);
         case GEMM_F16_128x128: return launch_variant<128, 6>(L, err);
+        case GEMM_F16_256x256_PAIR: return launch_pair<6>(L, err);
         default: err = "unknown fp16 variant"; return GEMM_ERR_INVALID_ARG;
     }
 }

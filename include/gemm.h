@@ -104,7 +104,8 @@ int gemm_check_device_status(gemm_stream_t stream);
 /*
  * One kernel configuration of the fp16 path.  `variant` names a compiled
  * instance (GEMM_F16_* below); grid is the persistent CTA count
- * (0 = choose from the device's SM count).
+ * (0 = choose from the device's SM count; for the pair variant it is rounded
+ * down to whole pairs and capped by the pairs the device can hold at once).
  */
 typedef struct {
     int variant;
@@ -115,7 +116,9 @@ enum {
     GEMM_F16_AUTO = 0,          /* let gemm_f16_select decide                     */
     GEMM_F16_128x256 = 1,       /* one CTA per 128 x 256 output tile, 4 stages    */
     GEMM_F16_128x128 = 2,       /* one CTA per 128 x 128 output tile, 6 stages    */
-    GEMM_F16_NUM_VARIANTS = 3
+    GEMM_F16_256x256_PAIR = 3,  /* a 2-CTA cluster per 256 x 256 tile (pair MMA,  */
+                                /* each CTA 128 rows of A and half of B), 6 stages */
+    GEMM_F16_NUM_VARIANTS = 4
 };
 
 /*

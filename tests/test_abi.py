@@ -88,9 +88,13 @@ def test_bad_config_is_rejected(lib):
 
 
 def test_f16_selector(lib):
-    # the two fp16 workloads: wide tiles, one persistent CTA per SM
-    assert g.gemm_f16_select(5376, 5376, 2048, 152) == (g.GEMM_F16_128x256, 152)
-    assert g.gemm_f16_select(5000, 5376, 2040, 152) == (g.GEMM_F16_128x256, 152)
+    # the two fp16 workloads: CTA-pair 256 x 256 tiles, one CTA per SM
+    assert g.gemm_f16_select(5376, 5376, 2048, 152) == (g.GEMM_F16_256x256_PAIR, 152)
+    assert g.gemm_f16_select(5000, 5376, 2040, 152) == (g.GEMM_F16_256x256_PAIR, 152)
+    assert g.gemm_f16_select(5376, 5376, 2048, 151) == (g.GEMM_F16_256x256_PAIR, 150)
+    assert g.gemm_f16_select(4096, 2048, 512, 148) == (g.GEMM_F16_256x256_PAIR, 148)
+    # fewer pair tiles than SM pairs: narrow tiles
+    assert g.gemm_f16_select(2048, 2048, 512, 152) == (g.GEMM_F16_128x128, 152)
     # too few wide tiles to fill the SMs: narrow tiles, grid = tile count
     assert g.gemm_f16_select(1024, 1024, 1024, 152) == (g.GEMM_F16_128x128, 64)
     assert g.gemm_f16_select(100, 100, 64, 152) == (g.GEMM_F16_128x128, 1)

@@ -59,7 +59,10 @@ SHAPES = [
 ]
 
 
-@pytest.mark.parametrize("variant", [g.GEMM_F16_128x256, g.GEMM_F16_128x128])
+VARIANTS = [g.GEMM_F16_128x256, g.GEMM_F16_128x128, g.GEMM_F16_256x256_PAIR]
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("M,N,K", SHAPES)
 def test_f16_nt_full_compare(M, N, K, variant):
     A = wl.draw_f16((M, K), seed=M + 1)
@@ -70,10 +73,12 @@ def test_f16_nt_full_compare(M, N, K, variant):
 
 
 @pytest.mark.parametrize("variant,grid", [(g.GEMM_F16_128x256, 1), (g.GEMM_F16_128x256, 3),
-                                          (g.GEMM_F16_128x128, 1), (g.GEMM_F16_128x128, 5)])
+                                          (g.GEMM_F16_128x128, 1), (g.GEMM_F16_128x128, 5),
+                                          (g.GEMM_F16_256x256_PAIR, 2),
+                                          (g.GEMM_F16_256x256_PAIR, 6)])
 def test_f16_nt_persistent_many_tiles_per_cta(variant, grid):
-    # 5 x 3 (wide) or 5 x 6 (narrow) tiles on 1..5 CTAs: every stage and
-    # accumulator barrier goes through several phases.
+    # 5 x 3 (wide), 5 x 6 (narrow) or 3 x 3 (pair) tiles on 1..5 CTAs or 1..3
+    # CTA pairs: every stage and accumulator barrier goes through several phases.
     M, N, K = 600, 700, 392
     A = wl.draw_f16((M, K), seed=31, dist="normal")
     B = wl.draw_f16((N, K), seed=32, dist="normal")
@@ -145,6 +150,17 @@ def test_f16_nt_on_a_side_stream_and_tensor_wrapper():
     s.synchronize()
     Cref, S = oracle.gemm_f16_nt(A, B)
     check_f16(C.cpu().numpy(), Cref, S, what="side stream")
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_f16_nt_long_k_many_tiles(variant):
+    # K = 4096 (64 k-blocks) over a grid that cycles each CTA through tiles.
+    M, N, K = 1024, 1280, 4096
+    A = wl.draw_f16((M, K), seed=51, dist="normal")
+    B = wl.draw_f16((N, K), seed=52, dist="normal")
+    C = _run(A, B, variant, grid=8)
+    Cref, S = oracle.gemm_f16_nt(A, B)
+    check_f16(C, Cref, S, what=f"long K v{variant}")
 
 
 @pytest.mark.parametrize("name", ["f16_nt_5376x5376x2048", "f16_nt_5000x5376x2040"])
