@@ -331,6 +331,12 @@ def run_ours(args):
     value = world * w.flop * args.steps / (region_ms * 1e-3) / 1e12
     avg_launch_ms = statistics.mean(launch_ms)
 
+    sm_count = torch.cuda.get_device_properties(local).multi_processor_count
+    variant, grid = g.gemm_f16_select(M, N, K, sm_count)
+    kernel_name = {g.GEMM_F16_128x256: "gemm_f16_nt_tc_kernel<256,4> (1-CTA 128x256)",
+                   g.GEMM_F16_128x128: "gemm_f16_nt_tc_kernel<128,6> (1-CTA 128x128)",
+                   g.GEMM_F16_256x256_PAIR: "gemm_f16_nt_pair_kernel<6> (CTA pair 256x256)"
+                   }[variant] + f", grid {grid}"
     peaks, peak_kind = measured_peaks()
     peak = float(peaks.get("bf16_tflops", FALLBACK_TENSOR_TFLOPS))
     achieved = w.flop / (avg_launch_ms * 1e-3) / 1e12
@@ -350,7 +356,7 @@ def run_ours(args):
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": profiled_traffic(),
                      "peak_source": f"{peak_kind} bf16 dense burst (fp16 runs at the bf16 rate)",
-                     "kernel": "gemm_f16_nt_tc_kernel<256,4>",
+                     "kernel": kernel_name,
                      "avg_launch_us": 1e3 * avg_launch_ms},
         "gpu_launches": args.steps,
         "clocks": clocks.summary(),
@@ -407,7 +413,6 @@ def run_ours(args):
                     dsc.data_ptr(), sh)
         time_launches(sg, stream, 3)
         st = time_launches(sg, stream, max(5, min(args.steps, 20)))
-        sm_count = torch.cuda.get_device_properties(local).multi_processor_count
         fp32_peak = sm_count * 128 * 2 * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6 / 1e12
         sval = sw.flop / (statistics.mean(st) * 1e-3) / 1e12
         line["sgemm"] = {"workload": sw.name, "value": sval, "unit": "TFLOP/s",
