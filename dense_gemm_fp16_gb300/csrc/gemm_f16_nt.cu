@@ -23,6 +23,10 @@
 //                 masked stores;
 //  * the accumulator is double-buffered in TMEM (2 x BN columns), so the
 //    epilogue of tile i overlaps the main loop of tile i+1;
+//  * programmatic dependent launch: the prologue (barrier init, TMEM alloc,
+//    descriptor prefetch) of one call overlaps the tail of the previous
+//    kernel in the stream; global memory is touched only after
+//    griddepcontrol.wait;
 //  * every wait is bounded in time: on expiry the kernel records a status
 //    code, tells the other roles to stop, waits (bounded) for its own copies
 //    and MMAs in flight, frees TMEM and returns.
@@ -31,6 +35,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdio>
+#include <cstring>
 #include <mutex>
 
 #include "gemm.h"
@@ -44,6 +49,10 @@ constexpr int kBM = 128;       // rows of an output tile (= MMA M, = TMEM lanes)
 constexpr int kBK = 64;        // halves per k-block: one 128-byte swizzle row
 constexpr int kUmmaK = 16;     // K of one kind::f16 MMA
 constexpr int kThreads = 192;  // 6 warps
+// Epilogue staging: each of the 4 epilogue warps owns two 4 KB buffers, each
+// holding 32 rows x 64 halves (128 B per row, 128-byte swizzled) for a TMA store.
+constexpr int kEpiBufBytes = 32 * 128;
+constexpr int kEpiBytes = 4 * 2 * kEpiBufBytes;
 
 // Device-side status: first timeout code recorded by any CTA (0 = none).
 // 1 = producer (empty-slot wait), 2 = MMA (full-slot or accumulator-free
@@ -55,6 +64,7 @@ struct F16Args {
     int M, N, K;
     int m_tiles, n_tiles, num_kb;
     int vec_store;          // N % 8 == 0 and C 16-byte aligned
+    int tma_store;          // same condition: the epilogue stores through a C tensor map
     uint64_t timeout_ns;
     int debug_skip_kblock;  // -1 = none
 };
@@ -66,8 +76,10 @@ struct TileCfg {
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kTmemCols = 2 * BN;  // two accumulator buffers
     static constexpr int kNumBars = 2 * STAGES + 5;
-    static constexpr int kBarOffset = STAGES * kStageBytes;
+    static constexpr int kEpiOffset = STAGES * kStageBytes;
+    static constexpr int kBarOffset = kEpiOffset + kEpiBytes;
     static constexpr int kSmemBytes = 1024 + kBarOffset + kNumBars * 8 + 16;
+    static_assert(kSmemBytes <= 232448, "fits the 227 KB opt-in limit");
     static_assert(kABytes % 1024 == 0 && kBBytes % 1024 == 0, "swizzle atoms stay aligned");
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "valid UMMA N for M = 128");
     static_assert(kTmemCols == 256 || kTmemCols == 512, "TMEM allocation is a power of two");
@@ -103,10 +115,69 @@ __device__ __forceinline__ void store_row_chunk(__half *crow, bool row_ok, int n
     }
 }
 
+// Epilogue of one accumulator tile for one epilogue warp: output rows
+// row0 .. row0+31 (lane i holds row row0+i, the TMEM lane it may read),
+// columns n_base .. n_base+BN-1, read from TMEM address `taddr` onwards.
+// With a C tensor map, each 64-column slab is rounded to half, written into
+// one of the warp's two swizzled staging buffers and stored by one TMA
+// instruction (out-of-range rows and columns are clipped by the TMA unit);
+// otherwise each thread stores its own row directly.
+template <int BN>
+__device__ __forceinline__ void epilogue_warp_tile(const F16Args &args, const CUtensorMap *tmC,
+                                                   uint32_t taddr, int row0, int n_base, int lane,
+                                                   uint32_t stage_smem, uint32_t &step) {
+    if (args.tma_store) {
+#pragma unroll 1
+        for (int c = 0; c < BN / 64; ++c) {
+            uint32_t lo[32], hi[32];
+            tmem_load_32cols(taddr + static_cast<uint32_t>(c * 64), lo);
+            tmem_load_32cols(taddr + static_cast<uint32_t>(c * 64 + 32), hi);
+            const uint32_t buf = stage_smem + (step & 1u) * kEpiBufBytes;
+            // The store issued from this buffer two slabs ago must have read it.
+            if (lane == 0) bulk_wait_group_read<1>();
+            __syncwarp();
+            const uint32_t row_addr = buf + static_cast<uint32_t>(lane) * 128u;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t *v = j < 4 ? &lo[j * 8] : &hi[(j - 4) * 8];
+                __half2 h0 = __floats2half2_rn(__uint_as_float(v[0]), __uint_as_float(v[1]));
+                __half2 h1 = __floats2half2_rn(__uint_as_float(v[2]), __uint_as_float(v[3]));
+                __half2 h2 = __floats2half2_rn(__uint_as_float(v[4]), __uint_as_float(v[5]));
+                __half2 h3 = __floats2half2_rn(__uint_as_float(v[6]), __uint_as_float(v[7]));
+                // 16-byte chunk j of row `lane` sits at chunk j ^ (lane % 8): the
+                // TMA's 128-byte swizzle, which also spreads a quarter-warp's
+                // writes over all 32 banks.
+                st_shared_v4(row_addr + (static_cast<uint32_t>(j ^ (lane & 7)) << 4),
+                             *reinterpret_cast<uint32_t *>(&h0), *reinterpret_cast<uint32_t *>(&h1),
+                             *reinterpret_cast<uint32_t *>(&h2), *reinterpret_cast<uint32_t *>(&h3));
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                // A box wholly past the last row or column would store nothing.
+                if (row0 < args.M && n_base + c * 64 < args.N)
+                    tma_store_2d(tmC, buf, n_base + c * 64, row0);
+                bulk_commit_group();
+            }
+            ++step;
+        }
+    } else {
+        const int m = row0 + lane;
+        __half *crow = args.C + static_cast<size_t>(m) * args.N;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+            uint32_t r[32];
+            tmem_load_32cols(taddr + static_cast<uint32_t>(c * 32), r);
+            store_row_chunk(crow, m < args.M, n_base + c * 32, args.N, args.vec_store, r);
+        }
+    }
+}
+
 template <int BN, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_f16_nt_tc_kernel(const __grid_constant__ CUtensorMap tmA,
-                          const __grid_constant__ CUtensorMap tmB, const F16Args args) {
+                          const __grid_constant__ CUtensorMap tmB,
+                          const __grid_constant__ CUtensorMap tmC, const F16Args args) {
     using T = TileCfg<BN, STAGES>;
     extern __shared__ uint8_t smem_raw[];
     // 128-byte swizzle atoms must sit on 1024-byte boundaries of the shared window.
@@ -131,6 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        if (args.tma_store) tma_prefetch_desc(&tmC);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);   // producer's arrive.expect_tx + TMA bytes
             mbar_init(empty_bar(s), 1);  // one tcgen05.commit
@@ -152,6 +224,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    // Everything above overlaps the previous kernel's tail under programmatic
+    // dependent launch; A and B are read and C written only after this wait.
+    pdl_launch_dependents();
+    pdl_wait_prerequisites();
 
     const int total_tiles = args.m_tiles * args.n_tiles;
     const int num_kb = args.num_kb;
@@ -249,6 +325,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ epilogue
         const int quarter = warp & 3;  // TMEM lanes this warp may read: 32*quarter ..
         const uint32_t lane_field = static_cast<uint32_t>(quarter * 32) << 16;
+        const uint32_t stage_smem = sbase + T::kEpiOffset + (warp - 2) * 2 * kEpiBufBytes;
+        uint32_t step = 0;
         int i = 0;
         for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++i) {
             const int b = i & 1;
@@ -266,18 +344,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after_sync();
             const int mt = tile % args.m_tiles;
             const int nt = tile / args.m_tiles;
-            const int m = mt * kBM + quarter * 32 + lane;
-            __half *crow = args.C + static_cast<size_t>(m) * args.N;
-#pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t r[32];
-                tmem_load_32cols(tmem_base + lane_field + static_cast<uint32_t>(b * BN + c * 32), r);
-                store_row_chunk(crow, m < args.M, nt * BN + c * 32, args.N, args.vec_store, r);
-            }
+            epilogue_warp_tile<BN>(args, &tmC, tmem_base + lane_field + static_cast<uint32_t>(b * BN),
+                                   mt * kBM + quarter * 32, nt * BN, lane, stage_smem, step);
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(acce_bar(b));
         }
+        if (lane == 0) bulk_wait_group_all();  // C fully written before the CTA retires
+        __syncwarp();
     }
 
     tc_fence_before_sync();
@@ -331,7 +405,8 @@ struct PairCfg {
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kTmemCols = 512;           // two 256-column accumulators
     static constexpr int kNumBars = 2 * STAGES + 5;
-    static constexpr int kBarOffset = STAGES * kStageBytes;
+    static constexpr int kEpiOffset = STAGES * kStageBytes;
+    static constexpr int kBarOffset = kEpiOffset + kEpiBytes;
     static constexpr int kSmemBytes = 1024 + kBarOffset + kNumBars * 8 + 16;
     static_assert(kSmemBytes <= 232448, "fits the 227 KB opt-in limit");
 };
@@ -339,7 +414,8 @@ struct PairCfg {
 template <int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_f16_nt_pair_kernel(const __grid_constant__ CUtensorMap tmA,
-                            const __grid_constant__ CUtensorMap tmB, const F16Args args) {
+                            const __grid_constant__ CUtensorMap tmB,
+                            const __grid_constant__ CUtensorMap tmC, const F16Args args) {
     using T = PairCfg<STAGES>;
     constexpr int BN = T::kBN;
     extern __shared__ uint8_t smem_raw[];
@@ -368,6 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        if (args.tma_store) tma_prefetch_desc(&tmC);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
@@ -389,6 +466,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     cluster_sync();  // barriers of both CTAs initialised, TMEM allocated in both
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    pdl_launch_dependents();
+    pdl_wait_prerequisites();
 
     const int total_tiles = args.m_tiles * args.n_tiles;  // pair tiles
     const int num_kb = args.num_kb;
@@ -485,6 +564,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ epilogue (both CTAs)
         const int quarter = warp & 3;
         const uint32_t lane_field = static_cast<uint32_t>(quarter * 32) << 16;
+        const uint32_t stage_smem = sbase + T::kEpiOffset + (warp - 2) * 2 * kEpiBufBytes;
+        uint32_t step = 0;
         int i = 0;
         for (int tile = pair; tile < total_tiles; tile += num_pairs, ++i) {
             const int b = i & 1;
@@ -503,18 +584,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after_sync();
             const int mt = tile % args.m_tiles;
             const int nt = tile / args.m_tiles;
-            const int m = mt * 256 + static_cast<int>(rank) * 128 + quarter * 32 + lane;
-            __half *crow = args.C + static_cast<size_t>(m) * args.N;
-#pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t r[32];
-                tmem_load_32cols(tmem_base + lane_field + static_cast<uint32_t>(b * BN + c * 32), r);
-                store_row_chunk(crow, m < args.M, nt * BN + c * 32, args.N, args.vec_store, r);
-            }
+            epilogue_warp_tile<BN>(args, &tmC, tmem_base + lane_field + static_cast<uint32_t>(b * BN),
+                                   mt * 256 + static_cast<int>(rank) * 128 + quarter * 32, nt * BN,
+                                   lane, stage_smem, step);
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(mapa_shared(acce_bar(b), 0));
         }
+        if (lane == 0) bulk_wait_group_all();
+        __syncwarp();
     }
 
     tc_fence_before_sync();
@@ -580,15 +658,16 @@ EncodeTiledFn get_encode_fn(std::string &err) {
     return fn;
 }
 
-// 2-D K-major operand [rows, K] of halves; box = box_rows x 64 halves, 128B swizzle,
-// zero fill out of bounds.
-bool encode_operand_map(CUtensorMap *map, const void *ptr, int rows, int K, int box_rows,
-                        std::string &err) {
+// Row-major 2-D tensor of halves [rows, cols]: box = box_rows x box_cols,
+// 128-byte swizzle (box_cols * 2 == 128), zero fill out of bounds on loads,
+// clipping on stores.
+bool encode_half_map(CUtensorMap *map, const void *ptr, int rows, int cols, int box_rows,
+                     int box_cols, std::string &err) {
     EncodeTiledFn enc = get_encode_fn(err);
     if (!enc) return false;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
     const cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(ptr), dims,
                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -596,8 +675,8 @@ bool encode_operand_map(CUtensorMap *map, const void *ptr, int rows, int K, int 
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
         char buf[160];
-        std::snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled failed (CUresult %d) rows=%d K=%d",
-                      static_cast<int>(r), rows, K);
+        std::snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled failed (CUresult %d) rows=%d cols=%d",
+                      static_cast<int>(r), rows, cols);
         err = buf;
         return false;
     }
@@ -626,8 +705,8 @@ int launch_variant(const F16Launch &L, std::string &err) {
         if (dev >= 0 && dev < 64) configured[dev] = 1;
     }
     CUtensorMap tmA, tmB;
-    if (!encode_operand_map(&tmA, L.A, L.M, L.K, kBM, err)) return GEMM_ERR_CUDA;
-    if (!encode_operand_map(&tmB, L.B, L.N, L.K, BN, err)) return GEMM_ERR_CUDA;
+    if (!encode_half_map(&tmA, L.A, L.M, L.K, kBM, kBK, err)) return GEMM_ERR_CUDA;
+    if (!encode_half_map(&tmB, L.B, L.N, L.K, BN, kBK, err)) return GEMM_ERR_CUDA;
 
     F16Args args;
     args.C = static_cast<__half *>(L.C);
@@ -638,12 +717,25 @@ int launch_variant(const F16Launch &L, std::string &err) {
     args.n_tiles = (L.N + BN - 1) / BN;
     args.num_kb = (L.K + kBK - 1) / kBK;
     args.vec_store = (L.N % 8 == 0) && ((reinterpret_cast<uintptr_t>(L.C) & 15u) == 0);
+    args.tma_store = args.vec_store;
     args.timeout_ns = L.timeout_ns;
     args.debug_skip_kblock = L.debug_skip_kblock;
+    CUtensorMap tmC;
+    std::memset(&tmC, 0, sizeof tmC);
+    if (args.tma_store && !encode_half_map(&tmC, L.C, L.M, L.N, 32, 64, err)) return GEMM_ERR_CUDA;
     const int tiles = args.m_tiles * args.n_tiles;
     const int grid = L.grid < tiles ? L.grid : tiles;
-    kernel<<<grid, kThreads, T::kSmemBytes, L.stream>>>(tmA, tmB, args);
-    e = cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = T::kSmemBytes;
+    cfg.stream = L.stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, tmC, args);
     if (e != cudaSuccess) {
         err = std::string("gemm_f16_nt kernel launch: ") + cudaGetErrorString(e);
         return GEMM_ERR_CUDA;
@@ -671,11 +763,13 @@ int launch_pair(const F16Launch &L, std::string &err) {
         }
     }
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = T::kSmemBytes;
     cfg.stream = L.stream;
@@ -693,8 +787,8 @@ int launch_pair(const F16Launch &L, std::string &err) {
         if (dev >= 0 && dev < 64) max_clusters[dev] = clusters;
     }
     CUtensorMap tmA, tmB;
-    if (!encode_operand_map(&tmA, L.A, L.M, L.K, kBM, err)) return GEMM_ERR_CUDA;
-    if (!encode_operand_map(&tmB, L.B, L.N, L.K, 128, err)) return GEMM_ERR_CUDA;
+    if (!encode_half_map(&tmA, L.A, L.M, L.K, kBM, kBK, err)) return GEMM_ERR_CUDA;
+    if (!encode_half_map(&tmB, L.B, L.N, L.K, 128, kBK, err)) return GEMM_ERR_CUDA;
 
     F16Args args;
     args.C = static_cast<__half *>(L.C);
@@ -705,15 +799,20 @@ int launch_pair(const F16Launch &L, std::string &err) {
     args.n_tiles = (L.N + 255) / 256;
     args.num_kb = (L.K + kBK - 1) / kBK;
     args.vec_store = (L.N % 8 == 0) && ((reinterpret_cast<uintptr_t>(L.C) & 15u) == 0);
+    args.tma_store = args.vec_store;
     args.timeout_ns = L.timeout_ns;
     args.debug_skip_kblock = L.debug_skip_kblock;
+    CUtensorMap tmC;
+    std::memset(&tmC, 0, sizeof tmC);
+    if (args.tma_store && !encode_half_map(&tmC, L.C, L.M, L.N, 32, 64, err)) return GEMM_ERR_CUDA;
     const int tiles = args.m_tiles * args.n_tiles;
     int pairs = L.grid / 2;
     if (pairs < 1) pairs = 1;
     if (pairs > clusters) pairs = clusters;
     if (pairs > tiles) pairs = tiles;
     cfg.gridDim = dim3(2 * pairs);
-    e = cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, args);
+    cfg.numAttrs = 2;  // cluster shape + programmatic dependent launch
+    e = cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, tmC, args);
     if (e != cudaSuccess) {
         err = std::string("gemm_f16_nt pair kernel launch: ") + cudaGetErrorString(e);
         return GEMM_ERR_CUDA;
