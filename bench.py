@@ -260,18 +260,18 @@ def run_reference(args):
 # our arm
 # ---------------------------------------------------------------------------
 
-def time_launches(fn, stream, n):
-    """Average device time of n launches of fn, CUDA events on `stream`."""
+def region_time(fn, stream, n):
+    """Device time (ms) of n back-to-back calls fn(0..n-1), CUDA events on `stream`."""
     import torch
 
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(n)]
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
     for i in range(n):
-        ev[i][0].record(stream)
         fn(i)
-        ev[i][1].record(stream)
+    b.record(stream)
     stream.synchronize()
-    return [a.elapsed_time(b) for a, b in ev]
+    return a.elapsed_time(b)
 
 
 def run_ours(args):
@@ -306,30 +306,32 @@ def run_ours(args):
     # ---- timed region: exactly K steps, barrier + synchronize on both sides.
     # nvidia-smi samples every 100 ms, so the sampler also covers a short soak
     # of the same launches right before and right after the timed region.
-    ev_start = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ev_end = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    soak = max(1, int(args.soak_s / max(1e-4, 1e-3 * statistics.mean(
-        time_launches(step, stream, 5)))))
+    # Only two events bracket the K launches: an event recorded between two
+    # launches would serialise them and hide the programmatic-dependent-launch
+    # overlap that back-to-back calls get.  The average launch duration is the
+    # region time over K (one launch per step).
+    ev_start = torch.cuda.Event(enable_timing=True)
+    ev_end = torch.cuda.Event(enable_timing=True)
+    soak = max(1, int(args.soak_s / max(1e-4, 1e-3 * region_time(step, stream, 5) / 5)))
     with ClockSampler(local) as clocks:
-        time_launches(step, stream, soak)
+        region_time(step, stream, soak)
         barrier(world)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
+        ev_start.record(stream)
         for i in range(args.steps):
-            ev_start[i].record(stream)
             step(i)
-            ev_end[i].record(stream)
+        ev_end.record(stream)
         torch.cuda.synchronize()
         barrier(world)
         wall = time.perf_counter() - t0
-        time_launches(step, stream, soak)
+        region_time(step, stream, soak)
     g.gemm_check_device_status(sh)
-    launch_ms = [a.elapsed_time(b) for a, b in zip(ev_start, ev_end)]
-    region_ms = ev_start[0].elapsed_time(ev_end[-1])
-    region_ms = max_over_ranks(region_ms, world)
+    local_ms = ev_start.elapsed_time(ev_end)
+    region_ms = max_over_ranks(local_ms, world)
     ms_per_step = region_ms / args.steps
     value = world * w.flop * args.steps / (region_ms * 1e-3) / 1e12
-    avg_launch_ms = statistics.mean(launch_ms)
+    avg_launch_ms = local_ms / args.steps
 
     sm_count = torch.cuda.get_device_properties(local).multi_processor_count
     variant, grid = g.gemm_f16_select(M, N, K, sm_count)
@@ -395,9 +397,9 @@ def run_ours(args):
         def cublas_step(i):
             x, y, z = sets[i % ROTATE]
             torch.matmul(x, y.t(), out=z)
-        time_launches(cublas_step, stream, args.warmup + 2)
-        cb = time_launches(cublas_step, stream, args.steps)
-    line["cublas"] = {"value": w.flop / (statistics.mean(cb) * 1e-3) / 1e12, "unit": "TFLOP/s",
+        region_time(cublas_step, stream, args.warmup + 2)
+        cb = region_time(cublas_step, stream, args.steps) / args.steps
+    line["cublas"] = {"value": w.flop / (cb * 1e-3) / 1e12, "unit": "TFLOP/s",
                       "what": "torch.matmul(A, B.t()) fp16, fp32 accumulation; reference only"}
 
     # ---- fp32 SGEMM 4096^3 (alpha 1, beta 0.5) against the FP32 FFMA peak
@@ -411,10 +413,11 @@ def run_ours(args):
         def sg(_):
             g.sgemm(sw.M, sw.N, sw.K, sw.alpha, dsa.data_ptr(), dsb.data_ptr(), sw.beta,
                     dsc.data_ptr(), sh)
-        time_launches(sg, stream, 3)
-        st = time_launches(sg, stream, max(5, min(args.steps, 20)))
+        region_time(sg, stream, 3)
+        n_sg = max(5, min(args.steps, 20))
+        st = region_time(sg, stream, n_sg) / n_sg
         fp32_peak = sm_count * 128 * 2 * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6 / 1e12
-        sval = sw.flop / (statistics.mean(st) * 1e-3) / 1e12
+        sval = sw.flop / (st * 1e-3) / 1e12
         line["sgemm"] = {"workload": sw.name, "value": sval, "unit": "TFLOP/s",
                          "roofline": {"bound": "alu", "achieved": sval, "peak": fp32_peak,
                                       "unit": "TFLOP/s", "frac": sval / fp32_peak,
