@@ -9,14 +9,16 @@
 // Design: each CTA of 256 threads owns a BM x BN tile of C; every thread owns
 // a TM x TN register micro-tile made of 4 x 4 blocks spread BM/RM rows and
 // BN/RN columns apart ("第 6 章 · Shared Memory & Tile", section "6.3.1 寄存器
-// tile").  K is walked in BK = 8 slices through two shared-memory buffers: the
-// next slice is fetched from global memory into registers while the current
-// one is multiplied, then stored, so one __syncthreads per slice suffices.
-// A is stored transposed (As[k][m]) so that every thread reads its rows as
-// float4; the +4 padding of each As row puts the two k-halves a warp writes
-// on disjoint banks (section "6.4 Bank Conflict" of the same page).  Warps
-// are 4 x 8 thread blocks of the 16 x 16 thread grid, so a warp's float4 reads
-// of As and Bs touch 64 B and 128 B respectively: one wavefront each.
+// tile").  K is walked in BK-deep slices through a STAGES-deep ring of shared
+// memory filled by cp.async, STAGES-1 slices ahead of the multiply, one
+// barrier per slice (the multi-stage scheme of the same source section
+// "cp.async 与多级流水 sm_80+", here with zero-filled tails).  Warps are 4 x 8
+// thread blocks of the 16 x 16 thread grid.  On sm_103a the FP32 pipe retires
+// 128 FMA per clock per SM, twice the rate the pages' Ampere kernels were
+// tuned for, so issue slots and shared-memory wavefronts are the limits:
+// the outer product uses the packed two-wide fp32 FMA (fma.rn.f32x2, each
+// lane's two FMAs rounded exactly like fmaf), and the 8 x 8 micro-tile keeps
+// one 128-byte shared-memory wavefront per four FMAs per lane.
 // Out-of-range rows, columns and k are loaded as zeros and never stored, which
 // makes any M, N, K exact.
 #include <cuda_runtime.h>
@@ -28,137 +30,141 @@ namespace gb300 {
 namespace {
 
 constexpr int kSgemmThreads = 256;
-constexpr int kBK = 8;
 
-template <int BM, int BN, int TM, int TN>
-struct SgemmCfg {
-    static constexpr int RM = TM / 4;  // 4-row groups per thread
-    static constexpr int RN = TN / 4;  // 4-column groups per thread
-    static constexpr int kAPitch = BM + 4;
-    static_assert((BM / TM) * (BN / TN) == kSgemmThreads, "16 x 16 thread grid");
-    static_assert(BM / TM == 16 && BN / TN == 16, "thread grid layout assumes 16 x 16");
-    static_assert(TM % 4 == 0 && TN % 4 == 0, "micro-tiles are 4 x 4 blocks");
-};
+// ---------------------------------------------------------------------------
+// A and B slices go straight from global to shared memory
+// with cp.async (16-byte copies, zero-filled past the matrix edges), STAGES-1
+// slices ahead of the multiply, one barrier per slice.  A keeps its row-major
+// layout in shared memory: a thread reads 4 consecutive k of one of its rows as
+// a float4 (all 8 lanes of a quarter-warp read the same row: a broadcast), so
+// no transpose is needed and the loads issue no register-staged stores.
+// ---------------------------------------------------------------------------
 
-template <bool VEC>
-__device__ __forceinline__ float4 load4(const float *__restrict__ p, bool row_ok, int col,
-                                        int ncols) {
-    // Four consecutive elements p[col .. col+3] of one row, zero beyond ncols.
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (!row_ok) return v;
-    if (VEC) {
-        // ncols % 4 == 0 and col % 4 == 0: the group is entirely in or out.
-        if (col < ncols) v = *reinterpret_cast<const float4 *>(p + col);
-    } else {
-        if (col + 0 < ncols) v.x = p[col + 0];
-        if (col + 1 < ncols) v.y = p[col + 1];
-        if (col + 2 < ncols) v.z = p[col + 2];
-        if (col + 3 < ncols) v.w = p[col + 3];
-    }
-    return v;
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                 "r"(valid ? 16 : 0)
+                 : "memory");
 }
 
-template <int BM, int BN, int TM, int TN, bool VEC>
-__global__ void __launch_bounds__(kSgemmThreads)
-    sgemm_kernel(int M, int N, int K, float alpha, const float *__restrict__ A,
-                 const float *__restrict__ B, float beta, float *__restrict__ C) {
-    using Cfg = SgemmCfg<BM, BN, TM, TN>;
-    constexpr int RM = Cfg::RM, RN = Cfg::RN, AP = Cfg::kAPitch;
-    constexpr int A_LOADS = (BM * kBK / 4 + kSgemmThreads - 1) / kSgemmThreads;
-    constexpr int B_LOADS = (BN * kBK / 4 + kSgemmThreads - 1) / kSgemmThreads;
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src, bool valid) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src),
+                 "r"(valid ? 4 : 0)
+                 : "memory");
+}
 
-    __shared__ __align__(16) float As[2][kBK][AP];
-    __shared__ __align__(16) float Bs[2][kBK][BN];
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+template <int BM, int BN, int BK, int TM, int TN, int STAGES, bool VEC>
+__global__ void __launch_bounds__(kSgemmThreads, (TM * TN <= 64) ? 2 : 1)
+    sgemm_pipe_kernel(int M, int N, int K, float alpha, const float *__restrict__ A,
+                      const float *__restrict__ B, float beta, float *__restrict__ C) {
+    constexpr int RM = TM / 4, RN = TN / 4;
+    constexpr int A_CHUNKS = BM * BK / 4, B_CHUNKS = BK * BN / 4;
+    static_assert((BM / TM) * (BN / TN) == kSgemmThreads && BM / TM == 16, "16 x 16 threads");
+    static_assert(BK % 4 == 0, "A is read as float4 along k");
+
+    __shared__ __align__(16) float As[STAGES][BM][BK];
+    __shared__ __align__(16) float Bs[STAGES][BK][BN];
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int ty = (warp >> 1) * 4 + (lane >> 3);  // 0..15
-    const int tx = (warp & 1) * 8 + (lane & 7);    // 0..15
+    const int ty = (warp >> 1) * 4 + (lane >> 3);
+    const int tx = (warp & 1) * 8 + (lane & 7);
     const int m0 = blockIdx.y * BM;
     const int n0 = blockIdx.x * BN;
 
-    float4 ra[A_LOADS], rb[B_LOADS];
-
-    auto fetch = [&](int k0) {
+    auto load_slice = [&](int buf, int k0) {
 #pragma unroll
-        for (int l = 0; l < A_LOADS; ++l) {
-            const int idx = tid + l * kSgemmThreads;
-            if (idx < BM * kBK / 4) {
-                const int row = idx / (kBK / 4), kq = idx % (kBK / 4);
-                const int m = m0 + row;
-                ra[l] = load4<VEC>(A + static_cast<size_t>(m < M ? m : 0) * K, m < M, k0 + kq * 4, K);
+        for (int c = tid; c < A_CHUNKS; c += kSgemmThreads) {
+            const int row = c / (BK / 4), kq = c % (BK / 4);
+            const int m = m0 + row, k = k0 + kq * 4;
+            const float *src = A + static_cast<size_t>(m < M ? m : 0) * K;
+            const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(&As[buf][row][kq * 4]));
+            if (VEC) {
+                cp_async_16(dst, src + (k < K ? k : 0), m < M && k < K);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    cp_async_4(dst + 4 * e, src + (k + e < K ? k + e : 0), m < M && k + e < K);
             }
         }
 #pragma unroll
-        for (int l = 0; l < B_LOADS; ++l) {
-            const int idx = tid + l * kSgemmThreads;
-            if (idx < BN * kBK / 4) {
-                const int kr = idx / (BN / 4), nq = idx % (BN / 4);
-                const int k = k0 + kr;
-                rb[l] = load4<VEC>(B + static_cast<size_t>(k < K ? k : 0) * N, k < K, n0 + nq * 4, N);
-            }
-        }
-    };
-    auto stash = [&](int buf) {
+        for (int c = tid; c < B_CHUNKS; c += kSgemmThreads) {
+            const int kr = c / (BN / 4), nq = c % (BN / 4);
+            const int k = k0 + kr, n = n0 + nq * 4;
+            const float *src = B + static_cast<size_t>(k < K ? k : 0) * N;
+            const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(&Bs[buf][kr][nq * 4]));
+            if (VEC) {
+                cp_async_16(dst, src + (n < N ? n : 0), k < K && n < N);
+            } else {
 #pragma unroll
-        for (int l = 0; l < A_LOADS; ++l) {
-            const int idx = tid + l * kSgemmThreads;
-            if (idx < BM * kBK / 4) {
-                const int row = idx / (kBK / 4), kq = idx % (kBK / 4);
-                As[buf][kq * 4 + 0][row] = ra[l].x;
-                As[buf][kq * 4 + 1][row] = ra[l].y;
-                As[buf][kq * 4 + 2][row] = ra[l].z;
-                As[buf][kq * 4 + 3][row] = ra[l].w;
-            }
-        }
-#pragma unroll
-        for (int l = 0; l < B_LOADS; ++l) {
-            const int idx = tid + l * kSgemmThreads;
-            if (idx < BN * kBK / 4) {
-                const int kr = idx / (BN / 4), nq = idx % (BN / 4);
-                *reinterpret_cast<float4 *>(&Bs[buf][kr][nq * 4]) = rb[l];
+                for (int e = 0; e < 4; ++e)
+                    cp_async_4(dst + 4 * e, src + (n + e < N ? n + e : 0), k < K && n + e < N);
             }
         }
     };
 
-    float acc[TM][TN];
+    // Accumulators in column pairs: accp[i][p] = (acc[i][2p], acc[i][2p+1]).
+    // One packed fma.rn.f32x2 performs both fp32 FMAs (each rounded once, as
+    // fmaf would), halving the FFMA issue slots of the outer product.
+    float2 accp[TM][TN / 2];
 #pragma unroll
     for (int i = 0; i < TM; ++i)
 #pragma unroll
-        for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
+        for (int j = 0; j < TN / 2; ++j) accp[i][j] = make_float2(0.f, 0.f);
 
-    const int KT = (K + kBK - 1) / kBK;
-    if (KT > 0) {
-        fetch(0);
-        stash(0);
+    const int KT = (K + BK - 1) / BK;
+#pragma unroll
+    for (int s = 0; s < STAGES - 1; ++s) {
+        if (s < KT) load_slice(s, s * BK);
+        cp_async_commit();  // one group per slice, empty ones included
     }
-    __syncthreads();
     for (int kt = 0; kt < KT; ++kt) {
-        const int cur = kt & 1;
-        if (kt + 1 < KT) fetch((kt + 1) * kBK);
+        cp_async_wait<STAGES - 2>();  // slice kt has landed (this thread's part)
+        __syncthreads();              // ... everyone's part; slice kt-1 is no longer read
+        const int next = kt + STAGES - 1;
+        if (next < KT) load_slice(next % STAGES, next * BK);
+        cp_async_commit();
+        const int buf = kt % STAGES;
 #pragma unroll
-        for (int k = 0; k < kBK; ++k) {
-            float a[TM], b[TN];
+        for (int kq = 0; kq < BK / 4; ++kq) {
+            float4 av[TM];
 #pragma unroll
-            for (int g = 0; g < RM; ++g) {
-                const float4 v = *reinterpret_cast<const float4 *>(&As[cur][k][g * (BM / RM) + ty * 4]);
-                a[g * 4 + 0] = v.x; a[g * 4 + 1] = v.y; a[g * 4 + 2] = v.z; a[g * 4 + 3] = v.w;
+            for (int g = 0; g < RM; ++g)
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    av[g * 4 + i] = *reinterpret_cast<const float4 *>(
+                        &As[buf][g * (BM / RM) + ty * 4 + i][kq * 4]);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                float2 bp[TN / 2];
+#pragma unroll
+                for (int g = 0; g < RN; ++g) {
+                    const float4 v = *reinterpret_cast<const float4 *>(
+                        &Bs[buf][kq * 4 + kk][g * (BN / RN) + tx * 4]);
+                    bp[g * 2 + 0] = make_float2(v.x, v.y);
+                    bp[g * 2 + 1] = make_float2(v.z, v.w);
+                }
+#pragma unroll
+                for (int i = 0; i < TM; ++i) {
+                    const float a = kk == 0 ? av[i].x : kk == 1 ? av[i].y : kk == 2 ? av[i].z : av[i].w;
+                    const float2 aa = make_float2(a, a);
+#pragma unroll
+                    for (int j = 0; j < TN / 2; ++j) accp[i][j] = __ffma2_rn(aa, bp[j], accp[i][j]);
+                }
             }
-#pragma unroll
-            for (int g = 0; g < RN; ++g) {
-                const float4 v = *reinterpret_cast<const float4 *>(&Bs[cur][k][g * (BN / RN) + tx * 4]);
-                b[g * 4 + 0] = v.x; b[g * 4 + 1] = v.y; b[g * 4 + 2] = v.z; b[g * 4 + 3] = v.w;
-            }
-#pragma unroll
-            for (int i = 0; i < TM; ++i)
-#pragma unroll
-                for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
         }
-        if (kt + 1 < KT) stash(cur ^ 1);
-        __syncthreads();
     }
+    cp_async_wait<0>();
+    const float(&acc)[TM][TN] = *reinterpret_cast<const float(*)[TM][TN]>(&accp[0][0]);
 
-    // Epilogue: C = alpha * acc + beta * C, masked; C is not read when beta == 0.
 #pragma unroll
     for (int gi = 0; gi < RM; ++gi) {
 #pragma unroll
@@ -204,17 +210,17 @@ __global__ void scale_kernel(float *C, size_t count, float beta) {
         C[i] = (beta == 0.f) ? 0.f : beta * C[i];
 }
 
-template <int BM, int BN, int TM, int TN>
-int launch_tile(const SgemmLaunch &L, std::string &err) {
+template <int BM, int BN, int BK, int TM, int TN, int STAGES>
+int launch_pipe(const SgemmLaunch &L, std::string &err) {
     const dim3 grid((L.N + BN - 1) / BN, (L.M + BM - 1) / BM);
     const bool vec = (L.K % 4 == 0) && (L.N % 4 == 0) &&
                      ((reinterpret_cast<uintptr_t>(L.A) | reinterpret_cast<uintptr_t>(L.B) |
                        reinterpret_cast<uintptr_t>(L.C)) & 15u) == 0;
     if (vec)
-        sgemm_kernel<BM, BN, TM, TN, true><<<grid, kSgemmThreads, 0, L.stream>>>(
+        sgemm_pipe_kernel<BM, BN, BK, TM, TN, STAGES, true><<<grid, kSgemmThreads, 0, L.stream>>>(
             L.M, L.N, L.K, L.alpha, L.A, L.B, L.beta, L.C);
     else
-        sgemm_kernel<BM, BN, TM, TN, false><<<grid, kSgemmThreads, 0, L.stream>>>(
+        sgemm_pipe_kernel<BM, BN, BK, TM, TN, STAGES, false><<<grid, kSgemmThreads, 0, L.stream>>>(
             L.M, L.N, L.K, L.alpha, L.A, L.B, L.beta, L.C);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
@@ -239,8 +245,8 @@ int sgemm_launch(const SgemmLaunch &L, std::string &err) {
         return GEMM_OK;
     }
     switch (L.variant) {
-        case GEMM_SGEMM_128x128: return launch_tile<128, 128, 8, 8>(L, err);
-        case GEMM_SGEMM_64x64: return launch_tile<64, 64, 4, 4>(L, err);
+        case GEMM_SGEMM_128x128: return launch_pipe<128, 128, 16, 8, 8, 3>(L, err);
+        case GEMM_SGEMM_64x64: return launch_pipe<64, 64, 16, 4, 4, 3>(L, err);
         default: err = "unknown sgemm variant"; return GEMM_ERR_INVALID_ARG;
     }
 }
