@@ -174,27 +174,50 @@ class ClockSampler:
     def summary(self):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        allrows = []
         with open(self.path) as f:
-            for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) >= 9:
-                    allrows.append(parts)
-        # nvidia-smi prints the bus id as DDDDDDDD:BB:DD.F; match bus and device
-        want = self.bus_id.upper()[-7:] if self.bus_id else None
-        rows = [r for r in allrows if want and r[0].upper().endswith(want)]
-        if not rows and len({r[0] for r in allrows}) == 1:
-            rows = allrows
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
-        loaded = [s for s in sm if mx and s >= 0.3 * max(mx)] or sm
-        return {"sm_mhz": statistics.median(loaded) if loaded else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
-                "samples": len(rows)}
+            return summarize_clock_samples(f.read().splitlines(), self.bus_id)
+
+
+THROTTLE_FIELDS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+
+def summarize_clock_samples(lines, bus_id=None):
+    """Median SM clock under load, max clock and the throttle reasons seen, from
+    nvidia-smi rows `bus_id, sm, max_sm, power, active, hw, hw_thermal,
+    sw_thermal, sw_power` (csv, no header, no units).  Rows of other GPUs are
+    dropped (bus ids end in BB:DD.F); with one GPU listed, all rows count."""
+    allrows = []
+    for line in lines:
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) >= 9:
+            allrows.append(parts)
+    def pci(text):
+        # "DDDDDDDD:BB:DD.F" (any domain width) -> (domain, bus, device)
+        try:
+            dom, bus, rest = text.strip().split(":")
+            return int(dom, 16), int(bus, 16), int(rest.split(".")[0], 16)
+        except ValueError:
+            return None
+
+    want = pci(bus_id) if bus_id else None
+    rows = [r for r in allrows if want is not None and pci(r[0]) == want]
+    if not rows and len({r[0] for r in allrows}) == 1:
+        rows = allrows
+    if not rows:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+    def num(x):
+        try:
+            return float(x)
+        except ValueError:
+            return None
+
+    sm = [v for v in (num(r[1]) for r in rows) if v is not None]
+    mx = [v for v in (num(r[2]) for r in rows) if v is not None]
+    reasons = sorted({THROTTLE_FIELDS[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+    loaded = [v for v in sm if mx and v >= 0.3 * max(mx)] or sm
+    return {"sm_mhz": statistics.median(loaded) if loaded else None,
+            "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
 
 
 # ---------------------------------------------------------------------------
