@@ -21,6 +21,7 @@ GEMM_ERR_DEVICE_TIMEOUT = -5
 
 GEMM_F16_AUTO, GEMM_F16_128x256, GEMM_F16_128x128, GEMM_F16_256x256_PAIR = 0, 1, 2, 3
 GEMM_SGEMM_AUTO, GEMM_SGEMM_128x128, GEMM_SGEMM_64x64 = 0, 1, 2
+GEMM_F16_FLAG_STREAM_K = 1
 
 STATUS_NAMES = {
     GEMM_OK: "GEMM_OK",
@@ -39,7 +40,7 @@ class GemmError(RuntimeError):
 
 
 class _F16Config(ctypes.Structure):
-    _fields_ = [("variant", ctypes.c_int), ("grid", ctypes.c_int)]
+    _fields_ = [("variant", ctypes.c_int), ("grid", ctypes.c_int), ("flags", ctypes.c_int)]
 
 
 class _SgemmConfig(ctypes.Structure):
@@ -102,8 +103,8 @@ def gemm_f16_nt(M: int, N: int, K: int, A: int, B: int, C: int, stream: int | No
     return _check(load_library().gemm_f16_nt(M, N, K, A, B, C, stream or None))
 
 
-def gemm_f16_nt_ex(M, N, K, A, B, C, stream=0, variant=GEMM_F16_AUTO, grid=0) -> int:
-    cfg = _F16Config(variant, grid)
+def gemm_f16_nt_ex(M, N, K, A, B, C, stream=0, variant=GEMM_F16_AUTO, grid=0, flags=0) -> int:
+    cfg = _F16Config(variant, grid, flags)
     return _check(load_library().gemm_f16_nt_ex(M, N, K, A, B, C, stream or None, ctypes.byref(cfg)))
 
 
@@ -123,7 +124,7 @@ def gemm_check_device_status(stream: int | None = 0) -> int:
 
 
 def gemm_f16_select(M: int, N: int, K: int, sm_count: int) -> tuple[int, int]:
-    cfg = _F16Config(0, 0)
+    cfg = _F16Config(0, 0, 0)
     _check(load_library().gemm_f16_select(M, N, K, sm_count, ctypes.byref(cfg)))
     return cfg.variant, cfg.grid
 
@@ -151,7 +152,7 @@ def _stream_handle(stream) -> int:
     return int(s.cuda_stream)
 
 
-def f16_nt(A, B, C=None, stream=None, variant: int = GEMM_F16_AUTO, grid: int = 0):
+def f16_nt(A, B, C=None, stream=None, variant: int = GEMM_F16_AUTO, grid: int = 0, flags: int = 0):
     """C = A·Bᵀ for contiguous half CUDA tensors A [M,K], B [N,K]; returns C [M,N]."""
     import torch
 
@@ -168,7 +169,7 @@ def f16_nt(A, B, C=None, stream=None, variant: int = GEMM_F16_AUTO, grid: int = 
     elif C.shape != (M, N) or C.dtype != torch.float16 or not C.is_contiguous():
         raise ValueError("C must be a contiguous float16 [M, N] tensor")
     gemm_f16_nt_ex(M, N, K, A.data_ptr(), B.data_ptr(), C.data_ptr(), _stream_handle(stream),
-                   variant, grid)
+                   variant, grid, flags)
     return C
 
 

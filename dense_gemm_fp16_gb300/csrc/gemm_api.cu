@@ -104,6 +104,7 @@ int gemm_f16_select(int M, int N, int K, int sm_count, gemm_f16_config *cfg) {
                                                                 : GEMM_F16_128x128;
     cfg->variant = variant;
     cfg->grid = f16_default_grid(variant, M, N, sm_count);
+    cfg->flags = 0;
     return GEMM_OK;
 }
 
@@ -137,9 +138,10 @@ static int f16_nt_impl(int M, int N, int K, const void *A, const void *B, void *
     if (K % 8 != 0)
         return fail(GEMM_ERR_UNSUPPORTED,
                     "gemm_f16_nt: K=%d; K*2 bytes must be a multiple of 16 (K %% 8 == 0)", K);
-    if (cfg && (cfg->variant < 0 || cfg->variant >= GEMM_F16_NUM_VARIANTS || cfg->grid < 0))
-        return fail(GEMM_ERR_INVALID_ARG, "gemm_f16_nt_ex: bad config variant=%d grid=%d",
-                    cfg->variant, cfg->grid);
+    if (cfg && (cfg->variant < 0 || cfg->variant >= GEMM_F16_NUM_VARIANTS || cfg->grid < 0 ||
+                (cfg->flags & ~GEMM_F16_FLAG_STREAM_K) != 0))
+        return fail(GEMM_ERR_INVALID_ARG, "gemm_f16_nt_ex: bad config variant=%d grid=%d flags=%d",
+                    cfg->variant, cfg->grid, cfg->flags);
     int sms = 0;
     int st = sm_count_of_current_device(&sms);
     if (st != GEMM_OK) return st;
@@ -164,6 +166,7 @@ static int f16_nt_impl(int M, int N, int K, const void *A, const void *B, void *
     L.grid = sel.grid;
     L.timeout_ns = timeout_ns;
     L.debug_skip_kblock = debug_skip_kblock;
+    L.allow_stream_k = cfg && (cfg->flags & GEMM_F16_FLAG_STREAM_K);
     std::string err;
     st = gb300::f16_launch(L, err);
     if (st != GEMM_OK) return fail_str(st, err);
@@ -243,10 +246,11 @@ int gemm_check_device_status(gemm_stream_t stream) {
     if (code != 0) {
         static const char *role[] = {"?", "TMA producer (free-slot wait)",
                                      "MMA issuer (data or accumulator wait)",
-                                     "epilogue (accumulator-ready wait)"};
+                                     "epilogue (accumulator-ready wait)",
+                                     "epilogue (stream-K partial wait)"};
         return fail(GEMM_ERR_DEVICE_TIMEOUT,
                     "gemm_f16_nt: a bounded pipeline wait expired in the %s",
-                    role[(code >= 1 && code <= 3) ? code : 0]);
+                    role[(code >= 1 && code <= 4) ? code : 0]);
     }
     return GEMM_OK;
 }

@@ -36,6 +36,8 @@
 
 #include <cstdio>
 #include <cstring>
+#include <map>
+#include <utility>
 #include <mutex>
 
 #include "gemm.h"
@@ -67,6 +69,54 @@ struct F16Args {
     int tma_store;          // same condition: the epilogue stores through a C tensor map
     uint64_t timeout_ns;
     int debug_skip_kblock;  // -1 = none
+    // Stream-K (pair kernel only): tiles [0, dp_tiles) are data-parallel, one
+    // whole tile per work item; the k-blocks of the remaining tiles are split
+    // evenly over the pairs (sk_units k-blocks in all).  A pair whose share
+    // starts inside a tile writes its fp32 partial tile to its workspace slot
+    // and sets its flag to `seq`; the pair holding k-block 0 adds those partials.
+    int dp_tiles;
+    int sk_units;
+    float *sk_ws;           // slot (pair, rank): 128 rows x 256 fp32, row-major
+    uint32_t *sk_flags;     // flag (pair, rank, epilogue warp), 8 per (pair, rank)
+    uint32_t seq;           // this launch's sequence number (never 0)
+};
+
+// The work items of one CTA pair: whole data-parallel tiles first, then its
+// contiguous share of the stream-K k-blocks cut at tile boundaries.  Every role
+// of both CTAs walks the same sequence.  Shares are handed out in reverse pair
+// order (share rank = num_pairs - 1 - pair): the pair that finishes a split
+// tile (it holds k-block 0, which comes last in its share) then has a higher
+// block index than the pairs contributing the tile's later k-blocks, so it is
+// never resident before them and its wait for their partials cannot stall the
+// launch of a contributor.
+struct PairWork {
+    int num_pairs, dp_tiles, num_kb, sk_units;
+    int next_dp, u, u_end;
+    __device__ PairWork(const F16Args &a, int pair, int pairs)
+        : num_pairs(pairs), dp_tiles(a.dp_tiles), num_kb(a.num_kb), sk_units(a.sk_units),
+          next_dp(pair), u(sk_begin(pairs - 1 - pair)), u_end(sk_begin(pairs - pair)) {}
+    // first stream-K k-block of share rank r
+    __device__ int sk_begin(int r) const {
+        return static_cast<int>((static_cast<long long>(r) * sk_units) / num_pairs);
+    }
+    __device__ bool next(int &tile, int &kb0, int &kb1) {
+        if (next_dp < dp_tiles) {
+            tile = next_dp;
+            kb0 = 0;
+            kb1 = num_kb;
+            next_dp += num_pairs;
+            return true;
+        }
+        if (u < u_end) {
+            const int tl = u / num_kb;
+            kb0 = u - tl * num_kb;
+            kb1 = (num_kb < kb0 + (u_end - u)) ? num_kb : kb0 + (u_end - u);
+            tile = dp_tiles + tl;
+            u += kb1 - kb0;
+            return true;
+        }
+        return false;
+    }
 };
 
 template <int BN, int STAGES>
@@ -122,19 +172,81 @@ __device__ __forceinline__ void store_row_chunk(__half *crow, bool row_ok, int n
 // one of the warp's two swizzled staging buffers and stored by one TMA
 // instruction (out-of-range rows and columns are clipped by the TMA unit);
 // otherwise each thread stores its own row directly.
-template <int BN>
+// Stream-K partial tiles.  A slot holds one CTA's 128 x 256 fp32 partial
+// accumulators in a lane-interleaved order: the region of epilogue warp `ew`
+// starts at ew * NCOLS * 32 floats and element (slab c, vector v, lane l) --
+// columns 4v .. 4v+3 of the 64-column slab c of the row that lane l holds --
+// sits at float4 index (c * 16 + v) * 32 + l, so every warp-wide store or load
+// moves 512 contiguous bytes.  The owner's warp with the same `ew` reads what
+// the contributor's warp wrote.
+struct Partials {
+    const float *ws;
+    int count;           // 0: none
+    int first_slot;      // slots first_slot, first_slot - 2, ... (pairs below this one)
+    int region;          // float offset of this warp's region in a slot
+    int lane;
+};
+
+constexpr size_t kSkSlotFloatsDev = 128 * 256;
+
+__device__ __forceinline__ void add_partial_slab(const Partials &pp, int c, uint32_t (&lo)[32],
+                                                 uint32_t (&hi)[32]) {
+#pragma unroll 1
+    for (int q = 0; q < pp.count; ++q) {
+        const float4 *src = reinterpret_cast<const float4 *>(
+                                pp.ws + static_cast<size_t>(pp.first_slot - 2 * q) * kSkSlotFloatsDev +
+                                pp.region) +
+                            static_cast<size_t>(c) * 16 * 32 + pp.lane;
+        float4 x[16];
+#pragma unroll
+        for (int v = 0; v < 16; ++v) x[v] = src[v * 32];
+#pragma unroll
+        for (int v = 0; v < 16; ++v) {
+            uint32_t *d = v < 8 ? &lo[v * 4] : &hi[(v - 8) * 4];
+            d[0] = __float_as_uint(__uint_as_float(d[0]) + x[v].x);
+            d[1] = __float_as_uint(__uint_as_float(d[1]) + x[v].y);
+            d[2] = __float_as_uint(__uint_as_float(d[2]) + x[v].z);
+            d[3] = __float_as_uint(__uint_as_float(d[3]) + x[v].w);
+        }
+    }
+}
+
+// A stream-K contributor's share: the warp's 32 rows x NCOLS fp32 accumulators
+// go to its region of the slot unrounded.
+template <int NCOLS>
+__device__ __forceinline__ void epilogue_warp_partial(float *slot, uint32_t taddr, int region,
+                                                      int lane) {
+#pragma unroll 1
+    for (int c = 0; c < NCOLS / 64; ++c) {
+        uint32_t lo[32], hi[32];
+        tmem_load_32cols(taddr + static_cast<uint32_t>(c * 64), lo);
+        tmem_load_32cols(taddr + static_cast<uint32_t>(c * 64 + 32), hi);
+        float4 *dst = reinterpret_cast<float4 *>(slot + region) + static_cast<size_t>(c) * 16 * 32 + lane;
+#pragma unroll
+        for (int v = 0; v < 16; ++v) {
+            const uint32_t *s = v < 8 ? &lo[v * 4] : &hi[(v - 8) * 4];
+            dst[v * 32] = make_float4(__uint_as_float(s[0]), __uint_as_float(s[1]),
+                                      __uint_as_float(s[2]), __uint_as_float(s[3]));
+        }
+    }
+}
+
+template <int NCOLS, int NBUF>
 __device__ __forceinline__ void epilogue_warp_tile(const F16Args &args, const CUtensorMap *tmC,
                                                    uint32_t taddr, int row0, int n_base, int lane,
-                                                   uint32_t stage_smem, uint32_t &step) {
+                                                   uint32_t stage_smem, uint32_t &step,
+                                                   const Partials &pp = Partials{nullptr, 0, 0, 0, 0}) {
+    static_assert(NCOLS % 64 == 0 && (NBUF == 1 || NBUF == 2), "64-column slabs, 1 or 2 buffers");
     if (args.tma_store) {
 #pragma unroll 1
-        for (int c = 0; c < BN / 64; ++c) {
+        for (int c = 0; c < NCOLS / 64; ++c) {
             uint32_t lo[32], hi[32];
             tmem_load_32cols(taddr + static_cast<uint32_t>(c * 64), lo);
             tmem_load_32cols(taddr + static_cast<uint32_t>(c * 64 + 32), hi);
-            const uint32_t buf = stage_smem + (step & 1u) * kEpiBufBytes;
-            // The store issued from this buffer two slabs ago must have read it.
-            if (lane == 0) bulk_wait_group_read<1>();
+            if (pp.count) add_partial_slab(pp, c, lo, hi);
+            const uint32_t buf = stage_smem + (NBUF == 2 ? (step & 1u) : 0u) * kEpiBufBytes;
+            // The store issued from this buffer NBUF slabs ago must have read it.
+            if (lane == 0) bulk_wait_group_read<NBUF - 1>();
             __syncwarp();
             const uint32_t row_addr = buf + static_cast<uint32_t>(lane) * 128u;
 #pragma unroll
@@ -165,7 +277,7 @@ __device__ __forceinline__ void epilogue_warp_tile(const F16Args &args, const CU
         const int m = row0 + lane;
         __half *crow = args.C + static_cast<size_t>(m) * args.N;
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = 0; c < NCOLS / 32; ++c) {
             uint32_t r[32];
             tmem_load_32cols(taddr + static_cast<uint32_t>(c * 32), r);
             store_row_chunk(crow, m < args.M, n_base + c * 32, args.N, args.vec_store, r);
@@ -344,8 +456,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after_sync();
             const int mt = tile % args.m_tiles;
             const int nt = tile / args.m_tiles;
-            epilogue_warp_tile<BN>(args, &tmC, tmem_base + lane_field + static_cast<uint32_t>(b * BN),
-                                   mt * kBM + quarter * 32, nt * BN, lane, stage_smem, step);
+            epilogue_warp_tile<BN, 2>(args, &tmC, tmem_base + lane_field + static_cast<uint32_t>(b * BN),
+                                      mt * kBM + quarter * 32, nt * BN, lane, stage_smem, step);
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(acce_bar(b));
@@ -411,8 +523,8 @@ struct PairCfg {
     static_assert(kSmemBytes <= 232448, "fits the 227 KB opt-in limit");
 };
 
-template <int STAGES>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int STAGES, int EPI>
+__global__ void __launch_bounds__((2 + EPI) * 32, 1)
     gemm_f16_nt_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                             const __grid_constant__ CUtensorMap tmB,
                             const __grid_constant__ CUtensorMap tmC, const F16Args args) {
@@ -451,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(accf_bar(b), 1);
-            mbar_init(acce_bar(b), 8);
+            mbar_init(acce_bar(b), 2 * EPI);  // every epilogue warp of both CTAs
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
@@ -469,8 +581,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_launch_dependents();
     pdl_wait_prerequisites();
 
-    const int total_tiles = args.m_tiles * args.n_tiles;  // pair tiles
-    const int num_kb = args.num_kb;
     uint32_t armed = 0, arm_parity = 0;
 
     if (warp == 0) {
@@ -480,12 +590,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             bool ok = true;
             bool first_tile = true;
-            for (int tile = pair; tile < total_tiles && ok; tile += num_pairs) {
+            PairWork work(args, pair, num_pairs);
+            int tile, kb0, kb1;
+            while (ok && work.next(tile, kb0, kb1)) {
                 const int mt = tile % args.m_tiles;
                 const int nt = tile / args.m_tiles;
                 const int a_row = mt * 256 + static_cast<int>(rank) * 128;
                 const int b_row = nt * BN + static_cast<int>(rank) * 128;
-                for (int kb = 0; kb < num_kb; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait_cluster(empty_bar(stage), phase ^ 1u, args.timeout_ns, abort_flag)) {
                         ok = false;
                         break;
@@ -522,8 +634,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            int i = 0;
-            for (int tile = pair; tile < total_tiles; tile += num_pairs, ++i) {
+            PairWork work(args, pair, num_pairs);
+            int tile, kb0, kb1;
+            for (int i = 0; work.next(tile, kb0, kb1); ++i) {
                 const int b = i & 1;
                 const uint32_t ap = (i >> 1) & 1;
                 if (!mbar_wait_cluster(acce_bar(b), ap ^ 1u, args.timeout_ns, abort_flag)) {
@@ -532,7 +645,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
-                for (int kb = 0; kb < num_kb; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait_cluster(full_bar(stage), phase, args.timeout_ns, abort_flag)) {
                         ok = false;
                         break;
@@ -544,7 +657,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int k = 0; k < kBK / kUmmaK; ++k)
                         mma_f16_ss_pair(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc,
-                                        (kb > 0 || k > 0) ? 1u : 0u);
+                                        (kb > kb0 || k > 0) ? 1u : 0u);
                     mma_commit_pair_multicast(empty_bar(stage), 0x3);
                     if (++stage == STAGES) {
                         stage = 0;
@@ -562,12 +675,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue (both CTAs)
+        // EPI warps share the tile: warp w reads TMEM lane quarter w % 4 and,
+        // with 8 warps, one half of the columns.
+        constexpr int kCols = BN * 4 / EPI;
+        constexpr int kBufs = 8 / EPI;
+        const int ew = warp - 2;
         const int quarter = warp & 3;
+        const int col0 = (ew / 4) * kCols;
         const uint32_t lane_field = static_cast<uint32_t>(quarter * 32) << 16;
-        const uint32_t stage_smem = sbase + T::kEpiOffset + (warp - 2) * 2 * kEpiBufBytes;
+        const uint32_t stage_smem = sbase + T::kEpiOffset + ew * kBufs * kEpiBufBytes;
         uint32_t step = 0;
-        int i = 0;
-        for (int tile = pair; tile < total_tiles; tile += num_pairs, ++i) {
+        PairWork work(args, pair, num_pairs);
+        int tile, kb0, kb1;
+        for (int i = 0; work.next(tile, kb0, kb1); ++i) {
             const int b = i & 1;
             const uint32_t ap = (i >> 1) & 1;
             int ok = 1;
@@ -584,9 +704,48 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after_sync();
             const int mt = tile % args.m_tiles;
             const int nt = tile / args.m_tiles;
-            epilogue_warp_tile<BN>(args, &tmC, tmem_base + lane_field + static_cast<uint32_t>(b * BN),
-                                   mt * 256 + static_cast<int>(rank) * 128 + quarter * 32, nt * BN,
-                                   lane, stage_smem, step);
+            const uint32_t taddr = tmem_base + lane_field + static_cast<uint32_t>(b * BN + col0);
+            const int region = ew * kCols * 32;    // this warp's part of a partial slot
+            if (kb0 > 0) {
+                // Stream-K contributor: this warp publishes its rows of the
+                // unrounded partial, then its own flag (no barrier between warps).
+                float *slot = args.sk_ws + static_cast<size_t>(pair * 2 + rank) * kSkSlotFloatsDev;
+                epilogue_warp_partial<kCols>(slot, taddr, region, lane);
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) st_release_gpu(args.sk_flags + (pair * 2 + rank) * 8 + ew, args.seq);
+            } else {
+                Partials pp{args.sk_ws, 0, 0, region, lane};
+                if (kb1 < args.num_kb) {
+                    // Owner of a split tile: the following share ranks (pairs
+                    // pair-1, pair-2, ...), whose shares begin inside this tile,
+                    // hold its remaining k-blocks; every share is non-empty, so
+                    // they are consecutive.  This warp waits for the flag of the
+                    // warp that wrote the same rows and columns.
+                    const int tile_end = (tile - args.dp_tiles + 1) * args.num_kb;
+                    const int my_rank = num_pairs - 1 - pair;
+                    pp.first_slot = (pair - 1) * 2 + static_cast<int>(rank);
+                    while (my_rank + 1 + pp.count < num_pairs &&
+                           work.sk_begin(my_rank + 1 + pp.count) < tile_end)
+                        ++pp.count;
+                    int fine = 1;
+                    if (lane == 0)
+                        for (int q = 0; q < pp.count && fine; ++q)
+                            fine = wait_flag_equal(args.sk_flags + (pp.first_slot - 2 * q) * 8 + ew,
+                                                   args.seq, args.timeout_ns, abort_flag) ? 1 : 0;
+                    fine = __shfl_sync(0xffffffffu, fine, 0);
+                    if (!fine) {
+                        if (lane == 0) {
+                            if (!*abort_flag) record_timeout(4);
+                            *abort_flag = 1;
+                        }
+                        break;
+                    }
+                }
+                epilogue_warp_tile<kCols, kBufs>(args, &tmC, taddr,
+                                                 mt * 256 + static_cast<int>(rank) * 128 + quarter * 32,
+                                                 nt * BN + col0, lane, stage_smem, step, pp);
+            }
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(mapa_shared(acce_bar(b), 0));
@@ -745,10 +904,62 @@ int launch_variant(const F16Launch &L, std::string &err) {
     return GEMM_OK;
 }
 
-template <int STAGES>
+// Stream-K workspace of one (device, stream): partial-tile slots and flags,
+// allocated on first use and kept for the life of the process.  Calls on one
+// stream run in order (the kernel touches global memory only after the
+// previous grid has finished), so a stream never has two users of its slots.
+struct SkWorkspace {
+    float *ws = nullptr;
+    uint32_t *flags = nullptr;
+    int pairs = 0;
+    uint32_t seq = 0;
+};
+
+constexpr size_t kSkSlotFloats = 128 * 256;  // one CTA's half of a 256 x 256 tile
+
+int sk_workspace(cudaStream_t stream, int pairs, SkWorkspace **out, std::string &err) {
+    static std::mutex mu;
+    static std::map<std::pair<int, cudaStream_t>, SkWorkspace> cache;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        err = std::string("cudaGetDevice: ") + cudaGetErrorString(e);
+        return GEMM_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    SkWorkspace &w = cache[std::make_pair(dev, stream)];
+    if (w.pairs < pairs) {
+        if (w.ws) cudaFree(w.ws);
+        if (w.flags) cudaFree(w.flags);
+        w = SkWorkspace{};
+        e = cudaMalloc(&w.ws, static_cast<size_t>(pairs) * 2 * kSkSlotFloats * sizeof(float));
+        if (e == cudaSuccess)
+            e = cudaMalloc(&w.flags, static_cast<size_t>(pairs) * 2 * 8 * sizeof(uint32_t));
+        if (e != cudaSuccess) {
+            err = std::string("stream-K workspace allocation: ") + cudaGetErrorString(e);
+            w = SkWorkspace{};
+            return GEMM_ERR_CUDA;
+        }
+        w.pairs = pairs;
+    }
+    if (++w.seq == 0 || w.seq == 1) {
+        // first use, or the sequence number wrapped: no flag may hold a live value
+        e = cudaMemsetAsync(w.flags, 0, static_cast<size_t>(w.pairs) * 2 * 8 * sizeof(uint32_t),
+                            stream);
+        if (e != cudaSuccess) {
+            err = std::string("stream-K flag reset: ") + cudaGetErrorString(e);
+            return GEMM_ERR_CUDA;
+        }
+        w.seq = 1;
+    }
+    *out = &w;
+    return GEMM_OK;
+}
+
+template <int STAGES, int EPI>
 int launch_pair(const F16Launch &L, std::string &err) {
     using T = PairCfg<STAGES>;
-    auto kernel = gemm_f16_nt_pair_kernel<STAGES>;
+    auto kernel = gemm_f16_nt_pair_kernel<STAGES, EPI>;
     static int max_clusters[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -772,7 +983,7 @@ int launch_pair(const F16Launch &L, std::string &err) {
     attr[0].val.clusterDim.z = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3((2 + EPI) * 32);
     cfg.dynamicSmemBytes = T::kSmemBytes;
     cfg.stream = L.stream;
     cfg.attrs = attr;
@@ -812,6 +1023,37 @@ int launch_pair(const F16Launch &L, std::string &err) {
     if (pairs < 1) pairs = 1;
     if (pairs > clusters) pairs = clusters;
     if (pairs > tiles) pairs = tiles;
+
+    // Stream-K for the last, partial round of tiles when it would leave many
+    // pairs idle: their k-blocks are shared out evenly instead.  Needs the TMA
+    // store epilogue, a share of at least one k-block per pair, and a stream
+    // that is not being captured (a replayed graph would reuse the sequence
+    // number baked into its arguments).
+    args.dp_tiles = tiles;
+    args.sk_units = 0;
+    args.sk_ws = nullptr;
+    args.sk_flags = nullptr;
+    args.seq = 0;
+    const int rem = tiles % pairs;
+    if (L.allow_stream_k && args.tma_store && tiles > pairs && rem != 0 &&
+        10 * rem < 9 * pairs && static_cast<long long>(rem) * args.num_kb >= pairs) {
+        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+        e = cudaStreamIsCapturing(L.stream, &cap);
+        if (e != cudaSuccess) {
+            err = std::string("cudaStreamIsCapturing: ") + cudaGetErrorString(e);
+            return GEMM_ERR_CUDA;
+        }
+        if (cap == cudaStreamCaptureStatusNone) {
+            SkWorkspace *w = nullptr;
+            const int st = sk_workspace(L.stream, pairs, &w, err);
+            if (st != GEMM_OK) return st;
+            args.dp_tiles = tiles - rem;
+            args.sk_units = rem * args.num_kb;
+            args.sk_ws = w->ws;
+            args.sk_flags = w->flags;
+            args.seq = w->seq;
+        }
+    }
     cfg.gridDim = dim3(2 * pairs);
     cfg.numAttrs = 2;  // cluster shape + programmatic dependent launch
     e = cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, tmC, args);
@@ -839,7 +1081,7 @@ int f16_launch(const F16Launch &L, std::string &err) {
     switch (L.variant) {
         case GEMM_F16_128x256: return launch_variant<256, 4>(L, err);
         case GEMM_F16_128x128: return launch_variant<128, 6>(L, err);
-        case GEMM_F16_256x256_PAIR: return launch_pair<6>(L, err);
+        case GEMM_F16_256x256_PAIR: return launch_pair<6, 4>(L, err);
         default: err = "unknown fp16 variant"; return GEMM_ERR_INVALID_ARG;
     }
 }

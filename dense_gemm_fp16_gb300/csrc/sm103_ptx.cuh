@@ -338,6 +338,38 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 }
 
 // ---------------------------------------------------------------------------
+// Global flags between CTAs of one grid (all co-resident)
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(uint32_t *p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Bounded wait until *flag == value; false when `budget_ns` passed or *abort was set.
+__device__ __forceinline__ bool wait_flag_equal(const uint32_t *flag, uint32_t value,
+                                                uint64_t budget_ns, const volatile int *abort) {
+    if (ld_acquire_gpu(flag) == value) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        __nanosleep(64);
+        if (ld_acquire_gpu(flag) == value) return true;
+        if (*abort) return false;
+        if (global_timer_ns() - t0 > budget_ns) return false;
+    }
+}
+
+// Named barrier over `count` threads (a multiple of 32) with id `id` (1..15).
+__device__ __forceinline__ void named_barrier_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// ---------------------------------------------------------------------------
 // Descriptors
 // ---------------------------------------------------------------------------
 

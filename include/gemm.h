@@ -110,7 +110,21 @@ int gemm_check_device_status(gemm_stream_t stream);
 typedef struct {
     int variant;
     int grid;
+    int flags;      /* GEMM_F16_FLAG_* below, 0 for none */
 } gemm_f16_config;
+
+/*
+ * Stream-K (pair variant only): when the last round of 256 x 256 tiles would
+ * leave many CTA pairs idle, split those tiles' k-blocks evenly over all
+ * pairs; a pair that takes over part of a tile's k-range writes its fp32
+ * partial to a workspace that the tile's first pair adds in before rounding.
+ * The workspace (per device and stream, about 256 KB per CTA pair) is
+ * allocated by the library on the first such call on a stream and kept; the
+ * split is skipped while the stream is being captured into a graph.  Off by
+ * default: on GB300 at the benchmark shapes the partial hand-off costs more
+ * than the balanced last round gains.
+ */
+#define GEMM_F16_FLAG_STREAM_K 1
 
 enum {
     GEMM_F16_AUTO = 0,          /* let gemm_f16_select decide                     */
@@ -129,8 +143,9 @@ enum {
 int gemm_f16_select(int M, int N, int K, int sm_count, gemm_f16_config *cfg);
 
 /* gemm_f16_nt with an explicit configuration (cfg == NULL or variant AUTO
- * means the selector's choice).  Same argument rules and errors as
- * gemm_f16_nt, plus GEMM_ERR_INVALID_ARG for an unknown variant. */
+ * means the selector's choice; grid 0 means the default grid; flags as
+ * above).  Same argument rules and errors as gemm_f16_nt, plus
+ * GEMM_ERR_INVALID_ARG for an unknown variant or flag. */
 int gemm_f16_nt_ex(int M, int N, int K, const void *A, const void *B, void *C,
                    gemm_stream_t stream, const gemm_f16_config *cfg);
 

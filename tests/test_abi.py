@@ -83,6 +83,9 @@ def test_bad_config_is_rejected(lib):
         g.gemm_f16_nt_ex(16, 16, 16, 0x1000, 0x1000, 0x1000, variant=99)
     assert e.value.status == g.GEMM_ERR_INVALID_ARG
     with pytest.raises(g.GemmError) as e:
+        g.gemm_f16_nt_ex(16, 16, 16, 0x1000, 0x1000, 0x1000, flags=4)
+    assert e.value.status == g.GEMM_ERR_INVALID_ARG
+    with pytest.raises(g.GemmError) as e:
         g.sgemm_ex(16, 16, 16, 1.0, 0x1000, 0x1000, 0.0, 0x1000, variant=7)
     assert e.value.status == g.GEMM_ERR_INVALID_ARG
 

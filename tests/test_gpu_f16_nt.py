@@ -29,7 +29,7 @@ def _lib():
     torch.cuda.init()
 
 
-def _run(A, B, variant=g.GEMM_F16_AUTO, grid=0, pad=64):
+def _run(A, B, variant=g.GEMM_F16_AUTO, grid=0, pad=64, flags=0):
     """Run on the GPU with a sentinel guard of `pad` halves around C."""
     M, K = A.shape
     N = B.shape[0]
@@ -39,7 +39,7 @@ def _run(A, B, variant=g.GEMM_F16_AUTO, grid=0, pad=64):
     buf = buf.view(torch.float16)
     C = buf[pad:pad + M * N].view(M, N)
     g.gemm_f16_nt_ex(M, N, K, dA.data_ptr(), dB.data_ptr(), C.data_ptr(),
-                     torch.cuda.current_stream().cuda_stream, variant, grid)
+                     torch.cuda.current_stream().cuda_stream, variant, grid, flags)
     g.gemm_check_device_status(torch.cuda.current_stream().cuda_stream)
     host = buf.cpu()
     guard = torch.cat([host[:pad], host[pad + M * N:]]).view(torch.int16).numpy().view(np.uint16)
@@ -164,6 +164,20 @@ def test_f16_nt_long_k_many_tiles(variant):
 
 
 @pytest.mark.parametrize("name", ["f16_nt_5376x5376x2048", "f16_nt_5000x5376x2040"])
+def test_f16_nt_full_size_stream_k_sampled(name):
+    # The same workloads with the last round of tiles split along K.
+    w = wl.WORKLOADS[name]
+    A, B, _ = wl.make_inputs(w)
+    dA, dB = A.cuda(), B.cuda()
+    C = g.f16_nt(dA, dB, variant=g.GEMM_F16_256x256_PAIR, flags=g.GEMM_F16_FLAG_STREAM_K)
+    g.gemm_check_device_status(0)
+    Ch = C.cpu().numpy()
+    rows, cols = wl.sample_positions(w.M, w.N, 65536, seed=2025)
+    Cref, S = oracle.gemm_f16_nt_sampled(A, B, rows, cols)
+    check_f16(Ch[rows, cols], Cref, S, what=name + " stream-K")
+
+
+@pytest.mark.parametrize("name", ["f16_nt_5376x5376x2048", "f16_nt_5000x5376x2040"])
 def test_f16_nt_full_size_sampled(name):
     # The launch configuration the benchmark times (selector default).
     w = wl.WORKLOADS[name]
@@ -179,3 +193,42 @@ def test_f16_nt_full_size_sampled(name):
     rows, cols = wl.sample_positions(w.M, w.N, 65536, seed=2024, tail_rows=tail)
     Cref, S = oracle.gemm_f16_nt_sampled(A, B, rows, cols)
     check_f16(Ch[rows, cols], Cref, S, what=name)
+
+
+@pytest.mark.parametrize("M,N,K,grid", [
+    (1024, 1024, 512, 6),     # 16 pair tiles on 3 pairs: the 16th tile split over all three
+    (1024, 1024, 512, 10),    # 5 pairs, one leftover tile
+    (1024, 1024, 512, 14),    # 7 pairs, two leftover tiles: each split over ~4 pairs
+    (1000, 1100, 1000, 10),   # ragged M, N, K with split tiles
+    (2304, 2304, 256, 152),   # 81 tiles on 76 pairs: the selector's grid
+])
+def test_f16_nt_pair_stream_k(M, N, K, grid):
+    # The leftover round of pair tiles is split along K across the pairs;
+    # owners add the fp32 partials of the following shares before rounding.
+    A = wl.draw_f16((M, K), seed=61, dist="normal")
+    B = wl.draw_f16((N, K), seed=62, dist="normal")
+    Cref, S = oracle.gemm_f16_nt(A, B)
+    for rep in range(3):   # sequence numbers advance between calls on one stream
+        C = _run(A, B, g.GEMM_F16_256x256_PAIR, grid, flags=g.GEMM_F16_FLAG_STREAM_K)
+        check_f16(C, Cref, S, what=f"stream-K {M}x{N}x{K} grid {grid} rep {rep}")
+
+
+def test_f16_nt_pair_stream_k_two_streams():
+    M, N, K = 1024, 1024, 512
+    A = wl.draw_f16((M, K), seed=71)
+    B = wl.draw_f16((N, K), seed=72)
+    Cref, S = oracle.gemm_f16_nt(A, B)
+    dA, dB = A.cuda(), B.cuda()
+    outs = []
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for s in streams:
+        with torch.cuda.stream(s):
+            C = torch.empty((M, N), dtype=torch.float16, device="cuda")
+            g.gemm_f16_nt_ex(M, N, K, dA.data_ptr(), dB.data_ptr(), C.data_ptr(), s.cuda_stream,
+                             g.GEMM_F16_256x256_PAIR, 10, g.GEMM_F16_FLAG_STREAM_K)
+            outs.append(C)
+    for s in streams:
+        s.synchronize()
+    g.gemm_check_device_status(0)
+    for C in outs:
+        check_f16(C.cpu().numpy(), Cref, S, what="two streams")
