@@ -34,6 +34,7 @@ from ._binding import (  # noqa: F401
     gemm_debug_f16_nt_skip_load,
     gemm_f16_nt,
     gemm_f16_nt_ex,
+    gemm_f16_nt_stream_k_noalloc,
     gemm_f16_select,
     gemm_last_error,
     gemm_sgemm_select,

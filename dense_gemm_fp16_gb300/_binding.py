@@ -79,6 +79,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gemm_f16_select.restype = i
         lib.gemm_sgemm_select.argtypes = [i, i, i, i, ctypes.POINTER(_SgemmConfig)]
         lib.gemm_sgemm_select.restype = i
+        lib.gemm_f16_nt_stream_k_noalloc.argtypes = [i, i, i, vp, vp, vp, vp]
+        lib.gemm_f16_nt_stream_k_noalloc.restype = i
         lib.gemm_debug_f16_nt_skip_load.argtypes = [i, i, i, vp, vp, vp, vp, i, ctypes.c_ulonglong]
         lib.gemm_debug_f16_nt_skip_load.restype = i
         _lib = lib
@@ -106,6 +108,15 @@ def gemm_f16_nt(M: int, N: int, K: int, A: int, B: int, C: int, stream: int | No
 def gemm_f16_nt_ex(M, N, K, A, B, C, stream=0, variant=GEMM_F16_AUTO, grid=0, flags=0) -> int:
     cfg = _F16Config(variant, grid, flags)
     return _check(load_library().gemm_f16_nt_ex(M, N, K, A, B, C, stream or None, ctypes.byref(cfg)))
+
+
+def gemm_f16_nt_stream_k_noalloc(M: int, N: int, K: int, A: int, B: int, C: int,
+                                 stream: int | None = 0) -> int:
+    """gemm_f16_nt without any allocation by the library: for callers that must
+    not let it cudaMalloc (a pre-reserved memory pool, a latency-critical path,
+    an allocator that owns every byte).  Uses a static 19.0 MiB array; calls
+    that overlap on the GPU race on it."""
+    return _check(load_library().gemm_f16_nt_stream_k_noalloc(M, N, K, A, B, C, stream or None))
 
 
 def sgemm(M: int, N: int, K: int, alpha: float, A: int, B: int, beta: float, C: int,

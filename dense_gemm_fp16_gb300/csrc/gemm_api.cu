@@ -127,7 +127,7 @@ int gemm_sgemm_select(int M, int N, int K, int sm_count, gemm_sgemm_config *cfg)
 
 static int f16_nt_impl(int M, int N, int K, const void *A, const void *B, void *C,
                        gemm_stream_t stream, const gemm_f16_config *cfg, uint64_t timeout_ns,
-                       int debug_skip_kblock) {
+                       int debug_skip_kblock, bool static_scratch = false) {
     if (M < 0 || N < 0 || K < 0)
         return fail(GEMM_ERR_INVALID_ARG, "gemm_f16_nt: negative size M=%d N=%d K=%d", M, N, K);
     if (M == 0 || N == 0) return GEMM_OK;
@@ -167,6 +167,7 @@ static int f16_nt_impl(int M, int N, int K, const void *A, const void *B, void *
     L.timeout_ns = timeout_ns;
     L.debug_skip_kblock = debug_skip_kblock;
     L.allow_stream_k = cfg && (cfg->flags & GEMM_F16_FLAG_STREAM_K);
+    L.static_scratch = static_scratch;
     std::string err;
     st = gb300::f16_launch(L, err);
     if (st != GEMM_OK) return fail_str(st, err);
@@ -180,6 +181,14 @@ int gemm_f16_nt(int M, int N, int K, const void *A, const void *B, void *C, gemm
 int gemm_f16_nt_ex(int M, int N, int K, const void *A, const void *B, void *C,
                    gemm_stream_t stream, const gemm_f16_config *cfg) {
     return f16_nt_impl(M, N, K, A, B, C, stream, cfg, kDefaultTimeoutNs, -1);
+}
+
+// The allocation-free variant declared in gemm.h: the CTA-pair kernel with
+// stream-K, its partials in the library's static scratch array.
+int gemm_f16_nt_stream_k_noalloc(int M, int N, int K, const void *A, const void *B, void *C,
+                                 gemm_stream_t stream) {
+    const gemm_f16_config cfg = {GEMM_F16_256x256_PAIR, 0, GEMM_F16_FLAG_STREAM_K};
+    return f16_nt_impl(M, N, K, A, B, C, stream, &cfg, kDefaultTimeoutNs, -1, true);
 }
 
 // Test hook declared in gemm_testing.h: one TMA load left out so that the

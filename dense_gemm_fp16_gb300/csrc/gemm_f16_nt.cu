@@ -956,6 +956,60 @@ int sk_workspace(cudaStream_t stream, int pairs, SkWorkspace **out, std::string 
     return GEMM_OK;
 }
 
+// Scratch of gemm_f16_nt_stream_k_noalloc: the same partial slots and flags as
+// a stream-K workspace, in module memory instead of a cudaMalloc'd buffer, for
+// up to kNoAllocMaxPairs CTA pairs (76 pairs = one GB300's 152 SMs).  Every
+// GPU that loads the library holds it until the process exits.  It starts out
+// zero (module memory is zero-initialised); each call tags its flags with a
+// fresh per-device sequence number, so stale slots and flags from earlier
+// calls are never mistaken for this call's, and only a wrap of that counter
+// needs the flags cleared.  All calls on a device share it: calls whose
+// kernels overlap on the GPU (on different streams) race on it.
+constexpr int kNoAllocMaxPairs = 76;
+constexpr size_t kNoAllocSlotBytes =
+    static_cast<size_t>(kNoAllocMaxPairs) * 2 * kSkSlotFloats * sizeof(float);
+constexpr size_t kNoAllocFlagBytes = static_cast<size_t>(kNoAllocMaxPairs) * 2 * 8 * sizeof(uint32_t);
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocSlotBytes + kNoAllocFlagBytes];
+
+// Device address of the scratch array for the current device, looked up once
+// per device with that device current (in host code the symbol itself is only
+// a host-side stand-in).  Also advances and returns that device's sequence number.
+int noalloc_scratch(cudaStream_t stream, float **ws, uint32_t **flags, uint32_t *seq,
+                    std::string &err) {
+    static std::mutex mu;
+    static void *addr[64] = {nullptr};
+    static uint32_t counter[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 64) {
+        err = std::string("cudaGetDevice: ") + cudaGetErrorString(e);
+        return GEMM_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || !p) {
+            err = std::string("cudaGetSymbolAddress(stream-K scratch): ") + cudaGetErrorString(e);
+            return GEMM_ERR_CUDA;
+        }
+        addr[dev] = p;
+    }
+    uint32_t *f = reinterpret_cast<uint32_t *>(static_cast<unsigned char *>(addr[dev]) + kNoAllocSlotBytes);
+    if (++counter[dev] == 0) {
+        e = cudaMemsetAsync(f, 0, kNoAllocFlagBytes, stream);  // the counter wrapped
+        if (e != cudaSuccess) {
+            err = std::string("stream-K scratch flag reset: ") + cudaGetErrorString(e);
+            return GEMM_ERR_CUDA;
+        }
+        counter[dev] = 1;
+    }
+    *ws = static_cast<float *>(addr[dev]);
+    *flags = f;
+    *seq = counter[dev];
+    return GEMM_OK;
+}
+
 template <int STAGES, int EPI>
 int launch_pair(const F16Launch &L, std::string &err) {
     using T = PairCfg<STAGES>;
@@ -1043,7 +1097,7 @@ int launch_pair(const F16Launch &L, std::string &err) {
             err = std::string("cudaStreamIsCapturing: ") + cudaGetErrorString(e);
             return GEMM_ERR_CUDA;
         }
-        if (cap == cudaStreamCaptureStatusNone) {
+        if (cap == cudaStreamCaptureStatusNone && !L.static_scratch) {
             SkWorkspace *w = nullptr;
             const int st = sk_workspace(L.stream, pairs, &w, err);
             if (st != GEMM_OK) return st;
@@ -1052,6 +1106,27 @@ int launch_pair(const F16Launch &L, std::string &err) {
             args.sk_ws = w->ws;
             args.sk_flags = w->flags;
             args.seq = w->seq;
+        } else if (cap == cudaStreamCaptureStatusNone) {
+            if (pairs > kNoAllocMaxPairs) {
+                char buf[200];
+                std::snprintf(buf, sizeof buf,
+                              "gemm_f16_nt_stream_k_noalloc: %d CTA pairs need %zu bytes of stream-K "
+                              "scratch; the static array holds %zu (%d pairs)",
+                              pairs, static_cast<size_t>(pairs) * 2 * kSkSlotFloats * sizeof(float),
+                              kNoAllocSlotBytes, kNoAllocMaxPairs);
+                err = buf;
+                return GEMM_ERR_UNSUPPORTED;
+            }
+            float *ws = nullptr;
+            uint32_t *flags = nullptr;
+            uint32_t seq = 0;
+            const int st = noalloc_scratch(L.stream, &ws, &flags, &seq, err);
+            if (st != GEMM_OK) return st;
+            args.dp_tiles = tiles - rem;
+            args.sk_units = rem * args.num_kb;
+            args.sk_ws = ws;
+            args.sk_flags = flags;
+            args.seq = seq;
         }
     }
     cfg.gridDim = dim3(2 * pairs);

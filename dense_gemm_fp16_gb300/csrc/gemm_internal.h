@@ -21,6 +21,7 @@ struct F16Launch {
     uint64_t timeout_ns;    // budget of every bounded wait in the kernel
     int debug_skip_kblock;  // test hook: producer skips this k-block of its first tile (-1: none)
     bool allow_stream_k;    // pair kernel: split the last partial round of tiles along K
+    bool static_scratch;    // stream-K partials in the library's static array, no allocation
 };
 
 int f16_launch(const F16Launch &L, std::string &err);

@@ -149,6 +149,40 @@ int gemm_f16_select(int M, int N, int K, int sm_count, gemm_f16_config *cfg);
 int gemm_f16_nt_ex(int M, int N, int K, const void *A, const void *B, void *C,
                    gemm_stream_t stream, const gemm_f16_config *cfg);
 
+/*
+ * gemm_f16_nt computed without any device-memory allocation by the library.
+ * The pages have no counterpart: this entry point exists for callers that
+ * cannot let a library call cudaMalloc -- servers that reserve their whole
+ * device-memory budget in their own pool up front (a later cudaMalloc may
+ * fail or break the budget), latency-critical paths (cudaMalloc and cudaFree
+ * can synchronise the device and stall other streams), and frameworks whose
+ * allocator must account for every byte.
+ *
+ * It runs the CTA-pair kernel (GEMM_F16_256x256_PAIR) with the stream-K split
+ * of GEMM_F16_FLAG_STREAM_K, but keeps the partial tiles and flags in a static
+ * array inside the library (19.0 MiB of device memory, enough for 76 CTA
+ * pairs; every GPU that loads the library holds it until the process exits)
+ * instead of a workspace it allocates.  The caller passes A, B and C exactly as
+ * for gemm_f16_nt, with the same argument rules, and gets the same result up to
+ * the order of the fp32 additions.
+ *
+ * Set-up: the first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.
+ *
+ * Sharing: every call on a device uses the same array and leaves its contents
+ * behind; each call tags its flags with a fresh sequence number, so nothing
+ * has to be cleared between calls.  Calls whose kernels overlap on the GPU
+ * (for example on two streams at once) race on the array and must not be
+ * made; calls on one stream never overlap.
+ *
+ * Errors: as gemm_f16_nt, plus GEMM_ERR_UNSUPPORTED when the launch would use
+ * more CTA pairs than the array holds slots for (a device with more than 152
+ * SMs), with the sizes in the message.
+ */
+int gemm_f16_nt_stream_k_noalloc(int M, int N, int K, const void *A, const void *B, void *C,
+                                 gemm_stream_t stream);
+
 /* One kernel configuration of the SGEMM path. */
 typedef struct {
     int variant;
