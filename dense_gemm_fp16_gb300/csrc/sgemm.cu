@@ -6,19 +6,21 @@
 // section "cp.async 与多级流水 sm_80+"; beta == 0 follows the BLAS convention
 // (C is not read).  fp32 semantics exclude TF32, so the work is plain FFMA.
 //
-// Design: each CTA of 256 threads owns a BM x BN tile of C; every thread owns
-// a TM x TN register micro-tile made of 4 x 4 blocks spread BM/RM rows and
-// BN/RN columns apart ("第 6 章 · Shared Memory & Tile", section "6.3.1 寄存器
-// tile").  K is walked in BK-deep slices through a STAGES-deep ring of shared
-// memory filled by cp.async, STAGES-1 slices ahead of the multiply, one
-// barrier per slice (the multi-stage scheme of the same source section
-// "cp.async 与多级流水 sm_80+", here with zero-filled tails).  Warps are 4 x 8
-// thread blocks of the 16 x 16 thread grid.  On sm_103a the FP32 pipe retires
-// 128 FMA per clock per SM, twice the rate the pages' Ampere kernels were
-// tuned for, so issue slots and shared-memory wavefronts are the limits:
-// the outer product uses the packed two-wide fp32 FMA (fma.rn.f32x2, each
-// lane's two FMAs rounded exactly like fmaf), and the 8 x 8 micro-tile keeps
-// one 128-byte shared-memory wavefront per four FMAs per lane.
+// Design: each CTA owns a BM x BN tile of C; every thread owns a TM x TN
+// register micro-tile made of 4 x 4 blocks spread BM/RM rows and BN/RN columns
+// apart ("第 6 章 · Shared Memory & Tile", section "6.3.1 寄存器 tile"), and a
+// warp is 4 x 8 such threads.  K is walked in BK-deep slices through a
+// STAGES-deep ring of shared memory filled by cp.async, STAGES-1 slices ahead
+// of the multiply, one barrier per slice (the multi-stage scheme of
+// "异步拷贝与 Hopper/Blackwell 新特性", section "cp.async 与多级流水 sm_80+",
+// here with zero-filled tails).  On sm_103a the FP32 pipe retires 128 FMA per
+// clock per SM, twice the rate the pages' Ampere kernels were tuned for, so
+// issue slots and shared-memory wavefronts are the limits: the outer product
+// uses the packed two-wide fp32 FMA (fma.rn.f32x2, each lane's two FMAs
+// rounded exactly like fmaf), and the main tile's 8 x 16 micro-tile (128
+// threads per 128 x 128 tile) does 5.3 FMAs per lane per 128-byte shared
+// wavefront, where an 8 x 8 micro-tile's 4 would tie shared memory to the
+// FMA pipe at peak.
 // Out-of-range rows, columns and k are loaded as zeros and never stored, which
 // makes any M, N, K exact.
 #include <cuda_runtime.h>
@@ -28,8 +30,6 @@
 
 namespace gb300 {
 namespace {
-
-constexpr int kSgemmThreads = 256;
 
 // ---------------------------------------------------------------------------
 // A and B slices go straight from global to shared memory
@@ -61,13 +61,18 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-template <int BM, int BN, int BK, int TM, int TN, int STAGES, bool VEC>
-__global__ void __launch_bounds__(kSgemmThreads, (TM * TN <= 64) ? 2 : 1)
+template <int BM, int BN, int TM, int TN>
+constexpr int sgemm_threads() { return (BM / TM) * (BN / TN); }
+
+template <int BM, int BN, int BK, int TM, int TN, int STAGES, int MINB, bool VEC>
+__global__ void __launch_bounds__(sgemm_threads<BM, BN, TM, TN>(), MINB)
     sgemm_pipe_kernel(int M, int N, int K, float alpha, const float *__restrict__ A,
                       const float *__restrict__ B, float beta, float *__restrict__ C) {
     constexpr int RM = TM / 4, RN = TN / 4;
+    constexpr int kThreads = sgemm_threads<BM, BN, TM, TN>();
+    constexpr int kWarpsN = (BN / TN) / 8;  // a warp is 4 thread rows x 8 thread columns
     constexpr int A_CHUNKS = BM * BK / 4, B_CHUNKS = BK * BN / 4;
-    static_assert((BM / TM) * (BN / TN) == kSgemmThreads && BM / TM == 16, "16 x 16 threads");
+    static_assert((BM / TM) % 4 == 0 && (BN / TN) % 8 == 0, "whole 4 x 8 warps");
     static_assert(BK % 4 == 0, "A is read as float4 along k");
 
     __shared__ __align__(16) float As[STAGES][BM][BK];
@@ -75,14 +80,14 @@ __global__ void __launch_bounds__(kSgemmThreads, (TM * TN <= 64) ? 2 : 1)
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int ty = (warp >> 1) * 4 + (lane >> 3);
-    const int tx = (warp & 1) * 8 + (lane & 7);
+    const int ty = (warp / kWarpsN) * 4 + (lane >> 3);
+    const int tx = (warp % kWarpsN) * 8 + (lane & 7);
     const int m0 = blockIdx.y * BM;
     const int n0 = blockIdx.x * BN;
 
     auto load_slice = [&](int buf, int k0) {
 #pragma unroll
-        for (int c = tid; c < A_CHUNKS; c += kSgemmThreads) {
+        for (int c = tid; c < A_CHUNKS; c += kThreads) {
             const int row = c / (BK / 4), kq = c % (BK / 4);
             const int m = m0 + row, k = k0 + kq * 4;
             const float *src = A + static_cast<size_t>(m < M ? m : 0) * K;
@@ -96,7 +101,7 @@ __global__ void __launch_bounds__(kSgemmThreads, (TM * TN <= 64) ? 2 : 1)
             }
         }
 #pragma unroll
-        for (int c = tid; c < B_CHUNKS; c += kSgemmThreads) {
+        for (int c = tid; c < B_CHUNKS; c += kThreads) {
             const int kr = c / (BN / 4), nq = c % (BN / 4);
             const int k = k0 + kr, n = n0 + nq * 4;
             const float *src = B + static_cast<size_t>(k < K ? k : 0) * N;
@@ -210,17 +215,18 @@ __global__ void scale_kernel(float *C, size_t count, float beta) {
         C[i] = (beta == 0.f) ? 0.f : beta * C[i];
 }
 
-template <int BM, int BN, int BK, int TM, int TN, int STAGES>
+template <int BM, int BN, int BK, int TM, int TN, int STAGES, int MINB = 2>
 int launch_pipe(const SgemmLaunch &L, std::string &err) {
     const dim3 grid((L.N + BN - 1) / BN, (L.M + BM - 1) / BM);
     const bool vec = (L.K % 4 == 0) && (L.N % 4 == 0) &&
                      ((reinterpret_cast<uintptr_t>(L.A) | reinterpret_cast<uintptr_t>(L.B) |
                        reinterpret_cast<uintptr_t>(L.C)) & 15u) == 0;
+    constexpr int threads = sgemm_threads<BM, BN, TM, TN>();
     if (vec)
-        sgemm_pipe_kernel<BM, BN, BK, TM, TN, STAGES, true><<<grid, kSgemmThreads, 0, L.stream>>>(
+        sgemm_pipe_kernel<BM, BN, BK, TM, TN, STAGES, MINB, true><<<grid, threads, 0, L.stream>>>(
             L.M, L.N, L.K, L.alpha, L.A, L.B, L.beta, L.C);
     else
-        sgemm_pipe_kernel<BM, BN, BK, TM, TN, STAGES, false><<<grid, kSgemmThreads, 0, L.stream>>>(
+        sgemm_pipe_kernel<BM, BN, BK, TM, TN, STAGES, MINB, false><<<grid, threads, 0, L.stream>>>(
             L.M, L.N, L.K, L.alpha, L.A, L.B, L.beta, L.C);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
@@ -245,7 +251,7 @@ int sgemm_launch(const SgemmLaunch &L, std::string &err) {
         return GEMM_OK;
     }
     switch (L.variant) {
-        case GEMM_SGEMM_128x128: return launch_pipe<128, 128, 16, 8, 8, 3>(L, err);
+        case GEMM_SGEMM_128x128: return launch_pipe<128, 128, 16, 8, 16, 3>(L, err);
         case GEMM_SGEMM_64x64: return launch_pipe<64, 64, 16, 4, 4, 3>(L, err);
         default: err = "unknown sgemm variant"; return GEMM_ERR_INVALID_ARG;
     }

@@ -190,7 +190,7 @@ typedef struct {
 
 enum {
     GEMM_SGEMM_AUTO = 0,
-    GEMM_SGEMM_128x128 = 1,     /* 128 x 128 CTA tile, 8 x 8 per thread, BK 16, 3 stages */
+    GEMM_SGEMM_128x128 = 1,     /* 128 x 128 CTA tile, 8 x 16 per thread, BK 16, 3 stages */
     GEMM_SGEMM_64x64 = 2,       /* 64 x 64 CTA tile, 4 x 4 per thread, BK 16, 3 stages   */
     GEMM_SGEMM_NUM_VARIANTS = 3
 };
