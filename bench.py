@@ -447,6 +447,31 @@ def run_ours(args):
                                       "peak_source": f"{sm_count} SMs x 128 FFMA/clk x 2 FLOP x "
                                                      f"{peaks.get('sm_max_mhz', 2070.0)} MHz"}}
 
+    # ---- fp16 matrix-vector (M = 1) against the HBM copy bandwidth
+    if not args.skip_sgemm:
+        gw = wl.WORKLOADS["f16_gemv_1x16384x8192"]
+        gA, gB, _ = wl.make_inputs(gw)
+        with torch.cuda.stream(stream):
+            dga, dgb = gA.cuda(), gB.cuda()
+            dgc = torch.empty((gw.M, gw.N), dtype=torch.float16, device="cuda")
+        stream.synchronize()
+
+        def gv(_):
+            g.gemm_f16_nt(gw.M, gw.N, gw.K, dga.data_ptr(), dgb.data_ptr(), dgc.data_ptr(), sh)
+        region_time(gv, stream, 5)
+        n_gv = 50
+        t_gv = region_time(gv, stream, n_gv) / n_gv
+        gbytes = 2 * (gw.N * gw.K + gw.M * gw.K + gw.M * gw.N)
+        hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+        achieved_gbs = gbytes / (t_gv * 1e-3) / 1e9
+        line["gemv"] = {"workload": gw.name, "value": gw.flop / (t_gv * 1e-3) / 1e12,
+                        "unit": "TFLOP/s", "us_per_call": 1e3 * t_gv,
+                        "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm,
+                                     "unit": "GB/s", "frac": achieved_gbs / hbm,
+                                     "bytes_per_call": gbytes,
+                                     "peak_source": f"{peak_kind} HBM copy bandwidth"}}
+        g.gemm_check_device_status(sh)
+
     if rank == 0 and not args.skip_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, A, B, budget_s=args.cpu_budget)
     if rank == 0:

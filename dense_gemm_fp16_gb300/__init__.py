@@ -23,6 +23,7 @@ from ._binding import (  # noqa: F401
     GEMM_F16_256x256_PAIR,
     GEMM_F16_AUTO,
     GEMM_F16_FLAG_STREAM_K,
+    GEMM_F16_GEMV,
     GEMM_OK,
     GEMM_SGEMM_64x64,
     GEMM_SGEMM_128x128,

@@ -19,7 +19,7 @@ GEMM_ERR_UNSUPPORTED = -3
 GEMM_ERR_CUDA = -4
 GEMM_ERR_DEVICE_TIMEOUT = -5
 
-GEMM_F16_AUTO, GEMM_F16_128x256, GEMM_F16_128x128, GEMM_F16_256x256_PAIR = 0, 1, 2, 3
+GEMM_F16_AUTO, GEMM_F16_128x256, GEMM_F16_128x128, GEMM_F16_256x256_PAIR, GEMM_F16_GEMV = 0, 1, 2, 3, 4
 GEMM_SGEMM_AUTO, GEMM_SGEMM_128x128, GEMM_SGEMM_64x64 = 0, 1, 2
 GEMM_F16_FLAG_STREAM_K = 1
 

@@ -33,6 +33,9 @@ int fail_str(int status, const std::string &msg) {
     return status;
 }
 
+// Largest shared-memory staging of A the GEMV path accepts (8 rows x 10 240 halves).
+constexpr size_t kGemvMaxSmem = 160 * 1024;
+
 // Bounded-wait budget inside the fp16 kernel: long enough for any legitimate
 // stall (preemption by another context included), short enough that a broken
 // handshake ends the kernel instead of holding the GPU.
@@ -66,6 +69,7 @@ inline long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 // to one per SM.
 int f16_default_grid(int variant, int M, int N, int sm_count) {
     long long tiles;
+    if (variant == GEMM_F16_GEMV) return sm_count;  // planned per SM by the GEMV launcher
     switch (variant) {
         case GEMM_F16_128x256: tiles = ceil_div(M, 128) * ceil_div(N, 256); break;
         case GEMM_F16_256x256_PAIR: tiles = 2 * ceil_div(M, 256) * ceil_div(N, 256); break;
@@ -99,9 +103,13 @@ int gemm_f16_select(int M, int N, int K, int sm_count, gemm_f16_config *cfg) {
     // over the SMs.  (The 1-CTA 128 x 256 tile has no shape range of its own
     // between the two: it fills the SMs exactly when the pair tile fills the
     // pairs; it stays available through gemm_f16_nt_ex.)
+    // With at most 8 rows of A every element of B is used at most 8 times:
+    // reading B from HBM bounds the product, and the matrix-vector kernel
+    // streams B once (when those rows of A fit in its shared memory).
     const long long pair_tiles = ceil_div(M, 256) * ceil_div(N, 256);
-    const int variant = (pair_tiles >= sm_count / 2 && N > 128) ? GEMM_F16_256x256_PAIR
-                                                                : GEMM_F16_128x128;
+    int variant = (pair_tiles >= sm_count / 2 && N > 128) ? GEMM_F16_256x256_PAIR
+                                                          : GEMM_F16_128x128;
+    if (M <= 8 && gb300::gemv_smem_bytes(M, K) <= kGemvMaxSmem) variant = GEMM_F16_GEMV;
     cfg->variant = variant;
     cfg->grid = f16_default_grid(variant, M, N, sm_count);
     cfg->flags = 0;
@@ -151,6 +159,11 @@ static int f16_nt_impl(int M, int N, int K, const void *A, const void *B, void *
     if (cfg && cfg->variant != GEMM_F16_AUTO) {
         sel.variant = cfg->variant;
         sel.grid = f16_default_grid(sel.variant, M, N, sms);
+        if (sel.variant == GEMM_F16_GEMV &&
+            (M > 8 || (K > 0 && gb300::gemv_smem_bytes(M, K) > kGemvMaxSmem)))
+            return fail(GEMM_ERR_UNSUPPORTED,
+                        "gemm_f16_nt_ex: the GEMV variant takes M <= 8 and 8*K*2 <= %zu bytes "
+                        "(M=%d K=%d)", kGemvMaxSmem, M, K);
     }
     if (cfg && cfg->grid > 0) sel.grid = cfg->grid;
 
@@ -168,6 +181,7 @@ static int f16_nt_impl(int M, int N, int K, const void *A, const void *B, void *
     L.debug_skip_kblock = debug_skip_kblock;
     L.allow_stream_k = cfg && (cfg->flags & GEMM_F16_FLAG_STREAM_K);
     L.static_scratch = static_scratch;
+    L.sm_count = sms;
     std::string err;
     st = gb300::f16_launch(L, err);
     if (st != GEMM_OK) return fail_str(st, err);

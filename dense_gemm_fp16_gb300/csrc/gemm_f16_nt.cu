@@ -1157,6 +1157,10 @@ int f16_launch(const F16Launch &L, std::string &err) {
         case GEMM_F16_128x256: return launch_variant<256, 4>(L, err);
         case GEMM_F16_128x128: return launch_variant<128, 6>(L, err);
         case GEMM_F16_256x256_PAIR: return launch_pair<6, 4>(L, err);
+        case GEMM_F16_GEMV: {
+            GemvLaunch G{L.M, L.N, L.K, L.A, L.B, L.C, L.stream, L.sm_count, 4};
+            return gemv_launch(G, err);
+        }
         default: err = "unknown fp16 variant"; return GEMM_ERR_INVALID_ARG;
     }
 }

@@ -22,12 +22,32 @@ struct F16Launch {
     int debug_skip_kblock;  // test hook: producer skips this k-block of its first tile (-1: none)
     bool allow_stream_k;    // pair kernel: split the last partial round of tiles along K
     bool static_scratch;    // stream-K partials in the library's static array, no allocation
+    int sm_count;           // SMs of the current device
 };
 
 int f16_launch(const F16Launch &L, std::string &err);
 
 // Read-and-clear the fp16 kernel's device status word (0 = no fault).
 int f16_status_read_clear(cudaStream_t stream, int *code, std::string &err);
+
+// One fp16 matrix-vector launch (M <= 8), after validation and selection.
+struct GemvLaunch {
+    int M, N, K;
+    const void *A;
+    const void *B;
+    void *C;
+    cudaStream_t stream;
+    int sm_count;      // CTAs are planned per SM
+    int ctas_per_sm;
+};
+
+int gemv_launch(const GemvLaunch &L, std::string &err);
+
+// Shared memory a GEMV launch needs for its rows of A (bytes).
+inline size_t gemv_smem_bytes(int M, int K) {
+    const int mt = M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8;
+    return static_cast<size_t>(mt) * static_cast<size_t>(K) * 2;
+}
 
 // One SGEMM launch, after validation and selection.
 struct SgemmLaunch {
