@@ -33,7 +33,7 @@ int fail_str(int status, const std::string &msg) {
     return status;
 }
 
-// Largest shared-memory staging of A the GEMV path accepts (8 rows x 10 240 halves).
+// Largest shared-memory staging of A the GEMV path accepts (2 rows x 40 960 halves).
 constexpr size_t kGemvMaxSmem = 160 * 1024;
 
 // Bounded-wait budget inside the fp16 kernel: long enough for any legitimate
@@ -103,13 +103,14 @@ int gemm_f16_select(int M, int N, int K, int sm_count, gemm_f16_config *cfg) {
     // over the SMs.  (The 1-CTA 128 x 256 tile has no shape range of its own
     // between the two: it fills the SMs exactly when the pair tile fills the
     // pairs; it stays available through gemm_f16_nt_ex.)
-    // With at most 8 rows of A every element of B is used at most 8 times:
+    // With one or two rows of A every element of B is used at most twice:
     // reading B from HBM bounds the product, and the matrix-vector kernel
-    // streams B once (when those rows of A fit in its shared memory).
+    // streams B once (when those rows of A fit in its shared memory).  From
+    // three rows on, its fp32 FMAs fall behind HBM and the tensor cores win.
     const long long pair_tiles = ceil_div(M, 256) * ceil_div(N, 256);
     int variant = (pair_tiles >= sm_count / 2 && N > 128) ? GEMM_F16_256x256_PAIR
                                                           : GEMM_F16_128x128;
-    if (M <= 8 && gb300::gemv_smem_bytes(M, K) <= kGemvMaxSmem) variant = GEMM_F16_GEMV;
+    if (M <= 2 && gb300::gemv_smem_bytes(M, K) <= kGemvMaxSmem) variant = GEMM_F16_GEMV;
     cfg->variant = variant;
     cfg->grid = f16_default_grid(variant, M, N, sm_count);
     cfg->flags = 0;
@@ -160,9 +161,9 @@ static int f16_nt_impl(int M, int N, int K, const void *A, const void *B, void *
         sel.variant = cfg->variant;
         sel.grid = f16_default_grid(sel.variant, M, N, sms);
         if (sel.variant == GEMM_F16_GEMV &&
-            (M > 8 || (K > 0 && gb300::gemv_smem_bytes(M, K) > kGemvMaxSmem)))
+            (M > 2 || (K > 0 && gb300::gemv_smem_bytes(M, K) > kGemvMaxSmem)))
             return fail(GEMM_ERR_UNSUPPORTED,
-                        "gemm_f16_nt_ex: the GEMV variant takes M <= 8 and 8*K*2 <= %zu bytes "
+                        "gemm_f16_nt_ex: the GEMV variant takes M <= 2 and M*K*2 <= %zu bytes "
                         "(M=%d K=%d)", kGemvMaxSmem, M, K);
     }
     if (cfg && cfg->grid > 0) sel.grid = cfg->grid;

@@ -30,7 +30,7 @@ int f16_launch(const F16Launch &L, std::string &err);
 // Read-and-clear the fp16 kernel's device status word (0 = no fault).
 int f16_status_read_clear(cudaStream_t stream, int *code, std::string &err);
 
-// One fp16 matrix-vector launch (M <= 8), after validation and selection.
+// One fp16 matrix-vector launch (M <= 2), after validation and selection.
 struct GemvLaunch {
     int M, N, K;
     const void *A;
@@ -45,7 +45,7 @@ int gemv_launch(const GemvLaunch &L, std::string &err);
 
 // Shared memory a GEMV launch needs for its rows of A (bytes).
 inline size_t gemv_smem_bytes(int M, int K) {
-    const int mt = M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8;
+    const int mt = M <= 1 ? 1 : 2;
     return static_cast<size_t>(mt) * static_cast<size_t>(K) * 2;
 }
 

@@ -1,20 +1,22 @@
-// gemv_f16_nt.cu -- C = A * B^T for very few rows of A (M <= 8): the
+// gemv_f16_nt.cu -- C = A * B^T for one or two rows of A (M <= 2): the
 // matrix-vector regime of an LLM decode step.
 //
 // Same operation and numerics as gemm_f16_nt (half inputs, fp32 accumulation,
 // one round-to-nearest-even per output), but with M this small every element
-// of B is used only M times, so the product is bound by reading B from HBM,
+// of B is used only M times, so the product is bound by reading B from HBM
+// (from M = 3 on, the fp32 FMAs on the CUDA cores no longer keep pace with
+// HBM and the tensor-core path is faster; measured at N = 16384, K = 8192),
 // not by the tensor cores ("第 6 章 · Shared Memory & Tile", section "6.5.5
 // GEMV (M=1)：LLM decode 完全不能用 tile": tiling has nothing to reuse; one
 // warp per output row, a shuffle reduction).
 //
-// Design for sm_103a's HBM: each warp owns one row of B at a time (a dot
-// product of K halves with each of the M rows of A) and streams it with
-// 16-byte loads that bypass L1 allocation, four in flight per lane; the M rows
-// of A (at most 8 x K halves) sit in shared memory, read as 16-byte vectors;
-// the grid is a whole number of CTAs per SM; partial sums meet through warp
-// shuffles.  Reading B once and A once per CTA, the algorithmic bytes are
-// N*K*2 + M*K*2 + M*N*2.
+// Design for sm_103a's HBM: B is streamed once with 16-byte loads that skip
+// L1 allocation; each CTA takes a balanced block of rows (the grid is a whole
+// number of CTAs per SM) and its warps split every row's K range, so no warp
+// waits on a longer share of rows than the others; the M rows of A (at most
+// 2 x K halves) sit in shared memory, read as 16-byte vectors; partial sums
+// meet through warp shuffles and a small shared array.  Reading B once and A
+// once per CTA, the algorithmic bytes are N*K*2 + M*K*2 + M*N*2.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -54,11 +56,19 @@ __device__ __forceinline__ void dot8(float (&acc)[MT], const uint4 &bv, const ui
 }
 
 // VEC: K % 8 == 0 and A, B 16-byte aligned (16-byte vectors); else halves one by one.
-template <int MT, bool VEC>
+//
+// Work split: CTA b owns rows [b*N/G, (b+1)*N/G) of B (balanced to one row),
+// and all its warps share every row: warp w reads the w-th eighth of the row's
+// K range.  Rows go kGemvRows at a time with kVec 16-byte vectors of each in
+// flight per lane; each warp's partial dot products meet in a double-buffered
+// shared array, so one barrier per group of rows suffices, and the first
+// kGemvRows * M threads finish the sums.
+template <int MT, int kGemvRows, int kVec, bool VEC>
 __global__ void __launch_bounds__(kGemvWarps * 32)
     gemv_f16_nt_kernel(int M, int N, int K, const __half *__restrict__ A,
                        const __half *__restrict__ B, __half *__restrict__ C) {
     extern __shared__ __align__(16) unsigned char gemv_smem[];
+    __shared__ float red[2][kGemvWarps][kGemvRows][MT];
     __half *As = reinterpret_cast<__half *>(gemv_smem);  // [MT][K]
     // Programmatic dependent launch: nothing global before the predecessor is done.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -71,65 +81,92 @@ __global__ void __launch_bounds__(kGemvWarps * 32)
     __syncthreads();
 
     const int lane = threadIdx.x & 31;
-    const int warp_global = blockIdx.x * kGemvWarps + (threadIdx.x >> 5);
-    const int warps_total = gridDim.x * kGemvWarps;
-    for (int n = warp_global; n < N; n += warps_total) {
-        const __half *brow = B + static_cast<size_t>(n) * K;
-        float acc[MT];
+    const int warp = threadIdx.x >> 5;
+    const int r0 = static_cast<int>(static_cast<long long>(blockIdx.x) * N / gridDim.x);
+    const int r1 = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * N / gridDim.x);
+    // this warp's slice of K: whole 16-byte vectors (VEC) or single halves
+    const int units = VEC ? K / 8 : K;
+    const int u0 = static_cast<int>(static_cast<long long>(warp) * units / kGemvWarps);
+    const int u1 = static_cast<int>(static_cast<long long>(warp + 1) * units / kGemvWarps);
+
+    int buf = 0;
+    for (int n0 = r0; n0 < r1; n0 += kGemvRows, buf ^= 1) {
+        float acc[kGemvRows][MT];
 #pragma unroll
-        for (int m = 0; m < MT; ++m) acc[m] = 0.f;
+        for (int r = 0; r < kGemvRows; ++r)
+#pragma unroll
+            for (int m = 0; m < MT; ++m) acc[r][m] = 0.f;
         if (VEC) {
-            const int kv = K / 8;  // 16-byte vectors per row
-            int v = lane;
-            // four vectors of B in flight per lane
-            for (; v + 96 < kv; v += 128) {
-                uint4 bv[4];
+            for (int u = u0 + lane; u < u1; u += 32 * kVec) {
+                // up to kVec vectors of each of the rows in flight per lane
+                uint4 bv[kGemvRows][kVec];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) bv[u] = ld_stream_v4(brow + (v + 32 * u) * 8);
+                for (int r = 0; r < kGemvRows; ++r) {
+                    const int n = n0 + r < r1 ? n0 + r : r1 - 1;
+                    const __half *brow = B + static_cast<size_t>(n) * K;
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
+                    for (int h = 0; h < kVec; ++h)
+                        if (u + 32 * h < u1) bv[r][h] = ld_stream_v4(brow + (u + 32 * h) * 8);
+                }
+#pragma unroll
+                for (int h = 0; h < kVec; ++h) {
+                    if (u + 32 * h >= u1) break;
                     uint4 av[MT];
 #pragma unroll
                     for (int m = 0; m < MT; ++m)
-                        av[m] = *reinterpret_cast<const uint4 *>(As + m * K + (v + 32 * u) * 8);
-                    dot8<MT>(acc, bv[u], av);
+                        av[m] = *reinterpret_cast<const uint4 *>(As + m * K + (u + 32 * h) * 8);
+#pragma unroll
+                    for (int r = 0; r < kGemvRows; ++r) dot8<MT>(acc[r], bv[r][h], av);
                 }
             }
-            for (; v < kv; v += 32) {
-                const uint4 bv = ld_stream_v4(brow + v * 8);
-                uint4 av[MT];
-#pragma unroll
-                for (int m = 0; m < MT; ++m) av[m] = *reinterpret_cast<const uint4 *>(As + m * K + v * 8);
-                dot8<MT>(acc, bv, av);
-            }
         } else {
-            for (int k = lane; k < K; k += 32) {
-                const float b = __half2float(brow[k]);
+            for (int k = u0 + lane; k < u1; k += 32) {
 #pragma unroll
-                for (int m = 0; m < MT; ++m) acc[m] = fmaf(__half2float(As[m * K + k]), b, acc[m]);
+                for (int r = 0; r < kGemvRows; ++r) {
+                    const int n = n0 + r < r1 ? n0 + r : r1 - 1;
+                    const float b = __half2float(B[static_cast<size_t>(n) * K + k]);
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) acc[r][m] = fmaf(__half2float(As[m * K + k]), b, acc[r][m]);
+                }
             }
         }
 #pragma unroll
-        for (int m = 0; m < MT; ++m) {
+        for (int r = 0; r < kGemvRows; ++r)
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) acc[m] += __shfl_xor_sync(0xffffffffu, acc[m], off);
+            for (int m = 0; m < MT; ++m) {
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1)
+                    acc[r][m] += __shfl_xor_sync(0xffffffffu, acc[r][m], off);
+            }
+        if (lane == 0) {
+#pragma unroll
+            for (int r = 0; r < kGemvRows; ++r)
+#pragma unroll
+                for (int m = 0; m < MT; ++m) red[buf][warp][r][m] = acc[r][m];
         }
-        if (lane < MT && lane < M) {
-            float out = acc[0];
+        __syncthreads();
+        // Thread t < rows*MT finishes output (row t / MT, column t % MT) of
+        // this pair; the next pair writes the other buffer, and the barrier
+        // after it orders this read before that buffer is written again.
+        if (threadIdx.x < kGemvRows * MT) {
+            const int r = threadIdx.x / MT, m = threadIdx.x % MT;
+            if (n0 + r < r1 && m < M) {
+                float sum = 0.f;
 #pragma unroll
-            for (int m = 1; m < MT; ++m)
-                if (lane == m) out = acc[m];
-            C[static_cast<size_t>(lane) * N + n] = __float2half_rn(out);
+                for (int w = 0; w < kGemvWarps; ++w) sum += red[buf][w][r][m];
+                C[static_cast<size_t>(m) * N + n0 + r] = __float2half_rn(sum);
+            }
         }
     }
 }
 
 template <int MT>
 int launch_mt(const GemvLaunch &L, std::string &err) {
+    constexpr int R = 2, V = 4;  // rows per step, vectors per row per lane in flight
     const bool vec = (L.K % 8 == 0) &&
                      ((reinterpret_cast<uintptr_t>(L.A) | reinterpret_cast<uintptr_t>(L.B)) & 15u) == 0;
     const size_t smem = static_cast<size_t>(MT) * L.K * sizeof(__half);
-    auto kernel = vec ? gemv_f16_nt_kernel<MT, true> : gemv_f16_nt_kernel<MT, false>;
+    auto kernel = vec ? gemv_f16_nt_kernel<MT, R, V, true> : gemv_f16_nt_kernel<MT, R, V, false>;
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
@@ -138,10 +175,9 @@ int launch_mt(const GemvLaunch &L, std::string &err) {
             return GEMM_ERR_CUDA;
         }
     }
-    // Whole CTAs per SM, about one warp per row of B at most.
-    const long long want = (static_cast<long long>(L.N) + kGemvWarps - 1) / kGemvWarps;
+    // Whole CTAs per SM, at most one CTA per row of B.
     const long long cap = static_cast<long long>(L.sm_count) * L.ctas_per_sm;
-    const int grid = static_cast<int>(want < cap ? (want > 0 ? want : 1) : cap);
+    const int grid = static_cast<int>(L.N < cap ? (L.N > 0 ? L.N : 1) : cap);
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -166,9 +202,7 @@ int launch_mt(const GemvLaunch &L, std::string &err) {
 int gemv_launch(const GemvLaunch &L, std::string &err) {
     if (L.M <= 1) return launch_mt<1>(L, err);
     if (L.M <= 2) return launch_mt<2>(L, err);
-    if (L.M <= 4) return launch_mt<4>(L, err);
-    if (L.M <= 8) return launch_mt<8>(L, err);
-    err = "gemv: M > 8";
+    err = "gemv: M > 2";
     return GEMM_ERR_INVALID_ARG;
 }
 

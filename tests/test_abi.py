@@ -98,12 +98,12 @@ def test_f16_selector(lib):
     assert g.gemm_f16_select(4096, 2048, 512, 148) == (g.GEMM_F16_256x256_PAIR, 148)
     # fewer pair tiles than SM pairs: narrow tiles
     assert g.gemm_f16_select(2048, 2048, 512, 152) == (g.GEMM_F16_128x128, 152)
-    # at most 8 rows of A: the HBM-bound matrix-vector kernel, planned per SM
+    # one or two rows of A: the HBM-bound matrix-vector kernel, planned per SM
     assert g.gemm_f16_select(1, 5376, 2048, 152) == (g.GEMM_F16_GEMV, 152)
-    assert g.gemm_f16_select(8, 16384, 8192, 152) == (g.GEMM_F16_GEMV, 152)
-    assert g.gemm_f16_select(9, 16384, 8192, 152)[0] == g.GEMM_F16_128x128
+    assert g.gemm_f16_select(2, 16384, 8192, 152) == (g.GEMM_F16_GEMV, 152)
+    assert g.gemm_f16_select(3, 16384, 8192, 152)[0] == g.GEMM_F16_128x128
     # its shared-memory staging of A would not fit: the tensor-core path
-    assert g.gemm_f16_select(8, 4096, 16384, 152)[0] != g.GEMM_F16_GEMV
+    assert g.gemm_f16_select(2, 4096, 65536, 152)[0] != g.GEMM_F16_GEMV
     assert g.gemm_f16_select(1, 4096, 65536, 152)[0] == g.GEMM_F16_GEMV
     # too few wide tiles to fill the SMs: narrow tiles, grid = tile count
     assert g.gemm_f16_select(1024, 1024, 1024, 152) == (g.GEMM_F16_128x128, 64)
