@@ -14,6 +14,9 @@ each function follows:
   "0. Naive Implementation" (C = A·Bᵀ, A [M,K], B [N,K] half).
 * ``sgemm``: "异步拷贝与 Hopper/Blackwell 新特性", section
   "cp.async 与多级流水 sm_80+" (C = alpha·A·B + beta·C, row-major fp32).
+* ``gemm_f16_nt_epilogue``: "第 6 章 · Shared Memory & Tile", section
+  "6.5.4 Epilogue 融合" (activation(GEMM + bias)), with alpha, beta and a
+  residual.
 
 Every function returns the unrounded float64 result C and the tolerance
 scale S = |alpha|·Σ_k |A·B| per element.
@@ -67,6 +70,11 @@ def _load():
             lib.oracle_gemm_f16_nt_sampled.argtypes = [i64, i64, i64, vp, vp, i64, vp, vp, vp, vp]
             lib.oracle_sgemm.restype = ctypes.c_int
             lib.oracle_sgemm.argtypes = [i64, i64, i64, dbl, vp, vp, dbl, vp, vp, vp]
+            lib.oracle_activation.restype = dbl
+            lib.oracle_activation.argtypes = [dbl, ctypes.c_int]
+            lib.oracle_gemm_f16_nt_epilogue.restype = ctypes.c_int
+            lib.oracle_gemm_f16_nt_epilogue.argtypes = [i64, i64, i64, vp, vp, dbl, vp, dbl, vp,
+                                                        ctypes.c_int, vp, vp]
             lib.oracle_sgemm_sampled.restype = ctypes.c_int
             lib.oracle_sgemm_sampled.argtypes = [i64, i64, i64, dbl, vp, vp, dbl, vp, i64, vp, vp,
                                                  vp, vp]
@@ -205,3 +213,35 @@ def sgemm_sampled(A, B, rows, cols, alpha=1.0, beta=0.0, C0=None):
     if rc != 0:
         raise RuntimeError(f"oracle_sgemm_sampled failed ({rc})")
     return C, S
+
+
+ACTIVATIONS = {"none": 0, "relu": 1, "silu": 2, "gelu_tanh": 3}
+
+
+def activation(v, act: str) -> float:
+    """The activation the fused epilogue applies, in float64."""
+    return float(_load().oracle_activation(float(v), ACTIVATIONS[act]))
+
+
+def gemm_f16_nt_epilogue(A, B, alpha=1.0, bias=None, beta=0.0, R=None, act="none"):
+    """act(alpha·A·Bᵀ + bias[n] + beta·R[m,n]) in float64 for half A [M,K],
+    B [N,K], bias [N], R [M,N].  Returns (Y, S), S the pre-activation scale."""
+    a, b = _as_half_bits(A), _as_half_bits(B)
+    if a.ndim != 2 or b.ndim != 2 or a.shape[1] != b.shape[1]:
+        raise ValueError(f"shape mismatch {a.shape} x {b.shape}^T")
+    M, K = a.shape
+    N = b.shape[0]
+    bb = None if bias is None else _as_half_bits(bias)
+    rr = None if R is None else _as_half_bits(R)
+    if bb is not None and bb.shape != (N,):
+        raise ValueError("bias must be [N]")
+    if rr is not None and rr.shape != (M, N):
+        raise ValueError("R must be [M, N]")
+    Y = np.zeros((M, N), dtype=np.float64)
+    S = np.zeros((M, N), dtype=np.float64)
+    rc = _load().oracle_gemm_f16_nt_epilogue(M, N, K, _ptr(a), _ptr(b), float(alpha), _ptr(bb),
+                                             float(beta), _ptr(rr), ACTIVATIONS[act], _ptr(Y),
+                                             _ptr(S))
+    if rc != 0:
+        raise RuntimeError(f"oracle_gemm_f16_nt_epilogue failed ({rc})")
+    return Y, S

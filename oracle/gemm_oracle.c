@@ -34,8 +34,12 @@
  * Build: plain C99 + OpenMP, no fast-math, no FP contraction:
  *   gcc -O2 -std=c99 -fopenmp -ffp-contract=off -fPIC -shared
  */
+#define _USE_MATH_DEFINES
 #include <math.h>
 #include <stdint.h>
+#ifndef M_PI
+#define M_PI 3.14159265358979323846
+#endif
 #include <stdlib.h>
 #include <string.h>
 #ifdef _OPENMP
@@ -261,6 +265,60 @@ int oracle_sgemm_sampled(int64_t M, int64_t N, int64_t K, double alpha,
             if (S) S[t] = fabs(alpha) * mag;
         }
         free(b);
+    }
+    return 0;
+}
+
+/* ---------------------------------------------------------------------- */
+/* Fused epilogue of the fp16 product ("第 6 章 · Shared Memory & Tile",    */
+/* section "6.5.4 Epilogue 融合": Y = activation(GEMM(X, W) + bias)), with   */
+/* the scalars and residual of the usual GEMM epilogue:                     */
+/*   Y[i][j] = act(alpha * sum_k A[i][k] B[j][k] + bias[j] + beta * R[i][j]) */
+/* act: 0 none, 1 ReLU max(v, 0), 2 SiLU v / (1 + e^-v), 3 GELU with the    */
+/* tanh approximation 0.5 v (1 + tanh(sqrt(2/pi) (v + 0.044715 v^3))).       */
+/* bias (half [N]) and R (half [M,N]) may be NULL (no term).  Y, S: double  */
+/* [M,N]; S = |alpha| sum_k |A B| + |bias[j]| + |beta R[i][j]|, the          */
+/* pre-activation magnitude.                                                 */
+/* ---------------------------------------------------------------------- */
+
+double oracle_activation(double v, int act)
+{
+    switch (act) {
+    case 0: return v;
+    case 1: return v > 0.0 ? v : 0.0;
+    case 2: return v / (1.0 + exp(-v));
+    case 3: return 0.5 * v * (1.0 + tanh(sqrt(2.0 / M_PI) * (v + 0.044715 * v * v * v)));
+    default: return NAN;
+    }
+}
+
+int oracle_gemm_f16_nt_epilogue(int64_t M, int64_t N, int64_t K,
+                                const uint16_t *A, const uint16_t *B,
+                                double alpha, const uint16_t *bias,
+                                double beta, const uint16_t *R, int act,
+                                double *Y, double *S)
+{
+    if (act < 0 || act > 3) return -1;
+    int rc = oracle_gemm_f16_nt(M, N, K, A, B, Y, S);
+    if (rc != 0) return rc;
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < M; ++i) {
+        for (int64_t j = 0; j < N; ++j) {
+            double v = alpha * Y[i * N + j];
+            double mag = fabs(alpha) * S[i * N + j];
+            if (bias) {
+                const double b = oracle_half_to_f64(bias[j]);
+                v += b;
+                mag += fabs(b);
+            }
+            if (R) {
+                const double r = beta * oracle_half_to_f64(R[i * N + j]);
+                v += r;
+                mag += fabs(r);
+            }
+            Y[i * N + j] = oracle_activation(v, act);
+            S[i * N + j] = mag;
+        }
     }
     return 0;
 }

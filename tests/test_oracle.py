@@ -213,3 +213,65 @@ def test_sgemm_sampled_equals_full():
 
 def test_oracle_reports_threads():
     assert oracle.num_threads() >= 1
+
+
+# ----------------------------------------------------------------------------
+# fused epilogue: act(alpha·A·Bᵀ + bias[n] + beta·R[m,n])
+# ----------------------------------------------------------------------------
+
+def test_activations_against_library_and_identities():
+    from scipy.special import erf, expit
+
+    xs = np.linspace(-12, 12, 481)
+    silu = np.array([oracle.activation(x, "silu") for x in xs])
+    assert np.allclose(silu, xs * expit(xs), rtol=1e-13, atol=1e-15)
+    gelu = np.array([oracle.activation(x, "gelu_tanh") for x in xs])
+    exact_gelu = 0.5 * xs * (1 + erf(xs / np.sqrt(2)))
+    assert np.max(np.abs(gelu - exact_gelu)) < 1e-3      # the tanh form's approximation error
+    relu = np.array([oracle.activation(x, "relu") for x in xs])
+    assert np.array_equal(relu, np.maximum(xs, 0))
+    # x·σ(x) and the tanh GELU are both of the form x·(1+g(x))/2 with g odd:
+    # act(x) − act(−x) = x
+    for act in ("silu", "gelu_tanh", "relu"):
+        for x in (0.3, 1.7, -4.2, 9.0):
+            assert abs(oracle.activation(x, act) - oracle.activation(-x, act) - x) < 1e-12
+    assert oracle.activation(0.0, "silu") == 0.0 and oracle.activation(0.0, "gelu_tanh") == 0.0
+
+
+def test_epilogue_exact_through_identity():
+    # B = I: alpha·A + bias + beta·R exactly for small integers; ReLU clips.
+    rng = np.random.default_rng(31)
+    M, K = 6, 10
+    A = rng.integers(-4, 5, (M, K)).astype(np.float16)
+    bias = rng.integers(-3, 4, K).astype(np.float16)
+    R = rng.integers(-5, 6, (M, K)).astype(np.float16)
+    B = np.eye(K, dtype=np.float16)
+    Y, S = oracle.gemm_f16_nt_epilogue(A, B, alpha=2.0, bias=bias, beta=-1.5, R=R)
+    exact = 2.0 * A.astype(np.float64) + bias.astype(np.float64) - 1.5 * R.astype(np.float64)
+    assert np.array_equal(Y, exact)
+    assert np.array_equal(S, 2 * np.abs(A.astype(np.float64)) + np.abs(bias.astype(np.float64))
+                          + 1.5 * np.abs(R.astype(np.float64)))
+    Yr, _ = oracle.gemm_f16_nt_epilogue(A, B, alpha=2.0, bias=bias, beta=-1.5, R=R, act="relu")
+    assert np.array_equal(Yr, np.maximum(exact, 0))
+
+
+@pytest.mark.parametrize("act", ["none", "relu", "silu", "gelu_tanh"])
+def test_epilogue_matches_numpy(act):
+    from scipy.special import expit
+
+    rng = np.random.default_rng(41)
+    M, N, K = 13, 29, 37
+    A = rng.standard_normal((M, K)).astype(np.float16)
+    B = rng.standard_normal((N, K)).astype(np.float16)
+    bias = rng.standard_normal(N).astype(np.float16)
+    R = rng.standard_normal((M, N)).astype(np.float16)
+    Y, S = oracle.gemm_f16_nt_epilogue(A, B, alpha=0.5, bias=bias, beta=2.0, R=R, act=act)
+    v = 0.5 * (A.astype(np.float64) @ B.astype(np.float64).T) + bias.astype(np.float64) \
+        + 2.0 * R.astype(np.float64)
+    f = {"none": lambda x: x, "relu": lambda x: np.maximum(x, 0), "silu": lambda x: x * expit(x),
+         "gelu_tanh": lambda x: 0.5 * x * (1 + np.tanh(np.sqrt(2 / np.pi) * (x + 0.044715 * x ** 3)))}
+    assert np.allclose(Y, f[act](v), rtol=1e-12, atol=1e-12)
+    # without bias or residual the epilogue reduces to the plain product
+    Y0, S0 = oracle.gemm_f16_nt_epilogue(A, B)
+    C, Sc = oracle.gemm_f16_nt(A, B)
+    assert np.array_equal(Y0, C) and np.array_equal(S0, Sc)
