@@ -4,15 +4,22 @@ Two products behind the C ABI of ``include/gemm.h`` (``libgemm.so``):
 
 * ``gemm_f16_nt(M, N, K, A, B, C, stream)``: C = A·Bᵀ, half in, fp32
   accumulation on the tcgen05 tensor cores, half out.
+* ``gemm_f16_nt_fused(..., epi, stream, cfg)``: the same product passed
+  through a fused epilogue act(alpha·A·Bᵀ + bias + beta·R) before rounding.
 * ``sgemm(M, N, K, alpha, A, B, beta, C, stream)``: C = alpha·A·B + beta·C in
   fp32 on the CUDA cores.
 
 This package is the thin Python binding (same names, pointers as ints) plus
-tensor conveniences ``f16_nt`` and ``sgemm_``; ``workloads`` holds the seeded
+tensor conveniences ``f16_nt``, ``f16_nt_fused`` and ``sgemm_``; ``workloads`` holds the seeded
 synthetic inputs.  The library is built in-tree by
 ``python -m dense_gemm_fp16_gb300.build``; without it every call raises.
 """
 from ._binding import (  # noqa: F401
+    ACTIVATIONS,
+    GEMM_ACT_GELU_TANH,
+    GEMM_ACT_NONE,
+    GEMM_ACT_RELU,
+    GEMM_ACT_SILU,
     GEMM_ERR_CUDA,
     GEMM_ERR_DEVICE_TIMEOUT,
     GEMM_ERR_INVALID_ARG,
@@ -31,10 +38,12 @@ from ._binding import (  # noqa: F401
     LIB_PATH,
     GemmError,
     f16_nt,
+    f16_nt_fused,
     gemm_check_device_status,
     gemm_debug_f16_nt_skip_load,
     gemm_f16_nt,
     gemm_f16_nt_ex,
+    gemm_f16_nt_fused,
     gemm_f16_nt_stream_k_noalloc,
     gemm_f16_select,
     gemm_last_error,

@@ -22,6 +22,9 @@ GEMM_ERR_DEVICE_TIMEOUT = -5
 GEMM_F16_AUTO, GEMM_F16_128x256, GEMM_F16_128x128, GEMM_F16_256x256_PAIR, GEMM_F16_GEMV = 0, 1, 2, 3, 4
 GEMM_SGEMM_AUTO, GEMM_SGEMM_128x128, GEMM_SGEMM_64x64 = 0, 1, 2
 GEMM_F16_FLAG_STREAM_K = 1
+GEMM_ACT_NONE, GEMM_ACT_RELU, GEMM_ACT_SILU, GEMM_ACT_GELU_TANH = 0, 1, 2, 3
+ACTIVATIONS = {"none": GEMM_ACT_NONE, "relu": GEMM_ACT_RELU, "silu": GEMM_ACT_SILU,
+               "gelu_tanh": GEMM_ACT_GELU_TANH}
 
 STATUS_NAMES = {
     GEMM_OK: "GEMM_OK",
@@ -41,6 +44,11 @@ class GemmError(RuntimeError):
 
 class _F16Config(ctypes.Structure):
     _fields_ = [("variant", ctypes.c_int), ("grid", ctypes.c_int), ("flags", ctypes.c_int)]
+
+
+class _F16Epilogue(ctypes.Structure):
+    _fields_ = [("alpha", ctypes.c_float), ("beta", ctypes.c_float), ("bias", ctypes.c_void_p),
+                ("residual", ctypes.c_void_p), ("activation", ctypes.c_int)]
 
 
 class _SgemmConfig(ctypes.Structure):
@@ -67,6 +75,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gemm_f16_nt.restype = i
         lib.gemm_f16_nt_ex.argtypes = [i, i, i, vp, vp, vp, vp, ctypes.POINTER(_F16Config)]
         lib.gemm_f16_nt_ex.restype = i
+        lib.gemm_f16_nt_fused.argtypes = [i, i, i, vp, vp, vp, ctypes.POINTER(_F16Epilogue), vp,
+                                          ctypes.POINTER(_F16Config)]
+        lib.gemm_f16_nt_fused.restype = i
         lib.sgemm.argtypes = [i, i, i, f, vp, vp, f, vp, vp]
         lib.sgemm.restype = i
         lib.sgemm_ex.argtypes = [i, i, i, f, vp, vp, f, vp, vp, ctypes.POINTER(_SgemmConfig)]
@@ -108,6 +119,17 @@ def gemm_f16_nt(M: int, N: int, K: int, A: int, B: int, C: int, stream: int | No
 def gemm_f16_nt_ex(M, N, K, A, B, C, stream=0, variant=GEMM_F16_AUTO, grid=0, flags=0) -> int:
     cfg = _F16Config(variant, grid, flags)
     return _check(load_library().gemm_f16_nt_ex(M, N, K, A, B, C, stream or None, ctypes.byref(cfg)))
+
+
+def gemm_f16_nt_fused(M, N, K, A, B, C, alpha=1.0, beta=0.0, bias=0, residual=0,
+                      activation=GEMM_ACT_NONE, stream=0, variant=GEMM_F16_AUTO, grid=0,
+                      flags=0) -> int:
+    """C = act(alpha·A·Bᵀ + bias + beta·residual) rounded to half once; bias and
+    residual are device pointers or 0 (absent)."""
+    epi = _F16Epilogue(float(alpha), float(beta), bias or None, residual or None, int(activation))
+    cfg = _F16Config(variant, grid, flags)
+    return _check(load_library().gemm_f16_nt_fused(M, N, K, A, B, C, ctypes.byref(epi),
+                                                   stream or None, ctypes.byref(cfg)))
 
 
 def gemm_f16_nt_stream_k_noalloc(M: int, N: int, K: int, A: int, B: int, C: int,
@@ -181,6 +203,37 @@ def f16_nt(A, B, C=None, stream=None, variant: int = GEMM_F16_AUTO, grid: int = 
         raise ValueError("C must be a contiguous float16 [M, N] tensor")
     gemm_f16_nt_ex(M, N, K, A.data_ptr(), B.data_ptr(), C.data_ptr(), _stream_handle(stream),
                    variant, grid, flags)
+    return C
+
+
+def f16_nt_fused(A, B, C=None, alpha: float = 1.0, bias=None, beta: float = 0.0, residual=None,
+                 activation: str | int = "none", stream=None, variant: int = GEMM_F16_AUTO,
+                 grid: int = 0, flags: int = 0):
+    """C = act(alpha·A·Bᵀ + bias + beta·residual) for contiguous half CUDA
+    tensors A [M,K], B [N,K], bias [N], residual [M,N] (residual may be C)."""
+    import torch
+
+    if A.dtype != torch.float16 or B.dtype != torch.float16:
+        raise TypeError("f16_nt_fused expects float16 tensors")
+    if not (A.is_cuda and B.is_cuda and A.is_contiguous() and B.is_contiguous()):
+        raise ValueError("f16_nt_fused expects contiguous CUDA tensors")
+    if A.dim() != 2 or B.dim() != 2 or A.shape[1] != B.shape[1]:
+        raise ValueError(f"shape mismatch {tuple(A.shape)} x {tuple(B.shape)}^T")
+    M, K = A.shape
+    N = B.shape[0]
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.float16, device=A.device)
+    elif C.shape != (M, N) or C.dtype != torch.float16 or not C.is_contiguous():
+        raise ValueError("C must be a contiguous float16 [M, N] tensor")
+    for name, t, shape in (("bias", bias, (N,)), ("residual", residual, (M, N))):
+        if t is not None and (t.shape != shape or t.dtype != torch.float16 or not t.is_cuda
+                              or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous float16 CUDA tensor of shape {shape}")
+    act = ACTIVATIONS[activation] if isinstance(activation, str) else int(activation)
+    gemm_f16_nt_fused(M, N, K, A.data_ptr(), B.data_ptr(), C.data_ptr(), alpha, beta,
+                      bias.data_ptr() if bias is not None else 0,
+                      residual.data_ptr() if residual is not None else 0, act,
+                      _stream_handle(stream), variant, grid, flags)
     return C
 
 

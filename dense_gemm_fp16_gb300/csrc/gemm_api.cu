@@ -136,7 +136,8 @@ int gemm_sgemm_select(int M, int N, int K, int sm_count, gemm_sgemm_config *cfg)
 
 static int f16_nt_impl(int M, int N, int K, const void *A, const void *B, void *C,
                        gemm_stream_t stream, const gemm_f16_config *cfg, uint64_t timeout_ns,
-                       int debug_skip_kblock, bool static_scratch = false) {
+                       int debug_skip_kblock, bool static_scratch = false,
+                       const gemm_f16_epilogue *epi = nullptr) {
     if (M < 0 || N < 0 || K < 0)
         return fail(GEMM_ERR_INVALID_ARG, "gemm_f16_nt: negative size M=%d N=%d K=%d", M, N, K);
     if (M == 0 || N == 0) return GEMM_OK;
@@ -147,6 +148,8 @@ static int f16_nt_impl(int M, int N, int K, const void *A, const void *B, void *
     if (K % 8 != 0)
         return fail(GEMM_ERR_UNSUPPORTED,
                     "gemm_f16_nt: K=%d; K*2 bytes must be a multiple of 16 (K %% 8 == 0)", K);
+    if (epi && (epi->activation < 0 || epi->activation >= GEMM_ACT_NUM))
+        return fail(GEMM_ERR_INVALID_ARG, "gemm_f16_nt_fused: unknown activation %d", epi->activation);
     if (cfg && (cfg->variant < 0 || cfg->variant >= GEMM_F16_NUM_VARIANTS || cfg->grid < 0 ||
                 (cfg->flags & ~GEMM_F16_FLAG_STREAM_K) != 0))
         return fail(GEMM_ERR_INVALID_ARG, "gemm_f16_nt_ex: bad config variant=%d grid=%d flags=%d",
@@ -183,6 +186,14 @@ static int f16_nt_impl(int M, int N, int K, const void *A, const void *B, void *
     L.allow_stream_k = cfg && (cfg->flags & GEMM_F16_FLAG_STREAM_K);
     L.static_scratch = static_scratch;
     L.sm_count = sms;
+    if (epi) {
+        L.epi.alpha = epi->alpha;
+        L.epi.beta = epi->beta;
+        L.epi.bias = epi->bias;
+        L.epi.res = epi->residual;
+        L.epi.act = epi->activation;
+        L.epi.on = 1;
+    }
     std::string err;
     st = gb300::f16_launch(L, err);
     if (st != GEMM_OK) return fail_str(st, err);
@@ -196,6 +207,12 @@ int gemm_f16_nt(int M, int N, int K, const void *A, const void *B, void *C, gemm
 int gemm_f16_nt_ex(int M, int N, int K, const void *A, const void *B, void *C,
                    gemm_stream_t stream, const gemm_f16_config *cfg) {
     return f16_nt_impl(M, N, K, A, B, C, stream, cfg, kDefaultTimeoutNs, -1);
+}
+
+int gemm_f16_nt_fused(int M, int N, int K, const void *A, const void *B, void *C,
+                      const gemm_f16_epilogue *epi, gemm_stream_t stream,
+                      const gemm_f16_config *cfg) {
+    return f16_nt_impl(M, N, K, A, B, C, stream, cfg, kDefaultTimeoutNs, -1, false, epi);
 }
 
 // The allocation-free variant declared in gemm.h: the CTA-pair kernel with

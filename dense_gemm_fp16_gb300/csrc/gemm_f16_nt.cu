@@ -41,6 +41,7 @@
 #include <mutex>
 
 #include "gemm.h"
+#include "epilogue.cuh"
 #include "gemm_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -67,6 +68,7 @@ struct F16Args {
     int m_tiles, n_tiles, num_kb;
     int vec_store;          // N % 8 == 0 and C 16-byte aligned
     int tma_store;          // same condition: the epilogue stores through a C tensor map
+    Epi epi;                // fused epilogue (epi.on == 0: the plain product)
     uint64_t timeout_ns;
     int debug_skip_kblock;  // -1 = none
     // Stream-K (pair kernel only): tiles [0, dp_tiles) are data-parallel, one
@@ -244,6 +246,12 @@ __device__ __forceinline__ void epilogue_warp_tile(const F16Args &args, const CU
             tmem_load_32cols(taddr + static_cast<uint32_t>(c * 64), lo);
             tmem_load_32cols(taddr + static_cast<uint32_t>(c * 64 + 32), hi);
             if (pp.count) add_partial_slab(pp, c, lo, hi);
+            if (args.epi.on) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    epi_apply8(args.epi, q < 4 ? &lo[q * 8] : &hi[(q - 4) * 8], row0 + lane,
+                               n_base + c * 64 + q * 8, args.M, args.N);
+            }
             const uint32_t buf = stage_smem + (NBUF == 2 ? (step & 1u) : 0u) * kEpiBufBytes;
             // The store issued from this buffer NBUF slabs ago must have read it.
             if (lane == 0) bulk_wait_group_read<NBUF - 1>();
@@ -280,6 +288,11 @@ __device__ __forceinline__ void epilogue_warp_tile(const F16Args &args, const CU
         for (int c = 0; c < NCOLS / 32; ++c) {
             uint32_t r[32];
             tmem_load_32cols(taddr + static_cast<uint32_t>(c * 32), r);
+            if (args.epi.on) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    epi_apply8(args.epi, &r[q * 8], m, n_base + c * 32 + q * 8, args.M, args.N);
+            }
             store_row_chunk(crow, m < args.M, n_base + c * 32, args.N, args.vec_store, r);
         }
     }
@@ -783,11 +796,14 @@ __global__ void __launch_bounds__((2 + EPI) * 32, 1)
     }
 }
 
-// C = 0 for K == 0 (the empty sum).
-__global__ void zero_half_kernel(__half *C, size_t count) {
+// K == 0: the product is the empty sum; C = 0, or the fused epilogue of 0.
+__global__ void zero_half_kernel(__half *C, int M, int N, Epi epi) {
+    const size_t count = static_cast<size_t>(M) * N;
     const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
-    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < count; i += stride)
-        C[i] = __float2half_rn(0.0f);
+    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < count; i += stride) {
+        const int m = static_cast<int>(i / N), n = static_cast<int>(i % N);
+        C[i] = __float2half_rn(epi.on ? epi_apply1(epi, 0.f, m, n, N) : 0.0f);
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -879,6 +895,7 @@ int launch_variant(const F16Launch &L, std::string &err) {
     args.num_kb = (L.K + kBK - 1) / kBK;
     args.vec_store = (L.N % 8 == 0) && ((reinterpret_cast<uintptr_t>(L.C) & 15u) == 0);
     args.tma_store = args.vec_store;
+    args.epi = make_epi(L.epi, L.N);
     args.timeout_ns = L.timeout_ns;
     args.debug_skip_kblock = L.debug_skip_kblock;
     CUtensorMap tmC;
@@ -1067,6 +1084,7 @@ int launch_pair(const F16Launch &L, std::string &err) {
     args.num_kb = (L.K + kBK - 1) / kBK;
     args.vec_store = (L.N % 8 == 0) && ((reinterpret_cast<uintptr_t>(L.C) & 15u) == 0);
     args.tma_store = args.vec_store;
+    args.epi = make_epi(L.epi, L.N);
     args.timeout_ns = L.timeout_ns;
     args.debug_skip_kblock = L.debug_skip_kblock;
     CUtensorMap tmC;
@@ -1145,7 +1163,8 @@ int f16_launch(const F16Launch &L, std::string &err) {
     if (L.K == 0) {
         const size_t count = static_cast<size_t>(L.M) * L.N;
         const int blocks = static_cast<int>((count + 255) / 256 < 4096 ? (count + 255) / 256 : 4096);
-        zero_half_kernel<<<blocks, 256, 0, L.stream>>>(static_cast<__half *>(L.C), count);
+        zero_half_kernel<<<blocks, 256, 0, L.stream>>>(static_cast<__half *>(L.C), L.M, L.N,
+                                                        make_epi(L.epi, L.N));
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) {
             err = std::string("zero fill launch: ") + cudaGetErrorString(e);
@@ -1158,7 +1177,7 @@ int f16_launch(const F16Launch &L, std::string &err) {
         case GEMM_F16_128x128: return launch_variant<128, 6>(L, err);
         case GEMM_F16_256x256_PAIR: return launch_pair<6, 4>(L, err);
         case GEMM_F16_GEMV: {
-            GemvLaunch G{L.M, L.N, L.K, L.A, L.B, L.C, L.stream, L.sm_count, 4};
+            GemvLaunch G{L.M, L.N, L.K, L.A, L.B, L.C, L.stream, L.sm_count, 4, L.epi};
             return gemv_launch(G, err);
         }
         default: err = "unknown fp16 variant"; return GEMM_ERR_INVALID_ARG;

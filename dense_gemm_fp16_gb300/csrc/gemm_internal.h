@@ -9,6 +9,16 @@
 
 namespace gb300 {
 
+// Fused epilogue of the fp16 product: out = act(alpha * acc + bias[n] + beta * res[m][n]).
+// act: 0 none, 1 ReLU, 2 SiLU, 3 tanh-GELU.  on == 0: out = acc (the plain product).
+struct EpiSpec {
+    float alpha = 1.f, beta = 0.f;
+    const void *bias = nullptr;  // half [N] or null
+    const void *res = nullptr;   // half [M, N] row-major or null (not read when beta == 0)
+    int act = 0;
+    int on = 0;
+};
+
 // One fp16 NT launch, after argument validation and selection.
 struct F16Launch {
     int M, N, K;
@@ -23,6 +33,7 @@ struct F16Launch {
     bool allow_stream_k;    // pair kernel: split the last partial round of tiles along K
     bool static_scratch;    // stream-K partials in the library's static array, no allocation
     int sm_count;           // SMs of the current device
+    EpiSpec epi;            // fused epilogue (off by default)
 };
 
 int f16_launch(const F16Launch &L, std::string &err);
@@ -39,6 +50,7 @@ struct GemvLaunch {
     cudaStream_t stream;
     int sm_count;      // CTAs are planned per SM
     int ctas_per_sm;
+    EpiSpec epi;
 };
 
 int gemv_launch(const GemvLaunch &L, std::string &err);

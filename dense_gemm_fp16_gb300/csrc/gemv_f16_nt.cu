@@ -20,6 +20,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include "epilogue.cuh"
 #include "gemm.h"
 #include "gemm_internal.h"
 
@@ -66,7 +67,7 @@ __device__ __forceinline__ void dot8(float (&acc)[MT], const uint4 &bv, const ui
 template <int MT, int kGemvRows, int kVec, bool VEC>
 __global__ void __launch_bounds__(kGemvWarps * 32)
     gemv_f16_nt_kernel(int M, int N, int K, const __half *__restrict__ A,
-                       const __half *__restrict__ B, __half *__restrict__ C) {
+                       const __half *__restrict__ B, __half *__restrict__ C, const Epi epi) {
     extern __shared__ __align__(16) unsigned char gemv_smem[];
     __shared__ float red[2][kGemvWarps][kGemvRows][MT];
     __half *As = reinterpret_cast<__half *>(gemv_smem);  // [MT][K]
@@ -154,7 +155,9 @@ __global__ void __launch_bounds__(kGemvWarps * 32)
                 float sum = 0.f;
 #pragma unroll
                 for (int w = 0; w < kGemvWarps; ++w) sum += red[buf][w][r][m];
-                C[static_cast<size_t>(m) * N + n0 + r] = __float2half_rn(sum);
+                const int n = n0 + r;
+                C[static_cast<size_t>(m) * N + n] =
+                    __float2half_rn(epi.on ? epi_apply1(epi, sum, m, n, N) : sum);
             }
         }
     }
@@ -189,7 +192,8 @@ int launch_mt(const GemvLaunch &L, std::string &err) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, L.M, L.N, L.K, static_cast<const __half *>(L.A),
-                                       static_cast<const __half *>(L.B), static_cast<__half *>(L.C));
+                                       static_cast<const __half *>(L.B), static_cast<__half *>(L.C),
+                                       make_epi(L.epi, L.N));
     if (e != cudaSuccess) {
         err = std::string("gemv kernel launch: ") + cudaGetErrorString(e);
         return GEMM_ERR_CUDA;

@@ -185,6 +185,45 @@ int gemm_f16_nt_ex(int M, int N, int K, const void *A, const void *B, void *C,
 int gemm_f16_nt_stream_k_noalloc(int M, int N, int K, const void *A, const void *B, void *C,
                                  gemm_stream_t stream);
 
+/* Activation applied by the fused epilogue of gemm_f16_nt_fused. */
+enum {
+    GEMM_ACT_NONE = 0,
+    GEMM_ACT_RELU = 1,       /* max(v, 0)                                              */
+    GEMM_ACT_SILU = 2,       /* v / (1 + exp(-v))                                      */
+    GEMM_ACT_GELU_TANH = 3,  /* 0.5 v (1 + tanh(sqrt(2/pi) (v + 0.044715 v^3)))        */
+    GEMM_ACT_NUM = 4
+};
+
+/* The fused epilogue: every output is
+ *     C[m][n] = half_rn( act( alpha * sum_k A[m][k] B[n][k] + bias[n] + beta * residual[m][n] ) )
+ * computed in fp32 from the fp32 accumulators, rounded to half once.
+ *   bias      device pointer to N halves, or NULL (no bias term);
+ *   residual  device pointer to an M x N row-major half matrix, or NULL; it is
+ *             read only when beta != 0 and it MAY be C itself (each output
+ *             reads its own residual before it is written, so in-place
+ *             C = act(alpha*A*B^T + beta*C) works);
+ *   activation  one of GEMM_ACT_*.
+ * Bias and residual need no alignment; when both are 16-byte aligned and
+ * N % 8 == 0 they are read as 16-byte vectors. */
+typedef struct {
+    float alpha;
+    float beta;
+    const void *bias;
+    const void *residual;
+    int activation;
+} gemm_f16_epilogue;
+
+/* gemm_f16_nt with the product passed through a fused epilogue before the
+ * single rounding to half ("第 6 章 · Shared Memory & Tile", section "6.5.4
+ * Epilogue 融合": bias and activation applied while the accumulators are on
+ * chip, so C makes one trip to HBM instead of three).  Same arguments, layout,
+ * validation and kernel choice as gemm_f16_nt_ex (cfg may be NULL); epi NULL
+ * is the plain product.  epi->activation outside GEMM_ACT_* returns
+ * GEMM_ERR_INVALID_ARG.  K == 0 gives act(bias + beta * residual). */
+int gemm_f16_nt_fused(int M, int N, int K, const void *A, const void *B, void *C,
+                      const gemm_f16_epilogue *epi, gemm_stream_t stream,
+                      const gemm_f16_config *cfg);
+
 /* One kernel configuration of the SGEMM path. */
 typedef struct {
     int variant;

@@ -75,6 +75,9 @@ def _load():
             lib.oracle_gemm_f16_nt_epilogue.restype = ctypes.c_int
             lib.oracle_gemm_f16_nt_epilogue.argtypes = [i64, i64, i64, vp, vp, dbl, vp, dbl, vp,
                                                         ctypes.c_int, vp, vp]
+            lib.oracle_gemm_f16_nt_epilogue_sampled.restype = ctypes.c_int
+            lib.oracle_gemm_f16_nt_epilogue_sampled.argtypes = [
+                i64, i64, i64, vp, vp, dbl, vp, dbl, vp, ctypes.c_int, i64, vp, vp, vp, vp]
             lib.oracle_sgemm_sampled.restype = ctypes.c_int
             lib.oracle_sgemm_sampled.argtypes = [i64, i64, i64, dbl, vp, vp, dbl, vp, i64, vp, vp,
                                                  vp, vp]
@@ -244,4 +247,33 @@ def gemm_f16_nt_epilogue(A, B, alpha=1.0, bias=None, beta=0.0, R=None, act="none
                                              _ptr(S))
     if rc != 0:
         raise RuntimeError(f"oracle_gemm_f16_nt_epilogue failed ({rc})")
+    return Y, S
+
+
+def gemm_f16_nt_epilogue_sampled(A, B, rows, cols, alpha=1.0, bias=None, beta=0.0, R=None,
+                                 act="none"):
+    """Entries (rows[t], cols[t]) of gemm_f16_nt_epilogue.  Returns (Y[t], S[t])."""
+    a, b = _as_half_bits(A), _as_half_bits(B)
+    if a.ndim != 2 or b.ndim != 2 or a.shape[1] != b.shape[1]:
+        raise ValueError(f"shape mismatch {a.shape} x {b.shape}^T")
+    M, K = a.shape
+    N = b.shape[0]
+    bb = None if bias is None else _as_half_bits(bias)
+    rr = None if R is None else _as_half_bits(R)
+    if bb is not None and bb.shape != (N,):
+        raise ValueError("bias must be [N]")
+    if rr is not None and rr.shape != (M, N):
+        raise ValueError("R must be [M, N]")
+    r = np.ascontiguousarray(rows, dtype=np.int64)
+    c = np.ascontiguousarray(cols, dtype=np.int64)
+    if r.shape != c.shape:
+        raise ValueError("rows and cols differ in length")
+    Y = np.zeros(r.shape, dtype=np.float64)
+    S = np.zeros(r.shape, dtype=np.float64)
+    rc = _load().oracle_gemm_f16_nt_epilogue_sampled(M, N, K, _ptr(a), _ptr(b), float(alpha),
+                                                     _ptr(bb), float(beta), _ptr(rr),
+                                                     ACTIVATIONS[act], r.size, _ptr(r), _ptr(c),
+                                                     _ptr(Y), _ptr(S))
+    if rc != 0:
+        raise RuntimeError(f"oracle_gemm_f16_nt_epilogue_sampled failed ({rc})")
     return Y, S

@@ -292,6 +292,28 @@ double oracle_activation(double v, int act)
     }
 }
 
+/* One output of the epilogue from its product acc and scale mag:
+ * Y = act(alpha*acc + bias[j] + beta*R[i][j]), S = |alpha|*mag + |bias[j]| + |beta*R[i][j]|. */
+static void epilogue_at(double acc, double mag, int64_t i, int64_t j, int64_t N,
+                        double alpha, const uint16_t *bias, double beta, const uint16_t *R,
+                        int act, double *y, double *s)
+{
+    double v = alpha * acc;
+    double scale = fabs(alpha) * mag;
+    if (bias) {
+        const double b = oracle_half_to_f64(bias[j]);
+        v += b;
+        scale += fabs(b);
+    }
+    if (R) {
+        const double r = beta * oracle_half_to_f64(R[i * N + j]);
+        v += r;
+        scale += fabs(r);
+    }
+    *y = oracle_activation(v, act);
+    *s = scale;
+}
+
 int oracle_gemm_f16_nt_epilogue(int64_t M, int64_t N, int64_t K,
                                 const uint16_t *A, const uint16_t *B,
                                 double alpha, const uint16_t *bias,
@@ -302,23 +324,25 @@ int oracle_gemm_f16_nt_epilogue(int64_t M, int64_t N, int64_t K,
     int rc = oracle_gemm_f16_nt(M, N, K, A, B, Y, S);
     if (rc != 0) return rc;
 #pragma omp parallel for schedule(static)
-    for (int64_t i = 0; i < M; ++i) {
-        for (int64_t j = 0; j < N; ++j) {
-            double v = alpha * Y[i * N + j];
-            double mag = fabs(alpha) * S[i * N + j];
-            if (bias) {
-                const double b = oracle_half_to_f64(bias[j]);
-                v += b;
-                mag += fabs(b);
-            }
-            if (R) {
-                const double r = beta * oracle_half_to_f64(R[i * N + j]);
-                v += r;
-                mag += fabs(r);
-            }
-            Y[i * N + j] = oracle_activation(v, act);
-            S[i * N + j] = mag;
-        }
-    }
+    for (int64_t i = 0; i < M; ++i)
+        for (int64_t j = 0; j < N; ++j)
+            epilogue_at(Y[i * N + j], S[i * N + j], i, j, N, alpha, bias, beta, R, act,
+                        &Y[i * N + j], &S[i * N + j]);
+    return 0;
+}
+
+/* The same epilogue at n listed positions (rows[t], cols[t]) only. */
+int oracle_gemm_f16_nt_epilogue_sampled(int64_t M, int64_t N, int64_t K,
+                                        const uint16_t *A, const uint16_t *B,
+                                        double alpha, const uint16_t *bias,
+                                        double beta, const uint16_t *R, int act,
+                                        int64_t n, const int64_t *rows, const int64_t *cols,
+                                        double *Y, double *S)
+{
+    if (act < 0 || act > 3) return -1;
+    int rc = oracle_gemm_f16_nt_sampled(M, N, K, A, B, n, rows, cols, Y, S);
+    if (rc != 0) return rc;
+    for (int64_t t = 0; t < n; ++t)
+        epilogue_at(Y[t], S[t], rows[t], cols[t], N, alpha, bias, beta, R, act, &Y[t], &S[t]);
     return 0;
 }

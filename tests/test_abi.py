@@ -34,7 +34,7 @@ def test_headers_declare_the_boundary():
     names = _declared_functions()
     for n in ["gemm_f16_nt", "sgemm", "gemm_last_error", "gemm_check_device_status",
               "gemm_f16_select", "gemm_sgemm_select", "gemm_f16_nt_ex", "sgemm_ex",
-              "gemm_debug_f16_nt_skip_load"]:
+              "gemm_debug_f16_nt_skip_load", "gemm_f16_nt_fused", "gemm_f16_nt_stream_k_noalloc"]:
         assert n in names
 
 
@@ -88,6 +88,22 @@ def test_bad_config_is_rejected(lib):
     with pytest.raises(g.GemmError) as e:
         g.sgemm_ex(16, 16, 16, 1.0, 0x1000, 0x1000, 0.0, 0x1000, variant=7)
     assert e.value.status == g.GEMM_ERR_INVALID_ARG
+
+
+def test_fused_epilogue_arguments_are_checked_on_the_host(lib):
+    for act in (-1, 4, 99):
+        with pytest.raises(g.GemmError) as e:
+            g.gemm_f16_nt_fused(16, 16, 16, 0x1000, 0x1000, 0x1000, activation=act)
+        assert e.value.status == g.GEMM_ERR_INVALID_ARG
+        assert "activation" in str(e.value)
+    with pytest.raises(g.GemmError) as e:
+        g.gemm_f16_nt_fused(-2, 16, 16, 0x1000, 0x1000, 0x1000, activation=g.GEMM_ACT_RELU)
+    assert e.value.status == g.GEMM_ERR_INVALID_ARG
+    with pytest.raises(g.GemmError) as e:
+        g.gemm_f16_nt_fused(16, 16, 16, 0x1008, 0x1000, 0x1000, activation=g.GEMM_ACT_SILU)
+    assert e.value.status == g.GEMM_ERR_MISALIGNED
+    assert g.gemm_f16_nt_fused(0, 16, 16, 0, 0, 0, activation=g.GEMM_ACT_GELU_TANH) == g.GEMM_OK
+    assert g.ACTIVATIONS == {"none": 0, "relu": 1, "silu": 2, "gelu_tanh": 3}
 
 
 def test_f16_selector(lib):

@@ -275,3 +275,21 @@ def test_epilogue_matches_numpy(act):
     Y0, S0 = oracle.gemm_f16_nt_epilogue(A, B)
     C, Sc = oracle.gemm_f16_nt(A, B)
     assert np.array_equal(Y0, C) and np.array_equal(S0, Sc)
+
+
+@pytest.mark.parametrize("act", ["relu", "gelu_tanh"])
+def test_epilogue_sampled_agrees_with_full(act):
+    rng = np.random.default_rng(43)
+    M, N, K = 11, 17, 24
+    A = rng.standard_normal((M, K)).astype(np.float16)
+    B = rng.standard_normal((N, K)).astype(np.float16)
+    bias = rng.standard_normal(N).astype(np.float16)
+    R = rng.standard_normal((M, N)).astype(np.float16)
+    Y, S = oracle.gemm_f16_nt_epilogue(A, B, alpha=-0.75, bias=bias, beta=0.5, R=R, act=act)
+    rows = np.array([0, 10, 3, 7, 10])
+    cols = np.array([0, 16, 5, 0, 2])
+    Ys, Ss = oracle.gemm_f16_nt_epilogue_sampled(A, B, rows, cols, alpha=-0.75, bias=bias,
+                                                 beta=0.5, R=R, act=act)
+    assert np.array_equal(Ys, Y[rows, cols]) and np.array_equal(Ss, S[rows, cols])
+    with pytest.raises(RuntimeError):
+        oracle.gemm_f16_nt_epilogue_sampled(A, B, [M], [0], act=act)
