@@ -22,6 +22,11 @@ ranks is taken and rank 0 prints one JSON line.
   way, as a reference line only.
 * ``sgemm``: the fp32 SGEMM at 4096³ (alpha 1, beta 0.5), a second line
   against the FP32 FFMA peak.
+* ``gemv``: the M = 1 matrix-vector product 1 × 16384 × 8192 against the
+  measured HBM copy bandwidth.
+* ``fused_epilogue``: the headline product with bias, residual and
+  tanh-GELU fused (``gemm_f16_nt_fused``), beside the plain product and the
+  unfused sequence (plain product, then PyTorch element-wise kernels).
 
 N > 1 runs N independent replicas (one per GPU; the product has no exchange
 step), ``scaling: weak``.  ``--impl reference`` times the float64 oracle on
@@ -46,7 +51,8 @@ ROTATE = 4
 FALLBACK_TENSOR_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ["dense_gemm_fp16_gb300/csrc/gemm_f16_nt.cu",
-                  "dense_gemm_fp16_gb300/csrc/sm103_ptx.cuh"]
+                  "dense_gemm_fp16_gb300/csrc/sm103_ptx.cuh",
+                  "dense_gemm_fp16_gb300/csrc/epilogue.cuh"]
 TRAFFIC_FILE = "profiles/gemm_f16_nt_5376x5376x2048_traffic.txt"
 
 
@@ -472,6 +478,48 @@ def run_ours(args):
                                      "peak_source": f"{peak_kind} HBM copy bandwidth"}}
         g.gemm_check_device_status(sh)
 
+    # ---- fused epilogue on the headline product: tanh-GELU(A·Bᵀ + bias + R)
+    # against the plain product and against the unfused sequence (the plain
+    # product, then bias, residual and GELU as separate PyTorch element-wise
+    # kernels, C making three more trips through HBM).
+    if not args.skip_sgemm:
+        with torch.cuda.stream(stream):
+            epi_sets = [(wl.draw_f16((N,), seed=91 + j).cuda(),
+                         wl.draw_f16((M, N), seed=95 + j).cuda()) for j in range(ROTATE)]
+        stream.synchronize()
+
+        def fused(i):
+            a, b, c = sets[i % ROTATE]
+            bias, r = epi_sets[i % ROTATE]
+            g.gemm_f16_nt_fused(M, N, K, a.data_ptr(), b.data_ptr(), c.data_ptr(), 1.0, 1.0,
+                                bias.data_ptr(), r.data_ptr(), g.GEMM_ACT_GELU_TANH, sh)
+
+        def unfused(i):
+            a, b, c = sets[i % ROTATE]
+            bias, r = epi_sets[i % ROTATE]
+            g.gemm_f16_nt(M, N, K, a.data_ptr(), b.data_ptr(), c.data_ptr(), sh)
+            torch.nn.functional.gelu(c + bias + r, approximate="tanh")
+
+        n_ep = 50
+        with torch.cuda.stream(stream):
+            region_time(fused, stream, 5)
+            region_time(unfused, stream, 3)
+            t_plain = region_time(step, stream, n_ep) / n_ep
+            t_fused = region_time(fused, stream, n_ep) / n_ep
+            t_unfused = region_time(unfused, stream, n_ep) / n_ep
+        g.gemm_check_device_status(sh)
+        fval = w.flop / (t_fused * 1e-3) / 1e12
+        line["fused_epilogue"] = {
+            "workload": f"{w.name} + bias[N] + residual[M,N], tanh-GELU",
+            "value": fval, "unit": "TFLOP/s", "us_per_call": 1e3 * t_fused,
+            "plain_us_per_call": 1e3 * t_plain,
+            "unfused_us_per_call": 1e3 * t_unfused,
+            "unfused": "gemm_f16_nt, then PyTorch gelu(C + bias + R) element-wise",
+            "extra_bytes_per_call": 2 * N + 2 * M * N,
+            "roofline": {"bound": "tensor", "achieved": fval, "peak": peak, "unit": "TFLOP/s",
+                         "frac": fval / peak,
+                         "peak_source": f"{peak_kind} bf16 dense burst"}}
+
     if rank == 0 and not args.skip_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, A, B, budget_s=args.cpu_budget)
     if rank == 0:
@@ -495,7 +543,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle work for the cpu_baseline sample")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
-    ap.add_argument("--skip-sgemm", action="store_true")
+    ap.add_argument("--skip-extras", "--skip-sgemm", dest="skip_sgemm", action="store_true",
+                    help="only the headline line: no sgemm, gemv or fused_epilogue objects")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)   # timing rule: at least 3 warm-up steps
     if args.impl == "reference":

@@ -233,30 +233,125 @@ __device__ __forceinline__ void epilogue_warp_partial(float *slot, uint32_t tadd
     }
 }
 
-template <int NCOLS, int NBUF>
-__device__ __forceinline__ void epilogue_warp_tile(const F16Args &args, const CUtensorMap *tmC,
+// The residual of the fused epilogue fetched by TMA (pair kernel, RES
+// instances): the warp's slab s (its s-th 32 x 64 output box) has its
+// residual box loaded into staging buffer s % kResBufs, completing on that
+// buffer's mbarrier, kResAhead slabs before it is needed; the output is then
+// written over it in place and stored from there.  Loading a 128-byte row per
+// request and one instruction per box keeps the residual off the load/store
+// unit, which the accumulator reads and the staging writes also use.
+constexpr int kResBufs = 4;
+constexpr int kResAhead = 2;
+
+struct ResRing {
+    const CUtensorMap *map;
+    uint32_t bar0;    // this warp's kResBufs mbarriers
+    uint32_t issued;  // slabs requested so far (lane 0's count)
+};
+
+// Lane 0: request slab t's residual box (columns n0.., rows row0..).  PENDING
+// is the number of stores committed after the one that last read buffer
+// t % kResBufs (slab t - kResBufs), so after the wait that buffer is free.  A
+// box wholly outside C is not fetched: a plain arrival completes its phase
+// and the lanes read stale values for outputs the store clips anyway.
+template <int PENDING>
+__device__ __forceinline__ void res_request(ResRing &rr, const F16Args &args, uint32_t stage_smem,
+                                            uint32_t t, int n0, int row0) {
+    bulk_wait_group_read<PENDING>();
+    const uint32_t j = t % kResBufs;
+    const uint32_t bar = rr.bar0 + 8u * j;
+    if (row0 < args.M && n0 < args.N) {
+        mbar_arrive_expect_tx(bar, kEpiBufBytes);
+        tma_load_2d(stage_smem + j * kEpiBufBytes, rr.map, bar, n0, row0);
+    } else {
+        mbar_arrive(bar);
+    }
+    ++rr.issued;
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+// ACT < 0: the plain product (no epilogue code); 0..3: the fused epilogue
+// with that activation (0 none, 1 ReLU, 2 SiLU, 3 tanh-GELU).  RES: the
+// residual comes through the TMA ring `rr` (NBUF == kResBufs); otherwise it
+// is loaded into registers.  Returns false when a residual wait ran out.
+template <int NCOLS, int NBUF, int ACT, bool RES = false>
+__device__ __forceinline__ bool epilogue_warp_tile(const F16Args &args, const CUtensorMap *tmC,
                                                    uint32_t taddr, int row0, int n_base, int lane,
                                                    uint32_t stage_smem, uint32_t &step,
-                                                   const Partials &pp = Partials{nullptr, 0, 0, 0, 0}) {
-    static_assert(NCOLS % 64 == 0 && (NBUF == 1 || NBUF == 2), "64-column slabs, 1 or 2 buffers");
+                                                   const Partials &pp = Partials{nullptr, 0, 0, 0, 0},
+                                                   ResRing *rr = nullptr,
+                                                   const volatile int *abort_flag = nullptr) {
+    static_assert(NCOLS % 64 == 0 && (NBUF == 1 || NBUF == 2 || NBUF == kResBufs),
+                  "64-column slabs, 1, 2 or 4 buffers");
+    static_assert(!RES || (ACT >= 0 && NBUF == kResBufs), "the residual ring is the fused path's");
     if (args.tma_store) {
+        // Fused epilogue: the row's 8 residual words of a slab are loaded
+        // together, one slab ahead (issued before the previous slab's stores
+        // and this slab's accumulator reads); the slab's bias is spread over
+        // lanes 0..7 and handed round by shuffles.
+        uint4 res8[8];
+        if constexpr (ACT >= 0 && !RES) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) res8[q] = epi_load_res8(args.epi, row0 + lane, n_base + 8 * q, args.M, args.N);
+        }
 #pragma unroll 1
         for (int c = 0; c < NCOLS / 64; ++c) {
+            const int n0 = n_base + c * 64;
+            const uint32_t buf = stage_smem + (step % NBUF) * kEpiBufBytes;
+            const uint32_t row_addr = buf + static_cast<uint32_t>(lane) * 128u;
+            uint4 bias_l = make_uint4(0u, 0u, 0u, 0u);
+            if constexpr (ACT >= 0) bias_l = epi_load_bias_lane<8>(args.epi, n0, lane, args.N);
+            if constexpr (RES) {
+                // Keep kResAhead slabs of this tile in flight, then take this
+                // slab's residual row from its buffer (chunk q of row `lane` is
+                // at chunk q ^ (lane % 8): the 128-byte swizzle).
+                if (lane == 0 && c + kResAhead < NCOLS / 64)
+                    res_request<kResBufs - 1 - kResAhead>(*rr, args, stage_smem, step + kResAhead,
+                                                          n0 + 64 * kResAhead, row0);
+                // Lane 0 waits (bounded) and the verdict is the warp's; then
+                // every lane observes the completed phase itself (one try_wait,
+                // true at once: the phase cannot move on before this buffer is
+                // requested again), which makes the TMA-written bytes visible
+                // to it.
+                const uint32_t rbar = rr->bar0 + 8u * (step % kResBufs);
+                const uint32_t rpar = (step / kResBufs) & 1u;
+                int arrived = 1;
+                if (lane == 0) arrived = mbar_wait(rbar, rpar, args.timeout_ns, abort_flag) ? 1 : 0;
+                if (!__shfl_sync(0xffffffffu, arrived, 0)) return false;
+                (void)mbar_try_wait(rbar, rpar);
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    res8[q] = ld_shared_v4(row_addr + (static_cast<uint32_t>(q ^ (lane & 7)) << 4));
+            }
             uint32_t lo[32], hi[32];
             tmem_load_32cols(taddr + static_cast<uint32_t>(c * 64), lo);
             tmem_load_32cols(taddr + static_cast<uint32_t>(c * 64 + 32), hi);
             if (pp.count) add_partial_slab(pp, c, lo, hi);
-            if (args.epi.on) {
+            if constexpr (ACT >= 0) {
 #pragma unroll
                 for (int q = 0; q < 8; ++q)
-                    epi_apply8(args.epi, q < 4 ? &lo[q * 8] : &hi[(q - 4) * 8], row0 + lane,
-                               n_base + c * 64 + q * 8, args.M, args.N);
+                    epi_apply8<ACT>(args.epi, q < 4 ? &lo[q * 8] : &hi[(q - 4) * 8], shfl_u4(bias_l, q), res8[q]);
+                if (!RES && c + 1 < NCOLS / 64) {
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        res8[q] = epi_load_res8(args.epi, row0 + lane, n0 + 64 + 8 * q, args.M, args.N);
+                }
             }
-            const uint32_t buf = stage_smem + (NBUF == 2 ? (step & 1u) : 0u) * kEpiBufBytes;
-            // The store issued from this buffer NBUF slabs ago must have read it.
-            if (lane == 0) bulk_wait_group_read<NBUF - 1>();
-            __syncwarp();
-            const uint32_t row_addr = buf + static_cast<uint32_t>(lane) * 128u;
+            // The store issued from this buffer NBUF slabs ago must have read
+            // it (with the residual ring that was ensured before the residual
+            // was loaded into it).
+            if constexpr (!RES) {
+                if (lane == 0) bulk_wait_group_read<NBUF - 1>();
+                __syncwarp();
+            }
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const uint32_t *v = j < 4 ? &lo[j * 8] : &hi[(j - 4) * 8];
@@ -281,24 +376,32 @@ __device__ __forceinline__ void epilogue_warp_tile(const F16Args &args, const CU
             }
             ++step;
         }
+        return true;
     } else {
         const int m = row0 + lane;
         __half *crow = args.C + static_cast<size_t>(m) * args.N;
 #pragma unroll 1
         for (int c = 0; c < NCOLS / 32; ++c) {
+            const int n0 = n_base + c * 32;
+            uint4 res8[4], bias_l = make_uint4(0u, 0u, 0u, 0u);
+            if constexpr (ACT >= 0) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) res8[q] = epi_load_res8(args.epi, m, n0 + 8 * q, args.M, args.N);
+                bias_l = epi_load_bias_lane<4>(args.epi, n0, lane, args.N);
+            }
             uint32_t r[32];
             tmem_load_32cols(taddr + static_cast<uint32_t>(c * 32), r);
-            if (args.epi.on) {
+            if constexpr (ACT >= 0) {
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    epi_apply8(args.epi, &r[q * 8], m, n_base + c * 32 + q * 8, args.M, args.N);
+                for (int q = 0; q < 4; ++q) epi_apply8<ACT>(args.epi, &r[q * 8], shfl_u4(bias_l, q), res8[q]);
             }
             store_row_chunk(crow, m < args.M, n_base + c * 32, args.N, args.vec_store, r);
         }
+        return true;
     }
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int ACT>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_f16_nt_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                           const __grid_constant__ CUtensorMap tmB,
@@ -456,6 +559,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++i) {
             const int b = i & 1;
             const uint32_t ap = (i >> 1) & 1;
+            if constexpr (ACT >= 0) {
+                // The residual rows of this tile (first tile only) and of the
+                // next one go to L2 while the accumulators are being made.
+                const int pf = i == 0 ? tile : tile + static_cast<int>(gridDim.x);
+                if (pf < total_tiles)
+                    epi_prefetch_res(args.epi, (pf % args.m_tiles) * kBM + quarter * 32 + lane,
+                                     (pf / args.m_tiles) * BN, BN, args.M, args.N);
+                if (i == 0 && tile + static_cast<int>(gridDim.x) < total_tiles) {
+                    const int nx = tile + static_cast<int>(gridDim.x);
+                    epi_prefetch_res(args.epi, (nx % args.m_tiles) * kBM + quarter * 32 + lane,
+                                     (nx / args.m_tiles) * BN, BN, args.M, args.N);
+                }
+            }
             int ok = 1;
             if (lane == 0) ok = mbar_wait(accf_bar(b), ap, args.timeout_ns, abort_flag) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -469,7 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after_sync();
             const int mt = tile % args.m_tiles;
             const int nt = tile / args.m_tiles;
-            epilogue_warp_tile<BN, 2>(args, &tmC, tmem_base + lane_field + static_cast<uint32_t>(b * BN),
+            epilogue_warp_tile<BN, 2, ACT>(args, &tmC, tmem_base + lane_field + static_cast<uint32_t>(b * BN),
                                       mt * kBM + quarter * 32, nt * BN, lane, stage_smem, step);
             tc_fence_before_sync();
             __syncwarp();
@@ -522,26 +638,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 //   acce[b]   (even CTA)  accumulator drained: 4 epilogue warps x 2 CTAs.
 // ---------------------------------------------------------------------------
 
-template <int STAGES>
+// EPI_BYTES: epilogue staging; RES_BARS: mbarriers of the residual rings.
+template <int STAGES, int EPI_BYTES = kEpiBytes, int RES_BARS = 0>
 struct PairCfg {
     static constexpr int kBN = 256;                 // pair tile N (= MMA N)
     static constexpr int kABytes = kBM * kBK * 2;   // this CTA's 128 rows of A
     static constexpr int kBBytes = 128 * kBK * 2;   // this CTA's half of B
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kTmemCols = 512;           // two 256-column accumulators
-    static constexpr int kNumBars = 2 * STAGES + 5;
+    static constexpr int kNumBars = 2 * STAGES + 5 + RES_BARS;
     static constexpr int kEpiOffset = STAGES * kStageBytes;
-    static constexpr int kBarOffset = kEpiOffset + kEpiBytes;
+    static constexpr int kBarOffset = kEpiOffset + EPI_BYTES;
     static constexpr int kSmemBytes = 1024 + kBarOffset + kNumBars * 8 + 16;
     static_assert(kSmemBytes <= 232448, "fits the 227 KB opt-in limit");
 };
 
-template <int STAGES, int EPI>
+// RES: the fused epilogue's residual comes through per-warp TMA rings
+// (kResBufs staging buffers per epilogue warp; 4 epilogue warps).
+template <int STAGES, int EPI, int ACT, bool RES>
 __global__ void __launch_bounds__((2 + EPI) * 32, 1)
     gemm_f16_nt_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                             const __grid_constant__ CUtensorMap tmB,
-                            const __grid_constant__ CUtensorMap tmC, const F16Args args) {
-    using T = PairCfg<STAGES>;
+                            const __grid_constant__ CUtensorMap tmC,
+                            const __grid_constant__ CUtensorMap tmR, const F16Args args) {
+    static_assert(!RES || EPI == 4, "residual rings are laid out for 4 epilogue warps");
+    constexpr int kBufs = RES ? kResBufs : 8 / EPI;
+    using T = PairCfg<STAGES, EPI * kBufs * kEpiBufBytes, RES ? EPI * kResBufs : 0>;
     constexpr int BN = T::kBN;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
@@ -555,6 +677,7 @@ __global__ void __launch_bounds__((2 + EPI) * 32, 1)
     auto accf_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
     auto acce_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
     const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+    const uint32_t res_bar0 = bar0 + 8u * (2 * STAGES + 5);  // RES: kResBufs per epilogue warp
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + T::kNumBars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     __shared__ int never_abort;
@@ -570,6 +693,7 @@ __global__ void __launch_bounds__((2 + EPI) * 32, 1)
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
         if (args.tma_store) tma_prefetch_desc(&tmC);
+        if (RES) tma_prefetch_desc(&tmR);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
@@ -578,6 +702,8 @@ __global__ void __launch_bounds__((2 + EPI) * 32, 1)
             mbar_init(accf_bar(b), 1);
             mbar_init(acce_bar(b), 2 * EPI);  // every epilogue warp of both CTAs
         }
+        if (RES)
+            for (int j = 0; j < EPI * kResBufs; ++j) mbar_init(res_bar0 + 8u * j, 1);
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
         never_abort = 0;
@@ -691,18 +817,42 @@ __global__ void __launch_bounds__((2 + EPI) * 32, 1)
         // EPI warps share the tile: warp w reads TMEM lane quarter w % 4 and,
         // with 8 warps, one half of the columns.
         constexpr int kCols = BN * 4 / EPI;
-        constexpr int kBufs = 8 / EPI;
         const int ew = warp - 2;
         const int quarter = warp & 3;
         const int col0 = (ew / 4) * kCols;
         const uint32_t lane_field = static_cast<uint32_t>(quarter * 32) << 16;
         const uint32_t stage_smem = sbase + T::kEpiOffset + ew * kBufs * kEpiBufBytes;
         uint32_t step = 0;
+        ResRing rr{&tmR, res_bar0 + 8u * kResBufs * ew, 0};
         PairWork work(args, pair, num_pairs);
         int tile, kb0, kb1;
         for (int i = 0; work.next(tile, kb0, kb1); ++i) {
             const int b = i & 1;
             const uint32_t ap = (i >> 1) & 1;
+            const int row0 = (tile % args.m_tiles) * 256 + static_cast<int>(rank) * 128 + quarter * 32;
+            const int n_base = (tile / args.m_tiles) * BN + col0;
+            if constexpr (RES) {
+                // The tile's first kResAhead residual boxes load while its
+                // accumulators are being made (stores of earlier slabs pending:
+                // see res_request).
+                if (lane == 0 && kb0 == 0) {
+                    res_request<kResBufs - 1>(rr, args, stage_smem, step, n_base, row0);
+                    res_request<kResBufs - 2>(rr, args, stage_smem, step + 1, n_base + 64, row0);
+                }
+            }
+            if constexpr (ACT >= 0) {
+                // The residual rows of this tile (first tile only) and of the
+                // next one go to L2 while the accumulators are being made.
+                auto prefetch = [&](int t) {
+                    epi_prefetch_res(args.epi, (t % args.m_tiles) * 256 + static_cast<int>(rank) * 128 +
+                                                   quarter * 32 + lane,
+                                     (t / args.m_tiles) * BN + col0, kCols, args.M, args.N);
+                };
+                if (i == 0 && kb0 == 0) prefetch(tile);
+                PairWork peek = work;
+                int t2, k0, k1;
+                if (peek.next(t2, k0, k1) && k0 == 0) prefetch(t2);
+            }
             int ok = 1;
             if (lane == 0)
                 ok = mbar_wait_cluster(accf_bar(b), ap, args.timeout_ns, abort_flag) ? 1 : 0;
@@ -715,8 +865,6 @@ __global__ void __launch_bounds__((2 + EPI) * 32, 1)
                 break;
             }
             tc_fence_after_sync();
-            const int mt = tile % args.m_tiles;
-            const int nt = tile / args.m_tiles;
             const uint32_t taddr = tmem_base + lane_field + static_cast<uint32_t>(b * BN + col0);
             const int region = ew * kCols * 32;    // this warp's part of a partial slot
             if (kb0 > 0) {
@@ -755,13 +903,27 @@ __global__ void __launch_bounds__((2 + EPI) * 32, 1)
                         break;
                     }
                 }
-                epilogue_warp_tile<kCols, kBufs>(args, &tmC, taddr,
-                                                 mt * 256 + static_cast<int>(rank) * 128 + quarter * 32,
-                                                 nt * BN + col0, lane, stage_smem, step, pp);
+                const bool fine = epilogue_warp_tile<kCols, kBufs, ACT, RES>(
+                    args, &tmC, taddr, row0, n_base, lane, stage_smem, step, pp, &rr, abort_flag);
+                if (!fine) {
+                    if (lane == 0) {
+                        if (!*abort_flag) record_timeout(3);
+                        *abort_flag = 1;
+                    }
+                    break;
+                }
             }
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(mapa_shared(acce_bar(b), 0));
+        }
+        if constexpr (RES) {
+            // Residual loads still in flight (only after an abort) land before
+            // this CTA's shared memory is released.
+            if (lane == 0)
+                for (uint32_t t = step; t < rr.issued; ++t)
+                    (void)mbar_wait(rr.bar0 + 8u * (t % kResBufs), (t / kResBufs) & 1u, args.timeout_ns,
+                                    &never_abort);
         }
         if (lane == 0) bulk_wait_group_all();
         __syncwarp();
@@ -801,8 +963,14 @@ __global__ void zero_half_kernel(__half *C, int M, int N, Epi epi) {
     const size_t count = static_cast<size_t>(M) * N;
     const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
     for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < count; i += stride) {
-        const int m = static_cast<int>(i / N), n = static_cast<int>(i % N);
-        C[i] = __float2half_rn(epi.on ? epi_apply1(epi, 0.f, m, n, N) : 0.0f);
+        const int n = static_cast<int>(i % N);
+        float v = 0.f;
+        if (epi.on) {
+            const float b = epi.bias ? __half2float(epi.bias[n]) : 0.f;
+            const float r = epi.reads_res() ? __half2float(epi.res[i]) : 0.f;
+            v = epi_apply1(epi, 0.f, b, r);
+        }
+        C[i] = __float2half_rn(v);
     }
 }
 
@@ -860,10 +1028,10 @@ bool encode_half_map(CUtensorMap *map, const void *ptr, int rows, int cols, int 
     return true;
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int ACT>
 int launch_variant(const F16Launch &L, std::string &err) {
     using T = TileCfg<BN, STAGES>;
-    auto kernel = gemm_f16_nt_tc_kernel<BN, STAGES>;
+    auto kernel = gemm_f16_nt_tc_kernel<BN, STAGES, ACT>;
     // The opt-in for more than 48 KB of dynamic shared memory is per device.
     static int configured[64] = {0};
     int dev = 0;
@@ -1027,10 +1195,11 @@ int noalloc_scratch(cudaStream_t stream, float **ws, uint32_t **flags, uint32_t 
     return GEMM_OK;
 }
 
-template <int STAGES, int EPI>
+template <int STAGES, int EPI, int ACT, bool RES>
 int launch_pair(const F16Launch &L, std::string &err) {
-    using T = PairCfg<STAGES>;
-    auto kernel = gemm_f16_nt_pair_kernel<STAGES, EPI>;
+    constexpr int kBufs = RES ? kResBufs : 8 / EPI;
+    using T = PairCfg<STAGES, EPI * kBufs * kEpiBufBytes, RES ? EPI * kResBufs : 0>;
+    auto kernel = gemm_f16_nt_pair_kernel<STAGES, EPI, ACT, RES>;
     static int max_clusters[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -1087,9 +1256,11 @@ int launch_pair(const F16Launch &L, std::string &err) {
     args.epi = make_epi(L.epi, L.N);
     args.timeout_ns = L.timeout_ns;
     args.debug_skip_kblock = L.debug_skip_kblock;
-    CUtensorMap tmC;
+    CUtensorMap tmC, tmR;
     std::memset(&tmC, 0, sizeof tmC);
+    std::memset(&tmR, 0, sizeof tmR);
     if (args.tma_store && !encode_half_map(&tmC, L.C, L.M, L.N, 32, 64, err)) return GEMM_ERR_CUDA;
+    if (RES && !encode_half_map(&tmR, L.epi.res, L.M, L.N, 32, 64, err)) return GEMM_ERR_CUDA;
     const int tiles = args.m_tiles * args.n_tiles;
     int pairs = L.grid / 2;
     if (pairs < 1) pairs = 1;
@@ -1149,12 +1320,46 @@ int launch_pair(const F16Launch &L, std::string &err) {
     }
     cfg.gridDim = dim3(2 * pairs);
     cfg.numAttrs = 2;  // cluster shape + programmatic dependent launch
-    e = cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, tmC, args);
+    e = cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, tmC, tmR, args);
     if (e != cudaSuccess) {
         err = std::string("gemm_f16_nt pair kernel launch: ") + cudaGetErrorString(e);
         return GEMM_ERR_CUDA;
     }
     return GEMM_OK;
+}
+
+// One kernel per epilogue: the plain product, or the fused epilogue with
+// each activation.
+template <int BN, int STAGES>
+int launch_variant_epi(const F16Launch &L, std::string &err) {
+    switch (L.epi.on ? L.epi.act : -1) {
+        case 0: return launch_variant<BN, STAGES, 0>(L, err);
+        case 1: return launch_variant<BN, STAGES, 1>(L, err);
+        case 2: return launch_variant<BN, STAGES, 2>(L, err);
+        case 3: return launch_variant<BN, STAGES, 3>(L, err);
+        default: return launch_variant<BN, STAGES, -1>(L, err);
+    }
+}
+
+// Pair kernels: 6-stage ring for the plain product and for epilogues without
+// a residual; with a residual that TMA can fetch (16-byte aligned, N % 8 == 0,
+// TMA-store epilogue) a 5-stage ring, whose 32 KB go to the residual rings.
+template <bool RES>
+int launch_pair_act(const F16Launch &L, std::string &err) {
+    constexpr int S = RES ? 5 : 6;
+    switch (L.epi.on ? L.epi.act : -1) {
+        case 0: return launch_pair<S, 4, 0, RES>(L, err);
+        case 1: return launch_pair<S, 4, 1, RES>(L, err);
+        case 2: return launch_pair<S, 4, 2, RES>(L, err);
+        case 3: return launch_pair<S, 4, 3, RES>(L, err);
+        default: return launch_pair<6, 4, -1, false>(L, err);
+    }
+}
+
+int launch_pair_epi(const F16Launch &L, std::string &err) {
+    const bool res_tma = L.epi.on && L.epi.res != nullptr && L.epi.beta != 0.f && L.N % 8 == 0 &&
+                         ((reinterpret_cast<uintptr_t>(L.C) | reinterpret_cast<uintptr_t>(L.epi.res)) & 15u) == 0;
+    return res_tma ? launch_pair_act<true>(L, err) : launch_pair_act<false>(L, err);
 }
 
 }  // namespace
@@ -1173,9 +1378,9 @@ int f16_launch(const F16Launch &L, std::string &err) {
         return GEMM_OK;
     }
     switch (L.variant) {
-        case GEMM_F16_128x256: return launch_variant<256, 4>(L, err);
-        case GEMM_F16_128x128: return launch_variant<128, 6>(L, err);
-        case GEMM_F16_256x256_PAIR: return launch_pair<6, 4>(L, err);
+        case GEMM_F16_128x256: return launch_variant_epi<256, 4>(L, err);
+        case GEMM_F16_128x128: return launch_variant_epi<128, 6>(L, err);
+        case GEMM_F16_256x256_PAIR: return launch_pair_epi(L, err);
         case GEMM_F16_GEMV: {
             GemvLaunch G{L.M, L.N, L.K, L.A, L.B, L.C, L.stream, L.sm_count, 4, L.epi};
             return gemv_launch(G, err);

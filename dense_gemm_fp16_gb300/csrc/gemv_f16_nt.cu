@@ -92,6 +92,16 @@ __global__ void __launch_bounds__(kGemvWarps * 32)
 
     int buf = 0;
     for (int n0 = r0; n0 < r1; n0 += kGemvRows, buf ^= 1) {
+        // The finishing threads fetch their bias and residual now; the loads
+        // complete under this group's dot products.
+        float eb = 0.f, er = 0.f;
+        if (epi.on && threadIdx.x < kGemvRows * MT) {
+            const int r = threadIdx.x / MT, m = threadIdx.x % MT;
+            if (n0 + r < r1 && m < M) {
+                if (epi.bias) eb = __half2float(epi.bias[n0 + r]);
+                if (epi.reads_res()) er = __half2float(epi.res[static_cast<size_t>(m) * N + n0 + r]);
+            }
+        }
         float acc[kGemvRows][MT];
 #pragma unroll
         for (int r = 0; r < kGemvRows; ++r)
@@ -157,7 +167,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32)
                 for (int w = 0; w < kGemvWarps; ++w) sum += red[buf][w][r][m];
                 const int n = n0 + r;
                 C[static_cast<size_t>(m) * N + n] =
-                    __float2half_rn(epi.on ? epi_apply1(epi, sum, m, n, N) : sum);
+                    __float2half_rn(epi.on ? epi_apply1(epi, sum, eb, er) : sum);
             }
         }
     }

@@ -109,13 +109,16 @@ def test_fused_identity_epilogue_equals_plain_product():
     assert torch.equal(plain, fused)
 
 
-def test_fused_in_place_residual():
-    # C = gelu(A·Bᵀ + bias + C): the residual is the output buffer itself.
+@pytest.mark.parametrize("variant", [g.GEMM_F16_AUTO, g.GEMM_F16_256x256_PAIR])
+def test_fused_in_place_residual(variant):
+    # C = gelu(A·Bᵀ + bias + C): the residual is the output buffer itself
+    # (the pair kernel fetches it by TMA into the staging it stores from).
     M, N, K = 520, 776, 200
     A, B, bias, R = _inputs(M, N, K, seed=31)
     dA, dB, dbias = A.cuda(), B.cuda(), bias.cuda()
     C = R.cuda()
-    g.f16_nt_fused(dA, dB, C, alpha=1.0, bias=dbias, beta=1.0, residual=C, activation="gelu_tanh")
+    g.f16_nt_fused(dA, dB, C, alpha=1.0, bias=dbias, beta=1.0, residual=C, activation="gelu_tanh",
+                   variant=variant)
     torch.cuda.synchronize()
     Y, S = oracle.gemm_f16_nt_epilogue(A, B, alpha=1.0, bias=bias, beta=1.0, R=R, act="gelu_tanh")
     check_f16_epilogue(C.cpu().numpy(), Y, S, what="in place")
