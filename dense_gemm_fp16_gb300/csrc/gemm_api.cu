@@ -67,7 +67,7 @@ inline long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 
 // Persistent CTA count of an fp16 variant: one CTA (or CTA pair) per tile up
 // to one per SM.
-int f16_default_grid(int variant, int M, int N, int sm_count) {
+int f16_default_grid(int variant, int M, int N, int K, int sm_count) {
     long long tiles;
     if (variant == GEMM_F16_GEMV) return sm_count;  // planned per SM by the GEMV launcher
     switch (variant) {
@@ -76,7 +76,11 @@ int f16_default_grid(int variant, int M, int N, int sm_count) {
         default: tiles = ceil_div(M, 128) * ceil_div(N, 128); break;
     }
     long long cap = sm_count;
-    if (variant == GEMM_F16_256x256_PAIR) cap = sm_count & ~1;
+    if (variant == GEMM_F16_256x256_PAIR) {
+        cap = sm_count & ~1;
+        // Split-K spreads few tiles over all the pairs.
+        if (gb300::pair_split_pairs(tiles / 2, ceil_div(K, 64), sm_count / 2) > 0) return static_cast<int>(cap);
+    }
     long long g = tiles < cap ? tiles : cap;
     return static_cast<int>(g > 0 ? g : 1);
 }
@@ -107,12 +111,17 @@ int gemm_f16_select(int M, int N, int K, int sm_count, gemm_f16_config *cfg) {
     // reading B from HBM bounds the product, and the matrix-vector kernel
     // streams B once (when those rows of A fit in its shared memory).  From
     // three rows on, its fp32 FMAs fall behind HBM and the tensor cores win.
+    // When even the 128 x 128 tiles would leave most SMs idle over a long K,
+    // the pair kernel splits each pair tile's k-blocks over several pairs
+    // (split-K) and spreads the work over all of them.
     const long long pair_tiles = ceil_div(M, 256) * ceil_div(N, 256);
-    int variant = (pair_tiles >= sm_count / 2 && N > 128) ? GEMM_F16_256x256_PAIR
-                                                          : GEMM_F16_128x128;
+    const bool split = ceil_div(M, 128) * ceil_div(N, 128) * 2 <= sm_count &&
+                       gb300::pair_split_pairs(pair_tiles, ceil_div(K, 64), sm_count / 2) > 0;
+    int variant = ((pair_tiles >= sm_count / 2 && N > 128) || split) ? GEMM_F16_256x256_PAIR
+                                                                     : GEMM_F16_128x128;
     if (M <= 2 && gb300::gemv_smem_bytes(M, K) <= kGemvMaxSmem) variant = GEMM_F16_GEMV;
     cfg->variant = variant;
-    cfg->grid = f16_default_grid(variant, M, N, sm_count);
+    cfg->grid = f16_default_grid(variant, M, N, K, sm_count);
     cfg->flags = 0;
     return GEMM_OK;
 }
@@ -162,7 +171,7 @@ static int f16_nt_impl(int M, int N, int K, const void *A, const void *B, void *
     if (st != GEMM_OK) return st;
     if (cfg && cfg->variant != GEMM_F16_AUTO) {
         sel.variant = cfg->variant;
-        sel.grid = f16_default_grid(sel.variant, M, N, sms);
+        sel.grid = f16_default_grid(sel.variant, M, N, K, sms);
         if (sel.variant == GEMM_F16_GEMV &&
             (M > 2 || (K > 0 && gb300::gemv_smem_bytes(M, K) > kGemvMaxSmem)))
             return fail(GEMM_ERR_UNSUPPORTED,

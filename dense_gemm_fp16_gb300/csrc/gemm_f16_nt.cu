@@ -1265,27 +1265,41 @@ int launch_pair(const F16Launch &L, std::string &err) {
     int pairs = L.grid / 2;
     if (pairs < 1) pairs = 1;
     if (pairs > clusters) pairs = clusters;
-    if (pairs > tiles) pairs = tiles;
 
-    // Stream-K for the last, partial round of tiles when it would leave many
-    // pairs idle: their k-blocks are shared out evenly instead.  Needs the TMA
-    // store epilogue, a share of at least one k-block per pair, and a stream
-    // that is not being captured (a replayed graph would reuse the sequence
-    // number baked into its arguments).
+    // The k-blocks of some tiles shared out over several pairs (stream-K),
+    // whose fp32 partials the pair holding k-block 0 adds before rounding:
+    //  * split-K, by default, when the tiles would leave most pairs idle (fewer
+    //    than half as many tiles as pairs, enough k-blocks per share): every
+    //    tile is split, over at most kMaxSplit pairs;
+    //  * on request (GEMM_F16_FLAG_STREAM_K), the last partial round of tiles
+    //    when it would leave many pairs idle.
+    // Both need the TMA store epilogue and a stream that is not being captured
+    // (a replayed graph would reuse the sequence number baked into its
+    // arguments); otherwise every tile is whole.
     args.dp_tiles = tiles;
     args.sk_units = 0;
     args.sk_ws = nullptr;
     args.sk_flags = nullptr;
     args.seq = 0;
-    const int rem = tiles % pairs;
-    if (L.allow_stream_k && args.tma_store && tiles > pairs && rem != 0 &&
-        10 * rem < 9 * pairs && static_cast<long long>(rem) * args.num_kb >= pairs) {
+    const int split_pairs = args.tma_store ? pair_split_pairs(tiles, args.num_kb, pairs) : 0;
+    int rem = 0;  // tiles of the shared round
+    if (split_pairs > 0) {
+        rem = tiles;
+    } else {
+        if (pairs > tiles) pairs = tiles;
+        const int r = tiles % pairs;
+        if (L.allow_stream_k && args.tma_store && tiles > pairs && r != 0 && 10 * r < 9 * pairs &&
+            static_cast<long long>(r) * args.num_kb >= pairs)
+            rem = r;
+    }
+    if (rem > 0) {
         cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
         e = cudaStreamIsCapturing(L.stream, &cap);
         if (e != cudaSuccess) {
             err = std::string("cudaStreamIsCapturing: ") + cudaGetErrorString(e);
             return GEMM_ERR_CUDA;
         }
+        if (split_pairs > 0) pairs = cap == cudaStreamCaptureStatusNone ? split_pairs : (pairs < tiles ? pairs : tiles);
         if (cap == cudaStreamCaptureStatusNone && !L.static_scratch) {
             SkWorkspace *w = nullptr;
             const int st = sk_workspace(L.stream, pairs, &w, err);

@@ -125,6 +125,13 @@ def test_f16_selector(lib):
     assert g.gemm_f16_select(1024, 1024, 1024, 152) == (g.GEMM_F16_128x128, 64)
     assert g.gemm_f16_select(100, 100, 64, 152) == (g.GEMM_F16_128x128, 1)
     assert g.gemm_f16_select(128, 8192, 64, 148)[0] == g.GEMM_F16_128x128
+    # few tiles over a long K: pair tiles split along K over all the pairs
+    assert g.gemm_f16_select(512, 512, 32768, 152) == (g.GEMM_F16_256x256_PAIR, 152)
+    assert g.gemm_f16_select(256, 256, 65536, 152) == (g.GEMM_F16_256x256_PAIR, 152)
+    assert g.gemm_f16_select(128, 4096, 8192, 152) == (g.GEMM_F16_256x256_PAIR, 152)
+    # ... but not when a split would be shallower than four ways
+    assert g.gemm_f16_select(1024, 1024, 4096, 152) == (g.GEMM_F16_128x128, 64)
+    assert g.gemm_f16_select(64, 8192, 8192, 152) == (g.GEMM_F16_128x128, 64)
     with pytest.raises(g.GemmError):
         g.gemm_f16_select(1, 1, 1, 0)
 

@@ -232,3 +232,34 @@ def test_f16_nt_pair_stream_k_two_streams():
     g.gemm_check_device_status(0)
     for C in outs:
         check_f16(C.cpu().numpy(), Cref, S, what="two streams")
+
+
+@pytest.mark.parametrize("M,N,K,grid", [
+    (256, 256, 8192, 8),      # one tile split four ways (4 pairs, 32 k-blocks each)
+    (200, 300, 8200, 16),     # two ragged tiles split eight ways, a partial last k-block
+    (512, 256, 16384, 152),   # two tiles over the full grid: eight ways each
+])
+def test_f16_nt_split_k_underfilled(M, N, K, grid):
+    # Few pair tiles over a long K: every tile's k-blocks are shared out over
+    # several pairs by default (no flag); the owner adds the partials.
+    A = wl.draw_f16((M, K), seed=81, dist="normal")
+    B = wl.draw_f16((N, K), seed=82, dist="normal")
+    Cref, S = oracle.gemm_f16_nt(A, B)
+    for rep in range(2):
+        C = _run(A, B, g.GEMM_F16_256x256_PAIR, grid)
+        check_f16(C, Cref, S, what=f"split-K {M}x{N}x{K} grid {grid} rep {rep}")
+
+
+@pytest.mark.parametrize("M,N,K", [(512, 512, 32768), (256, 256, 65536), (128, 4096, 8192)])
+def test_f16_nt_split_k_selector_shapes_sampled(M, N, K):
+    # The selector's choice for these shapes is the split pair kernel.
+    A = wl.draw_f16((M, K), seed=83)
+    B = wl.draw_f16((N, K), seed=84)
+    dA, dB = A.cuda(), B.cuda()
+    C = g.f16_nt(dA, dB)
+    g.gemm_check_device_status(0)
+    Ch = C.cpu().numpy()
+    rows, cols = wl.sample_positions(M, N, 8192, seed=2027)
+    Cref, S = oracle.gemm_f16_nt_sampled(A, B, rows, cols)
+    check_f16(Ch[rows, cols], Cref, S, what=f"split-K default {M}x{N}x{K}")
+

@@ -157,6 +157,17 @@ def test_fused_with_stream_k(M, N, K, grid):
         check_f16_epilogue(C, Y, S, what=f"stream-K grid {grid} rep {rep}")
 
 
+@pytest.mark.parametrize("act", ["relu", "gelu_tanh"])
+def test_fused_with_split_k(act):
+    # One tile split four ways (4 pairs): the owner adds the partials, then
+    # applies the epilogue with the residual from its TMA ring.
+    M, N, K = 256, 256, 8192
+    A, B, bias, R = _inputs(M, N, K, seed=65)
+    Y, S = oracle.gemm_f16_nt_epilogue(A, B, alpha=0.5, bias=bias, beta=-1.0, R=R, act=act)
+    C = _run(A, B, bias, R, 0.5, -1.0, act, g.GEMM_F16_256x256_PAIR, 8)
+    check_f16_epilogue(C, Y, S, what=f"split-K {act}")
+
+
 @pytest.mark.parametrize("act", ACTS)
 @pytest.mark.parametrize("M,N,K", [(1, 1000, 4096), (2, 777, 520)])
 def test_fused_gemv(M, N, K, act):
