@@ -95,6 +95,20 @@ def draw_int(shape, seed: int, lo: int, hi: int, dtype=torch.float32) -> torch.T
     return torch.randint(lo, hi + 1, tuple(shape), generator=g, dtype=torch.int64).to(dtype)
 
 
+def draw_mxfp8(rows: int, K: int, seed: int, scale_lo: int = 125, scale_hi: int = 129):
+    """Block-scaled FP8 operands as stored: E4M3 codes [rows, K] (uint8) and
+    UE8M0 scale codes [rows, K/32] (uint8).  Elements are standard-normal
+    draws cast to E4M3 by PyTorch; scale codes are uniform integers in
+    [scale_lo, scale_hi] (2^-2 .. 2^2 by default)."""
+    if K % 32:
+        raise ValueError("K must be a multiple of 32")
+    g = _gen(seed)
+    x = torch.randn((rows, K), generator=g, dtype=torch.float32)
+    codes = x.to(torch.float8_e4m3fn).view(torch.uint8)
+    scales = torch.randint(scale_lo, scale_hi + 1, (rows, K // 32), generator=g, dtype=torch.int64)
+    return codes.contiguous(), scales.to(torch.uint8).contiguous()
+
+
 def make_inputs(w: Workload):
     """Host tensors (A, B, C0) of a workload; C0 is None when beta == 0."""
     if w.form == "f16_nt":

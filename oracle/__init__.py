@@ -17,6 +17,9 @@ each function follows:
 * ``gemm_f16_nt_epilogue``: "第 6 章 · Shared Memory & Tile", section
   "6.5.4 Epilogue 融合" (activation(GEMM + bias)), with alpha, beta and a
   residual.
+* ``gemm_mxfp8_nt``: "异步拷贝与 Hopper/Blackwell 新特性", section
+  "Blackwell 概览 sm_100" (MXFP8: 32 elements share one 8-bit exponent
+  scale), E4M3 elements and UE8M0 scales.
 
 Every function returns the unrounded float64 result C and the tolerance
 scale S = |alpha|·Σ_k |A·B| per element.
@@ -78,6 +81,16 @@ def _load():
             lib.oracle_gemm_f16_nt_epilogue_sampled.restype = ctypes.c_int
             lib.oracle_gemm_f16_nt_epilogue_sampled.argtypes = [
                 i64, i64, i64, vp, vp, dbl, vp, dbl, vp, ctypes.c_int, i64, vp, vp, vp, vp]
+            u8 = ctypes.c_uint8
+            lib.oracle_e4m3_to_f64.restype = dbl
+            lib.oracle_e4m3_to_f64.argtypes = [u8]
+            lib.oracle_ue8m0_to_f64.restype = dbl
+            lib.oracle_ue8m0_to_f64.argtypes = [u8]
+            lib.oracle_gemm_mxfp8_nt.restype = ctypes.c_int
+            lib.oracle_gemm_mxfp8_nt.argtypes = [i64, i64, i64, vp, vp, vp, vp, vp, vp]
+            lib.oracle_gemm_mxfp8_nt_sampled.restype = ctypes.c_int
+            lib.oracle_gemm_mxfp8_nt_sampled.argtypes = [i64, i64, i64, vp, vp, vp, vp, i64, vp, vp,
+                                                         vp, vp]
             lib.oracle_sgemm_sampled.restype = ctypes.c_int
             lib.oracle_sgemm_sampled.argtypes = [i64, i64, i64, dbl, vp, vp, dbl, vp, i64, vp, vp,
                                                  vp, vp]
@@ -277,3 +290,70 @@ def gemm_f16_nt_epilogue_sampled(A, B, rows, cols, alpha=1.0, bias=None, beta=0.
     if rc != 0:
         raise RuntimeError(f"oracle_gemm_f16_nt_epilogue_sampled failed ({rc})")
     return Y, S
+
+
+def _as_u8(x) -> np.ndarray:
+    if hasattr(x, "numpy"):
+        x = x.contiguous().cpu()
+        import torch
+
+        if x.dtype != torch.uint8:
+            x = x.view(torch.uint8)
+        x = x.numpy()
+    return np.ascontiguousarray(x, dtype=np.uint8)
+
+
+def e4m3_to_f64(codes) -> np.ndarray:
+    """FP8 E4M3 codes (uint8) decoded to float64 (NaN for S.1111.111)."""
+    c = _as_u8(codes)
+    f = _load().oracle_e4m3_to_f64
+    return np.array([f(int(v)) for v in c.ravel()], dtype=np.float64).reshape(c.shape)
+
+
+def ue8m0_to_f64(codes) -> np.ndarray:
+    """UE8M0 scale codes decoded to float64: 2^(e-127), NaN for 0xFF."""
+    c = _as_u8(codes)
+    f = _load().oracle_ue8m0_to_f64
+    return np.array([f(int(v)) for v in c.ravel()], dtype=np.float64).reshape(c.shape)
+
+
+def _mx_args(A, SA, B, SB):
+    a, sa, b, sb = _as_u8(A), _as_u8(SA), _as_u8(B), _as_u8(SB)
+    if a.ndim != 2 or b.ndim != 2 or a.shape[1] != b.shape[1]:
+        raise ValueError(f"shape mismatch {a.shape} x {b.shape}^T")
+    M, K = a.shape
+    N = b.shape[0]
+    if K % 32:
+        raise ValueError("K must be a multiple of the 32-element scale block")
+    if sa.shape != (M, K // 32) or sb.shape != (N, K // 32):
+        raise ValueError(f"scales must be [M, K/32] and [N, K/32], got {sa.shape} and {sb.shape}")
+    return a, sa, b, sb, M, N, K
+
+
+def gemm_mxfp8_nt(A, SA, B, SB):
+    """sum_k e4m3(A[m,k]) 2^(SA[m,k/32]-127) * e4m3(B[n,k]) 2^(SB[n,k/32]-127)
+    in float64 for uint8 codes A [M,K], B [N,K] and scales SA [M,K/32],
+    SB [N,K/32].  Returns (C, S)."""
+    a, sa, b, sb, M, N, K = _mx_args(A, SA, B, SB)
+    C = np.zeros((M, N), dtype=np.float64)
+    S = np.zeros((M, N), dtype=np.float64)
+    rc = _load().oracle_gemm_mxfp8_nt(M, N, K, _ptr(a), _ptr(sa), _ptr(b), _ptr(sb), _ptr(C), _ptr(S))
+    if rc != 0:
+        raise RuntimeError(f"oracle_gemm_mxfp8_nt failed ({rc})")
+    return C, S
+
+
+def gemm_mxfp8_nt_sampled(A, SA, B, SB, rows, cols):
+    """Entries (rows[t], cols[t]) of gemm_mxfp8_nt.  Returns (C[t], S[t])."""
+    a, sa, b, sb, M, N, K = _mx_args(A, SA, B, SB)
+    r = np.ascontiguousarray(rows, dtype=np.int64)
+    c = np.ascontiguousarray(cols, dtype=np.int64)
+    if r.shape != c.shape:
+        raise ValueError("rows and cols differ in length")
+    C = np.zeros(r.shape, dtype=np.float64)
+    S = np.zeros(r.shape, dtype=np.float64)
+    rc = _load().oracle_gemm_mxfp8_nt_sampled(M, N, K, _ptr(a), _ptr(sa), _ptr(b), _ptr(sb), r.size,
+                                              _ptr(r), _ptr(c), _ptr(C), _ptr(S))
+    if rc != 0:
+        raise RuntimeError(f"oracle_gemm_mxfp8_nt_sampled failed ({rc})")
+    return C, S

@@ -25,6 +25,8 @@
  *    section "cp.async 与多级流水 sm_80+", the gemm_cp_async listing's
  *    epilogue c = alpha*acc + beta*c over row-major A[M,K], B[K,N], C[M,N],
  *    and the CPU reference loop of its host harness.
+ *  - block-scaled FP8 (MXFP8) NT product: the same page, section
+ *    "Blackwell 概览 sm_100" (32 elements share one 8-bit exponent scale).
  *
  * Precision: the pages accumulate in float; this oracle accumulates in
  * float64 and keeps the result unrounded, so that the GPU result can be
@@ -132,7 +134,9 @@ static void dot_nt(const double *a_row, const double *b_row, int64_t K,
 {
     double acc = 0.0, mag = 0.0;
     for (int64_t k = 0; k < K; ++k) {
-        const double p = a_row[k] * b_row[k];  /* exact: 11 x 11 bit significands */
+        /* exact: two halves (11-bit significands) or two scaled E4M3 values
+         * (4-bit significands, exponents far inside double's range) */
+        const double p = a_row[k] * b_row[k];
         acc += p;
         mag += fabs(p);
     }
@@ -344,5 +348,113 @@ int oracle_gemm_f16_nt_epilogue_sampled(int64_t M, int64_t N, int64_t K,
     if (rc != 0) return rc;
     for (int64_t t = 0; t < n; ++t)
         epilogue_at(Y[t], S[t], rows[t], cols[t], N, alpha, bias, beta, R, act, &Y[t], &S[t]);
+    return 0;
+}
+
+/* ---------------------------------------------------------------------- */
+/* Block-scaled FP8 (MXFP8): "异步拷贝与 Hopper/Blackwell 新特性", section   */
+/* "Blackwell 概览 sm_100": in MXFP8 every 32 consecutive elements share   */
+/* one 8-bit exponent scale factor.  The element format is FP8 E4M3 and    */
+/* the scale UE8M0 (the OCP microscaling formats Blackwell's block-scaled   */
+/* MMA reads):                                                               */
+/*   E4M3: 1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits;        */
+/*         exponent 0 = subnormal m/8 * 2^-6; S.1111.111 = NaN; no inf.     */
+/*   UE8M0: an unsigned exponent alone, 2^(e - 127); 0xFF = NaN.            */
+/* The product of one row of A with one row of B (both K-major):            */
+/*   C[m][n] = sum_k e4m3(A[m][k]) 2^(SA[m][k/32] - 127)                    */
+/*                   * e4m3(B[n][k]) 2^(SB[n][k/32] - 127)                  */
+/* with SA [M][K/32], SB [N][K/32] row-major.  Each term is exact in        */
+/* double (4 + 4 significant bits, exponents within range).                 */
+/* ---------------------------------------------------------------------- */
+
+double oracle_e4m3_to_f64(uint8_t c)
+{
+    const int sign = (c >> 7) & 1;
+    const int expo = (c >> 3) & 0xf;
+    const int mant = c & 0x7;
+    double v;
+    if (expo == 0xf && mant == 0x7) return NAN;
+    if (expo == 0)
+        v = ldexp((double)mant / 8.0, -6);
+    else
+        v = ldexp(1.0 + (double)mant / 8.0, expo - 7);
+    return sign ? -v : v;
+}
+
+double oracle_ue8m0_to_f64(uint8_t e)
+{
+    if (e == 0xff) return NAN;
+    return ldexp(1.0, (int)e - 127);
+}
+
+/* Row r of an MXFP8 matrix (K codes, K/32 scales) decoded to doubles. */
+static void decode_mx_row(const uint8_t *codes, const uint8_t *scales, int64_t K, double *out)
+{
+    for (int64_t k = 0; k < K; ++k)
+        out[k] = oracle_e4m3_to_f64(codes[k]) * oracle_ue8m0_to_f64(scales[k / 32]);
+}
+
+static double *decode_mx_matrix(int64_t rows, int64_t K, const uint8_t *codes, const uint8_t *scales)
+{
+    double *d = (double *)malloc((size_t)(rows > 0 ? rows : 1) * (size_t)(K > 0 ? K : 1) * sizeof(double));
+    if (!d) return NULL;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r)
+        decode_mx_row(codes + r * K, scales + r * (K / 32), K, d + r * K);
+    return d;
+}
+
+int oracle_gemm_mxfp8_nt(int64_t M, int64_t N, int64_t K,
+                         const uint8_t *A, const uint8_t *SA,
+                         const uint8_t *B, const uint8_t *SB,
+                         double *C, double *S)
+{
+    if (M < 0 || N < 0 || K < 0 || K % 32 != 0) return -1;
+    double *a = decode_mx_matrix(M, K, A, SA);
+    double *b = decode_mx_matrix(N, K, B, SB);
+    if (!a || !b) {
+        free(a);
+        free(b);
+        return -2;
+    }
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < M; ++i)
+        for (int64_t j = 0; j < N; ++j) {
+            double acc, mag;
+            dot_nt(a + i * K, b + j * K, K, &acc, &mag);
+            C[i * N + j] = acc;
+            if (S) S[i * N + j] = mag;
+        }
+    free(a);
+    free(b);
+    return 0;
+}
+
+/* The same product at n listed positions (rows[t], cols[t]) only. */
+int oracle_gemm_mxfp8_nt_sampled(int64_t M, int64_t N, int64_t K,
+                                 const uint8_t *A, const uint8_t *SA,
+                                 const uint8_t *B, const uint8_t *SB,
+                                 int64_t n, const int64_t *rows, const int64_t *cols,
+                                 double *C, double *S)
+{
+    if (M < 0 || N < 0 || K < 0 || K % 32 != 0 || n < 0) return -1;
+    for (int64_t t = 0; t < n; ++t)
+        if (rows[t] < 0 || rows[t] >= M || cols[t] < 0 || cols[t] >= N) return -1;
+#pragma omp parallel
+    {
+        double *a = (double *)malloc((size_t)(K > 0 ? K : 1) * sizeof(double));
+        double *b = (double *)malloc((size_t)(K > 0 ? K : 1) * sizeof(double));
+#pragma omp for schedule(static)
+        for (int64_t t = 0; t < n; ++t) {
+            decode_mx_row(A + rows[t] * K, SA + rows[t] * (K / 32), K, a);
+            decode_mx_row(B + cols[t] * K, SB + cols[t] * (K / 32), K, b);
+            double acc, mag;
+            dot_nt(a, b, K, &acc, &mag);
+            C[t] = acc;
+            if (S) S[t] = mag;
+        }
+        free(a);
+        free(b);
+    }
     return 0;
 }

@@ -293,3 +293,102 @@ def test_epilogue_sampled_agrees_with_full(act):
     assert np.array_equal(Ys, Y[rows, cols]) and np.array_equal(Ss, S[rows, cols])
     with pytest.raises(RuntimeError):
         oracle.gemm_f16_nt_epilogue_sampled(A, B, [M], [0], act=act)
+
+
+# ---------------------------------------------------------------------------
+# Block-scaled FP8 (MXFP8)
+# ---------------------------------------------------------------------------
+
+def test_e4m3_and_ue8m0_decode_every_code_like_torch():
+    import torch
+
+    codes = np.arange(256, dtype=np.uint8)
+    for ours, dt in ((oracle.e4m3_to_f64(codes), torch.float8_e4m3fn),
+                     (oracle.ue8m0_to_f64(codes), getattr(torch, "float8_e8m0fnu", None))):
+        if dt is None:
+            continue
+        ref = torch.from_numpy(codes).view(dt).double().numpy()
+        assert np.array_equal(np.isnan(ours), np.isnan(ref))
+        assert np.array_equal(ours[~np.isnan(ours)], ref[~np.isnan(ref)])
+    # the closed forms: largest finite E4M3 is 448, smallest subnormal 2^-9,
+    # UE8M0 127 is 1 and every code e is 2^(e-127)
+    e = oracle.e4m3_to_f64(np.array([0x7E, 0x01, 0x38, 0xB8, 0x7F], dtype=np.uint8))
+    assert e[0] == 448.0 and e[1] == 2.0 ** -9 and e[2] == 1.0 and e[3] == -1.0 and np.isnan(e[4])
+    u = oracle.ue8m0_to_f64(np.arange(255, dtype=np.uint8))
+    assert np.array_equal(u, 2.0 ** (np.arange(255) - 127.0))
+
+
+def _mx_decode_ref(codes, scales):
+    # independent decode for the pins: PyTorch's float8 cast, scale repeated
+    import torch
+
+    v = torch.from_numpy(np.ascontiguousarray(codes)).view(torch.float8_e4m3fn).double().numpy()
+    return v * np.repeat(2.0 ** (scales.astype(np.float64) - 127.0), 32, axis=1)
+
+
+def test_mxfp8_small_integers_exact_against_brute_force():
+    # E4M3 represents the integers -8..8 exactly; scales 127 (x1), 128 (x2)
+    # and 126 (x1/2) keep every product and sum exact.
+    rng = np.random.default_rng(51)
+    M, N, K = 5, 7, 64
+    import torch
+
+    ai = rng.integers(-8, 9, (M, K))
+    bi = rng.integers(-8, 9, (N, K))
+    A = torch.from_numpy(ai.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    B = torch.from_numpy(bi.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    SA = rng.integers(126, 129, (M, K // 32)).astype(np.uint8)
+    SB = rng.integers(126, 129, (N, K // 32)).astype(np.uint8)
+    C, S = oracle.gemm_mxfp8_nt(A, SA, B, SB)
+    from fractions import Fraction
+
+    for i in range(M):
+        for j in range(N):
+            exact = sum(Fraction(int(ai[i, k]) * int(bi[j, k])) *
+                        Fraction(2) ** (int(SA[i, k // 32]) + int(SB[j, k // 32]) - 254)
+                        for k in range(K))
+            assert C[i, j] == float(exact)
+            assert S[i, j] == float(sum(abs(Fraction(int(ai[i, k]) * int(bi[j, k]))) *
+                                        Fraction(2) ** (int(SA[i, k // 32]) + int(SB[j, k // 32]) - 254)
+                                        for k in range(K)))
+
+
+def test_mxfp8_each_scale_covers_its_own_32_elements():
+    # Ones everywhere; only block b of row 0 of A gets scale 2^3: the result
+    # grows by exactly 7 * 32 (one block of ones now worth 8 instead of 1).
+    M, N, K = 2, 3, 128
+    one = 0x38
+    A = np.full((M, K), one, np.uint8)
+    B = np.full((N, K), one, np.uint8)
+    SA = np.full((M, K // 32), 127, np.uint8)
+    SB = np.full((N, K // 32), 127, np.uint8)
+    base, _ = oracle.gemm_mxfp8_nt(A, SA, B, SB)
+    assert np.all(base == K)
+    for b in range(K // 32):
+        SA2 = SA.copy()
+        SA2[0, b] = 130
+        C, _ = oracle.gemm_mxfp8_nt(A, SA2, B, SB)
+        assert np.all(C[0] == K + 7 * 32) and np.all(C[1] == K)
+        SB2 = SB.copy()
+        SB2[2, b] = 125
+        C, _ = oracle.gemm_mxfp8_nt(A, SA, B, SB2)
+        assert np.all(C[:, 2] == K - 0.75 * 32) and np.all(C[:, :2] == K)
+
+
+def test_mxfp8_matches_numpy_and_sampled():
+    from dense_gemm_fp16_gb300 import workloads as wl
+
+    M, N, K = 37, 29, 160
+    A, SA = wl.draw_mxfp8(M, K, seed=61)
+    B, SB = wl.draw_mxfp8(N, K, seed=62)
+    A, SA, B, SB = A.numpy(), SA.numpy(), B.numpy(), SB.numpy()
+    C, S = oracle.gemm_mxfp8_nt(A, SA, B, SB)
+    a, b = _mx_decode_ref(A, SA), _mx_decode_ref(B, SB)
+    assert np.allclose(C, a @ b.T, rtol=0, atol=1e-12 * S.max())
+    assert np.allclose(S, np.abs(a) @ np.abs(b).T, rtol=1e-13)
+    rows = np.array([0, 36, 5, 17])
+    cols = np.array([0, 28, 3, 11])
+    Cs, Ss = oracle.gemm_mxfp8_nt_sampled(A, SA, B, SB, rows, cols)
+    assert np.array_equal(Cs, C[rows, cols]) and np.array_equal(Ss, S[rows, cols])
+    with pytest.raises(ValueError):
+        oracle.gemm_mxfp8_nt(A[:, :40], SA[:, :1], B[:, :40], SB[:, :1])
