@@ -6,6 +6,8 @@ Two products behind the C ABI of ``include/gemm.h`` (``libgemm.so``):
   accumulation on the tcgen05 tensor cores, half out.
 * ``gemm_f16_nt_fused(..., epi, stream, cfg)``: the same product passed
   through a fused epilogue act(alpha·A·Bᵀ + bias + beta·R) before rounding.
+* ``gemm_mxfp8_nt(M, N, K, A, SFA, B, SFB, C, stream)``: the block-scaled
+  FP8 (MXFP8) product on the tensor cores, half out.
 * ``sgemm(M, N, K, alpha, A, B, beta, C, stream)``: C = alpha·A·B + beta·C in
   fp32 on the CUDA cores.
 
@@ -45,10 +47,15 @@ from ._binding import (  # noqa: F401
     gemm_f16_nt_ex,
     gemm_f16_nt_fused,
     gemm_f16_nt_stream_k_noalloc,
+    gemm_mxfp8_nt,
+    gemm_mxfp8_pack_scales,
+    gemm_mxfp8_scale_bytes,
     gemm_f16_select,
     gemm_last_error,
     gemm_sgemm_select,
     load_library,
+    mxfp8_nt,
+    mxfp8_pack_scales,
     sgemm,
     sgemm_,
     sgemm_ex,

@@ -78,6 +78,12 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gemm_f16_nt_fused.argtypes = [i, i, i, vp, vp, vp, ctypes.POINTER(_F16Epilogue), vp,
                                           ctypes.POINTER(_F16Config)]
         lib.gemm_f16_nt_fused.restype = i
+        lib.gemm_mxfp8_nt.argtypes = [i, i, i, vp, vp, vp, vp, vp, vp]
+        lib.gemm_mxfp8_nt.restype = i
+        lib.gemm_mxfp8_scale_bytes.argtypes = [i, i]
+        lib.gemm_mxfp8_scale_bytes.restype = ctypes.c_size_t
+        lib.gemm_mxfp8_pack_scales.argtypes = [i, i, vp, vp, vp]
+        lib.gemm_mxfp8_pack_scales.restype = i
         lib.sgemm.argtypes = [i, i, i, f, vp, vp, f, vp, vp]
         lib.sgemm.restype = i
         lib.sgemm_ex.argtypes = [i, i, i, f, vp, vp, f, vp, vp, ctypes.POINTER(_SgemmConfig)]
@@ -130,6 +136,19 @@ def gemm_f16_nt_fused(M, N, K, A, B, C, alpha=1.0, beta=0.0, bias=0, residual=0,
     cfg = _F16Config(variant, grid, flags)
     return _check(load_library().gemm_f16_nt_fused(M, N, K, A, B, C, ctypes.byref(epi),
                                                    stream or None, ctypes.byref(cfg)))
+
+
+def gemm_mxfp8_nt(M, N, K, A, SFA, B, SFB, C, stream=0) -> int:
+    """Block-scaled FP8 product; SFA/SFB in the chunk layout (pointers as ints)."""
+    return _check(load_library().gemm_mxfp8_nt(M, N, K, A, SFA, B, SFB, C, stream or None))
+
+
+def gemm_mxfp8_scale_bytes(rows: int, K: int) -> int:
+    return int(load_library().gemm_mxfp8_scale_bytes(rows, K))
+
+
+def gemm_mxfp8_pack_scales(rows, K, plain, blocked, stream=0) -> int:
+    return _check(load_library().gemm_mxfp8_pack_scales(rows, K, plain, blocked, stream or None))
 
 
 def gemm_f16_nt_stream_k_noalloc(M: int, N: int, K: int, A: int, B: int, C: int,
@@ -234,6 +253,41 @@ def f16_nt_fused(A, B, C=None, alpha: float = 1.0, bias=None, beta: float = 0.0,
                       bias.data_ptr() if bias is not None else 0,
                       residual.data_ptr() if residual is not None else 0, act,
                       _stream_handle(stream), variant, grid, flags)
+    return C
+
+
+def mxfp8_pack_scales(S, stream=None):
+    """Plain UE8M0 scales [rows, K/32] (uint8 CUDA tensor) -> the chunk layout."""
+    import torch
+
+    if S.dtype != torch.uint8 or not S.is_cuda or not S.is_contiguous() or S.dim() != 2:
+        raise ValueError("scales must be a contiguous uint8 CUDA tensor [rows, K/32]")
+    rows, ksf = S.shape
+    K = 32 * ksf
+    out = torch.empty(gemm_mxfp8_scale_bytes(rows, K), dtype=torch.uint8, device=S.device)
+    gemm_mxfp8_pack_scales(rows, K, S.data_ptr(), out.data_ptr(), _stream_handle(stream))
+    return out
+
+
+def mxfp8_nt(A, SA, B, SB, C=None, stream=None, packed=False):
+    """C (half) = MXFP8 product of E4M3 codes A [M,K], B [N,K] (uint8 CUDA
+    tensors) with UE8M0 scales SA [M,K/32], SB [N,K/32] (or, with packed=True,
+    already in the chunk layout)."""
+    import torch
+
+    for t in (A, B):
+        if t.dtype != torch.uint8 or not t.is_cuda or not t.is_contiguous() or t.dim() != 2:
+            raise ValueError("A and B must be contiguous uint8 CUDA tensors (E4M3 codes)")
+    if A.shape[1] != B.shape[1]:
+        raise ValueError(f"shape mismatch {tuple(A.shape)} x {tuple(B.shape)}^T")
+    M, K = A.shape
+    N = B.shape[0]
+    if not packed:
+        SA, SB = mxfp8_pack_scales(SA, stream), mxfp8_pack_scales(SB, stream)
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.float16, device=A.device)
+    gemm_mxfp8_nt(M, N, K, A.data_ptr(), SA.data_ptr(), B.data_ptr(), SB.data_ptr(), C.data_ptr(),
+                  _stream_handle(stream))
     return C
 
 

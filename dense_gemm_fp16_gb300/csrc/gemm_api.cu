@@ -240,6 +240,64 @@ int gemm_debug_f16_nt_skip_load(int M, int N, int K, const void *A, const void *
 }
 
 // ---------------------------------------------------------------------------
+// Block-scaled FP8 (MXFP8)
+// ---------------------------------------------------------------------------
+
+size_t gemm_mxfp8_scale_bytes(int rows, int K) {
+    if (rows <= 0 || K <= 0) return 0;
+    return static_cast<size_t>((rows + 127) / 128) * static_cast<size_t>((K + 127) / 128) * 512;
+}
+
+int gemm_mxfp8_pack_scales(int rows, int K, const void *plain, void *blocked, gemm_stream_t stream) {
+    if (rows < 0 || K < 0)
+        return fail(GEMM_ERR_INVALID_ARG, "gemm_mxfp8_pack_scales: negative size rows=%d K=%d", rows, K);
+    if (K % 32 != 0)
+        return fail(GEMM_ERR_UNSUPPORTED, "gemm_mxfp8_pack_scales: K=%d is not a multiple of 32", K);
+    if (rows == 0 || K == 0) return GEMM_OK;
+    if (!plain || !blocked) return fail(GEMM_ERR_INVALID_ARG, "gemm_mxfp8_pack_scales: NULL pointer");
+    std::string err;
+    const int st = gb300::mx_pack_scales_launch(rows, K, plain, blocked,
+                                                reinterpret_cast<cudaStream_t>(stream), err);
+    if (st != GEMM_OK) return fail_str(st, err);
+    return GEMM_OK;
+}
+
+int gemm_mxfp8_nt(int M, int N, int K, const void *A, const void *SFA, const void *B,
+                  const void *SFB, void *C, gemm_stream_t stream) {
+    if (M < 0 || N < 0 || K < 0)
+        return fail(GEMM_ERR_INVALID_ARG, "gemm_mxfp8_nt: negative size M=%d N=%d K=%d", M, N, K);
+    if (M == 0 || N == 0) return GEMM_OK;
+    if (!C) return fail(GEMM_ERR_INVALID_ARG, "gemm_mxfp8_nt: C is NULL");
+    if (K % 32 != 0)
+        return fail(GEMM_ERR_UNSUPPORTED,
+                    "gemm_mxfp8_nt: K=%d; the 32-element scale blocks need K %% 32 == 0", K);
+    if (K == 0) return f16_nt_impl(M, N, 0, nullptr, nullptr, C, stream, nullptr, kDefaultTimeoutNs, -1);
+    if (!A || !B || !SFA || !SFB) return fail(GEMM_ERR_INVALID_ARG, "gemm_mxfp8_nt: NULL operand");
+    if (!aligned16(A) || !aligned16(B) || !aligned16(SFA) || !aligned16(SFB))
+        return fail(GEMM_ERR_MISALIGNED, "gemm_mxfp8_nt: A, B, SFA and SFB must be 16-byte aligned");
+    int sms = 0;
+    int st = sm_count_of_current_device(&sms);
+    if (st != GEMM_OK) return st;
+    gb300::MxLaunch L;
+    L.M = M;
+    L.N = N;
+    L.K = K;
+    L.A = A;
+    L.SFA = SFA;
+    L.B = B;
+    L.SFB = SFB;
+    L.C = C;
+    L.stream = reinterpret_cast<cudaStream_t>(stream);
+    L.grid = 0;
+    L.timeout_ns = kDefaultTimeoutNs;
+    L.sm_count = sms;
+    std::string err;
+    st = gb300::mx_launch(L, err);
+    if (st != GEMM_OK) return fail_str(st, err);
+    return GEMM_OK;
+}
+
+// ---------------------------------------------------------------------------
 // SGEMM
 // ---------------------------------------------------------------------------
 

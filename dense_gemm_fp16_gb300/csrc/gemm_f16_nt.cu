@@ -624,6 +624,270 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
+// Block-scaled FP8 (MXFP8) NT product, "异步拷贝与 Hopper/Blackwell 新特性",
+// section "Blackwell 概览 sm_100": E4M3 A [M,K] and B [N,K] (K-major), one
+// UE8M0 scale per row per 32 elements of K, fp32 accumulation on the tensor
+// cores (tcgen05.mma kind::mxf8f6f4, block_scale, scale_vec::1X), half C.
+//
+// The same warp roles as the 1-CTA fp16 kernel, with 128 x 128 output tiles
+// and 128-element (128-byte) k-blocks.  Each stage also carries the two
+// tiles' scales for the k-block: 128 rows x 4 scales each, a 512-byte chunk
+// stored contiguously in the operand's scale array (see gemm_mxfp8_nt in
+// gemm.h for the layout: byte 16*(r % 32) + 4*(r / 32) + j of the chunk is
+// row r's j-th scale).  The MMA thread copies each chunk into TMEM
+// (tcgen05.cp 32x128b.warpx4: TMEM lane r holds, in column c, the four
+// scales of row 32c + r % 32) ahead of the four K = 32 MMAs of the k-block,
+// which pick scale j through the descriptor's scale-factor IDs; copies and
+// MMAs from one thread run in order, so one scale area per stage suffices.
+// ---------------------------------------------------------------------------
+
+constexpr int kMxBK = 128;       // K elements (bytes) per k-block: one 128-byte swizzle row
+constexpr int kMxBN = 128;       // output tile columns
+constexpr int kMxStages = 5;
+constexpr int kMxUmmaK = 32;     // K per MMA instruction
+constexpr int kMxSfChunk = 512;  // 128 rows x 4 scales
+
+struct MxCfg {
+    static constexpr int kABytes = kBM * kMxBK;
+    static constexpr int kBBytes = kMxBN * kMxBK;
+    static constexpr int kStageBytes = kABytes + kBBytes + 2 * kMxSfChunk;
+    static constexpr int kTmemCols = 512;  // 2 x 128 accumulator columns, then 8 scale columns per stage
+    static constexpr int kSfCol0 = 2 * kMxBN;
+    static constexpr int kNumBars = 2 * kMxStages + 5;
+    static constexpr int kEpiOffset = kMxStages * kStageBytes;
+    static constexpr int kBarOffset = kEpiOffset + kEpiBytes;
+    static constexpr int kSmemBytes = 1024 + kBarOffset + kNumBars * 8 + 16;
+    static_assert(kStageBytes % 1024 == 0, "swizzle atoms stay 1024-byte aligned");
+    static_assert(kSfCol0 + 8 * kMxStages <= kTmemCols, "scale columns fit the allocation");
+    static_assert(kSmemBytes <= 232448, "fits the 227 KB opt-in limit");
+};
+
+struct MxArgs {
+    const uint8_t *sfa;  // scale chunks of A: [ceil(M/128)][ceil(K/128)][512]
+    const uint8_t *sfb;  // scale chunks of B: [ceil(N/128)][ceil(K/128)][512]
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_mxfp8_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                         const __grid_constant__ CUtensorMap tmC, const F16Args args, const MxArgs mx) {
+    using T = MxCfg;
+    constexpr int BN = kMxBN;
+    constexpr int STAGES = kMxStages;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+    const uint32_t sbase = smem_addr(smem);
+
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + T::kBarOffset);
+    const uint32_t bar0 = smem_addr(bars);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto accf_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+    auto acce_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + T::kNumBars);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    __shared__ int never_abort;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+        if (args.tma_store) tma_prefetch_desc(&tmC);
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf_bar(b), 1);
+            mbar_init(acce_bar(b), 4);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        never_abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr(tmem_slot), T::kTmemCols);
+        tmem_relinquish_alloc_permit();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+    pdl_launch_dependents();
+    pdl_wait_prerequisites();
+
+    const int total_tiles = args.m_tiles * args.n_tiles;
+    const int num_kb = args.num_kb;
+    uint32_t armed = 0, arm_parity = 0;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+                const int mt = tile % args.m_tiles;
+                const int nt = tile / args.m_tiles;
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, args.timeout_ns, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sa = sbase + stage * T::kStageBytes;
+                    const uint32_t sb = sa + T::kABytes;
+                    const uint32_t ssf = sb + T::kBBytes;
+                    mbar_arrive_expect_tx(full_bar(stage), T::kStageBytes);
+                    tma_load_2d(sa, &tmA, full_bar(stage), kb * kMxBK, mt * kBM);
+                    tma_load_2d(sb, &tmB, full_bar(stage), kb * kMxBK, nt * BN);
+                    bulk_load(ssf, mx.sfa + (static_cast<size_t>(mt) * num_kb + kb) * kMxSfChunk,
+                              kMxSfChunk, full_bar(stage));
+                    bulk_load(ssf + kMxSfChunk, mx.sfb + (static_cast<size_t>(nt) * num_kb + kb) * kMxSfChunk,
+                              kMxSfChunk, full_bar(stage));
+                    armed |= 1u << stage;
+                    arm_parity ^= 1u << stage;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                if (!*abort_flag) record_timeout(1);
+                *abort_flag = 1;
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ scale copies + MMA issuer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            int i = 0;
+            for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++i) {
+                const int b = i & 1;
+                const uint32_t ap = (i >> 1) & 1;
+                if (!mbar_wait(acce_bar(b), ap ^ 1u, args.timeout_ns, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait(full_bar(stage), phase, args.timeout_ns, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t sa = sbase + stage * T::kStageBytes;
+                    const uint32_t sb = sa + T::kABytes;
+                    const uint32_t ssf = sb + T::kBBytes;
+                    const uint32_t sfa_tmem = tmem_base + static_cast<uint32_t>(T::kSfCol0 + 8 * stage);
+                    const uint32_t sfb_tmem = sfa_tmem + 4u;
+                    // each chunk: 32 rows of 16 bytes, 8-row core matrices 128 bytes apart
+                    tmem_cp_32x128b_warpx4(sfa_tmem, plain_kmajor_desc(ssf, 128, 128));
+                    tmem_cp_32x128b_warpx4(sfb_tmem, plain_kmajor_desc(ssf + kMxSfChunk, 128, 128));
+                    const uint64_t adesc = sw128_kmajor_desc(sa);
+                    const uint64_t bdesc = sw128_kmajor_desc(sb);
+#pragma unroll
+                    for (int j = 0; j < kMxBK / kMxUmmaK; ++j) {
+                        // K = 32 FP8 per MMA: the start address advances 32 bytes;
+                        // scale j of each row (its 32-element block) applies.
+                        mma_mxf8_ss(d_tmem, adesc + 2u * j, bdesc + 2u * j, idesc_mxf8_e4m3(kBM, BN, j),
+                                    sfa_tmem, sfb_tmem, (kb > 0 || j > 0) ? 1u : 0u);
+                    }
+                    mma_commit(empty_bar(stage));
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                mma_commit(accf_bar(b));
+            }
+            if (!ok) {
+                if (!*abort_flag) record_timeout(2);
+                *abort_flag = 1;
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int quarter = warp & 3;
+        const uint32_t lane_field = static_cast<uint32_t>(quarter * 32) << 16;
+        const uint32_t stage_smem = sbase + T::kEpiOffset + (warp - 2) * 2 * kEpiBufBytes;
+        uint32_t step = 0;
+        int i = 0;
+        for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++i) {
+            const int b = i & 1;
+            const uint32_t ap = (i >> 1) & 1;
+            int ok = 1;
+            if (lane == 0) ok = mbar_wait(accf_bar(b), ap, args.timeout_ns, abort_flag) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) {
+                if (lane == 0) {
+                    if (!*abort_flag) record_timeout(3);
+                    *abort_flag = 1;
+                }
+                break;
+            }
+            tc_fence_after_sync();
+            const int mt = tile % args.m_tiles;
+            const int nt = tile / args.m_tiles;
+            epilogue_warp_tile<BN, 2, -1>(args, &tmC, tmem_base + lane_field + static_cast<uint32_t>(b * BN),
+                                          mt * kBM + quarter * 32, nt * BN, lane, stage_smem, step);
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acce_bar(b));
+        }
+        if (lane == 0) bulk_wait_group_all();
+        __syncwarp();
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (*abort_flag) {
+        if (warp == 0 && lane == 0) {
+            for (int s = 0; s < STAGES; ++s)
+                if (armed & (1u << s))
+                    (void)mbar_wait(full_bar(s), ((arm_parity >> s) & 1u) ^ 1u, args.timeout_ns,
+                                    &never_abort);
+        }
+        if (warp == 1 && lane == 0) {
+            mma_commit(drain_bar);
+            (void)mbar_wait(drain_bar, 0, args.timeout_ns, &never_abort);
+        }
+        __syncwarp();
+        tc_fence_before_sync();
+        __syncthreads();
+    }
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, T::kTmemCols);
+    }
+}
+
+// Plain scales [rows][K/32] -> the kernel's chunk layout, padded with 127
+// (2^0) past the last row and the last scale; one thread per output byte.
+__global__ void mx_pack_scales_kernel(const uint8_t *__restrict__ plain, uint8_t *__restrict__ blocked,
+                                      int rows, int ksf, int kbt, size_t total) {
+    const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+    for (size_t o = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; o < total; o += stride) {
+        const size_t chunk = o / kMxSfChunk;
+        const int within = static_cast<int>(o % kMxSfChunk);
+        const int rt = static_cast<int>(chunk / kbt), kb = static_cast<int>(chunk % kbt);
+        const int r = rt * 128 + (within >> 4) + 32 * ((within >> 2) & 3);
+        const int j = kb * 4 + (within & 3);
+        blocked[o] = (r < rows && j < ksf) ? plain[static_cast<size_t>(r) * ksf + j] : uint8_t(127);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // CTA-pair variant: a cluster of two CTAs computes a 256 x 256 output tile
 // with tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16).  CTA r of the pair
 // loads rows 128r .. 128r+127 of the tile's A block and rows 128r .. 128r+127
@@ -1004,17 +1268,19 @@ EncodeTiledFn get_encode_fn(std::string &err) {
 // Row-major 2-D tensor of halves [rows, cols]: box = box_rows x box_cols,
 // 128-byte swizzle (box_cols * 2 == 128), zero fill out of bounds on loads,
 // clipping on stores.
-bool encode_half_map(CUtensorMap *map, const void *ptr, int rows, int cols, int box_rows,
-                     int box_cols, std::string &err) {
+// A row-major [rows][cols] matrix of `elem_bytes`-byte elements, boxes of
+// box_rows x box_cols, 128-byte swizzle.
+bool encode_map(CUtensorMap *map, CUtensorMapDataType dtype, int elem_bytes, const void *ptr, int rows,
+                int cols, int box_rows, int box_cols, std::string &err) {
     EncodeTiledFn enc = get_encode_fn(err);
     if (!enc) return false;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * elem_bytes};
     const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
     const cuuint32_t estr[2] = {1, 1};
     // No L2 promotion: the operands are L2-resident after their first use and
     // wider L2 fetches measured slower on this path.
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(ptr), dims,
+    CUresult r = enc(map, dtype, 2, const_cast<void *>(ptr), dims,
                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -1026,6 +1292,11 @@ bool encode_half_map(CUtensorMap *map, const void *ptr, int rows, int cols, int 
         return false;
     }
     return true;
+}
+
+bool encode_half_map(CUtensorMap *map, const void *ptr, int rows, int cols, int box_rows,
+                     int box_cols, std::string &err) {
+    return encode_map(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, ptr, rows, cols, box_rows, box_cols, err);
 }
 
 template <int BN, int STAGES, int ACT>
@@ -1377,6 +1648,88 @@ int launch_pair_epi(const F16Launch &L, std::string &err) {
 }
 
 }  // namespace
+
+int mx_launch(const MxLaunch &L, std::string &err) {
+    using T = MxCfg;
+    auto kernel = gemm_mxfp8_nt_kernel;
+    static int configured[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        err = std::string("cudaGetDevice: ") + cudaGetErrorString(e);
+        return GEMM_ERR_CUDA;
+    }
+    if (dev < 0 || dev >= 64 || !configured[dev]) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, T::kSmemBytes);
+        if (e != cudaSuccess) {
+            err = std::string("cudaFuncSetAttribute(max dynamic smem): ") + cudaGetErrorString(e);
+            return GEMM_ERR_CUDA;
+        }
+        if (dev >= 0 && dev < 64) configured[dev] = 1;
+    }
+    CUtensorMap tmA, tmB, tmC;
+    std::memset(&tmC, 0, sizeof tmC);
+    if (!encode_map(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, L.A, L.M, L.K, kBM, kMxBK, err)) return GEMM_ERR_CUDA;
+    if (!encode_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, L.B, L.N, L.K, kMxBN, kMxBK, err))
+        return GEMM_ERR_CUDA;
+    F16Args args;
+    args.C = static_cast<__half *>(L.C);
+    args.M = L.M;
+    args.N = L.N;
+    args.K = L.K;
+    args.m_tiles = (L.M + kBM - 1) / kBM;
+    args.n_tiles = (L.N + kMxBN - 1) / kMxBN;
+    args.num_kb = (L.K + kMxBK - 1) / kMxBK;
+    args.vec_store = (L.N % 8 == 0) && ((reinterpret_cast<uintptr_t>(L.C) & 15u) == 0);
+    args.tma_store = args.vec_store;
+    args.epi = make_epi(EpiSpec{}, L.N);
+    args.timeout_ns = L.timeout_ns;
+    args.debug_skip_kblock = -1;
+    args.dp_tiles = 0;
+    args.sk_units = 0;
+    args.sk_ws = nullptr;
+    args.sk_flags = nullptr;
+    args.seq = 0;
+    if (args.tma_store && !encode_half_map(&tmC, L.C, L.M, L.N, 32, 64, err)) return GEMM_ERR_CUDA;
+    MxArgs mx{static_cast<const uint8_t *>(L.SFA), static_cast<const uint8_t *>(L.SFB)};
+    const int tiles = args.m_tiles * args.n_tiles;
+    int grid = L.grid > 0 ? L.grid : L.sm_count;
+    if (grid > tiles) grid = tiles;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = T::kSmemBytes;
+    cfg.stream = L.stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, tmC, args, mx);
+    if (e != cudaSuccess) {
+        err = std::string("gemm_mxfp8_nt kernel launch: ") + cudaGetErrorString(e);
+        return GEMM_ERR_CUDA;
+    }
+    return GEMM_OK;
+}
+
+int mx_pack_scales_launch(int rows, int K, const void *plain, void *blocked, cudaStream_t stream,
+                          std::string &err) {
+    const int ksf = K / 32;
+    const int kbt = (K + kMxBK - 1) / kMxBK;
+    const size_t total = static_cast<size_t>((rows + 127) / 128) * kbt * kMxSfChunk;
+    if (total == 0) return GEMM_OK;
+    const size_t want = (total + 255) / 256;
+    const int blocks = static_cast<int>(want < 4096 ? want : 4096);
+    mx_pack_scales_kernel<<<blocks, 256, 0, stream>>>(static_cast<const uint8_t *>(plain),
+                                                      static_cast<uint8_t *>(blocked), rows, ksf, kbt, total);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        err = std::string("scale packing launch: ") + cudaGetErrorString(e);
+        return GEMM_ERR_CUDA;
+    }
+    return GEMM_OK;
+}
 
 int f16_launch(const F16Launch &L, std::string &err) {
     if (L.K == 0) {

@@ -57,6 +57,22 @@ struct F16Launch {
 int f16_launch(const F16Launch &L, std::string &err);
 
 // Read-and-clear the fp16 kernel's device status word (0 = no fault).
+// Block-scaled FP8 (MXFP8) NT product: E4M3 A [M,K], B [N,K], scale chunks
+// SFA, SFB (the layout gemm.h documents), half C [M,N].
+struct MxLaunch {
+    int M, N, K;
+    const void *A, *SFA, *B, *SFB;
+    void *C;
+    cudaStream_t stream;
+    int grid;  // 0: one CTA per SM (at most one per tile)
+    uint64_t timeout_ns;
+    int sm_count;
+};
+int mx_launch(const MxLaunch &L, std::string &err);
+// Plain scales [rows][K/32] -> chunk layout (device pointers, on `stream`).
+int mx_pack_scales_launch(int rows, int K, const void *plain, void *blocked, cudaStream_t stream,
+                          std::string &err);
+
 int f16_status_read_clear(cudaStream_t stream, int *code, std::string &err);
 
 // One fp16 matrix-vector launch (M <= 2), after validation and selection.

@@ -403,4 +403,59 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32acc(int m, int n) {
            (static_cast<uint32_t>(m >> 4) << 24);
 }
 
+// ---------------------------------------------------------------------------
+// Block-scaled FP8 (kind::mxf8f6f4): scale factors, bulk copies, the MMA
+// ---------------------------------------------------------------------------
+
+// Contiguous global -> shared copy of `bytes` (multiple of 16, both addresses
+// 16-byte aligned), completing on the mbarrier's transaction count.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// Shared-memory descriptor of an unswizzled K-major block: rows of 16 bytes,
+// 8-row core matrices `sbo` bytes apart along M/N (`lbo` along K).
+__device__ __forceinline__ uint64_t plain_kmajor_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1) << 46;  // descriptor version of sm_100+; layout 0 = no swizzle
+    return d;
+}
+
+// Shared -> TMEM: 32 rows of 128 bits (16 bytes) into TMEM lanes 0..31,
+// repeated in each of the four 32-lane quarters, 4 columns from `taddr`.
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// D (fp32, TMEM) (+)= (A * 2^SA) (B * 2^SB)^T for FP8 A, B in shared memory
+// and UE8M0 scale factors in TMEM (one per row per 32 K, the byte chosen by
+// the descriptor's scale-factor IDs).
+__device__ __forceinline__ void mma_mxf8_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// Instruction descriptor of the block-scaled kinds: B scale-factor ID in
+// [4,6), A and B formats in [7,10) and [10,13) (E4M3 = 0), K-major (bits 15,
+// 16 = 0), N >> 3 in [17,23), scale format UE8M0 (bit 23 = 1), M >> 4 in
+// [24,29), A scale-factor ID in [29,31); D is fp32.
+__host__ __device__ constexpr uint32_t idesc_mxf8_e4m3(int m, int n, int sf_id) {
+    return (static_cast<uint32_t>(sf_id) << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (1u << 23) |
+           (static_cast<uint32_t>(m >> 4) << 24) | (static_cast<uint32_t>(sf_id) << 29);
+}
+
 }  // namespace gb300

@@ -224,6 +224,40 @@ int gemm_f16_nt_fused(int M, int N, int K, const void *A, const void *B, void *C
                       const gemm_f16_epilogue *epi, gemm_stream_t stream,
                       const gemm_f16_config *cfg);
 
+/* Block-scaled FP8 (MXFP8) product, C = A_s * B_s^T with
+ *     A_s[m][k] = e4m3(A[m][k]) * 2^(SA[m][k/32] - 127),
+ *     B_s[n][k] = e4m3(B[n][k]) * 2^(SB[n][k/32] - 127),
+ * accumulated in fp32 on the tensor cores and rounded once to half ("异步拷贝与
+ * Hopper/Blackwell 新特性", section "Blackwell 概览 sm_100": in MXFP8 every 32
+ * elements share one 8-bit exponent scale).
+ *   A    device, M x K bytes, row-major: FP8 E4M3 codes (1 sign, 4 exponent
+ *        bits with bias 7, 3 mantissa bits; S.1111.111 is NaN);
+ *   B    device, N x K bytes, row-major (the transposed right operand, as in
+ *        gemm_f16_nt);
+ *   SFA, SFB  device, the UE8M0 scale codes (2^(e - 127)) of A and B in the
+ *        chunk layout below, gemm_mxfp8_scale_bytes(M or N, K) bytes each;
+ *   C    device, half M x N, row-major.
+ * Scale chunk layout: for a matrix of `rows` rows, rows are grouped in tiles
+ * of 128 and K in blocks of 128 (4 scales); chunk (t, b) is 512 bytes at
+ * offset (t * ceil(K/128) + b) * 512, and byte 16*(r % 32) + 4*(r / 32) + j of
+ * it holds the scale of row 128t + r for K elements 128b + 32j .. +31.
+ * Entries past the last row or scale must be finite codes (the packer writes
+ * 127).  gemm_mxfp8_pack_scales converts plain [rows][K/32] scales.
+ * K must be a multiple of 32 (GEMM_ERR_UNSUPPORTED otherwise); A, B, SFA and
+ * SFB 16-byte aligned (GEMM_ERR_MISALIGNED).  K = 0 writes C = 0. */
+int gemm_mxfp8_nt(int M, int N, int K, const void *A, const void *SFA, const void *B,
+                  const void *SFB, void *C, gemm_stream_t stream);
+
+/* Bytes of the chunk layout of the scales of a `rows` x K MXFP8 matrix:
+ * ceil(rows/128) * ceil(K/128) * 512.  0 for an empty matrix. */
+size_t gemm_mxfp8_scale_bytes(int rows, int K);
+
+/* Device-side conversion of plain row-major UE8M0 scales [rows][K/32]
+ * (`plain`) into the chunk layout (`blocked`, gemm_mxfp8_scale_bytes(rows,
+ * K) bytes), padding with 127; enqueued on `stream`.  K % 32 != 0 ->
+ * GEMM_ERR_UNSUPPORTED. */
+int gemm_mxfp8_pack_scales(int rows, int K, const void *plain, void *blocked, gemm_stream_t stream);
+
 /* One kernel configuration of the SGEMM path. */
 typedef struct {
     int variant;

@@ -34,7 +34,8 @@ def test_headers_declare_the_boundary():
     names = _declared_functions()
     for n in ["gemm_f16_nt", "sgemm", "gemm_last_error", "gemm_check_device_status",
               "gemm_f16_select", "gemm_sgemm_select", "gemm_f16_nt_ex", "sgemm_ex",
-              "gemm_debug_f16_nt_skip_load", "gemm_f16_nt_fused", "gemm_f16_nt_stream_k_noalloc"]:
+              "gemm_debug_f16_nt_skip_load", "gemm_f16_nt_fused", "gemm_f16_nt_stream_k_noalloc",
+              "gemm_mxfp8_nt", "gemm_mxfp8_scale_bytes", "gemm_mxfp8_pack_scales"]:
         assert n in names
 
 
@@ -104,6 +105,29 @@ def test_fused_epilogue_arguments_are_checked_on_the_host(lib):
     assert e.value.status == g.GEMM_ERR_MISALIGNED
     assert g.gemm_f16_nt_fused(0, 16, 16, 0, 0, 0, activation=g.GEMM_ACT_GELU_TANH) == g.GEMM_OK
     assert g.ACTIVATIONS == {"none": 0, "relu": 1, "silu": 2, "gelu_tanh": 3}
+
+
+def test_mxfp8_arguments_are_checked_on_the_host(lib):
+    assert g.gemm_mxfp8_scale_bytes(0, 64) == 0 and g.gemm_mxfp8_scale_bytes(64, 0) == 0
+    assert g.gemm_mxfp8_scale_bytes(1, 32) == 512
+    assert g.gemm_mxfp8_scale_bytes(129, 160) == 2 * 2 * 512
+    assert g.gemm_mxfp8_scale_bytes(5376, 2048) == 42 * 16 * 512
+    with pytest.raises(g.GemmError) as e:
+        g.gemm_mxfp8_nt(16, 16, 48, 0x1000, 0x1000, 0x1000, 0x1000, 0x1000)
+    assert e.value.status == g.GEMM_ERR_UNSUPPORTED and "K=48" in str(e.value)
+    with pytest.raises(g.GemmError) as e:
+        g.gemm_mxfp8_nt(16, 16, 64, 0x1000, 0x1004, 0x1000, 0x1000, 0x1000)
+    assert e.value.status == g.GEMM_ERR_MISALIGNED
+    with pytest.raises(g.GemmError) as e:
+        g.gemm_mxfp8_nt(16, 16, 64, 0, 0x1000, 0x1000, 0x1000, 0x1000)
+    assert e.value.status == g.GEMM_ERR_INVALID_ARG
+    with pytest.raises(g.GemmError) as e:
+        g.gemm_mxfp8_nt(-1, 16, 64, 0x1000, 0x1000, 0x1000, 0x1000, 0x1000)
+    assert e.value.status == g.GEMM_ERR_INVALID_ARG
+    assert g.gemm_mxfp8_nt(0, 16, 64, 0, 0, 0, 0, 0) == g.GEMM_OK
+    with pytest.raises(g.GemmError) as e:
+        g.gemm_mxfp8_pack_scales(16, 40, 0x1000, 0x1000)
+    assert e.value.status == g.GEMM_ERR_UNSUPPORTED
 
 
 def test_f16_selector(lib):
