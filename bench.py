@@ -27,6 +27,8 @@ ranks is taken and rank 0 prints one JSON line.
 * ``fused_epilogue``: the headline product with bias, residual and
   tanh-GELU fused (``gemm_f16_nt_fused``), beside the plain product and the
   unfused sequence (plain product, then PyTorch element-wise kernels).
+* ``mxfp8``: the block-scaled FP8 product (``gemm_mxfp8_nt``) at the same
+  shape against the fp8 dense peak.
 
 N > 1 runs N independent replicas (one per GPU; the product has no exchange
 step), ``scaling: weak``.  ``--impl reference`` times the float64 oracle on
@@ -520,6 +522,37 @@ def run_ours(args):
                          "frac": fval / peak,
                          "peak_source": f"{peak_kind} bf16 dense burst"}}
 
+    # ---- block-scaled FP8 (MXFP8) at the headline shape against the fp8
+    # dense peak (the measured bf16 peak x the nominal fp8/bf16 ratio of 2)
+    if not args.skip_sgemm:
+        mx_sets = []
+        with torch.cuda.stream(stream):
+            for j in range(ROTATE):
+                xa, xsa = wl.draw_mxfp8(M, K, seed=31 + j)
+                xb, xsb = wl.draw_mxfp8(N, K, seed=41 + j)
+                mx_sets.append((xa.cuda(), g.mxfp8_pack_scales(xsa.cuda(), stream), xb.cuda(),
+                                g.mxfp8_pack_scales(xsb.cuda(), stream),
+                                torch.empty((M, N), dtype=torch.float16, device="cuda")))
+        stream.synchronize()
+
+        def mxs(i):
+            xa, pa, xb, pb, xc = mx_sets[i % ROTATE]
+            g.gemm_mxfp8_nt(M, N, K, xa.data_ptr(), pa.data_ptr(), xb.data_ptr(), pb.data_ptr(),
+                            xc.data_ptr(), sh)
+        with torch.cuda.stream(stream):
+            region_time(mxs, stream, 5)
+            n_mx = 50
+            t_mx = region_time(mxs, stream, n_mx) / n_mx
+        g.gemm_check_device_status(sh)
+        fp8_peak = 2.0 * peak
+        mval = w.flop / (t_mx * 1e-3) / 1e12
+        line["mxfp8"] = {
+            "workload": f"mxfp8_nt_{M}x{N}x{K} (E4M3, UE8M0 scale per 32 of K, half out)",
+            "value": mval, "unit": "TFLOP/s", "us_per_call": 1e3 * t_mx,
+            "roofline": {"bound": "tensor", "achieved": mval, "peak": fp8_peak, "unit": "TFLOP/s",
+                         "frac": mval / fp8_peak,
+                         "peak_source": f"{peak_kind} bf16 dense burst x 2 (nominal fp8/bf16 ratio)"}}
+
     if rank == 0 and not args.skip_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, A, B, budget_s=args.cpu_budget)
     if rank == 0:
@@ -544,7 +577,7 @@ def main():
                     help="seconds of oracle work for the cpu_baseline sample")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--skip-extras", "--skip-sgemm", dest="skip_sgemm", action="store_true",
-                    help="only the headline line: no sgemm, gemv or fused_epilogue objects")
+                    help="only the headline line: no sgemm, gemv, fused_epilogue or mxfp8 objects")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)   # timing rule: at least 3 warm-up steps
     if args.impl == "reference":
