@@ -33,6 +33,9 @@ from ._binding import (  # noqa: F401
     GEMM_F16_AUTO,
     GEMM_F16_FLAG_STREAM_K,
     GEMM_F16_GEMV,
+    GEMM_MXFP8_128x128,
+    GEMM_MXFP8_256x128_PAIR,
+    GEMM_MXFP8_AUTO,
     GEMM_OK,
     GEMM_SGEMM_64x64,
     GEMM_SGEMM_128x128,
@@ -48,6 +51,7 @@ from ._binding import (  # noqa: F401
     gemm_f16_nt_fused,
     gemm_f16_nt_stream_k_noalloc,
     gemm_mxfp8_nt,
+    gemm_mxfp8_nt_ex,
     gemm_mxfp8_pack_scales,
     gemm_mxfp8_scale_bytes,
     gemm_f16_select,

@@ -22,6 +22,7 @@ GEMM_ERR_DEVICE_TIMEOUT = -5
 GEMM_F16_AUTO, GEMM_F16_128x256, GEMM_F16_128x128, GEMM_F16_256x256_PAIR, GEMM_F16_GEMV = 0, 1, 2, 3, 4
 GEMM_SGEMM_AUTO, GEMM_SGEMM_128x128, GEMM_SGEMM_64x64 = 0, 1, 2
 GEMM_F16_FLAG_STREAM_K = 1
+GEMM_MXFP8_AUTO, GEMM_MXFP8_128x128, GEMM_MXFP8_256x128_PAIR = 0, 1, 2
 GEMM_ACT_NONE, GEMM_ACT_RELU, GEMM_ACT_SILU, GEMM_ACT_GELU_TANH = 0, 1, 2, 3
 ACTIVATIONS = {"none": GEMM_ACT_NONE, "relu": GEMM_ACT_RELU, "silu": GEMM_ACT_SILU,
                "gelu_tanh": GEMM_ACT_GELU_TANH}
@@ -49,6 +50,10 @@ class _F16Config(ctypes.Structure):
 class _F16Epilogue(ctypes.Structure):
     _fields_ = [("alpha", ctypes.c_float), ("beta", ctypes.c_float), ("bias", ctypes.c_void_p),
                 ("residual", ctypes.c_void_p), ("activation", ctypes.c_int)]
+
+
+class _MxConfig(ctypes.Structure):
+    _fields_ = [("variant", ctypes.c_int), ("grid", ctypes.c_int)]
 
 
 class _SgemmConfig(ctypes.Structure):
@@ -80,6 +85,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gemm_f16_nt_fused.restype = i
         lib.gemm_mxfp8_nt.argtypes = [i, i, i, vp, vp, vp, vp, vp, vp]
         lib.gemm_mxfp8_nt.restype = i
+        lib.gemm_mxfp8_nt_ex.argtypes = [i, i, i, vp, vp, vp, vp, vp, vp, ctypes.POINTER(_MxConfig)]
+        lib.gemm_mxfp8_nt_ex.restype = i
         lib.gemm_mxfp8_scale_bytes.argtypes = [i, i]
         lib.gemm_mxfp8_scale_bytes.restype = ctypes.c_size_t
         lib.gemm_mxfp8_pack_scales.argtypes = [i, i, vp, vp, vp]
@@ -141,6 +148,12 @@ def gemm_f16_nt_fused(M, N, K, A, B, C, alpha=1.0, beta=0.0, bias=0, residual=0,
 def gemm_mxfp8_nt(M, N, K, A, SFA, B, SFB, C, stream=0) -> int:
     """Block-scaled FP8 product; SFA/SFB in the chunk layout (pointers as ints)."""
     return _check(load_library().gemm_mxfp8_nt(M, N, K, A, SFA, B, SFB, C, stream or None))
+
+
+def gemm_mxfp8_nt_ex(M, N, K, A, SFA, B, SFB, C, stream=0, variant=GEMM_MXFP8_AUTO, grid=0) -> int:
+    cfg = _MxConfig(variant, grid)
+    return _check(load_library().gemm_mxfp8_nt_ex(M, N, K, A, SFA, B, SFB, C, stream or None,
+                                                  ctypes.byref(cfg)))
 
 
 def gemm_mxfp8_scale_bytes(rows: int, K: int) -> int:
@@ -269,7 +282,7 @@ def mxfp8_pack_scales(S, stream=None):
     return out
 
 
-def mxfp8_nt(A, SA, B, SB, C=None, stream=None, packed=False):
+def mxfp8_nt(A, SA, B, SB, C=None, stream=None, packed=False, variant=GEMM_MXFP8_AUTO, grid=0):
     """C (half) = MXFP8 product of E4M3 codes A [M,K], B [N,K] (uint8 CUDA
     tensors) with UE8M0 scales SA [M,K/32], SB [N,K/32] (or, with packed=True,
     already in the chunk layout)."""
@@ -286,8 +299,8 @@ def mxfp8_nt(A, SA, B, SB, C=None, stream=None, packed=False):
         SA, SB = mxfp8_pack_scales(SA, stream), mxfp8_pack_scales(SB, stream)
     if C is None:
         C = torch.empty((M, N), dtype=torch.float16, device=A.device)
-    gemm_mxfp8_nt(M, N, K, A.data_ptr(), SA.data_ptr(), B.data_ptr(), SB.data_ptr(), C.data_ptr(),
-                  _stream_handle(stream))
+    gemm_mxfp8_nt_ex(M, N, K, A.data_ptr(), SA.data_ptr(), B.data_ptr(), SB.data_ptr(), C.data_ptr(),
+                     _stream_handle(stream), variant, grid)
     return C
 
 

@@ -264,6 +264,14 @@ int gemm_mxfp8_pack_scales(int rows, int K, const void *plain, void *blocked, ge
 
 int gemm_mxfp8_nt(int M, int N, int K, const void *A, const void *SFA, const void *B,
                   const void *SFB, void *C, gemm_stream_t stream) {
+    return gemm_mxfp8_nt_ex(M, N, K, A, SFA, B, SFB, C, stream, nullptr);
+}
+
+int gemm_mxfp8_nt_ex(int M, int N, int K, const void *A, const void *SFA, const void *B,
+                     const void *SFB, void *C, gemm_stream_t stream, const gemm_mxfp8_config *cfg) {
+    if (cfg && (cfg->variant < 0 || cfg->variant >= GEMM_MXFP8_NUM_VARIANTS || cfg->grid < 0))
+        return fail(GEMM_ERR_INVALID_ARG, "gemm_mxfp8_nt_ex: bad config variant=%d grid=%d",
+                    cfg->variant, cfg->grid);
     if (M < 0 || N < 0 || K < 0)
         return fail(GEMM_ERR_INVALID_ARG, "gemm_mxfp8_nt: negative size M=%d N=%d K=%d", M, N, K);
     if (M == 0 || N == 0) return GEMM_OK;
@@ -288,9 +296,14 @@ int gemm_mxfp8_nt(int M, int N, int K, const void *A, const void *SFA, const voi
     L.SFB = SFB;
     L.C = C;
     L.stream = reinterpret_cast<cudaStream_t>(stream);
-    L.grid = 0;
+    L.grid = cfg ? cfg->grid : 0;
     L.timeout_ns = kDefaultTimeoutNs;
     L.sm_count = sms;
+    // The 1-CTA 128 x 128 tiles by default: measured at 5376 x 5376 x 2048
+    // and x 8192, the CTA pair (fewer bytes per SM per MMA cycle, but a
+    // cross-CTA hand-off every 256 MMA cycles of a 128-element k-block) was
+    // 11-15 % slower.
+    L.variant = (cfg && cfg->variant != GEMM_MXFP8_AUTO) ? cfg->variant : GEMM_MXFP8_128x128;
     std::string err;
     st = gb300::mx_launch(L, err);
     if (st != GEMM_OK) return fail_str(st, err);

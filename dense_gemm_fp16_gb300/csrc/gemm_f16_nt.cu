@@ -872,6 +872,244 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// CTA-pair form: a 2-CTA cluster computes a 256 x 128 output tile with
+// tcgen05.mma.cta_group::2 (M 256, N 128, K 32).  CTA r loads its 128 rows of
+// A, its 64 rows of B and the two scale chunks its TMEM needs (its own rows
+// of A; all 128 rows of B), all completing on the even CTA's full barrier;
+// per k-block an SM takes 25 KB (against 33 KB for a 1-CTA 128 x 128 tile)
+// for the same MMA time.  The scale chunks go through TMA (a 2D view of the
+// chunk arrays as 256-byte rows) so that the odd CTA's copies can complete on
+// the even CTA's barrier.  Barriers and roles as in the fp16 pair kernel.
+constexpr int kMxPairStages = 7;
+
+struct MxPairCfg {
+    static constexpr int kABytes = kBM * kMxBK;             // this CTA's 128 rows of A
+    static constexpr int kBBytes = (kMxBN / 2) * kMxBK;     // this CTA's 64 rows of B
+    static constexpr int kStageBytes = kABytes + kBBytes + 2 * kMxSfChunk;
+    static constexpr int kTmemCols = 512;  // 2 x 128 accumulator columns, then 8 scale columns per stage
+    static constexpr int kSfCol0 = 2 * kMxBN;
+    static constexpr int kNumBars = 2 * kMxPairStages + 5;
+    static constexpr int kEpiOffset = kMxPairStages * kStageBytes;
+    static constexpr int kBarOffset = kEpiOffset + kEpiBytes;
+    static constexpr int kSmemBytes = 1024 + kBarOffset + kNumBars * 8 + 16;
+    static_assert(kStageBytes % 1024 == 0, "swizzle atoms stay 1024-byte aligned");
+    static_assert(kSfCol0 + 8 * kMxPairStages <= kTmemCols, "scale columns fit the allocation");
+    static_assert(kSmemBytes <= 232448, "fits the 227 KB opt-in limit");
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_mxfp8_nt_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                              const __grid_constant__ CUtensorMap tmC,
+                              const __grid_constant__ CUtensorMap tmSFA,
+                              const __grid_constant__ CUtensorMap tmSFB, const F16Args args) {
+    using T = MxPairCfg;
+    constexpr int BN = kMxBN;
+    constexpr int STAGES = kMxPairStages;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+    const uint32_t sbase = smem_addr(smem);
+
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + T::kBarOffset);
+    const uint32_t bar0 = smem_addr(bars);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto accf_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+    auto acce_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + T::kNumBars);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    __shared__ int never_abort;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int pair = blockIdx.x >> 1;
+    const int num_pairs = gridDim.x >> 1;
+
+    if (threadIdx.x == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmSFA);
+        tma_prefetch_desc(&tmSFB);
+        if (args.tma_store) tma_prefetch_desc(&tmC);
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf_bar(b), 1);
+            mbar_init(acce_bar(b), 2 * 4);  // every epilogue warp of both CTAs
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        never_abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_addr(tmem_slot), T::kTmemCols);
+        tmem_relinquish_alloc_permit_pair();
+    }
+    tc_fence_before_sync();
+    cluster_sync();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+    pdl_launch_dependents();
+    pdl_wait_prerequisites();
+
+    const int total_tiles = args.m_tiles * args.n_tiles;
+    const int num_kb = args.num_kb;
+    uint32_t armed = 0, arm_parity = 0;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer (both CTAs)
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int tile = pair; tile < total_tiles && ok; tile += num_pairs) {
+                const int mt = tile % args.m_tiles;
+                const int nt = tile / args.m_tiles;
+                const int a_tile128 = 2 * mt + static_cast<int>(rank);  // this CTA's 128-row tile of A
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait_cluster(empty_bar(stage), phase ^ 1u, args.timeout_ns, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sa = sbase + stage * T::kStageBytes;
+                    const uint32_t ssf = sa + T::kABytes + T::kBBytes;
+                    const uint32_t full_leader = mapa_shared(full_bar(stage), 0);
+                    if (leader) {
+                        mbar_arrive_expect_tx(full_bar(stage), 2 * T::kStageBytes);
+                        armed |= 1u << stage;
+                        arm_parity ^= 1u << stage;
+                    }
+                    tma_load_2d_pair(sa, &tmA, full_leader, kb * kMxBK, a_tile128 * kBM);
+                    tma_load_2d_pair(sa + T::kABytes, &tmB, full_leader, kb * kMxBK,
+                                     nt * BN + static_cast<int>(rank) * (BN / 2));
+                    // scale chunks: 512 bytes = two 256-byte rows of the 2D view
+                    tma_load_2d_pair(ssf, &tmSFA, full_leader, 0, 2 * (a_tile128 * num_kb + kb));
+                    tma_load_2d_pair(ssf + kMxSfChunk, &tmSFB, full_leader, 0, 2 * (nt * num_kb + kb));
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                if (!*abort_flag) record_timeout(1);
+                *abort_flag = 1;
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ scale copies + MMA issuer (even CTA)
+        if (lane == 0 && leader) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            int i = 0;
+            for (int tile = pair; tile < total_tiles; tile += num_pairs, ++i) {
+                const int b = i & 1;
+                const uint32_t ap = (i >> 1) & 1;
+                if (!mbar_wait_cluster(acce_bar(b), ap ^ 1u, args.timeout_ns, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait_cluster(full_bar(stage), phase, args.timeout_ns, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t sa = sbase + stage * T::kStageBytes;
+                    const uint32_t ssf = sa + T::kABytes + T::kBBytes;
+                    const uint32_t sfa_tmem = tmem_base + static_cast<uint32_t>(T::kSfCol0 + 8 * stage);
+                    const uint32_t sfb_tmem = sfa_tmem + 4u;
+                    tmem_cp_32x128b_warpx4_pair(sfa_tmem, plain_kmajor_desc(ssf, 128, 128));
+                    tmem_cp_32x128b_warpx4_pair(sfb_tmem, plain_kmajor_desc(ssf + kMxSfChunk, 128, 128));
+                    const uint64_t adesc = sw128_kmajor_desc(sa);
+                    const uint64_t bdesc = sw128_kmajor_desc(sa + T::kABytes);
+#pragma unroll
+                    for (int j = 0; j < kMxBK / kMxUmmaK; ++j)
+                        mma_mxf8_ss_pair(d_tmem, adesc + 2u * j, bdesc + 2u * j, idesc_mxf8_e4m3(256, BN, j),
+                                         sfa_tmem, sfb_tmem, (kb > 0 || j > 0) ? 1u : 0u);
+                    mma_commit_pair_multicast(empty_bar(stage), 0x3);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                mma_commit_pair_multicast(accf_bar(b), 0x3);
+            }
+            if (!ok) {
+                if (!*abort_flag) record_timeout(2);
+                *abort_flag = 1;
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue (both CTAs)
+        const int quarter = warp & 3;
+        const uint32_t lane_field = static_cast<uint32_t>(quarter * 32) << 16;
+        const uint32_t stage_smem = sbase + T::kEpiOffset + (warp - 2) * 2 * kEpiBufBytes;
+        uint32_t step = 0;
+        int i = 0;
+        for (int tile = pair; tile < total_tiles; tile += num_pairs, ++i) {
+            const int b = i & 1;
+            const uint32_t ap = (i >> 1) & 1;
+            int ok = 1;
+            if (lane == 0) ok = mbar_wait_cluster(accf_bar(b), ap, args.timeout_ns, abort_flag) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) {
+                if (lane == 0) {
+                    if (!*abort_flag) record_timeout(3);
+                    *abort_flag = 1;
+                }
+                break;
+            }
+            tc_fence_after_sync();
+            const int mt = tile % args.m_tiles;
+            const int nt = tile / args.m_tiles;
+            epilogue_warp_tile<BN, 2, -1>(args, &tmC, tmem_base + lane_field + static_cast<uint32_t>(b * BN),
+                                          mt * 256 + static_cast<int>(rank) * 128 + quarter * 32, nt * BN,
+                                          lane, stage_smem, step);
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(mapa_shared(acce_bar(b), 0));
+        }
+        if (lane == 0) bulk_wait_group_all();
+        __syncwarp();
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (*abort_flag) {
+        if (leader && warp == 0 && lane == 0) {
+            for (int s = 0; s < STAGES; ++s)
+                if (armed & (1u << s))
+                    (void)mbar_wait_cluster(full_bar(s), ((arm_parity >> s) & 1u) ^ 1u, args.timeout_ns,
+                                            &never_abort);
+        }
+        if (leader && warp == 1 && lane == 0) {
+            mma_commit_pair(drain_bar);
+            (void)mbar_wait_cluster(drain_bar, 0, args.timeout_ns, &never_abort);
+        }
+        __syncwarp();
+        tc_fence_before_sync();
+        __syncthreads();
+    }
+    cluster_sync();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc_pair(tmem_base, T::kTmemCols);
+    }
+}
+
 // Plain scales [rows][K/32] -> the kernel's chunk layout, padded with 127
 // (2^0) past the last row and the last scale; one thread per output byte.
 __global__ void mx_pack_scales_kernel(const uint8_t *__restrict__ plain, uint8_t *__restrict__ blocked,
@@ -1271,7 +1509,8 @@ EncodeTiledFn get_encode_fn(std::string &err) {
 // A row-major [rows][cols] matrix of `elem_bytes`-byte elements, boxes of
 // box_rows x box_cols, 128-byte swizzle.
 bool encode_map(CUtensorMap *map, CUtensorMapDataType dtype, int elem_bytes, const void *ptr, int rows,
-                int cols, int box_rows, int box_cols, std::string &err) {
+                int cols, int box_rows, int box_cols, std::string &err,
+                CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
     EncodeTiledFn enc = get_encode_fn(err);
     if (!enc) return false;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
@@ -1282,7 +1521,7 @@ bool encode_map(CUtensorMap *map, CUtensorMapDataType dtype, int elem_bytes, con
     // wider L2 fetches measured slower on this path.
     CUresult r = enc(map, dtype, 2, const_cast<void *>(ptr), dims,
                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                     swizzle, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
         char buf[160];
@@ -1649,7 +1888,99 @@ int launch_pair_epi(const F16Launch &L, std::string &err) {
 
 }  // namespace
 
+namespace {
+
+int mx_launch_pair(const MxLaunch &L, std::string &err) {
+    using T = MxPairCfg;
+    auto kernel = gemm_mxfp8_nt_pair_kernel;
+    static int max_clusters[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        err = std::string("cudaGetDevice: ") + cudaGetErrorString(e);
+        return GEMM_ERR_CUDA;
+    }
+    const bool cached = dev >= 0 && dev < 64 && max_clusters[dev] > 0;
+    if (!cached) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, T::kSmemBytes);
+        if (e != cudaSuccess) {
+            err = std::string("cudaFuncSetAttribute(max dynamic smem): ") + cudaGetErrorString(e);
+            return GEMM_ERR_CUDA;
+        }
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = T::kSmemBytes;
+    cfg.stream = L.stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = cached ? max_clusters[dev] : 0;
+    if (!cached) {
+        cfg.gridDim = dim3(2);
+        e = cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg);
+        if (e != cudaSuccess || clusters <= 0) {
+            err = std::string("cudaOccupancyMaxActiveClusters: ") + cudaGetErrorString(e);
+            return GEMM_ERR_CUDA;
+        }
+        if (dev >= 0 && dev < 64) max_clusters[dev] = clusters;
+    }
+    const int kbt = (L.K + kMxBK - 1) / kMxBK;
+    const int sfa_rows = ((L.M + 127) / 128) * kbt * 2;  // 256-byte rows of the scale chunk arrays
+    const int sfb_rows = ((L.N + 127) / 128) * kbt * 2;
+    CUtensorMap tmA, tmB, tmC, tmSFA, tmSFB;
+    std::memset(&tmC, 0, sizeof tmC);
+    if (!encode_map(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, L.A, L.M, L.K, kBM, kMxBK, err) ||
+        !encode_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, L.B, L.N, L.K, kMxBN / 2, kMxBK, err) ||
+        !encode_map(&tmSFA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, L.SFA, sfa_rows, 256, 2, 256, err,
+                    CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_map(&tmSFB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, L.SFB, sfb_rows, 256, 2, 256, err,
+                    CU_TENSOR_MAP_SWIZZLE_NONE))
+        return GEMM_ERR_CUDA;
+    F16Args args;
+    args.C = static_cast<__half *>(L.C);
+    args.M = L.M;
+    args.N = L.N;
+    args.K = L.K;
+    args.m_tiles = (L.M + 255) / 256;
+    args.n_tiles = (L.N + kMxBN - 1) / kMxBN;
+    args.num_kb = kbt;
+    args.vec_store = (L.N % 8 == 0) && ((reinterpret_cast<uintptr_t>(L.C) & 15u) == 0);
+    args.tma_store = args.vec_store;
+    args.epi = make_epi(EpiSpec{}, L.N);
+    args.timeout_ns = L.timeout_ns;
+    args.debug_skip_kblock = -1;
+    args.dp_tiles = 0;
+    args.sk_units = 0;
+    args.sk_ws = nullptr;
+    args.sk_flags = nullptr;
+    args.seq = 0;
+    if (args.tma_store && !encode_half_map(&tmC, L.C, L.M, L.N, 32, 64, err)) return GEMM_ERR_CUDA;
+    const int tiles = args.m_tiles * args.n_tiles;
+    int pairs = L.grid > 0 ? L.grid / 2 : clusters;
+    if (pairs < 1) pairs = 1;
+    if (pairs > clusters) pairs = clusters;
+    if (pairs > tiles) pairs = tiles;
+    cfg.gridDim = dim3(2 * pairs);
+    cfg.numAttrs = 2;
+    e = cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, tmC, tmSFA, tmSFB, args);
+    if (e != cudaSuccess) {
+        err = std::string("gemm_mxfp8_nt pair kernel launch: ") + cudaGetErrorString(e);
+        return GEMM_ERR_CUDA;
+    }
+    return GEMM_OK;
+}
+
+}  // namespace
+
 int mx_launch(const MxLaunch &L, std::string &err) {
+    if (L.variant == 2) return mx_launch_pair(L, err);
     using T = MxCfg;
     auto kernel = gemm_mxfp8_nt_kernel;
     static int configured[64] = {0};

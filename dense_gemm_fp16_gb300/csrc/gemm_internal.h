@@ -67,6 +67,7 @@ struct MxLaunch {
     int grid;  // 0: one CTA per SM (at most one per tile)
     uint64_t timeout_ns;
     int sm_count;
+    int variant;  // 1: 1-CTA 128 x 128 tiles, 2: CTA pair 256 x 128 tiles
 };
 int mx_launch(const MxLaunch &L, std::string &err);
 // Plain scales [rows][K/32] -> chunk layout (device pointers, on `stream`).

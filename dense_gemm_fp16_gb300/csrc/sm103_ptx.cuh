@@ -449,6 +449,25 @@ __device__ __forceinline__ void mma_mxf8_ss(uint32_t d_tmem, uint64_t a_desc, ui
         : "memory");
 }
 
+// The CTA-pair forms (issued by the even CTA for both): the copy moves the
+// chunk at the same shared-memory offset of each CTA into that CTA's TMEM;
+// the MMA takes A's rows and half of B's from each CTA.
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4_pair(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+__device__ __forceinline__ void mma_mxf8_ss_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                 uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                 uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
 // Instruction descriptor of the block-scaled kinds: B scale-factor ID in
 // [4,6), A and B formats in [7,10) and [10,13) (E4M3 = 0), K-major (bits 15,
 // 16 = 0), N >> 3 in [17,23), scale format UE8M0 (bit 23 = 1), M >> 4 in

@@ -248,6 +248,24 @@ int gemm_f16_nt_fused(int M, int N, int K, const void *A, const void *B, void *C
 int gemm_mxfp8_nt(int M, int N, int K, const void *A, const void *SFA, const void *B,
                   const void *SFB, void *C, gemm_stream_t stream);
 
+/* One kernel configuration of the MXFP8 path. */
+typedef struct {
+    int variant;
+    int grid;  /* CTAs (a multiple of 2 for the pair kernel); 0 = one per SM */
+} gemm_mxfp8_config;
+
+enum {
+    GEMM_MXFP8_AUTO = 0,
+    GEMM_MXFP8_128x128 = 1,       /* 1-CTA 128 x 128 tiles, 5-stage ring (the default)    */
+    GEMM_MXFP8_256x128_PAIR = 2,  /* CTA pair (cta_group::2) 256 x 128 tiles, 7 stages      */
+    GEMM_MXFP8_NUM_VARIANTS = 3
+};
+
+/* gemm_mxfp8_nt with an explicit kernel configuration (NULL or AUTO: the
+ * library's choice). */
+int gemm_mxfp8_nt_ex(int M, int N, int K, const void *A, const void *SFA, const void *B,
+                     const void *SFB, void *C, gemm_stream_t stream, const gemm_mxfp8_config *cfg);
+
 /* Bytes of the chunk layout of the scales of a `rows` x K MXFP8 matrix:
  * ceil(rows/128) * ceil(K/128) * 512.  0 for an empty matrix. */
 size_t gemm_mxfp8_scale_bytes(int rows, int K);

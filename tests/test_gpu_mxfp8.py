@@ -37,14 +37,17 @@ def _e4m3(x):
     return torch.as_tensor(np.asarray(x, dtype=np.float32)).to(torch.float8_e4m3fn).view(torch.uint8)
 
 
-def _run(A, SA, B, SB, pad=64):
+VARIANTS = [g.GEMM_MXFP8_128x128, g.GEMM_MXFP8_256x128_PAIR]
+
+
+def _run(A, SA, B, SB, pad=64, variant=g.GEMM_MXFP8_AUTO, grid=0):
     M, K = A.shape
     N = B.shape[0]
     buf = torch.empty((M * N + 2 * pad,), dtype=torch.int16, device="cuda")
     buf.fill_(SENTINEL)
     buf = buf.view(torch.float16)
     C = buf[pad:pad + M * N].view(M, N)
-    g.mxfp8_nt(A.cuda(), SA.cuda(), B.cuda(), SB.cuda(), C)
+    g.mxfp8_nt(A.cuda(), SA.cuda(), B.cuda(), SB.cuda(), C, variant=variant, grid=grid)
     g.gemm_check_device_status(torch.cuda.current_stream().cuda_stream)
     host = buf.cpu()
     guard = torch.cat([host[:pad], host[pad + M * N:]]).view(torch.int16).numpy().view(np.uint16)
@@ -73,19 +76,21 @@ def test_pack_scales_layout(rows, K):
     assert np.array_equal(packed, _pack_ref(S.numpy(), rows, K))
 
 
+@pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("M,N,K", [(128, 128, 128), (256, 384, 256), (130, 136, 96)])
-def test_unit_scales_small_integers_bit_exact(M, N, K):
+def test_unit_scales_small_integers_bit_exact(M, N, K, variant):
     rng = np.random.default_rng(M + N + K)
     ai = rng.integers(-2, 3, (M, K))
     bi = rng.integers(-2, 3, (N, K))
     A, B = _e4m3(ai), _e4m3(bi)
     SA = torch.full((M, K // 32), 127, dtype=torch.uint8)
     SB = torch.full((N, K // 32), 127, dtype=torch.uint8)
-    C = _run(A, SA, B, SB)
+    C = _run(A, SA, B, SB, variant=variant)
     assert np.array_equal(C.astype(np.float64), (ai @ bi.T).astype(np.float64))
 
 
-def test_row_scales_place_each_rows_scale():
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_row_scales_place_each_rows_scale(variant):
     # Scales constant along K but different for every row of A and of B:
     # integers times powers of two, still exact.
     M, N, K = 256, 256, 256
@@ -96,14 +101,15 @@ def test_row_scales_place_each_rows_scale():
     eb = rng.integers(-3, 4, N)
     SA = torch.from_numpy(np.repeat((127 + ea)[:, None], K // 32, axis=1).astype(np.uint8))
     SB = torch.from_numpy(np.repeat((127 + eb)[:, None], K // 32, axis=1).astype(np.uint8))
-    C = _run(_e4m3(ai), SA, _e4m3(bi), SB)
+    C = _run(_e4m3(ai), SA, _e4m3(bi), SB, variant=variant)
     ref = (ai @ bi.T).astype(np.float64) * np.ldexp(1.0, ea)[:, None] * np.ldexp(1.0, eb)[None, :]
     Cref, S = oracle.gemm_mxfp8_nt(_e4m3(ai), SA, _e4m3(bi), SB)
     assert np.array_equal(Cref, ref)
     check_f16(C, Cref, S, what="row scales")
 
 
-def test_block_scales_pick_their_32_elements():
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_block_scales_pick_their_32_elements(variant):
     # Ones everywhere; scales vary along K only: each 32-element block
     # contributes 32 * 2^(ea_b + eb_b) exactly, and the sum is rounded to half
     # once (a scale taken from the wrong block would move it by far more).
@@ -115,12 +121,13 @@ def test_block_scales_pick_their_32_elements():
     B = _e4m3(np.ones((N, K)))
     SA = torch.from_numpy(np.tile((127 + ea).astype(np.uint8), (M, 1)))
     SB = torch.from_numpy(np.tile((127 + eb).astype(np.uint8), (N, 1)))
-    C = _run(A, SA, B, SB)
+    C = _run(A, SA, B, SB, variant=variant)
     exact = float(np.sum(32 * np.ldexp(1.0, ea + eb)))
     want = float(np.float16(exact))  # round to nearest even
     assert np.all(C.astype(np.float64) == want), (C[0, :4], exact)
 
 
+@pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("M,N,K", [
     (128, 128, 128),
     (256, 512, 1024),     # several tiles, 8 k-blocks
@@ -128,26 +135,39 @@ def test_block_scales_pick_their_32_elements():
     (1000, 24, 2080),     # thin N, long K
     (7, 1000, 96),        # thin M, K below one k-block
 ])
-def test_random_full_compare(M, N, K):
+def test_random_full_compare(M, N, K, variant):
     A, SA = wl.draw_mxfp8(M, K, seed=M + 3)
     B, SB = wl.draw_mxfp8(N, K, seed=N + 4)
-    C = _run(A, SA, B, SB)
+    C = _run(A, SA, B, SB, variant=variant)
     Cref, S = oracle.gemm_mxfp8_nt(A, SA, B, SB)
-    check_f16(C, Cref, S, what=f"mxfp8 {M}x{N}x{K}")
+    check_f16(C, Cref, S, what=f"mxfp8 {M}x{N}x{K} v{variant}")
 
 
-def test_scalar_store_path_and_k0():
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_scalar_store_path_and_k0(variant):
     # N % 8 != 0 takes the element-wise epilogue; K = 0 writes zeros.
     M, N, K = 200, 250, 256
     A, SA = wl.draw_mxfp8(M, K, seed=21)
     B, SB = wl.draw_mxfp8(N, K, seed=22)
-    C = _run(A, SA, B, SB)
+    C = _run(A, SA, B, SB, variant=variant)
     Cref, S = oracle.gemm_mxfp8_nt(A, SA, B, SB)
     check_f16(C, Cref, S, what="scalar stores")
     Cz = torch.full((33, 17), 3.0, dtype=torch.float16, device="cuda")
     g.gemm_mxfp8_nt(33, 17, 0, 0, 0, 0, 0, Cz.data_ptr(), 0)
     torch.cuda.synchronize()
     assert (Cz == 0).all()
+
+
+@pytest.mark.parametrize("variant,grid", [(g.GEMM_MXFP8_AUTO, 0), (g.GEMM_MXFP8_128x128, 0),
+                                          (g.GEMM_MXFP8_256x128_PAIR, 6)])
+def test_persistent_many_tiles_per_cta(variant, grid):
+    # every CTA (pair) walks several tiles: accumulator buffers and stages cycle
+    M, N, K = 768, 640, 512
+    A, SA = wl.draw_mxfp8(M, K, seed=41)
+    B, SB = wl.draw_mxfp8(N, K, seed=42)
+    C = _run(A, SA, B, SB, variant=variant, grid=grid if grid else 3)
+    Cref, S = oracle.gemm_mxfp8_nt(A, SA, B, SB)
+    check_f16(C, Cref, S, what=f"persistent v{variant}")
 
 
 def test_full_size_sampled():
