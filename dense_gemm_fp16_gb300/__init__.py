@@ -34,7 +34,9 @@ from ._binding import (  # noqa: F401
     GEMM_F16_FLAG_STREAM_K,
     GEMM_F16_GEMV,
     GEMM_MXFP8_128x128,
+    GEMM_MXFP8_128x256,
     GEMM_MXFP8_256x128_PAIR,
+    GEMM_MXFP8_256x256_PAIR,
     GEMM_MXFP8_AUTO,
     GEMM_OK,
     GEMM_SGEMM_64x64,

@@ -299,11 +299,13 @@ int gemm_mxfp8_nt_ex(int M, int N, int K, const void *A, const void *SFA, const 
     L.grid = cfg ? cfg->grid : 0;
     L.timeout_ns = kDefaultTimeoutNs;
     L.sm_count = sms;
-    // The 1-CTA 128 x 128 tiles by default: measured at 5376 x 5376 x 2048
-    // and x 8192, the CTA pair (fewer bytes per SM per MMA cycle, but a
-    // cross-CTA hand-off every 256 MMA cycles of a 128-element k-block) was
-    // 11-15 % slower.
-    L.variant = (cfg && cfg->variant != GEMM_MXFP8_AUTO) ? cfg->variant : GEMM_MXFP8_128x128;
+    // Measured on GB300 at 5376 x 5376 x 2048 / x 8192 (us): 1-CTA 128 x 256
+    // with N = 256 MMAs 52 / 157, 1-CTA 128 x 128 62 / 215, CTA pair 256 x 256
+    // 56 / 175, CTA pair 256 x 128 68 / 248.  The wide MMA pays more than the
+    // second accumulator it costs (two 256-column accumulators and the scale
+    // columns do not fit TMEM together); narrow N keeps the 128 x 128 tiles.
+    L.variant = (cfg && cfg->variant != GEMM_MXFP8_AUTO) ? cfg->variant
+                : (N > 128 ? GEMM_MXFP8_128x256 : GEMM_MXFP8_128x128);
     std::string err;
     st = gb300::mx_launch(L, err);
     if (st != GEMM_OK) return fail_str(st, err);

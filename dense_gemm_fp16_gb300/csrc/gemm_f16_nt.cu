@@ -647,18 +647,26 @@ constexpr int kMxStages = 5;
 constexpr int kMxUmmaK = 32;     // K per MMA instruction
 constexpr int kMxSfChunk = 512;  // 128 rows x 4 scales
 
+// BN output columns per tile (128 or 256: B's scales are BN/128 chunks),
+// STAGES ring stages, EBUFS epilogue staging buffers per warp, ACC TMEM
+// accumulators (2: the epilogue of a tile overlaps the next tile's MMAs).
+template <int BN, int STAGES, int EBUFS, int ACC>
 struct MxCfg {
     static constexpr int kABytes = kBM * kMxBK;
-    static constexpr int kBBytes = kMxBN * kMxBK;
-    static constexpr int kStageBytes = kABytes + kBBytes + 2 * kMxSfChunk;
-    static constexpr int kTmemCols = 512;  // 2 x 128 accumulator columns, then 8 scale columns per stage
-    static constexpr int kSfCol0 = 2 * kMxBN;
-    static constexpr int kNumBars = 2 * kMxStages + 5;
-    static constexpr int kEpiOffset = kMxStages * kStageBytes;
-    static constexpr int kBarOffset = kEpiOffset + kEpiBytes;
+    static constexpr int kBBytes = BN * kMxBK;
+    static constexpr int kSfbChunks = BN / 128;
+    static constexpr int kSfBytes = (1 + kSfbChunks) * kMxSfChunk;
+    static constexpr int kStageBytes = (kABytes + kBBytes + kSfBytes + 1023) / 1024 * 1024;
+    static constexpr int kTmemCols = 512;  // accumulators, then the scale columns of each stage
+    static constexpr int kSfCols = 4 * (1 + kSfbChunks);
+    static constexpr int kSfCol0 = ACC * BN;
+    static constexpr int kNumBars = 2 * STAGES + 5;
+    static constexpr int kEpiOffset = STAGES * kStageBytes;
+    static constexpr int kBarOffset = kEpiOffset + 4 * EBUFS * kEpiBufBytes;
     static constexpr int kSmemBytes = 1024 + kBarOffset + kNumBars * 8 + 16;
-    static_assert(kStageBytes % 1024 == 0, "swizzle atoms stay 1024-byte aligned");
-    static_assert(kSfCol0 + 8 * kMxStages <= kTmemCols, "scale columns fit the allocation");
+    static_assert(BN == 128 || BN == 256, "B's scales come in whole 128-row chunks");
+    static_assert(ACC == 1 || ACC == 2, "one or two accumulators");
+    static_assert(kSfCol0 + kSfCols * STAGES <= kTmemCols, "scale columns fit the allocation");
     static_assert(kSmemBytes <= 232448, "fits the 227 KB opt-in limit");
 };
 
@@ -667,12 +675,11 @@ struct MxArgs {
     const uint8_t *sfb;  // scale chunks of B: [ceil(N/128)][ceil(K/128)][512]
 };
 
+template <int BN, int STAGES, int EBUFS, int ACC>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_mxfp8_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                          const __grid_constant__ CUtensorMap tmC, const F16Args args, const MxArgs mx) {
-    using T = MxCfg;
-    constexpr int BN = kMxBN;
-    constexpr int STAGES = kMxStages;
+    using T = MxCfg<BN, STAGES, EBUFS, ACC>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -741,13 +748,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t sa = sbase + stage * T::kStageBytes;
                     const uint32_t sb = sa + T::kABytes;
                     const uint32_t ssf = sb + T::kBBytes;
-                    mbar_arrive_expect_tx(full_bar(stage), T::kStageBytes);
+                    mbar_arrive_expect_tx(full_bar(stage), T::kABytes + T::kBBytes + T::kSfBytes);
                     tma_load_2d(sa, &tmA, full_bar(stage), kb * kMxBK, mt * kBM);
                     tma_load_2d(sb, &tmB, full_bar(stage), kb * kMxBK, nt * BN);
                     bulk_load(ssf, mx.sfa + (static_cast<size_t>(mt) * num_kb + kb) * kMxSfChunk,
                               kMxSfChunk, full_bar(stage));
-                    bulk_load(ssf + kMxSfChunk, mx.sfb + (static_cast<size_t>(nt) * num_kb + kb) * kMxSfChunk,
-                              kMxSfChunk, full_bar(stage));
+#pragma unroll
+                    for (int c = 0; c < T::kSfbChunks; ++c)
+                        bulk_load(ssf + (1 + c) * kMxSfChunk,
+                                  mx.sfb + (static_cast<size_t>(nt * T::kSfbChunks + c) * num_kb + kb) * kMxSfChunk,
+                                  kMxSfChunk, full_bar(stage));
                     armed |= 1u << stage;
                     arm_parity ^= 1u << stage;
                     if (++stage == STAGES) {
@@ -770,8 +780,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             int i = 0;
             for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++i) {
-                const int b = i & 1;
-                const uint32_t ap = (i >> 1) & 1;
+                const int b = i % ACC;
+                const uint32_t ap = (i / ACC) & 1;
                 if (!mbar_wait(acce_bar(b), ap ^ 1u, args.timeout_ns, abort_flag)) {
                     ok = false;
                     break;
@@ -787,11 +797,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t sa = sbase + stage * T::kStageBytes;
                     const uint32_t sb = sa + T::kABytes;
                     const uint32_t ssf = sb + T::kBBytes;
-                    const uint32_t sfa_tmem = tmem_base + static_cast<uint32_t>(T::kSfCol0 + 8 * stage);
+                    const uint32_t sfa_tmem = tmem_base + static_cast<uint32_t>(T::kSfCol0 + T::kSfCols * stage);
                     const uint32_t sfb_tmem = sfa_tmem + 4u;
-                    // each chunk: 32 rows of 16 bytes, 8-row core matrices 128 bytes apart
+                    // each chunk: 32 rows of 16 bytes, 8-row core matrices 128 bytes apart;
+                    // B's chunk c (rows 128c..) lands 4c columns on
                     tmem_cp_32x128b_warpx4(sfa_tmem, plain_kmajor_desc(ssf, 128, 128));
-                    tmem_cp_32x128b_warpx4(sfb_tmem, plain_kmajor_desc(ssf + kMxSfChunk, 128, 128));
+#pragma unroll
+                    for (int c = 0; c < T::kSfbChunks; ++c)
+                        tmem_cp_32x128b_warpx4(sfb_tmem + 4u * c,
+                                               plain_kmajor_desc(ssf + (1 + c) * kMxSfChunk, 128, 128));
                     const uint64_t adesc = sw128_kmajor_desc(sa);
                     const uint64_t bdesc = sw128_kmajor_desc(sb);
 #pragma unroll
@@ -820,12 +834,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ epilogue
         const int quarter = warp & 3;
         const uint32_t lane_field = static_cast<uint32_t>(quarter * 32) << 16;
-        const uint32_t stage_smem = sbase + T::kEpiOffset + (warp - 2) * 2 * kEpiBufBytes;
+        const uint32_t stage_smem = sbase + T::kEpiOffset + (warp - 2) * EBUFS * kEpiBufBytes;
         uint32_t step = 0;
         int i = 0;
         for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++i) {
-            const int b = i & 1;
-            const uint32_t ap = (i >> 1) & 1;
+            const int b = i % ACC;
+            const uint32_t ap = (i / ACC) & 1;
             int ok = 1;
             if (lane == 0) ok = mbar_wait(accf_bar(b), ap, args.timeout_ns, abort_flag) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -839,8 +853,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after_sync();
             const int mt = tile % args.m_tiles;
             const int nt = tile / args.m_tiles;
-            epilogue_warp_tile<BN, 2, -1>(args, &tmC, tmem_base + lane_field + static_cast<uint32_t>(b * BN),
-                                          mt * kBM + quarter * 32, nt * BN, lane, stage_smem, step);
+            epilogue_warp_tile<BN, EBUFS, -1>(args, &tmC, tmem_base + lane_field + static_cast<uint32_t>(b * BN),
+                                              mt * kBM + quarter * 32, nt * BN, lane, stage_smem, step);
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(acce_bar(b));
@@ -880,31 +894,35 @@ __global__ void __launch_bounds__(kThreads, 1)
 // for the same MMA time.  The scale chunks go through TMA (a 2D view of the
 // chunk arrays as 256-byte rows) so that the odd CTA's copies can complete on
 // the even CTA's barrier.  Barriers and roles as in the fp16 pair kernel.
-constexpr int kMxPairStages = 7;
-
+// BN: pair tile columns (128 or 256; each CTA loads BN/2 rows of B and all
+// BN/128 scale chunks of B), STAGES, EBUFS epilogue buffers per warp, ACC
+// accumulators.
+template <int BN, int STAGES, int EBUFS, int ACC>
 struct MxPairCfg {
     static constexpr int kABytes = kBM * kMxBK;             // this CTA's 128 rows of A
-    static constexpr int kBBytes = (kMxBN / 2) * kMxBK;     // this CTA's 64 rows of B
-    static constexpr int kStageBytes = kABytes + kBBytes + 2 * kMxSfChunk;
-    static constexpr int kTmemCols = 512;  // 2 x 128 accumulator columns, then 8 scale columns per stage
-    static constexpr int kSfCol0 = 2 * kMxBN;
-    static constexpr int kNumBars = 2 * kMxPairStages + 5;
-    static constexpr int kEpiOffset = kMxPairStages * kStageBytes;
-    static constexpr int kBarOffset = kEpiOffset + kEpiBytes;
+    static constexpr int kBBytes = (BN / 2) * kMxBK;        // this CTA's half of B
+    static constexpr int kSfbChunks = BN / 128;
+    static constexpr int kSfBytes = (1 + kSfbChunks) * kMxSfChunk;
+    static constexpr int kStageBytes = (kABytes + kBBytes + kSfBytes + 1023) / 1024 * 1024;
+    static constexpr int kTmemCols = 512;  // accumulators, then the scale columns of each stage
+    static constexpr int kSfCols = 4 * (1 + kSfbChunks);
+    static constexpr int kSfCol0 = ACC * BN;
+    static constexpr int kNumBars = 2 * STAGES + 5;
+    static constexpr int kEpiOffset = STAGES * kStageBytes;
+    static constexpr int kBarOffset = kEpiOffset + 4 * EBUFS * kEpiBufBytes;
     static constexpr int kSmemBytes = 1024 + kBarOffset + kNumBars * 8 + 16;
-    static_assert(kStageBytes % 1024 == 0, "swizzle atoms stay 1024-byte aligned");
-    static_assert(kSfCol0 + 8 * kMxPairStages <= kTmemCols, "scale columns fit the allocation");
+    static_assert(BN == 128 || BN == 256, "B's scales come in whole 128-row chunks");
+    static_assert(kSfCol0 + kSfCols * STAGES <= kTmemCols, "scale columns fit the allocation");
     static_assert(kSmemBytes <= 232448, "fits the 227 KB opt-in limit");
 };
 
+template <int BN, int STAGES, int EBUFS, int ACC>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_mxfp8_nt_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                               const __grid_constant__ CUtensorMap tmC,
                               const __grid_constant__ CUtensorMap tmSFA,
                               const __grid_constant__ CUtensorMap tmSFB, const F16Args args) {
-    using T = MxPairCfg;
-    constexpr int BN = kMxBN;
-    constexpr int STAGES = kMxPairStages;
+    using T = MxPairCfg<BN, STAGES, EBUFS, ACC>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -981,7 +999,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t ssf = sa + T::kABytes + T::kBBytes;
                     const uint32_t full_leader = mapa_shared(full_bar(stage), 0);
                     if (leader) {
-                        mbar_arrive_expect_tx(full_bar(stage), 2 * T::kStageBytes);
+                        // both CTAs' operand and scale bytes (the stage's padding is not loaded)
+                        mbar_arrive_expect_tx(full_bar(stage), 2 * (T::kABytes + T::kBBytes + T::kSfBytes));
                         armed |= 1u << stage;
                         arm_parity ^= 1u << stage;
                     }
@@ -990,7 +1009,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      nt * BN + static_cast<int>(rank) * (BN / 2));
                     // scale chunks: 512 bytes = two 256-byte rows of the 2D view
                     tma_load_2d_pair(ssf, &tmSFA, full_leader, 0, 2 * (a_tile128 * num_kb + kb));
-                    tma_load_2d_pair(ssf + kMxSfChunk, &tmSFB, full_leader, 0, 2 * (nt * num_kb + kb));
+#pragma unroll
+                    for (int c = 0; c < T::kSfbChunks; ++c)
+                        tma_load_2d_pair(ssf + (1 + c) * kMxSfChunk, &tmSFB, full_leader, 0,
+                                         2 * ((nt * T::kSfbChunks + c) * num_kb + kb));
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -1011,8 +1033,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             int i = 0;
             for (int tile = pair; tile < total_tiles; tile += num_pairs, ++i) {
-                const int b = i & 1;
-                const uint32_t ap = (i >> 1) & 1;
+                const int b = i % ACC;
+                const uint32_t ap = (i / ACC) & 1;
                 if (!mbar_wait_cluster(acce_bar(b), ap ^ 1u, args.timeout_ns, abort_flag)) {
                     ok = false;
                     break;
@@ -1027,10 +1049,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after_sync();
                     const uint32_t sa = sbase + stage * T::kStageBytes;
                     const uint32_t ssf = sa + T::kABytes + T::kBBytes;
-                    const uint32_t sfa_tmem = tmem_base + static_cast<uint32_t>(T::kSfCol0 + 8 * stage);
+                    const uint32_t sfa_tmem = tmem_base + static_cast<uint32_t>(T::kSfCol0 + T::kSfCols * stage);
                     const uint32_t sfb_tmem = sfa_tmem + 4u;
                     tmem_cp_32x128b_warpx4_pair(sfa_tmem, plain_kmajor_desc(ssf, 128, 128));
-                    tmem_cp_32x128b_warpx4_pair(sfb_tmem, plain_kmajor_desc(ssf + kMxSfChunk, 128, 128));
+#pragma unroll
+                    for (int c = 0; c < T::kSfbChunks; ++c)
+                        tmem_cp_32x128b_warpx4_pair(sfb_tmem + 4u * c,
+                                                    plain_kmajor_desc(ssf + (1 + c) * kMxSfChunk, 128, 128));
                     const uint64_t adesc = sw128_kmajor_desc(sa);
                     const uint64_t bdesc = sw128_kmajor_desc(sa + T::kABytes);
 #pragma unroll
@@ -1056,12 +1081,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ epilogue (both CTAs)
         const int quarter = warp & 3;
         const uint32_t lane_field = static_cast<uint32_t>(quarter * 32) << 16;
-        const uint32_t stage_smem = sbase + T::kEpiOffset + (warp - 2) * 2 * kEpiBufBytes;
+        const uint32_t stage_smem = sbase + T::kEpiOffset + (warp - 2) * EBUFS * kEpiBufBytes;
         uint32_t step = 0;
         int i = 0;
         for (int tile = pair; tile < total_tiles; tile += num_pairs, ++i) {
-            const int b = i & 1;
-            const uint32_t ap = (i >> 1) & 1;
+            const int b = i % ACC;
+            const uint32_t ap = (i / ACC) & 1;
             int ok = 1;
             if (lane == 0) ok = mbar_wait_cluster(accf_bar(b), ap, args.timeout_ns, abort_flag) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -1075,7 +1100,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after_sync();
             const int mt = tile % args.m_tiles;
             const int nt = tile / args.m_tiles;
-            epilogue_warp_tile<BN, 2, -1>(args, &tmC, tmem_base + lane_field + static_cast<uint32_t>(b * BN),
+            epilogue_warp_tile<BN, EBUFS, -1>(args, &tmC, tmem_base + lane_field + static_cast<uint32_t>(b * BN),
                                           mt * 256 + static_cast<int>(rank) * 128 + quarter * 32, nt * BN,
                                           lane, stage_smem, step);
             tc_fence_before_sync();
@@ -1890,9 +1915,10 @@ int launch_pair_epi(const F16Launch &L, std::string &err) {
 
 namespace {
 
+template <int BN, int STAGES, int EBUFS, int ACC>
 int mx_launch_pair(const MxLaunch &L, std::string &err) {
-    using T = MxPairCfg;
-    auto kernel = gemm_mxfp8_nt_pair_kernel;
+    using T = MxPairCfg<BN, STAGES, EBUFS, ACC>;
+    auto kernel = gemm_mxfp8_nt_pair_kernel<BN, STAGES, EBUFS, ACC>;
     static int max_clusters[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -1937,7 +1963,7 @@ int mx_launch_pair(const MxLaunch &L, std::string &err) {
     CUtensorMap tmA, tmB, tmC, tmSFA, tmSFB;
     std::memset(&tmC, 0, sizeof tmC);
     if (!encode_map(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, L.A, L.M, L.K, kBM, kMxBK, err) ||
-        !encode_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, L.B, L.N, L.K, kMxBN / 2, kMxBK, err) ||
+        !encode_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, L.B, L.N, L.K, BN / 2, kMxBK, err) ||
         !encode_map(&tmSFA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, L.SFA, sfa_rows, 256, 2, 256, err,
                     CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !encode_map(&tmSFB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, L.SFB, sfb_rows, 256, 2, 256, err,
@@ -1949,7 +1975,7 @@ int mx_launch_pair(const MxLaunch &L, std::string &err) {
     args.N = L.N;
     args.K = L.K;
     args.m_tiles = (L.M + 255) / 256;
-    args.n_tiles = (L.N + kMxBN - 1) / kMxBN;
+    args.n_tiles = (L.N + BN - 1) / BN;
     args.num_kb = kbt;
     args.vec_store = (L.N % 8 == 0) && ((reinterpret_cast<uintptr_t>(L.C) & 15u) == 0);
     args.tma_store = args.vec_store;
@@ -1977,12 +2003,10 @@ int mx_launch_pair(const MxLaunch &L, std::string &err) {
     return GEMM_OK;
 }
 
-}  // namespace
-
-int mx_launch(const MxLaunch &L, std::string &err) {
-    if (L.variant == 2) return mx_launch_pair(L, err);
-    using T = MxCfg;
-    auto kernel = gemm_mxfp8_nt_kernel;
+template <int BN, int STAGES, int EBUFS, int ACC>
+int mx_launch_1cta(const MxLaunch &L, std::string &err) {
+    using T = MxCfg<BN, STAGES, EBUFS, ACC>;
+    auto kernel = gemm_mxfp8_nt_kernel<BN, STAGES, EBUFS, ACC>;
     static int configured[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -2001,7 +2025,7 @@ int mx_launch(const MxLaunch &L, std::string &err) {
     CUtensorMap tmA, tmB, tmC;
     std::memset(&tmC, 0, sizeof tmC);
     if (!encode_map(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, L.A, L.M, L.K, kBM, kMxBK, err)) return GEMM_ERR_CUDA;
-    if (!encode_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, L.B, L.N, L.K, kMxBN, kMxBK, err))
+    if (!encode_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, L.B, L.N, L.K, BN, kMxBK, err))
         return GEMM_ERR_CUDA;
     F16Args args;
     args.C = static_cast<__half *>(L.C);
@@ -2009,7 +2033,7 @@ int mx_launch(const MxLaunch &L, std::string &err) {
     args.N = L.N;
     args.K = L.K;
     args.m_tiles = (L.M + kBM - 1) / kBM;
-    args.n_tiles = (L.N + kMxBN - 1) / kMxBN;
+    args.n_tiles = (L.N + BN - 1) / BN;
     args.num_kb = (L.K + kMxBK - 1) / kMxBK;
     args.vec_store = (L.N % 8 == 0) && ((reinterpret_cast<uintptr_t>(L.C) & 15u) == 0);
     args.tma_store = args.vec_store;
@@ -2042,6 +2066,17 @@ int mx_launch(const MxLaunch &L, std::string &err) {
         return GEMM_ERR_CUDA;
     }
     return GEMM_OK;
+}
+
+}  // namespace
+
+int mx_launch(const MxLaunch &L, std::string &err) {
+    switch (L.variant) {
+        case 2: return mx_launch_pair<128, 7, 2, 2>(L, err);
+        case 3: return mx_launch_1cta<256, 4, 1, 1>(L, err);
+        case 4: return mx_launch_pair<256, 6, 1, 1>(L, err);
+        default: return mx_launch_1cta<128, kMxStages, 2, 2>(L, err);
+    }
 }
 
 int mx_pack_scales_launch(int rows, int K, const void *plain, void *blocked, cudaStream_t stream,

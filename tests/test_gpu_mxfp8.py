@@ -37,7 +37,8 @@ def _e4m3(x):
     return torch.as_tensor(np.asarray(x, dtype=np.float32)).to(torch.float8_e4m3fn).view(torch.uint8)
 
 
-VARIANTS = [g.GEMM_MXFP8_128x128, g.GEMM_MXFP8_256x128_PAIR]
+VARIANTS = [g.GEMM_MXFP8_128x128, g.GEMM_MXFP8_256x128_PAIR, g.GEMM_MXFP8_128x256,
+            g.GEMM_MXFP8_256x256_PAIR]
 
 
 def _run(A, SA, B, SB, pad=64, variant=g.GEMM_MXFP8_AUTO, grid=0):
