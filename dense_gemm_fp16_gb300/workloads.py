@@ -109,6 +109,20 @@ def draw_mxfp8(rows: int, K: int, seed: int, scale_lo: int = 125, scale_hi: int 
     return codes.contiguous(), scales.to(torch.uint8).contiguous()
 
 
+def draw_nvfp4(rows: int, K: int, seed: int):
+    """Block-scaled FP4 operands as stored: E2M1 elements packed two per byte
+    [rows, K/2] (uint8, uniform random bits: every code equally likely) and
+    UE4M3 block scales [rows, K/16] (uint8): values uniform in [0.25, 4]
+    cast to E4M3 by PyTorch."""
+    if K % 32:
+        raise ValueError("K must be a multiple of 32")
+    g = _gen(seed)
+    packed = torch.randint(0, 256, (rows, K // 2), generator=g, dtype=torch.int64).to(torch.uint8)
+    sv = torch.rand((rows, K // 16), generator=g, dtype=torch.float32) * 3.75 + 0.25
+    scales = sv.to(torch.float8_e4m3fn).view(torch.uint8)
+    return packed.contiguous(), scales.contiguous()
+
+
 def make_inputs(w: Workload):
     """Host tensors (A, B, C0) of a workload; C0 is None when beta == 0."""
     if w.form == "f16_nt":

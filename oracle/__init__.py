@@ -20,6 +20,9 @@ each function follows:
 * ``gemm_mxfp8_nt``: "异步拷贝与 Hopper/Blackwell 新特性", section
   "Blackwell 概览 sm_100" (MXFP8: 32 elements share one 8-bit exponent
   scale), E4M3 elements and UE8M0 scales.
+* ``gemm_nvfp4_nt``: the same section (NVFP4: 16 elements share one FP8
+  scale, plus a tensor-level FP32 scale), E2M1 elements packed two per
+  byte, UE4M3 block scales, alpha the tensor-level scale.
 
 Every function returns the unrounded float64 result C and the tolerance
 scale S = |alpha|·Σ_k |A·B| per element.
@@ -91,6 +94,13 @@ def _load():
             lib.oracle_gemm_mxfp8_nt_sampled.restype = ctypes.c_int
             lib.oracle_gemm_mxfp8_nt_sampled.argtypes = [i64, i64, i64, vp, vp, vp, vp, i64, vp, vp,
                                                          vp, vp]
+            lib.oracle_e2m1_to_f64.restype = dbl
+            lib.oracle_e2m1_to_f64.argtypes = [u8]
+            lib.oracle_gemm_nvfp4_nt.restype = ctypes.c_int
+            lib.oracle_gemm_nvfp4_nt.argtypes = [i64, i64, i64, vp, vp, vp, vp, dbl, vp, vp]
+            lib.oracle_gemm_nvfp4_nt_sampled.restype = ctypes.c_int
+            lib.oracle_gemm_nvfp4_nt_sampled.argtypes = [i64, i64, i64, vp, vp, vp, vp, dbl, i64, vp,
+                                                         vp, vp, vp]
             lib.oracle_sgemm_sampled.restype = ctypes.c_int
             lib.oracle_sgemm_sampled.argtypes = [i64, i64, i64, dbl, vp, vp, dbl, vp, i64, vp, vp,
                                                  vp, vp]
@@ -356,4 +366,54 @@ def gemm_mxfp8_nt_sampled(A, SA, B, SB, rows, cols):
                                               _ptr(r), _ptr(c), _ptr(C), _ptr(S))
     if rc != 0:
         raise RuntimeError(f"oracle_gemm_mxfp8_nt_sampled failed ({rc})")
+    return C, S
+
+
+def e2m1_to_f64(nibbles) -> np.ndarray:
+    """FP4 E2M1 codes (one per uint8, low 4 bits) decoded to float64."""
+    c = _as_u8(nibbles)
+    f = _load().oracle_e2m1_to_f64
+    return np.array([f(int(v) & 0xF) for v in c.ravel()], dtype=np.float64).reshape(c.shape)
+
+
+def _nv_args(A, SA, B, SB):
+    a, sa, b, sb = _as_u8(A), _as_u8(SA), _as_u8(B), _as_u8(SB)
+    if a.ndim != 2 or b.ndim != 2 or a.shape[1] != b.shape[1]:
+        raise ValueError(f"shape mismatch {a.shape} x {b.shape}^T")
+    M, K = a.shape[0], 2 * a.shape[1]
+    N = b.shape[0]
+    if K % 16:
+        raise ValueError("K must be a multiple of the 16-element scale block")
+    if sa.shape != (M, K // 16) or sb.shape != (N, K // 16):
+        raise ValueError(f"scales must be [M, K/16] and [N, K/16], got {sa.shape} and {sb.shape}")
+    return a, sa, b, sb, M, N, K
+
+
+def gemm_nvfp4_nt(A, SA, B, SB, alpha=1.0):
+    """alpha * sum_k e2m1(A[m,k]) e4m3(SA[m,k/16]) e2m1(B[n,k]) e4m3(SB[n,k/16])
+    in float64; A [M,K/2], B [N,K/2] packed (element 2i in the low nibble of
+    byte i), SA [M,K/16], SB [N,K/16].  Returns (C, S)."""
+    a, sa, b, sb, M, N, K = _nv_args(A, SA, B, SB)
+    C = np.zeros((M, N), dtype=np.float64)
+    S = np.zeros((M, N), dtype=np.float64)
+    rc = _load().oracle_gemm_nvfp4_nt(M, N, K, _ptr(a), _ptr(sa), _ptr(b), _ptr(sb), float(alpha),
+                                      _ptr(C), _ptr(S))
+    if rc != 0:
+        raise RuntimeError(f"oracle_gemm_nvfp4_nt failed ({rc})")
+    return C, S
+
+
+def gemm_nvfp4_nt_sampled(A, SA, B, SB, rows, cols, alpha=1.0):
+    """Entries (rows[t], cols[t]) of gemm_nvfp4_nt.  Returns (C[t], S[t])."""
+    a, sa, b, sb, M, N, K = _nv_args(A, SA, B, SB)
+    r = np.ascontiguousarray(rows, dtype=np.int64)
+    c = np.ascontiguousarray(cols, dtype=np.int64)
+    if r.shape != c.shape:
+        raise ValueError("rows and cols differ in length")
+    C = np.zeros(r.shape, dtype=np.float64)
+    S = np.zeros(r.shape, dtype=np.float64)
+    rc = _load().oracle_gemm_nvfp4_nt_sampled(M, N, K, _ptr(a), _ptr(sa), _ptr(b), _ptr(sb),
+                                              float(alpha), r.size, _ptr(r), _ptr(c), _ptr(C), _ptr(S))
+    if rc != 0:
+        raise RuntimeError(f"oracle_gemm_nvfp4_nt_sampled failed ({rc})")
     return C, S

@@ -27,6 +27,8 @@
  *    and the CPU reference loop of its host harness.
  *  - block-scaled FP8 (MXFP8) NT product: the same page, section
  *    "Blackwell 概览 sm_100" (32 elements share one 8-bit exponent scale).
+ *  - block-scaled FP4 (NVFP4) NT product: the same section (16 elements
+ *    share one FP8 scale, plus a tensor-level FP32 scale).
  *
  * Precision: the pages accumulate in float; this oracle accumulates in
  * float64 and keeps the result unrounded, so that the GPU result can be
@@ -452,6 +454,101 @@ int oracle_gemm_mxfp8_nt_sampled(int64_t M, int64_t N, int64_t K,
             dot_nt(a, b, K, &acc, &mag);
             C[t] = acc;
             if (S) S[t] = mag;
+        }
+        free(a);
+        free(b);
+    }
+    return 0;
+}
+
+/* ---------------------------------------------------------------------- */
+/* Block-scaled FP4 (NVFP4): "异步拷贝与 Hopper/Blackwell 新特性", section    */
+/* "Blackwell 概览 sm_100": every 16 elements share one FP8 scale factor,   */
+/* and a tensor-level FP32 scale applies on top.  Read here as:             */
+/*   elements FP4 E2M1: 1 sign bit, 2 exponent bits with bias 1, 1          */
+/*     mantissa bit; exponent 0 = subnormal m/2; no inf or NaN.  Two per    */
+/*     byte, element 2i in the low nibble of byte i, 2i+1 in the high one.  */
+/*   block scales UE4M3: the E4M3 value of the byte (positive codes);       */
+/*   C[m][n] = alpha * sum_k a(m,k) SA[m][k/16] * b(n,k) SB[n][k/16],       */
+/*     alpha the product of the two tensor-level scales.                    */
+/* Each term is exact in double (2 x 2 significant bits, 4 x 4 for the      */
+/* scales).                                                                  */
+/* ---------------------------------------------------------------------- */
+
+double oracle_e2m1_to_f64(uint8_t nibble)
+{
+    const int sign = (nibble >> 3) & 1;
+    const int expo = (nibble >> 1) & 3;
+    const int mant = nibble & 1;
+    double v;
+    if (expo == 0)
+        v = 0.5 * (double)mant;
+    else
+        v = ldexp(1.0 + 0.5 * (double)mant, expo - 1);
+    return sign ? -v : v;
+}
+
+static void decode_nvfp4_row(const uint8_t *packed, const uint8_t *scales, int64_t K, double *out)
+{
+    for (int64_t k = 0; k < K; ++k) {
+        const uint8_t byte = packed[k / 2];
+        const uint8_t nib = (k % 2 == 0) ? (uint8_t)(byte & 0xf) : (uint8_t)(byte >> 4);
+        out[k] = oracle_e2m1_to_f64(nib) * oracle_e4m3_to_f64(scales[k / 16]);
+    }
+}
+
+int oracle_gemm_nvfp4_nt(int64_t M, int64_t N, int64_t K,
+                         const uint8_t *A, const uint8_t *SA,
+                         const uint8_t *B, const uint8_t *SB, double alpha,
+                         double *C, double *S)
+{
+    if (M < 0 || N < 0 || K < 0 || K % 16 != 0) return -1;
+    double *a = (double *)malloc((size_t)(M > 0 ? M : 1) * (size_t)(K > 0 ? K : 1) * sizeof(double));
+    double *b = (double *)malloc((size_t)(N > 0 ? N : 1) * (size_t)(K > 0 ? K : 1) * sizeof(double));
+    if (!a || !b) {
+        free(a);
+        free(b);
+        return -2;
+    }
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < M; ++r) decode_nvfp4_row(A + r * (K / 2), SA + r * (K / 16), K, a + r * K);
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < N; ++r) decode_nvfp4_row(B + r * (K / 2), SB + r * (K / 16), K, b + r * K);
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < M; ++i)
+        for (int64_t j = 0; j < N; ++j) {
+            double acc, mag;
+            dot_nt(a + i * K, b + j * K, K, &acc, &mag);
+            C[i * N + j] = alpha * acc;
+            if (S) S[i * N + j] = fabs(alpha) * mag;
+        }
+    free(a);
+    free(b);
+    return 0;
+}
+
+/* The same product at n listed positions (rows[t], cols[t]) only. */
+int oracle_gemm_nvfp4_nt_sampled(int64_t M, int64_t N, int64_t K,
+                                 const uint8_t *A, const uint8_t *SA,
+                                 const uint8_t *B, const uint8_t *SB, double alpha,
+                                 int64_t n, const int64_t *rows, const int64_t *cols,
+                                 double *C, double *S)
+{
+    if (M < 0 || N < 0 || K < 0 || K % 16 != 0 || n < 0) return -1;
+    for (int64_t t = 0; t < n; ++t)
+        if (rows[t] < 0 || rows[t] >= M || cols[t] < 0 || cols[t] >= N) return -1;
+#pragma omp parallel
+    {
+        double *a = (double *)malloc((size_t)(K > 0 ? K : 1) * sizeof(double));
+        double *b = (double *)malloc((size_t)(K > 0 ? K : 1) * sizeof(double));
+#pragma omp for schedule(static)
+        for (int64_t t = 0; t < n; ++t) {
+            decode_nvfp4_row(A + rows[t] * (K / 2), SA + rows[t] * (K / 16), K, a);
+            decode_nvfp4_row(B + cols[t] * (K / 2), SB + cols[t] * (K / 16), K, b);
+            double acc, mag;
+            dot_nt(a, b, K, &acc, &mag);
+            C[t] = alpha * acc;
+            if (S) S[t] = fabs(alpha) * mag;
         }
         free(a);
         free(b);

@@ -392,3 +392,93 @@ def test_mxfp8_matches_numpy_and_sampled():
     assert np.array_equal(Cs, C[rows, cols]) and np.array_equal(Ss, S[rows, cols])
     with pytest.raises(ValueError):
         oracle.gemm_mxfp8_nt(A[:, :40], SA[:, :1], B[:, :40], SB[:, :1])
+
+
+# ---------------------------------------------------------------------------
+# Block-scaled FP4 (NVFP4)
+# ---------------------------------------------------------------------------
+
+def _e2m1_via_e4m3(nib):
+    # widen each E2M1 field into an E4M3 code (exponent bias 1 -> 7, the
+    # mantissa bit to the top of three, the subnormal 0.5 = 2^-1) and let
+    # PyTorch's float8_e4m3fn cast decode it
+    import torch
+
+    s, e, m = (nib >> 3) & 1, (nib >> 1) & 3, nib & 1
+    if e == 0:
+        code = (s << 7) | ((6 << 3) if m else 0)
+    else:
+        code = (s << 7) | ((e + 6) << 3) | (m << 2)
+    return float(torch.tensor([code], dtype=torch.uint8).view(torch.float8_e4m3fn).float())
+
+
+def _nv_decode_ref(packed, scales):
+    import torch
+
+    lo, hi = packed & 0xF, packed >> 4
+    nib = np.stack([lo, hi], axis=-1).reshape(packed.shape[0], -1)
+    lut = np.array([_e2m1_via_e4m3(c) for c in range(16)])
+    sv = torch.from_numpy(np.ascontiguousarray(scales)).view(torch.float8_e4m3fn).double().numpy()
+    return lut[nib] * np.repeat(sv, 16, axis=1)
+
+
+def test_e2m1_decode_every_code():
+    ours = oracle.e2m1_to_f64(np.arange(16, dtype=np.uint8))
+    ref = np.array([_e2m1_via_e4m3(c) for c in range(16)])
+    assert np.array_equal(ours, ref)
+    assert ours.max() == 6.0 and ours[1] == 0.5 and np.all(np.diff(ours[:8]) > 0)
+
+
+def test_nvfp4_nibble_order_and_block_scales():
+    # B's single row holds distinct values; A selects one element k at a time:
+    # C = value at k, so the packing order (element 2i in the low nibble) and
+    # the 16-element scale blocks are both checked position by position.
+    K = 64
+    bcodes = np.array([(k % 7) + 1 for k in range(K)], dtype=np.uint8)  # 0.5 .. 4
+    B = (bcodes[0::2] | (bcodes[1::2] << 4)).astype(np.uint8)[None, :]
+    SB = np.array([[0x38, 0x40, 0x30, 0x48]], dtype=np.uint8)  # 1, 2, 0.5, 4
+    for k in range(K):
+        a = np.zeros(K, dtype=np.uint8)
+        a[k] = 0x2  # 1.0
+        A = (a[0::2] | (a[1::2] << 4)).astype(np.uint8)[None, :]
+        SA = np.full((1, K // 16), 0x38, np.uint8)
+        C, _ = oracle.gemm_nvfp4_nt(A, SA, B, SB, alpha=1.0)
+        want = _e2m1_via_e4m3(int(bcodes[k])) * [1.0, 2.0, 0.5, 4.0][k // 16]
+        assert C[0, 0] == want, k
+
+
+def test_nvfp4_small_values_exact_against_brute_force():
+    from fractions import Fraction
+    from dense_gemm_fp16_gb300 import workloads as wl
+
+    M, N, K = 4, 5, 64
+    A, SA = wl.draw_nvfp4(M, K, seed=71)
+    B, SB = wl.draw_nvfp4(N, K, seed=72)
+    A, SA, B, SB = A.numpy(), SA.numpy(), B.numpy(), SB.numpy()
+    C, S = oracle.gemm_nvfp4_nt(A, SA, B, SB, alpha=0.375)
+    a, b = _nv_decode_ref(A, SA), _nv_decode_ref(B, SB)
+    for i in range(M):
+        for j in range(N):
+            exact = Fraction(0.375) * sum(Fraction(a[i, k]) * Fraction(b[j, k]) for k in range(K))
+            assert C[i, j] == float(exact)
+            assert S[i, j] == float(Fraction(0.375) * sum(abs(Fraction(a[i, k]) * Fraction(b[j, k]))
+                                                          for k in range(K)))
+
+
+def test_nvfp4_matches_numpy_and_sampled():
+    from dense_gemm_fp16_gb300 import workloads as wl
+
+    M, N, K = 33, 27, 192
+    A, SA = wl.draw_nvfp4(M, K, seed=73)
+    B, SB = wl.draw_nvfp4(N, K, seed=74)
+    A, SA, B, SB = A.numpy(), SA.numpy(), B.numpy(), SB.numpy()
+    C, S = oracle.gemm_nvfp4_nt(A, SA, B, SB, alpha=-2.0)
+    a, b = _nv_decode_ref(A, SA), _nv_decode_ref(B, SB)
+    assert np.allclose(C, -2.0 * (a @ b.T), rtol=0, atol=1e-12 * S.max())
+    assert np.allclose(S, 2.0 * (np.abs(a) @ np.abs(b).T), rtol=1e-13)
+    rows = np.array([0, 32, 7, 19])
+    cols = np.array([0, 26, 3, 13])
+    Cs, Ss = oracle.gemm_nvfp4_nt_sampled(A, SA, B, SB, rows, cols, alpha=-2.0)
+    assert np.array_equal(Cs, C[rows, cols]) and np.array_equal(Ss, S[rows, cols])
+    with pytest.raises(ValueError):
+        oracle.gemm_nvfp4_nt(A[:, :5], SA[:, :1], B[:, :5], SB[:, :1])
