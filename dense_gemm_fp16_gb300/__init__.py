@@ -8,6 +8,8 @@ Two products behind the C ABI of ``include/gemm.h`` (``libgemm.so``):
   through a fused epilogue act(alpha·A·Bᵀ + bias + beta·R) before rounding.
 * ``gemm_mxfp8_nt(M, N, K, A, SFA, B, SFB, C, stream)``: the block-scaled
   FP8 (MXFP8) product on the tensor cores, half out.
+* ``gemm_nvfp4_nt(M, N, K, A, SFA, B, SFB, alpha, C, stream)``: the
+  block-scaled FP4 (NVFP4) product, half out.
 * ``sgemm(M, N, K, alpha, A, B, beta, C, stream)``: C = alpha·A·B + beta·C in
   fp32 on the CUDA cores.
 
@@ -56,12 +58,18 @@ from ._binding import (  # noqa: F401
     gemm_mxfp8_nt_ex,
     gemm_mxfp8_pack_scales,
     gemm_mxfp8_scale_bytes,
+    gemm_nvfp4_nt,
+    gemm_nvfp4_nt_ex,
+    gemm_nvfp4_pack_scales,
+    gemm_nvfp4_scale_bytes,
     gemm_f16_select,
     gemm_last_error,
     gemm_sgemm_select,
     load_library,
     mxfp8_nt,
     mxfp8_pack_scales,
+    nvfp4_nt,
+    nvfp4_pack_scales,
     sgemm,
     sgemm_,
     sgemm_ex,

@@ -88,6 +88,14 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gemm_mxfp8_nt.restype = i
         lib.gemm_mxfp8_nt_ex.argtypes = [i, i, i, vp, vp, vp, vp, vp, vp, ctypes.POINTER(_MxConfig)]
         lib.gemm_mxfp8_nt_ex.restype = i
+        lib.gemm_nvfp4_nt_ex.argtypes = [i, i, i, vp, vp, vp, vp, f, vp, vp, ctypes.POINTER(_MxConfig)]
+        lib.gemm_nvfp4_nt_ex.restype = i
+        lib.gemm_nvfp4_nt.argtypes = [i, i, i, vp, vp, vp, vp, f, vp, vp]
+        lib.gemm_nvfp4_nt.restype = i
+        lib.gemm_nvfp4_scale_bytes.argtypes = [i, i]
+        lib.gemm_nvfp4_scale_bytes.restype = ctypes.c_size_t
+        lib.gemm_nvfp4_pack_scales.argtypes = [i, i, vp, vp, vp]
+        lib.gemm_nvfp4_pack_scales.restype = i
         lib.gemm_mxfp8_scale_bytes.argtypes = [i, i]
         lib.gemm_mxfp8_scale_bytes.restype = ctypes.c_size_t
         lib.gemm_mxfp8_pack_scales.argtypes = [i, i, vp, vp, vp]
@@ -155,6 +163,25 @@ def gemm_mxfp8_nt_ex(M, N, K, A, SFA, B, SFB, C, stream=0, variant=GEMM_MXFP8_AU
     cfg = _MxConfig(variant, grid)
     return _check(load_library().gemm_mxfp8_nt_ex(M, N, K, A, SFA, B, SFB, C, stream or None,
                                                   ctypes.byref(cfg)))
+
+
+def gemm_nvfp4_nt(M, N, K, A, SFA, B, SFB, alpha, C, stream=0) -> int:
+    """Block-scaled FP4 product; SFA/SFB in the NVFP4 chunk layout (pointers as ints)."""
+    return _check(load_library().gemm_nvfp4_nt(M, N, K, A, SFA, B, SFB, float(alpha), C, stream or None))
+
+
+def gemm_nvfp4_nt_ex(M, N, K, A, SFA, B, SFB, alpha, C, stream=0, variant=GEMM_MXFP8_AUTO, grid=0) -> int:
+    cfg = _MxConfig(variant, grid)
+    return _check(load_library().gemm_nvfp4_nt_ex(M, N, K, A, SFA, B, SFB, float(alpha), C,
+                                                  stream or None, ctypes.byref(cfg)))
+
+
+def gemm_nvfp4_scale_bytes(rows: int, K: int) -> int:
+    return int(load_library().gemm_nvfp4_scale_bytes(rows, K))
+
+
+def gemm_nvfp4_pack_scales(rows, K, plain, blocked, stream=0) -> int:
+    return _check(load_library().gemm_nvfp4_pack_scales(rows, K, plain, blocked, stream or None))
 
 
 def gemm_mxfp8_scale_bytes(rows: int, K: int) -> int:
@@ -302,6 +329,42 @@ def mxfp8_nt(A, SA, B, SB, C=None, stream=None, packed=False, variant=GEMM_MXFP8
         C = torch.empty((M, N), dtype=torch.float16, device=A.device)
     gemm_mxfp8_nt_ex(M, N, K, A.data_ptr(), SA.data_ptr(), B.data_ptr(), SB.data_ptr(), C.data_ptr(),
                      _stream_handle(stream), variant, grid)
+    return C
+
+
+def nvfp4_pack_scales(S, stream=None):
+    """Plain E4M3 block scales [rows, K/16] (uint8 CUDA tensor) -> the NVFP4 chunk layout."""
+    import torch
+
+    if S.dtype != torch.uint8 or not S.is_cuda or not S.is_contiguous() or S.dim() != 2:
+        raise ValueError("scales must be a contiguous uint8 CUDA tensor [rows, K/16]")
+    rows, ksf = S.shape
+    K = 16 * ksf
+    out = torch.empty(gemm_nvfp4_scale_bytes(rows, K), dtype=torch.uint8, device=S.device)
+    gemm_nvfp4_pack_scales(rows, K, S.data_ptr(), out.data_ptr(), _stream_handle(stream))
+    return out
+
+
+def nvfp4_nt(A, SA, B, SB, alpha: float = 1.0, C=None, stream=None, packed=False,
+             variant=GEMM_MXFP8_AUTO, grid=0):
+    """C (half) = alpha * NVFP4 product of packed E2M1 A [M,K/2], B [N,K/2]
+    (uint8 CUDA tensors) with E4M3 block scales SA [M,K/16], SB [N,K/16] (or,
+    with packed=True, already in the chunk layout)."""
+    import torch
+
+    for t in (A, B):
+        if t.dtype != torch.uint8 or not t.is_cuda or not t.is_contiguous() or t.dim() != 2:
+            raise ValueError("A and B must be contiguous uint8 CUDA tensors (packed E2M1)")
+    if A.shape[1] != B.shape[1]:
+        raise ValueError(f"shape mismatch {tuple(A.shape)} x {tuple(B.shape)}^T")
+    M, K = A.shape[0], 2 * A.shape[1]
+    N = B.shape[0]
+    if not packed:
+        SA, SB = nvfp4_pack_scales(SA, stream), nvfp4_pack_scales(SB, stream)
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.float16, device=A.device)
+    gemm_nvfp4_nt_ex(M, N, K, A.data_ptr(), SA.data_ptr(), B.data_ptr(), SB.data_ptr(), alpha,
+                     C.data_ptr(), _stream_handle(stream), variant, grid)
     return C
 
 

@@ -256,7 +256,7 @@ int gemm_mxfp8_pack_scales(int rows, int K, const void *plain, void *blocked, ge
     if (rows == 0 || K == 0) return GEMM_OK;
     if (!plain || !blocked) return fail(GEMM_ERR_INVALID_ARG, "gemm_mxfp8_pack_scales: NULL pointer");
     std::string err;
-    const int st = gb300::mx_pack_scales_launch(rows, K, plain, blocked,
+    const int st = gb300::mx_pack_scales_launch(0, rows, K, plain, blocked,
                                                 reinterpret_cast<cudaStream_t>(stream), err);
     if (st != GEMM_OK) return fail_str(st, err);
     return GEMM_OK;
@@ -306,10 +306,84 @@ int gemm_mxfp8_nt_ex(int M, int N, int K, const void *A, const void *SFA, const 
     // columns do not fit TMEM together); narrow N keeps the 128 x 128 tiles.
     L.variant = (cfg && cfg->variant != GEMM_MXFP8_AUTO) ? cfg->variant
                 : (N > 128 ? GEMM_MXFP8_128x256 : GEMM_MXFP8_128x128);
+    L.fmt = 0;
+    L.alpha = 1.f;
     std::string err;
     st = gb300::mx_launch(L, err);
     if (st != GEMM_OK) return fail_str(st, err);
     return GEMM_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Block-scaled FP4 (NVFP4)
+// ---------------------------------------------------------------------------
+
+size_t gemm_nvfp4_scale_bytes(int rows, int K) {
+    if (rows <= 0 || K <= 0) return 0;
+    return static_cast<size_t>((rows + 127) / 128) * 4 * static_cast<size_t>((K + 255) / 256) * 512;
+}
+
+int gemm_nvfp4_pack_scales(int rows, int K, const void *plain, void *blocked, gemm_stream_t stream) {
+    if (rows < 0 || K < 0)
+        return fail(GEMM_ERR_INVALID_ARG, "gemm_nvfp4_pack_scales: negative size rows=%d K=%d", rows, K);
+    if (K % 32 != 0)
+        return fail(GEMM_ERR_UNSUPPORTED, "gemm_nvfp4_pack_scales: K=%d is not a multiple of 32", K);
+    if (rows == 0 || K == 0) return GEMM_OK;
+    if (!plain || !blocked) return fail(GEMM_ERR_INVALID_ARG, "gemm_nvfp4_pack_scales: NULL pointer");
+    std::string err;
+    const int st = gb300::mx_pack_scales_launch(1, rows, K, plain, blocked,
+                                                reinterpret_cast<cudaStream_t>(stream), err);
+    if (st != GEMM_OK) return fail_str(st, err);
+    return GEMM_OK;
+}
+
+int gemm_nvfp4_nt_ex(int M, int N, int K, const void *A, const void *SFA, const void *B,
+                     const void *SFB, float alpha, void *C, gemm_stream_t stream,
+                     const gemm_mxfp8_config *cfg) {
+    if (cfg && (cfg->grid < 0 || (cfg->variant != GEMM_MXFP8_AUTO && cfg->variant != GEMM_MXFP8_128x128 &&
+                                  cfg->variant != GEMM_MXFP8_128x256)))
+        return fail(GEMM_ERR_INVALID_ARG, "gemm_nvfp4_nt_ex: bad config variant=%d grid=%d (the 1-CTA "
+                    "128x128 and 128x256 kernels only)", cfg->variant, cfg->grid);
+    if (M < 0 || N < 0 || K < 0)
+        return fail(GEMM_ERR_INVALID_ARG, "gemm_nvfp4_nt: negative size M=%d N=%d K=%d", M, N, K);
+    if (M == 0 || N == 0) return GEMM_OK;
+    if (!C) return fail(GEMM_ERR_INVALID_ARG, "gemm_nvfp4_nt: C is NULL");
+    if (K % 32 != 0)
+        return fail(GEMM_ERR_UNSUPPORTED,
+                    "gemm_nvfp4_nt: K=%d; rows of K/2 bytes must be multiples of 16 bytes (K %% 32 == 0)", K);
+    if (K == 0) return f16_nt_impl(M, N, 0, nullptr, nullptr, C, stream, nullptr, kDefaultTimeoutNs, -1);
+    if (!A || !B || !SFA || !SFB) return fail(GEMM_ERR_INVALID_ARG, "gemm_nvfp4_nt: NULL operand");
+    if (!aligned16(A) || !aligned16(B) || !aligned16(SFA) || !aligned16(SFB))
+        return fail(GEMM_ERR_MISALIGNED, "gemm_nvfp4_nt: A, B, SFA and SFB must be 16-byte aligned");
+    int sms = 0;
+    int st = sm_count_of_current_device(&sms);
+    if (st != GEMM_OK) return st;
+    gb300::MxLaunch L;
+    L.M = M;
+    L.N = N;
+    L.K = K;
+    L.A = A;
+    L.SFA = SFA;
+    L.B = B;
+    L.SFB = SFB;
+    L.C = C;
+    L.stream = reinterpret_cast<cudaStream_t>(stream);
+    L.grid = cfg ? cfg->grid : 0;
+    L.timeout_ns = kDefaultTimeoutNs;
+    L.sm_count = sms;
+    L.variant = (cfg && cfg->variant != GEMM_MXFP8_AUTO) ? cfg->variant
+                : (N > 128 ? GEMM_MXFP8_128x256 : GEMM_MXFP8_128x128);
+    L.fmt = 1;
+    L.alpha = alpha;
+    std::string err;
+    st = gb300::mx_launch(L, err);
+    if (st != GEMM_OK) return fail_str(st, err);
+    return GEMM_OK;
+}
+
+int gemm_nvfp4_nt(int M, int N, int K, const void *A, const void *SFA, const void *B, const void *SFB,
+                  float alpha, void *C, gemm_stream_t stream) {
+    return gemm_nvfp4_nt_ex(M, N, K, A, SFA, B, SFB, alpha, C, stream, nullptr);
 }
 
 // ---------------------------------------------------------------------------

@@ -650,15 +650,22 @@ constexpr int kMxSfChunk = 512;  // 128 rows x 4 scales
 // BN output columns per tile (128 or 256: B's scales are BN/128 chunks),
 // STAGES ring stages, EBUFS epilogue staging buffers per warp, ACC TMEM
 // accumulators (2: the epilogue of a tile overlaps the next tile's MMAs).
-template <int BN, int STAGES, int EBUFS, int ACC>
+// FMT: kFmtMx8 (E4M3, a UE8M0 scale per 32 of K: one 512-byte chunk per
+// 128 rows per 128-byte k-block) or kFmtNv4 (E2M1 pairs, a UE4M3 scale per
+// 16 of K: four chunks per 128 rows per 128-byte k-block, one per MMA).
+constexpr int kFmtMx8 = 0;
+constexpr int kFmtNv4 = 1;
+
+template <int BN, int STAGES, int EBUFS, int ACC, int FMT = kFmtMx8>
 struct MxCfg {
     static constexpr int kABytes = kBM * kMxBK;
     static constexpr int kBBytes = BN * kMxBK;
-    static constexpr int kSfbChunks = BN / 128;
-    static constexpr int kSfBytes = (1 + kSfbChunks) * kMxSfChunk;
+    static constexpr int kSfbChunks = BN / 128;                 // B's 128-row tiles
+    static constexpr int kCpt = FMT == kFmtNv4 ? 4 : 1;         // chunks per row tile per k-block
+    static constexpr int kSfBytes = (1 + kSfbChunks) * kCpt * kMxSfChunk;
     static constexpr int kStageBytes = (kABytes + kBBytes + kSfBytes + 1023) / 1024 * 1024;
     static constexpr int kTmemCols = 512;  // accumulators, then the scale columns of each stage
-    static constexpr int kSfCols = 4 * (1 + kSfbChunks);
+    static constexpr int kSfCols = 4 * (1 + kSfbChunks) * kCpt;
     static constexpr int kSfCol0 = ACC * BN;
     static constexpr int kNumBars = 2 * STAGES + 5;
     static constexpr int kEpiOffset = STAGES * kStageBytes;
@@ -666,6 +673,7 @@ struct MxCfg {
     static constexpr int kSmemBytes = 1024 + kBarOffset + kNumBars * 8 + 16;
     static_assert(BN == 128 || BN == 256, "B's scales come in whole 128-row chunks");
     static_assert(ACC == 1 || ACC == 2, "one or two accumulators");
+    static_assert(FMT == kFmtMx8 || FMT == kFmtNv4, "MXFP8 or NVFP4");
     static_assert(kSfCol0 + kSfCols * STAGES <= kTmemCols, "scale columns fit the allocation");
     static_assert(kSmemBytes <= 232448, "fits the 227 KB opt-in limit");
 };
@@ -675,11 +683,11 @@ struct MxArgs {
     const uint8_t *sfb;  // scale chunks of B: [ceil(N/128)][ceil(K/128)][512]
 };
 
-template <int BN, int STAGES, int EBUFS, int ACC>
+template <int BN, int STAGES, int EBUFS, int ACC, int FMT = kFmtMx8>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_mxfp8_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                          const __grid_constant__ CUtensorMap tmC, const F16Args args, const MxArgs mx) {
-    using T = MxCfg<BN, STAGES, EBUFS, ACC>;
+    using T = MxCfg<BN, STAGES, EBUFS, ACC, FMT>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -748,16 +756,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t sa = sbase + stage * T::kStageBytes;
                     const uint32_t sb = sa + T::kABytes;
                     const uint32_t ssf = sb + T::kBBytes;
-                    mbar_arrive_expect_tx(full_bar(stage), T::kABytes + T::kBBytes + T::kSfBytes);
+                    // the k-block's scale chunks: kCpt consecutive chunks per
+                    // 128-row tile; B's row tiles past N do not exist in the
+                    // scale array and are not fetched (their stale values meet
+                    // only output columns >= N, which the store clips)
+                    constexpr uint32_t kTileSf = T::kCpt * kMxSfChunk;
+                    const int b_tiles = (args.N - nt * BN + 127) / 128;
+                    const int b_here = b_tiles < T::kSfbChunks ? b_tiles : T::kSfbChunks;
+                    mbar_arrive_expect_tx(full_bar(stage),
+                                          T::kABytes + T::kBBytes + (1 + b_here) * kTileSf);
                     tma_load_2d(sa, &tmA, full_bar(stage), kb * kMxBK, mt * kBM);
                     tma_load_2d(sb, &tmB, full_bar(stage), kb * kMxBK, nt * BN);
-                    bulk_load(ssf, mx.sfa + (static_cast<size_t>(mt) * num_kb + kb) * kMxSfChunk,
-                              kMxSfChunk, full_bar(stage));
-#pragma unroll
-                    for (int c = 0; c < T::kSfbChunks; ++c)
-                        bulk_load(ssf + (1 + c) * kMxSfChunk,
-                                  mx.sfb + (static_cast<size_t>(nt * T::kSfbChunks + c) * num_kb + kb) * kMxSfChunk,
-                                  kMxSfChunk, full_bar(stage));
+                    bulk_load(ssf, mx.sfa + (static_cast<size_t>(mt) * num_kb + kb) * kTileSf, kTileSf,
+                              full_bar(stage));
+                    for (int c = 0; c < b_here; ++c)
+                        bulk_load(ssf + (1 + c) * kTileSf,
+                                  mx.sfb + (static_cast<size_t>(nt * T::kSfbChunks + c) * num_kb + kb) * kTileSf,
+                                  kTileSf, full_bar(stage));
                     armed |= 1u << stage;
                     arm_parity ^= 1u << stage;
                     if (++stage == STAGES) {
@@ -797,23 +812,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t sa = sbase + stage * T::kStageBytes;
                     const uint32_t sb = sa + T::kABytes;
                     const uint32_t ssf = sb + T::kBBytes;
+                    // Each chunk is 32 rows of 16 bytes (8-row core matrices 128
+                    // bytes apart) and fills 4 TMEM columns.  A's chunk a lands at
+                    // sfa + 4a; B's chunk a of row tile c at sfb + 4(a * tiles + c),
+                    // so that each MMA's B scales (all of B's rows) are contiguous.
                     const uint32_t sfa_tmem = tmem_base + static_cast<uint32_t>(T::kSfCol0 + T::kSfCols * stage);
-                    const uint32_t sfb_tmem = sfa_tmem + 4u;
-                    // each chunk: 32 rows of 16 bytes, 8-row core matrices 128 bytes apart;
-                    // B's chunk c (rows 128c..) lands 4c columns on
-                    tmem_cp_32x128b_warpx4(sfa_tmem, plain_kmajor_desc(ssf, 128, 128));
+                    const uint32_t sfb_tmem = sfa_tmem + 4u * T::kCpt;
 #pragma unroll
-                    for (int c = 0; c < T::kSfbChunks; ++c)
-                        tmem_cp_32x128b_warpx4(sfb_tmem + 4u * c,
-                                               plain_kmajor_desc(ssf + (1 + c) * kMxSfChunk, 128, 128));
+                    for (int a = 0; a < T::kCpt; ++a) {
+                        tmem_cp_32x128b_warpx4(sfa_tmem + 4u * a, plain_kmajor_desc(ssf + a * kMxSfChunk, 128, 128));
+#pragma unroll
+                        for (int c = 0; c < T::kSfbChunks; ++c)
+                            tmem_cp_32x128b_warpx4(
+                                sfb_tmem + 4u * (a * T::kSfbChunks + c),
+                                plain_kmajor_desc(ssf + ((1 + c) * T::kCpt + a) * kMxSfChunk, 128, 128));
+                    }
                     const uint64_t adesc = sw128_kmajor_desc(sa);
                     const uint64_t bdesc = sw128_kmajor_desc(sb);
 #pragma unroll
-                    for (int j = 0; j < kMxBK / kMxUmmaK; ++j) {
-                        // K = 32 FP8 per MMA: the start address advances 32 bytes;
-                        // scale j of each row (its 32-element block) applies.
-                        mma_mxf8_ss(d_tmem, adesc + 2u * j, bdesc + 2u * j, idesc_mxf8_e4m3(kBM, BN, j),
-                                    sfa_tmem, sfb_tmem, (kb > 0 || j > 0) ? 1u : 0u);
+                    for (int j = 0; j < 4; ++j) {
+                        // 32 bytes of K per MMA (32 FP8 or 64 FP4): the start
+                        // address advances 32 bytes.
+                        if constexpr (FMT == kFmtMx8) {
+                            // scale j of each row (its 32-element block) applies
+                            mma_mxf8_ss(d_tmem, adesc + 2u * j, bdesc + 2u * j, idesc_mxf8_e4m3(kBM, BN, j),
+                                        sfa_tmem, sfb_tmem, (kb > 0 || j > 0) ? 1u : 0u);
+                        } else {
+                            // the four 16-element scales of chunk j apply
+                            mma_nvf4_ss(d_tmem, adesc + 2u * j, bdesc + 2u * j, idesc_nvf4_e2m1(kBM, BN),
+                                        sfa_tmem + 4u * j, sfb_tmem + 4u * T::kSfbChunks * j,
+                                        (kb > 0 || j > 0) ? 1u : 0u);
+                        }
                     }
                     mma_commit(empty_bar(stage));
                     if (++stage == STAGES) {
@@ -853,8 +882,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after_sync();
             const int mt = tile % args.m_tiles;
             const int nt = tile / args.m_tiles;
-            epilogue_warp_tile<BN, EBUFS, -1>(args, &tmC, tmem_base + lane_field + static_cast<uint32_t>(b * BN),
-                                              mt * kBM + quarter * 32, nt * BN, lane, stage_smem, step);
+            // NVFP4: the tensor-level scale alpha through the epilogue (ACT 0)
+            epilogue_warp_tile<BN, EBUFS, FMT == kFmtNv4 ? 0 : -1>(
+                args, &tmC, tmem_base + lane_field + static_cast<uint32_t>(b * BN), mt * kBM + quarter * 32,
+                nt * BN, lane, stage_smem, step);
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(acce_bar(b));
@@ -1135,18 +1166,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// Plain scales [rows][K/32] -> the kernel's chunk layout, padded with 127
-// (2^0) past the last row and the last scale; one thread per output byte.
+// Plain scales [rows][ksf] -> the kernels' chunk layout (`cpr` chunks of 4
+// scales per 128-row tile), padded with `pad` (a scale of 1) past the last
+// row and the last scale; one thread per output byte.
 __global__ void mx_pack_scales_kernel(const uint8_t *__restrict__ plain, uint8_t *__restrict__ blocked,
-                                      int rows, int ksf, int kbt, size_t total) {
+                                      int rows, int ksf, int cpr, uint8_t pad, size_t total) {
     const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
     for (size_t o = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; o < total; o += stride) {
         const size_t chunk = o / kMxSfChunk;
         const int within = static_cast<int>(o % kMxSfChunk);
-        const int rt = static_cast<int>(chunk / kbt), kb = static_cast<int>(chunk % kbt);
+        const int rt = static_cast<int>(chunk / cpr), kb = static_cast<int>(chunk % cpr);
         const int r = rt * 128 + (within >> 4) + 32 * ((within >> 2) & 3);
         const int j = kb * 4 + (within & 3);
-        blocked[o] = (r < rows && j < ksf) ? plain[static_cast<size_t>(r) * ksf + j] : uint8_t(127);
+        blocked[o] = (r < rows && j < ksf) ? plain[static_cast<size_t>(r) * ksf + j] : pad;
     }
 }
 
@@ -2003,10 +2035,11 @@ int mx_launch_pair(const MxLaunch &L, std::string &err) {
     return GEMM_OK;
 }
 
-template <int BN, int STAGES, int EBUFS, int ACC>
+template <int BN, int STAGES, int EBUFS, int ACC, int FMT = kFmtMx8>
 int mx_launch_1cta(const MxLaunch &L, std::string &err) {
-    using T = MxCfg<BN, STAGES, EBUFS, ACC>;
-    auto kernel = gemm_mxfp8_nt_kernel<BN, STAGES, EBUFS, ACC>;
+    using T = MxCfg<BN, STAGES, EBUFS, ACC, FMT>;
+    auto kernel = gemm_mxfp8_nt_kernel<BN, STAGES, EBUFS, ACC, FMT>;
+    const int kbytes = FMT == kFmtNv4 ? L.K / 2 : L.K;  // bytes of K per row
     static int configured[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -2024,8 +2057,9 @@ int mx_launch_1cta(const MxLaunch &L, std::string &err) {
     }
     CUtensorMap tmA, tmB, tmC;
     std::memset(&tmC, 0, sizeof tmC);
-    if (!encode_map(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, L.A, L.M, L.K, kBM, kMxBK, err)) return GEMM_ERR_CUDA;
-    if (!encode_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, L.B, L.N, L.K, BN, kMxBK, err))
+    if (!encode_map(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, L.A, L.M, kbytes, kBM, kMxBK, err))
+        return GEMM_ERR_CUDA;
+    if (!encode_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, L.B, L.N, kbytes, BN, kMxBK, err))
         return GEMM_ERR_CUDA;
     F16Args args;
     args.C = static_cast<__half *>(L.C);
@@ -2034,10 +2068,15 @@ int mx_launch_1cta(const MxLaunch &L, std::string &err) {
     args.K = L.K;
     args.m_tiles = (L.M + kBM - 1) / kBM;
     args.n_tiles = (L.N + BN - 1) / BN;
-    args.num_kb = (L.K + kMxBK - 1) / kMxBK;
+    args.num_kb = (kbytes + kMxBK - 1) / kMxBK;
     args.vec_store = (L.N % 8 == 0) && ((reinterpret_cast<uintptr_t>(L.C) & 15u) == 0);
     args.tma_store = args.vec_store;
-    args.epi = make_epi(EpiSpec{}, L.N);
+    EpiSpec scale;  // NVFP4: C = alpha * (the block-scaled product)
+    if (FMT == kFmtNv4) {
+        scale.alpha = L.alpha;
+        scale.on = 1;
+    }
+    args.epi = make_epi(scale, L.N);
     args.timeout_ns = L.timeout_ns;
     args.debug_skip_kblock = -1;
     args.dp_tiles = 0;
@@ -2071,6 +2110,13 @@ int mx_launch_1cta(const MxLaunch &L, std::string &err) {
 }  // namespace
 
 int mx_launch(const MxLaunch &L, std::string &err) {
+    if (L.fmt == kFmtNv4) {
+        switch (L.variant) {
+            case 3: return mx_launch_1cta<256, 3, 1, 1, kFmtNv4>(L, err);
+            case 1: return mx_launch_1cta<128, kMxStages, 2, 2, kFmtNv4>(L, err);
+            default: err = "the NVFP4 product has the 1-CTA kernels only"; return GEMM_ERR_UNSUPPORTED;
+        }
+    }
     switch (L.variant) {
         case 2: return mx_launch_pair<128, 7, 2, 2>(L, err);
         case 3: return mx_launch_1cta<256, 4, 1, 1>(L, err);
@@ -2079,16 +2125,20 @@ int mx_launch(const MxLaunch &L, std::string &err) {
     }
 }
 
-int mx_pack_scales_launch(int rows, int K, const void *plain, void *blocked, cudaStream_t stream,
+int mx_pack_scales_launch(int fmt, int rows, int K, const void *plain, void *blocked, cudaStream_t stream,
                           std::string &err) {
-    const int ksf = K / 32;
-    const int kbt = (K + kMxBK - 1) / kMxBK;
-    const size_t total = static_cast<size_t>((rows + 127) / 128) * kbt * kMxSfChunk;
+    // MXFP8: a scale per 32 elements, one chunk per 128 of K; NVFP4: a scale
+    // per 16, four chunks per 256 of K (whole 128-byte k-blocks).
+    const int ksf = fmt == kFmtNv4 ? K / 16 : K / 32;
+    const int cpr = fmt == kFmtNv4 ? 4 * ((K + 255) / 256) : (K + kMxBK - 1) / kMxBK;
+    const uint8_t pad = fmt == kFmtNv4 ? uint8_t(0x38) : uint8_t(127);  // 1.0 in E4M3 / UE8M0
+    const size_t total = static_cast<size_t>((rows + 127) / 128) * cpr * kMxSfChunk;
     if (total == 0) return GEMM_OK;
     const size_t want = (total + 255) / 256;
     const int blocks = static_cast<int>(want < 4096 ? want : 4096);
     mx_pack_scales_kernel<<<blocks, 256, 0, stream>>>(static_cast<const uint8_t *>(plain),
-                                                      static_cast<uint8_t *>(blocked), rows, ksf, kbt, total);
+                                                      static_cast<uint8_t *>(blocked), rows, ksf, cpr, pad,
+                                                      total);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         err = std::string("scale packing launch: ") + cudaGetErrorString(e);

@@ -67,11 +67,14 @@ struct MxLaunch {
     int grid;  // 0: one CTA per SM (at most one per tile)
     uint64_t timeout_ns;
     int sm_count;
-    int variant;  // 1: 1-CTA 128 x 128 tiles, 2: CTA pair 256 x 128 tiles
+    int variant;  // GEMM_MXFP8_* of gemm.h
+    int fmt;      // 0: MXFP8 (E4M3, UE8M0 per 32), 1: NVFP4 (E2M1 pairs, UE4M3 per 16)
+    float alpha;  // NVFP4: the tensor-level scale applied to the product
 };
 int mx_launch(const MxLaunch &L, std::string &err);
-// Plain scales [rows][K/32] -> chunk layout (device pointers, on `stream`).
-int mx_pack_scales_launch(int rows, int K, const void *plain, void *blocked, cudaStream_t stream,
+// Plain scales [rows][K/block] -> chunk layout (device pointers, on
+// `stream`); fmt as in MxLaunch.
+int mx_pack_scales_launch(int fmt, int rows, int K, const void *plain, void *blocked, cudaStream_t stream,
                           std::string &err);
 
 int f16_status_read_clear(cudaStream_t stream, int *code, std::string &err);

@@ -468,6 +468,28 @@ __device__ __forceinline__ void mma_mxf8_ss_pair(uint32_t d_tmem, uint64_t a_des
         : "memory");
 }
 
+// D (fp32) (+)= (A * SA) (B * SB)^T for packed FP4 (E2M1) A, B and 8-bit
+// scales, one per row per 16 elements of K: each MMA (K = 64) takes all four
+// scale bytes of the row's TMEM word.
+__device__ __forceinline__ void mma_nvf4_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// Block-scaled descriptor for FP4 E2M1 operands (format 1 in [7,10) and
+// [10,13)) with UE4M3 scales (bit 23 = 0), K = 64 (bit 31 = 0), scale IDs 0.
+__host__ __device__ constexpr uint32_t idesc_nvf4_e2m1(int m, int n) {
+    return (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
+           (static_cast<uint32_t>(m >> 4) << 24);
+}
+
 // Instruction descriptor of the block-scaled kinds: B scale-factor ID in
 // [4,6), A and B formats in [7,10) and [10,13) (E4M3 = 0), K-major (bits 15,
 // 16 = 0), N >> 3 in [17,23), scale format UE8M0 (bit 23 = 1), M >> 4 in

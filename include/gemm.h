@@ -279,6 +279,48 @@ size_t gemm_mxfp8_scale_bytes(int rows, int K);
  * GEMM_ERR_UNSUPPORTED. */
 int gemm_mxfp8_pack_scales(int rows, int K, const void *plain, void *blocked, gemm_stream_t stream);
 
+/* Block-scaled FP4 (NVFP4) product, C = alpha * A_s * B_s^T with
+ *     A_s[m][k] = e2m1(A, m, k) * e4m3(SA[m][k/16]),
+ *     B_s[n][k] = e2m1(B, n, k) * e4m3(SB[n][k/16]),
+ * accumulated in fp32 on the tensor cores (tcgen05.mma kind::mxf4nvf4,
+ * block_scale, scale_vec::4X) and rounded once to half ("异步拷贝与
+ * Hopper/Blackwell 新特性", section "Blackwell 概览 sm_100": in NVFP4 every 16
+ * elements share one FP8 scale, plus a tensor-level FP32 scale).
+ *   A    device, M x K/2 bytes, row-major: FP4 E2M1 codes (1 sign, 2 exponent
+ *        bits with bias 1, 1 mantissa bit), two per byte, element 2i of a
+ *        row in the low 4 bits of byte i;
+ *   B    device, N x K/2 bytes, row-major (the transposed right operand);
+ *   SFA, SFB  device, the E4M3 block scales (positive codes) of A and B in
+ *        the chunk layout below, gemm_nvfp4_scale_bytes(M or N, K) bytes each;
+ *   alpha  the tensor-level scale (the product of A's and B's);
+ *   C    device, half M x N, row-major.
+ * Scale chunk layout: rows in tiles of 128, K in blocks of 256 split into four
+ * 64-element chunks; chunk (t, c) (c counts 64-element blocks, 4 per 256)
+ * is 512 bytes at offset (t * 4 * ceil(K/256) + c) * 512, and byte
+ * 16*(r % 32) + 4*(r / 32) + j of it holds the scale of row 128t + r for K
+ * elements 64c + 16j .. +15.  Entries past the last row or scale must be
+ * finite (the packer writes 0x38 = 1.0).  gemm_nvfp4_pack_scales converts
+ * plain [rows][K/16] scales.  K must be a multiple of 32
+ * (GEMM_ERR_UNSUPPORTED otherwise); A, B, SFA and SFB 16-byte aligned
+ * (GEMM_ERR_MISALIGNED).  K = 0 writes C = 0. */
+int gemm_nvfp4_nt(int M, int N, int K, const void *A, const void *SFA, const void *B,
+                  const void *SFB, float alpha, void *C, gemm_stream_t stream);
+
+/* gemm_nvfp4_nt with a kernel configuration: GEMM_MXFP8_AUTO,
+ * GEMM_MXFP8_128x128 or GEMM_MXFP8_128x256 (the pair kernels are MXFP8 only:
+ * GEMM_ERR_INVALID_ARG). */
+int gemm_nvfp4_nt_ex(int M, int N, int K, const void *A, const void *SFA, const void *B,
+                     const void *SFB, float alpha, void *C, gemm_stream_t stream,
+                     const gemm_mxfp8_config *cfg);
+
+/* Bytes of the NVFP4 scale chunk layout: ceil(rows/128) * 4 * ceil(K/256) * 512. */
+size_t gemm_nvfp4_scale_bytes(int rows, int K);
+
+/* Device-side conversion of plain [rows][K/16] E4M3 scales into the chunk
+ * layout (padding 0x38), enqueued on `stream`.  K % 32 != 0 ->
+ * GEMM_ERR_UNSUPPORTED. */
+int gemm_nvfp4_pack_scales(int rows, int K, const void *plain, void *blocked, gemm_stream_t stream);
+
 /* One kernel configuration of the SGEMM path. */
 typedef struct {
     int variant;

@@ -35,7 +35,8 @@ def test_headers_declare_the_boundary():
     for n in ["gemm_f16_nt", "sgemm", "gemm_last_error", "gemm_check_device_status",
               "gemm_f16_select", "gemm_sgemm_select", "gemm_f16_nt_ex", "sgemm_ex",
               "gemm_debug_f16_nt_skip_load", "gemm_f16_nt_fused", "gemm_f16_nt_stream_k_noalloc",
-              "gemm_mxfp8_nt", "gemm_mxfp8_scale_bytes", "gemm_mxfp8_pack_scales"]:
+              "gemm_mxfp8_nt", "gemm_mxfp8_scale_bytes", "gemm_mxfp8_pack_scales",
+              "gemm_nvfp4_nt", "gemm_nvfp4_nt_ex", "gemm_nvfp4_scale_bytes", "gemm_nvfp4_pack_scales"]:
         assert n in names
 
 
@@ -128,6 +129,23 @@ def test_mxfp8_arguments_are_checked_on_the_host(lib):
     with pytest.raises(g.GemmError) as e:
         g.gemm_mxfp8_pack_scales(16, 40, 0x1000, 0x1000)
     assert e.value.status == g.GEMM_ERR_UNSUPPORTED
+
+
+def test_nvfp4_arguments_are_checked_on_the_host(lib):
+    assert g.gemm_nvfp4_scale_bytes(0, 64) == 0
+    assert g.gemm_nvfp4_scale_bytes(1, 32) == 4 * 512
+    assert g.gemm_nvfp4_scale_bytes(129, 320) == 2 * 4 * 2 * 512
+    with pytest.raises(g.GemmError) as e:
+        g.gemm_nvfp4_nt(16, 16, 48, 0x1000, 0x1000, 0x1000, 0x1000, 1.0, 0x1000)
+    assert e.value.status == g.GEMM_ERR_UNSUPPORTED and "K=48" in str(e.value)
+    with pytest.raises(g.GemmError) as e:
+        g.gemm_nvfp4_nt(16, 16, 64, 0x1008, 0x1000, 0x1000, 0x1000, 1.0, 0x1000)
+    assert e.value.status == g.GEMM_ERR_MISALIGNED
+    with pytest.raises(g.GemmError) as e:
+        g.gemm_nvfp4_nt_ex(16, 16, 64, 0x1000, 0x1000, 0x1000, 0x1000, 1.0, 0x1000,
+                           variant=g.GEMM_MXFP8_256x256_PAIR)
+    assert e.value.status == g.GEMM_ERR_INVALID_ARG
+    assert g.gemm_nvfp4_nt(16, 0, 64, 0, 0, 0, 0, 1.0, 0) == g.GEMM_OK
 
 
 def test_f16_selector(lib):
