@@ -32,6 +32,8 @@ ranks is taken and rank 0 prints one JSON line.
   unfused sequence (plain product, then PyTorch element-wise kernels).
 * ``mxfp8``: the block-scaled FP8 product (``gemm_mxfp8_nt``) at the same
   shape against the fp8 dense peak.
+* ``nvfp4``: the block-scaled FP4 product (``gemm_nvfp4_nt``) at the same
+  shape against the fp4 dense peak.
 
 N > 1 runs N independent replicas (one per GPU; the product has no exchange
 step), ``scaling: weak``.  ``--impl reference`` times the float64 oracle on
@@ -572,6 +574,38 @@ def run_ours(args):
                          "peak_source": peak_note + " x 2 (nominal fp8/bf16 ratio)",
                          "frac_of_burst_peak": mval / (2.0 * burst)}}
 
+    # ---- block-scaled FP4 (NVFP4) at the headline shape against the fp4
+    # dense peak (the measured bf16 peak x the nominal fp4/bf16 ratio of 6)
+    if not args.skip_sgemm:
+        nv_sets = []
+        with torch.cuda.stream(stream):
+            for j in range(ROTATE):
+                xa, xsa = wl.draw_nvfp4(M, K, seed=51 + j)
+                xb, xsb = wl.draw_nvfp4(N, K, seed=61 + j)
+                nv_sets.append((xa.cuda(), g.nvfp4_pack_scales(xsa.cuda(), stream), xb.cuda(),
+                                g.nvfp4_pack_scales(xsb.cuda(), stream),
+                                torch.empty((M, N), dtype=torch.float16, device="cuda")))
+        stream.synchronize()
+
+        def nvs(i):
+            xa, pa, xb, pb, xc = nv_sets[i % ROTATE]
+            g.gemm_nvfp4_nt(M, N, K, xa.data_ptr(), pa.data_ptr(), xb.data_ptr(), pb.data_ptr(), 1.0,
+                            xc.data_ptr(), sh)
+        with torch.cuda.stream(stream):
+            region_time(nvs, stream, 5)
+            n_nv = 50
+            t_nv = region_time(nvs, stream, n_nv) / n_nv
+        g.gemm_check_device_status(sh)
+        fp4_peak = 6.0 * peak
+        nval = w.flop / (t_nv * 1e-3) / 1e12
+        line["nvfp4"] = {
+            "workload": f"nvfp4_nt_{M}x{N}x{K} (E2M1 pairs, E4M3 scale per 16 of K, alpha, half out)",
+            "value": nval, "unit": "TFLOP/s", "us_per_call": 1e3 * t_nv,
+            "roofline": {"bound": "tensor", "achieved": nval, "peak": fp4_peak, "unit": "TFLOP/s",
+                         "frac": nval / fp4_peak,
+                         "peak_source": peak_note + " x 6 (nominal fp4/bf16 ratio)",
+                         "frac_of_burst_peak": nval / (6.0 * burst)}}
+
     if rank == 0 and not args.skip_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, A, B, budget_s=args.cpu_budget)
     if rank == 0:
@@ -596,7 +630,7 @@ def main():
                     help="seconds of oracle work for the cpu_baseline sample")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--skip-extras", "--skip-sgemm", dest="skip_sgemm", action="store_true",
-                    help="only the headline line: no sgemm, gemv, fused_epilogue or mxfp8 objects")
+                    help="only the headline line: no sgemm, gemv, fused_epilogue, mxfp8 or nvfp4 objects")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)   # timing rule: at least 3 warm-up steps
     if args.impl == "reference":
