@@ -17,7 +17,8 @@ ranks is taken and rank 0 prints one JSON line.
   sustained figure (the region follows a soak and runs power-capped), with
   the fraction of the burst figure beside it.
 * ``e2e``: the same metric through the C ABI with host buffers: each step
-  copies A and B from pinned host memory, runs the GEMM and copies C back.
+  copies A and B from pinned host memory, runs the GEMM and copies C back;
+  uploads, GEMMs and downloads of successive steps overlap on three streams.
 * ``cpu_baseline``: the float64 oracle on the host cores, on a bounded row
   sample of the same product.
 * ``cublas``: torch.matmul(A, Bᵀ) (cuBLAS, fp32 accumulation) timed the same
@@ -410,31 +411,55 @@ def run_ours(args):
         "wall_s_timed_region": wall,
     }
 
-    # ---- end to end through the C ABI with pinned host buffers
+    # ---- end to end through the C ABI with pinned host buffers.  Every step
+    # uploads its A and B from pinned host memory, runs gemm_f16_nt and
+    # downloads its C; the three run on their own streams over two device
+    # buffer sets, so step i's download, step i+1's GEMM and step i+2's
+    # upload overlap (NVLink-C2C moves both directions at once).  Events keep
+    # each buffer's uses in order; the timed region ends when the last
+    # download has landed in host memory.
     hA, hB = A.pin_memory(), B.pin_memory()
-    hC = torch.empty((M, N), dtype=torch.float16).pin_memory()
-    a, b, c = sets[0]
+    hCs = [torch.empty((M, N), dtype=torch.float16).pin_memory() for _ in range(2)]
+    dev = [(sets[j][0], sets[j][1], sets[j][2]) for j in range(2)]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_gemm = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    for j in range(2):  # all buffers start free
+        ev_gemm[j].record(stream)
+        ev_out[j].record(s_out)
 
-    def e2e_step(_):
-        a.copy_(hA, non_blocking=True)
-        b.copy_(hB, non_blocking=True)
+    def e2e_step(i):
+        j = i % 2
+        a, b, c = dev[j]
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(ev_gemm[j])        # the GEMM of step i-2 has read a, b
+            a.copy_(hA, non_blocking=True)
+            b.copy_(hB, non_blocking=True)
+            ev_in[j].record(s_in)
+        stream.wait_event(ev_in[j])
+        stream.wait_event(ev_out[j])           # the download of step i-2 has read c
         g.gemm_f16_nt(M, N, K, a.data_ptr(), b.data_ptr(), c.data_ptr(), sh)
-        hC.copy_(c, non_blocking=True)
+        ev_gemm[j].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_gemm[j])
+            hCs[j].copy_(c, non_blocking=True)
+            ev_out[j].record(s_out)
 
-    with torch.cuda.stream(stream):
-        for i in range(args.warmup):
-            e2e_step(i)
-        stream.synchronize()
-        barrier(world)
-        t0 = time.perf_counter()
-        for i in range(args.steps):
-            e2e_step(i)
-        stream.synchronize()
-        e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    for i in range(args.warmup):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
     line["e2e"] = {"value": world * w.flop * args.steps / e2e_s / 1e12, "unit": "TFLOP/s",
                    "h2d_bytes_per_step": hA.numel() * 2 + hB.numel() * 2,
-                   "d2h_bytes_per_step": hC.numel() * 2,
-                   "gpu_launches": args.steps}
+                   "d2h_bytes_per_step": hCs[0].numel() * 2,
+                   "gpu_launches": args.steps,
+                   "pipelining": "upload, GEMM and download on separate streams, two buffer sets"}
 
     # ---- cuBLAS reference line (context only, never on the product path)
     torch.backends.cuda.matmul.allow_fp16_reduced_precision_reduction = False
