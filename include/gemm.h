@@ -23,7 +23,12 @@
  * Common rules for every entry point below:
  *  - Ownership: all matrix pointers are device memory owned by the caller;
  *    the library keeps no reference after the call returns and allocates no
- *    device memory per call.  C must not overlap A or B.
+ *    device memory per call.  One exception: the fp16 pair kernel's split-K
+ *    and stream-K partials (see GEMM_F16_FLAG_STREAM_K) live in a workspace
+ *    of about 256 KB per CTA pair (19 MiB on a 152-SM GB300), allocated once
+ *    per device and stream by the first call that splits and kept for the
+ *    life of the process; gemm_f16_nt_stream_k_noalloc never allocates.
+ *    C must not overlap A or B.
  *  - Asynchrony: work is enqueued on `stream` (a cudaStream_t; NULL means
  *    the legacy default stream) on the calling thread's current device.  The
  *    call returns once the work is enqueued; it does not synchronise.
@@ -123,6 +128,14 @@ typedef struct {
  * split is skipped while the stream is being captured into a graph.  Off by
  * default: on GB300 at the benchmark shapes the partial hand-off costs more
  * than the balanced last round gains.
+ *
+ * Split-K, by contrast, is on by default, with no flag: when there are so few
+ * pair tiles that each would get at least four CTA pairs ("第 6 章 · Shared
+ * Memory & Tile", section "6.5.6 Split-K / Stream-K"), every tile's k-blocks
+ * are shared over up to 8 pairs (at least 32 k-blocks each) through the same
+ * workspace, and gemm_f16_select picks the pair kernel with all pairs for
+ * such shapes.  The partials are added in a fixed order: results do not
+ * depend on timing.  Also skipped under stream capture.
  */
 #define GEMM_F16_FLAG_STREAM_K 1
 
