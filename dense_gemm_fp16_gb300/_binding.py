@@ -58,7 +58,7 @@ class _MxConfig(ctypes.Structure):
 
 
 class _SgemmConfig(ctypes.Structure):
-    _fields_ = [("variant", ctypes.c_int)]
+    _fields_ = [("variant", ctypes.c_int), ("splits", ctypes.c_int)]
 
 
 _lock = threading.Lock()
@@ -206,8 +206,8 @@ def sgemm(M: int, N: int, K: int, alpha: float, A: int, B: int, beta: float, C: 
     return _check(load_library().sgemm(M, N, K, alpha, A, B, beta, C, stream or None))
 
 
-def sgemm_ex(M, N, K, alpha, A, B, beta, C, stream=0, variant=GEMM_SGEMM_AUTO) -> int:
-    cfg = _SgemmConfig(variant)
+def sgemm_ex(M, N, K, alpha, A, B, beta, C, stream=0, variant=GEMM_SGEMM_AUTO, splits=0) -> int:
+    cfg = _SgemmConfig(variant, splits)
     return _check(load_library().sgemm_ex(M, N, K, alpha, A, B, beta, C, stream or None,
                                           ctypes.byref(cfg)))
 
@@ -222,10 +222,10 @@ def gemm_f16_select(M: int, N: int, K: int, sm_count: int) -> tuple[int, int]:
     return cfg.variant, cfg.grid
 
 
-def gemm_sgemm_select(M: int, N: int, K: int, sm_count: int) -> int:
-    cfg = _SgemmConfig(0)
+def gemm_sgemm_select(M: int, N: int, K: int, sm_count: int) -> tuple[int, int]:
+    cfg = _SgemmConfig(0, 0)
     _check(load_library().gemm_sgemm_select(M, N, K, sm_count, ctypes.byref(cfg)))
-    return cfg.variant
+    return cfg.variant, cfg.splits
 
 
 def gemm_debug_f16_nt_skip_load(M, N, K, A, B, C, stream, skip_kblock, timeout_ns) -> int:

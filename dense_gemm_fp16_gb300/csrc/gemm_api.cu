@@ -4,6 +4,7 @@
 // in include/gemm.h.
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
@@ -126,16 +127,61 @@ int gemm_f16_select(int M, int N, int K, int sm_count, gemm_f16_config *cfg) {
     return GEMM_OK;
 }
 
+// Predicted time in microseconds of one SGEMM launch with a given tile and
+// split count.  The CTAs spread over the SMs, so the busiest SM runs
+// ceil(ctas / sms) of them, each over its K share; one 128 x 128 CTA costs
+// about 0.094 us per K element and one 64 x 64 CTA 0.041 us (13% less each
+// when two share an SM); a split adds the partial-slot writes, the fence and
+// the last CTA's pass over the slots.  The constants are GB300 measurements;
+// the model only has to rank the candidates.
+static double sgemm_cost(int variant, int M, int N, int sms, int splits, int chunk) {
+    const bool big = variant == GEMM_SGEMM_128x128;
+    const int bm = big ? 128 : 64;
+    const double tiles = static_cast<double>(ceil_div(M, bm)) * static_cast<double>(ceil_div(N, bm));
+    const double per_sm = std::ceil(tiles * splits / sms);
+    const double share = (!big && per_sm >= 2) ? 0.87 : 1.0;
+    double cost = per_sm * chunk * (big ? 0.094 : 0.041) * share;
+    if (splits > 1) cost += big ? 2.0 + 1.0 * splits : 1.0 + 0.4 * splits;
+    return cost;
+}
+
+// Tile and split count of the lowest predicted time; a caller's fixed
+// variant or split count (non-zero) narrows the search.  Splits are only
+// considered when the tiles number at most twice the SMs: beyond that the
+// last wave is a small part of the run and the slots' traffic is not.
+static void sgemm_plan(int M, int N, int K, int sms, int fix_variant, int fix_splits, int *variant,
+                       int *splits) {
+    bool have = false;
+    double best = 0.0;
+    *variant = fix_variant ? fix_variant : GEMM_SGEMM_128x128;
+    *splits = 1;
+    for (int v = GEMM_SGEMM_128x128; v < GEMM_SGEMM_NUM_VARIANTS; ++v) {
+        if (fix_variant && v != fix_variant) continue;
+        const int bm = v == GEMM_SGEMM_128x128 ? 128 : 64;
+        const long long tiles = ceil_div(M, bm) * ceil_div(N, bm);
+        const int smax = (K > 0 && tiles <= 2LL * sms) ? gb300::kSgemmMaxSplits : 1;
+        const int s_lo = fix_splits ? fix_splits : 1, s_hi = fix_splits ? fix_splits : smax;
+        for (int s = s_lo; s <= s_hi; ++s) {
+            int chunk = K;
+            const int eff = gb300::sgemm_split_chunk(K, s, &chunk);
+            if (eff != s && !fix_splits) continue;  // the same as a smaller count
+            const double c = sgemm_cost(v, M, N, sms, eff, chunk);
+            if (!have || c < best) {
+                have = true;
+                best = c;
+                *variant = v;
+                *splits = eff;
+            }
+        }
+    }
+}
+
 int gemm_sgemm_select(int M, int N, int K, int sm_count, gemm_sgemm_config *cfg) {
     if (!cfg) return fail(GEMM_ERR_INVALID_ARG, "gemm_sgemm_select: cfg is NULL");
     if (M < 0 || N < 0 || K < 0 || sm_count <= 0)
         return fail(GEMM_ERR_INVALID_ARG, "gemm_sgemm_select: bad M=%d N=%d K=%d sm_count=%d", M,
                     N, K, sm_count);
-    // The 128 x 128 tile does 16 FFMA per shared-memory load; use it whenever
-    // it still gives every SM at least one CTA, else the 64 x 64 tile (4x the
-    // CTAs) so small problems do not run on a handful of SMs.
-    const long long big = ceil_div(M, 128) * ceil_div(N, 128);
-    cfg->variant = (big >= sm_count) ? GEMM_SGEMM_128x128 : GEMM_SGEMM_64x64;
+    sgemm_plan(M, N, K, sm_count, 0, 0, &cfg->variant, &cfg->splits);
     return GEMM_OK;
 }
 
@@ -397,19 +443,18 @@ int sgemm_ex(int M, int N, int K, float alpha, const float *A, const float *B, f
     if (M == 0 || N == 0) return GEMM_OK;
     if (!C) return fail(GEMM_ERR_INVALID_ARG, "sgemm: C is NULL");
     if (K > 0 && (!A || !B)) return fail(GEMM_ERR_INVALID_ARG, "sgemm: A or B is NULL");
-    if (cfg && (cfg->variant < 0 || cfg->variant >= GEMM_SGEMM_NUM_VARIANTS))
-        return fail(GEMM_ERR_INVALID_ARG, "sgemm_ex: bad config variant=%d", cfg->variant);
-    int variant = cfg ? cfg->variant : GEMM_SGEMM_AUTO;
-    if (variant == GEMM_SGEMM_AUTO) {
-        int sms = 0;
-        int st = sm_count_of_current_device(&sms);
-        if (st != GEMM_OK) return st;
-        gemm_sgemm_config sel;
-        st = gemm_sgemm_select(M, N, K, sms, &sel);
-        if (st != GEMM_OK) return st;
-        variant = sel.variant;
-    }
+    if (cfg && (cfg->variant < 0 || cfg->variant >= GEMM_SGEMM_NUM_VARIANTS || cfg->splits < 0 ||
+                cfg->splits > gb300::kSgemmMaxSplits))
+        return fail(GEMM_ERR_INVALID_ARG, "sgemm_ex: bad config variant=%d splits=%d", cfg->variant,
+                    cfg->splits);
+    int sms = 0;
+    int st0 = sm_count_of_current_device(&sms);
+    if (st0 != GEMM_OK) return st0;
+    int variant = GEMM_SGEMM_128x128, splits = 1;
+    sgemm_plan(M, N, K, sms, cfg ? cfg->variant : 0, cfg ? cfg->splits : 0, &variant, &splits);
     gb300::SgemmLaunch L;
+    L.sm_count = sms;
+    L.splits = splits;
     L.M = M;
     L.N = N;
     L.K = K;

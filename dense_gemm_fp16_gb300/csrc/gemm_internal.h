@@ -107,8 +107,29 @@ struct SgemmLaunch {
     const float *B;
     float *C;
     cudaStream_t stream;
-    int variant;  // GEMM_SGEMM_128x128 or GEMM_SGEMM_64x64
+    int variant;   // GEMM_SGEMM_128x128 or GEMM_SGEMM_64x64
+    int sm_count;  // SMs of the current device
+    int splits;    // split-K depth, 1 = none (sgemm_split_chunk gives the shares)
 };
+
+// Split-K of the SGEMM path: at most this many CTAs share one tile's K.
+constexpr int kSgemmMaxSplits = 8;
+
+// K share of each of `splits` CTAs: ceil(K / splits) rounded up to the
+// 16-deep k-slice and at least 64 deep; returns how many shares that makes
+// (at most `splits`; 1 = no split).
+inline int sgemm_split_chunk(int K, int splits, int *chunk) {
+    if (splits <= 1 || K <= 0) {
+        *chunk = K;
+        return 1;
+    }
+    int c = (K + splits - 1) / splits;
+    c = (c + 15) / 16 * 16;
+    if (c < 64) c = 64;
+    const int eff = (K + c - 1) / c;
+    *chunk = eff > 1 ? c : K;
+    return eff;
+}
 
 int sgemm_launch(const SgemmLaunch &L, std::string &err);
 

@@ -25,6 +25,10 @@
 // makes any M, N, K exact.
 #include <cuda_runtime.h>
 
+#include <map>
+#include <mutex>
+#include <utility>
+
 #include "gemm.h"
 #include "gemm_internal.h"
 
@@ -64,10 +68,24 @@ __device__ __forceinline__ void cp_async_wait() {
 template <int BM, int BN, int TM, int TN>
 constexpr int sgemm_threads() { return (BM / TM) * (BN / TN); }
 
+// Split-K ("第 6 章 · Shared Memory & Tile", section "6.5.6 Split-K /
+// Stream-K"): with few tiles, blockIdx.z = s takes K elements
+// [s * kchunk, (s + 1) * kchunk) of its tile and writes alpha times its partial
+// to the tile's workspace slot s; the CTA that finishes a tile last (a
+// counter per tile, reset by that CTA for the next launch) adds the slots in
+// the order s = 0, 1, ... -- so the result does not depend on timing -- and
+// applies beta * C.
+struct SplitK {
+    int splits;         // 1: no split
+    int kchunk;         // K elements per split, a multiple of BK
+    float *ws;          // [tiles][splits][BM * BN] partials
+    unsigned *counters; // [tiles], zero between launches
+};
+
 template <int BM, int BN, int BK, int TM, int TN, int STAGES, int MINB, bool VEC>
 __global__ void __launch_bounds__(sgemm_threads<BM, BN, TM, TN>(), MINB)
     sgemm_pipe_kernel(int M, int N, int K, float alpha, const float *__restrict__ A,
-                      const float *__restrict__ B, float beta, float *__restrict__ C) {
+                      const float *__restrict__ B, float beta, float *__restrict__ C, const SplitK sk) {
     constexpr int RM = TM / 4, RN = TN / 4;
     constexpr int kThreads = sgemm_threads<BM, BN, TM, TN>();
     constexpr int kWarpsN = (BN / TN) / 8;  // a warp is 4 thread rows x 8 thread columns
@@ -125,17 +143,20 @@ __global__ void __launch_bounds__(sgemm_threads<BM, BN, TM, TN>(), MINB)
 #pragma unroll
         for (int j = 0; j < TN / 2; ++j) accp[i][j] = make_float2(0.f, 0.f);
 
-    const int KT = (K + BK - 1) / BK;
+    // this CTA's share of K (all of it without a split)
+    const int kbeg = static_cast<int>(blockIdx.z) * sk.kchunk;
+    const int kend = sk.splits > 1 ? min(K, kbeg + sk.kchunk) : K;
+    const int KT = (kend - kbeg + BK - 1) / BK;
 #pragma unroll
     for (int s = 0; s < STAGES - 1; ++s) {
-        if (s < KT) load_slice(s, s * BK);
+        if (s < KT) load_slice(s, kbeg + s * BK);
         cp_async_commit();  // one group per slice, empty ones included
     }
     for (int kt = 0; kt < KT; ++kt) {
         cp_async_wait<STAGES - 2>();  // slice kt has landed (this thread's part)
         __syncthreads();              // ... everyone's part; slice kt-1 is no longer read
         const int next = kt + STAGES - 1;
-        if (next < KT) load_slice(next % STAGES, next * BK);
+        if (next < KT) load_slice(next % STAGES, kbeg + next * BK);
         cp_async_commit();
         const int buf = kt % STAGES;
 #pragma unroll
@@ -169,6 +190,79 @@ __global__ void __launch_bounds__(sgemm_threads<BM, BN, TM, TN>(), MINB)
     }
     cp_async_wait<0>();
     const float(&acc)[TM][TN] = *reinterpret_cast<const float(*)[TM][TN]>(&accp[0][0]);
+
+    if (sk.splits > 1) {
+        // Partial of this split, alpha applied, into slot blockIdx.z: float4 q
+        // of thread t at (q * threads + t) * 4, so a warp writes 512
+        // contiguous bytes per store.
+        constexpr int Q = TM * TN / 4;
+        const int tile = blockIdx.y * gridDim.x + blockIdx.x;
+        float4 *slots = reinterpret_cast<float4 *>(sk.ws) + static_cast<size_t>(tile) * sk.splits * (Q * kThreads);
+        float4 *mine = slots + static_cast<size_t>(blockIdx.z) * (Q * kThreads);
+#pragma unroll
+        for (int q = 0; q < Q; ++q) {
+            const float *a = &acc[q / (TN / 4)][(q % (TN / 4)) * 4];
+            mine[q * kThreads + tid] = make_float4(alpha * a[0], alpha * a[1], alpha * a[2], alpha * a[3]);
+        }
+        __threadfence();
+        __syncthreads();
+        __shared__ int last;
+        if (tid == 0) last = atomicAdd(&sk.counters[tile], 1u) == static_cast<unsigned>(sk.splits - 1);
+        __syncthreads();
+        if (!last) return;
+        __threadfence();  // every split's partial is visible to this CTA
+        if (tid == 0) sk.counters[tile] = 0u;
+        // Sum the slots in split order, QC float4 of each slot in flight at
+        // once (one L2 round trip per slot and chunk, not per float4).
+        constexpr int QC = Q < 16 ? Q : 16;
+        const size_t sstride = static_cast<size_t>(Q) * kThreads;
+#pragma unroll
+        for (int qc = 0; qc < Q; qc += QC) {
+            float4 o[QC];
+#pragma unroll
+            for (int u = 0; u < QC; ++u) o[u] = __ldcg(&slots[(qc + u) * kThreads + tid]);
+            for (int sp = 1; sp < sk.splits; ++sp) {
+                const float4 *src = slots + sp * sstride;
+                float4 v[QC];
+#pragma unroll
+                for (int u = 0; u < QC; ++u) v[u] = __ldcg(&src[(qc + u) * kThreads + tid]);
+#pragma unroll
+                for (int u = 0; u < QC; ++u) {
+                    o[u].x += v[u].x;
+                    o[u].y += v[u].y;
+                    o[u].z += v[u].z;
+                    o[u].w += v[u].w;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < QC; ++u) {
+                const int q = qc + u, r = q / (TN / 4), gj = q % (TN / 4);
+                const int m = m0 + (r / 4) * (BM / RM) + ty * 4 + (r % 4);
+                if (m >= M) continue;
+                float *crow = C + static_cast<size_t>(m) * N;
+                const int n = n0 + gj * (BN / RN) + tx * 4;
+                float4 w = o[u];
+                if (VEC) {
+                    if (n < N) {
+                        if (beta != 0.f) {
+                            const float4 c = *reinterpret_cast<const float4 *>(crow + n);
+                            w.x = fmaf(beta, c.x, w.x);
+                            w.y = fmaf(beta, c.y, w.y);
+                            w.z = fmaf(beta, c.z, w.z);
+                            w.w = fmaf(beta, c.w, w.w);
+                        }
+                        *reinterpret_cast<float4 *>(crow + n) = w;
+                    }
+                } else {
+                    const float ov[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        if (n + j < N) crow[n + j] = beta != 0.f ? fmaf(beta, crow[n + j], ov[j]) : ov[j];
+                }
+            }
+        }
+        return;
+    }
 
 #pragma unroll
     for (int gi = 0; gi < RM; ++gi) {
@@ -215,19 +309,88 @@ __global__ void scale_kernel(float *C, size_t count, float beta) {
         C[i] = (beta == 0.f) ? 0.f : beta * C[i];
 }
 
+// Split-K workspace of one (device, stream): partial slots and per-tile
+// counters (zeroed once; every launch leaves them zero), grown on demand.
+// Calls on one stream run in order, so a stream has one user at a time.
+struct SgWorkspace {
+    float *ws = nullptr;
+    unsigned *counters = nullptr;
+    size_t ws_bytes = 0;
+    int tiles = 0;
+};
+
+int sg_workspace(cudaStream_t stream, size_t ws_bytes, int tiles, bool capturing, SgWorkspace **out,
+                 std::string &err) {
+    static std::mutex mu;
+    static std::map<std::pair<int, cudaStream_t>, SgWorkspace> cache;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        err = std::string("cudaGetDevice: ") + cudaGetErrorString(e);
+        return GEMM_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    SgWorkspace &w = cache[{dev, stream}];
+    if (w.ws_bytes >= ws_bytes && w.tiles >= tiles) {
+        *out = &w;
+        return GEMM_OK;
+    }
+    *out = nullptr;
+    if (capturing) return GEMM_OK;  // no allocation inside a graph capture: do not split
+    // The stream may still be running a launch that uses the old buffers.
+    e = cudaStreamSynchronize(stream);
+    if (e == cudaSuccess && w.ws) e = cudaFree(w.ws);
+    if (e == cudaSuccess && w.counters) e = cudaFree(w.counters);
+    w = SgWorkspace{};
+    const size_t bytes = ws_bytes > 0 ? ws_bytes : 16;
+    if (e == cudaSuccess) e = cudaMalloc(&w.ws, bytes);
+    if (e == cudaSuccess) e = cudaMalloc(&w.counters, static_cast<size_t>(tiles) * sizeof(unsigned));
+    if (e == cudaSuccess) e = cudaMemset(w.counters, 0, static_cast<size_t>(tiles) * sizeof(unsigned));
+    if (e != cudaSuccess) {
+        err = std::string("sgemm split-K workspace: ") + cudaGetErrorString(e);
+        return GEMM_ERR_CUDA;
+    }
+    w.ws_bytes = bytes;
+    w.tiles = tiles;
+    *out = &w;
+    return GEMM_OK;
+}
+
 template <int BM, int BN, int BK, int TM, int TN, int STAGES, int MINB = 2>
 int launch_pipe(const SgemmLaunch &L, std::string &err) {
-    const dim3 grid((L.N + BN - 1) / BN, (L.M + BM - 1) / BM);
+    dim3 grid((L.N + BN - 1) / BN, (L.M + BM - 1) / BM);
+    // Split-K as planned by the caller: blockIdx.z picks a K share.
+    static_assert(BK == 16, "sgemm_split_chunk rounds shares to 16-deep slices");
+    SplitK sk{1, L.K, nullptr, nullptr};
+    const int tiles = static_cast<int>(grid.x * grid.y);
+    int kchunk = L.K;
+    const int splits = sgemm_split_chunk(L.K, L.splits, &kchunk);
+    if (splits > 1) {
+        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+        cudaError_t e = cudaStreamIsCapturing(L.stream, &cap);
+        if (e != cudaSuccess) {
+            err = std::string("cudaStreamIsCapturing: ") + cudaGetErrorString(e);
+            return GEMM_ERR_CUDA;
+        }
+        SgWorkspace *w = nullptr;
+        const size_t need = static_cast<size_t>(tiles) * splits * BM * BN * sizeof(float);
+        const int st = sg_workspace(L.stream, need, tiles, cap != cudaStreamCaptureStatusNone, &w, err);
+        if (st != GEMM_OK) return st;
+        if (w) {  // null under capture when the workspace would have to grow: no split
+            sk = SplitK{splits, kchunk, w->ws, w->counters};
+            grid.z = splits;
+        }
+    }
     const bool vec = (L.K % 4 == 0) && (L.N % 4 == 0) &&
                      ((reinterpret_cast<uintptr_t>(L.A) | reinterpret_cast<uintptr_t>(L.B) |
                        reinterpret_cast<uintptr_t>(L.C)) & 15u) == 0;
     constexpr int threads = sgemm_threads<BM, BN, TM, TN>();
     if (vec)
         sgemm_pipe_kernel<BM, BN, BK, TM, TN, STAGES, MINB, true><<<grid, threads, 0, L.stream>>>(
-            L.M, L.N, L.K, L.alpha, L.A, L.B, L.beta, L.C);
+            L.M, L.N, L.K, L.alpha, L.A, L.B, L.beta, L.C, sk);
     else
         sgemm_pipe_kernel<BM, BN, BK, TM, TN, STAGES, MINB, false><<<grid, threads, 0, L.stream>>>(
-            L.M, L.N, L.K, L.alpha, L.A, L.B, L.beta, L.C);
+            L.M, L.N, L.K, L.alpha, L.A, L.B, L.beta, L.C, sk);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         err = std::string("sgemm kernel launch: ") + cudaGetErrorString(e);

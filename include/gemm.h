@@ -335,9 +335,19 @@ size_t gemm_nvfp4_scale_bytes(int rows, int K);
  * GEMM_ERR_UNSUPPORTED. */
 int gemm_nvfp4_pack_scales(int rows, int K, const void *plain, void *blocked, gemm_stream_t stream);
 
-/* One kernel configuration of the SGEMM path. */
+/* One kernel configuration of the SGEMM path.  splits: how many CTAs share
+ * each tile's K (split-K, "第 6 章 · Shared Memory & Tile", section "6.5.6
+ * Split-K / Stream-K"): 0 = the library's choice (gemm_sgemm_select), 1 =
+ * never, 2..8 = that many (each share at least 64 deep, so fewer when K is
+ * short).  variant 0 with splits n picks the tile for that split count.
+ * The last CTA of a tile adds the
+ * shares in a fixed order, so results do not depend on timing.  The partials
+ * live in a workspace allocated once per device and stream (the first call
+ * that splits) and kept; under stream capture a split that would need it is
+ * not taken. */
 typedef struct {
     int variant;
+    int splits;
 } gemm_sgemm_config;
 
 enum {
@@ -347,7 +357,12 @@ enum {
     GEMM_SGEMM_NUM_VARIANTS = 3
 };
 
-/* Shape-keyed choice of the SGEMM tile (host logic only). */
+/* Shape-keyed choice of the SGEMM tile and split count (host logic only):
+ * the pair with the lowest predicted time, where a launch takes as long as
+ * its busiest SM (ceil(CTAs / sm_count) CTAs, each over its K share) plus the
+ * cost of adding the split partials.  Splits are only considered when the
+ * tiles number at most 2 * sm_count.  Fills cfg->variant and cfg->splits
+ * (>= 1). */
 int gemm_sgemm_select(int M, int N, int K, int sm_count, gemm_sgemm_config *cfg);
 
 /* sgemm with an explicit configuration (NULL or AUTO = selector's choice). */

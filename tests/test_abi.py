@@ -179,9 +179,31 @@ def test_f16_selector(lib):
 
 
 def test_sgemm_selector(lib):
-    assert g.gemm_sgemm_select(4096, 4096, 4096, 152) == g.GEMM_SGEMM_128x128
-    assert g.gemm_sgemm_select(1024, 1024, 1024, 152) == g.GEMM_SGEMM_64x64
-    assert g.gemm_sgemm_select(256, 256, 256, 152) == g.GEMM_SGEMM_64x64
+    sel = g.gemm_sgemm_select
+    # many tiles: the 128 x 128 tile, unsplit
+    assert sel(4096, 4096, 4096, 152) == (g.GEMM_SGEMM_128x128, 1)
+    assert sel(3000, 3000, 3000, 152) == (g.GEMM_SGEMM_128x128, 1)
+    # shapes where the GB300 sweep of every (tile, splits) pair had a clear winner
+    assert sel(2048, 2048, 2048, 152) == (g.GEMM_SGEMM_128x128, 4)   # 256 tiles: 4 splits even the waves
+    assert sel(512, 512, 8192, 152) == (g.GEMM_SGEMM_128x128, 8)
+    assert sel(256, 256, 4096, 152) == (g.GEMM_SGEMM_64x64, 8)
+    assert sel(1536, 1536, 1536, 152)[1] == 1                       # 144 tiles: one wave already
+    # no K: nothing to split
+    assert sel(4096, 4096, 0, 152)[1] == 1
+    assert sel(16, 16, 16, 152)[1] == 1
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (100, 100, 64), (1024, 1024, 256), (64, 4096, 4096),
+                                   (8192, 64, 1024), (128, 128, 65536), (777, 333, 5000)])
+@pytest.mark.parametrize("sms", [1, 148, 152])
+def test_sgemm_selector_plans_are_valid(lib, M, N, K, sms):
+    variant, splits = g.gemm_sgemm_select(M, N, K, sms)
+    assert variant in (g.GEMM_SGEMM_128x128, g.GEMM_SGEMM_64x64)
+    assert 1 <= splits <= 8
+    # each share of K is at least 64 deep, and splits only come with few tiles
+    assert splits == 1 or splits <= -(-K // 64)
+    bm = 128 if variant == g.GEMM_SGEMM_128x128 else 64
+    assert splits == 1 or -(-M // bm) * -(-N // bm) <= 2 * sms
 
 
 def test_product_path_never_imports_the_oracle():

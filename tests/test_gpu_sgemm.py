@@ -23,7 +23,7 @@ def _lib():
     torch.cuda.init()
 
 
-def _run(A, B, C0, alpha, beta, variant=g.GEMM_SGEMM_AUTO, pad=64):
+def _run(A, B, C0, alpha, beta, variant=g.GEMM_SGEMM_AUTO, pad=64, splits=0):
     M, K = A.shape
     N = B.shape[1]
     dA, dB = A.cuda(), B.cuda()
@@ -32,7 +32,7 @@ def _run(A, B, C0, alpha, beta, variant=g.GEMM_SGEMM_AUTO, pad=64):
     if C0 is not None:
         C.copy_(C0.cuda())
     g.sgemm_ex(M, N, K, alpha, dA.data_ptr(), dB.data_ptr(), beta, C.data_ptr(),
-               torch.cuda.current_stream().cuda_stream, variant)
+               torch.cuda.current_stream().cuda_stream, variant, splits)
     torch.cuda.synchronize()
     host = buf.cpu().numpy()
     assert np.all(host[:pad] == -7.25) and np.all(host[pad + M * N:] == -7.25), "wrote outside C"
@@ -127,3 +127,82 @@ def test_sgemm_tensor_wrapper():
     g.sgemm_(A, B, C)
     Cref, S = oracle.sgemm(A.cpu(), B.cpu())
     check_sgemm(C.cpu().numpy(), Cref, S, what="wrapper")
+
+
+V1, V2 = g.GEMM_SGEMM_128x128, g.GEMM_SGEMM_64x64
+
+
+@pytest.mark.parametrize("M,N,K,alpha,beta,variant,splits", [
+    (1024, 1024, 1024, 1.0, 0.5, V1, 4),    # the 1024-cube size with a beta term: 64 tiles
+    (1024, 1024, 1024, 1.0, 0.5, 0, 0),     # the library's own plan for it
+    (300, 200, 1000, -2.0, 0.25, V1, 8),    # 6 ragged tiles, a partial last share
+    (130, 260, 4100, 0.5, 0.0, V1, 0),      # K not a multiple of 4: the element-wise loads
+    (128, 128, 65536, 1.0, 1.0, V1, 8),     # one tile, 8 shares of 8192
+    (200, 150, 3000, 1.0, 0.5, V2, 6),      # the 64 x 64 tile, ragged
+    (64, 1024, 4096, 1.5, 0.0, V2, 7),      # skinny M
+    (96, 80, 150, 1.0, 1.0, V1, 8),         # short K: 8 requested, 3 shares of >= 64
+    (256, 256, 4096, 1.0, 0.0, 0, 0),
+])
+def test_sgemm_split_k(M, N, K, alpha, beta, variant, splits):
+    # Each tile's K is shared over several CTAs; the last to finish adds the
+    # partials in split order and applies beta * C.  Three calls on one
+    # stream: the per-tile counters reset.
+    A = wl.draw_f32((M, K), seed=M + 11)
+    B = wl.draw_f32((K, N), seed=N + 12)
+    C0 = wl.draw_f32((M, N), seed=13)
+    Cref, S = oracle.sgemm(A, B, alpha, beta, C0)
+    for rep in range(3):
+        C = _run(A, B, C0, alpha, beta, variant, splits=splits)
+        check_sgemm(C, Cref, S, beta_c0=beta * C0.numpy().astype(np.float64),
+                    what=f"split-K {M}x{N}x{K} v{variant} s{splits} rep {rep}")
+
+
+def test_sgemm_split_k_matches_unsplit_within_rounding():
+    # The same product with 1..8 shares: every result within the bound of the
+    # oracle, and 1 share gives the plain kernel's bits.
+    M, N, K = 256, 192, 2048
+    A = wl.draw_f32((M, K), seed=41)
+    B = wl.draw_f32((K, N), seed=42)
+    Cref, S = oracle.sgemm(A, B, 1.0, 0.0, None)
+    for v in (V1, V2):
+        plain = _run(A, B, None, 1.0, 0.0, v, splits=1)
+        for sp in range(1, 9):
+            C = _run(A, B, None, 1.0, 0.0, v, splits=sp)
+            check_sgemm(C, Cref, S, what=f"v{v} splits {sp}")
+            if sp == 1:
+                assert np.array_equal(C, plain)
+
+
+def test_sgemm_split_k_beta_zero_ignores_nan_c_and_is_deterministic():
+    M, N, K = 256, 384, 2048
+    A = wl.draw_f32((M, K), seed=21)
+    B = wl.draw_f32((K, N), seed=22)
+    dA, dB = A.cuda(), B.cuda()
+    outs = []
+    for _ in range(2):
+        C = torch.full((M, N), float("nan"), device="cuda")
+        g.sgemm(M, N, K, 1.0, dA.data_ptr(), dB.data_ptr(), 0.0, C.data_ptr(), 0)
+        torch.cuda.synchronize()
+        outs.append(C.cpu().numpy())
+    Cref, S = oracle.sgemm(A, B, 1.0, 0.0, None)
+    check_sgemm(outs[0], Cref, S, what="split-K beta 0")
+    assert np.array_equal(outs[0], outs[1]), "split-K partials must add in a fixed order"
+
+
+def test_sgemm_split_k_under_graph_capture():
+    # Inside a capture the workspace cannot be allocated; a stream that has
+    # one already splits, a fresh stream runs unsplit.  Either way: correct.
+    M, N, K = 512, 512, 2048
+    A = wl.draw_f32((M, K), seed=31)
+    B = wl.draw_f32((K, N), seed=32)
+    dA, dB = A.cuda(), B.cuda()
+    Cref, S = oracle.sgemm(A, B, 1.0, 0.0, None)
+    s = torch.cuda.Stream()
+    C = torch.zeros((M, N), device="cuda")
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        g.sgemm(M, N, K, 1.0, dA.data_ptr(), dB.data_ptr(), 0.0, C.data_ptr(), s.cuda_stream)
+    graph.replay()
+    graph.replay()
+    torch.cuda.synchronize()
+    check_sgemm(C.cpu().numpy(), Cref, S, what="captured")
