@@ -58,6 +58,9 @@ METRIC = "TFLOP/s (2MNK/t) fp16 NT GEMM 5376x5376x2048 on 1 GB300; % of dense FP
 ROTATE = 4
 FALLBACK_TENSOR_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
+# The sources of the fp16 NT kernels; the profiled traffic holds only while
+# their hash matches (gemm_blockscaled.cuh, also compiled in gemm_f16_nt.cu's
+# unit, holds none of their code).
 KERNEL_SOURCES = ["dense_gemm_fp16_gb300/csrc/gemm_f16_nt.cu",
                   "dense_gemm_fp16_gb300/csrc/sm103_ptx.cuh",
                   "dense_gemm_fp16_gb300/csrc/epilogue.cuh"]
