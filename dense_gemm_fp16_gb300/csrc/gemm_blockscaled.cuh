@@ -71,14 +71,17 @@ struct MxArgs {
 // EW epilogue warps: 4 (one per TMEM lane quarter, the tile through the
 // staged TMA-store epilogue) or 8 (two per quarter, each reading its half of
 // the columns into registers and releasing the accumulator before it
-// converts and stores them with 16-byte stores: with one accumulator, the
-// next tile's MMAs wait only for the TMEM reads).
+// converts and stores them: with one accumulator, the next tile's MMAs wait
+// only for the TMEM reads).  With EW = 8, EBUFS = 1 stores 32 x 32 halves at
+// a time through a 2 KB buffer per warp and one TMA store (coalesced), and
+// EBUFS = 0 stores each lane's row with 16-byte stores.
 template <int BN, int STAGES, int EBUFS, int ACC, int FMT = kFmtMx8, int EW = 4>
 __global__ void __launch_bounds__((2 + EW) * 32, 1)
     gemm_mxfp8_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                          const __grid_constant__ CUtensorMap tmC, const F16Args args, const MxArgs mx) {
     using T = MxCfg<BN, STAGES, EBUFS, ACC, FMT>;
-    static_assert(EW == 4 || (EW == 8 && EBUFS == 0), "the 8-warp epilogue stores from registers");
+    static_assert(EW == 4 || (EW == 8 && (EBUFS == 0 || EBUFS == 1)),
+                  "the 8-warp epilogue stores from registers, directly or through 2 KB per warp");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -282,7 +285,8 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
             if (lane == 0) mbar_arrive(acce_bar(b));
             const int mt = tile % args.m_tiles;
             const int nt = tile / args.m_tiles;
-            const int m = mt * kBM + quarter * 32 + lane;
+            const int row0 = mt * kBM + quarter * 32;
+            const int m = row0 + lane;
             const int n0 = nt * BN + half * kHalf;
             if constexpr (FMT == kFmtNv4) {
                 // C = alpha * (the block-scaled product)
@@ -290,12 +294,46 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
 #pragma unroll
                 for (int q = 0; q < kHalf / 8; ++q) epi_apply8<0>(args.epi, &v[8 * q], zero, zero);
             }
-            __half *crow = args.C + static_cast<size_t>(m) * args.N;
+            if (EBUFS > 0 && args.tma_store) {
+                // 32 x 32 halves at a time through this warp's 2 KB buffer and
+                // one TMA store: row `lane` is 64 bytes, its 16-byte chunk j
+                // at chunk j ^ ((lane / 2) % 4) -- the TMA's 64-byte swizzle,
+                // under which every 8 lanes' stores cover all 32 banks.
+                const uint32_t buf = sbase + T::kEpiOffset + static_cast<uint32_t>(warp - 2) * 2048u;
+                const uint32_t row_addr = buf + static_cast<uint32_t>(lane) * 64u;
 #pragma unroll
-            for (int c = 0; c < kHalf / 32; ++c)
-                store_row_chunk(crow, m < args.M, n0 + 32 * c, args.N, args.vec_store,
-                                *reinterpret_cast<const uint32_t(*)[32]>(&v[32 * c]));
+                for (int c = 0; c < kHalf / 32; ++c) {
+                    if (lane == 0) bulk_wait_group_read<0>();  // the last store has read the buffer
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const uint32_t *p = &v[32 * c + 8 * j];
+                        __half2 h0 = __floats2half2_rn(__uint_as_float(p[0]), __uint_as_float(p[1]));
+                        __half2 h1 = __floats2half2_rn(__uint_as_float(p[2]), __uint_as_float(p[3]));
+                        __half2 h2 = __floats2half2_rn(__uint_as_float(p[4]), __uint_as_float(p[5]));
+                        __half2 h3 = __floats2half2_rn(__uint_as_float(p[6]), __uint_as_float(p[7]));
+                        st_shared_v4(row_addr + (static_cast<uint32_t>(j ^ ((lane >> 1) & 3)) << 4),
+                                     *reinterpret_cast<uint32_t *>(&h0), *reinterpret_cast<uint32_t *>(&h1),
+                                     *reinterpret_cast<uint32_t *>(&h2), *reinterpret_cast<uint32_t *>(&h3));
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        // a box wholly past the last row or column would store nothing
+                        if (row0 < args.M && n0 + 32 * c < args.N) tma_store_2d(&tmC, buf, n0 + 32 * c, row0);
+                        bulk_commit_group();
+                    }
+                }
+            } else {
+                __half *crow = args.C + static_cast<size_t>(m) * args.N;
+#pragma unroll
+                for (int c = 0; c < kHalf / 32; ++c)
+                    store_row_chunk(crow, m < args.M, n0 + 32 * c, args.N, args.vec_store,
+                                    *reinterpret_cast<const uint32_t(*)[32]>(&v[32 * c]));
+            }
         }
+        if (lane == 0) bulk_wait_group_all();
+        __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue
         const int quarter = warp & 3;
@@ -760,7 +798,12 @@ int mx_launch_1cta(const MxLaunch &L, std::string &err) {
     args.sk_ws = nullptr;
     args.sk_flags = nullptr;
     args.seq = 0;
-    if (args.tma_store && !encode_half_map(&tmC, L.C, L.M, L.N, 32, 64, err)) return GEMM_ERR_CUDA;
+    // C boxes: 32 rows x 64 columns (128-byte swizzle) for the 4-warp staged
+    // epilogue, 32 x 32 (64-byte swizzle) for the 8-warp one
+    if (args.tma_store && !encode_map(&tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, L.C, L.M, L.N, 32,
+                                      EW == 8 ? 32 : 64, err,
+                                      EW == 8 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B))
+        return GEMM_ERR_CUDA;
     MxArgs mx{static_cast<const uint8_t *>(L.SFA), static_cast<const uint8_t *>(L.SFB)};
     const int tiles = args.m_tiles * args.n_tiles;
     int grid = L.grid > 0 ? L.grid : L.sm_count;
@@ -787,20 +830,24 @@ int mx_launch_1cta(const MxLaunch &L, std::string &err) {
 
 int mx_launch(const MxLaunch &L, std::string &err) {
     if (L.fmt == kFmtNv4) {
-        // 128 x 256: the 8-warp register epilogue (no staging buffers, so a
-        // fourth stage fits): measured 40.2 against 50.4 us with 4 warps and
-        // 3 stages at 5376 x 5376 x 2048, 118 against 132 at K = 8192.
+        // 128 x 256: the 8-warp register epilogue staging through 2 KB per
+        // warp, 3 stages: 38.8 us at 5376 x 5376 x 2048 (direct 16-byte
+        // stores with 4 stages: 40.3; the 4-warp staged epilogue: 50.4), 118
+        // at K = 8192 like the direct form.
         switch (L.variant) {
-            case 3: return mx_launch_1cta<256, 4, 0, 1, kFmtNv4, 8>(L, err);
+            case 3: return mx_launch_1cta<256, 3, 1, 1, kFmtNv4, 8>(L, err);
             case 1: return mx_launch_1cta<128, kMxStages, 2, 2, kFmtNv4>(L, err);
             default: err = "the NVFP4 product has the 1-CTA kernels only"; return GEMM_ERR_UNSUPPORTED;
         }
     }
     switch (L.variant) {
         case 2: return mx_launch_pair<128, 7, 2, 2>(L, err);
-        // 128 x 256: the 4-warp staged epilogue (the 8-warp register one
-        // measured equal at K = 2048 and 5 % slower at K = 8192).
-        case 3: return mx_launch_1cta<256, 4, 1, 1>(L, err);
+        // 128 x 256: the 8-warp register epilogue staging through 2 KB per
+        // warp: 46.1 us at 5376 x 5376 x 2048 against 52.0 for the 4-warp
+        // staged one (whose single accumulator waits for the whole drain) and
+        // 52 for direct 16-byte stores (uncoalesced, one row per lane); equal
+        // within the spread at K = 8192.
+        case 3: return mx_launch_1cta<256, 4, 1, 1, kFmtMx8, 8>(L, err);
         case 4: return mx_launch_pair<256, 6, 1, 1>(L, err);
         default: return mx_launch_1cta<128, kMxStages, 2, 2>(L, err);
     }
