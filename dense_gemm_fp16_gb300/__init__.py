@@ -39,6 +39,7 @@ from ._binding import (  # noqa: F401
     GEMM_MXFP8_128x256,
     GEMM_MXFP8_256x128_PAIR,
     GEMM_MXFP8_256x256_PAIR,
+    GEMM_MXFP8_NUM_VARIANTS,
     GEMM_MXFP8_AUTO,
     GEMM_OK,
     GEMM_SGEMM_64x64,

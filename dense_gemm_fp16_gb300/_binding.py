@@ -23,7 +23,7 @@ GEMM_F16_AUTO, GEMM_F16_128x256, GEMM_F16_128x128, GEMM_F16_256x256_PAIR, GEMM_F
 GEMM_SGEMM_AUTO, GEMM_SGEMM_128x128, GEMM_SGEMM_64x64 = 0, 1, 2
 GEMM_F16_FLAG_STREAM_K = 1
 GEMM_MXFP8_AUTO, GEMM_MXFP8_128x128, GEMM_MXFP8_256x128_PAIR, GEMM_MXFP8_128x256 = 0, 1, 2, 3
-GEMM_MXFP8_256x256_PAIR = 4
+GEMM_MXFP8_256x256_PAIR, GEMM_MXFP8_NUM_VARIANTS = 4, 5
 GEMM_ACT_NONE, GEMM_ACT_RELU, GEMM_ACT_SILU, GEMM_ACT_GELU_TANH = 0, 1, 2, 3
 ACTIVATIONS = {"none": GEMM_ACT_NONE, "relu": GEMM_ACT_RELU, "silu": GEMM_ACT_SILU,
                "gelu_tanh": GEMM_ACT_GELU_TANH}

@@ -386,10 +386,9 @@ int gemm_nvfp4_pack_scales(int rows, int K, const void *plain, void *blocked, ge
 int gemm_nvfp4_nt_ex(int M, int N, int K, const void *A, const void *SFA, const void *B,
                      const void *SFB, float alpha, void *C, gemm_stream_t stream,
                      const gemm_mxfp8_config *cfg) {
-    if (cfg && (cfg->grid < 0 || (cfg->variant != GEMM_MXFP8_AUTO && cfg->variant != GEMM_MXFP8_128x128 &&
-                                  cfg->variant != GEMM_MXFP8_128x256)))
-        return fail(GEMM_ERR_INVALID_ARG, "gemm_nvfp4_nt_ex: bad config variant=%d grid=%d (the 1-CTA "
-                    "128x128 and 128x256 kernels only)", cfg->variant, cfg->grid);
+    if (cfg && (cfg->grid < 0 || cfg->variant < 0 || cfg->variant >= GEMM_MXFP8_NUM_VARIANTS))
+        return fail(GEMM_ERR_INVALID_ARG, "gemm_nvfp4_nt_ex: bad config variant=%d grid=%d", cfg->variant,
+                    cfg->grid);
     if (M < 0 || N < 0 || K < 0)
         return fail(GEMM_ERR_INVALID_ARG, "gemm_nvfp4_nt: negative size M=%d N=%d K=%d", M, N, K);
     if (M == 0 || N == 0) return GEMM_OK;

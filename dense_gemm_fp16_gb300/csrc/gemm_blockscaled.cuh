@@ -48,14 +48,18 @@ struct MxCfg {
     static constexpr int kSfbChunks = BN / 128;                 // B's 128-row tiles
     static constexpr int kCpt = FMT == kFmtNv4 ? 4 : 1;         // chunks per row tile per k-block
     static constexpr int kSfBytes = (1 + kSfbChunks) * kCpt * kMxSfChunk;
-    static constexpr int kStageBytes = (kABytes + kBBytes + kSfBytes + 1023) / 1024 * 1024;
+    // operand stages (whole 1 KB multiples: the 128-byte swizzle), then each
+    // stage's scale chunks, then the epilogue buffers
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kSfOffset = STAGES * kStageBytes;
     static constexpr int kTmemCols = 512;  // accumulators, then the scale columns of each stage
     static constexpr int kSfCols = 4 * (1 + kSfbChunks) * kCpt;
     static constexpr int kSfCol0 = ACC * BN;
     static constexpr int kNumBars = 2 * STAGES + 5;
-    static constexpr int kEpiOffset = STAGES * kStageBytes;
+    static constexpr int kEpiOffset = (kSfOffset + STAGES * kSfBytes + 1023) / 1024 * 1024;
     static constexpr int kBarOffset = kEpiOffset + 4 * EBUFS * kEpiBufBytes;
     static constexpr int kSmemBytes = 1024 + kBarOffset + kNumBars * 8 + 16;
+    static_assert(kStageBytes % 1024 == 0, "stages keep the 1 KB alignment of the swizzled boxes");
     static_assert(BN == 128 || BN == 256, "B's scales come in whole 128-row chunks");
     static_assert(ACC == 1 || ACC == 2, "one or two accumulators");
     static_assert(FMT == kFmtMx8 || FMT == kFmtNv4, "MXFP8 or NVFP4");
@@ -67,6 +71,69 @@ struct MxArgs {
     const uint8_t *sfa;  // scale chunks of A: [ceil(M/128)][ceil(K/128)][512]
     const uint8_t *sfb;  // scale chunks of B: [ceil(N/128)][ceil(K/128)][512]
 };
+
+// The CTA-pair form of the NVFP4 MMA (issued by the even CTA for both).
+__device__ __forceinline__ void mma_nvf4_ss_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                 uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                 uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// Stores of the 8-warp epilogue: KH accumulator columns (fp32 bits in v) of
+// output row row0 + lane from column n0 on, rounded to half (NVFP4: times
+// alpha first).  STAGED, and when C allows TMA stores, 32 x 32 halves at a
+// time go through the warp's 2 KB buffer `buf` and one TMA store: row `lane`
+// is 64 bytes, its 16-byte chunk j at chunk j ^ ((lane / 2) % 4) -- the TMA's
+// 64-byte swizzle, under which every 8 lanes' stores cover all 32 banks.
+// Otherwise each lane stores its own row with 16-byte stores.
+template <int KH, int FMT, bool STAGED>
+__device__ __forceinline__ void mx_epi8_store(const F16Args &args, const CUtensorMap *tmC, uint32_t (&v)[KH],
+                                              int row0, int n0, int lane, uint32_t buf) {
+    if constexpr (FMT == kFmtNv4) {
+        const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int q = 0; q < KH / 8; ++q) epi_apply8<0>(args.epi, &v[8 * q], zero, zero);
+    }
+    if (STAGED && args.tma_store) {
+        const uint32_t row_addr = buf + static_cast<uint32_t>(lane) * 64u;
+#pragma unroll
+        for (int c = 0; c < KH / 32; ++c) {
+            if (lane == 0) bulk_wait_group_read<0>();  // the last store has read the buffer
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t *p = &v[32 * c + 8 * j];
+                __half2 h0 = __floats2half2_rn(__uint_as_float(p[0]), __uint_as_float(p[1]));
+                __half2 h1 = __floats2half2_rn(__uint_as_float(p[2]), __uint_as_float(p[3]));
+                __half2 h2 = __floats2half2_rn(__uint_as_float(p[4]), __uint_as_float(p[5]));
+                __half2 h3 = __floats2half2_rn(__uint_as_float(p[6]), __uint_as_float(p[7]));
+                st_shared_v4(row_addr + (static_cast<uint32_t>(j ^ ((lane >> 1) & 3)) << 4),
+                             *reinterpret_cast<uint32_t *>(&h0), *reinterpret_cast<uint32_t *>(&h1),
+                             *reinterpret_cast<uint32_t *>(&h2), *reinterpret_cast<uint32_t *>(&h3));
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                // a box wholly past the last row or column would store nothing
+                if (row0 < args.M && n0 + 32 * c < args.N) tma_store_2d(tmC, buf, n0 + 32 * c, row0);
+                bulk_commit_group();
+            }
+        }
+    } else {
+        const int m = row0 + lane;
+        __half *crow = args.C + static_cast<size_t>(m) * args.N;
+#pragma unroll
+        for (int c = 0; c < KH / 32; ++c)
+            store_row_chunk(crow, m < args.M, n0 + 32 * c, args.N, args.vec_store,
+                            *reinterpret_cast<const uint32_t(*)[32]>(&v[32 * c]));
+    }
+}
 
 // EW epilogue warps: 4 (one per TMEM lane quarter, the tile through the
 // staged TMA-store epilogue) or 8 (two per quarter, each reading its half of
@@ -149,7 +216,7 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
                     }
                     const uint32_t sa = sbase + stage * T::kStageBytes;
                     const uint32_t sb = sa + T::kABytes;
-                    const uint32_t ssf = sb + T::kBBytes;
+                    const uint32_t ssf = sbase + T::kSfOffset + stage * T::kSfBytes;
                     // the k-block's scale chunks: kCpt consecutive chunks per
                     // 128-row tile; B's row tiles past N do not exist in the
                     // scale array and are not fetched (their stale values meet
@@ -205,7 +272,7 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
                     tc_fence_after_sync();
                     const uint32_t sa = sbase + stage * T::kStageBytes;
                     const uint32_t sb = sa + T::kABytes;
-                    const uint32_t ssf = sb + T::kBBytes;
+                    const uint32_t ssf = sbase + T::kSfOffset + stage * T::kSfBytes;
                     // Each chunk is 32 rows of 16 bytes (8-row core matrices 128
                     // bytes apart) and fills 4 TMEM columns.  A's chunk a lands at
                     // sfa + 4a; B's chunk a of row tile c at sfb + 4(a * tiles + c),
@@ -285,52 +352,8 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
             if (lane == 0) mbar_arrive(acce_bar(b));
             const int mt = tile % args.m_tiles;
             const int nt = tile / args.m_tiles;
-            const int row0 = mt * kBM + quarter * 32;
-            const int m = row0 + lane;
-            const int n0 = nt * BN + half * kHalf;
-            if constexpr (FMT == kFmtNv4) {
-                // C = alpha * (the block-scaled product)
-                const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-                for (int q = 0; q < kHalf / 8; ++q) epi_apply8<0>(args.epi, &v[8 * q], zero, zero);
-            }
-            if (EBUFS > 0 && args.tma_store) {
-                // 32 x 32 halves at a time through this warp's 2 KB buffer and
-                // one TMA store: row `lane` is 64 bytes, its 16-byte chunk j
-                // at chunk j ^ ((lane / 2) % 4) -- the TMA's 64-byte swizzle,
-                // under which every 8 lanes' stores cover all 32 banks.
-                const uint32_t buf = sbase + T::kEpiOffset + static_cast<uint32_t>(warp - 2) * 2048u;
-                const uint32_t row_addr = buf + static_cast<uint32_t>(lane) * 64u;
-#pragma unroll
-                for (int c = 0; c < kHalf / 32; ++c) {
-                    if (lane == 0) bulk_wait_group_read<0>();  // the last store has read the buffer
-                    __syncwarp();
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const uint32_t *p = &v[32 * c + 8 * j];
-                        __half2 h0 = __floats2half2_rn(__uint_as_float(p[0]), __uint_as_float(p[1]));
-                        __half2 h1 = __floats2half2_rn(__uint_as_float(p[2]), __uint_as_float(p[3]));
-                        __half2 h2 = __floats2half2_rn(__uint_as_float(p[4]), __uint_as_float(p[5]));
-                        __half2 h3 = __floats2half2_rn(__uint_as_float(p[6]), __uint_as_float(p[7]));
-                        st_shared_v4(row_addr + (static_cast<uint32_t>(j ^ ((lane >> 1) & 3)) << 4),
-                                     *reinterpret_cast<uint32_t *>(&h0), *reinterpret_cast<uint32_t *>(&h1),
-                                     *reinterpret_cast<uint32_t *>(&h2), *reinterpret_cast<uint32_t *>(&h3));
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        // a box wholly past the last row or column would store nothing
-                        if (row0 < args.M && n0 + 32 * c < args.N) tma_store_2d(&tmC, buf, n0 + 32 * c, row0);
-                        bulk_commit_group();
-                    }
-                }
-            } else {
-                __half *crow = args.C + static_cast<size_t>(m) * args.N;
-#pragma unroll
-                for (int c = 0; c < kHalf / 32; ++c)
-                    store_row_chunk(crow, m < args.M, n0 + 32 * c, args.N, args.vec_store,
-                                    *reinterpret_cast<const uint32_t(*)[32]>(&v[32 * c]));
-            }
+            mx_epi8_store<kHalf, FMT, (EBUFS > 0)>(args, &tmC, v, mt * kBM + quarter * 32, nt * BN + half * kHalf,
+                                                  lane, sbase + T::kEpiOffset + static_cast<uint32_t>(warp - 2) * 2048u);
         }
         if (lane == 0) bulk_wait_group_all();
         __syncwarp();
@@ -402,33 +425,42 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
 // the even CTA's barrier.  Barriers and roles as in the fp16 pair kernel.
 // BN: pair tile columns (128 or 256; each CTA loads BN/2 rows of B and all
 // BN/128 scale chunks of B), STAGES, EBUFS epilogue buffers per warp, ACC
-// accumulators.
-template <int BN, int STAGES, int EBUFS, int ACC>
+// accumulators, FMT as in the 1-CTA kernel (NVFP4: four chunks per row tile
+// per k-block, one TMA box of 8 rows), EW epilogue warps per CTA (4: the
+// staged epilogue; 8: the register epilogue that releases the accumulator
+// early, EBUFS = 1).
+template <int BN, int STAGES, int EBUFS, int ACC, int FMT = kFmtMx8>
 struct MxPairCfg {
     static constexpr int kABytes = kBM * kMxBK;             // this CTA's 128 rows of A
     static constexpr int kBBytes = (BN / 2) * kMxBK;        // this CTA's half of B
     static constexpr int kSfbChunks = BN / 128;
-    static constexpr int kSfBytes = (1 + kSfbChunks) * kMxSfChunk;
-    static constexpr int kStageBytes = (kABytes + kBBytes + kSfBytes + 1023) / 1024 * 1024;
+    static constexpr int kCpt = FMT == kFmtNv4 ? 4 : 1;     // chunks per row tile per k-block
+    static constexpr int kSfBytes = (1 + kSfbChunks) * kCpt * kMxSfChunk;
+    // operand stages (whole 1 KB multiples: the 128-byte swizzle), then each
+    // stage's scale chunks, then the epilogue buffers
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kSfOffset = STAGES * kStageBytes;
     static constexpr int kTmemCols = 512;  // accumulators, then the scale columns of each stage
-    static constexpr int kSfCols = 4 * (1 + kSfbChunks);
+    static constexpr int kSfCols = 4 * (1 + kSfbChunks) * kCpt;
     static constexpr int kSfCol0 = ACC * BN;
     static constexpr int kNumBars = 2 * STAGES + 5;
-    static constexpr int kEpiOffset = STAGES * kStageBytes;
+    static constexpr int kEpiOffset = (kSfOffset + STAGES * kSfBytes + 1023) / 1024 * 1024;
     static constexpr int kBarOffset = kEpiOffset + 4 * EBUFS * kEpiBufBytes;
     static constexpr int kSmemBytes = 1024 + kBarOffset + kNumBars * 8 + 16;
+    static_assert(kStageBytes % 1024 == 0, "stages keep the 1 KB alignment of the swizzled boxes");
     static_assert(BN == 128 || BN == 256, "B's scales come in whole 128-row chunks");
     static_assert(kSfCol0 + kSfCols * STAGES <= kTmemCols, "scale columns fit the allocation");
     static_assert(kSmemBytes <= 232448, "fits the 227 KB opt-in limit");
 };
 
-template <int BN, int STAGES, int EBUFS, int ACC>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int BN, int STAGES, int EBUFS, int ACC, int FMT = kFmtMx8, int EW = 4>
+__global__ void __launch_bounds__((2 + EW) * 32, 1)
     gemm_mxfp8_nt_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                               const __grid_constant__ CUtensorMap tmC,
                               const __grid_constant__ CUtensorMap tmSFA,
                               const __grid_constant__ CUtensorMap tmSFB, const F16Args args) {
-    using T = MxPairCfg<BN, STAGES, EBUFS, ACC>;
+    using T = MxPairCfg<BN, STAGES, EBUFS, ACC, FMT>;
+    static_assert(EW == 4 || (EW == 8 && EBUFS == 1), "8 epilogue warps stage through 2 KB each");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -464,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(accf_bar(b), 1);
-            mbar_init(acce_bar(b), 2 * 4);  // every epilogue warp of both CTAs
+            mbar_init(acce_bar(b), 2 * EW);  // every epilogue warp of both CTAs
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
@@ -502,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     const uint32_t sa = sbase + stage * T::kStageBytes;
-                    const uint32_t ssf = sa + T::kABytes + T::kBBytes;
+                    const uint32_t ssf = sbase + T::kSfOffset + stage * T::kSfBytes;
                     const uint32_t full_leader = mapa_shared(full_bar(stage), 0);
                     if (leader) {
                         // both CTAs' operand and scale bytes (the stage's padding is not loaded)
@@ -513,12 +545,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_2d_pair(sa, &tmA, full_leader, kb * kMxBK, a_tile128 * kBM);
                     tma_load_2d_pair(sa + T::kABytes, &tmB, full_leader, kb * kMxBK,
                                      nt * BN + static_cast<int>(rank) * (BN / 2));
-                    // scale chunks: 512 bytes = two 256-byte rows of the 2D view
-                    tma_load_2d_pair(ssf, &tmSFA, full_leader, 0, 2 * (a_tile128 * num_kb + kb));
+                    // scale chunks: 512 bytes = two 256-byte rows of the 2D view;
+                    // the k-block's kCpt chunks of a row tile are contiguous
+                    tma_load_2d_pair(ssf, &tmSFA, full_leader, 0, 2 * T::kCpt * (a_tile128 * num_kb + kb));
 #pragma unroll
                     for (int c = 0; c < T::kSfbChunks; ++c)
-                        tma_load_2d_pair(ssf + (1 + c) * kMxSfChunk, &tmSFB, full_leader, 0,
-                                         2 * ((nt * T::kSfbChunks + c) * num_kb + kb));
+                        tma_load_2d_pair(ssf + (1 + c) * T::kCpt * kMxSfChunk, &tmSFB, full_leader, 0,
+                                         2 * T::kCpt * ((nt * T::kSfbChunks + c) * num_kb + kb));
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -537,6 +570,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
+            // the k-block's scale chunks into this stage's TMEM columns (the
+            // chunk placement of the 1-CTA kernel)
+            auto copy_scales = [&](int st) {
+                const uint32_t ssf = sbase + T::kSfOffset + st * T::kSfBytes;
+                const uint32_t sfa_tmem = tmem_base + static_cast<uint32_t>(T::kSfCol0 + T::kSfCols * st);
+                const uint32_t sfb_tmem = sfa_tmem + 4u * T::kCpt;
+#pragma unroll
+                for (int a = 0; a < T::kCpt; ++a) {
+                    tmem_cp_32x128b_warpx4_pair(sfa_tmem + 4u * a, plain_kmajor_desc(ssf + a * kMxSfChunk, 128, 128));
+#pragma unroll
+                    for (int c = 0; c < T::kSfbChunks; ++c)
+                        tmem_cp_32x128b_warpx4_pair(
+                            sfb_tmem + 4u * (a * T::kSfbChunks + c),
+                            plain_kmajor_desc(ssf + ((1 + c) * T::kCpt + a) * kMxSfChunk, 128, 128));
+                }
+            };
             int i = 0;
             for (int tile = pair; tile < total_tiles; tile += num_pairs, ++i) {
                 const int b = i % ACC;
@@ -553,26 +602,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after_sync();
+                    copy_scales(stage);
                     const uint32_t sa = sbase + stage * T::kStageBytes;
-                    const uint32_t ssf = sa + T::kABytes + T::kBBytes;
                     const uint32_t sfa_tmem = tmem_base + static_cast<uint32_t>(T::kSfCol0 + T::kSfCols * stage);
-                    const uint32_t sfb_tmem = sfa_tmem + 4u;
-                    tmem_cp_32x128b_warpx4_pair(sfa_tmem, plain_kmajor_desc(ssf, 128, 128));
-#pragma unroll
-                    for (int c = 0; c < T::kSfbChunks; ++c)
-                        tmem_cp_32x128b_warpx4_pair(sfb_tmem + 4u * c,
-                                                    plain_kmajor_desc(ssf + (1 + c) * kMxSfChunk, 128, 128));
+                    const uint32_t sfb_tmem = sfa_tmem + 4u * T::kCpt;
                     const uint64_t adesc = sw128_kmajor_desc(sa);
                     const uint64_t bdesc = sw128_kmajor_desc(sa + T::kABytes);
 #pragma unroll
-                    for (int j = 0; j < kMxBK / kMxUmmaK; ++j)
-                        mma_mxf8_ss_pair(d_tmem, adesc + 2u * j, bdesc + 2u * j, idesc_mxf8_e4m3(256, BN, j),
-                                         sfa_tmem, sfb_tmem, (kb > 0 || j > 0) ? 1u : 0u);
-                    mma_commit_pair_multicast(empty_bar(stage), 0x3);
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
+                    for (int j = 0; j < 4; ++j) {
+                        if constexpr (FMT == kFmtMx8)
+                            mma_mxf8_ss_pair(d_tmem, adesc + 2u * j, bdesc + 2u * j, idesc_mxf8_e4m3(256, BN, j),
+                                             sfa_tmem, sfb_tmem, (kb > 0 || j > 0) ? 1u : 0u);
+                        else
+                            mma_nvf4_ss_pair(d_tmem, adesc + 2u * j, bdesc + 2u * j, idesc_nvf4_e2m1(256, BN),
+                                             sfa_tmem + 4u * j, sfb_tmem + 4u * T::kSfbChunks * j,
+                                             (kb > 0 || j > 0) ? 1u : 0u);
                     }
+                    const int nstage = stage + 1 == STAGES ? 0 : stage + 1;
+                    const uint32_t nphase = nstage == 0 ? phase ^ 1u : phase;
+                    mma_commit_pair_multicast(empty_bar(stage), 0x3);
+                    stage = nstage;
+                    phase = nphase;
                 }
                 if (!ok) break;
                 mma_commit_pair_multicast(accf_bar(b), 0x3);
@@ -606,12 +656,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after_sync();
             const int mt = tile % args.m_tiles;
             const int nt = tile / args.m_tiles;
-            epilogue_warp_tile<BN, EBUFS, -1>(args, &tmC, tmem_base + lane_field + static_cast<uint32_t>(b * BN),
-                                          mt * 256 + static_cast<int>(rank) * 128 + quarter * 32, nt * BN,
-                                          lane, stage_smem, step);
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(mapa_shared(acce_bar(b), 0));
+            const int row0 = mt * 256 + static_cast<int>(rank) * 128 + quarter * 32;
+            if constexpr (EW == 8) {
+                // this warp's half of the columns into registers, then the
+                // accumulator goes back to the MMAs before the stores
+                constexpr int kHalf = BN / 2;
+                const int half = (warp - 2) >> 2;
+                uint32_t v[kHalf];
+                const uint32_t taddr = tmem_base + lane_field + static_cast<uint32_t>(b * BN + half * kHalf);
+#pragma unroll
+                for (int c = 0; c < kHalf / 32; ++c)
+                    tmem_load_32cols(taddr + 32u * c, *reinterpret_cast<uint32_t(*)[32]>(&v[32 * c]));
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(mapa_shared(acce_bar(b), 0));
+                mx_epi8_store<kHalf, FMT, true>(args, &tmC, v, row0, nt * BN + half * kHalf, lane,
+                                                sbase + T::kEpiOffset + static_cast<uint32_t>(warp - 2) * 2048u);
+            } else {
+                // NVFP4: the tensor-level scale alpha through the epilogue (ACT 0)
+                epilogue_warp_tile<BN, EBUFS, FMT == kFmtNv4 ? 0 : -1>(
+                    args, &tmC, tmem_base + lane_field + static_cast<uint32_t>(b * BN), row0, nt * BN, lane,
+                    stage_smem, step);
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(mapa_shared(acce_bar(b), 0));
+            }
         }
         if (lane == 0) bulk_wait_group_all();
         __syncwarp();
@@ -661,10 +730,11 @@ __global__ void mx_pack_scales_kernel(const uint8_t *__restrict__ plain, uint8_t
 
 namespace {
 
-template <int BN, int STAGES, int EBUFS, int ACC>
+template <int BN, int STAGES, int EBUFS, int ACC, int FMT = kFmtMx8, int EW = 4>
 int mx_launch_pair(const MxLaunch &L, std::string &err) {
-    using T = MxPairCfg<BN, STAGES, EBUFS, ACC>;
-    auto kernel = gemm_mxfp8_nt_pair_kernel<BN, STAGES, EBUFS, ACC>;
+    using T = MxPairCfg<BN, STAGES, EBUFS, ACC, FMT>;
+    auto kernel = gemm_mxfp8_nt_pair_kernel<BN, STAGES, EBUFS, ACC, FMT, EW>;
+    const int kbytes = FMT == kFmtNv4 ? L.K / 2 : L.K;  // bytes of K per row
     static int max_clusters[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -688,7 +758,7 @@ int mx_launch_pair(const MxLaunch &L, std::string &err) {
     attr[0].val.clusterDim.z = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3((2 + EW) * 32);
     cfg.dynamicSmemBytes = T::kSmemBytes;
     cfg.stream = L.stream;
     cfg.attrs = attr;
@@ -703,16 +773,18 @@ int mx_launch_pair(const MxLaunch &L, std::string &err) {
         }
         if (dev >= 0 && dev < 64) max_clusters[dev] = clusters;
     }
-    const int kbt = (L.K + kMxBK - 1) / kMxBK;
-    const int sfa_rows = ((L.M + 127) / 128) * kbt * 2;  // 256-byte rows of the scale chunk arrays
-    const int sfb_rows = ((L.N + 127) / 128) * kbt * 2;
+    const int kbt = (kbytes + kMxBK - 1) / kMxBK;
+    // 256-byte rows of the scale chunk arrays; a k-block's chunks of one row
+    // tile are 2 * kCpt of them
+    const int sfa_rows = ((L.M + 127) / 128) * kbt * T::kCpt * 2;
+    const int sfb_rows = ((L.N + 127) / 128) * kbt * T::kCpt * 2;
     CUtensorMap tmA, tmB, tmC, tmSFA, tmSFB;
     std::memset(&tmC, 0, sizeof tmC);
-    if (!encode_map(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, L.A, L.M, L.K, kBM, kMxBK, err) ||
-        !encode_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, L.B, L.N, L.K, BN / 2, kMxBK, err) ||
-        !encode_map(&tmSFA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, L.SFA, sfa_rows, 256, 2, 256, err,
+    if (!encode_map(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, L.A, L.M, kbytes, kBM, kMxBK, err) ||
+        !encode_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, L.B, L.N, kbytes, BN / 2, kMxBK, err) ||
+        !encode_map(&tmSFA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, L.SFA, sfa_rows, 256, 2 * T::kCpt, 256, err,
                     CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !encode_map(&tmSFB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, L.SFB, sfb_rows, 256, 2, 256, err,
+        !encode_map(&tmSFB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, L.SFB, sfb_rows, 256, 2 * T::kCpt, 256, err,
                     CU_TENSOR_MAP_SWIZZLE_NONE))
         return GEMM_ERR_CUDA;
     F16Args args;
@@ -725,7 +797,12 @@ int mx_launch_pair(const MxLaunch &L, std::string &err) {
     args.num_kb = kbt;
     args.vec_store = (L.N % 8 == 0) && ((reinterpret_cast<uintptr_t>(L.C) & 15u) == 0);
     args.tma_store = args.vec_store;
-    args.epi = make_epi(EpiSpec{}, L.N);
+    EpiSpec scale;  // NVFP4: C = alpha * (the block-scaled product)
+    if (FMT == kFmtNv4) {
+        scale.alpha = L.alpha;
+        scale.on = 1;
+    }
+    args.epi = make_epi(scale, L.N);
     args.timeout_ns = L.timeout_ns;
     args.debug_skip_kblock = -1;
     args.dp_tiles = 0;
@@ -733,7 +810,10 @@ int mx_launch_pair(const MxLaunch &L, std::string &err) {
     args.sk_ws = nullptr;
     args.sk_flags = nullptr;
     args.seq = 0;
-    if (args.tma_store && !encode_half_map(&tmC, L.C, L.M, L.N, 32, 64, err)) return GEMM_ERR_CUDA;
+    if (args.tma_store && !encode_map(&tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, L.C, L.M, L.N, 32,
+                                      EW == 8 ? 32 : 64, err,
+                                      EW == 8 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B))
+        return GEMM_ERR_CUDA;
     const int tiles = args.m_tiles * args.n_tiles;
     int pairs = L.grid > 0 ? L.grid / 2 : clusters;
     if (pairs < 1) pairs = 1;
@@ -830,14 +910,16 @@ int mx_launch_1cta(const MxLaunch &L, std::string &err) {
 
 int mx_launch(const MxLaunch &L, std::string &err) {
     if (L.fmt == kFmtNv4) {
-        // 128 x 256: the 8-warp register epilogue staging through 2 KB per
-        // warp, 3 stages: 38.8 us at 5376 x 5376 x 2048 (direct 16-byte
-        // stores with 4 stages: 40.3; the 4-warp staged epilogue: 50.4), 118
-        // at K = 8192 like the direct form.
         switch (L.variant) {
+            // 128 x 256: the 8-warp register epilogue staging through 2 KB per
+            // warp, 3 stages: 38.8 us at 5376 x 5376 x 2048 (direct 16-byte
+            // stores with 4 stages: 40.3; the 4-warp staged epilogue: 50.4),
+            // 118 at K = 8192 like the direct form.
             case 3: return mx_launch_1cta<256, 3, 1, 1, kFmtNv4, 8>(L, err);
             case 1: return mx_launch_1cta<128, kMxStages, 2, 2, kFmtNv4>(L, err);
-            default: err = "the NVFP4 product has the 1-CTA kernels only"; return GEMM_ERR_UNSUPPORTED;
+            case 2: return mx_launch_pair<128, 6, 2, 2, kFmtNv4, 4>(L, err);
+            case 4: return mx_launch_pair<256, 5, 1, 1, kFmtNv4, 8>(L, err);
+            default: err = "unknown NVFP4 variant"; return GEMM_ERR_INVALID_ARG;
         }
     }
     switch (L.variant) {
@@ -848,7 +930,7 @@ int mx_launch(const MxLaunch &L, std::string &err) {
         // 52 for direct 16-byte stores (uncoalesced, one row per lane); equal
         // within the spread at K = 8192.
         case 3: return mx_launch_1cta<256, 4, 1, 1, kFmtMx8, 8>(L, err);
-        case 4: return mx_launch_pair<256, 6, 1, 1>(L, err);
+        case 4: return mx_launch_pair<256, 6, 1, 1, kFmtMx8, 8>(L, err);
         default: return mx_launch_1cta<128, kMxStages, 2, 2>(L, err);
     }
 }

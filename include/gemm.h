@@ -320,9 +320,8 @@ int gemm_mxfp8_pack_scales(int rows, int K, const void *plain, void *blocked, ge
 int gemm_nvfp4_nt(int M, int N, int K, const void *A, const void *SFA, const void *B,
                   const void *SFB, float alpha, void *C, gemm_stream_t stream);
 
-/* gemm_nvfp4_nt with a kernel configuration: GEMM_MXFP8_AUTO,
- * GEMM_MXFP8_128x128 or GEMM_MXFP8_128x256 (the pair kernels are MXFP8 only:
- * GEMM_ERR_INVALID_ARG). */
+/* gemm_nvfp4_nt with a kernel configuration: any GEMM_MXFP8_* variant
+ * (the same tile shapes, with four scale chunks per 128 rows per 256 of K). */
 int gemm_nvfp4_nt_ex(int M, int N, int K, const void *A, const void *SFA, const void *B,
                      const void *SFB, float alpha, void *C, gemm_stream_t stream,
                      const gemm_mxfp8_config *cfg);

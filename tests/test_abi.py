@@ -143,7 +143,7 @@ def test_nvfp4_arguments_are_checked_on_the_host(lib):
     assert e.value.status == g.GEMM_ERR_MISALIGNED
     with pytest.raises(g.GemmError) as e:
         g.gemm_nvfp4_nt_ex(16, 16, 64, 0x1000, 0x1000, 0x1000, 0x1000, 1.0, 0x1000,
-                           variant=g.GEMM_MXFP8_256x256_PAIR)
+                           variant=g.GEMM_MXFP8_NUM_VARIANTS)
     assert e.value.status == g.GEMM_ERR_INVALID_ARG
     assert g.gemm_nvfp4_nt(16, 0, 64, 0, 0, 0, 0, 1.0, 0) == g.GEMM_OK
 

@@ -21,7 +21,8 @@ from parity import check_f16
 pytestmark = pytest.mark.gpu
 
 SENTINEL = 0x7E5A
-VARIANTS = [g.GEMM_MXFP8_128x128, g.GEMM_MXFP8_128x256]
+VARIANTS = [g.GEMM_MXFP8_128x128, g.GEMM_MXFP8_256x128_PAIR, g.GEMM_MXFP8_128x256,
+            g.GEMM_MXFP8_256x256_PAIR]
 E2M1 = {0.0: 0, 0.5: 1, 1.0: 2, 1.5: 3, 2.0: 4, 3.0: 5, 4.0: 6, 6.0: 7}
 ONE, TWO, HALF = 0x38, 0x40, 0x30  # E4M3 scale codes
 
