@@ -7,9 +7,9 @@
 // (C is not read).  fp32 semantics exclude TF32, so the work is plain FFMA.
 //
 // Design: each CTA owns a BM x BN tile of C; every thread owns a TM x TN
-// register micro-tile made of 4 x 4 blocks spread BM/RM rows and BN/RN columns
-// apart ("第 6 章 · Shared Memory & Tile", section "6.3.1 寄存器 tile"), and a
-// warp is 4 x 8 such threads.  K is walked in BK-deep slices through a
+// register micro-tile ("第 6 章 · Shared Memory & Tile", section "6.3.1 寄存器
+// tile"): rows ty + i * (BM/TM) + g * (BM/RM) and groups of 4 columns spread
+// BN/RN apart, and a warp is 4 x 8 such threads.  K is walked in BK-deep slices through a
 // STAGES-deep ring of shared memory filled by cp.async, STAGES-1 slices ahead
 // of the multiply, one barrier per slice (the multi-stage scheme of
 // "异步拷贝与 Hopper/Blackwell 新特性", section "cp.async 与多级流水 sm_80+",
@@ -82,7 +82,7 @@ struct SplitK {
     unsigned *counters; // [tiles], zero between launches
 };
 
-template <int BM, int BN, int BK, int TM, int TN, int STAGES, int MINB, bool VEC>
+template <int BM, int BN, int BK, int TM, int TN, int STAGES, int MINB, bool VEC, bool PADA>
 __global__ void __launch_bounds__(sgemm_threads<BM, BN, TM, TN>(), MINB)
     sgemm_pipe_kernel(int M, int N, int K, float alpha, const float *__restrict__ A,
                       const float *__restrict__ B, float beta, float *__restrict__ C, const SplitK sk) {
@@ -93,12 +93,21 @@ __global__ void __launch_bounds__(sgemm_threads<BM, BN, TM, TN>(), MINB)
     static_assert((BM / TM) % 4 == 0 && (BN / TN) % 8 == 0, "whole 4 x 8 warps");
     static_assert(BK % 4 == 0, "A is read as float4 along k");
 
-    __shared__ __align__(16) float As[STAGES][BM][BK];
+    // PADA: A rows padded to BK + 4 floats (80 bytes for BK = 16) and a
+    // thread's rows BM/TM apart, so that the four quarter-warps read four
+    // consecutive rows in four different 16-byte bank groups (unpadded, with
+    // a thread's 4 rows adjacent, the quarter-warps' rows are 4 apart and all
+    // fall in one group).  Measured: 512^3 on 64 x 64 tiles 16.5 -> 14.4 us;
+    // the 128 x 128 tile ran 2.5 % slower with it, so it keeps the plain layout.
+    constexpr int BKP = PADA ? BK + 4 : BK;
+    __shared__ __align__(16) float As[STAGES][BM][BKP];
     __shared__ __align__(16) float Bs[STAGES][BK][BN];
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int ty = (warp / kWarpsN) * 4 + (lane >> 3);
+    // tile row of this thread's row i of row group g
+    auto trow = [&](int g, int i) { return g * (BM / RM) + (PADA ? i * (BM / TM) + ty : ty * 4 + i); };
     const int tx = (warp % kWarpsN) * 8 + (lane & 7);
     const int m0 = blockIdx.y * BM;
     const int n0 = blockIdx.x * BN;
@@ -167,7 +176,7 @@ __global__ void __launch_bounds__(sgemm_threads<BM, BN, TM, TN>(), MINB)
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
                     av[g * 4 + i] = *reinterpret_cast<const float4 *>(
-                        &As[buf][g * (BM / RM) + ty * 4 + i][kq * 4]);
+                        &As[buf][trow(g, i)][kq * 4]);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
                 float2 bp[TN / 2];
@@ -237,7 +246,7 @@ __global__ void __launch_bounds__(sgemm_threads<BM, BN, TM, TN>(), MINB)
 #pragma unroll
             for (int u = 0; u < QC; ++u) {
                 const int q = qc + u, r = q / (TN / 4), gj = q % (TN / 4);
-                const int m = m0 + (r / 4) * (BM / RM) + ty * 4 + (r % 4);
+                const int m = m0 + trow(r / 4, r % 4);
                 if (m >= M) continue;
                 float *crow = C + static_cast<size_t>(m) * N;
                 const int n = n0 + gj * (BN / RN) + tx * 4;
@@ -268,7 +277,7 @@ __global__ void __launch_bounds__(sgemm_threads<BM, BN, TM, TN>(), MINB)
     for (int gi = 0; gi < RM; ++gi) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const int m = m0 + gi * (BM / RM) + ty * 4 + i;
+            const int m = m0 + trow(gi, i);
             if (m >= M) continue;
             float *crow = C + static_cast<size_t>(m) * N;
 #pragma unroll
@@ -356,7 +365,7 @@ int sg_workspace(cudaStream_t stream, size_t ws_bytes, int tiles, bool capturing
     return GEMM_OK;
 }
 
-template <int BM, int BN, int BK, int TM, int TN, int STAGES, int MINB = 2>
+template <int BM, int BN, int BK, int TM, int TN, int STAGES, int MINB, bool PADA>
 int launch_pipe(const SgemmLaunch &L, std::string &err) {
     dim3 grid((L.N + BN - 1) / BN, (L.M + BM - 1) / BM);
     // Split-K as planned by the caller: blockIdx.z picks a K share.
@@ -385,12 +394,12 @@ int launch_pipe(const SgemmLaunch &L, std::string &err) {
                      ((reinterpret_cast<uintptr_t>(L.A) | reinterpret_cast<uintptr_t>(L.B) |
                        reinterpret_cast<uintptr_t>(L.C)) & 15u) == 0;
     constexpr int threads = sgemm_threads<BM, BN, TM, TN>();
+    auto kvec = sgemm_pipe_kernel<BM, BN, BK, TM, TN, STAGES, MINB, true, PADA>;
+    auto kscalar = sgemm_pipe_kernel<BM, BN, BK, TM, TN, STAGES, MINB, false, PADA>;
     if (vec)
-        sgemm_pipe_kernel<BM, BN, BK, TM, TN, STAGES, MINB, true><<<grid, threads, 0, L.stream>>>(
-            L.M, L.N, L.K, L.alpha, L.A, L.B, L.beta, L.C, sk);
+        kvec<<<grid, threads, 0, L.stream>>>(L.M, L.N, L.K, L.alpha, L.A, L.B, L.beta, L.C, sk);
     else
-        sgemm_pipe_kernel<BM, BN, BK, TM, TN, STAGES, MINB, false><<<grid, threads, 0, L.stream>>>(
-            L.M, L.N, L.K, L.alpha, L.A, L.B, L.beta, L.C, sk);
+        kscalar<<<grid, threads, 0, L.stream>>>(L.M, L.N, L.K, L.alpha, L.A, L.B, L.beta, L.C, sk);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         err = std::string("sgemm kernel launch: ") + cudaGetErrorString(e);
@@ -414,8 +423,8 @@ int sgemm_launch(const SgemmLaunch &L, std::string &err) {
         return GEMM_OK;
     }
     switch (L.variant) {
-        case GEMM_SGEMM_128x128: return launch_pipe<128, 128, 16, 8, 16, 3>(L, err);
-        case GEMM_SGEMM_64x64: return launch_pipe<64, 64, 16, 4, 4, 3>(L, err);
+        case GEMM_SGEMM_128x128: return launch_pipe<128, 128, 16, 8, 16, 3, 2, false>(L, err);
+        case GEMM_SGEMM_64x64: return launch_pipe<64, 64, 16, 4, 4, 3, 2, true>(L, err);
         default: err = "unknown sgemm variant"; return GEMM_ERR_INVALID_ARG;
     }
 }
