@@ -387,6 +387,10 @@ def run_ours(args):
     burst = float(peaks.get("bf16_tflops", FALLBACK_TENSOR_TFLOPS))
     sustained = peaks.get("bf16_tflops_sustained")
     peak = float(sustained) if sustained else burst
+    # The fused, MXFP8 and NVFP4 objects are short runs (50 launches) after
+    # the idle pause before the SGEMM and GEMV: the burst figure applies.
+    burst_note = (f"{peak_kind} bf16 dense burst (a short run after an idle pause; fp16 runs at the "
+                  f"bf16 rate)")
     peak_note = (f"{peak_kind} bf16 dense sustained (fp16 runs at the bf16 rate; the region is timed "
                  f"after a soak, under the power cap)" if sustained else
                  f"{peak_kind} bf16 dense burst (no sustained figure available)")
@@ -574,9 +578,9 @@ def run_ours(args):
             "unfused_us_per_call": 1e3 * t_unfused,
             "unfused": "gemm_f16_nt, then PyTorch gelu(C + bias + R) element-wise",
             "extra_bytes_per_call": 2 * N + 2 * M * N,
-            "roofline": {"bound": "tensor", "achieved": fval, "peak": peak, "unit": "TFLOP/s",
-                         "frac": fval / peak,
-                         "peak_source": peak_note, "frac_of_burst_peak": fval / burst}}
+            "roofline": {"bound": "tensor", "achieved": fval, "peak": burst, "unit": "TFLOP/s",
+                         "frac": fval / burst, "peak_source": burst_note,
+                         "frac_of_sustained_peak": fval / peak}}
 
     # ---- block-scaled FP8 (MXFP8) at the headline shape against the fp8
     # dense peak (the measured bf16 peak x the nominal fp8/bf16 ratio of 2)
@@ -600,15 +604,15 @@ def run_ours(args):
             n_mx = 50
             t_mx = region_time(mxs, stream, n_mx) / n_mx
         g.gemm_check_device_status(sh)
-        fp8_peak = 2.0 * peak
+        fp8_peak = 2.0 * burst
         mval = w.flop / (t_mx * 1e-3) / 1e12
         line["mxfp8"] = {
             "workload": f"mxfp8_nt_{M}x{N}x{K} (E4M3, UE8M0 scale per 32 of K, half out)",
             "value": mval, "unit": "TFLOP/s", "us_per_call": 1e3 * t_mx,
             "roofline": {"bound": "tensor", "achieved": mval, "peak": fp8_peak, "unit": "TFLOP/s",
                          "frac": mval / fp8_peak,
-                         "peak_source": peak_note + " x 2 (nominal fp8/bf16 ratio)",
-                         "frac_of_burst_peak": mval / (2.0 * burst)}}
+                         "peak_source": burst_note + " x 2 (nominal fp8/bf16 ratio)",
+                         "frac_of_sustained_peak": mval / (2.0 * peak)}}
 
     # ---- block-scaled FP4 (NVFP4) at the headline shape against the fp4
     # dense peak (the measured bf16 peak x the nominal fp4/bf16 ratio of 6)
@@ -632,15 +636,15 @@ def run_ours(args):
             n_nv = 50
             t_nv = region_time(nvs, stream, n_nv) / n_nv
         g.gemm_check_device_status(sh)
-        fp4_peak = 6.0 * peak
+        fp4_peak = 6.0 * burst
         nval = w.flop / (t_nv * 1e-3) / 1e12
         line["nvfp4"] = {
             "workload": f"nvfp4_nt_{M}x{N}x{K} (E2M1 pairs, E4M3 scale per 16 of K, alpha, half out)",
             "value": nval, "unit": "TFLOP/s", "us_per_call": 1e3 * t_nv,
             "roofline": {"bound": "tensor", "achieved": nval, "peak": fp4_peak, "unit": "TFLOP/s",
                          "frac": nval / fp4_peak,
-                         "peak_source": peak_note + " x 6 (nominal fp4/bf16 ratio)",
-                         "frac_of_burst_peak": nval / (6.0 * burst)}}
+                         "peak_source": burst_note + " x 6 (nominal fp4/bf16 ratio)",
+                         "frac_of_sustained_peak": nval / (6.0 * peak)}}
 
     if rank == 0 and not args.skip_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, A, B, budget_s=args.cpu_budget)
