@@ -99,7 +99,12 @@ __global__ void __launch_bounds__(sgemm_threads<BM, BN, TM, TN>(), MINB)
     // a thread's 4 rows adjacent, the quarter-warps' rows are 4 apart and all
     // fall in one group).  Measured: 512^3 on 64 x 64 tiles 16.5 -> 14.4 us;
     // the 128 x 128 tile ran 2.5 % slower with it, so it keeps the plain layout.
+    // Without PADA the rows stay BK floats and a row's float4 chunk q is
+    // stored at chunk q ^ ((row / 4) % 4): the quarter-warps' rows are 4
+    // apart, and the XOR puts their reads in four different bank groups.
+    static_assert(PADA || BK == 16, "the chunk swizzle permutes 4 chunks per row");
     constexpr int BKP = PADA ? BK + 4 : BK;
+    auto achunk = [](int row, int kq) { return PADA ? kq : (kq ^ ((row >> 2) & 3)); };
     __shared__ __align__(16) float As[STAGES][BM][BKP];
     __shared__ __align__(16) float Bs[STAGES][BK][BN];
 
@@ -118,7 +123,8 @@ __global__ void __launch_bounds__(sgemm_threads<BM, BN, TM, TN>(), MINB)
             const int row = c / (BK / 4), kq = c % (BK / 4);
             const int m = m0 + row, k = k0 + kq * 4;
             const float *src = A + static_cast<size_t>(m < M ? m : 0) * K;
-            const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(&As[buf][row][kq * 4]));
+            const uint32_t dst =
+                static_cast<uint32_t>(__cvta_generic_to_shared(&As[buf][row][achunk(row, kq) * 4]));
             if (VEC) {
                 cp_async_16(dst, src + (k < K ? k : 0), m < M && k < K);
             } else {
@@ -176,7 +182,7 @@ __global__ void __launch_bounds__(sgemm_threads<BM, BN, TM, TN>(), MINB)
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
                     av[g * 4 + i] = *reinterpret_cast<const float4 *>(
-                        &As[buf][trow(g, i)][kq * 4]);
+                        &As[buf][trow(g, i)][achunk(trow(g, i), kq) * 4]);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
                 float2 bp[TN / 2];
