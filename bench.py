@@ -374,7 +374,7 @@ def run_ours(args):
     avg_launch_ms = local_ms / args.steps
 
     sm_count = torch.cuda.get_device_properties(local).multi_processor_count
-    variant, grid = g.gemm_f16_select(M, N, K, sm_count)
+    variant, grid, _ = g.gemm_f16_select(M, N, K, sm_count)
     kernel_name = {g.GEMM_F16_128x256: "gemm_f16_nt_tc_kernel<256,4> (1-CTA 128x256)",
                    g.GEMM_F16_128x128: "gemm_f16_nt_tc_kernel<128,6> (1-CTA 128x128)",
                    g.GEMM_F16_256x256_PAIR: "gemm_f16_nt_pair_kernel<6> (CTA pair 256x256)"

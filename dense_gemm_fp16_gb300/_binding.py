@@ -45,7 +45,8 @@ class GemmError(RuntimeError):
 
 
 class _F16Config(ctypes.Structure):
-    _fields_ = [("variant", ctypes.c_int), ("grid", ctypes.c_int), ("flags", ctypes.c_int)]
+    _fields_ = [("variant", ctypes.c_int), ("grid", ctypes.c_int), ("flags", ctypes.c_int),
+                ("raster", ctypes.c_int)]
 
 
 class _F16Epilogue(ctypes.Structure):
@@ -138,18 +139,18 @@ def gemm_f16_nt(M: int, N: int, K: int, A: int, B: int, C: int, stream: int | No
     return _check(load_library().gemm_f16_nt(M, N, K, A, B, C, stream or None))
 
 
-def gemm_f16_nt_ex(M, N, K, A, B, C, stream=0, variant=GEMM_F16_AUTO, grid=0, flags=0) -> int:
-    cfg = _F16Config(variant, grid, flags)
+def gemm_f16_nt_ex(M, N, K, A, B, C, stream=0, variant=GEMM_F16_AUTO, grid=0, flags=0, raster=0) -> int:
+    cfg = _F16Config(variant, grid, flags, raster)
     return _check(load_library().gemm_f16_nt_ex(M, N, K, A, B, C, stream or None, ctypes.byref(cfg)))
 
 
 def gemm_f16_nt_fused(M, N, K, A, B, C, alpha=1.0, beta=0.0, bias=0, residual=0,
                       activation=GEMM_ACT_NONE, stream=0, variant=GEMM_F16_AUTO, grid=0,
-                      flags=0) -> int:
+                      flags=0, raster=0) -> int:
     """C = act(alpha·A·Bᵀ + bias + beta·residual) rounded to half once; bias and
     residual are device pointers or 0 (absent)."""
     epi = _F16Epilogue(float(alpha), float(beta), bias or None, residual or None, int(activation))
-    cfg = _F16Config(variant, grid, flags)
+    cfg = _F16Config(variant, grid, flags, raster)
     return _check(load_library().gemm_f16_nt_fused(M, N, K, A, B, C, ctypes.byref(epi),
                                                    stream or None, ctypes.byref(cfg)))
 
@@ -216,10 +217,11 @@ def gemm_check_device_status(stream: int | None = 0) -> int:
     return _check(load_library().gemm_check_device_status(stream or None))
 
 
-def gemm_f16_select(M: int, N: int, K: int, sm_count: int) -> tuple[int, int]:
-    cfg = _F16Config(0, 0, 0)
+def gemm_f16_select(M: int, N: int, K: int, sm_count: int) -> tuple[int, int, int]:
+    """(variant, grid, raster) of the library's choice."""
+    cfg = _F16Config(0, 0, 0, 0)
     _check(load_library().gemm_f16_select(M, N, K, sm_count, ctypes.byref(cfg)))
-    return cfg.variant, cfg.grid
+    return cfg.variant, cfg.grid, cfg.raster
 
 
 def gemm_sgemm_select(M: int, N: int, K: int, sm_count: int) -> tuple[int, int]:

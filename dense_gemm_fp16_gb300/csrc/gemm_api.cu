@@ -96,6 +96,16 @@ const char *gemm_last_error(void) { return t_last_error.c_str(); }
 // Selection (host logic only; no device call)
 // ---------------------------------------------------------------------------
 
+// Tile rows per band of the tile order.  While A and B fit comfortably in
+// L2 (129 MB) the plain column order is kept; beyond that a wave of tiles
+// walking every tile row would stream all of A through L2 once per wave, so
+// the tiles go in bands of a few rows.
+static int f16_default_raster(int variant, int M, int N, int K) {
+    const double operand_bytes = 2.0 * (static_cast<double>(M) + N) * K;
+    if (variant == GEMM_F16_GEMV || operand_bytes <= 96.0 * 1024 * 1024) return 1 << 30;
+    return variant == GEMM_F16_256x256_PAIR ? 8 : 16;
+}
+
 int gemm_f16_select(int M, int N, int K, int sm_count, gemm_f16_config *cfg) {
     if (!cfg) return fail(GEMM_ERR_INVALID_ARG, "gemm_f16_select: cfg is NULL");
     if (M < 0 || N < 0 || K < 0 || sm_count <= 0)
@@ -124,6 +134,7 @@ int gemm_f16_select(int M, int N, int K, int sm_count, gemm_f16_config *cfg) {
     cfg->variant = variant;
     cfg->grid = f16_default_grid(variant, M, N, K, sm_count);
     cfg->flags = 0;
+    cfg->raster = f16_default_raster(variant, M, N, K);
     return GEMM_OK;
 }
 
@@ -206,9 +217,9 @@ static int f16_nt_impl(int M, int N, int K, const void *A, const void *B, void *
     if (epi && (epi->activation < 0 || epi->activation >= GEMM_ACT_NUM))
         return fail(GEMM_ERR_INVALID_ARG, "gemm_f16_nt_fused: unknown activation %d", epi->activation);
     if (cfg && (cfg->variant < 0 || cfg->variant >= GEMM_F16_NUM_VARIANTS || cfg->grid < 0 ||
-                (cfg->flags & ~GEMM_F16_FLAG_STREAM_K) != 0))
-        return fail(GEMM_ERR_INVALID_ARG, "gemm_f16_nt_ex: bad config variant=%d grid=%d flags=%d",
-                    cfg->variant, cfg->grid, cfg->flags);
+                (cfg->flags & ~GEMM_F16_FLAG_STREAM_K) != 0 || cfg->raster < 0))
+        return fail(GEMM_ERR_INVALID_ARG, "gemm_f16_nt_ex: bad config variant=%d grid=%d flags=%d raster=%d",
+                    cfg->variant, cfg->grid, cfg->flags, cfg->raster);
     int sms = 0;
     int st = sm_count_of_current_device(&sms);
     if (st != GEMM_OK) return st;
@@ -225,6 +236,8 @@ static int f16_nt_impl(int M, int N, int K, const void *A, const void *B, void *
                         "(M=%d K=%d)", kGemvMaxSmem, M, K);
     }
     if (cfg && cfg->grid > 0) sel.grid = cfg->grid;
+    if (cfg && cfg->variant != GEMM_F16_AUTO) sel.raster = f16_default_raster(sel.variant, M, N, K);
+    if (cfg && cfg->raster > 0) sel.raster = cfg->raster;
 
     gb300::F16Launch L;
     L.M = M;
@@ -240,6 +253,7 @@ static int f16_nt_impl(int M, int N, int K, const void *A, const void *B, void *
     L.debug_skip_kblock = debug_skip_kblock;
     L.allow_stream_k = cfg && (cfg->flags & GEMM_F16_FLAG_STREAM_K);
     L.static_scratch = static_scratch;
+    L.raster = sel.raster;
     L.sm_count = sms;
     if (epi) {
         L.epi.alpha = epi->alpha;

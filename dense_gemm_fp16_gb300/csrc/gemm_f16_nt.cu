@@ -81,7 +81,23 @@ struct F16Args {
     float *sk_ws;           // slot (pair, rank): 128 rows x 256 fp32, row-major
     uint32_t *sk_flags;     // flag (pair, rank, epilogue warp), 8 per (pair, rank)
     uint32_t seq;           // this launch's sequence number (never 0)
+    int raster = 1 << 30;   // tile rows per band of the tile order
 };
+
+// Output tile `tile` of the persistent order -> its tile row and column: bands
+// of `raster` tile rows (the last one shorter), each walked column by column
+// with the rows of a column consecutive.  With raster >= m_tiles this is the
+// plain column order (tile % m_tiles, tile / m_tiles).
+__device__ __forceinline__ void tile_mn(int tile, const F16Args &a, int &mt, int &nt) {
+    const int g = a.raster < a.m_tiles ? a.raster : a.m_tiles;
+    const int band_tiles = g * a.n_tiles;
+    const int band = tile / band_tiles;
+    const int first = band * g;
+    const int h = a.m_tiles - first < g ? a.m_tiles - first : g;  // this band's rows
+    const int r = tile - band * band_tiles;
+    mt = first + r % h;
+    nt = r / h;
+}
 
 // The work items of one CTA pair: whole data-parallel tiles first, then its
 // contiguous share of the stream-K k-blocks cut at tile boundaries.  Every role
@@ -472,8 +488,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             bool first_tile = true;
             for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
-                const int mt = tile % args.m_tiles;
-                const int nt = tile / args.m_tiles;
+                int mt, nt;
+                tile_mn(tile, args, mt, nt);
                 for (int kb = 0; kb < num_kb; ++kb) {
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, args.timeout_ns, abort_flag)) {
                         ok = false;
@@ -563,13 +579,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // The residual rows of this tile (first tile only) and of the
                 // next one go to L2 while the accumulators are being made.
                 const int pf = i == 0 ? tile : tile + static_cast<int>(gridDim.x);
-                if (pf < total_tiles)
-                    epi_prefetch_res(args.epi, (pf % args.m_tiles) * kBM + quarter * 32 + lane,
-                                     (pf / args.m_tiles) * BN, BN, args.M, args.N);
+                if (pf < total_tiles) {
+                    int pm, pn;
+                    tile_mn(pf, args, pm, pn);
+                    epi_prefetch_res(args.epi, pm * kBM + quarter * 32 + lane, pn * BN, BN, args.M, args.N);
+                }
                 if (i == 0 && tile + static_cast<int>(gridDim.x) < total_tiles) {
                     const int nx = tile + static_cast<int>(gridDim.x);
-                    epi_prefetch_res(args.epi, (nx % args.m_tiles) * kBM + quarter * 32 + lane,
-                                     (nx / args.m_tiles) * BN, BN, args.M, args.N);
+                    int pm, pn;
+                    tile_mn(nx, args, pm, pn);
+                    epi_prefetch_res(args.epi, pm * kBM + quarter * 32 + lane, pn * BN, BN, args.M, args.N);
                 }
             }
             int ok = 1;
@@ -583,8 +602,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after_sync();
-            const int mt = tile % args.m_tiles;
-            const int nt = tile / args.m_tiles;
+            int mt, nt;
+            tile_mn(tile, args, mt, nt);
             epilogue_warp_tile<BN, 2, ACT>(args, &tmC, tmem_base + lane_field + static_cast<uint32_t>(b * BN),
                                       mt * kBM + quarter * 32, nt * BN, lane, stage_smem, step);
             tc_fence_before_sync();
@@ -732,8 +751,8 @@ __global__ void __launch_bounds__((2 + EPI) * 32, 1)
             PairWork work(args, pair, num_pairs);
             int tile, kb0, kb1;
             while (ok && work.next(tile, kb0, kb1)) {
-                const int mt = tile % args.m_tiles;
-                const int nt = tile / args.m_tiles;
+                int mt, nt;
+                tile_mn(tile, args, mt, nt);
                 const int a_row = mt * 256 + static_cast<int>(rank) * 128;
                 const int b_row = nt * BN + static_cast<int>(rank) * 128;
                 for (int kb = kb0; kb < kb1; ++kb) {
@@ -829,8 +848,10 @@ __global__ void __launch_bounds__((2 + EPI) * 32, 1)
         for (int i = 0; work.next(tile, kb0, kb1); ++i) {
             const int b = i & 1;
             const uint32_t ap = (i >> 1) & 1;
-            const int row0 = (tile % args.m_tiles) * 256 + static_cast<int>(rank) * 128 + quarter * 32;
-            const int n_base = (tile / args.m_tiles) * BN + col0;
+            int tm, tn;
+            tile_mn(tile, args, tm, tn);
+            const int row0 = tm * 256 + static_cast<int>(rank) * 128 + quarter * 32;
+            const int n_base = tn * BN + col0;
             if constexpr (RES) {
                 // The tile's first kResAhead residual boxes load while its
                 // accumulators are being made (stores of earlier slabs pending:
@@ -844,9 +865,10 @@ __global__ void __launch_bounds__((2 + EPI) * 32, 1)
                 // The residual rows of this tile (first tile only) and of the
                 // next one go to L2 while the accumulators are being made.
                 auto prefetch = [&](int t) {
-                    epi_prefetch_res(args.epi, (t % args.m_tiles) * 256 + static_cast<int>(rank) * 128 +
-                                                   quarter * 32 + lane,
-                                     (t / args.m_tiles) * BN + col0, kCols, args.M, args.N);
+                    int pm, pn;
+                    tile_mn(t, args, pm, pn);
+                    epi_prefetch_res(args.epi, pm * 256 + static_cast<int>(rank) * 128 + quarter * 32 + lane,
+                                     pn * BN + col0, kCols, args.M, args.N);
                 };
                 if (i == 0 && kb0 == 0) prefetch(tile);
                 PairWork peek = work;
@@ -1067,6 +1089,7 @@ int launch_variant(const F16Launch &L, std::string &err) {
     args.N = L.N;
     args.K = L.K;
     args.m_tiles = (L.M + kBM - 1) / kBM;
+    args.raster = L.raster > 0 ? L.raster : (1 << 30);
     args.n_tiles = (L.N + BN - 1) / BN;
     args.num_kb = (L.K + kBK - 1) / kBK;
     args.vec_store = (L.N % 8 == 0) && ((reinterpret_cast<uintptr_t>(L.C) & 15u) == 0);
@@ -1257,6 +1280,7 @@ int launch_pair(const F16Launch &L, std::string &err) {
     args.N = L.N;
     args.K = L.K;
     args.m_tiles = (L.M + 255) / 256;
+    args.raster = L.raster > 0 ? L.raster : (1 << 30);
     args.n_tiles = (L.N + 255) / 256;
     args.num_kb = (L.K + kBK - 1) / kBK;
     args.vec_store = (L.N % 8 == 0) && ((reinterpret_cast<uintptr_t>(L.C) & 15u) == 0);

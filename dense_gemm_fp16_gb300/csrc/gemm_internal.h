@@ -52,6 +52,7 @@ struct F16Launch {
     bool static_scratch;    // stream-K partials in the library's static array, no allocation
     int sm_count;           // SMs of the current device
     EpiSpec epi;            // fused epilogue (off by default)
+    int raster = 1 << 30;   // tile rows per band of the tile order (>= tile rows: plain)
 };
 
 int f16_launch(const F16Launch &L, std::string &err);

@@ -116,6 +116,11 @@ typedef struct {
     int variant;
     int grid;
     int flags;      /* GEMM_F16_FLAG_* below, 0 for none */
+    int raster;     /* tile order: the persistent CTAs walk the output tiles in
+                       bands of `raster` tile rows (M), each band column by
+                       column, so that a wave's A rows and B columns stay in
+                       L2 when the operands do not fit it; 0 = the library's
+                       choice, a value >= the tile rows = plain column order */
 } gemm_f16_config;
 
 /*

@@ -150,32 +150,64 @@ def test_nvfp4_arguments_are_checked_on_the_host(lib):
 
 def test_f16_selector(lib):
     # the two fp16 workloads: CTA-pair 256 x 256 tiles, one CTA per SM
-    assert g.gemm_f16_select(5376, 5376, 2048, 152) == (g.GEMM_F16_256x256_PAIR, 152)
-    assert g.gemm_f16_select(5000, 5376, 2040, 152) == (g.GEMM_F16_256x256_PAIR, 152)
-    assert g.gemm_f16_select(5376, 5376, 2048, 151) == (g.GEMM_F16_256x256_PAIR, 150)
-    assert g.gemm_f16_select(4096, 2048, 512, 148) == (g.GEMM_F16_256x256_PAIR, 148)
+    assert g.gemm_f16_select(5376, 5376, 2048, 152)[:2] == (g.GEMM_F16_256x256_PAIR, 152)
+    assert g.gemm_f16_select(5000, 5376, 2040, 152)[:2] == (g.GEMM_F16_256x256_PAIR, 152)
+    assert g.gemm_f16_select(5376, 5376, 2048, 151)[:2] == (g.GEMM_F16_256x256_PAIR, 150)
+    assert g.gemm_f16_select(4096, 2048, 512, 148)[:2] == (g.GEMM_F16_256x256_PAIR, 148)
     # fewer pair tiles than SM pairs: narrow tiles
-    assert g.gemm_f16_select(2048, 2048, 512, 152) == (g.GEMM_F16_128x128, 152)
+    assert g.gemm_f16_select(2048, 2048, 512, 152)[:2] == (g.GEMM_F16_128x128, 152)
     # one or two rows of A: the HBM-bound matrix-vector kernel, planned per SM
-    assert g.gemm_f16_select(1, 5376, 2048, 152) == (g.GEMM_F16_GEMV, 152)
-    assert g.gemm_f16_select(2, 16384, 8192, 152) == (g.GEMM_F16_GEMV, 152)
+    assert g.gemm_f16_select(1, 5376, 2048, 152)[:2] == (g.GEMM_F16_GEMV, 152)
+    assert g.gemm_f16_select(2, 16384, 8192, 152)[:2] == (g.GEMM_F16_GEMV, 152)
     assert g.gemm_f16_select(3, 16384, 8192, 152)[0] == g.GEMM_F16_128x128
     # its shared-memory staging of A would not fit: the tensor-core path
     assert g.gemm_f16_select(2, 4096, 65536, 152)[0] != g.GEMM_F16_GEMV
     assert g.gemm_f16_select(1, 4096, 65536, 152)[0] == g.GEMM_F16_GEMV
     # too few wide tiles to fill the SMs: narrow tiles, grid = tile count
-    assert g.gemm_f16_select(1024, 1024, 1024, 152) == (g.GEMM_F16_128x128, 64)
-    assert g.gemm_f16_select(100, 100, 64, 152) == (g.GEMM_F16_128x128, 1)
+    assert g.gemm_f16_select(1024, 1024, 1024, 152)[:2] == (g.GEMM_F16_128x128, 64)
+    assert g.gemm_f16_select(100, 100, 64, 152)[:2] == (g.GEMM_F16_128x128, 1)
     assert g.gemm_f16_select(128, 8192, 64, 148)[0] == g.GEMM_F16_128x128
     # few tiles over a long K: pair tiles split along K over all the pairs
-    assert g.gemm_f16_select(512, 512, 32768, 152) == (g.GEMM_F16_256x256_PAIR, 152)
-    assert g.gemm_f16_select(256, 256, 65536, 152) == (g.GEMM_F16_256x256_PAIR, 152)
-    assert g.gemm_f16_select(128, 4096, 8192, 152) == (g.GEMM_F16_256x256_PAIR, 152)
+    assert g.gemm_f16_select(512, 512, 32768, 152)[:2] == (g.GEMM_F16_256x256_PAIR, 152)
+    assert g.gemm_f16_select(256, 256, 65536, 152)[:2] == (g.GEMM_F16_256x256_PAIR, 152)
+    assert g.gemm_f16_select(128, 4096, 8192, 152)[:2] == (g.GEMM_F16_256x256_PAIR, 152)
     # ... but not when a split would be shallower than four ways
-    assert g.gemm_f16_select(1024, 1024, 4096, 152) == (g.GEMM_F16_128x128, 64)
-    assert g.gemm_f16_select(64, 8192, 8192, 152) == (g.GEMM_F16_128x128, 64)
+    assert g.gemm_f16_select(1024, 1024, 4096, 152)[:2] == (g.GEMM_F16_128x128, 64)
+    assert g.gemm_f16_select(64, 8192, 8192, 152)[:2] == (g.GEMM_F16_128x128, 64)
     with pytest.raises(g.GemmError):
         g.gemm_f16_select(1, 1, 1, 0)
+
+
+def test_f16_selector_raster(lib):
+    plain = 1 << 30
+    # operands that fit in L2 keep the plain column order of tiles
+    assert g.gemm_f16_select(5376, 5376, 2048, 152)[2] == plain
+    assert g.gemm_f16_select(5000, 5376, 2040, 152)[2] == plain
+    # beyond it, bands of tile rows (8 pair tiles = 2048 rows)
+    assert g.gemm_f16_select(8192, 8192, 8192, 152)[2] == 8
+    assert g.gemm_f16_select(16384, 16384, 2048, 152)[2] == 8
+    assert g.gemm_f16_select(1, 16384, 8192, 152)[2] == plain  # GEMV has no tiles
+    with pytest.raises(g.GemmError):
+        g.gemm_f16_nt_ex(16, 16, 16, 0x1000, 0x1000, 0x1000, raster=-1)
+
+
+def _tile_mn(tile, m_tiles, n_tiles, raster):
+    # the kernels' band order, restated: bands of `raster` tile rows, column by column
+    gsz = min(raster, m_tiles)
+    band, r = divmod(tile, gsz * n_tiles)
+    first = band * gsz
+    h = min(gsz, m_tiles - first)
+    return first + r % h, r // h
+
+
+@pytest.mark.parametrize("m_tiles,n_tiles,raster", [(21, 21, 8), (32, 32, 8), (5, 7, 3), (7, 3, 1 << 30),
+                                                    (9, 4, 4), (1, 5, 8)])
+def test_band_order_visits_every_tile_once(m_tiles, n_tiles, raster):
+    seen = {_tile_mn(t, m_tiles, n_tiles, raster) for t in range(m_tiles * n_tiles)}
+    assert seen == {(m, n) for m in range(m_tiles) for n in range(n_tiles)}
+    if raster >= m_tiles:
+        assert [_tile_mn(t, m_tiles, n_tiles, raster) for t in range(m_tiles * n_tiles)] == \
+            [(t % m_tiles, t // m_tiles) for t in range(m_tiles * n_tiles)]
 
 
 def test_sgemm_selector(lib):
