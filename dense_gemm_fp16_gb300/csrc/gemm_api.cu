@@ -466,7 +466,6 @@ int sgemm_ex(int M, int N, int K, float alpha, const float *A, const float *B, f
     int variant = GEMM_SGEMM_128x128, splits = 1;
     sgemm_plan(M, N, K, sms, cfg ? cfg->variant : 0, cfg ? cfg->splits : 0, &variant, &splits);
     gb300::SgemmLaunch L;
-    L.sm_count = sms;
     L.splits = splits;
     L.M = M;
     L.N = N;

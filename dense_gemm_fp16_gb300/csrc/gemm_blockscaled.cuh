@@ -14,22 +14,23 @@ namespace {
 // UE8M0 scale per row per 32 elements of K, fp32 accumulation on the tensor
 // cores (tcgen05.mma kind::mxf8f6f4, block_scale, scale_vec::1X), half C.
 //
-// The same warp roles as the 1-CTA fp16 kernel, with 128 x 128 output tiles
-// and 128-element (128-byte) k-blocks.  Each stage also carries the two
-// tiles' scales for the k-block: 128 rows x 4 scales each, a 512-byte chunk
-// stored contiguously in the operand's scale array (see gemm_mxfp8_nt in
-// gemm.h for the layout: byte 16*(r % 32) + 4*(r / 32) + j of the chunk is
-// row r's j-th scale).  The MMA thread copies each chunk into TMEM
-// (tcgen05.cp 32x128b.warpx4: TMEM lane r holds, in column c, the four
-// scales of row 32c + r % 32) ahead of the four K = 32 MMAs of the k-block,
-// which pick scale j through the descriptor's scale-factor IDs; copies and
-// MMAs from one thread run in order, so one scale area per stage suffices.
+// The same warp roles as the 1-CTA fp16 kernel, with 128 x BN output tiles
+// and 128-byte k-blocks.  With each stage's A and B boxes, the producer
+// loads the k-block's scales into that stage's slot of a scale region after
+// the stages: per 128-row tile a 512-byte chunk of 128 rows x 4 scales (four
+// chunks for NVFP4), stored contiguously in the operand's scale array (see
+// gemm_mxfp8_nt in gemm.h for the layout: byte 16*(r % 32) + 4*(r / 32) + j
+// of the chunk is row r's j-th scale).  The MMA thread copies each chunk into
+// TMEM (tcgen05.cp 32x128b.warpx4: TMEM lane r holds, in column c, the four
+// scales of row 32c + r % 32) ahead of the k-block's four MMAs, which pick
+// scale j through the descriptor's scale-factor IDs (MXFP8, K = 32) or take
+// all four bytes of their own chunk (NVFP4, K = 64); copies and MMAs from one
+// thread run in order, so one scale area per stage suffices.
 // ---------------------------------------------------------------------------
 
 constexpr int kMxBK = 128;       // K elements (bytes) per k-block: one 128-byte swizzle row
-constexpr int kMxBN = 128;       // output tile columns
 constexpr int kMxStages = 5;
-constexpr int kMxUmmaK = 32;     // K per MMA instruction
+constexpr int kMxUmmaK = 32;     // bytes of K per MMA instruction (32 E4M3 or 64 E2M1 elements)
 constexpr int kMxSfChunk = 512;  // 128 rows x 4 scales
 
 // BN output columns per tile (128 or 256: B's scales are BN/128 chunks),
@@ -291,7 +292,7 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
                     const uint64_t adesc = sw128_kmajor_desc(sa);
                     const uint64_t bdesc = sw128_kmajor_desc(sb);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
+                    for (int j = 0; j < kMxBK / kMxUmmaK; ++j) {
                         // 32 bytes of K per MMA (32 FP8 or 64 FP4): the start
                         // address advances 32 bytes.
                         if constexpr (FMT == kFmtMx8) {
@@ -609,7 +610,7 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
                     const uint64_t adesc = sw128_kmajor_desc(sa);
                     const uint64_t bdesc = sw128_kmajor_desc(sa + T::kABytes);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
+                    for (int j = 0; j < kMxBK / kMxUmmaK; ++j) {
                         if constexpr (FMT == kFmtMx8)
                             mma_mxf8_ss_pair(d_tmem, adesc + 2u * j, bdesc + 2u * j, idesc_mxf8_e4m3(256, BN, j),
                                              sfa_tmem, sfb_tmem, (kb > 0 || j > 0) ? 1u : 0u);

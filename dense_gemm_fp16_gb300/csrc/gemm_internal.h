@@ -109,7 +109,6 @@ struct SgemmLaunch {
     float *C;
     cudaStream_t stream;
     int variant;   // GEMM_SGEMM_128x128 or GEMM_SGEMM_64x64
-    int sm_count;  // SMs of the current device
     int splits;    // split-K depth, 1 = none (sgemm_split_chunk gives the shares)
 };
 
