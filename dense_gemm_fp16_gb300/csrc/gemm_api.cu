@@ -35,7 +35,6 @@ int fail_str(int status, const std::string &msg) {
 }
 
 // Largest shared-memory staging of A the GEMV path accepts (2 rows x 40 960 halves).
-constexpr size_t kGemvMaxSmem = 160 * 1024;
 
 // Bounded-wait budget inside the fp16 kernel: long enough for any legitimate
 // stall (preemption by another context included), short enough that a broken
@@ -118,10 +117,10 @@ int gemm_f16_select(int M, int N, int K, int sm_count, gemm_f16_config *cfg) {
     // over the SMs.  (The 1-CTA 128 x 256 tile has no shape range of its own
     // between the two: it fills the SMs exactly when the pair tile fills the
     // pairs; it stays available through gemm_f16_nt_ex.)
-    // With one or two rows of A every element of B is used at most twice:
-    // reading B from HBM bounds the product, and the matrix-vector kernel
-    // streams B once (when those rows of A fit in its shared memory).  From
-    // three rows on, its fp32 FMAs fall behind HBM and the tensor cores win.
+    // With up to four rows of A every element of B is used at most four
+    // times: reading B from HBM bounds the product, and the matrix-vector
+    // kernel streams B once.  From five rows on, the A vectors it reads from
+    // L1 per vector of B hold it below HBM speed and the tensor cores win.
     // When even the 128 x 128 tiles would leave most SMs idle over a long K,
     // the pair kernel splits each pair tile's k-blocks over several pairs
     // (split-K) and spreads the work over all of them.
@@ -130,7 +129,7 @@ int gemm_f16_select(int M, int N, int K, int sm_count, gemm_f16_config *cfg) {
                        gb300::pair_split_pairs(pair_tiles, ceil_div(K, 64), sm_count / 2) > 0;
     int variant = ((pair_tiles >= sm_count / 2 && N > 128) || split) ? GEMM_F16_256x256_PAIR
                                                                      : GEMM_F16_128x128;
-    if (M <= 2 && gb300::gemv_smem_bytes(M, K) <= kGemvMaxSmem) variant = GEMM_F16_GEMV;
+    if (M <= 4) variant = GEMM_F16_GEMV;
     cfg->variant = variant;
     cfg->grid = f16_default_grid(variant, M, N, K, sm_count);
     cfg->flags = 0;
@@ -229,11 +228,8 @@ static int f16_nt_impl(int M, int N, int K, const void *A, const void *B, void *
     if (cfg && cfg->variant != GEMM_F16_AUTO) {
         sel.variant = cfg->variant;
         sel.grid = f16_default_grid(sel.variant, M, N, K, sms);
-        if (sel.variant == GEMM_F16_GEMV &&
-            (M > 2 || (K > 0 && gb300::gemv_smem_bytes(M, K) > kGemvMaxSmem)))
-            return fail(GEMM_ERR_UNSUPPORTED,
-                        "gemm_f16_nt_ex: the GEMV variant takes M <= 2 and M*K*2 <= %zu bytes "
-                        "(M=%d K=%d)", kGemvMaxSmem, M, K);
+        if (sel.variant == GEMM_F16_GEMV && M > 4)
+            return fail(GEMM_ERR_UNSUPPORTED, "gemm_f16_nt_ex: the GEMV variant takes M <= 4 (M=%d)", M);
     }
     if (cfg && cfg->grid > 0) sel.grid = cfg->grid;
     if (cfg && cfg->variant != GEMM_F16_AUTO) sel.raster = f16_default_raster(sel.variant, M, N, K);

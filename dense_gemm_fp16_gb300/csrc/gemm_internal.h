@@ -80,7 +80,7 @@ int mx_pack_scales_launch(int fmt, int rows, int K, const void *plain, void *blo
 
 int f16_status_read_clear(cudaStream_t stream, int *code, std::string &err);
 
-// One fp16 matrix-vector launch (M <= 2), after validation and selection.
+// One fp16 matrix-vector launch (M <= 4), after validation and selection.
 struct GemvLaunch {
     int M, N, K;
     const void *A;
@@ -88,17 +88,11 @@ struct GemvLaunch {
     void *C;
     cudaStream_t stream;
     int sm_count;      // CTAs are planned per SM
-    int ctas_per_sm;
+    int ctas_per_sm;   // at most this many CTAs per SM (fewer if the registers do not allow them)
     EpiSpec epi;
 };
 
 int gemv_launch(const GemvLaunch &L, std::string &err);
-
-// Shared memory a GEMV launch needs for its rows of A (bytes).
-inline size_t gemv_smem_bytes(int M, int K) {
-    const int mt = M <= 1 ? 1 : 2;
-    return static_cast<size_t>(mt) * static_cast<size_t>(K) * 2;
-}
 
 // One SGEMM launch, after validation and selection.
 struct SgemmLaunch {

@@ -150,8 +150,8 @@ enum {
     GEMM_F16_128x128 = 2,       /* one CTA per 128 x 128 output tile, 6 stages    */
     GEMM_F16_256x256_PAIR = 3,  /* a 2-CTA cluster per 256 x 256 tile (pair MMA,  */
                                 /* each CTA 128 rows of A and half of B), 6 stages */
-    GEMM_F16_GEMV = 4,          /* M <= 2: B streamed once from HBM on the CUDA    */
-                                /* cores, A's rows in shared memory                */
+    GEMM_F16_GEMV = 4,          /* M <= 4: B streamed once from HBM on the CUDA    */
+                                /* cores, a warp per row block, A read through L1  */
     GEMM_F16_NUM_VARIANTS = 5
 };
 

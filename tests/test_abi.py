@@ -156,13 +156,13 @@ def test_f16_selector(lib):
     assert g.gemm_f16_select(4096, 2048, 512, 148)[:2] == (g.GEMM_F16_256x256_PAIR, 148)
     # fewer pair tiles than SM pairs: narrow tiles
     assert g.gemm_f16_select(2048, 2048, 512, 152)[:2] == (g.GEMM_F16_128x128, 152)
-    # one or two rows of A: the HBM-bound matrix-vector kernel, planned per SM
+    # up to four rows of A: the HBM-bound matrix-vector kernel, planned per SM
     assert g.gemm_f16_select(1, 5376, 2048, 152)[:2] == (g.GEMM_F16_GEMV, 152)
     assert g.gemm_f16_select(2, 16384, 8192, 152)[:2] == (g.GEMM_F16_GEMV, 152)
-    assert g.gemm_f16_select(3, 16384, 8192, 152)[0] == g.GEMM_F16_128x128
-    # its shared-memory staging of A would not fit: the tensor-core path
-    assert g.gemm_f16_select(2, 4096, 65536, 152)[0] != g.GEMM_F16_GEMV
-    assert g.gemm_f16_select(1, 4096, 65536, 152)[0] == g.GEMM_F16_GEMV
+    assert g.gemm_f16_select(4, 16384, 8192, 152)[0] == g.GEMM_F16_GEMV
+    assert g.gemm_f16_select(5, 16384, 8192, 152)[0] == g.GEMM_F16_128x128
+    # A is read through L1, so any K goes
+    assert g.gemm_f16_select(4, 4096, 65536, 152)[0] == g.GEMM_F16_GEMV
     # too few wide tiles to fill the SMs: narrow tiles, grid = tile count
     assert g.gemm_f16_select(1024, 1024, 1024, 152)[:2] == (g.GEMM_F16_128x128, 64)
     assert g.gemm_f16_select(100, 100, 64, 152)[:2] == (g.GEMM_F16_128x128, 1)

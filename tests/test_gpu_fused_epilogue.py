@@ -3,7 +3,7 @@ rounded to half once, against the float64 oracle ("第 6 章 · Shared Memory &
 Tile", section "6.5.4 Epilogue 融合"), through the C ABI.
 
 Every fp16 kernel variant carries the epilogue: the 1-CTA tiles, the CTA pair
-(also with stream-K partials), the M <= 2 matrix-vector kernel and the K = 0
+(also with stream-K partials), the M <= 4 matrix-vector kernel and the K = 0
 fill.  Covered: all four activations, bias and residual present or absent,
 the residual aliasing C, the scalar paths (N % 8 != 0, a bias that is not
 16-byte aligned, C offset by one element), beta = 0 never reading R, and the
