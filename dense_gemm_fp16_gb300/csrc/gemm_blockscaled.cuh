@@ -731,6 +731,37 @@ __global__ void mx_pack_scales_kernel(const uint8_t *__restrict__ plain, uint8_t
 
 namespace {
 
+// The argument block of a block-scaled launch: tile_rows (128, or 256 for a
+// CTA pair) by BN output tiles, num_kb 128-byte k-blocks, TMA stores when C
+// allows them, and for NVFP4 the tensor-level scale alpha through the
+// epilogue (C = alpha * the block-scaled product); no stream-K.
+inline F16Args mx_args(const MxLaunch &L, int tile_rows, int BN, int num_kb) {
+    F16Args args;
+    args.C = static_cast<__half *>(L.C);
+    args.M = L.M;
+    args.N = L.N;
+    args.K = L.K;
+    args.m_tiles = (L.M + tile_rows - 1) / tile_rows;
+    args.n_tiles = (L.N + BN - 1) / BN;
+    args.num_kb = num_kb;
+    args.vec_store = (L.N % 8 == 0) && ((reinterpret_cast<uintptr_t>(L.C) & 15u) == 0);
+    args.tma_store = args.vec_store;
+    EpiSpec scale;
+    if (L.fmt == kFmtNv4) {
+        scale.alpha = L.alpha;
+        scale.on = 1;
+    }
+    args.epi = make_epi(scale, L.N);
+    args.timeout_ns = L.timeout_ns;
+    args.debug_skip_kblock = -1;
+    args.dp_tiles = 0;
+    args.sk_units = 0;
+    args.sk_ws = nullptr;
+    args.sk_flags = nullptr;
+    args.seq = 0;
+    return args;
+}
+
 template <int BN, int STAGES, int EBUFS, int ACC, int FMT = kFmtMx8, int EW = 4>
 int mx_launch_pair(const MxLaunch &L, std::string &err) {
     using T = MxPairCfg<BN, STAGES, EBUFS, ACC, FMT>;
@@ -788,29 +819,7 @@ int mx_launch_pair(const MxLaunch &L, std::string &err) {
         !encode_map(&tmSFB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, L.SFB, sfb_rows, 256, 2 * T::kCpt, 256, err,
                     CU_TENSOR_MAP_SWIZZLE_NONE))
         return GEMM_ERR_CUDA;
-    F16Args args;
-    args.C = static_cast<__half *>(L.C);
-    args.M = L.M;
-    args.N = L.N;
-    args.K = L.K;
-    args.m_tiles = (L.M + 255) / 256;
-    args.n_tiles = (L.N + BN - 1) / BN;
-    args.num_kb = kbt;
-    args.vec_store = (L.N % 8 == 0) && ((reinterpret_cast<uintptr_t>(L.C) & 15u) == 0);
-    args.tma_store = args.vec_store;
-    EpiSpec scale;  // NVFP4: C = alpha * (the block-scaled product)
-    if (FMT == kFmtNv4) {
-        scale.alpha = L.alpha;
-        scale.on = 1;
-    }
-    args.epi = make_epi(scale, L.N);
-    args.timeout_ns = L.timeout_ns;
-    args.debug_skip_kblock = -1;
-    args.dp_tiles = 0;
-    args.sk_units = 0;
-    args.sk_ws = nullptr;
-    args.sk_flags = nullptr;
-    args.seq = 0;
+    const F16Args args = mx_args(L, 256, BN, kbt);
     if (args.tma_store && !encode_map(&tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, L.C, L.M, L.N, 32,
                                       EW == 8 ? 32 : 64, err,
                                       EW == 8 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B))
@@ -856,29 +865,7 @@ int mx_launch_1cta(const MxLaunch &L, std::string &err) {
         return GEMM_ERR_CUDA;
     if (!encode_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, L.B, L.N, kbytes, BN, kMxBK, err))
         return GEMM_ERR_CUDA;
-    F16Args args;
-    args.C = static_cast<__half *>(L.C);
-    args.M = L.M;
-    args.N = L.N;
-    args.K = L.K;
-    args.m_tiles = (L.M + kBM - 1) / kBM;
-    args.n_tiles = (L.N + BN - 1) / BN;
-    args.num_kb = (kbytes + kMxBK - 1) / kMxBK;
-    args.vec_store = (L.N % 8 == 0) && ((reinterpret_cast<uintptr_t>(L.C) & 15u) == 0);
-    args.tma_store = args.vec_store;
-    EpiSpec scale;  // NVFP4: C = alpha * (the block-scaled product)
-    if (FMT == kFmtNv4) {
-        scale.alpha = L.alpha;
-        scale.on = 1;
-    }
-    args.epi = make_epi(scale, L.N);
-    args.timeout_ns = L.timeout_ns;
-    args.debug_skip_kblock = -1;
-    args.dp_tiles = 0;
-    args.sk_units = 0;
-    args.sk_ws = nullptr;
-    args.sk_flags = nullptr;
-    args.seq = 0;
+    const F16Args args = mx_args(L, kBM, BN, (kbytes + kMxBK - 1) / kMxBK);
     // C boxes: 32 rows x 64 columns (128-byte swizzle) for the 4-warp staged
     // epilogue, 32 x 32 (64-byte swizzle) for the 8-warp one
     if (args.tma_store && !encode_map(&tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, L.C, L.M, L.N, 32,
