@@ -29,7 +29,7 @@ def _lib():
     torch.cuda.init()
 
 
-def _run(A, B, variant=g.GEMM_F16_AUTO, grid=0, pad=64, flags=0):
+def _run(A, B, variant=g.GEMM_F16_AUTO, grid=0, pad=64, flags=0, raster=0):
     """Run on the GPU with a sentinel guard of `pad` halves around C."""
     M, K = A.shape
     N = B.shape[0]
@@ -39,7 +39,7 @@ def _run(A, B, variant=g.GEMM_F16_AUTO, grid=0, pad=64, flags=0):
     buf = buf.view(torch.float16)
     C = buf[pad:pad + M * N].view(M, N)
     g.gemm_f16_nt_ex(M, N, K, dA.data_ptr(), dB.data_ptr(), C.data_ptr(),
-                     torch.cuda.current_stream().cuda_stream, variant, grid, flags)
+                     torch.cuda.current_stream().cuda_stream, variant, grid, flags, raster)
     g.gemm_check_device_status(torch.cuda.current_stream().cuda_stream)
     host = buf.cpu()
     guard = torch.cat([host[:pad], host[pad + M * N:]]).view(torch.int16).numpy().view(np.uint16)
@@ -263,3 +263,21 @@ def test_f16_nt_split_k_selector_shapes_sampled(M, N, K):
     Cref, S = oracle.gemm_f16_nt_sampled(A, B, rows, cols)
     check_f16(Ch[rows, cols], Cref, S, what=f"split-K default {M}x{N}x{K}")
 
+
+
+@pytest.mark.parametrize("variant,grid,flags", [
+    (g.GEMM_F16_256x256_PAIR, 0, 0),
+    (g.GEMM_F16_256x256_PAIR, 6, g.GEMM_F16_FLAG_STREAM_K),  # 3 pairs: stream-K over the last round
+    (g.GEMM_F16_128x128, 7, 0),
+    (g.GEMM_F16_128x256, 0, 0),
+])
+@pytest.mark.parametrize("raster", [1, 2, 3, 8])
+def test_f16_nt_banded_tile_order(variant, grid, flags, raster):
+    # The persistent CTAs walk the tiles in bands of `raster` tile rows (the
+    # last band shorter); every tile is computed once, whatever the band.
+    M, N, K = 1160, 1100, 192
+    A = wl.draw_f16((M, K), seed=71, dist="normal")
+    B = wl.draw_f16((N, K), seed=72, dist="normal")
+    Cref, S = oracle.gemm_f16_nt(A, B)
+    C = _run(A, B, variant, grid, flags=flags, raster=raster)
+    check_f16(C, Cref, S, what=f"raster {raster} v{variant} grid {grid} flags {flags}")

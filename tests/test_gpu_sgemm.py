@@ -136,7 +136,7 @@ V1, V2 = g.GEMM_SGEMM_128x128, g.GEMM_SGEMM_64x64
     (1024, 1024, 1024, 1.0, 0.5, V1, 4),    # the 1024-cube size with a beta term: 64 tiles
     (1024, 1024, 1024, 1.0, 0.5, 0, 0),     # the library's own plan for it
     (300, 200, 1000, -2.0, 0.25, V1, 8),    # 6 ragged tiles, a partial last share
-    (130, 260, 4100, 0.5, 0.0, V1, 0),      # K not a multiple of 4: the element-wise loads
+    (130, 260, 4099, 0.5, 0.0, V1, 0),      # K not a multiple of 4: the element-wise loads
     (128, 128, 65536, 1.0, 1.0, V1, 8),     # one tile, 8 shares of 8192
     (200, 150, 3000, 1.0, 0.5, V2, 6),      # the 64 x 64 tile, ragged
     (64, 1024, 4096, 1.5, 0.0, V2, 7),      # skinny M
