@@ -275,11 +275,13 @@ typedef struct {
 enum {
     GEMM_MXFP8_AUTO = 0,
     GEMM_MXFP8_128x128 = 1,       /* 1-CTA 128 x 128 tiles, 5 stages (default for N <= 128) */
-    GEMM_MXFP8_256x128_PAIR = 2,  /* CTA pair (cta_group::2) 256 x 128 tiles, 7 stages      */
-    GEMM_MXFP8_128x256 = 3,       /* 1-CTA 128 x 256 tiles, N = 256 MMAs, one accumulator,
-                                     4 stages (default for N > 128); NVFP4: 8 epilogue warps
-                                     that release the accumulator from registers             */
-    GEMM_MXFP8_256x256_PAIR = 4,  /* CTA pair 256 x 256 tiles, one accumulator, 6 stages    */
+    GEMM_MXFP8_256x128_PAIR = 2,  /* CTA pair (cta_group::2) 256 x 128 tiles, 7 stages
+                                     (NVFP4: 6)                                            */
+    GEMM_MXFP8_128x256 = 3,       /* 1-CTA 128 x 256 tiles, N = 256 MMAs, one accumulator
+                                     that 8 epilogue warps release from registers, 4 stages
+                                     (NVFP4: 3); default for N > 128                        */
+    GEMM_MXFP8_256x256_PAIR = 4,  /* CTA pair 256 x 256 tiles, one accumulator released by
+                                     8 epilogue warps, 6 stages (NVFP4: 5)                  */
     GEMM_MXFP8_NUM_VARIANTS = 5
 };
 
