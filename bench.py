@@ -28,6 +28,8 @@ ranks is taken and rank 0 prints one JSON line.
   against the FP32 FFMA peak.
 * ``gemv``: the M = 1 matrix-vector product 1 × 16384 × 8192 against the
   measured HBM copy bandwidth.
+* ``skinny``: the same B against 16 rows of A (16 × 16384 × 8192, the skinny
+  tensor-core kernel), also against the HBM copy bandwidth.
 * ``fused_epilogue``: the headline product with bias, residual and
   tanh-GELU fused (``gemm_f16_nt_fused``), beside the plain product and the
   unfused sequence (plain product, then PyTorch element-wise kernels).
@@ -539,6 +541,32 @@ def run_ours(args):
                                      "bytes_per_call": gbytes,
                                      "peak_source": f"{peak_kind} HBM copy bandwidth"}}
         g.gemm_check_device_status(sh)
+
+        # ---- 16 rows of A against the same B: the skinny tensor-core kernel
+        kw = wl.WORKLOADS["f16_skinny_16x16384x8192"]
+        # (its B is the matrix-vector workload's, already on the device)
+        assert (kw.N, kw.K, kw.seed_b, kw.dist) == (gw.N, gw.K, gw.seed_b, gw.dist)
+        kA = wl.draw_f16((kw.M, kw.K), kw.seed_a, kw.dist)
+        with torch.cuda.stream(stream):
+            dka = kA.cuda()
+            dkc = torch.empty((kw.M, kw.N), dtype=torch.float16, device="cuda")
+        stream.synchronize()
+        k_variant = g.gemm_f16_select(kw.M, kw.N, kw.K, sm_count)[0]
+
+        def sk(_):
+            g.gemm_f16_nt(kw.M, kw.N, kw.K, dka.data_ptr(), dgb.data_ptr(), dkc.data_ptr(), sh)
+        region_time(sk, stream, 5)
+        t_sk = region_time(sk, stream, n_gv) / n_gv
+        kbytes = 2 * (kw.N * kw.K + kw.M * kw.K + kw.M * kw.N)
+        k_gbs = kbytes / (t_sk * 1e-3) / 1e9
+        line["skinny"] = {"workload": kw.name, "value": kw.flop / (t_sk * 1e-3) / 1e12,
+                          "unit": "TFLOP/s", "us_per_call": 1e3 * t_sk, "variant": k_variant,
+                          "roofline": {"bound": "hbm", "achieved": k_gbs, "peak": hbm,
+                                       "unit": "GB/s", "frac": k_gbs / hbm,
+                                       "bytes_per_call": kbytes,
+                                       "peak_source": f"{peak_kind} HBM copy bandwidth"}}
+        g.gemm_check_device_status(sh)
+        del dka, dkc
 
     # ---- fused epilogue on the headline product: tanh-GELU(A·Bᵀ + bias + R)
     # against the plain product and against the unfused sequence (the plain

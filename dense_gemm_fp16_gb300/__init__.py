@@ -35,6 +35,8 @@ from ._binding import (  # noqa: F401
     GEMM_F16_AUTO,
     GEMM_F16_FLAG_STREAM_K,
     GEMM_F16_GEMV,
+    GEMM_F16_SKINNY,
+    GEMM_F16_NUM_VARIANTS,
     GEMM_MXFP8_128x128,
     GEMM_MXFP8_128x256,
     GEMM_MXFP8_256x128_PAIR,

@@ -25,7 +25,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(PKG, "libgemm.so")
 
-SOURCES = ["gemm_f16_nt.cu", "gemv_f16_nt.cu", "sgemm.cu", "gemm_api.cu"]
+SOURCES = ["gemm_f16_nt.cu", "gemv_f16_nt.cu", "gemm_skinny.cu", "sgemm.cu", "gemm_api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
               "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

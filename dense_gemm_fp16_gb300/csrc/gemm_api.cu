@@ -69,7 +69,8 @@ inline long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 // to one per SM.
 int f16_default_grid(int variant, int M, int N, int K, int sm_count) {
     long long tiles;
-    if (variant == GEMM_F16_GEMV) return sm_count;  // planned per SM by the GEMV launcher
+    if (variant == GEMM_F16_GEMV) return sm_count;  // planned per SM by the launcher
+    if (variant == GEMM_F16_SKINNY) return sm_count * gb300::skinny_ctas_per_sm();  // the split's CTA target
     switch (variant) {
         case GEMM_F16_128x256: tiles = ceil_div(M, 128) * ceil_div(N, 256); break;
         case GEMM_F16_256x256_PAIR: tiles = 2 * ceil_div(M, 256) * ceil_div(N, 256); break;
@@ -101,7 +102,8 @@ const char *gemm_last_error(void) { return t_last_error.c_str(); }
 // the tiles go in bands of a few rows.
 static int f16_default_raster(int variant, int M, int N, int K) {
     const double operand_bytes = 2.0 * (static_cast<double>(M) + N) * K;
-    if (variant == GEMM_F16_GEMV || operand_bytes <= 96.0 * 1024 * 1024) return 1 << 30;
+    if (variant == GEMM_F16_GEMV || variant == GEMM_F16_SKINNY || operand_bytes <= 96.0 * 1024 * 1024)
+        return 1 << 30;
     return variant == GEMM_F16_256x256_PAIR ? 8 : 16;
 }
 
@@ -117,10 +119,12 @@ int gemm_f16_select(int M, int N, int K, int sm_count, gemm_f16_config *cfg) {
     // over the SMs.  (The 1-CTA 128 x 256 tile has no shape range of its own
     // between the two: it fills the SMs exactly when the pair tile fills the
     // pairs; it stays available through gemm_f16_nt_ex.)
-    // With up to four rows of A every element of B is used at most four
-    // times: reading B from HBM bounds the product, and the matrix-vector
-    // kernel streams B once.  From five rows on, the A vectors it reads from
-    // L1 per vector of B hold it below HBM speed and the tensor cores win.
+    // With a few rows of A every element of B is used only a few times:
+    // reading B from HBM bounds the product.  For one row the matrix-vector
+    // kernel streams B once on the CUDA cores; from two rows up to 64 the
+    // skinny kernel does (B's rows on the MMA's 128-row side, A's rows on
+    // its N side, K split over clusters so the tiles fill the SMs), where
+    // the 128-row tiles of A would leave most of each MMA and most SMs idle.
     // When even the 128 x 128 tiles would leave most SMs idle over a long K,
     // the pair kernel splits each pair tile's k-blocks over several pairs
     // (split-K) and spreads the work over all of them.
@@ -129,7 +133,7 @@ int gemm_f16_select(int M, int N, int K, int sm_count, gemm_f16_config *cfg) {
                        gb300::pair_split_pairs(pair_tiles, ceil_div(K, 64), sm_count / 2) > 0;
     int variant = ((pair_tiles >= sm_count / 2 && N > 128) || split) ? GEMM_F16_256x256_PAIR
                                                                      : GEMM_F16_128x128;
-    if (M <= 4) variant = GEMM_F16_GEMV;
+    if (M <= 64) variant = M <= 1 ? GEMM_F16_GEMV : GEMM_F16_SKINNY;
     cfg->variant = variant;
     cfg->grid = f16_default_grid(variant, M, N, K, sm_count);
     cfg->flags = 0;
@@ -230,6 +234,8 @@ static int f16_nt_impl(int M, int N, int K, const void *A, const void *B, void *
         sel.grid = f16_default_grid(sel.variant, M, N, K, sms);
         if (sel.variant == GEMM_F16_GEMV && M > 4)
             return fail(GEMM_ERR_UNSUPPORTED, "gemm_f16_nt_ex: the GEMV variant takes M <= 4 (M=%d)", M);
+        if (sel.variant == GEMM_F16_SKINNY && M > 64)
+            return fail(GEMM_ERR_UNSUPPORTED, "gemm_f16_nt_ex: the skinny variant takes M <= 64 (M=%d)", M);
     }
     if (cfg && cfg->grid > 0) sel.grid = cfg->grid;
     if (cfg && cfg->variant != GEMM_F16_AUTO) sel.raster = f16_default_raster(sel.variant, M, N, K);
@@ -493,6 +499,10 @@ int gemm_check_device_status(gemm_stream_t stream) {
     std::string err;
     int st = gb300::f16_status_read_clear(reinterpret_cast<cudaStream_t>(stream), &code, err);
     if (st != GEMM_OK) return fail_str(st, err);
+    int sk = 0;
+    st = gb300::skinny_status_read_clear(reinterpret_cast<cudaStream_t>(stream), &sk, err);
+    if (st != GEMM_OK) return fail_str(st, err);
+    if (code == 0 && sk >= 1 && sk <= 3) code = sk;
     if (code != 0) {
         static const char *role[] = {"?", "TMA producer (free-slot wait)",
                                      "MMA issuer (data or accumulator wait)",

@@ -1006,6 +1006,8 @@ __global__ void zero_half_kernel(__half *C, int M, int N, Epi epi) {
 // Host side: tensor maps and launch
 // ---------------------------------------------------------------------------
 
+}  // namespace
+
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                    const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
                                    const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -1029,14 +1031,9 @@ EncodeTiledFn get_encode_fn(std::string &err) {
     return fn;
 }
 
-// Row-major 2-D tensor of halves [rows, cols]: box = box_rows x box_cols,
-// 128-byte swizzle (box_cols * 2 == 128), zero fill out of bounds on loads,
-// clipping on stores.
-// A row-major [rows][cols] matrix of `elem_bytes`-byte elements, boxes of
-// box_rows x box_cols, 128-byte swizzle.
+// (declared in gemm_internal.h, shared with the other translation units)
 bool encode_map(CUtensorMap *map, CUtensorMapDataType dtype, int elem_bytes, const void *ptr, int rows,
-                int cols, int box_rows, int box_cols, std::string &err,
-                CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
+                int cols, int box_rows, int box_cols, std::string &err, CUtensorMapSwizzle swizzle) {
     EncodeTiledFn enc = get_encode_fn(err);
     if (!enc) return false;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
@@ -1058,6 +1055,8 @@ bool encode_map(CUtensorMap *map, CUtensorMapDataType dtype, int elem_bytes, con
     }
     return true;
 }
+
+namespace {
 
 bool encode_half_map(CUtensorMap *map, const void *ptr, int rows, int cols, int box_rows,
                      int box_cols, std::string &err) {
@@ -1442,6 +1441,12 @@ int f16_launch(const F16Launch &L, std::string &err) {
         case GEMM_F16_GEMV: {
             GemvLaunch G{L.M, L.N, L.K, L.A, L.B, L.C, L.stream, L.sm_count, 4, L.epi};
             return gemv_launch(G, err);
+        }
+        case GEMM_F16_SKINNY: {
+            // the grid is the CTA count the K split aims for
+            SkinnyLaunch S{L.M, L.N, L.K, L.A, L.B, L.C, L.stream,
+                           L.grid > 0 ? L.grid : L.sm_count * skinny_ctas_per_sm(), L.timeout_ns, L.epi};
+            return skinny_launch(S, err);
         }
         default: err = "unknown fp16 variant"; return GEMM_ERR_INVALID_ARG;
     }

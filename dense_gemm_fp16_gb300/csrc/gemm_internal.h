@@ -2,12 +2,21 @@
 // libgemm.so (never installed, never part of the C ABI).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
 #include <string>
 
 namespace gb300 {
+
+// A row-major [rows][cols] matrix of `elem_bytes`-byte elements at `ptr` as a
+// 2-D TMA tensor map with boxes of box_rows x box_cols (zero fill past the
+// edges on loads, clipping on stores).  cuTensorMapEncodeTiled is looked up
+// through the runtime once.  false, with `err` set, on failure.
+bool encode_map(CUtensorMap *map, CUtensorMapDataType dtype, int elem_bytes, const void *ptr, int rows,
+                int cols, int box_rows, int box_cols, std::string &err,
+                CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B);
 
 // Split-K for pair-tile grids the tiles alone would leave mostly idle: how
 // many CTA pairs share the k-blocks of all `tiles` tiles (each tile split
@@ -93,6 +102,36 @@ struct GemvLaunch {
 };
 
 int gemv_launch(const GemvLaunch &L, std::string &err);
+
+// One fp16 product with a few rows of A (M <= 64), computed as B * A^T on the
+// tensor cores with the K range split over CTAs, after validation.
+struct SkinnyLaunch {
+    int M, N, K;
+    const void *A;
+    const void *B;
+    void *C;
+    cudaStream_t stream;
+    int ctas;              // CTA count the K split aims for (tiles x shares <= ctas)
+    uint64_t timeout_ns;
+    EpiSpec epi;           // fused epilogue (epi.on == 0: the plain product)
+};
+
+constexpr int kSkMaxSplits = 8;
+
+// CTAs of the skinny kernel resident per SM (its default CTA target is this
+// times the SM count).
+int skinny_ctas_per_sm();
+
+// The shares of K a skinny launch plans for (1, 2, 4 or 8: the cluster size;
+// returned) and the 64-deep k-blocks of each (*kb_per_split; the last share
+// may be shorter).  The launch halves the shares while the device cannot
+// hold all the clusters at once.
+int skinny_split_plan(int N, int K, int ctas, int *kb_per_split);
+
+int skinny_launch(const SkinnyLaunch &L, std::string &err);
+
+// Read-and-clear the skinny kernel's device status word (0 = no timeout).
+int skinny_status_read_clear(cudaStream_t stream, int *code, std::string &err);
 
 // One SGEMM launch, after validation and selection.
 struct SgemmLaunch {

@@ -1,0 +1,486 @@
+// gemm_skinny.cu -- C = A * B^T for a few rows of A (5 <= M <= 64) on the
+// tensor cores, as the swapped product D = B * A^T (D = C^T).
+//
+// Same operation and numerics as gemm_f16_nt (half inputs, fp32
+// accumulation, one round-to-nearest-even per output).  With M this small, B
+// is read once and the work is bound by HBM.  The tile kernels' 128-row tiles
+// of A would leave 120 of the MMA's 128 rows empty and give one tile per
+// 128 columns of C: at N = 8192, 64 CTAs for 152 SMs.  Here B's rows take the
+// MMA's M = 128 and A's rows its N (16, 32 or 64, the rows past M zero-filled
+// by TMA), so a tile is 128 columns of C by all of its rows, and the K range
+// is split over enough CTAs to fill the SMs ("第 6 章 · Shared Memory & Tile",
+// section "6.5.6 Split-K / Stream-K").
+//
+// Per CTA: warp 0 issues TMA loads of B's 128 x 64 box and A's MN x 64 box
+// per k-block into a ring of STAGES stages (128-byte swizzle), warp 1 issues
+// the k-blocks' tcgen05.mma (M = 128, N = MN, K = 16) into one TMEM
+// accumulator, warps 2-5 read it back: TMEM lane n holds D[n][0..MN), so lane
+// n stores C[m][n] for every m, 32 consecutive columns of C per warp and row.
+// With a split, the CTAs that share a tile's K range form one thread-block
+// cluster (2, 4 or 8 CTAs): each puts its fp32 share in its own shared
+// memory, and after a cluster barrier CTA r adds slice r of the tile over all
+// the shares, read through distributed shared memory in split order, so
+// results do not depend on timing and no share goes through HBM.
+// Every wait is bounded as in the other kernels.
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "gemm.h"
+#include "epilogue.cuh"
+#include "gemm_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace gb300 {
+namespace {
+
+__device__ int g_skinny_status = 0;
+__device__ __forceinline__ void skinny_timeout(int code) { atomicCAS(&g_skinny_status, 0, code); }
+
+constexpr int kSkBM = 128;       // rows of B per tile: the MMA's M
+constexpr int kSkBK = 64;        // halves per k-block: one 128-byte swizzle row
+constexpr int kSkThreads = 192;  // warp 0 producer, warp 1 MMA, warps 2-5 epilogue
+constexpr int kSkCtasPerSm = 1;  // CTAs resident per SM (their stages keep HBM busy)
+
+template <int MN, int STAGES>
+struct SkCfg {
+    static constexpr int kBBytes = kSkBM * kSkBK * 2;  // 16 KB: 128 rows of B
+    static constexpr int kABytes = MN * kSkBK * 2;     // MN rows of A (zero past M)
+    static constexpr int kStageBytes = kBBytes + kABytes;
+    static constexpr int kTmemCols = MN < 32 ? 32 : MN;
+    static constexpr int kNumBars = 2 * STAGES + 2;    // full, empty, accumulator ready, drain
+    static constexpr int kBarOffset = STAGES * kStageBytes;
+    static constexpr int kSmemBytes = 1024 + kBarOffset + kNumBars * 8 + 16;  // + TMEM slot and flags
+    static_assert(MN == 16 || MN == 32 || MN == 64, "an MMA N for M = 128");
+    static_assert(kABytes % 1024 == 0, "stages keep the 1 KB alignment of the swizzled boxes");
+    static_assert(kSmemBytes <= 232448, "fits the 227 KB opt-in limit");
+};
+
+// Ring stages that let kSkCtasPerSm CTAs share an SM's 228 KB (1 KB of it
+// reserved per CTA), at most 8.
+template <int MN>
+constexpr int sk_stages() {
+    constexpr int stage = kSkBM * kSkBK * 2 + MN * kSkBK * 2;
+    constexpr int per_cta = 233472 / kSkCtasPerSm - 1024 - 1024 - 256;  // reserve, alignment, barriers
+    return per_cta / stage > 8 ? 8 : per_cta / stage;
+}
+
+struct SkArgs {
+    __half *C;
+    int M, N, K;
+    int num_kb;        // 64-deep k-blocks of K
+    int kb_per_split;  // k-blocks per share (the last may be shorter)
+    int splits;        // shares of K per tile: 1, or the cluster size (2, 4, 8)
+    uint64_t timeout_ns;
+    Epi epi;           // fused epilogue, applied where the fp32 sum is rounded
+};
+
+// One output through the epilogue and rounded to half.
+__device__ __forceinline__ __half skinny_out(const Epi &e, float x, int m, int n, int N) {
+    if (e.on) {
+        const float b = e.bias ? __half2float(e.bias[n]) : 0.f;
+        const float r = e.reads_res() ? __half2float(e.res[static_cast<size_t>(m) * N + n]) : 0.f;
+        x = epi_apply1(e, x, b, r);
+    }
+    return __float2half_rn(x);
+}
+
+// Four fp32 values at a shared::cluster address (another CTA's shared memory).
+__device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+// Whole warp: 16 consecutive 32-bit TMEM columns of this warp's 32 lanes.
+__device__ __forceinline__ void tmem_load_16cols(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+
+template <int MN, int STAGES>
+__global__ void __launch_bounds__(kSkThreads, 1)
+    gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmA,
+                       const SkArgs args) {
+    using T = SkCfg<MN, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+    const uint32_t sbase = smem_addr(smem);
+
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + T::kBarOffset);
+    const uint32_t bar0 = smem_addr(bars);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    const uint32_t accf_bar = bar0 + 8u * (2 * STAGES);
+    const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 1);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + T::kNumBars);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    __shared__ int never_abort;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int tile = blockIdx.x;   // 128 columns of C
+    const int split = blockIdx.y;  // share of K
+    const int kb0 = split * args.kb_per_split;
+    const int kb1 = kb0 + args.kb_per_split < args.num_kb ? kb0 + args.kb_per_split : args.num_kb;
+
+    if (threadIdx.x == 0) {
+        tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmA);
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        mbar_init(accf_bar, 1);
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        never_abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr(tmem_slot), T::kTmemCols);
+        tmem_relinquish_alloc_permit();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+    pdl_launch_dependents();
+    pdl_wait_prerequisites();
+
+    uint32_t armed = 0, arm_parity = 0;
+    uint32_t v[MN];  // epilogue warps: this lane's accumulators (fp32 bits)
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int kb = kb0; kb < kb1; ++kb) {
+                if (!mbar_wait(empty_bar(stage), phase ^ 1u, args.timeout_ns, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t sb = sbase + stage * T::kStageBytes;
+                mbar_arrive_expect_tx(full_bar(stage), T::kStageBytes);
+                armed |= 1u << stage;
+                arm_parity ^= 1u << stage;
+                tma_load_2d(sb, &tmB, full_bar(stage), kb * kSkBK, tile * kSkBM);
+                tma_load_2d(sb + T::kBBytes, &tmA, full_bar(stage), kb * kSkBK, 0);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) {
+                if (!*abort_flag) skinny_timeout(1);
+                *abort_flag = 1;
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            constexpr uint32_t idesc = idesc_f16_f32acc(kSkBM, MN);
+            for (int kb = kb0; kb < kb1; ++kb) {
+                if (!mbar_wait(full_bar(stage), phase, args.timeout_ns, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t sb = sbase + stage * T::kStageBytes;
+                const uint64_t bdesc_rows = sw128_kmajor_desc(sb);               // B: the MMA's A operand
+                const uint64_t adesc_rows = sw128_kmajor_desc(sb + T::kBBytes);  // A: the MMA's B operand
+#pragma unroll
+                for (int k = 0; k < kSkBK / 16; ++k)
+                    mma_f16_ss(tmem_base, bdesc_rows + 2u * k, adesc_rows + 2u * k, idesc,
+                               (kb > kb0 || k > 0) ? 1u : 0u);
+                mma_commit(empty_bar(stage));
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            // (with no k-blocks the commit arrives at once and the epilogue writes zeros)
+            if (ok) mma_commit(accf_bar);
+            if (!ok) {
+                if (!*abort_flag) skinny_timeout(2);
+                *abort_flag = 1;
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue, 4 warps
+        const int quarter = warp & 3;  // TMEM lanes this warp may read
+        int ok = 1;
+        if (lane == 0) ok = mbar_wait(accf_bar, 0, args.timeout_ns, abort_flag) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+#pragma unroll
+        for (int m = 0; m < MN; ++m) v[m] = 0u;  // (stays 0 with no k-blocks)
+        if (ok && kb1 > kb0) {
+            tc_fence_after_sync();
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+            if constexpr (MN == 16) {
+                tmem_load_16cols(taddr, v);
+            } else {
+#pragma unroll
+                for (int c = 0; c < MN / 32; ++c)
+                    tmem_load_32cols(taddr + 32u * c, *reinterpret_cast<uint32_t(*)[32]>(&v[32 * c]));
+            }
+        }
+        if (!ok && lane == 0) {
+            if (!*abort_flag) skinny_timeout(3);
+            *abort_flag = 1;
+        }
+        const int n = tile * kSkBM + quarter * 32 + lane;
+        if (args.splits == 1 && ok && n < args.N) {
+#pragma unroll
+            for (int m = 0; m < MN; ++m) {
+                if (m >= args.M) break;
+                args.C[static_cast<size_t>(m) * args.N + n] =
+                    skinny_out(args.epi, __uint_as_float(v[m]), m, n, args.N);
+            }
+        }
+        __syncwarp();
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (*abort_flag) {
+        // let this CTA's own copies and MMAs in flight finish before its
+        // shared memory and TMEM are released
+        if (warp == 0 && lane == 0) {
+            for (int s = 0; s < STAGES; ++s)
+                if (armed & (1u << s))
+                    (void)mbar_wait(full_bar(s), ((arm_parity >> s) & 1u) ^ 1u, args.timeout_ns, &never_abort);
+        }
+        if (warp == 1 && lane == 0) {
+            mma_commit(drain_bar);
+            (void)mbar_wait(drain_bar, 0, args.timeout_ns, &never_abort);
+        }
+        __syncwarp();
+        tc_fence_before_sync();
+        __syncthreads();
+    }
+    if (args.splits > 1) {
+        // ------------------------------------------- sum of the cluster's shares
+        // The ring is idle now (every load was consumed by an MMA that has
+        // completed, or drained above): its first 32 KB hold this CTA's share,
+        // [M][128] fp32.  Every thread of every CTA in the cluster passes
+        // both cluster barriers.
+        float *share = reinterpret_cast<float *>(smem);
+        if (warp >= 2) {
+            const int nl = (warp & 3) * 32 + lane;
+#pragma unroll
+            for (int m = 0; m < MN; ++m) {
+                if (m >= args.M) break;
+                share[m * kSkBM + nl] = __uint_as_float(v[m]);
+            }
+        }
+        cluster_sync();
+        // CTA r of the cluster (r = its share of K) adds slice r of the tile,
+        // four consecutive columns per thread, over the shares in order.
+        const int groups = args.M * (kSkBM / 4);
+        const int per = (groups + args.splits - 1) / args.splits;
+        const int g0 = split * per;
+        const int g1 = g0 + per < groups ? g0 + per : groups;
+        const bool vec = (args.N & 3) == 0 && (reinterpret_cast<uintptr_t>(args.C) & 7u) == 0;
+        for (int gi = g0 + static_cast<int>(threadIdx.x); gi < g1; gi += kSkThreads) {
+            const uint32_t at = sbase + static_cast<uint32_t>(gi) * 16u;
+            float4 sum = ld_dsmem_f4(mapa_shared(at, 0));
+            for (int sp = 1; sp < args.splits; ++sp) {
+                const float4 x = ld_dsmem_f4(mapa_shared(at, static_cast<uint32_t>(sp)));
+                sum.x += x.x;
+                sum.y += x.y;
+                sum.z += x.z;
+                sum.w += x.w;
+            }
+            const int m = gi / (kSkBM / 4);
+            const int n = tile * kSkBM + (gi % (kSkBM / 4)) * 4;
+            __half *out = args.C + static_cast<size_t>(m) * args.N + n;
+            const float s4[4] = {sum.x, sum.y, sum.z, sum.w};
+            if (vec && n + 3 < args.N) {
+                __half2 lo = __halves2half2(skinny_out(args.epi, s4[0], m, n, args.N),
+                                            skinny_out(args.epi, s4[1], m, n + 1, args.N));
+                __half2 hi = __halves2half2(skinny_out(args.epi, s4[2], m, n + 2, args.N),
+                                            skinny_out(args.epi, s4[3], m, n + 3, args.N));
+                uint2 w;
+                w.x = *reinterpret_cast<uint32_t *>(&lo);
+                w.y = *reinterpret_cast<uint32_t *>(&hi);
+                *reinterpret_cast<uint2 *>(out) = w;
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (n + j < args.N) out[j] = skinny_out(args.epi, s4[j], m, n + j, args.N);
+            }
+        }
+        cluster_sync();  // no CTA leaves while another still reads its share
+    }
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, T::kTmemCols);
+    }
+}
+
+// Clusters of `size` CTAs of this kernel the device holds at once (cached).
+template <int MN, int S>
+int max_clusters(int size, std::string &err) {
+    static std::mutex mu;
+    static std::map<std::pair<int, int>, int> cache;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        err = std::string("cudaGetDevice: ") + cudaGetErrorString(e);
+        return -1;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find({dev, size});
+    if (it != cache.end()) return it->second;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = size;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(1, size);
+    cfg.blockDim = dim3(kSkThreads);
+    cfg.dynamicSmemBytes = SkCfg<MN, S>::kSmemBytes;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, gemm_skinny_kernel<MN, S>, &cfg);
+    if (e != cudaSuccess) {
+        err = std::string("cudaOccupancyMaxActiveClusters: ") + cudaGetErrorString(e);
+        return -1;
+    }
+    cache[{dev, size}] = n;
+    return n;
+}
+
+template <int MN>
+int launch_mn(const SkinnyLaunch &L, std::string &err) {
+    constexpr int S = sk_stages<MN>();
+    using T = SkCfg<MN, S>;
+    auto kernel = gemm_skinny_kernel<MN, S>;
+    static int configured[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        err = std::string("cudaGetDevice: ") + cudaGetErrorString(e);
+        return GEMM_ERR_CUDA;
+    }
+    if (dev < 0 || dev >= 64 || !configured[dev]) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, T::kSmemBytes);
+        if (e != cudaSuccess) {
+            err = std::string("cudaFuncSetAttribute(max dynamic smem): ") + cudaGetErrorString(e);
+            return GEMM_ERR_CUDA;
+        }
+        if (dev >= 0 && dev < 64) configured[dev] = 1;
+    }
+    const int tiles = (L.N + kSkBM - 1) / kSkBM;
+    const int num_kb = (L.K + kSkBK - 1) / kSkBK;
+    int kb_per_split = num_kb;
+    int splits = skinny_split_plan(L.N, L.K, L.ctas, &kb_per_split);
+    // fewer shares while the clusters would not all be resident at once
+    while (splits > 1) {
+        const int fit = max_clusters<MN, S>(splits, err);
+        if (fit < 0) return GEMM_ERR_CUDA;
+        if (fit >= tiles) break;
+        splits /= 2;
+        kb_per_split = (num_kb + splits - 1) / splits;
+    }
+    const SkArgs args{static_cast<__half *>(L.C), L.M, L.N, L.K, num_kb, kb_per_split, splits, L.timeout_ns,
+                      make_epi(L.epi, L.N)};
+    CUtensorMap tmB, tmA;
+    if (!encode_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, L.B, L.N, L.K, kSkBM, kSkBK, err) ||
+        !encode_map(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, L.A, L.M, L.K, MN, kSkBK, err))
+        return GEMM_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 1;
+    attr[1].val.clusterDim.y = splits;
+    attr[1].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(tiles, splits);
+    cfg.blockDim = dim3(kSkThreads);
+    cfg.dynamicSmemBytes = T::kSmemBytes;
+    cfg.stream = L.stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = splits > 1 ? 2 : 1;
+    e = cudaLaunchKernelEx(&cfg, kernel, tmB, tmA, args);
+    if (e != cudaSuccess) {
+        err = std::string("skinny kernel launch: ") + cudaGetErrorString(e);
+        return GEMM_ERR_CUDA;
+    }
+    return GEMM_OK;
+}
+
+}  // namespace
+
+int skinny_ctas_per_sm() { return kSkCtasPerSm; }
+
+int skinny_split_plan(int N, int K, int ctas, int *kb_per_split) {
+    const int tiles = (N + kSkBM - 1) / kSkBM;
+    const int num_kb = (K + kSkBK - 1) / kSkBK;
+    // the largest power of two of shares that the CTA target allows, each
+    // share at least 8 k-blocks, at most 8 shares (the portable cluster size)
+    int cap = ctas / (tiles > 0 ? tiles : 1);
+    if (cap > num_kb / 8) cap = num_kb / 8;
+    if (cap > kSkMaxSplits) cap = kSkMaxSplits;
+    int splits = 1;
+    while (splits * 2 <= cap) splits *= 2;
+    const int per = (num_kb + splits - 1) / splits;
+    *kb_per_split = per > 1 ? per : 1;
+    return splits;
+}
+
+int skinny_launch(const SkinnyLaunch &L, std::string &err) {
+    if (L.M < 1 || L.M > 64) {
+        err = "skinny: M must be 1..64";
+        return GEMM_ERR_INVALID_ARG;
+    }
+    if (L.M <= 16) return launch_mn<16>(L, err);
+    if (L.M <= 32) return launch_mn<32>(L, err);
+    return launch_mn<64>(L, err);
+}
+
+int skinny_status_read_clear(cudaStream_t stream, int *code, std::string &err) {
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) {
+        err = std::string("cudaStreamSynchronize: ") + cudaGetErrorString(e);
+        return GEMM_ERR_CUDA;
+    }
+    int v = 0;
+    e = cudaMemcpyFromSymbol(&v, g_skinny_status, sizeof(int));
+    if (e == cudaSuccess && v != 0) {
+        const int zero = 0;
+        e = cudaMemcpyToSymbol(g_skinny_status, &zero, sizeof(int));
+    }
+    if (e != cudaSuccess) {
+        err = std::string("status word access: ") + cudaGetErrorString(e);
+        return GEMM_ERR_CUDA;
+    }
+    *code = v;
+    return GEMM_OK;
+}
+
+}  // namespace gb300

@@ -19,7 +19,7 @@ The first five named workloads follow the pages' own test and benchmark shapes:
   the same problem with M and K off the tile grid, to exercise the tails.
 
 A sixth, 1 × 16384 × 8192, is a decode-sized matrix-vector product for the
-M <= 4 path ("第 6 章 · Shared Memory & Tile", section "6.5.5 GEMV (M=1)").
+M = 1 path ("第 6 章 · Shared Memory & Tile", section "6.5.5 GEMV (M=1)").
 """
 from __future__ import annotations
 
@@ -57,10 +57,13 @@ WORKLOADS = {
         Workload("sgemm_4096", "sgemm", 4096, 4096, 4096, "uniform", 1, 2, 3, 1.0, 0.5),
         Workload("f16_nt_5376x5376x2048", "f16_nt", 5376, 5376, 2048, "uniform", 1, 2),
         Workload("f16_nt_5000x5376x2040", "f16_nt", 5000, 5376, 2040, "normal", 4, 5),
-        # A decode-sized matrix-vector product for the M <= 4 path: one row of A
+        # A decode-sized matrix-vector product for the M = 1 path: one row of A
         # against a 256 MB B (not a page workload; it measures that path's HBM
         # roofline).
         Workload("f16_gemv_1x16384x8192", "f16_nt", 1, 16384, 8192, "uniform", 6, 7),
+        # The same B against 16 rows of A (a small decode batch): the skinny
+        # tensor-core path, also bound by reading B once.
+        Workload("f16_skinny_16x16384x8192", "f16_nt", 16, 16384, 8192, "uniform", 8, 7),
     ]
 }
 

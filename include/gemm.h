@@ -152,7 +152,10 @@ enum {
                                 /* each CTA 128 rows of A and half of B), 6 stages */
     GEMM_F16_GEMV = 4,          /* M <= 4: B streamed once from HBM on the CUDA    */
                                 /* cores, a warp per row block, A read through L1  */
-    GEMM_F16_NUM_VARIANTS = 5
+    GEMM_F16_SKINNY = 5,        /* M <= 64: C^T = B A^T on the tensor cores, 128   */
+                                /* rows of B by all of A per tile, K split so the  */
+                                /* tiles fill the SMs, shares added in split order */
+    GEMM_F16_NUM_VARIANTS = 6
 };
 
 /*

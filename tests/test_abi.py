@@ -156,13 +156,16 @@ def test_f16_selector(lib):
     assert g.gemm_f16_select(4096, 2048, 512, 148)[:2] == (g.GEMM_F16_256x256_PAIR, 148)
     # fewer pair tiles than SM pairs: narrow tiles
     assert g.gemm_f16_select(2048, 2048, 512, 152)[:2] == (g.GEMM_F16_128x128, 152)
-    # up to four rows of A: the HBM-bound matrix-vector kernel, planned per SM
+    # one row of A: the HBM-bound matrix-vector kernel, planned per SM
     assert g.gemm_f16_select(1, 5376, 2048, 152)[:2] == (g.GEMM_F16_GEMV, 152)
-    assert g.gemm_f16_select(2, 16384, 8192, 152)[:2] == (g.GEMM_F16_GEMV, 152)
-    assert g.gemm_f16_select(4, 16384, 8192, 152)[0] == g.GEMM_F16_GEMV
-    assert g.gemm_f16_select(5, 16384, 8192, 152)[0] == g.GEMM_F16_128x128
-    # A is read through L1, so any K goes
-    assert g.gemm_f16_select(4, 4096, 65536, 152)[0] == g.GEMM_F16_GEMV
+    assert g.gemm_f16_select(1, 4096, 65536, 152)[0] == g.GEMM_F16_GEMV
+    # two to 64 rows: the skinny tensor-core kernel, one CTA per SM as the
+    # target of its K split
+    assert g.gemm_f16_select(2, 16384, 8192, 152)[:2] == (g.GEMM_F16_SKINNY, 152)
+    assert g.gemm_f16_select(4, 16384, 8192, 148)[:2] == (g.GEMM_F16_SKINNY, 148)
+    assert g.gemm_f16_select(5, 4096, 65536, 152)[0] == g.GEMM_F16_SKINNY
+    assert g.gemm_f16_select(64, 8192, 8192, 152)[0] == g.GEMM_F16_SKINNY
+    assert g.gemm_f16_select(65, 8192, 8192, 152)[0] == g.GEMM_F16_128x128
     # too few wide tiles to fill the SMs: narrow tiles, grid = tile count
     assert g.gemm_f16_select(1024, 1024, 1024, 152)[:2] == (g.GEMM_F16_128x128, 64)
     assert g.gemm_f16_select(100, 100, 64, 152)[:2] == (g.GEMM_F16_128x128, 1)
@@ -173,7 +176,7 @@ def test_f16_selector(lib):
     assert g.gemm_f16_select(128, 4096, 8192, 152)[:2] == (g.GEMM_F16_256x256_PAIR, 152)
     # ... but not when a split would be shallower than four ways
     assert g.gemm_f16_select(1024, 1024, 4096, 152)[:2] == (g.GEMM_F16_128x128, 64)
-    assert g.gemm_f16_select(64, 8192, 8192, 152)[:2] == (g.GEMM_F16_128x128, 64)
+    assert g.gemm_f16_select(96, 8192, 8192, 152)[:2] == (g.GEMM_F16_128x128, 64)
     with pytest.raises(g.GemmError):
         g.gemm_f16_select(1, 1, 1, 0)
 
@@ -187,6 +190,7 @@ def test_f16_selector_raster(lib):
     assert g.gemm_f16_select(8192, 8192, 8192, 152)[2] == 8
     assert g.gemm_f16_select(16384, 16384, 2048, 152)[2] == 8
     assert g.gemm_f16_select(1, 16384, 8192, 152)[2] == plain  # GEMV has no tiles
+    assert g.gemm_f16_select(8, 16384, 8192, 152)[2] == plain  # nor has the skinny kernel a band order
     with pytest.raises(g.GemmError):
         g.gemm_f16_nt_ex(16, 16, 16, 0x1000, 0x1000, 0x1000, raster=-1)
 

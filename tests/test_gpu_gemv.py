@@ -1,5 +1,5 @@
-"""GPU parity of the matrix-vector path of gemm_f16_nt (M <= 4 rows of A),
-chosen by the selector and forced through gemm_f16_nt_ex, against the float64
+"""GPU parity of the matrix-vector path of gemm_f16_nt (M <= 4 rows of A;
+chosen by the selector for M = 1, forced through gemm_f16_nt_ex, against the float64
 oracle: ragged N and K, several rows per warp, and the decode-sized shape the
 benchmark times (sampled)."""
 import numpy as np
@@ -41,14 +41,14 @@ def _run(A, B, variant=g.GEMM_F16_AUTO):
 @pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 8])
 @pytest.mark.parametrize("N,K", [(1, 8), (77, 72), (5376, 2048), (3000, 1032), (1000, 12008), (9, 4096)])
 def test_small_m_full_compare(M, N, K):
-    # M <= 4 takes the matrix-vector kernel, M >= 5 the tensor cores; both agree
-    # with the oracle, and the matrix-vector kernel can also be forced.  (9
-    # rows of B: more warps than rows, odd row blocks.)
+    # M = 1 takes the matrix-vector kernel, larger M the tensor cores; both
+    # agree with the oracle, and the matrix-vector kernel can be forced up to
+    # M = 4.  (9 rows of B: more warps than rows, odd row blocks.)
     A = wl.draw_f16((M, K), seed=M + 100, dist="normal")
     B = wl.draw_f16((N, K), seed=N + 200, dist="normal")
     Cref, S = oracle.gemm_f16_nt(A, B)
     sm = torch.cuda.get_device_properties(0).multi_processor_count
-    assert (g.gemm_f16_select(M, N, K, sm)[0] == g.GEMM_F16_GEMV) == (M <= 4)
+    assert (g.gemm_f16_select(M, N, K, sm)[0] == g.GEMM_F16_GEMV) == (M == 1)
     check_f16(_run(A, B), Cref, S, what=f"M={M} {N}x{K}")
     if M <= 4:
         check_f16(_run(A, B, g.GEMM_F16_GEMV), Cref, S, what=f"gemv forced {M}x{N}x{K}")

@@ -1,0 +1,142 @@
+"""GPU parity of the skinny variant of gemm_f16_nt (a few rows of A, computed
+as B·Aᵀ on the tensor cores with the K range split over a cluster of CTAs)
+against the float64 oracle: every MMA width (16, 32, 64 rows of A), ragged
+M, N and K, 1, 2, 4 and 8 shares, the fused epilogue on both paths, an
+unaligned C, graph capture, and run-to-run equality of the split sums."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import dense_gemm_fp16_gb300 as g
+from dense_gemm_fp16_gb300 import workloads as wl
+from parity import check_f16, check_f16_epilogue
+
+pytestmark = pytest.mark.gpu
+
+SENTINEL = 0x7E5A  # a NaN payload nothing in the product writes
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from dense_gemm_fp16_gb300 import build
+
+    build.build()
+    g.load_library()
+    torch.cuda.init()
+
+
+def _guarded(M, N, pad=64):
+    buf = torch.full((M * N + 2 * pad,), SENTINEL, dtype=torch.int16, device="cuda").view(torch.float16)
+    return buf, buf[pad:pad + M * N].view(M, N)
+
+
+def _unguard(buf, M, N, pad=64):
+    host = buf.cpu()
+    guard = torch.cat([host[:pad], host[pad + M * N:]]).view(torch.int16).numpy()
+    assert np.all(guard == SENTINEL), "kernel wrote outside C"
+    return host[pad:pad + M * N].view(M, N).numpy()
+
+
+def _run(A, B, variant=g.GEMM_F16_SKINNY, pad=64):
+    M, K = A.shape
+    N = B.shape[0]
+    dA, dB = A.cuda(), B.cuda()
+    buf, C = _guarded(M, N, pad)
+    stream = torch.cuda.current_stream().cuda_stream
+    g.gemm_f16_nt_ex(M, N, K, dA.data_ptr(), dB.data_ptr(), C.data_ptr(), stream, variant, 0)
+    g.gemm_check_device_status(stream)
+    return _unguard(buf, M, N, pad)
+
+
+# (N, K) and the shares of K each tile gets on 152 SMs: one partial tile and
+# two k-blocks (1), several tiles with a partial k-block (2), ragged tiles
+# and k-blocks (4), few tiles over a long K (8), N % 4 != 0 (8: the split
+# sum's scalar stores), a full wave of tiles (2).
+SHAPES = [(77, 72), (3000, 1032), (4000, 2056), (1000, 12008), (1001, 4104), (8192, 1024)]
+
+
+@pytest.mark.parametrize("M", [1, 5, 16, 17, 32, 33, 64])
+@pytest.mark.parametrize("N,K", SHAPES)
+def test_skinny_full_compare(M, N, K):
+    A = wl.draw_f16((M, K), seed=M + 300, dist="normal")
+    B = wl.draw_f16((N, K), seed=N + K, dist="normal")
+    Cref, S = oracle.gemm_f16_nt(A, B)
+    check_f16(_run(A, B), Cref, S, what=f"skinny {M}x{N}x{K}")
+
+
+def test_skinny_unaligned_output():
+    # C two bytes off an 8-byte boundary: the split sum stores half by half.
+    M, N, K = 20, 1000, 4096
+    A = wl.draw_f16((M, K), seed=61, dist="normal")
+    B = wl.draw_f16((N, K), seed=62, dist="normal")
+    Cref, S = oracle.gemm_f16_nt(A, B)
+    check_f16(_run(A, B, pad=65), Cref, S, what="skinny unaligned C")
+
+
+def test_skinny_is_selected_for_few_rows():
+    sm = torch.cuda.get_device_properties(0).multi_processor_count
+    for M in (2, 5, 64):
+        assert g.gemm_f16_select(M, 8192, 8192, sm)[0] == g.GEMM_F16_SKINNY
+    M, N, K = 7, 2000, 3000
+    A = wl.draw_f16((M, K), seed=71, dist="normal")
+    B = wl.draw_f16((N, K), seed=72, dist="normal")
+    Cref, S = oracle.gemm_f16_nt(A, B)
+    check_f16(_run(A, B, variant=g.GEMM_F16_AUTO), Cref, S, what="skinny by the selector")
+
+
+def test_skinny_split_sum_is_deterministic():
+    # The shares are added in split order: equal runs give equal bits.
+    M, N, K = 24, 1000, 12008
+    A = wl.draw_f16((M, K), seed=41, dist="normal")
+    B = wl.draw_f16((N, K), seed=42, dist="normal")
+    first = _run(A, B)
+    for _ in range(3):
+        assert np.array_equal(_run(A, B).view(np.uint16), first.view(np.uint16))
+
+
+@pytest.mark.parametrize("act", ["none", "relu", "gelu_tanh"])
+@pytest.mark.parametrize("M,N,K", [(9, 300, 136), (40, 1000, 12008)])
+def test_skinny_fused_epilogue(M, N, K, act):
+    # (the first shape runs unsplit, the second with 8 shares summed over the cluster)
+    A = wl.draw_f16((M, K), seed=M, dist="normal")
+    B = wl.draw_f16((N, K), seed=N, dist="normal")
+    bias = wl.draw_f16((N,), seed=7, dist="normal")
+    R = wl.draw_f16((M, N), seed=8, dist="normal")
+    dA, dB, dbias, dR = A.cuda(), B.cuda(), bias.cuda(), R.cuda()
+    buf, C = _guarded(M, N)
+    stream = torch.cuda.current_stream().cuda_stream
+    g.gemm_f16_nt_fused(M, N, K, dA.data_ptr(), dB.data_ptr(), C.data_ptr(), 0.5, -1.25,
+                        dbias.data_ptr(), dR.data_ptr(), g.ACTIVATIONS[act], stream, g.GEMM_F16_SKINNY)
+    g.gemm_check_device_status(stream)
+    Y, S = oracle.gemm_f16_nt_epilogue(A, B, alpha=0.5, bias=bias, beta=-1.25, R=R, act=act)
+    check_f16_epilogue(_unguard(buf, M, N), Y, S, what=f"skinny fused {M}x{N}x{K} {act}")
+
+
+def test_skinny_under_graph_capture():
+    # The split (8 shares per tile here) needs no workspace, so a captured
+    # call runs as a plain one; the replayed graph gives the oracle's result.
+    M, N, K = 12, 640, 4096
+    A = wl.draw_f16((M, K), seed=51, dist="normal")
+    B = wl.draw_f16((N, K), seed=52, dist="normal")
+    dA, dB = A.cuda(), B.cuda()
+    C = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    with torch.cuda.graph(graph, stream=side):
+        g.gemm_f16_nt_ex(M, N, K, dA.data_ptr(), dB.data_ptr(), C.data_ptr(), side.cuda_stream,
+                         g.GEMM_F16_SKINNY)
+    C.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    g.gemm_check_device_status(0)
+    Cref, S = oracle.gemm_f16_nt(A, B)
+    check_f16(C.cpu().numpy(), Cref, S, what="skinny captured")
+
+
+def test_skinny_variant_rejects_too_many_rows():
+    A = torch.zeros((65, 64), dtype=torch.float16, device="cuda")
+    C = torch.zeros((65, 65), dtype=torch.float16, device="cuda")
+    with pytest.raises(g.GemmError) as e:
+        g.gemm_f16_nt_ex(65, 65, 64, A.data_ptr(), A.data_ptr(), C.data_ptr(), 0, g.GEMM_F16_SKINNY)
+    assert e.value.status == g.GEMM_ERR_UNSUPPORTED
