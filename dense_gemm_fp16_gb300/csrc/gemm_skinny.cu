@@ -1,4 +1,4 @@
-// gemm_skinny.cu -- C = A * B^T for a few rows of A (5 <= M <= 64) on the
+// gemm_skinny.cu -- C = A * B^T for a few rows of A (M <= 64) on the
 // tensor cores, as the swapped product D = B * A^T (D = C^T).
 //
 // Same operation and numerics as gemm_f16_nt (half inputs, fp32
@@ -19,8 +19,10 @@
 // With a split, the CTAs that share a tile's K range form one thread-block
 // cluster (2, 4 or 8 CTAs): each puts its fp32 share in its own shared
 // memory, and after a cluster barrier CTA r adds slice r of the tile over all
-// the shares, read through distributed shared memory in split order, so
-// results do not depend on timing and no share goes through HBM.
+// the shares, read through distributed shared memory in split order
+// ("异步拷贝与 Hopper/Blackwell 新特性", section "线程块集群与分布式共享内存
+// sm_90+": CTAs of a cluster synchronise and read one another's shared
+// memory), so results do not depend on timing and no share goes through HBM.
 // Every wait is bounded as in the other kernels.
 #include <cuda.h>
 #include <cuda_fp16.h>

@@ -111,6 +111,10 @@ int gemm_check_device_status(gemm_stream_t stream);
  * instance (GEMM_F16_* below); grid is the persistent CTA count
  * (0 = choose from the device's SM count; for the pair variant it is rounded
  * down to whole pairs and capped by the pairs the device can hold at once).
+ * For the skinny variant, grid is instead the CTA count its K split aims
+ * for: each 128-column tile gets the largest power of two of shares (at most
+ * 8, each at least 8 k-blocks of 64) with tiles x shares <= grid, halved
+ * while the device cannot hold all the tiles' clusters at once.
  */
 typedef struct {
     int variant;
@@ -150,11 +154,15 @@ enum {
     GEMM_F16_128x128 = 2,       /* one CTA per 128 x 128 output tile, 6 stages    */
     GEMM_F16_256x256_PAIR = 3,  /* a 2-CTA cluster per 256 x 256 tile (pair MMA,  */
                                 /* each CTA 128 rows of A and half of B), 6 stages */
-    GEMM_F16_GEMV = 4,          /* M <= 4: B streamed once from HBM on the CUDA    */
-                                /* cores, a warp per row block, A read through L1  */
-    GEMM_F16_SKINNY = 5,        /* M <= 64: C^T = B A^T on the tensor cores, 128   */
-                                /* rows of B by all of A per tile, K split so the  */
-                                /* tiles fill the SMs, shares added in split order */
+    GEMM_F16_GEMV = 4,          /* M <= 4 (chosen for M = 1): B streamed once from */
+                                /* HBM on the CUDA cores, a warp per row block, A  */
+                                /* read through L1                                  */
+    GEMM_F16_SKINNY = 5,        /* M <= 64 (chosen for 2..64): C^T = B A^T on the  */
+                                /* tensor cores, 128 rows of B by all of A per     */
+                                /* tile, K split over a cluster of 2-8 CTAs so the */
+                                /* tiles fill the SMs, the shares added in split   */
+                                /* order through distributed shared memory (no     */
+                                /* workspace; same numerics as the tile kernels)   */
     GEMM_F16_NUM_VARIANTS = 6
 };
 
