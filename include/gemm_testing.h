@@ -26,6 +26,18 @@ int gemm_debug_f16_nt_skip_load(int M, int N, int K, const void *A, const void *
                                 gemm_stream_t stream, int skip_kblock,
                                 unsigned long long timeout_ns);
 
+/*
+ * The K split the skinny fp16 variant (GEMM_F16_SKINNY) plans for a product
+ * with N columns of C and depth K, aiming at `ctas` CTAs: pure host logic,
+ * no device call.  Returns the shares of K per 128-column tile (1, 2, 4 or 8:
+ * the largest power of two with tiles x shares <= ctas and at least 8
+ * k-blocks of 64 per share; 1 when none fits) and stores the k-blocks per
+ * share in *kb_per_split (the last share may be shorter).  The launch halves
+ * the shares further while the device cannot hold all the clusters at once.
+ * Returns -1 for N < 1, K < 0, ctas < 1 or a NULL kb_per_split.
+ */
+int gemm_debug_skinny_split_plan(int N, int K, int ctas, int *kb_per_split);
+
 #ifdef __cplusplus
 }
 #endif

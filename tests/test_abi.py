@@ -34,7 +34,8 @@ def test_headers_declare_the_boundary():
     names = _declared_functions()
     for n in ["gemm_f16_nt", "sgemm", "gemm_last_error", "gemm_check_device_status",
               "gemm_f16_select", "gemm_sgemm_select", "gemm_f16_nt_ex", "sgemm_ex",
-              "gemm_debug_f16_nt_skip_load", "gemm_f16_nt_fused", "gemm_f16_nt_stream_k_noalloc",
+              "gemm_debug_f16_nt_skip_load", "gemm_debug_skinny_split_plan",
+              "gemm_f16_nt_fused", "gemm_f16_nt_stream_k_noalloc",
               "gemm_mxfp8_nt", "gemm_mxfp8_scale_bytes", "gemm_mxfp8_pack_scales",
               "gemm_nvfp4_nt", "gemm_nvfp4_nt_ex", "gemm_nvfp4_scale_bytes", "gemm_nvfp4_pack_scales"]:
         assert n in names
@@ -179,6 +180,35 @@ def test_f16_selector(lib):
     assert g.gemm_f16_select(96, 8192, 8192, 152)[:2] == (g.GEMM_F16_128x128, 64)
     with pytest.raises(g.GemmError):
         g.gemm_f16_select(1, 1, 1, 0)
+
+
+def test_skinny_split_plan(lib):
+    # Worked cases on 152 SMs: shares per 128-column tile, k-blocks per share.
+    assert g.gemm_debug_skinny_split_plan(8192, 8192, 152) == (2, 64)     # 64 tiles
+    assert g.gemm_debug_skinny_split_plan(16384, 8192, 152) == (1, 128)   # 128 tiles: no room
+    assert g.gemm_debug_skinny_split_plan(4096, 4096, 152) == (4, 16)     # 32 tiles
+    assert g.gemm_debug_skinny_split_plan(1000, 12008, 152) == (8, 24)    # 8 tiles, 188 k-blocks
+    assert g.gemm_debug_skinny_split_plan(4000, 2056, 152) == (4, 9)      # 33 k-blocks: ragged
+    assert g.gemm_debug_skinny_split_plan(77, 72, 152) == (1, 2)          # too shallow to split
+    assert g.gemm_debug_skinny_split_plan(77, 0, 152) == (1, 1)           # K = 0
+    with pytest.raises(ValueError):
+        g.gemm_debug_skinny_split_plan(0, 64, 152)
+
+
+def test_skinny_split_plan_properties(lib):
+    # Against the rule itself, over a grid of shapes: a power of two up to 8;
+    # tiles x shares within the CTA target; at least 8 k-blocks a share; the
+    # shares cover K with none empty; and the next power of two breaks a rule.
+    for N in (1, 127, 128, 129, 1000, 4096, 8192, 16384, 28672):
+        for K in (8, 64, 512, 520, 4096, 12008, 65536):
+            for ctas in (1, 19, 152, 304):
+                s, per = g.gemm_debug_skinny_split_plan(N, K, ctas)
+                tiles, nkb = -(-N // 128), -(-K // 64)
+                assert s in (1, 2, 4, 8)
+                assert per * s >= nkb and per >= 1
+                if s > 1:
+                    assert tiles * s <= ctas and nkb // s >= 8 and (s - 1) * per < nkb
+                assert 2 * s > 8 or tiles * 2 * s > ctas or nkb // (2 * s) < 8
 
 
 def test_f16_selector_raster(lib):

@@ -65,6 +65,21 @@ def test_skinny_full_compare(M, N, K):
     check_f16(_run(A, B), Cref, S, what=f"skinny {M}x{N}x{K}")
 
 
+def test_skinny_bench_shape_sampled():
+    # The 16-row product the benchmark times, as the selector runs it: B is
+    # 256 MB, larger than L2; sampled outputs against the oracle.
+    w = wl.WORKLOADS["f16_skinny_16x16384x8192"]
+    A, B, _ = wl.make_inputs(w)
+    sm = torch.cuda.get_device_properties(0).multi_processor_count
+    assert g.gemm_f16_select(w.M, w.N, w.K, sm)[0] == g.GEMM_F16_SKINNY
+    dA, dB = A.cuda(), B.cuda()
+    C = g.f16_nt(dA, dB)
+    g.gemm_check_device_status(0)
+    rows, cols = wl.sample_positions(w.M, w.N, 4096, seed=9)
+    Cref, S = oracle.gemm_f16_nt_sampled(A, B, rows, cols)
+    check_f16(C.cpu().numpy()[rows, cols], Cref, S, what="skinny bench shape")
+
+
 def test_skinny_unaligned_output():
     # C two bytes off an 8-byte boundary: the split sum stores half by half.
     M, N, K = 20, 1000, 4096
