@@ -1445,7 +1445,8 @@ int f16_launch(const F16Launch &L, std::string &err) {
         case GEMM_F16_SKINNY: {
             // the grid is the CTA count the K split aims for
             SkinnyLaunch S{L.M, L.N, L.K, L.A, L.B, L.C, L.stream,
-                           L.grid > 0 ? L.grid : L.sm_count * skinny_ctas_per_sm(), L.timeout_ns, L.epi};
+                           L.grid > 0 ? L.grid : L.sm_count * skinny_ctas_per_sm(), L.timeout_ns, L.epi,
+                           L.debug_skip_kblock};
             return skinny_launch(S, err);
         }
         default: err = "unknown fp16 variant"; return GEMM_ERR_INVALID_ARG;

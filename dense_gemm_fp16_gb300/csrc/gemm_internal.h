@@ -114,6 +114,7 @@ struct SkinnyLaunch {
     int ctas;              // CTA count the K split aims for (tiles x shares <= ctas)
     uint64_t timeout_ns;
     EpiSpec epi;           // fused epilogue (epi.on == 0: the plain product)
+    int debug_skip_kblock; // test hook: each CTA leaves out this k-block of its share (-1: none)
 };
 
 constexpr int kSkMaxSplits = 8;

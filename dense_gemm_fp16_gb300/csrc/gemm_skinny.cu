@@ -80,6 +80,7 @@ struct SkArgs {
     int splits;        // shares of K per tile: 1, or the cluster size (2, 4, 8)
     uint64_t timeout_ns;
     Epi epi;           // fused epilogue, applied where the fp32 sum is rounded
+    int debug_skip_kblock;  // test hook: every CTA leaves out this k-block of its share (-1: none)
 };
 
 // One output through the epilogue and rounded to half.
@@ -177,12 +178,14 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                     ok = false;
                     break;
                 }
-                const uint32_t sb = sbase + stage * T::kStageBytes;
-                mbar_arrive_expect_tx(full_bar(stage), T::kStageBytes);
-                armed |= 1u << stage;
-                arm_parity ^= 1u << stage;
-                tma_load_2d(sb, &tmB, full_bar(stage), kb * kSkBK, tile * kSkBM);
-                tma_load_2d(sb + T::kBBytes, &tmA, full_bar(stage), kb * kSkBK, 0);
+                if (kb - kb0 != args.debug_skip_kblock) {
+                    const uint32_t sb = sbase + stage * T::kStageBytes;
+                    mbar_arrive_expect_tx(full_bar(stage), T::kStageBytes);
+                    armed |= 1u << stage;
+                    arm_parity ^= 1u << stage;
+                    tma_load_2d(sb, &tmB, full_bar(stage), kb * kSkBK, tile * kSkBM);
+                    tma_load_2d(sb + T::kBBytes, &tmA, full_bar(stage), kb * kSkBK, 0);
+                }
                 if (++stage == STAGES) {
                     stage = 0;
                     phase ^= 1u;
@@ -409,7 +412,7 @@ int launch_mn(const SkinnyLaunch &L, std::string &err) {
         kb_per_split = (num_kb + splits - 1) / splits;
     }
     const SkArgs args{static_cast<__half *>(L.C), L.M, L.N, L.K, num_kb, kb_per_split, splits, L.timeout_ns,
-                      make_epi(L.epi, L.N)};
+                      make_epi(L.epi, L.N), L.debug_skip_kblock};
     CUtensorMap tmB, tmA;
     if (!encode_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, L.B, L.N, L.K, kSkBM, kSkBK, err) ||
         !encode_map(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, L.A, L.M, L.K, MN, kSkBK, err))

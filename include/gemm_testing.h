@@ -20,7 +20,10 @@ extern "C" {
  * finish, frees its Tensor Memory and exits.  The launch itself returns
  * GEMM_OK; the fault is then reported by gemm_check_device_status() as
  * GEMM_ERR_DEVICE_TIMEOUT and the CUDA context stays usable.  C is left
- * partially written.  Same argument rules as gemm_f16_nt.
+ * partially written.  Same argument rules as gemm_f16_nt.  When the
+ * selector picks the skinny variant (2 <= M <= 64), every CTA leaves out
+ * k-block `skip_kblock` of its own share of K instead, so the CTAs of a split
+ * cluster all give up and still meet at the cluster barriers.
  */
 int gemm_debug_f16_nt_skip_load(int M, int N, int K, const void *A, const void *B, void *C,
                                 gemm_stream_t stream, int skip_kblock,
