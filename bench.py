@@ -397,6 +397,17 @@ def run_ours(args):
                  f"after a soak, under the power cap)" if sustained else
                  f"{peak_kind} bf16 dense burst (no sustained figure available)")
     achieved = w.flop / (avg_launch_ms * 1e-3) / 1e12
+    # HBM side of the same launch: the compulsory bytes (A, B read, C written)
+    # and, when the committed ncu capture matches the source, the DRAM bytes
+    # it counted, both per average launch time
+    traffic = profiled_traffic()
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    alg_bytes = 2.0 * (M * K + N * K + M * N)
+    hbm = {"algorithmic_bytes": alg_bytes,
+           "algorithmic_gbs": alg_bytes / (avg_launch_ms * 1e-3) / 1e9,
+           "dram_gbs": traffic / (avg_launch_ms * 1e-3) / 1e9 if traffic else None,
+           "peak_gbs": hbm_peak, "peak_source": f"{peak_kind} HBM copy bandwidth"}
+    hbm["frac"] = (hbm["dram_gbs"] or hbm["algorithmic_gbs"]) / hbm_peak
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -411,10 +422,10 @@ def run_ours(args):
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "percent_of_peak": 100.0 * value / world / peak,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": profiled_traffic(),
+                     "frac": achieved / peak, "traffic": traffic,
                      "peak_source": peak_note, "frac_of_burst_peak": achieved / burst,
                      "kernel": kernel_name,
-                     "avg_launch_us": 1e3 * avg_launch_ms},
+                     "avg_launch_us": 1e3 * avg_launch_ms, "hbm": hbm},
         "gpu_launches": args.steps,
         "clocks": clocks.summary(),
         "wall_s_timed_region": wall,
