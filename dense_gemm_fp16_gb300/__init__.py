@@ -53,7 +53,7 @@ from ._binding import (  # noqa: F401
     f16_nt_fused,
     gemm_check_device_status,
     gemm_debug_f16_nt_skip_load,
-    gemm_debug_skinny_split_plan,
+    gemm_debug_skinny_plan,
     gemm_f16_nt,
     gemm_f16_nt_ex,
     gemm_f16_nt_fused,

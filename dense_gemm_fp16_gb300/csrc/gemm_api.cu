@@ -301,10 +301,15 @@ int gemm_debug_f16_nt_skip_load(int M, int N, int K, const void *A, const void *
     return f16_nt_impl(M, N, K, A, B, C, stream, nullptr, timeout_ns, skip_kblock);
 }
 
-// Test hook declared in gemm_testing.h: the skinny variant's K-split plan.
-int gemm_debug_skinny_split_plan(int N, int K, int ctas, int *kb_per_split) {
-    if (N < 1 || K < 0 || ctas < 1 || !kb_per_split) return -1;
-    return gb300::skinny_split_plan(N, K, ctas, kb_per_split);
+// Test hook declared in gemm_testing.h: the skinny variant's plan.
+int gemm_debug_skinny_plan(int N, int K, int ctas, int *rows, int *groups, int *kb_per_split) {
+    if (N < 1 || K < 0 || ctas < 1 || !rows || !groups || !kb_per_split) return -1;
+    gb300::SkinnyPlan p;
+    gb300::skinny_plan(N, K, ctas, nullptr, &p);
+    *rows = p.rows;
+    *groups = p.groups;
+    *kb_per_split = p.kb_per_split;
+    return p.splits;
 }
 
 // ---------------------------------------------------------------------------

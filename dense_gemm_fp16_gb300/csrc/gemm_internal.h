@@ -117,17 +117,25 @@ struct SkinnyLaunch {
     int debug_skip_kblock; // test hook: each CTA leaves out this k-block of its share (-1: none)
 };
 
-constexpr int kSkMaxSplits = 8;
-
 // CTAs of the skinny kernel resident per SM (its default CTA target is this
 // times the SM count).
 int skinny_ctas_per_sm();
 
-// The shares of K a skinny launch plans for (1, 2, 4 or 8: the cluster size;
-// returned) and the 64-deep k-blocks of each (*kb_per_split; the last share
-// may be shorter).  The launch halves the shares while the device cannot
-// hold all the clusters at once.
-int skinny_split_plan(int N, int K, int ctas, int *kb_per_split);
+// How a skinny launch spreads the product: `groups` groups of `rows`
+// columns of C (rows of B), each group's K range in `splits` shares of
+// `kb_per_split` 64-deep k-blocks (the last may be shorter), one CTA per
+// share, a group's shares one cluster.
+struct SkinnyPlan {
+    int splits;        // 1, 2, 4 or 8
+    int rows;          // a multiple of 8, at most 128
+    int groups;        // ceil(N / rows)
+    int kb_per_split;
+};
+
+// The plan for N columns of C and depth K on `ctas` CTA slots; cap[l] is the
+// number of clusters of 2^l CTAs the device holds at once (cap[0] = ctas), or
+// cap == nullptr to take ctas / 2^l.  Host logic only.
+void skinny_plan(int N, int K, int ctas, const int *cap, SkinnyPlan *plan);
 
 int skinny_launch(const SkinnyLaunch &L, std::string &err);
 

@@ -44,7 +44,7 @@ namespace {
 __device__ int g_skinny_status = 0;
 __device__ __forceinline__ void skinny_timeout(int code) { atomicCAS(&g_skinny_status, 0, code); }
 
-constexpr int kSkBM = 128;       // rows of B per tile: the MMA's M
+constexpr int kSkBM = 128;       // the MMA's M: at most this many rows of B per group
 constexpr int kSkBK = 64;        // halves per k-block: one 128-byte swizzle row
 constexpr int kSkThreads = 192;  // warp 0 producer, warp 1 MMA, warps 2-5 epilogue
 constexpr int kSkCtasPerSm = 1;  // CTAs resident per SM (their stages keep HBM busy)
@@ -77,7 +77,8 @@ struct SkArgs {
     int M, N, K;
     int num_kb;        // 64-deep k-blocks of K
     int kb_per_split;  // k-blocks per share (the last may be shorter)
-    int splits;        // shares of K per tile: 1, or the cluster size (2, 4, 8)
+    int splits;        // shares of K per group: 1, or the cluster size (2, 4, 8)
+    int rows;          // rows of B (columns of C) per group: a multiple of 8, <= 128
     uint64_t timeout_ns;
     Epi epi;           // fused epilogue, applied where the fp32 sum is rounded
     int debug_skip_kblock;  // test hook: every CTA leaves out this k-block of its share (-1: none)
@@ -136,7 +137,12 @@ __global__ void __launch_bounds__(kSkThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int tile = blockIdx.x;   // 128 columns of C
+    const int tile = blockIdx.x;   // group of `rows` columns of C
+    const int row0 = tile * args.rows;
+    const int nend = row0 + args.rows < args.N ? row0 + args.rows : args.N;
+    // the B box is `rows` rows tall; the stage's rows past it keep stale data,
+    // which only reaches TMEM lanes the epilogue never reads
+    const uint32_t stage_tx = static_cast<uint32_t>(args.rows + MN) * (kSkBK * 2);
     const int split = blockIdx.y;  // share of K
     const int kb0 = split * args.kb_per_split;
     const int kb1 = kb0 + args.kb_per_split < args.num_kb ? kb0 + args.kb_per_split : args.num_kb;
@@ -180,10 +186,10 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                 }
                 if (kb - kb0 != args.debug_skip_kblock) {
                     const uint32_t sb = sbase + stage * T::kStageBytes;
-                    mbar_arrive_expect_tx(full_bar(stage), T::kStageBytes);
+                    mbar_arrive_expect_tx(full_bar(stage), stage_tx);
                     armed |= 1u << stage;
                     arm_parity ^= 1u << stage;
-                    tma_load_2d(sb, &tmB, full_bar(stage), kb * kSkBK, tile * kSkBM);
+                    tma_load_2d(sb, &tmB, full_bar(stage), kb * kSkBK, row0);
                     tma_load_2d(sb + T::kBBytes, &tmA, full_bar(stage), kb * kSkBK, 0);
                 }
                 if (++stage == STAGES) {
@@ -254,8 +260,8 @@ __global__ void __launch_bounds__(kSkThreads, 1)
             if (!*abort_flag) skinny_timeout(3);
             *abort_flag = 1;
         }
-        const int n = tile * kSkBM + quarter * 32 + lane;
-        if (args.splits == 1 && ok && n < args.N) {
+        const int n = row0 + quarter * 32 + lane;
+        if (args.splits == 1 && ok && n < nend) {
 #pragma unroll
             for (int m = 0; m < MN; ++m) {
                 if (m >= args.M) break;
@@ -318,10 +324,10 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                 sum.w += x.w;
             }
             const int m = gi / (kSkBM / 4);
-            const int n = tile * kSkBM + (gi % (kSkBM / 4)) * 4;
+            const int n = row0 + (gi % (kSkBM / 4)) * 4;
             __half *out = args.C + static_cast<size_t>(m) * args.N + n;
             const float s4[4] = {sum.x, sum.y, sum.z, sum.w};
-            if (vec && n + 3 < args.N) {
+            if (vec && n + 3 < nend) {
                 __half2 lo = __halves2half2(skinny_out(args.epi, s4[0], m, n, args.N),
                                             skinny_out(args.epi, s4[1], m, n + 1, args.N));
                 __half2 hi = __halves2half2(skinny_out(args.epi, s4[2], m, n + 2, args.N),
@@ -333,7 +339,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
             } else {
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
-                    if (n + j < args.N) out[j] = skinny_out(args.epi, s4[j], m, n + j, args.N);
+                    if (n + j < nend) out[j] = skinny_out(args.epi, s4[j], m, n + j, args.N);
             }
         }
         cluster_sync();  // no CTA leaves while another still reads its share
@@ -399,22 +405,21 @@ int launch_mn(const SkinnyLaunch &L, std::string &err) {
         }
         if (dev >= 0 && dev < 64) configured[dev] = 1;
     }
-    const int tiles = (L.N + kSkBM - 1) / kSkBM;
-    const int num_kb = (L.K + kSkBK - 1) / kSkBK;
-    int kb_per_split = num_kb;
-    int splits = skinny_split_plan(L.N, L.K, L.ctas, &kb_per_split);
-    // fewer shares while the clusters would not all be resident at once
-    while (splits > 1) {
-        const int fit = max_clusters<MN, S>(splits, err);
-        if (fit < 0) return GEMM_ERR_CUDA;
-        if (fit >= tiles) break;
-        splits /= 2;
-        kb_per_split = (num_kb + splits - 1) / splits;
+    // clusters of 2, 4 and 8 CTAs the device holds at once
+    int cap[4] = {L.ctas, 0, 0, 0};
+    for (int l = 1; l < 4; ++l) {
+        cap[l] = max_clusters<MN, S>(1 << l, err);
+        if (cap[l] < 0) return GEMM_ERR_CUDA;
     }
-    const SkArgs args{static_cast<__half *>(L.C), L.M, L.N, L.K, num_kb, kb_per_split, splits, L.timeout_ns,
-                      make_epi(L.epi, L.N), L.debug_skip_kblock};
+    SkinnyPlan plan;
+    skinny_plan(L.N, L.K, L.ctas, cap, &plan);
+    const int num_kb = (L.K + kSkBK - 1) / kSkBK;
+    const int splits = plan.splits;
+    const int tiles = plan.groups;
+    const SkArgs args{static_cast<__half *>(L.C), L.M, L.N, L.K, num_kb, plan.kb_per_split, splits, plan.rows,
+                      L.timeout_ns, make_epi(L.epi, L.N), L.debug_skip_kblock};
     CUtensorMap tmB, tmA;
-    if (!encode_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, L.B, L.N, L.K, kSkBM, kSkBK, err) ||
+    if (!encode_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, L.B, L.N, L.K, plan.rows, kSkBK, err) ||
         !encode_map(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, L.A, L.M, L.K, MN, kSkBK, err))
         return GEMM_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
@@ -443,19 +448,34 @@ int launch_mn(const SkinnyLaunch &L, std::string &err) {
 
 int skinny_ctas_per_sm() { return kSkCtasPerSm; }
 
-int skinny_split_plan(int N, int K, int ctas, int *kb_per_split) {
-    const int tiles = (N + kSkBM - 1) / kSkBM;
+void skinny_plan(int N, int K, int ctas, const int *cap, SkinnyPlan *plan) {
     const int num_kb = (K + kSkBK - 1) / kSkBK;
-    // the largest power of two of shares that the CTA target allows, each
-    // share at least 8 k-blocks, at most 8 shares (the portable cluster size)
-    int cap = ctas / (tiles > 0 ? tiles : 1);
-    if (cap > num_kb / 8) cap = num_kb / 8;
-    if (cap > kSkMaxSplits) cap = kSkMaxSplits;
-    int splits = 1;
-    while (splits * 2 <= cap) splits *= 2;
-    const int per = (num_kb + splits - 1) / splits;
-    *kb_per_split = per > 1 ? per : 1;
-    return splits;
+    const int tiles = (N + kSkBM - 1) / kSkBM;
+    // An SM's rate goes with the k-blocks its ring keeps in flight, not with
+    // the rows each carries: shorter groups or fewer shares measured slower.
+    // So the groups stay 128 rows and each gets the largest power of two of
+    // shares (at most 8, each at least 8 k-blocks) for which all the groups'
+    // clusters are resident at once.
+    int s = 1;
+    for (int l = 3; l >= 1; --l) {
+        const int c = 1 << l;
+        int fit = ctas / c;
+        if (cap && cap[l] < fit) fit = cap[l];
+        if (num_kb / c >= 8 && tiles <= fit) {
+            s = c;
+            break;
+        }
+    }
+    int rows = kSkBM;
+    if (s == 1 && tiles > ctas && ctas > 0) {
+        // more than one wave: spread the rows evenly over the waves, so that
+        // the last wave is as full as the others
+        const long long slots = static_cast<long long>((tiles + ctas - 1) / ctas) * ctas;
+        rows = static_cast<int>((N + slots - 1) / slots);
+        rows = (rows + 7) & ~7;
+    }
+    const int kbs = (num_kb + s - 1) / s;
+    *plan = SkinnyPlan{s, rows, (N + rows - 1) / rows, kbs > 0 ? kbs : 1};
 }
 
 int skinny_launch(const SkinnyLaunch &L, std::string &err) {

@@ -111,10 +111,12 @@ int gemm_check_device_status(gemm_stream_t stream);
  * instance (GEMM_F16_* below); grid is the persistent CTA count
  * (0 = choose from the device's SM count; for the pair variant it is rounded
  * down to whole pairs and capped by the pairs the device can hold at once).
- * For the skinny variant, grid is instead the CTA count its K split aims
- * for: each 128-column tile gets the largest power of two of shares (at most
- * 8, each at least 8 k-blocks of 64) with tiles x shares <= grid, halved
- * while the device cannot hold all the tiles' clusters at once.
+ * For the skinny variant, grid is instead the number of CTA slots it plans
+ * for: C's columns go in groups of 128 and each group's K range in the
+ * largest of 2, 4 or 8 shares (a cluster, each share at least 8 k-blocks of
+ * 64) with groups x shares <= grid whose clusters the device holds at once,
+ * else 1; when the groups alone need more than one wave their height is
+ * evened out over the waves (gemm_testing.h exposes the plan).
  */
 typedef struct {
     int variant;
@@ -159,10 +161,11 @@ enum {
                                 /* read through L1                                  */
     GEMM_F16_SKINNY = 5,        /* M <= 64 (chosen for 2..64): C^T = B A^T on the  */
                                 /* tensor cores, 128 rows of B by all of A per     */
-                                /* tile, K split over a cluster of 2-8 CTAs so the */
-                                /* tiles fill the SMs, the shares added in split   */
-                                /* order through distributed shared memory (no     */
-                                /* workspace; same numerics as the tile kernels)   */
+                                /* group, K split over a cluster of 2-8 CTAs so    */
+                                /* the groups fill the SMs; the shares are added   */
+                                /* in split order through distributed shared       */
+                                /* memory (no workspace; the tile kernels'         */
+                                /* numerics)                                        */
     GEMM_F16_NUM_VARIANTS = 6
 };
 

@@ -34,7 +34,7 @@ def test_headers_declare_the_boundary():
     names = _declared_functions()
     for n in ["gemm_f16_nt", "sgemm", "gemm_last_error", "gemm_check_device_status",
               "gemm_f16_select", "gemm_sgemm_select", "gemm_f16_nt_ex", "sgemm_ex",
-              "gemm_debug_f16_nt_skip_load", "gemm_debug_skinny_split_plan",
+              "gemm_debug_f16_nt_skip_load", "gemm_debug_skinny_plan",
               "gemm_f16_nt_fused", "gemm_f16_nt_stream_k_noalloc",
               "gemm_mxfp8_nt", "gemm_mxfp8_scale_bytes", "gemm_mxfp8_pack_scales",
               "gemm_nvfp4_nt", "gemm_nvfp4_nt_ex", "gemm_nvfp4_scale_bytes", "gemm_nvfp4_pack_scales"]:
@@ -182,33 +182,44 @@ def test_f16_selector(lib):
         g.gemm_f16_select(1, 1, 1, 0)
 
 
-def test_skinny_split_plan(lib):
-    # Worked cases on 152 SMs: shares per 128-column tile, k-blocks per share.
-    assert g.gemm_debug_skinny_split_plan(8192, 8192, 152) == (2, 64)     # 64 tiles
-    assert g.gemm_debug_skinny_split_plan(16384, 8192, 152) == (1, 128)   # 128 tiles: no room
-    assert g.gemm_debug_skinny_split_plan(4096, 4096, 152) == (4, 16)     # 32 tiles
-    assert g.gemm_debug_skinny_split_plan(1000, 12008, 152) == (8, 24)    # 8 tiles, 188 k-blocks
-    assert g.gemm_debug_skinny_split_plan(4000, 2056, 152) == (4, 9)      # 33 k-blocks: ragged
-    assert g.gemm_debug_skinny_split_plan(77, 72, 152) == (1, 2)          # too shallow to split
-    assert g.gemm_debug_skinny_split_plan(77, 0, 152) == (1, 1)           # K = 0
+def test_skinny_plan(lib):
+    # Worked cases on 152 SMs: (shares, rows per group, groups, k-blocks a share).
+    assert g.gemm_debug_skinny_plan(8192, 8192, 152) == (2, 128, 64, 64)
+    assert g.gemm_debug_skinny_plan(16384, 8192, 152) == (1, 128, 128, 128)  # no room to split
+    assert g.gemm_debug_skinny_plan(4096, 4096, 152) == (4, 128, 32, 16)
+    assert g.gemm_debug_skinny_plan(1000, 12008, 152) == (8, 128, 8, 24)     # 188 k-blocks
+    assert g.gemm_debug_skinny_plan(4000, 2056, 152) == (4, 128, 32, 9)      # 33 k-blocks: ragged
+    assert g.gemm_debug_skinny_plan(19456, 1024, 152) == (1, 128, 152, 16)   # exactly one wave
+    assert g.gemm_debug_skinny_plan(28672, 8192, 152) == (1, 96, 299, 128)   # two even waves
+    assert g.gemm_debug_skinny_plan(77, 72, 152) == (1, 128, 1, 2)           # too shallow to split
+    assert g.gemm_debug_skinny_plan(77, 0, 152) == (1, 128, 1, 1)            # K = 0
     with pytest.raises(ValueError):
-        g.gemm_debug_skinny_split_plan(0, 64, 152)
+        g.gemm_debug_skinny_plan(0, 64, 152)
 
 
-def test_skinny_split_plan_properties(lib):
-    # Against the rule itself, over a grid of shapes: a power of two up to 8;
-    # tiles x shares within the CTA target; at least 8 k-blocks a share; the
-    # shares cover K with none empty; and the next power of two breaks a rule.
-    for N in (1, 127, 128, 129, 1000, 4096, 8192, 16384, 28672):
-        for K in (8, 64, 512, 520, 4096, 12008, 65536):
+def test_skinny_plan_properties(lib):
+    # Against the rule itself, over a grid of shapes: the shares a power of
+    # two up to 8, each at least 8 k-blocks, their CTAs within the slots, and
+    # the next power of two breaking one of these; groups of 128 rows unless
+    # 128-row groups need several waves, then the multiple of 8 that fills
+    # that many waves; groups and k-blocks covering N and K.
+    for N in (1, 127, 128, 129, 1000, 4096, 8192, 16384, 19456, 19457, 28672):
+        for K in (0, 8, 64, 512, 520, 4096, 12008, 65536):
             for ctas in (1, 19, 152, 304):
-                s, per = g.gemm_debug_skinny_split_plan(N, K, ctas)
+                s, rows, groups, kb = g.gemm_debug_skinny_plan(N, K, ctas)
                 tiles, nkb = -(-N // 128), -(-K // 64)
                 assert s in (1, 2, 4, 8)
-                assert per * s >= nkb and per >= 1
                 if s > 1:
-                    assert tiles * s <= ctas and nkb // s >= 8 and (s - 1) * per < nkb
+                    assert tiles * s <= ctas and nkb // s >= 8
                 assert 2 * s > 8 or tiles * 2 * s > ctas or nkb // (2 * s) < 8
+                if s > 1 or tiles <= ctas:
+                    assert rows == 128
+                else:
+                    waves = -(-tiles // ctas)
+                    assert rows % 8 == 0 and rows <= 128 and rows * waves * ctas >= N
+                    assert rows - 8 < -(-N // (waves * ctas))
+                assert groups == -(-N // rows) and (groups - 1) * rows < N
+                assert kb == max(1, -(-nkb // s)) and kb * s >= nkb
 
 
 def test_f16_selector_raster(lib):

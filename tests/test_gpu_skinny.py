@@ -49,11 +49,11 @@ def _run(A, B, variant=g.GEMM_F16_SKINNY, pad=64):
     return _unguard(buf, M, N, pad)
 
 
-# (N, K) and the shares of K each tile gets on 152 SMs: one partial tile and
-# two k-blocks (1), several tiles with a partial k-block (2), ragged tiles
-# and k-blocks (4), few tiles over a long K (8), N % 4 != 0 (8: the split
-# sum's scalar stores), a full wave of tiles (2).
-SHAPES = [(77, 72), (3000, 1032), (4000, 2056), (1000, 12008), (1001, 4104), (8192, 1024)]
+# (N, K) and the plan on 152 SMs (shares): one partial group over two
+# k-blocks (1), a partial k-block (2), ragged groups and k-blocks (4), a long
+# K (8), N % 4 != 0 (8: the split sum's scalar stores), exactly one wave of
+# groups (1).  Shorter groups (the multi-wave plan) have a test of their own.
+SHAPES = [(77, 72), (3000, 1032), (4000, 2056), (1000, 12008), (1001, 4104), (19456, 1024)]
 
 
 @pytest.mark.parametrize("M", [1, 5, 16, 17, 32, 33, 64])
@@ -78,6 +78,18 @@ def test_skinny_bench_shape_sampled():
     rows, cols = wl.sample_positions(w.M, w.N, 4096, seed=9)
     Cref, S = oracle.gemm_f16_nt_sampled(A, B, rows, cols)
     check_f16(C.cpu().numpy()[rows, cols], Cref, S, what="skinny bench shape")
+
+
+def test_skinny_two_even_waves():
+    # 128-row groups would need just over one wave: groups of 72 rows (not a
+    # power of two) fill two waves instead.
+    sm = torch.cuda.get_device_properties(0).multi_processor_count
+    M, N, K = 3, sm * 128 + 500, 256
+    A = wl.draw_f16((M, K), seed=81, dist="normal")
+    B = wl.draw_f16((N, K), seed=82, dist="normal")
+    assert g.gemm_debug_skinny_plan(N, K, sm)[1] < 128
+    Cref, S = oracle.gemm_f16_nt(A, B)
+    check_f16(_run(A, B), Cref, S, what=f"skinny two waves {M}x{N}x{K}")
 
 
 def test_skinny_unaligned_output():
