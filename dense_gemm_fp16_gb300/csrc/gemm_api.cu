@@ -123,17 +123,27 @@ int gemm_f16_select(int M, int N, int K, int sm_count, gemm_f16_config *cfg) {
     // reading B from HBM bounds the product.  For one row the matrix-vector
     // kernel streams B once on the CUDA cores; from two rows up to 64 the
     // skinny kernel does (B's rows on the MMA's 128-row side, A's rows on
-    // its N side, K split over clusters so the tiles fill the SMs), where
+    // its N side, K split over clusters so the groups fill the SMs), where
     // the 128-row tiles of A would leave most of each MMA and most SMs idle.
     // When even the 128 x 128 tiles would leave most SMs idle over a long K,
     // the pair kernel splits each pair tile's k-blocks over several pairs
     // (split-K) and spreads the work over all of them.
+    // Up to 128 rows of A the pair tile would be half empty: the 128 x 128
+    // tile serves them, unless the skinny kernel can split K into at least
+    // two shares of 16 k-blocks or more, which measured faster (8192^2 at
+    // M = 128: 27.8 against 35.9 us), as it is for every M <= 64.
     const long long pair_tiles = ceil_div(M, 256) * ceil_div(N, 256);
     const bool split = ceil_div(M, 128) * ceil_div(N, 128) * 2 <= sm_count &&
                        gb300::pair_split_pairs(pair_tiles, ceil_div(K, 64), sm_count / 2) > 0;
     int variant = ((pair_tiles >= sm_count / 2 && N > 128) || split) ? GEMM_F16_256x256_PAIR
                                                                      : GEMM_F16_128x128;
-    if (M <= 64) variant = M <= 1 ? GEMM_F16_GEMV : GEMM_F16_SKINNY;
+    if (M <= 128) {
+        gb300::SkinnyPlan plan;
+        gb300::skinny_plan(N, K, sm_count * gb300::skinny_ctas_per_sm(), nullptr, &plan);
+        const bool skinny_split = plan.splits >= 2 && plan.kb_per_split >= 16;
+        variant = M <= 1 ? GEMM_F16_GEMV
+                         : (M <= 64 || skinny_split) ? GEMM_F16_SKINNY : GEMM_F16_128x128;
+    }
     cfg->variant = variant;
     cfg->grid = f16_default_grid(variant, M, N, K, sm_count);
     cfg->flags = 0;
@@ -234,8 +244,8 @@ static int f16_nt_impl(int M, int N, int K, const void *A, const void *B, void *
         sel.grid = f16_default_grid(sel.variant, M, N, K, sms);
         if (sel.variant == GEMM_F16_GEMV && M > 4)
             return fail(GEMM_ERR_UNSUPPORTED, "gemm_f16_nt_ex: the GEMV variant takes M <= 4 (M=%d)", M);
-        if (sel.variant == GEMM_F16_SKINNY && M > 64)
-            return fail(GEMM_ERR_UNSUPPORTED, "gemm_f16_nt_ex: the skinny variant takes M <= 64 (M=%d)", M);
+        if (sel.variant == GEMM_F16_SKINNY && M > 128)
+            return fail(GEMM_ERR_UNSUPPORTED, "gemm_f16_nt_ex: the skinny variant takes M <= 128 (M=%d)", M);
     }
     if (cfg && cfg->grid > 0) sel.grid = cfg->grid;
     if (cfg && cfg->variant != GEMM_F16_AUTO) sel.raster = f16_default_raster(sel.variant, M, N, K);

@@ -103,7 +103,7 @@ struct GemvLaunch {
 
 int gemv_launch(const GemvLaunch &L, std::string &err);
 
-// One fp16 product with a few rows of A (M <= 64), computed as B * A^T on the
+// One fp16 product with a few rows of A (M <= 128), computed as B * A^T on the
 // tensor cores with the K range split over CTAs, after validation.
 struct SkinnyLaunch {
     int M, N, K;

@@ -6,7 +6,7 @@
 // is read once and the work is bound by HBM.  The tile kernels' 128-row tiles
 // of A would leave 120 of the MMA's 128 rows empty and give one tile per
 // 128 columns of C: at N = 8192, 64 CTAs for 152 SMs.  Here B's rows take the
-// MMA's M = 128 and A's rows its N (16, 32 or 64, the rows past M zero-filled
+// MMA's M = 128 and A's rows its N (16, 32, 64 or 128, the rows past M zero-filled
 // by TMA), so a tile is 128 columns of C by all of its rows, and the K range
 // is split over enough CTAs to fill the SMs ("第 6 章 · Shared Memory & Tile",
 // section "6.5.6 Split-K / Stream-K").
@@ -58,7 +58,7 @@ struct SkCfg {
     static constexpr int kNumBars = 2 * STAGES + 2;    // full, empty, accumulator ready, drain
     static constexpr int kBarOffset = STAGES * kStageBytes;
     static constexpr int kSmemBytes = 1024 + kBarOffset + kNumBars * 8 + 16;  // + TMEM slot and flags
-    static_assert(MN == 16 || MN == 32 || MN == 64, "an MMA N for M = 128");
+    static_assert(MN == 16 || MN == 32 || MN == 64 || MN == 128, "an MMA N for M = 128");
     static_assert(kABytes % 1024 == 0, "stages keep the 1 KB alignment of the swizzled boxes");
     static_assert(kSmemBytes <= 232448, "fits the 227 KB opt-in limit");
 };
@@ -263,10 +263,10 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         const int n = row0 + quarter * 32 + lane;
         if (args.splits == 1 && ok && n < nend) {
 #pragma unroll
-            for (int m = 0; m < MN; ++m) {
-                if (m >= args.M) break;
-                args.C[static_cast<size_t>(m) * args.N + n] =
-                    skinny_out(args.epi, __uint_as_float(v[m]), m, n, args.N);
+            for (int m = 0; m < MN; ++m) {  // (a guard, not an early exit: v stays in registers)
+                if (m < args.M)
+                    args.C[static_cast<size_t>(m) * args.N + n] =
+                        skinny_out(args.epi, __uint_as_float(v[m]), m, n, args.N);
             }
         }
         __syncwarp();
@@ -300,10 +300,8 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         if (warp >= 2) {
             const int nl = (warp & 3) * 32 + lane;
 #pragma unroll
-            for (int m = 0; m < MN; ++m) {
-                if (m >= args.M) break;
-                share[m * kSkBM + nl] = __uint_as_float(v[m]);
-            }
+            for (int m = 0; m < MN; ++m)
+                if (m < args.M) share[m * kSkBM + nl] = __uint_as_float(v[m]);
         }
         cluster_sync();
         // CTA r of the cluster (r = its share of K) adds slice r of the tile,
@@ -479,13 +477,14 @@ void skinny_plan(int N, int K, int ctas, const int *cap, SkinnyPlan *plan) {
 }
 
 int skinny_launch(const SkinnyLaunch &L, std::string &err) {
-    if (L.M < 1 || L.M > 64) {
-        err = "skinny: M must be 1..64";
+    if (L.M < 1 || L.M > 128) {
+        err = "skinny: M must be 1..128";
         return GEMM_ERR_INVALID_ARG;
     }
     if (L.M <= 16) return launch_mn<16>(L, err);
     if (L.M <= 32) return launch_mn<32>(L, err);
-    return launch_mn<64>(L, err);
+    if (L.M <= 64) return launch_mn<64>(L, err);
+    return launch_mn<128>(L, err);
 }
 
 int skinny_status_read_clear(cudaStream_t stream, int *code, std::string &err) {

@@ -159,8 +159,10 @@ enum {
     GEMM_F16_GEMV = 4,          /* M <= 4 (chosen for M = 1): B streamed once from */
                                 /* HBM on the CUDA cores, a warp per row block, A  */
                                 /* read through L1                                  */
-    GEMM_F16_SKINNY = 5,        /* M <= 64 (chosen for 2..64): C^T = B A^T on the  */
-                                /* tensor cores, 128 rows of B by all of A per     */
+    GEMM_F16_SKINNY = 5,        /* M <= 128 (chosen for 2..64, and for 65..128     */
+                                /* when K splits into 2+ shares of 16+ k-blocks):  */
+                                /* C^T = B A^T on the tensor cores, 128 rows of B  */
+                                /* by all of A per                                 */
                                 /* group, K split over a cluster of 2-8 CTAs so    */
                                 /* the groups fill the SMs; the shares are added   */
                                 /* in split order through distributed shared       */

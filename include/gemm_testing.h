@@ -21,7 +21,7 @@ extern "C" {
  * GEMM_OK; the fault is then reported by gemm_check_device_status() as
  * GEMM_ERR_DEVICE_TIMEOUT and the CUDA context stays usable.  C is left
  * partially written.  Same argument rules as gemm_f16_nt.  When the
- * selector picks the skinny variant (2 <= M <= 64), every CTA leaves out
+ * selector picks the skinny variant (2 <= M <= 128), every CTA leaves out
  * k-block `skip_kblock` of its own share of K instead, so the CTAs of a split
  * cluster all give up and still meet at the cluster barriers.
  */

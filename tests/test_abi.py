@@ -166,7 +166,16 @@ def test_f16_selector(lib):
     assert g.gemm_f16_select(4, 16384, 8192, 148)[:2] == (g.GEMM_F16_SKINNY, 148)
     assert g.gemm_f16_select(5, 4096, 65536, 152)[0] == g.GEMM_F16_SKINNY
     assert g.gemm_f16_select(64, 8192, 8192, 152)[0] == g.GEMM_F16_SKINNY
-    assert g.gemm_f16_select(65, 8192, 8192, 152)[0] == g.GEMM_F16_128x128
+    assert g.gemm_f16_select(64, 65536, 4096, 152)[0] == g.GEMM_F16_SKINNY
+    # 65 to 128 rows: the skinny kernel where it splits K into at least two
+    # shares of 16 k-blocks or more, else the 128 x 128 tile (never the pair
+    # tile, which would be half empty)
+    assert g.gemm_f16_select(65, 8192, 8192, 152)[0] == g.GEMM_F16_SKINNY
+    assert g.gemm_f16_select(128, 4096, 4096, 152)[0] == g.GEMM_F16_SKINNY
+    assert g.gemm_f16_select(128, 8192, 1024, 152)[0] == g.GEMM_F16_128x128   # 8 k-blocks a share
+    assert g.gemm_f16_select(96, 16384, 8192, 152)[:2] == (g.GEMM_F16_128x128, 128)  # no split
+    assert g.gemm_f16_select(128, 28672, 8192, 152)[:2] == (g.GEMM_F16_128x128, 152)
+    assert g.gemm_f16_select(129, 28672, 8192, 152)[0] == g.GEMM_F16_256x256_PAIR
     # too few wide tiles to fill the SMs: narrow tiles, grid = tile count
     assert g.gemm_f16_select(1024, 1024, 1024, 152)[:2] == (g.GEMM_F16_128x128, 64)
     assert g.gemm_f16_select(100, 100, 64, 152)[:2] == (g.GEMM_F16_128x128, 1)
@@ -174,10 +183,11 @@ def test_f16_selector(lib):
     # few tiles over a long K: pair tiles split along K over all the pairs
     assert g.gemm_f16_select(512, 512, 32768, 152)[:2] == (g.GEMM_F16_256x256_PAIR, 152)
     assert g.gemm_f16_select(256, 256, 65536, 152)[:2] == (g.GEMM_F16_256x256_PAIR, 152)
-    assert g.gemm_f16_select(128, 4096, 8192, 152)[:2] == (g.GEMM_F16_256x256_PAIR, 152)
+    assert g.gemm_f16_select(256, 4096, 8192, 152)[:2] == (g.GEMM_F16_256x256_PAIR, 152)
+    assert g.gemm_f16_select(128, 4096, 8192, 152)[0] == g.GEMM_F16_SKINNY  # its split instead
     # ... but not when a split would be shallower than four ways
     assert g.gemm_f16_select(1024, 1024, 4096, 152)[:2] == (g.GEMM_F16_128x128, 64)
-    assert g.gemm_f16_select(96, 8192, 8192, 152)[:2] == (g.GEMM_F16_128x128, 64)
+    assert g.gemm_f16_select(192, 8192, 8192, 152)[:2] == (g.GEMM_F16_128x128, 128)
     with pytest.raises(g.GemmError):
         g.gemm_f16_select(1, 1, 1, 0)
 

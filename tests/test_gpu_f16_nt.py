@@ -250,9 +250,11 @@ def test_f16_nt_split_k_underfilled(M, N, K, grid):
         check_f16(C, Cref, S, what=f"split-K {M}x{N}x{K} grid {grid} rep {rep}")
 
 
-@pytest.mark.parametrize("M,N,K", [(512, 512, 32768), (256, 256, 65536), (128, 4096, 8192)])
+@pytest.mark.parametrize("M,N,K", [(512, 512, 32768), (256, 256, 65536), (256, 4096, 8192)])
 def test_f16_nt_split_k_selector_shapes_sampled(M, N, K):
     # The selector's choice for these shapes is the split pair kernel.
+    sm = torch.cuda.get_device_properties(0).multi_processor_count
+    assert g.gemm_f16_select(M, N, K, sm)[0] == g.GEMM_F16_256x256_PAIR
     A = wl.draw_f16((M, K), seed=83)
     B = wl.draw_f16((N, K), seed=84)
     dA, dB = A.cuda(), B.cuda()

@@ -1,6 +1,6 @@
 """GPU parity of the skinny variant of gemm_f16_nt (a few rows of A, computed
 as B·Aᵀ on the tensor cores with the K range split over a cluster of CTAs)
-against the float64 oracle: every MMA width (16, 32, 64 rows of A), ragged
+against the float64 oracle: every MMA width (16, 32, 64, 128 rows of A), ragged
 M, N and K, 1, 2, 4 and 8 shares, the fused epilogue on both paths, an
 unaligned C, graph capture, and run-to-run equality of the split sums."""
 import numpy as np
@@ -56,7 +56,7 @@ def _run(A, B, variant=g.GEMM_F16_SKINNY, pad=64):
 SHAPES = [(77, 72), (3000, 1032), (4000, 2056), (1000, 12008), (1001, 4104), (19456, 1024)]
 
 
-@pytest.mark.parametrize("M", [1, 5, 16, 17, 32, 33, 64])
+@pytest.mark.parametrize("M", [1, 5, 16, 17, 32, 33, 64, 65, 128])
 @pytest.mark.parametrize("N,K", SHAPES)
 def test_skinny_full_compare(M, N, K):
     A = wl.draw_f16((M, K), seed=M + 300, dist="normal")
@@ -92,6 +92,19 @@ def test_skinny_two_even_waves():
     check_f16(_run(A, B), Cref, S, what=f"skinny two waves {M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("M", [100, 128])
+def test_skinny_128_rows_split_by_the_selector(M):
+    # 65 to 128 rows with a long K: the selector's skinny kernel, K split
+    # over clusters of 4 (the MMA's N = 128 instance).
+    N, K = 3000, 4104
+    A = wl.draw_f16((M, K), seed=91, dist="normal")
+    B = wl.draw_f16((N, K), seed=92, dist="normal")
+    sm = torch.cuda.get_device_properties(0).multi_processor_count
+    assert g.gemm_f16_select(M, N, K, sm)[0] == g.GEMM_F16_SKINNY
+    Cref, S = oracle.gemm_f16_nt(A, B)
+    check_f16(_run(A, B, variant=g.GEMM_F16_AUTO), Cref, S, what=f"skinny selected {M}x{N}x{K}")
+
+
 def test_skinny_unaligned_output():
     # C two bytes off an 8-byte boundary: the split sum stores half by half.
     M, N, K = 20, 1000, 4096
@@ -103,7 +116,7 @@ def test_skinny_unaligned_output():
 
 def test_skinny_is_selected_for_few_rows():
     sm = torch.cuda.get_device_properties(0).multi_processor_count
-    for M in (2, 5, 64):
+    for M in (2, 5, 64, 100, 128):
         assert g.gemm_f16_select(M, 8192, 8192, sm)[0] == g.GEMM_F16_SKINNY
     M, N, K = 7, 2000, 3000
     A = wl.draw_f16((M, K), seed=71, dist="normal")
@@ -162,8 +175,8 @@ def test_skinny_under_graph_capture():
 
 
 def test_skinny_variant_rejects_too_many_rows():
-    A = torch.zeros((65, 64), dtype=torch.float16, device="cuda")
-    C = torch.zeros((65, 65), dtype=torch.float16, device="cuda")
+    A = torch.zeros((129, 64), dtype=torch.float16, device="cuda")
+    C = torch.zeros((129, 129), dtype=torch.float16, device="cuda")
     with pytest.raises(g.GemmError) as e:
-        g.gemm_f16_nt_ex(65, 65, 64, A.data_ptr(), A.data_ptr(), C.data_ptr(), 0, g.GEMM_F16_SKINNY)
+        g.gemm_f16_nt_ex(129, 129, 64, A.data_ptr(), A.data_ptr(), C.data_ptr(), 0, g.GEMM_F16_SKINNY)
     assert e.value.status == g.GEMM_ERR_UNSUPPORTED
