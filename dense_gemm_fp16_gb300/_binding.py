@@ -118,7 +118,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gemm_f16_nt_stream_k_noalloc.restype = i
         lib.gemm_debug_f16_nt_skip_load.argtypes = [i, i, i, vp, vp, vp, vp, i, ctypes.c_ulonglong]
         lib.gemm_debug_f16_nt_skip_load.restype = i
-        lib.gemm_debug_skinny_plan.argtypes = [i, i, i, ctypes.POINTER(i), ctypes.POINTER(i),
+        lib.gemm_debug_skinny_plan.argtypes = [i, i, i, i, ctypes.POINTER(i), ctypes.POINTER(i),
                                                ctypes.POINTER(i)]
         lib.gemm_debug_skinny_plan.restype = i
         _lib = lib
@@ -240,14 +240,14 @@ def gemm_debug_f16_nt_skip_load(M, N, K, A, B, C, stream, skip_kblock, timeout_n
                                                       skip_kblock, timeout_ns)
 
 
-def gemm_debug_skinny_plan(N, K, ctas):
+def gemm_debug_skinny_plan(N, K, ctas, M=1):
     """(shares, rows per group, groups, k-blocks per share) the skinny variant
     plans (host logic only; every slot assumed to hold a cluster of each size)."""
     rows, groups, kb = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
-    splits = load_library().gemm_debug_skinny_plan(N, K, ctas, ctypes.byref(rows), ctypes.byref(groups),
+    splits = load_library().gemm_debug_skinny_plan(M, N, K, ctas, ctypes.byref(rows), ctypes.byref(groups),
                                                    ctypes.byref(kb))
     if splits < 0:
-        raise ValueError(f"bad plan arguments N={N} K={K} ctas={ctas}")
+        raise ValueError(f"bad plan arguments M={M} N={N} K={K} ctas={ctas}")
     return splits, rows.value, groups.value, kb.value
 
 

@@ -112,37 +112,49 @@ int gemm_f16_select(int M, int N, int K, int sm_count, gemm_f16_config *cfg) {
     if (M < 0 || N < 0 || K < 0 || sm_count <= 0)
         return fail(GEMM_ERR_INVALID_ARG, "gemm_f16_select: bad M=%d N=%d K=%d sm_count=%d", M, N,
                     K, sm_count);
-    // The CTA-pair 256 x 256 tile brings the fewest bytes into each SM per
-    // MMA (A and half of B: 32 KB per 64-deep k-block for 4 M FMA per SM) and
-    // is the default whenever its tiles keep every SM pair busy.  Otherwise
-    // the 128 x 128 tile gives 4x the tiles so small problems still spread
-    // over the SMs.  (The 1-CTA 128 x 256 tile has no shape range of its own
-    // between the two: it fills the SMs exactly when the pair tile fills the
-    // pairs; it stays available through gemm_f16_nt_ex.)
     // With a few rows of A every element of B is used only a few times:
     // reading B from HBM bounds the product.  For one row the matrix-vector
     // kernel streams B once on the CUDA cores; from two rows up to 64 the
     // skinny kernel does (B's rows on the MMA's 128-row side, A's rows on
-    // its N side, K split over clusters so the groups fill the SMs), where
+    // its N side, K split over clusters so the tiles fill the SMs), where
     // the 128-row tiles of A would leave most of each MMA and most SMs idle.
-    // When even the 128 x 128 tiles would leave most SMs idle over a long K,
-    // the pair kernel splits each pair tile's k-blocks over several pairs
-    // (split-K) and spreads the work over all of them.
-    // Up to 128 rows of A the pair tile would be half empty: the 128 x 128
-    // tile serves them, unless the skinny kernel can split K into at least
-    // two shares of 16 k-blocks or more, which measured faster (8192^2 at
-    // M = 128: 27.8 against 35.9 us), as it is for every M <= 64.
-    const long long pair_tiles = ceil_div(M, 256) * ceil_div(N, 256);
-    const bool split = ceil_div(M, 128) * ceil_div(N, 128) * 2 <= sm_count &&
-                       gb300::pair_split_pairs(pair_tiles, ceil_div(K, 64), sm_count / 2) > 0;
-    int variant = ((pair_tiles >= sm_count / 2 && N > 128) || split) ? GEMM_F16_256x256_PAIR
-                                                                     : GEMM_F16_128x128;
-    if (M <= 128) {
-        gb300::SkinnyPlan plan;
-        gb300::skinny_plan(N, K, sm_count * gb300::skinny_ctas_per_sm(), nullptr, &plan);
-        const bool skinny_split = plan.splits >= 2 && plan.kb_per_split >= 16;
-        variant = M <= 1 ? GEMM_F16_GEMV
-                         : (M <= 64 || skinny_split) ? GEMM_F16_SKINNY : GEMM_F16_128x128;
+    // The skinny kernel also takes any M whose 128 x 128 tiles are too few to
+    // fill the SMs, when it can split K into 2 shares of at least 16
+    // k-blocks or into 4 or more (measured 1.5-8x faster than the tile
+    // kernels there: 160 x 2048 x 8192 13.3 against 29.8 us).
+    int variant;
+    gb300::SkinnyPlan plan;
+    gb300::skinny_plan(M, N, K, sm_count * gb300::skinny_ctas_per_sm(), nullptr, &plan);
+    const bool skinny_split = plan.splits >= 4 || (plan.splits == 2 && plan.kb_per_split >= 16);
+    if (M <= 1) {
+        variant = GEMM_F16_GEMV;
+    } else if (M <= 64 || skinny_split) {
+        variant = GEMM_F16_SKINNY;
+    } else if (M <= 128) {
+        variant = GEMM_F16_128x128;  // a pair tile would be half empty
+    } else {
+        // Otherwise the tile whose waves cost least: a wave of 128 x 256 tiles
+        // or of 256 x 256 pair tiles takes about 1.15 and 1.1 times a wave of
+        // 128 x 128 tiles (1.5 for both with K <= 512, where the wider tiles'
+        // set-up and drain weigh more), fitted to a GB300 sweep of M 160-2048,
+        // N 2048-28672, K 512-8192 (mean 0.5 % from the best tile).  Ties go
+        // to the smaller tile.
+        const long long t128 = ceil_div(M, 128) * ceil_div(N, 128);
+        const long long t256 = ceil_div(M, 128) * ceil_div(N, 256);
+        const long long tpair = ceil_div(M, 256) * ceil_div(N, 256);
+        const bool short_k = ceil_div(K, 64) <= 8;
+        const double c256 = short_k ? 1.5 : 1.15, cpair = short_k ? 1.5 : 1.1;
+        const long long pairs = sm_count / 2 > 0 ? sm_count / 2 : 1;
+        const double w128 = static_cast<double>(ceil_div(t128, sm_count));
+        const double w256 = c256 * static_cast<double>(ceil_div(t256, sm_count));
+        const double wpair = cpair * static_cast<double>(ceil_div(tpair, pairs));
+        variant = GEMM_F16_128x128;
+        double best = w128;
+        if (w256 < best) {
+            variant = GEMM_F16_128x256;
+            best = w256;
+        }
+        if (wpair < best) variant = GEMM_F16_256x256_PAIR;
     }
     cfg->variant = variant;
     cfg->grid = f16_default_grid(variant, M, N, K, sm_count);
@@ -244,8 +256,6 @@ static int f16_nt_impl(int M, int N, int K, const void *A, const void *B, void *
         sel.grid = f16_default_grid(sel.variant, M, N, K, sms);
         if (sel.variant == GEMM_F16_GEMV && M > 4)
             return fail(GEMM_ERR_UNSUPPORTED, "gemm_f16_nt_ex: the GEMV variant takes M <= 4 (M=%d)", M);
-        if (sel.variant == GEMM_F16_SKINNY && M > 128)
-            return fail(GEMM_ERR_UNSUPPORTED, "gemm_f16_nt_ex: the skinny variant takes M <= 128 (M=%d)", M);
     }
     if (cfg && cfg->grid > 0) sel.grid = cfg->grid;
     if (cfg && cfg->variant != GEMM_F16_AUTO) sel.raster = f16_default_raster(sel.variant, M, N, K);
@@ -312,10 +322,10 @@ int gemm_debug_f16_nt_skip_load(int M, int N, int K, const void *A, const void *
 }
 
 // Test hook declared in gemm_testing.h: the skinny variant's plan.
-int gemm_debug_skinny_plan(int N, int K, int ctas, int *rows, int *groups, int *kb_per_split) {
-    if (N < 1 || K < 0 || ctas < 1 || !rows || !groups || !kb_per_split) return -1;
+int gemm_debug_skinny_plan(int M, int N, int K, int ctas, int *rows, int *groups, int *kb_per_split) {
+    if (M < 1 || N < 1 || K < 0 || ctas < 1 || !rows || !groups || !kb_per_split) return -1;
     gb300::SkinnyPlan p;
-    gb300::skinny_plan(N, K, ctas, nullptr, &p);
+    gb300::skinny_plan(M, N, K, ctas, nullptr, &p);
     *rows = p.rows;
     *groups = p.groups;
     *kb_per_split = p.kb_per_split;

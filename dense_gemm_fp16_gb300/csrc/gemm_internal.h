@@ -103,7 +103,7 @@ struct GemvLaunch {
 
 int gemv_launch(const GemvLaunch &L, std::string &err);
 
-// One fp16 product with a few rows of A (M <= 128), computed as B * A^T on the
+// One fp16 product computed as B * A^T on the
 // tensor cores with the K range split over CTAs, after validation.
 struct SkinnyLaunch {
     int M, N, K;
@@ -122,20 +122,21 @@ struct SkinnyLaunch {
 int skinny_ctas_per_sm();
 
 // How a skinny launch spreads the product: `groups` groups of `rows`
-// columns of C (rows of B), each group's K range in `splits` shares of
-// `kb_per_split` 64-deep k-blocks (the last may be shorter), one CTA per
-// share, a group's shares one cluster.
+// columns of C (rows of B) times `mtiles` tiles of up to 128 rows of A, each
+// tile's K range in `splits` shares of `kb_per_split` 64-deep k-blocks (the
+// last may be shorter), one CTA per share, a tile's shares one cluster.
 struct SkinnyPlan {
     int splits;        // 1, 2, 4 or 8
     int rows;          // a multiple of 8, at most 128
     int groups;        // ceil(N / rows)
     int kb_per_split;
+    int mtiles;        // 1 for M <= 128, else ceil(M / 128)
 };
 
-// The plan for N columns of C and depth K on `ctas` CTA slots; cap[l] is the
-// number of clusters of 2^l CTAs the device holds at once (cap[0] = ctas), or
-// cap == nullptr to take ctas / 2^l.  Host logic only.
-void skinny_plan(int N, int K, int ctas, const int *cap, SkinnyPlan *plan);
+// The plan for an M x N product of depth K on `ctas` CTA slots; cap[l] is
+// the number of clusters of 2^l CTAs the device holds at once (cap[0] =
+// ctas), or cap == nullptr to take ctas / 2^l.  Host logic only.
+void skinny_plan(int M, int N, int K, int ctas, const int *cap, SkinnyPlan *plan);
 
 int skinny_launch(const SkinnyLaunch &L, std::string &err);
 

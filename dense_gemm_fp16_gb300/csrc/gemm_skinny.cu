@@ -1,5 +1,6 @@
-// gemm_skinny.cu -- C = A * B^T for a few rows of A (M <= 64) on the
-// tensor cores, as the swapped product D = B * A^T (D = C^T).
+// gemm_skinny.cu -- C = A * B^T on the tensor cores as the swapped product
+// D = B * A^T (D = C^T), for a few rows of A or for too few tiles to fill
+// the SMs without splitting K.
 //
 // Same operation and numerics as gemm_f16_nt (half inputs, fp32
 // accumulation, one round-to-nearest-even per output).  With M this small, B
@@ -7,8 +8,9 @@
 // of A would leave 120 of the MMA's 128 rows empty and give one tile per
 // 128 columns of C: at N = 8192, 64 CTAs for 152 SMs.  Here B's rows take the
 // MMA's M = 128 and A's rows its N (16, 32, 64 or 128, the rows past M zero-filled
-// by TMA), so a tile is 128 columns of C by all of its rows, and the K range
-// is split over enough CTAs to fill the SMs ("第 6 章 · Shared Memory & Tile",
+// by TMA), so a tile is 128 columns of C by all of its rows (by 128 of them
+// per tile on the grid's third dimension when M > 128), and the K range is
+// split over enough CTAs to fill the SMs ("第 6 章 · Shared Memory & Tile",
 // section "6.5.6 Split-K / Stream-K").
 //
 // Per CTA: warp 0 issues TMA loads of B's 128 x 64 box and A's MN x 64 box
@@ -144,6 +146,8 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     // which only reaches TMEM lanes the epilogue never reads
     const uint32_t stage_tx = static_cast<uint32_t>(args.rows + MN) * (kSkBK * 2);
     const int split = blockIdx.y;  // share of K
+    const int m0 = static_cast<int>(blockIdx.z) * MN;  // first row of A (and of C) of this tile
+    const int mt = args.M - m0 < MN ? args.M - m0 : MN;  // its rows of A
     const int kb0 = split * args.kb_per_split;
     const int kb1 = kb0 + args.kb_per_split < args.num_kb ? kb0 + args.kb_per_split : args.num_kb;
 
@@ -190,7 +194,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                     armed |= 1u << stage;
                     arm_parity ^= 1u << stage;
                     tma_load_2d(sb, &tmB, full_bar(stage), kb * kSkBK, row0);
-                    tma_load_2d(sb + T::kBBytes, &tmA, full_bar(stage), kb * kSkBK, 0);
+                    tma_load_2d(sb + T::kBBytes, &tmA, full_bar(stage), kb * kSkBK, m0);
                 }
                 if (++stage == STAGES) {
                     stage = 0;
@@ -264,9 +268,9 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         if (args.splits == 1 && ok && n < nend) {
 #pragma unroll
             for (int m = 0; m < MN; ++m) {  // (a guard, not an early exit: v stays in registers)
-                if (m < args.M)
-                    args.C[static_cast<size_t>(m) * args.N + n] =
-                        skinny_out(args.epi, __uint_as_float(v[m]), m, n, args.N);
+                if (m < mt)
+                    args.C[static_cast<size_t>(m0 + m) * args.N + n] =
+                        skinny_out(args.epi, __uint_as_float(v[m]), m0 + m, n, args.N);
             }
         }
         __syncwarp();
@@ -301,12 +305,12 @@ __global__ void __launch_bounds__(kSkThreads, 1)
             const int nl = (warp & 3) * 32 + lane;
 #pragma unroll
             for (int m = 0; m < MN; ++m)
-                if (m < args.M) share[m * kSkBM + nl] = __uint_as_float(v[m]);
+                if (m < mt) share[m * kSkBM + nl] = __uint_as_float(v[m]);
         }
         cluster_sync();
         // CTA r of the cluster (r = its share of K) adds slice r of the tile,
         // four consecutive columns per thread, over the shares in order.
-        const int groups = args.M * (kSkBM / 4);
+        const int groups = mt * (kSkBM / 4);
         const int per = (groups + args.splits - 1) / args.splits;
         const int g0 = split * per;
         const int g1 = g0 + per < groups ? g0 + per : groups;
@@ -321,7 +325,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                 sum.z += x.z;
                 sum.w += x.w;
             }
-            const int m = gi / (kSkBM / 4);
+            const int m = m0 + gi / (kSkBM / 4);
             const int n = row0 + (gi % (kSkBM / 4)) * 4;
             __half *out = args.C + static_cast<size_t>(m) * args.N + n;
             const float s4[4] = {sum.x, sum.y, sum.z, sum.w};
@@ -410,7 +414,7 @@ int launch_mn(const SkinnyLaunch &L, std::string &err) {
         if (cap[l] < 0) return GEMM_ERR_CUDA;
     }
     SkinnyPlan plan;
-    skinny_plan(L.N, L.K, L.ctas, cap, &plan);
+    skinny_plan(L.M, L.N, L.K, L.ctas, cap, &plan);
     const int num_kb = (L.K + kSkBK - 1) / kSkBK;
     const int splits = plan.splits;
     const int tiles = plan.groups;
@@ -428,7 +432,7 @@ int launch_mn(const SkinnyLaunch &L, std::string &err) {
     attr[1].val.clusterDim.x = 1;
     attr[1].val.clusterDim.y = splits;
     attr[1].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(tiles, splits);
+    cfg.gridDim = dim3(tiles, splits, plan.mtiles);
     cfg.blockDim = dim3(kSkThreads);
     cfg.dynamicSmemBytes = T::kSmemBytes;
     cfg.stream = L.stream;
@@ -446,14 +450,15 @@ int launch_mn(const SkinnyLaunch &L, std::string &err) {
 
 int skinny_ctas_per_sm() { return kSkCtasPerSm; }
 
-void skinny_plan(int N, int K, int ctas, const int *cap, SkinnyPlan *plan) {
+void skinny_plan(int M, int N, int K, int ctas, const int *cap, SkinnyPlan *plan) {
     const int num_kb = (K + kSkBK - 1) / kSkBK;
-    const int tiles = (N + kSkBM - 1) / kSkBM;
+    const int mtiles = M <= kSkBM ? 1 : (M + kSkBM - 1) / kSkBM;  // 128-row tiles of A
+    const long long tiles = static_cast<long long>((N + kSkBM - 1) / kSkBM) * mtiles;
     // An SM's rate goes with the k-blocks its ring keeps in flight, not with
     // the rows each carries: shorter groups or fewer shares measured slower.
-    // So the groups stay 128 rows and each gets the largest power of two of
-    // shares (at most 8, each at least 8 k-blocks) for which all the groups'
-    // clusters are resident at once.
+    // So the groups stay 128 rows and each tile gets the largest power of
+    // two of shares (at most 8, each at least 8 k-blocks) for which all the
+    // tiles' clusters are resident at once.
     int s = 1;
     for (int l = 3; l >= 1; --l) {
         const int c = 1 << l;
@@ -465,20 +470,20 @@ void skinny_plan(int N, int K, int ctas, const int *cap, SkinnyPlan *plan) {
         }
     }
     int rows = kSkBM;
-    if (s == 1 && tiles > ctas && ctas > 0) {
+    if (s == 1 && mtiles == 1 && tiles > ctas && ctas > 0) {
         // more than one wave: spread the rows evenly over the waves, so that
         // the last wave is as full as the others
-        const long long slots = static_cast<long long>((tiles + ctas - 1) / ctas) * ctas;
+        const long long slots = ((tiles + ctas - 1) / ctas) * ctas;
         rows = static_cast<int>((N + slots - 1) / slots);
         rows = (rows + 7) & ~7;
     }
     const int kbs = (num_kb + s - 1) / s;
-    *plan = SkinnyPlan{s, rows, (N + rows - 1) / rows, kbs > 0 ? kbs : 1};
+    *plan = SkinnyPlan{s, rows, (N + rows - 1) / rows, kbs > 0 ? kbs : 1, mtiles};
 }
 
 int skinny_launch(const SkinnyLaunch &L, std::string &err) {
-    if (L.M < 1 || L.M > 128) {
-        err = "skinny: M must be 1..128";
+    if (L.M < 1 || (L.M + kSkBM - 1) / kSkBM > 65535) {
+        err = "skinny: M must be 1..65535*128";
         return GEMM_ERR_INVALID_ARG;
     }
     if (L.M <= 16) return launch_mn<16>(L, err);

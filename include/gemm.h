@@ -140,13 +140,14 @@ typedef struct {
  * default: on GB300 at the benchmark shapes the partial hand-off costs more
  * than the balanced last round gains.
  *
- * Split-K, by contrast, is on by default, with no flag: when there are so few
- * pair tiles that each would get at least four CTA pairs ("第 6 章 · Shared
- * Memory & Tile", section "6.5.6 Split-K / Stream-K"), every tile's k-blocks
- * are shared over up to 8 pairs (at least 32 k-blocks each) through the same
- * workspace, and gemm_f16_select picks the pair kernel with all pairs for
- * such shapes.  The partials are added in a fixed order: results do not
- * depend on timing.  Also skipped under stream capture.
+ * Split-K, by contrast, is on by default in the pair variant, with no flag:
+ * when there are so few pair tiles that each would get at least four CTA
+ * pairs ("第 6 章 · Shared Memory & Tile", section "6.5.6 Split-K /
+ * Stream-K"), every tile's k-blocks are shared over up to 8 pairs (at least
+ * 32 k-blocks each) through the same workspace.  The partials are added in a
+ * fixed order: results do not depend on timing.  Also skipped under stream
+ * capture.  gemm_f16_select sends such shapes to GEMM_F16_SKINNY instead,
+ * whose split needs no workspace.
  */
 #define GEMM_F16_FLAG_STREAM_K 1
 
@@ -159,15 +160,14 @@ enum {
     GEMM_F16_GEMV = 4,          /* M <= 4 (chosen for M = 1): B streamed once from */
                                 /* HBM on the CUDA cores, a warp per row block, A  */
                                 /* read through L1                                  */
-    GEMM_F16_SKINNY = 5,        /* M <= 128 (chosen for 2..64, and for 65..128     */
-                                /* when K splits into 2+ shares of 16+ k-blocks):  */
-                                /* C^T = B A^T on the tensor cores, 128 rows of B  */
-                                /* by all of A per                                 */
-                                /* group, K split over a cluster of 2-8 CTAs so    */
-                                /* the groups fill the SMs; the shares are added   */
-                                /* in split order through distributed shared       */
-                                /* memory (no workspace; the tile kernels'         */
-                                /* numerics)                                        */
+    GEMM_F16_SKINNY = 5,        /* C^T = B A^T on the tensor cores: 128 rows of B  */
+                                /* by up to 128 rows of A per tile, K split over a */
+                                /* cluster of 2-8 CTAs so the tiles fill the SMs,  */
+                                /* the shares added in split order through         */
+                                /* distributed shared memory (no workspace; the    */
+                                /* tile kernels' numerics).  Chosen for 2 <= M <=  */
+                                /* 64, and for any M whose tiles it splits in two  */
+                                /* shares of 16+ k-blocks or in four or more       */
     GEMM_F16_NUM_VARIANTS = 6
 };
 

@@ -30,18 +30,18 @@ int gemm_debug_f16_nt_skip_load(int M, int N, int K, const void *A, const void *
                                 unsigned long long timeout_ns);
 
 /*
- * How the skinny fp16 variant (GEMM_F16_SKINNY) spreads a product with N
- * columns of C and depth K over `ctas` CTA slots: pure host logic, no device
- * call, assuming every slot can hold a cluster of each size (the launch uses
- * the device's own cluster counts).  The columns go in *groups groups of
- * *rows (128, or, when 128-row groups need more than one wave, the multiple
- * of 8 that fills every wave evenly); each group's K range in the returned
- * number of shares (the largest of 2, 4, 8 with groups x shares <= ctas and
- * at least 8 k-blocks of 64 a share, else 1) of *kb_per_split k-blocks, one
- * CTA per share.  Returns -1 for N < 1, K < 0, ctas < 1 or a NULL output
- * pointer.
+ * How the skinny fp16 variant (GEMM_F16_SKINNY) spreads an M x N product of
+ * depth K over `ctas` CTA slots: pure host logic, no device call, assuming
+ * every slot can hold a cluster of each size (the launch uses the device's
+ * own cluster counts).  A's rows go in tiles of 128 (one tile for M <= 128),
+ * C's columns in *groups groups of *rows (128, or, when M <= 128 and 128-row
+ * groups need more than one wave, the multiple of 8 that fills every wave
+ * evenly); each tile's K range in the returned number of shares (the largest
+ * of 2, 4, 8 with tiles x shares <= ctas and at least 8 k-blocks of 64 a
+ * share, else 1) of *kb_per_split k-blocks, one CTA per share.  Returns -1
+ * for M < 1, N < 1, K < 0, ctas < 1 or a NULL output pointer.
  */
-int gemm_debug_skinny_plan(int N, int K, int ctas, int *rows, int *groups, int *kb_per_split);
+int gemm_debug_skinny_plan(int M, int N, int K, int ctas, int *rows, int *groups, int *kb_per_split);
 
 #ifdef __cplusplus
 }

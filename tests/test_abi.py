@@ -154,9 +154,7 @@ def test_f16_selector(lib):
     assert g.gemm_f16_select(5376, 5376, 2048, 152)[:2] == (g.GEMM_F16_256x256_PAIR, 152)
     assert g.gemm_f16_select(5000, 5376, 2040, 152)[:2] == (g.GEMM_F16_256x256_PAIR, 152)
     assert g.gemm_f16_select(5376, 5376, 2048, 151)[:2] == (g.GEMM_F16_256x256_PAIR, 150)
-    assert g.gemm_f16_select(4096, 2048, 512, 148)[:2] == (g.GEMM_F16_256x256_PAIR, 148)
-    # fewer pair tiles than SM pairs: narrow tiles
-    assert g.gemm_f16_select(2048, 2048, 512, 152)[:2] == (g.GEMM_F16_128x128, 152)
+    assert g.gemm_f16_select(8192, 8192, 8192, 152)[:2] == (g.GEMM_F16_256x256_PAIR, 152)
     # one row of A: the HBM-bound matrix-vector kernel, planned per SM
     assert g.gemm_f16_select(1, 5376, 2048, 152)[:2] == (g.GEMM_F16_GEMV, 152)
     assert g.gemm_f16_select(1, 4096, 65536, 152)[0] == g.GEMM_F16_GEMV
@@ -167,27 +165,30 @@ def test_f16_selector(lib):
     assert g.gemm_f16_select(5, 4096, 65536, 152)[0] == g.GEMM_F16_SKINNY
     assert g.gemm_f16_select(64, 8192, 8192, 152)[0] == g.GEMM_F16_SKINNY
     assert g.gemm_f16_select(64, 65536, 4096, 152)[0] == g.GEMM_F16_SKINNY
-    # 65 to 128 rows: the skinny kernel where it splits K into at least two
-    # shares of 16 k-blocks or more, else the 128 x 128 tile (never the pair
-    # tile, which would be half empty)
-    assert g.gemm_f16_select(65, 8192, 8192, 152)[0] == g.GEMM_F16_SKINNY
-    assert g.gemm_f16_select(128, 4096, 4096, 152)[0] == g.GEMM_F16_SKINNY
-    assert g.gemm_f16_select(128, 8192, 1024, 152)[0] == g.GEMM_F16_128x128   # 8 k-blocks a share
-    assert g.gemm_f16_select(96, 16384, 8192, 152)[:2] == (g.GEMM_F16_128x128, 128)  # no split
-    assert g.gemm_f16_select(128, 28672, 8192, 152)[:2] == (g.GEMM_F16_128x128, 152)
-    assert g.gemm_f16_select(129, 28672, 8192, 152)[0] == g.GEMM_F16_256x256_PAIR
-    # too few wide tiles to fill the SMs: narrow tiles, grid = tile count
+    # any M whose 128 x 128 tiles leave SMs idle: the skinny kernel when it
+    # splits K in two shares of 16+ k-blocks, or in four or more
+    assert g.gemm_f16_select(65, 8192, 8192, 152)[0] == g.GEMM_F16_SKINNY       # 2 x 64
+    assert g.gemm_f16_select(128, 4096, 4096, 152)[0] == g.GEMM_F16_SKINNY      # 4 x 16
+    assert g.gemm_f16_select(160, 2048, 8192, 152)[0] == g.GEMM_F16_SKINNY      # 4 x 32
+    assert g.gemm_f16_select(512, 512, 32768, 152)[0] == g.GEMM_F16_SKINNY      # 8 x 64
+    assert g.gemm_f16_select(256, 256, 65536, 152)[0] == g.GEMM_F16_SKINNY      # 8 x 128
+    assert g.gemm_f16_select(1024, 1024, 4096, 152)[0] == g.GEMM_F16_SKINNY     # 2 x 32
+    assert g.gemm_f16_select(128, 8192, 1024, 152)[0] == g.GEMM_F16_128x128     # 2 x 8 only
     assert g.gemm_f16_select(1024, 1024, 1024, 152)[:2] == (g.GEMM_F16_128x128, 64)
+    # up to 128 rows without such a split: the 128 x 128 tile (a pair tile
+    # would be half empty), grid = tile count up to one per SM
+    assert g.gemm_f16_select(96, 16384, 8192, 152)[:2] == (g.GEMM_F16_128x128, 128)
+    assert g.gemm_f16_select(128, 28672, 8192, 152)[:2] == (g.GEMM_F16_128x128, 152)
     assert g.gemm_f16_select(100, 100, 64, 152)[:2] == (g.GEMM_F16_128x128, 1)
-    assert g.gemm_f16_select(128, 8192, 64, 148)[0] == g.GEMM_F16_128x128
-    # few tiles over a long K: pair tiles split along K over all the pairs
-    assert g.gemm_f16_select(512, 512, 32768, 152)[:2] == (g.GEMM_F16_256x256_PAIR, 152)
-    assert g.gemm_f16_select(256, 256, 65536, 152)[:2] == (g.GEMM_F16_256x256_PAIR, 152)
-    assert g.gemm_f16_select(256, 4096, 8192, 152)[:2] == (g.GEMM_F16_256x256_PAIR, 152)
-    assert g.gemm_f16_select(128, 4096, 8192, 152)[0] == g.GEMM_F16_SKINNY  # its split instead
-    # ... but not when a split would be shallower than four ways
-    assert g.gemm_f16_select(1024, 1024, 4096, 152)[:2] == (g.GEMM_F16_128x128, 64)
-    assert g.gemm_f16_select(192, 8192, 8192, 152)[:2] == (g.GEMM_F16_128x128, 128)
+    assert g.gemm_f16_select(128, 8192, 64, 148)[:2] == (g.GEMM_F16_128x128, 64)
+    # more rows: the tile whose waves cost least (a 128 x 256 or pair wave
+    # about 1.15 / 1.1 of a 128 x 128 wave, 1.5 / 1.5 for K <= 512)
+    assert g.gemm_f16_select(192, 8192, 8192, 152)[:2] == (g.GEMM_F16_128x128, 128)   # 1 wave
+    assert g.gemm_f16_select(384, 8192, 8192, 152)[0] == g.GEMM_F16_256x256_PAIR      # 2 vs 1.1
+    assert g.gemm_f16_select(160, 16384, 8192, 152)[0] == g.GEMM_F16_256x256_PAIR
+    assert g.gemm_f16_select(129, 28672, 8192, 152)[0] == g.GEMM_F16_256x256_PAIR
+    assert g.gemm_f16_select(2048, 2048, 512, 152)[:2] == (g.GEMM_F16_128x256, 128)  # short K
+    assert g.gemm_f16_select(4096, 2048, 512, 148)[:2] == (g.GEMM_F16_128x256, 148)
     with pytest.raises(g.GemmError):
         g.gemm_f16_select(1, 1, 1, 0)
 

@@ -252,9 +252,11 @@ def test_f16_nt_split_k_underfilled(M, N, K, grid):
 
 @pytest.mark.parametrize("M,N,K", [(512, 512, 32768), (256, 256, 65536), (256, 4096, 8192)])
 def test_f16_nt_split_k_selector_shapes_sampled(M, N, K):
-    # The selector's choice for these shapes is the split pair kernel.
+    # Few tiles over a long K, through the selector: the skinny kernel with
+    # 128-row tiles of A and the K range split over clusters (the pair
+    # kernel's split stays reachable through gemm_f16_nt_ex, tested above).
     sm = torch.cuda.get_device_properties(0).multi_processor_count
-    assert g.gemm_f16_select(M, N, K, sm)[0] == g.GEMM_F16_256x256_PAIR
+    assert g.gemm_f16_select(M, N, K, sm)[0] == g.GEMM_F16_SKINNY
     A = wl.draw_f16((M, K), seed=83)
     B = wl.draw_f16((N, K), seed=84)
     dA, dB = A.cuda(), B.cuda()

@@ -174,9 +174,11 @@ def test_skinny_under_graph_capture():
     check_f16(C.cpu().numpy(), Cref, S, what="skinny captured")
 
 
-def test_skinny_variant_rejects_too_many_rows():
-    A = torch.zeros((129, 64), dtype=torch.float16, device="cuda")
-    C = torch.zeros((129, 129), dtype=torch.float16, device="cuda")
-    with pytest.raises(g.GemmError) as e:
-        g.gemm_f16_nt_ex(129, 129, 64, A.data_ptr(), A.data_ptr(), C.data_ptr(), 0, g.GEMM_F16_SKINNY)
-    assert e.value.status == g.GEMM_ERR_UNSUPPORTED
+@pytest.mark.parametrize("M,N,K", [(300, 1000, 4104), (300, 77, 72), (129, 2000, 2056)])
+def test_skinny_several_row_tiles_of_a(M, N, K):
+    # More than 128 rows of A: 128-row tiles of A on the grid's third
+    # dimension (the last one partial), with and without the K split.
+    A = wl.draw_f16((M, K), seed=M + 7, dist="normal")
+    B = wl.draw_f16((N, K), seed=N + 7, dist="normal")
+    Cref, S = oracle.gemm_f16_nt(A, B)
+    check_f16(_run(A, B), Cref, S, what=f"skinny {M}x{N}x{K}")
