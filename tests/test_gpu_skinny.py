@@ -136,9 +136,11 @@ def test_skinny_split_sum_is_deterministic():
 
 
 @pytest.mark.parametrize("act", ["none", "relu", "gelu_tanh"])
-@pytest.mark.parametrize("M,N,K", [(9, 300, 136), (40, 1000, 12008)])
+@pytest.mark.parametrize("M,N,K", [(9, 300, 136), (40, 1000, 12008), (300, 1000, 4104)])
 def test_skinny_fused_epilogue(M, N, K, act):
-    # (the first shape runs unsplit, the second with 8 shares summed over the cluster)
+    # (the first shape runs unsplit, the second with 8 shares summed over the
+    # cluster, the third as three 128-row tiles of A with 4 shares each: the
+    # residual rows offset by each tile's first row)
     A = wl.draw_f16((M, K), seed=M, dist="normal")
     B = wl.draw_f16((N, K), seed=N, dist="normal")
     bias = wl.draw_f16((N,), seed=7, dist="normal")
