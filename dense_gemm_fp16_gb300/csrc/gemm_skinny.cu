@@ -297,9 +297,9 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     if (args.splits > 1) {
         // ------------------------------------------- sum of the cluster's shares
         // The ring is idle now (every load was consumed by an MMA that has
-        // completed, or drained above): its first 32 KB hold this CTA's share,
-        // [M][128] fp32.  Every thread of every CTA in the cluster passes
-        // both cluster barriers.
+        // completed, or drained above): its start holds this CTA's share,
+        // [mt][128] fp32 (at most 64 KB).  Every thread of every CTA in the
+        // cluster passes both cluster barriers.
         float *share = reinterpret_cast<float *>(smem);
         if (warp >= 2) {
             const int nl = (warp & 3) * 32 + lane;
@@ -417,7 +417,6 @@ int launch_mn(const SkinnyLaunch &L, std::string &err) {
     skinny_plan(L.M, L.N, L.K, L.ctas, cap, &plan);
     const int num_kb = (L.K + kSkBK - 1) / kSkBK;
     const int splits = plan.splits;
-    const int tiles = plan.groups;
     const SkArgs args{static_cast<__half *>(L.C), L.M, L.N, L.K, num_kb, plan.kb_per_split, splits, plan.rows,
                       L.timeout_ns, make_epi(L.epi, L.N), L.debug_skip_kblock};
     CUtensorMap tmB, tmA;
@@ -432,7 +431,7 @@ int launch_mn(const SkinnyLaunch &L, std::string &err) {
     attr[1].val.clusterDim.x = 1;
     attr[1].val.clusterDim.y = splits;
     attr[1].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(tiles, splits, plan.mtiles);
+    cfg.gridDim = dim3(plan.groups, splits, plan.mtiles);
     cfg.blockDim = dim3(kSkThreads);
     cfg.dynamicSmemBytes = T::kSmemBytes;
     cfg.stream = L.stream;
