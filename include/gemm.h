@@ -173,7 +173,13 @@ enum {
 
 /*
  * Shape-keyed choice of the fp16 configuration: pure host logic, no device
- * call.  sm_count is the number of SMs to plan for (> 0).  Fills *cfg and
+ * call.  sm_count is the number of SMs to plan for (> 0).  The rules, in
+ * order: M = 1 takes GEMM_F16_GEMV; 2 <= M <= 64 takes GEMM_F16_SKINNY, and
+ * so does any M whose 128 x 128 tiles it splits along K into 2 shares of at
+ * least 16 k-blocks or into 4 or more; other M <= 128 take GEMM_F16_128x128;
+ * larger M take the tile (128 x 128, 128 x 256 or the CTA pair) whose waves
+ * over the SMs cost least, a wave of the wider tiles counting 1.15 / 1.1
+ * waves of 128 x 128 tiles (1.5 / 1.5 when K <= 512).  Fills *cfg and
  * returns GEMM_OK, or GEMM_ERR_INVALID_ARG.
  */
 int gemm_f16_select(int M, int N, int K, int sm_count, gemm_f16_config *cfg);

@@ -193,6 +193,32 @@ def test_f16_selector(lib):
         g.gemm_f16_select(1, 1, 1, 0)
 
 
+def test_f16_selector_rule_over_a_shape_grid(lib):
+    # The documented order of rules, checked against the skinny plan the
+    # library exposes and the wave counts restated here.
+    cdiv = lambda a, b: -(-a // b)
+    for sm in (148, 152):
+        for M in (1, 2, 64, 65, 128, 129, 200, 512, 1000, 4096):
+            for N in (64, 1000, 4096, 16384):
+                for K in (64, 512, 520, 4096, 32768):
+                    v, grid, _ = g.gemm_f16_select(M, N, K, sm)
+                    s, _, _, kb = g.gemm_debug_skinny_plan(N, K, sm, M)
+                    split = s >= 4 or (s == 2 and kb >= 16)
+                    if M == 1:
+                        assert v == g.GEMM_F16_GEMV
+                    elif M <= 64 or split:
+                        assert v == g.GEMM_F16_SKINNY and grid == sm
+                    elif M <= 128:
+                        assert v == g.GEMM_F16_128x128
+                    else:
+                        short = cdiv(K, 64) <= 8
+                        w = {g.GEMM_F16_128x128: cdiv(cdiv(M, 128) * cdiv(N, 128), sm),
+                             g.GEMM_F16_128x256: (1.5 if short else 1.15) * cdiv(cdiv(M, 128) * cdiv(N, 256), sm),
+                             g.GEMM_F16_256x256_PAIR: (1.5 if short else 1.1) * cdiv(cdiv(M, 256) * cdiv(N, 256), sm // 2)}
+                        assert v in w and w[v] == min(w.values()), (M, N, K, sm, v, w)
+                        assert 1 <= grid <= sm
+
+
 def test_skinny_plan(lib):
     # Worked cases on 152 SMs: (shares, rows per group, groups, k-blocks a share).
     assert g.gemm_debug_skinny_plan(8192, 8192, 152) == (2, 128, 64, 64)
