@@ -34,8 +34,6 @@ int fail_str(int status, const std::string &msg) {
     return status;
 }
 
-// Largest shared-memory staging of A the GEMV path accepts (2 rows x 40 960 halves).
-
 // Bounded-wait budget inside the fp16 kernel: long enough for any legitimate
 // stall (preemption by another context included), short enough that a broken
 // handshake ends the kernel instead of holding the GPU.
