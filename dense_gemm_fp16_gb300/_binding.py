@@ -240,7 +240,7 @@ def gemm_debug_f16_nt_skip_load(M, N, K, A, B, C, stream, skip_kblock, timeout_n
                                                       skip_kblock, timeout_ns)
 
 
-def gemm_debug_skinny_plan(N, K, ctas, M=1):
+def gemm_debug_skinny_plan(M, N, K, ctas):
     """(shares, rows per group, groups, k-blocks per share) the skinny variant
     plans (host logic only; every slot assumed to hold a cluster of each size)."""
     rows, groups, kb = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)

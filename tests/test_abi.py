@@ -202,7 +202,7 @@ def test_f16_selector_rule_over_a_shape_grid(lib):
             for N in (64, 1000, 4096, 16384):
                 for K in (64, 512, 520, 4096, 32768):
                     v, grid, _ = g.gemm_f16_select(M, N, K, sm)
-                    s, _, _, kb = g.gemm_debug_skinny_plan(N, K, sm, M)
+                    s, _, _, kb = g.gemm_debug_skinny_plan(M, N, K, sm)
                     split = s >= 4 or (s == 2 and kb >= 16)
                     if M == 1:
                         assert v == g.GEMM_F16_GEMV
@@ -221,17 +221,22 @@ def test_f16_selector_rule_over_a_shape_grid(lib):
 
 def test_skinny_plan(lib):
     # Worked cases on 152 SMs: (shares, rows per group, groups, k-blocks a share).
-    assert g.gemm_debug_skinny_plan(8192, 8192, 152) == (2, 128, 64, 64)
-    assert g.gemm_debug_skinny_plan(16384, 8192, 152) == (1, 128, 128, 128)  # no room to split
-    assert g.gemm_debug_skinny_plan(4096, 4096, 152) == (4, 128, 32, 16)
-    assert g.gemm_debug_skinny_plan(1000, 12008, 152) == (8, 128, 8, 24)     # 188 k-blocks
-    assert g.gemm_debug_skinny_plan(4000, 2056, 152) == (4, 128, 32, 9)      # 33 k-blocks: ragged
-    assert g.gemm_debug_skinny_plan(19456, 1024, 152) == (1, 128, 152, 16)   # exactly one wave
-    assert g.gemm_debug_skinny_plan(28672, 8192, 152) == (1, 96, 299, 128)   # two even waves
-    assert g.gemm_debug_skinny_plan(77, 72, 152) == (1, 128, 1, 2)           # too shallow to split
-    assert g.gemm_debug_skinny_plan(77, 0, 152) == (1, 128, 1, 1)            # K = 0
+    assert g.gemm_debug_skinny_plan(1, 8192, 8192, 152) == (2, 128, 64, 64)
+    assert g.gemm_debug_skinny_plan(1, 16384, 8192, 152) == (1, 128, 128, 128)  # no room to split
+    assert g.gemm_debug_skinny_plan(1, 4096, 4096, 152) == (4, 128, 32, 16)
+    assert g.gemm_debug_skinny_plan(1, 1000, 12008, 152) == (8, 128, 8, 24)     # 188 k-blocks
+    assert g.gemm_debug_skinny_plan(1, 4000, 2056, 152) == (4, 128, 32, 9)      # 33 k-blocks: ragged
+    assert g.gemm_debug_skinny_plan(1, 19456, 1024, 152) == (1, 128, 152, 16)   # exactly one wave
+    assert g.gemm_debug_skinny_plan(1, 28672, 8192, 152) == (1, 96, 299, 128)   # two even waves
+    assert g.gemm_debug_skinny_plan(1, 77, 72, 152) == (1, 128, 1, 2)           # too shallow to split
+    assert g.gemm_debug_skinny_plan(1, 77, 0, 152) == (1, 128, 1, 1)            # K = 0
+    # more than 128 rows of A: 128-row tiles of A count towards the SMs too
+    assert g.gemm_debug_skinny_plan(160, 2048, 8192, 152) == (4, 128, 16, 32)   # 2 x 16 tiles
+    assert g.gemm_debug_skinny_plan(512, 512, 32768, 152) == (8, 128, 4, 64)    # 4 x 4 tiles
+    assert g.gemm_debug_skinny_plan(2048, 2048, 8192, 152) == (1, 128, 16, 128)  # 256 tiles
+    assert g.gemm_debug_skinny_plan(300, 20000, 64, 152)[1] == 128             # no wave evening
     with pytest.raises(ValueError):
-        g.gemm_debug_skinny_plan(0, 64, 152)
+        g.gemm_debug_skinny_plan(1, 0, 64, 152)
 
 
 def test_skinny_plan_properties(lib):
@@ -243,7 +248,7 @@ def test_skinny_plan_properties(lib):
     for N in (1, 127, 128, 129, 1000, 4096, 8192, 16384, 19456, 19457, 28672):
         for K in (0, 8, 64, 512, 520, 4096, 12008, 65536):
             for ctas in (1, 19, 152, 304):
-                s, rows, groups, kb = g.gemm_debug_skinny_plan(N, K, ctas)
+                s, rows, groups, kb = g.gemm_debug_skinny_plan(1, N, K, ctas)
                 tiles, nkb = -(-N // 128), -(-K // 64)
                 assert s in (1, 2, 4, 8)
                 if s > 1:

@@ -87,7 +87,7 @@ def test_skinny_two_even_waves():
     M, N, K = 3, sm * 128 + 500, 256
     A = wl.draw_f16((M, K), seed=81, dist="normal")
     B = wl.draw_f16((N, K), seed=82, dist="normal")
-    assert g.gemm_debug_skinny_plan(N, K, sm)[1] < 128
+    assert g.gemm_debug_skinny_plan(M, N, K, sm)[1] < 128
     Cref, S = oracle.gemm_f16_nt(A, B)
     check_f16(_run(A, B), Cref, S, what=f"skinny two waves {M}x{N}x{K}")
 
