@@ -238,6 +238,64 @@ def test_activations_against_library_and_identities():
     assert oracle.activation(0.0, "silu") == 0.0 and oracle.activation(0.0, "gelu_tanh") == 0.0
 
 
+def _library_activation(xs, act):
+    """PyTorch's own float64 activations, an implementation independent of the oracle's C."""
+    import torch
+
+    x = torch.tensor(xs, dtype=torch.float64)
+    f = {"silu": torch.nn.functional.silu,
+         "gelu_tanh": lambda t: torch.nn.functional.gelu(t, approximate="tanh")}[act]
+    return f(x).numpy()
+
+
+# Pointwise agreement with the library: the two differ only in the rounding
+# order of a handful of float64 operations, while a wrong digit in a constant
+# (0.0447 for 0.044715 moves GELU by up to 4.7e-4) or a wrong sign is many
+# orders of magnitude above this bound.
+ACT_PIN_REL = 1e-13
+ACT_PIN_ABS = 1e-15
+ACT_PIN_XS = np.linspace(-8, 8, 1601)
+
+
+def _activation_pin_error(fn, act):
+    ref = _library_activation(ACT_PIN_XS, act)
+    got = np.array([fn(x) for x in ACT_PIN_XS])
+    return np.max(np.abs(got - ref) / (ACT_PIN_REL * np.abs(ref) + ACT_PIN_ABS))
+
+
+@pytest.mark.parametrize("act", ["silu", "gelu_tanh"])
+def test_activation_pinned_to_library_values(act):
+    # tanh-GELU 0.5 v (1 + tanh(sqrt(2/pi) (v + 0.044715 v^3))) and SiLU v σ(v)
+    # point by point against torch.nn.functional (gelu(approximate="tanh"),
+    # silu) in float64, e.g. GELU_tanh(1) = 0.8411919906082768.
+    assert _activation_pin_error(lambda x: oracle.activation(x, act), act) <= 1.0
+    assert oracle.activation(1.0, "gelu_tanh") == pytest.approx(0.8411919906082768, rel=1e-15)
+
+
+@pytest.mark.parametrize("old,new", [
+    ("0.044715 * v * v * v", "0.0447 * v * v * v"),          # a dropped digit
+    ("sqrt(2.0 / M_PI)", "sqrt(2.0 / 3.1416)"),              # a rounded pi
+    ("0.5 * v * (1.0 + tanh", "0.5 * v * (1.0 - tanh"),      # a wrong sign
+])
+def test_activation_pin_rejects_a_planted_mistake(tmp_path, old, new):
+    # The GELU pin above must fail for a plausible typo: build a scratch copy
+    # of the oracle with the mistake planted and evaluate it through the pin.
+    import ctypes
+    import subprocess
+
+    src = open(oracle._SRC).read()
+    assert src.count(old) == 1, f"mutation anchor {old!r} not found once"
+    path = tmp_path / "gemm_oracle_mutant.c"
+    path.write_text(src.replace(old, new))
+    lib_path = tmp_path / "libmutant.so"
+    subprocess.check_call(["gcc", *oracle.GCC_FLAGS, "-o", str(lib_path), str(path), "-lm"])
+    lib = ctypes.CDLL(str(lib_path))
+    lib.oracle_activation.restype = ctypes.c_double
+    lib.oracle_activation.argtypes = [ctypes.c_double, ctypes.c_int]
+    code = oracle.ACTIVATIONS["gelu_tanh"]
+    assert _activation_pin_error(lambda x: lib.oracle_activation(x, code), "gelu_tanh") > 1e3
+
+
 def test_epilogue_exact_through_identity():
     # B = I: alpha·A + bias + beta·R exactly for small integers; ReLU clips.
     rng = np.random.default_rng(31)
