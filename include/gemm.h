@@ -41,6 +41,8 @@
 #ifndef DENSE_GEMM_FP16_GB300_GEMM_H
 #define DENSE_GEMM_FP16_GB300_GEMM_H
 
+#include <stddef.h> /* size_t */
+
 #ifdef __cplusplus
 extern "C" {
 #endif

@@ -1,9 +1,11 @@
 """Tolerance checks between a GPU result and the float64 oracle.
 
 fp16 NT:  |C_gpu - C_ref| <= 4e-3 * S + 1e-6 per element,
-fp32 SGEMM: |C_gpu - C_ref| <= 1e-5 * S (+ 2^-22 |beta C0| for the rounding
-of the beta term, which S does not cover),
-where S = |alpha| * sum_k |A * B| comes from the oracle.  Every GPU output
+fp32 SGEMM: |C_gpu - C_ref| <= 1e-5 * S,
+where S = |alpha| * sum_k |A * B| comes from the oracle.  (The SGEMM bound
+has no term for beta * C0: its rounding, at most 2^-24 |result|, is far
+below 1e-5 * S wherever the product is not empty, and the K = 0 case is
+checked for exact equality with a beta whose product is exact.)  Every GPU output
 must also be finite.
 """
 import numpy as np
@@ -26,13 +28,11 @@ def check_f16(c_gpu, c_ref, s, what=""):
     return float((err / bound).max()) if err.size else 0.0
 
 
-def check_sgemm(c_gpu, c_ref, s, beta_c0=None, what=""):
+def check_sgemm(c_gpu, c_ref, s, what=""):
     c = np.asarray(c_gpu, dtype=np.float64)
     assert np.all(np.isfinite(c)), f"{what}: non-finite output"
     err = np.abs(c - c_ref)
     bound = SGEMM_REL * s
-    if beta_c0 is not None:
-        bound = bound + 2.0 ** -22 * np.abs(beta_c0)
     bad = err > bound
     if bad.any():
         idx = np.argwhere(bad)[:5]
