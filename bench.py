@@ -51,6 +51,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -58,6 +59,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "TFLOP/s (2MNK/t) fp16 NT GEMM 5376x5376x2048 on 1 GB300; % of dense FP16 peak"
 ROTATE = 4
+# Operand sets of the small SGEMM configs rotate until they exceed the 126 MB L2.
+L2_ROTATE_BYTES = 160 * 1000 * 1000
 FALLBACK_TENSOR_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
 # The sources of the fp16 NT kernels; the profiled traffic holds only while
@@ -166,7 +169,7 @@ class ClockSampler:
         dev = getattr(props, "pci_device_id", 0)
         self.bus_id = None if bus is None else f"{dom:08X}:{bus:02X}:{dev:02X}.0"
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        self.path = os.path.join(tempfile.gettempdir(), f"gemm_bench_clocks_{os.getpid()}.csv")
 
     def __enter__(self):
         try:
@@ -265,6 +268,106 @@ def cpu_baseline(w, A, B, budget_s=10.0):
                       f"float64 triple loop, {t:.1f} s"}
 
 
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), for the oracle lines."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.startswith("Model name:"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.lower().startswith(("model name", "cpu model")):
+                    return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def oracle_rows(w, A, B, C0, rows):
+    """Seconds the oracle takes for rows 0..rows-1 of workload w's product."""
+    import oracle
+
+    t0 = time.perf_counter()
+    if w.form == "f16_nt":
+        oracle.gemm_f16_nt(A[:rows], B)
+    else:
+        oracle.sgemm(A[:rows], B, w.alpha, w.beta, None if C0 is None else C0[:rows])
+    return time.perf_counter() - t0
+
+
+def oracle_sample(w, A, B, C0, budget_s):
+    """The oracle on a row sample of workload w sized to about budget_s seconds
+    (all rows when they fit), with its rate and the whole product's estimate."""
+    import oracle
+
+    rows = min(w.M, 4)
+    t = oracle_rows(w, A, B, C0, rows)
+    while t < 0.5 * budget_s and rows < w.M:   # fixed costs make a small probe overestimate
+        rows = int(min(w.M, max(rows + 1, rows * budget_s / max(t, 1e-6))))
+        t = oracle_rows(w, A, B, C0, rows)
+    flop = 2.0 * rows * w.N * w.K
+    return {"value": flop / t / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle", "seconds": t, "full_product_seconds_est": t * w.M / rows,
+            "sample": f"rows 0..{rows - 1} of {w.M} ({rows}x{w.N} outputs, K={w.K}), float64 "
+                      f"triple loop" + ("" if rows < w.M else " (the whole product)")}
+
+
+def oracle_single_thread(w, budget_s):
+    """The oracle on one host thread (OMP_NUM_THREADS=1 in a child process that
+    imports only numpy and the oracle), on a row sample of workload w."""
+    import tempfile as tf
+
+    import numpy as np
+    from dense_gemm_fp16_gb300 import workloads as wl
+
+    A, B, C0 = wl.make_inputs(w)
+    with tf.TemporaryDirectory() as d:
+        path = os.path.join(d, "inputs.npz")
+        np.savez(path, A=A.numpy(), B=B.numpy())
+        env = dict(os.environ, OMP_NUM_THREADS="1")
+        res = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-timing", path,
+                              w.form, str(w.alpha), str(w.beta), str(budget_s)],
+                             capture_output=True, text=True, env=env, timeout=600)
+    if res.returncode != 0:
+        return {"error": res.stderr.strip().splitlines()[-1:] or ["failed"]}
+    return json.loads(res.stdout.strip().splitlines()[-1])
+
+
+def oracle_timing_child(path, form, alpha, beta, budget_s):
+    """Child side of oracle_single_thread: time a row sample, print one JSON line."""
+    import numpy as np
+
+    import oracle
+
+    d = np.load(path)
+    A, B = d["A"], d["B"]
+    M, N, K = A.shape[0], B.shape[0] if form == "f16_nt" else B.shape[1], A.shape[1]
+
+    def run(rows):
+        t0 = time.perf_counter()
+        if form == "f16_nt":
+            oracle.gemm_f16_nt(A[:rows], B)
+        else:
+            oracle.sgemm(A[:rows], B, alpha, beta, None)
+        return time.perf_counter() - t0
+
+    rows = min(M, 2)
+    t = run(rows)
+    while t < 0.5 * budget_s and rows < M:
+        rows = int(min(M, max(rows + 1, rows * budget_s / max(t, 1e-6))))
+        t = run(rows)
+    print(json.dumps({"value": 2.0 * rows * N * K / t / 1e12, "unit": "TFLOP/s",
+                      "cores": oracle.num_threads(), "kind": "oracle", "seconds": t,
+                      "full_product_seconds_est": t * M / rows,
+                      "sample": f"rows 0..{rows - 1} of {M} ({rows}x{N} outputs, K={K}), float64 "
+                                f"triple loop on one thread"}))
+    return 0
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -314,6 +417,76 @@ def region_time(fn, stream, n):
     b.record(stream)
     stream.synchronize()
     return a.elapsed_time(b)
+
+
+def calls_for(fn, stream, target_ms):
+    """Calls per timed region: enough back-to-back calls for about target_ms."""
+    one = region_time(fn, stream, 3) / 3
+    return max(5, min(2000, int(target_ms / max(one, 1e-4))))
+
+
+def timed_trials(fn, stream, n, min_s=0.5, max_trials=200):
+    """Median per-call time (ms) over regions of n back-to-back calls, repeated
+    for at least min_s so that the clock sampler sees the work; (ms, regions)."""
+    ts = []
+    t0 = time.perf_counter()
+    while len(ts) < 3 or (time.perf_counter() - t0 < min_s and len(ts) < max_trials):
+        ts.append(region_time(fn, stream, n) / n)
+    return statistics.median(ts), len(ts)
+
+
+def f16_kernel_names(g):
+    return {g.GEMM_F16_128x256: "gemm_f16_nt_tc_kernel<256,4> (1-CTA 128x256)",
+            g.GEMM_F16_128x128: "gemm_f16_nt_tc_kernel<128,6> (1-CTA 128x128)",
+            g.GEMM_F16_256x256_PAIR: "gemm_f16_nt_pair_kernel<6> (CTA pair 256x256)",
+            g.GEMM_F16_GEMV: "gemv_rows_kernel (CUDA cores)",
+            g.GEMM_F16_SKINNY: "gemm_skinny_kernel (swapped tcgen05 product, K split over a cluster)"}
+
+
+def run_case(args):
+    """One workload, `--calls` back-to-back launches of our kernel (or, with
+    --cublas, of the cuBLAS reference), nothing timed: the command that the
+    committed ncu summaries profile, with -s/-c picking a launch after the
+    first ones."""
+    import torch
+
+    import dense_gemm_fp16_gb300 as g
+    from dense_gemm_fp16_gb300 import build, workloads as wl
+
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    build.build()
+    g.load_library()
+    w = wl.WORKLOADS[args.case]
+    A, B, C0 = wl.make_inputs(w)
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+    dA, dB = A.cuda(), B.cuda()
+    if w.form == "f16_nt":
+        C = torch.empty((w.M, w.N), dtype=torch.float16, device="cuda")
+        if args.cublas:
+            torch.backends.cuda.matmul.allow_fp16_reduced_precision_reduction = False
+            fn = lambda: torch.matmul(dA, dB.t(), out=C)
+        else:
+            fn = lambda: g.gemm_f16_nt_ex(w.M, w.N, w.K, dA.data_ptr(), dB.data_ptr(), C.data_ptr(),
+                                          sh, args.variant)
+    else:
+        C = (C0 if C0 is not None else torch.zeros(w.M, w.N)).cuda()
+        out = torch.empty_like(C)
+        if args.cublas:
+            torch.backends.cuda.matmul.allow_tf32 = False
+            fn = ((lambda: torch.mm(dA, dB, out=out)) if w.beta == 0.0 else
+                  (lambda: torch.addmm(C, dA, dB, beta=w.beta, alpha=w.alpha, out=out)))
+        else:
+            fn = lambda: g.sgemm_ex(w.M, w.N, w.K, w.alpha, dA.data_ptr(), dB.data_ptr(), w.beta,
+                                    C.data_ptr(), sh, args.variant)
+    for _ in range(args.calls):
+        fn()
+    torch.cuda.synchronize()
+    if not args.cublas:
+        g.gemm_check_device_status(sh)
+    print(json.dumps({"case": w.name, "calls": args.calls, "impl": "cublas" if args.cublas else "ours",
+                      "variant": args.variant}), flush=True)
+    return 0
 
 
 def run_ours(args):
@@ -377,10 +550,8 @@ def run_ours(args):
 
     sm_count = torch.cuda.get_device_properties(local).multi_processor_count
     variant, grid, _ = g.gemm_f16_select(M, N, K, sm_count)
-    kernel_name = {g.GEMM_F16_128x256: "gemm_f16_nt_tc_kernel<256,4> (1-CTA 128x256)",
-                   g.GEMM_F16_128x128: "gemm_f16_nt_tc_kernel<128,6> (1-CTA 128x128)",
-                   g.GEMM_F16_256x256_PAIR: "gemm_f16_nt_pair_kernel<6> (CTA pair 256x256)"
-                   }[variant] + f", grid {grid}"
+    F16_KERNEL_NAMES = f16_kernel_names(g)
+    kernel_name = F16_KERNEL_NAMES[variant] + f", grid {grid}"
     # The timed region follows a soak of the same launches, so it runs at the
     # power-capped clocks of a long run: the sustained peak (cuBLAS bf16 back
     # to back for seconds) is the matching denominator; the burst fraction is
@@ -498,34 +669,136 @@ def run_ours(args):
                       "what": "torch.matmul(A, B.t()) fp16, fp32 accumulation, timed like value "
                               "(after the same soak); burst_value: right after warm-up; reference only"}
 
-    # ---- fp32 SGEMM 4096^3 (alpha 1, beta 0.5) against the FP32 FFMA peak
-    # Its peak and the GEMV's (the HBM copy rate) are unthrottled figures, and
-    # the soaks above leave the power limiter holding the clocks down for a
-    # while (GEMV measured 48 us cool, 56-68 us right after them): both are
-    # timed after an idle pause.
+    # ---- every config of the workload list, each in one row: our time and
+    # TFLOP/s against its peak at the sampled clock, the same-run cuBLAS line
+    # and the oracle's time on the host cores.  The FP32 peak and the HBM copy
+    # rate are unthrottled figures and the soaks above leave the power limiter
+    # holding the clocks down for a while (GEMV measured 48 us cool, 56-68 us
+    # right after them), so the SGEMM and GEMV rows start after an idle pause;
+    # every row is timed over repeated regions for at least half a second with
+    # the clocks sampled meanwhile.
     idle_s = 2.0
+    line["configs"] = {}
     if not args.skip_sgemm:
-        time.sleep(idle_s)
-        sw = wl.WORKLOADS["sgemm_4096"]
-        sA, sB, sC0 = wl.make_inputs(sw)
+        fp32_nominal = sm_count * 128 * 2 * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6 / 1e12
+        max_mhz = float(peaks.get("sm_max_mhz", 2070.0))
+        hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+        torch.backends.cuda.matmul.allow_tf32 = False
+        for name in ("sgemm_256", "sgemm_1024", "sgemm_4096"):
+            time.sleep(idle_s)
+            sw = wl.WORKLOADS[name]
+            sA, sB, sC0 = wl.make_inputs(sw)
+            set_bytes = 4 * (sw.M * sw.K + sw.K * sw.N + 2 * sw.M * sw.N)
+            nsets = max(1, -(-L2_ROTATE_BYTES // set_bytes))
+            with torch.cuda.stream(stream):
+                ssets = [(sA.cuda(), sB.cuda(),
+                          (sC0 if sC0 is not None else torch.zeros(sw.M, sw.N)).cuda(),
+                          torch.empty((sw.M, sw.N), dtype=torch.float32, device="cuda"))
+                         for _ in range(nsets)]
+            stream.synchronize()
+
+            def sg(i, sw=sw, ssets=ssets):
+                a, b, c, _ = ssets[i % len(ssets)]
+                g.sgemm(sw.M, sw.N, sw.K, sw.alpha, a.data_ptr(), b.data_ptr(), sw.beta,
+                        c.data_ptr(), sh)
+
+            def sg_cublas(i, sw=sw, ssets=ssets):
+                a, b, c, out = ssets[i % len(ssets)]
+                if sw.beta == 0.0:
+                    torch.mm(a, b, out=out)
+                else:
+                    torch.addmm(c, a, b, beta=sw.beta, alpha=sw.alpha, out=out)
+
+            n = calls_for(sg, stream, target_ms=20.0)
+            with ClockSampler(local) as ck:
+                t_sg, trials = timed_trials(sg, stream, n)
+            g.gemm_check_device_status(sh)
+            with torch.cuda.stream(stream):
+                region_time(sg_cublas, stream, 3)
+                t_cb, _ = timed_trials(sg_cublas, stream, n)
+            clk = ck.summary()
+            sval = sw.flop / (t_sg * 1e-3) / 1e12
+            at_clock = (fp32_nominal * clk["sm_mhz"] / max_mhz) if clk.get("sm_mhz") else None
+            variant, splits = g.gemm_sgemm_select(sw.M, sw.N, sw.K, sm_count)
+            line["configs"][name] = {
+                "form": "sgemm", "M": sw.M, "N": sw.N, "K": sw.K, "alpha": sw.alpha,
+                "beta": sw.beta, "us_per_call": 1e3 * t_sg, "value": sval, "unit": "TFLOP/s",
+                "kernel": f"sgemm_pipe_kernel ({'128x128' if variant == g.GEMM_SGEMM_128x128 else '64x64'}"
+                          f" tile, {splits} K share{'s' if splits > 1 else ''})",
+                "timing": f"median of {trials} regions of {n} calls over {nsets} rotating operand "
+                          f"set{'s' if nsets > 1 else ''} ({nsets * set_bytes / 1e6:.0f} MB), after "
+                          f"a {idle_s:.0f} s idle pause",
+                "roofline": {"bound": "alu", "achieved": sval, "peak": fp32_nominal,
+                             "unit": "TFLOP/s", "frac": sval / fp32_nominal,
+                             "peak_source": f"{sm_count} SMs x 128 FFMA/clk x 2 FLOP x {max_mhz:.0f} MHz",
+                             "peak_at_sampled_clock": at_clock,
+                             "frac_at_sampled_clock": sval / at_clock if at_clock else None},
+                "clocks": clk,
+                "cublas": {"value": sw.flop / (t_cb * 1e-3) / 1e12, "unit": "TFLOP/s",
+                           "us_per_call": 1e3 * t_cb,
+                           "what": ("torch.mm" if sw.beta == 0.0 else "torch.addmm") +
+                                   " fp32 with TF32 off (cuBLAS SGEMM), timed the same way; "
+                                   "reference only"},
+            }
+            del ssets
+
+        # ---- the tail-shape fp16 config (M and K off the tile grid), timed like
+        # the headline: after a soak, at the power-capped clocks of a long run
+        tw = wl.WORKLOADS["f16_nt_5000x5376x2040"]
+        tA, tB, _ = wl.make_inputs(tw)
         with torch.cuda.stream(stream):
-            dsa, dsb, dsc = sA.cuda(), sB.cuda(), sC0.cuda()
+            tsets = [(tA.cuda(), tB.cuda(),
+                      torch.empty((tw.M, tw.N), dtype=torch.float16, device="cuda"))
+                     for _ in range(ROTATE)]
         stream.synchronize()
 
-        def sg(_):
-            g.sgemm(sw.M, sw.N, sw.K, sw.alpha, dsa.data_ptr(), dsb.data_ptr(), sw.beta,
-                    dsc.data_ptr(), sh)
-        region_time(sg, stream, 3)
-        n_sg = max(5, min(args.steps, 20))
-        st = region_time(sg, stream, n_sg) / n_sg
-        fp32_peak = sm_count * 128 * 2 * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6 / 1e12
-        sval = sw.flop / (st * 1e-3) / 1e12
-        line["sgemm"] = {"workload": sw.name, "value": sval, "unit": "TFLOP/s",
-                         "timed_after_idle_s": idle_s,
-                         "roofline": {"bound": "alu", "achieved": sval, "peak": fp32_peak,
-                                      "unit": "TFLOP/s", "frac": sval / fp32_peak,
-                                      "peak_source": f"{sm_count} SMs x 128 FFMA/clk x 2 FLOP x "
-                                                     f"{peaks.get('sm_max_mhz', 2070.0)} MHz"}}
+        def tstep(i):
+            a, b, c = tsets[i % ROTATE]
+            g.gemm_f16_nt(tw.M, tw.N, tw.K, a.data_ptr(), b.data_ptr(), c.data_ptr(), sh)
+
+        def tstep_cublas(i):
+            a, b, c = tsets[i % ROTATE]
+            torch.matmul(a, b.t(), out=c)
+
+        with torch.cuda.stream(stream):
+            region_time(tstep, stream, args.warmup)
+            region_time(tstep_cublas, stream, args.warmup)
+            with ClockSampler(local) as ck:
+                region_time(tstep, stream, soak)
+                t_t = region_time(tstep, stream, args.steps) / args.steps
+            region_time(tstep_cublas, stream, soak)
+            t_tc = region_time(tstep_cublas, stream, args.steps) / args.steps
+        g.gemm_check_device_status(sh)
+        tval = tw.flop / (t_t * 1e-3) / 1e12
+        tv, tg, _ = g.gemm_f16_select(tw.M, tw.N, tw.K, sm_count)
+        line["configs"][tw.name] = {
+            "form": "f16_nt", "M": tw.M, "N": tw.N, "K": tw.K, "us_per_call": 1e3 * t_t,
+            "value": tval, "unit": "TFLOP/s",
+            "kernel": f"{F16_KERNEL_NAMES[tv]}, grid {tg}",
+            "timing": f"{args.steps} back-to-back calls after a {args.soak_s} s soak, {ROTATE} "
+                      f"rotating operand sets (inputs larger than L2)",
+            "roofline": {"bound": "tensor", "achieved": tval, "peak": peak, "unit": "TFLOP/s",
+                         "frac": tval / peak, "peak_source": peak_note,
+                         "frac_of_burst_peak": tval / burst},
+            "per_flop_vs_headline": (t_t / tw.flop) / (avg_launch_ms / w.flop),
+            "clocks": ck.summary(),
+            "cublas": {"value": tw.flop / (t_tc * 1e-3) / 1e12, "unit": "TFLOP/s",
+                       "us_per_call": 1e3 * t_tc,
+                       "what": "torch.matmul(A, B.t()) fp16, fp32 accumulation, after the same "
+                               "soak; reference only"},
+        }
+        del tsets
+        # the headline config's own row (its numbers are the line's headline)
+        line["configs"][w.name] = {
+            "form": "f16_nt", "M": M, "N": N, "K": K, "us_per_call": 1e3 * avg_launch_ms,
+            "value": achieved, "unit": "TFLOP/s", "kernel": kernel_name,
+            "timing": "the headline region (see roofline)",
+            "roofline": {k: line["roofline"][k] for k in ("bound", "achieved", "peak", "unit",
+                                                          "frac", "frac_of_burst_peak")},
+            "clocks": line["clocks"],
+            "cublas": {"value": line["cublas"]["value"], "unit": "TFLOP/s",
+                       "us_per_call": 1e3 * cb, "what": line["cublas"]["what"]},
+        }
 
     # ---- fp16 matrix-vector (M = 1) against the HBM copy bandwidth
     if not args.skip_sgemm:
@@ -541,16 +814,19 @@ def run_ours(args):
             g.gemm_f16_nt(gw.M, gw.N, gw.K, dga.data_ptr(), dgb.data_ptr(), dgc.data_ptr(), sh)
         region_time(gv, stream, 5)
         n_gv = 50
-        t_gv = region_time(gv, stream, n_gv) / n_gv
+        with ClockSampler(local) as ck:
+            t_gv, trials = timed_trials(gv, stream, n_gv)
         gbytes = 2 * (gw.N * gw.K + gw.M * gw.K + gw.M * gw.N)
-        hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
         achieved_gbs = gbytes / (t_gv * 1e-3) / 1e9
         line["gemv"] = {"workload": gw.name, "value": gw.flop / (t_gv * 1e-3) / 1e12,
                         "unit": "TFLOP/s", "us_per_call": 1e3 * t_gv, "timed_after_idle_s": idle_s,
+                        "timing": f"median of {trials} regions of {n_gv} calls (B, 268 MB, is "
+                                  f"larger than L2)",
                         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm,
                                      "unit": "GB/s", "frac": achieved_gbs / hbm,
                                      "bytes_per_call": gbytes,
-                                     "peak_source": f"{peak_kind} HBM copy bandwidth"}}
+                                     "peak_source": f"{peak_kind} HBM copy bandwidth"},
+                        "clocks": ck.summary()}
         g.gemm_check_device_status(sh)
 
         # ---- 16 rows of A against the same B: the skinny tensor-core kernel
@@ -567,15 +843,18 @@ def run_ours(args):
         def sk(_):
             g.gemm_f16_nt(kw.M, kw.N, kw.K, dka.data_ptr(), dgb.data_ptr(), dkc.data_ptr(), sh)
         region_time(sk, stream, 5)
-        t_sk = region_time(sk, stream, n_gv) / n_gv
+        with ClockSampler(local) as ck:
+            t_sk, trials = timed_trials(sk, stream, n_gv)
         kbytes = 2 * (kw.N * kw.K + kw.M * kw.K + kw.M * kw.N)
         k_gbs = kbytes / (t_sk * 1e-3) / 1e9
         line["skinny"] = {"workload": kw.name, "value": kw.flop / (t_sk * 1e-3) / 1e12,
                           "unit": "TFLOP/s", "us_per_call": 1e3 * t_sk, "variant": k_variant,
+                          "timing": f"median of {trials} regions of {n_gv} calls",
                           "roofline": {"bound": "hbm", "achieved": k_gbs, "peak": hbm,
                                        "unit": "GB/s", "frac": k_gbs / hbm,
                                        "bytes_per_call": kbytes,
-                                       "peak_source": f"{peak_kind} HBM copy bandwidth"}}
+                                       "peak_source": f"{peak_kind} HBM copy bandwidth"},
+                          "clocks": ck.summary()}
         g.gemm_check_device_status(sh)
         del dka, dkc
 
@@ -686,7 +965,21 @@ def run_ours(args):
                          "frac_of_sustained_peak": nval / (6.0 * peak)}}
 
     if rank == 0 and not args.skip_cpu_baseline:
+        model = cpu_model()
         line["cpu_baseline"] = cpu_baseline(w, A, B, budget_s=args.cpu_budget)
+        line["cpu_baseline"]["cpu_model"] = model
+        # the oracle on every other config (a bounded row sample each), and on
+        # one thread for the 1024-cube SGEMM, for scale
+        for name, row in line["configs"].items():
+            if name == w.name:
+                row["cpu_oracle"] = line["cpu_baseline"]
+                continue
+            ow = wl.WORKLOADS[name]
+            oA, oB, oC0 = wl.make_inputs(ow)
+            row["cpu_oracle"] = dict(oracle_sample(ow, oA, oB, oC0, budget_s=2.0), cpu_model=model)
+        if "sgemm_1024" in line["configs"]:
+            line["configs"]["sgemm_1024"]["cpu_oracle_one_thread"] = dict(
+                oracle_single_thread(wl.WORKLOADS["sgemm_1024"], budget_s=4.0), cpu_model=model)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -710,8 +1003,21 @@ def main():
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--skip-extras", "--skip-sgemm", dest="skip_sgemm", action="store_true",
                     help="only the headline line: no sgemm, gemv, fused_epilogue, mxfp8 or nvfp4 objects")
+    ap.add_argument("--case", default=None,
+                    help="profiling mode: launch one named workload --calls times and exit")
+    ap.add_argument("--calls", type=int, default=3)
+    ap.add_argument("--variant", type=int, default=0,
+                    help="profiling mode: the kernel variant (gemm.h GEMM_F16_* / GEMM_SGEMM_*; 0 = auto)")
+    ap.add_argument("--cublas", action="store_true", help="profiling mode: the cuBLAS reference instead")
+    ap.add_argument("--oracle-timing", nargs=5, metavar=("NPZ", "FORM", "ALPHA", "BETA", "BUDGET_S"),
+                    help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.oracle_timing:
+        path, form, alpha, beta, budget = args.oracle_timing
+        return oracle_timing_child(path, form, float(alpha), float(beta), float(budget))
     args.warmup = max(args.warmup, 3)   # timing rule: at least 3 warm-up steps
+    if args.case:
+        return run_case(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -121,6 +121,15 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gemm_debug_skinny_plan.argtypes = [i, i, i, i, ctypes.POINTER(i), ctypes.POINTER(i),
                                                ctypes.POINTER(i)]
         lib.gemm_debug_skinny_plan.restype = i
+        lib.gemm_debug_last_pair_launch.argtypes = [ctypes.POINTER(i)] * 4
+        lib.gemm_debug_last_pair_launch.restype = i
+        lib.gemm_debug_blockscaled_skip_load.argtypes = [i, i, i, i, vp, vp, vp, vp, vp, vp,
+                                                         ctypes.POINTER(_MxConfig), i,
+                                                         ctypes.c_ulonglong]
+        lib.gemm_debug_blockscaled_skip_load.restype = i
+        lib.gemm_debug_f16_nt_stream_k_skip_publish.argtypes = [i, i, i, vp, vp, vp, vp,
+                                                                ctypes.c_ulonglong]
+        lib.gemm_debug_f16_nt_stream_k_skip_publish.restype = i
         _lib = lib
         return lib
 
@@ -238,6 +247,31 @@ def gemm_debug_f16_nt_skip_load(M, N, K, A, B, C, stream, skip_kblock, timeout_n
     """Raw status of the fault-injection hook of include/gemm_testing.h."""
     return load_library().gemm_debug_f16_nt_skip_load(M, N, K, A, B, C, stream or None,
                                                       skip_kblock, timeout_ns)
+
+
+def gemm_debug_blockscaled_skip_load(fmt, M, N, K, A, SFA, B, SFB, C, stream, variant, skip_kblock,
+                                     timeout_ns) -> int:
+    """Raw status of the block-scaled fault-injection hook (fmt 0 MXFP8, 1 NVFP4)."""
+    cfg = _MxConfig(variant, 0)
+    return load_library().gemm_debug_blockscaled_skip_load(fmt, M, N, K, A, SFA, B, SFB, C,
+                                                           stream or None, ctypes.byref(cfg),
+                                                           skip_kblock, timeout_ns)
+
+
+def gemm_debug_f16_nt_stream_k_skip_publish(M, N, K, A, B, C, stream, timeout_ns) -> int:
+    """Raw status of the stream-K hook whose partials are never flagged ready."""
+    return load_library().gemm_debug_f16_nt_stream_k_skip_publish(M, N, K, A, B, C, stream or None,
+                                                                  timeout_ns)
+
+
+def gemm_debug_last_pair_launch():
+    """(pairs, whole tiles, shared k-block units, scratch kind) of the last
+    CTA-pair launch on this thread (scratch kind: 0 none, 1 allocated
+    workspace, 2 the allocation-free entry point's static array), or None."""
+    vals = [ctypes.c_int(0) for _ in range(4)]
+    if load_library().gemm_debug_last_pair_launch(*[ctypes.byref(v) for v in vals]) != 0:
+        return None
+    return tuple(v.value for v in vals)
 
 
 def gemm_debug_skinny_plan(M, N, K, ctas):

@@ -226,7 +226,7 @@ int gemm_sgemm_select(int M, int N, int K, int sm_count, gemm_sgemm_config *cfg)
 static int f16_nt_impl(int M, int N, int K, const void *A, const void *B, void *C,
                        gemm_stream_t stream, const gemm_f16_config *cfg, uint64_t timeout_ns,
                        int debug_skip_kblock, bool static_scratch = false,
-                       const gemm_f16_epilogue *epi = nullptr) {
+                       const gemm_f16_epilogue *epi = nullptr, bool debug_skip_publish = false) {
     if (M < 0 || N < 0 || K < 0)
         return fail(GEMM_ERR_INVALID_ARG, "gemm_f16_nt: negative size M=%d N=%d K=%d", M, N, K);
     if (M == 0 || N == 0) return GEMM_OK;
@@ -273,6 +273,7 @@ static int f16_nt_impl(int M, int N, int K, const void *A, const void *B, void *
     L.debug_skip_kblock = debug_skip_kblock;
     L.allow_stream_k = cfg && (cfg->flags & GEMM_F16_FLAG_STREAM_K);
     L.static_scratch = static_scratch;
+    L.debug_skip_publish = debug_skip_publish;
     L.raster = sel.raster;
     L.sm_count = sms;
     if (epi) {
@@ -319,6 +320,27 @@ int gemm_debug_f16_nt_skip_load(int M, int N, int K, const void *A, const void *
     return f16_nt_impl(M, N, K, A, B, C, stream, nullptr, timeout_ns, skip_kblock);
 }
 
+// Test hook declared in gemm_testing.h: stream-K on the pair kernel with the
+// partials written but never flagged, so that each split tile's first pair
+// waits for them until its bounded wait (`timeout_ns`) runs out.
+int gemm_debug_f16_nt_stream_k_skip_publish(int M, int N, int K, const void *A, const void *B, void *C,
+                                            gemm_stream_t stream, unsigned long long timeout_ns) {
+    const gemm_f16_config cfg = {GEMM_F16_256x256_PAIR, 0, GEMM_F16_FLAG_STREAM_K, 0};
+    return f16_nt_impl(M, N, K, A, B, C, stream, &cfg, timeout_ns, -1, false, nullptr, true);
+}
+
+// Test hook declared in gemm_testing.h: the last pair launch's split.
+int gemm_debug_last_pair_launch(int *pairs, int *whole_tiles, int *shared_units, int *scratch_kind) {
+    if (!pairs || !whole_tiles || !shared_units || !scratch_kind) return -1;
+    const gb300::PairLaunchRecord r = gb300::last_pair_launch();
+    if (!r.valid) return -1;
+    *pairs = r.pairs;
+    *whole_tiles = r.whole_tiles;
+    *shared_units = r.shared_units;
+    *scratch_kind = r.scratch_kind;
+    return 0;
+}
+
 // Test hook declared in gemm_testing.h: the skinny variant's plan.
 int gemm_debug_skinny_plan(int M, int N, int K, int ctas, int *rows, int *groups, int *kb_per_split) {
     if (M < 1 || N < 1 || K < 0 || ctas < 1 || !rows || !groups || !kb_per_split) return -1;
@@ -358,22 +380,28 @@ int gemm_mxfp8_nt(int M, int N, int K, const void *A, const void *SFA, const voi
     return gemm_mxfp8_nt_ex(M, N, K, A, SFA, B, SFB, C, stream, nullptr);
 }
 
-int gemm_mxfp8_nt_ex(int M, int N, int K, const void *A, const void *SFA, const void *B,
-                     const void *SFB, void *C, gemm_stream_t stream, const gemm_mxfp8_config *cfg) {
+// Both block-scaled products: fmt 0 MXFP8 (alpha 1), 1 NVFP4.
+static int mx_impl(int fmt, int M, int N, int K, const void *A, const void *SFA, const void *B,
+                   const void *SFB, float alpha, void *C, gemm_stream_t stream,
+                   const gemm_mxfp8_config *cfg, uint64_t timeout_ns, int debug_skip_kblock) {
+    const char *name = fmt == 0 ? "gemm_mxfp8_nt" : "gemm_nvfp4_nt";
     if (cfg && (cfg->variant < 0 || cfg->variant >= GEMM_MXFP8_NUM_VARIANTS || cfg->grid < 0))
-        return fail(GEMM_ERR_INVALID_ARG, "gemm_mxfp8_nt_ex: bad config variant=%d grid=%d",
-                    cfg->variant, cfg->grid);
+        return fail(GEMM_ERR_INVALID_ARG, "%s_ex: bad config variant=%d grid=%d", name, cfg->variant,
+                    cfg->grid);
     if (M < 0 || N < 0 || K < 0)
-        return fail(GEMM_ERR_INVALID_ARG, "gemm_mxfp8_nt: negative size M=%d N=%d K=%d", M, N, K);
+        return fail(GEMM_ERR_INVALID_ARG, "%s: negative size M=%d N=%d K=%d", name, M, N, K);
     if (M == 0 || N == 0) return GEMM_OK;
-    if (!C) return fail(GEMM_ERR_INVALID_ARG, "gemm_mxfp8_nt: C is NULL");
+    if (!C) return fail(GEMM_ERR_INVALID_ARG, "%s: C is NULL", name);
     if (K % 32 != 0)
-        return fail(GEMM_ERR_UNSUPPORTED,
-                    "gemm_mxfp8_nt: K=%d; the 32-element scale blocks need K %% 32 == 0", K);
+        return fmt == 0 ? fail(GEMM_ERR_UNSUPPORTED,
+                               "gemm_mxfp8_nt: K=%d; the 32-element scale blocks need K %% 32 == 0", K)
+                        : fail(GEMM_ERR_UNSUPPORTED,
+                               "gemm_nvfp4_nt: K=%d; rows of K/2 bytes must be multiples of 16 bytes "
+                               "(K %% 32 == 0)", K);
     if (K == 0) return f16_nt_impl(M, N, 0, nullptr, nullptr, C, stream, nullptr, kDefaultTimeoutNs, -1);
-    if (!A || !B || !SFA || !SFB) return fail(GEMM_ERR_INVALID_ARG, "gemm_mxfp8_nt: NULL operand");
+    if (!A || !B || !SFA || !SFB) return fail(GEMM_ERR_INVALID_ARG, "%s: NULL operand", name);
     if (!aligned16(A) || !aligned16(B) || !aligned16(SFA) || !aligned16(SFB))
-        return fail(GEMM_ERR_MISALIGNED, "gemm_mxfp8_nt: A, B, SFA and SFB must be 16-byte aligned");
+        return fail(GEMM_ERR_MISALIGNED, "%s: A, B, SFA and SFB must be 16-byte aligned", name);
     int sms = 0;
     int st = sm_count_of_current_device(&sms);
     if (st != GEMM_OK) return st;
@@ -388,7 +416,7 @@ int gemm_mxfp8_nt_ex(int M, int N, int K, const void *A, const void *SFA, const 
     L.C = C;
     L.stream = reinterpret_cast<cudaStream_t>(stream);
     L.grid = cfg ? cfg->grid : 0;
-    L.timeout_ns = kDefaultTimeoutNs;
+    L.timeout_ns = timeout_ns;
     L.sm_count = sms;
     // Measured on GB300 at 5376 x 5376 x 2048 / x 8192 (us): 1-CTA 128 x 256
     // with N = 256 MMAs 52 / 157, 1-CTA 128 x 128 62 / 215, CTA pair 256 x 256
@@ -397,12 +425,29 @@ int gemm_mxfp8_nt_ex(int M, int N, int K, const void *A, const void *SFA, const 
     // columns do not fit TMEM together); narrow N keeps the 128 x 128 tiles.
     L.variant = (cfg && cfg->variant != GEMM_MXFP8_AUTO) ? cfg->variant
                 : (N > 128 ? GEMM_MXFP8_128x256 : GEMM_MXFP8_128x128);
-    L.fmt = 0;
-    L.alpha = 1.f;
+    L.fmt = fmt;
+    L.alpha = fmt == 0 ? 1.f : alpha;
+    L.debug_skip_kblock = debug_skip_kblock;
     std::string err;
     st = gb300::mx_launch(L, err);
     if (st != GEMM_OK) return fail_str(st, err);
     return GEMM_OK;
+}
+
+int gemm_mxfp8_nt_ex(int M, int N, int K, const void *A, const void *SFA, const void *B,
+                     const void *SFB, void *C, gemm_stream_t stream, const gemm_mxfp8_config *cfg) {
+    return mx_impl(0, M, N, K, A, SFA, B, SFB, 1.f, C, stream, cfg, kDefaultTimeoutNs, -1);
+}
+
+// Test hook declared in gemm_testing.h: a block-scaled product with one
+// k-block never loaded, so that the kernel's bounded waits run out.
+int gemm_debug_blockscaled_skip_load(int fmt, int M, int N, int K, const void *A, const void *SFA,
+                                     const void *B, const void *SFB, void *C, gemm_stream_t stream,
+                                     const gemm_mxfp8_config *cfg, int skip_kblock,
+                                     unsigned long long timeout_ns) {
+    if (fmt != 0 && fmt != 1)
+        return fail(GEMM_ERR_INVALID_ARG, "gemm_debug_blockscaled_skip_load: fmt %d is not 0 or 1", fmt);
+    return mx_impl(fmt, M, N, K, A, SFA, B, SFB, 1.f, C, stream, cfg, timeout_ns, skip_kblock);
 }
 
 // ---------------------------------------------------------------------------
@@ -431,44 +476,7 @@ int gemm_nvfp4_pack_scales(int rows, int K, const void *plain, void *blocked, ge
 int gemm_nvfp4_nt_ex(int M, int N, int K, const void *A, const void *SFA, const void *B,
                      const void *SFB, float alpha, void *C, gemm_stream_t stream,
                      const gemm_mxfp8_config *cfg) {
-    if (cfg && (cfg->grid < 0 || cfg->variant < 0 || cfg->variant >= GEMM_MXFP8_NUM_VARIANTS))
-        return fail(GEMM_ERR_INVALID_ARG, "gemm_nvfp4_nt_ex: bad config variant=%d grid=%d", cfg->variant,
-                    cfg->grid);
-    if (M < 0 || N < 0 || K < 0)
-        return fail(GEMM_ERR_INVALID_ARG, "gemm_nvfp4_nt: negative size M=%d N=%d K=%d", M, N, K);
-    if (M == 0 || N == 0) return GEMM_OK;
-    if (!C) return fail(GEMM_ERR_INVALID_ARG, "gemm_nvfp4_nt: C is NULL");
-    if (K % 32 != 0)
-        return fail(GEMM_ERR_UNSUPPORTED,
-                    "gemm_nvfp4_nt: K=%d; rows of K/2 bytes must be multiples of 16 bytes (K %% 32 == 0)", K);
-    if (K == 0) return f16_nt_impl(M, N, 0, nullptr, nullptr, C, stream, nullptr, kDefaultTimeoutNs, -1);
-    if (!A || !B || !SFA || !SFB) return fail(GEMM_ERR_INVALID_ARG, "gemm_nvfp4_nt: NULL operand");
-    if (!aligned16(A) || !aligned16(B) || !aligned16(SFA) || !aligned16(SFB))
-        return fail(GEMM_ERR_MISALIGNED, "gemm_nvfp4_nt: A, B, SFA and SFB must be 16-byte aligned");
-    int sms = 0;
-    int st = sm_count_of_current_device(&sms);
-    if (st != GEMM_OK) return st;
-    gb300::MxLaunch L;
-    L.M = M;
-    L.N = N;
-    L.K = K;
-    L.A = A;
-    L.SFA = SFA;
-    L.B = B;
-    L.SFB = SFB;
-    L.C = C;
-    L.stream = reinterpret_cast<cudaStream_t>(stream);
-    L.grid = cfg ? cfg->grid : 0;
-    L.timeout_ns = kDefaultTimeoutNs;
-    L.sm_count = sms;
-    L.variant = (cfg && cfg->variant != GEMM_MXFP8_AUTO) ? cfg->variant
-                : (N > 128 ? GEMM_MXFP8_128x256 : GEMM_MXFP8_128x128);
-    L.fmt = 1;
-    L.alpha = alpha;
-    std::string err;
-    st = gb300::mx_launch(L, err);
-    if (st != GEMM_OK) return fail_str(st, err);
-    return GEMM_OK;
+    return mx_impl(1, M, N, K, A, SFA, B, SFB, alpha, C, stream, cfg, kDefaultTimeoutNs, -1);
 }
 
 int gemm_nvfp4_nt(int M, int N, int K, const void *A, const void *SFA, const void *B, const void *SFB,

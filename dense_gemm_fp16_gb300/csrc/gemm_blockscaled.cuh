@@ -225,18 +225,21 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
                     constexpr uint32_t kTileSf = T::kCpt * kMxSfChunk;
                     const int b_tiles = (args.N - nt * BN + 127) / 128;
                     const int b_here = b_tiles < T::kSfbChunks ? b_tiles : T::kSfbChunks;
-                    mbar_arrive_expect_tx(full_bar(stage),
-                                          T::kABytes + T::kBBytes + (1 + b_here) * kTileSf);
-                    tma_load_2d(sa, &tmA, full_bar(stage), kb * kMxBK, mt * kBM);
-                    tma_load_2d(sb, &tmB, full_bar(stage), kb * kMxBK, nt * BN);
-                    bulk_load(ssf, mx.sfa + (static_cast<size_t>(mt) * num_kb + kb) * kTileSf, kTileSf,
-                              full_bar(stage));
-                    for (int c = 0; c < b_here; ++c)
-                        bulk_load(ssf + (1 + c) * kTileSf,
-                                  mx.sfb + (static_cast<size_t>(nt * T::kSfbChunks + c) * num_kb + kb) * kTileSf,
-                                  kTileSf, full_bar(stage));
-                    armed |= 1u << stage;
-                    arm_parity ^= 1u << stage;
+                    // test hook: the first tile's k-block debug_skip_kblock is never loaded
+                    if (!(tile == static_cast<int>(blockIdx.x) && kb == args.debug_skip_kblock)) {
+                        mbar_arrive_expect_tx(full_bar(stage),
+                                              T::kABytes + T::kBBytes + (1 + b_here) * kTileSf);
+                        tma_load_2d(sa, &tmA, full_bar(stage), kb * kMxBK, mt * kBM);
+                        tma_load_2d(sb, &tmB, full_bar(stage), kb * kMxBK, nt * BN);
+                        bulk_load(ssf, mx.sfa + (static_cast<size_t>(mt) * num_kb + kb) * kTileSf, kTileSf,
+                                  full_bar(stage));
+                        for (int c = 0; c < b_here; ++c)
+                            bulk_load(ssf + (1 + c) * kTileSf,
+                                      mx.sfb + (static_cast<size_t>(nt * T::kSfbChunks + c) * num_kb + kb) * kTileSf,
+                                      kTileSf, full_bar(stage));
+                        armed |= 1u << stage;
+                        arm_parity ^= 1u << stage;
+                    }
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -537,22 +540,28 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
                     const uint32_t sa = sbase + stage * T::kStageBytes;
                     const uint32_t ssf = sbase + T::kSfOffset + stage * T::kSfBytes;
                     const uint32_t full_leader = mapa_shared(full_bar(stage), 0);
-                    if (leader) {
-                        // both CTAs' operand and scale bytes (the stage's padding is not loaded)
-                        mbar_arrive_expect_tx(full_bar(stage), 2 * (T::kABytes + T::kBBytes + T::kSfBytes));
-                        armed |= 1u << stage;
-                        arm_parity ^= 1u << stage;
-                    }
-                    tma_load_2d_pair(sa, &tmA, full_leader, kb * kMxBK, a_tile128 * kBM);
-                    tma_load_2d_pair(sa + T::kABytes, &tmB, full_leader, kb * kMxBK,
-                                     nt * BN + static_cast<int>(rank) * (BN / 2));
-                    // scale chunks: 512 bytes = two 256-byte rows of the 2D view;
-                    // the k-block's kCpt chunks of a row tile are contiguous
-                    tma_load_2d_pair(ssf, &tmSFA, full_leader, 0, 2 * T::kCpt * (a_tile128 * num_kb + kb));
+                    // test hook: the even CTA never arms nor loads the first
+                    // tile's k-block debug_skip_kblock (the odd CTA's bytes
+                    // still land, but the stage's phase can never complete)
+                    const bool skip = tile == pair && kb == args.debug_skip_kblock && leader;
+                    if (!skip) {
+                        if (leader) {
+                            // both CTAs' operand and scale bytes (the stage's padding is not loaded)
+                            mbar_arrive_expect_tx(full_bar(stage), 2 * (T::kABytes + T::kBBytes + T::kSfBytes));
+                            armed |= 1u << stage;
+                            arm_parity ^= 1u << stage;
+                        }
+                        tma_load_2d_pair(sa, &tmA, full_leader, kb * kMxBK, a_tile128 * kBM);
+                        tma_load_2d_pair(sa + T::kABytes, &tmB, full_leader, kb * kMxBK,
+                                         nt * BN + static_cast<int>(rank) * (BN / 2));
+                        // scale chunks: 512 bytes = two 256-byte rows of the 2D view;
+                        // the k-block's kCpt chunks of a row tile are contiguous
+                        tma_load_2d_pair(ssf, &tmSFA, full_leader, 0, 2 * T::kCpt * (a_tile128 * num_kb + kb));
 #pragma unroll
-                    for (int c = 0; c < T::kSfbChunks; ++c)
-                        tma_load_2d_pair(ssf + (1 + c) * T::kCpt * kMxSfChunk, &tmSFB, full_leader, 0,
-                                         2 * T::kCpt * ((nt * T::kSfbChunks + c) * num_kb + kb));
+                        for (int c = 0; c < T::kSfbChunks; ++c)
+                            tma_load_2d_pair(ssf + (1 + c) * T::kCpt * kMxSfChunk, &tmSFB, full_leader, 0,
+                                             2 * T::kCpt * ((nt * T::kSfbChunks + c) * num_kb + kb));
+                    }
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -753,7 +762,7 @@ inline F16Args mx_args(const MxLaunch &L, int tile_rows, int BN, int num_kb) {
     }
     args.epi = make_epi(scale, L.N);
     args.timeout_ns = L.timeout_ns;
-    args.debug_skip_kblock = -1;
+    args.debug_skip_kblock = L.debug_skip_kblock;
     args.dp_tiles = 0;
     args.sk_units = 0;
     args.sk_ws = nullptr;

@@ -59,7 +59,8 @@ constexpr int kEpiBytes = 4 * 2 * kEpiBufBytes;
 
 // Device-side status: first timeout code recorded by any CTA (0 = none).
 // 1 = producer (empty-slot wait), 2 = MMA (full-slot or accumulator-free
-// wait), 3 = epilogue (accumulator-ready wait).
+// wait), 3 = epilogue (accumulator-ready wait), 4 = epilogue of a stream-K
+// tile's first pair (wait for the other pairs' partials).
 __device__ int g_f16_status = 0;
 
 struct F16Args {
@@ -71,6 +72,7 @@ struct F16Args {
     Epi epi;                // fused epilogue (epi.on == 0: the plain product)
     uint64_t timeout_ns;
     int debug_skip_kblock;  // -1 = none
+    int debug_skip_publish = 0;  // test hook: stream-K partials are written but never flagged
     // Stream-K (pair kernel only): tiles [0, dp_tiles) are data-parallel, one
     // whole tile per work item; the k-blocks of the remaining tiles are split
     // evenly over the pairs (sk_units k-blocks in all).  A pair whose share
@@ -902,7 +904,8 @@ __global__ void __launch_bounds__((2 + EPI) * 32, 1)
                 epilogue_warp_partial<kCols>(slot, taddr, region, lane);
                 __threadfence();
                 __syncwarp();
-                if (lane == 0) st_release_gpu(args.sk_flags + (pair * 2 + rank) * 8 + ew, args.seq);
+                if (lane == 0 && !args.debug_skip_publish)
+                    st_release_gpu(args.sk_flags + (pair * 2 + rank) * 8 + ew, args.seq);
             } else {
                 Partials pp{args.sk_ws, 0, 0, region, lane};
                 if (kb1 < args.num_kb) {
@@ -1195,16 +1198,28 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocSlotByt
 // Device address of the scratch array for the current device, looked up once
 // per device with that device current (in host code the symbol itself is only
 // a host-side stand-in).  Also advances and returns that device's sequence number.
+// The address stays valid for the life of the CUDA context it was looked up
+// in (a cudaDeviceReset ends that context, and the library must not be used
+// on that device afterwards).
 int noalloc_scratch(cudaStream_t stream, float **ws, uint32_t **flags, uint32_t *seq,
                     std::string &err) {
+    constexpr int kMaxDevices = 64;
     static std::mutex mu;
-    static void *addr[64] = {nullptr};
-    static uint32_t counter[64] = {0};
+    static void *addr[kMaxDevices] = {nullptr};
+    static uint32_t counter[kMaxDevices] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess || dev < 0 || dev >= 64) {
+    if (e != cudaSuccess) {
         err = std::string("cudaGetDevice: ") + cudaGetErrorString(e);
         return GEMM_ERR_CUDA;
+    }
+    if (dev < 0 || dev >= kMaxDevices) {
+        char buf[160];
+        std::snprintf(buf, sizeof buf,
+                      "gemm_f16_nt_stream_k_noalloc: device %d is beyond the %d devices it keeps "
+                      "scratch addresses for", dev, kMaxDevices);
+        err = buf;
+        return GEMM_ERR_UNSUPPORTED;
     }
     std::lock_guard<std::mutex> lock(mu);
     if (!addr[dev]) {
@@ -1230,6 +1245,8 @@ int noalloc_scratch(cudaStream_t stream, float **ws, uint32_t **flags, uint32_t 
     *seq = counter[dev];
     return GEMM_OK;
 }
+
+thread_local PairLaunchRecord t_last_pair;
 
 template <int STAGES, int EPI, int ACT, bool RES>
 int launch_pair(const F16Launch &L, std::string &err) {
@@ -1293,6 +1310,7 @@ int launch_pair(const F16Launch &L, std::string &err) {
     args.epi = make_epi(L.epi, L.N);
     args.timeout_ns = L.timeout_ns;
     args.debug_skip_kblock = L.debug_skip_kblock;
+    args.debug_skip_publish = L.debug_skip_publish ? 1 : 0;
     CUtensorMap tmC, tmR;
     std::memset(&tmC, 0, sizeof tmC);
     std::memset(&tmR, 0, sizeof tmR);
@@ -1302,6 +1320,9 @@ int launch_pair(const F16Launch &L, std::string &err) {
     int pairs = L.grid / 2;
     if (pairs < 1) pairs = 1;
     if (pairs > clusters) pairs = clusters;
+    // The allocation-free entry point's static array has partial slots for
+    // kNoAllocMaxPairs pairs: a larger device runs that many persistent pairs.
+    if (L.static_scratch && pairs > kNoAllocMaxPairs) pairs = kNoAllocMaxPairs;
 
     // The k-blocks of some tiles shared out over several pairs (stream-K),
     // whose fp32 partials the pair holding k-block 0 adds before rounding:
@@ -1347,16 +1368,6 @@ int launch_pair(const F16Launch &L, std::string &err) {
             args.sk_flags = w->flags;
             args.seq = w->seq;
         } else if (cap == cudaStreamCaptureStatusNone) {
-            if (pairs > kNoAllocMaxPairs) {
-                char buf[200];
-                std::snprintf(buf, sizeof buf,
-                              "gemm_f16_nt_stream_k_noalloc: %d CTA pairs need %zu bytes of stream-K "
-                              "scratch; the static array holds %zu (%d pairs)",
-                              pairs, static_cast<size_t>(pairs) * 2 * kSkSlotFloats * sizeof(float),
-                              kNoAllocSlotBytes, kNoAllocMaxPairs);
-                err = buf;
-                return GEMM_ERR_UNSUPPORTED;
-            }
             float *ws = nullptr;
             uint32_t *flags = nullptr;
             uint32_t seq = 0;
@@ -1376,6 +1387,11 @@ int launch_pair(const F16Launch &L, std::string &err) {
         err = std::string("gemm_f16_nt pair kernel launch: ") + cudaGetErrorString(e);
         return GEMM_ERR_CUDA;
     }
+    t_last_pair.valid = true;
+    t_last_pair.pairs = pairs;
+    t_last_pair.whole_tiles = args.dp_tiles;
+    t_last_pair.shared_units = args.sk_units;
+    t_last_pair.scratch_kind = args.sk_units == 0 ? 0 : (L.static_scratch ? 2 : 1);
     return GEMM_OK;
 }
 
@@ -1452,6 +1468,8 @@ int f16_launch(const F16Launch &L, std::string &err) {
         default: err = "unknown fp16 variant"; return GEMM_ERR_INVALID_ARG;
     }
 }
+
+PairLaunchRecord last_pair_launch() { return t_last_pair; }
 
 int f16_status_read_clear(cudaStream_t stream, int *code, std::string &err) {
     cudaError_t e = cudaStreamSynchronize(stream);

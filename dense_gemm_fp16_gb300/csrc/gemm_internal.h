@@ -62,9 +62,20 @@ struct F16Launch {
     int sm_count;           // SMs of the current device
     EpiSpec epi;            // fused epilogue (off by default)
     int raster = 1 << 30;   // tile rows per band of the tile order (>= tile rows: plain)
+    bool debug_skip_publish = false;  // test hook: stream-K partials never flagged ready
 };
 
 int f16_launch(const F16Launch &L, std::string &err);
+
+// What the last CTA-pair launch on this host thread chose (a test hook):
+// the pair count, the tiles computed whole, the k-block units shared out, and
+// where the partials went (0 nowhere, 1 an allocated workspace, 2 the static
+// array of the allocation-free entry point).  valid == false before the first.
+struct PairLaunchRecord {
+    bool valid = false;
+    int pairs = 0, whole_tiles = 0, shared_units = 0, scratch_kind = 0;
+};
+PairLaunchRecord last_pair_launch();
 
 // Read-and-clear the fp16 kernel's device status word (0 = no fault).
 // Block-scaled FP8 (MXFP8) NT product: E4M3 A [M,K], B [N,K], scale chunks
@@ -80,6 +91,7 @@ struct MxLaunch {
     int variant;  // GEMM_MXFP8_* of gemm.h
     int fmt;      // 0: MXFP8 (E4M3, UE8M0 per 32), 1: NVFP4 (E2M1 pairs, UE4M3 per 16)
     float alpha;  // NVFP4: the tensor-level scale applied to the product
+    int debug_skip_kblock = -1;  // test hook: producer skips this k-block of its first tile
 };
 int mx_launch(const MxLaunch &L, std::string &err);
 // Plain scales [rows][K/block] -> chunk layout (device pointers, on

@@ -37,6 +37,10 @@
  *    the device (a bounded wait inside a kernel that ran out) are reported by
  *    gemm_check_device_status().
  *  - Empty problems: M == 0 or N == 0 is a no-op returning GEMM_OK.
+ *  - Per-device state (SM counts, occupancy, workspaces, the static array's
+ *    address) is looked up once per device and kept for the CUDA context it
+ *    was made in: after cudaDeviceReset on a device, do not call the library
+ *    on that device again in the same process.
  */
 #ifndef DENSE_GEMM_FP16_GB300_GEMM_H
 #define DENSE_GEMM_FP16_GB300_GEMM_H
@@ -150,6 +154,19 @@ typedef struct {
  * fixed order: results do not depend on timing.  Also skipped under stream
  * capture.  gemm_f16_select sends such shapes to GEMM_F16_SKINNY instead,
  * whose split needs no workspace.
+ *
+ * Waiting between pairs (stream-K, this split-K and
+ * gemm_f16_nt_stream_k_noalloc): a split tile's first pair waits, inside the
+ * kernel, for the partials of the pairs that share its k-range, and those
+ * always have lower cluster indices than the pair that waits.  The GPU
+ * dispatches the clusters of a grid in index order (observed behaviour, not
+ * a documented guarantee), so when a long kernel on another stream holds
+ * some SMs, the pairs that are running form a prefix of the grid and every
+ * pair they wait for is running or done.  Should a wait still not end (a
+ * different dispatch order, or a preemption longer than the bound), it gives up
+ * after 2 s: the call leaves C partly written and gemm_check_device_status()
+ * reports GEMM_ERR_DEVICE_TIMEOUT.  The skinny and SGEMM splits never wait
+ * on another CTA's progress outside their own cluster.
  */
 #define GEMM_F16_FLAG_STREAM_K 1
 
@@ -220,9 +237,11 @@ int gemm_f16_nt_ex(int M, int N, int K, const void *A, const void *B, void *C,
  * (for example on two streams at once) race on the array and must not be
  * made; calls on one stream never overlap.
  *
- * Errors: as gemm_f16_nt, plus GEMM_ERR_UNSUPPORTED when the launch would use
- * more CTA pairs than the array holds slots for (a device with more than 152
- * SMs), with the sizes in the message.
+ * Size limit: the array holds partial slots for 76 CTA pairs; on a device
+ * that could run more pairs at once, the call runs 76 persistent pairs.
+ *
+ * Errors: as gemm_f16_nt, plus GEMM_ERR_UNSUPPORTED for a device id of 64 or
+ * more (the library keeps the array's address for devices 0..63).
  */
 int gemm_f16_nt_stream_k_noalloc(int M, int N, int K, const void *A, const void *B, void *C,
                                  gemm_stream_t stream);

@@ -43,6 +43,48 @@ int gemm_debug_f16_nt_skip_load(int M, int N, int K, const void *A, const void *
  */
 int gemm_debug_skinny_plan(int M, int N, int K, int ctas, int *rows, int *groups, int *kb_per_split);
 
+/*
+ * A block-scaled product (fmt 0: gemm_mxfp8_nt_ex, 1: gemm_nvfp4_nt_ex with
+ * alpha = 1) with one k-block deliberately never loaded: each CTA (the even
+ * CTA of each pair, for the pair variants) neither arms nor loads k-block
+ * `skip_kblock` of the first tile it processes, so the MMA issuer's wait for
+ * that stage can never succeed.  Every wait is bounded by `timeout_ns`; the
+ * kernel then records a status code, drains its own copies and MMAs, frees
+ * its Tensor Memory and exits, and gemm_check_device_status() reports
+ * GEMM_ERR_DEVICE_TIMEOUT.  C is left partially written.  Same argument rules
+ * as gemm_mxfp8_nt_ex / gemm_nvfp4_nt_ex (cfg may be NULL), plus
+ * GEMM_ERR_INVALID_ARG for another fmt.
+ */
+int gemm_debug_blockscaled_skip_load(int fmt, int M, int N, int K, const void *A, const void *SFA,
+                                     const void *B, const void *SFB, void *C, gemm_stream_t stream,
+                                     const gemm_mxfp8_config *cfg, int skip_kblock,
+                                     unsigned long long timeout_ns);
+
+/*
+ * gemm_f16_nt_ex on the CTA-pair variant with GEMM_F16_FLAG_STREAM_K, where
+ * every pair that takes over part of a tile's k-range writes its fp32
+ * partial but never flags it ready.  The tile's first pair then waits for
+ * the flags until its bounded wait (`timeout_ns`) runs out, and
+ * gemm_check_device_status() reports GEMM_ERR_DEVICE_TIMEOUT.  Whether the
+ * launch splits at all follows the stream-K rule (gemm_debug_last_pair_launch
+ * tells); the shape must have a partial last round of 256 x 256 tiles.
+ */
+int gemm_debug_f16_nt_stream_k_skip_publish(int M, int N, int K, const void *A, const void *B, void *C,
+                                            gemm_stream_t stream, unsigned long long timeout_ns);
+
+/*
+ * How the last launch of the CTA-pair kernel (GEMM_F16_256x256_PAIR) made on
+ * the calling host thread split its work: *pairs CTA pairs, *whole_tiles
+ * 256 x 256 tiles computed whole, *shared_units k-blocks of 64 shared out
+ * over the pairs (stream-K or split-K; 0 when nothing was split), and where
+ * the fp32 partials of the shared tiles went: *scratch_kind 0 nowhere, 1 the
+ * workspace the library allocates per device and stream, 2 the static array
+ * of gemm_f16_nt_stream_k_noalloc.  Host state only, no device call.
+ * Returns 0, or -1 (outputs untouched) when no pair launch has been made on
+ * this thread or an output pointer is NULL.
+ */
+int gemm_debug_last_pair_launch(int *pairs, int *whole_tiles, int *shared_units, int *scratch_kind);
+
 #ifdef __cplusplus
 }
 #endif

@@ -37,7 +37,8 @@ def test_headers_declare_the_boundary():
               "gemm_debug_f16_nt_skip_load", "gemm_debug_skinny_plan",
               "gemm_f16_nt_fused", "gemm_f16_nt_stream_k_noalloc",
               "gemm_mxfp8_nt", "gemm_mxfp8_scale_bytes", "gemm_mxfp8_pack_scales",
-              "gemm_nvfp4_nt", "gemm_nvfp4_nt_ex", "gemm_nvfp4_scale_bytes", "gemm_nvfp4_pack_scales"]:
+              "gemm_nvfp4_nt", "gemm_nvfp4_nt_ex", "gemm_nvfp4_scale_bytes", "gemm_nvfp4_pack_scales",
+              "gemm_debug_last_pair_launch"]:
         assert n in names
 
 
@@ -54,6 +55,11 @@ def test_negative_sizes_are_rejected_on_the_host(lib):
     with pytest.raises(g.GemmError) as e:
         g.sgemm(4, -4, 4, 1.0, 16, 16, 0.0, 16)
     assert e.value.status == g.GEMM_ERR_INVALID_ARG
+
+
+def test_pair_launch_record_is_empty_before_any_launch(lib):
+    # host-side state of the test hook: nothing launched in this process yet
+    assert g.gemm_debug_last_pair_launch() is None
 
 
 def test_empty_problems_are_no_ops(lib):

@@ -7,10 +7,15 @@ must account for every byte.  For them this entry point runs the CTA-pair
 kernel with its stream-K split but keeps the partial tiles and flags in a
 static array inside the library instead of a workspace it allocates.
 
-Through the C ABI, it must give gemm_f16_nt's result within the fp16
-tolerance (|difference| <= 4e-3 * sum_k |A*B| + 1e-6 per element), on two
-calls in a row: the second call finds the first call's partials and flags
-still in the shared array and must not be misled by them.
+Through the C ABI, on two calls in a row, it must
+  * match the float64 oracle within the fp16 tolerance
+    (|C - C_ref| <= 4e-3 * sum_k |A*B| + 1e-6 per element),
+  * agree with gemm_f16_nt's result within that same tolerance,
+  * really take the static-scratch split (the launch record of the test
+    hooks says so), and
+  * leave the device's free memory unchanged.
+The second call finds the first call's partials and flags still in the
+shared array and must not be misled by them.
 
 This file is named so that pytest collects it last.
 """
@@ -21,9 +26,11 @@ import torch
 import oracle
 import dense_gemm_fp16_gb300 as g
 from dense_gemm_fp16_gb300 import workloads as wl
-from parity import F16_ABS, F16_REL
+from parity import F16_ABS, F16_REL, check_f16
 
 pytestmark = pytest.mark.gpu
+
+SCRATCH_STATIC = 2  # gemm_debug_last_pair_launch: partials in the static array
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -35,30 +42,47 @@ def _lib():
     torch.cuda.init()
 
 
-def test_noalloc_entry_point_matches_gemm_f16_nt_on_two_calls():
+def test_noalloc_entry_point_matches_the_oracle_on_two_calls():
     # 2304 x 2304 gives 9 x 9 = 81 tiles of 256 x 256 for the 76 CTA pairs of a
     # GB300: the 5 tiles left after the full round have 5 x 16 = 80 k-blocks,
     # split over all pairs, so partials pass through the static array.
     M, N, K = 2304, 2304, 1024
     A = wl.draw_f16((M, K), seed=81, dist="normal")
     B = wl.draw_f16((N, K), seed=82, dist="normal")
-    _, S = oracle.gemm_f16_nt(A, B)
+    C_ref, S = oracle.gemm_f16_nt(A, B)
     bound = F16_REL * S + F16_ABS
 
-    stream = torch.cuda.current_stream().cuda_stream
     dA, dB = A.cuda(), B.cuda()
-    C_ref = torch.empty((M, N), dtype=torch.float16, device="cuda")
-    g.gemm_f16_nt(M, N, K, dA.data_ptr(), dB.data_ptr(), C_ref.data_ptr(), stream)
-    g.gemm_check_device_status(stream)
-    ref = C_ref.cpu().numpy().astype(np.float64)
+    # gemm_f16_nt's result for the same inputs (its pair kernel is the same
+    # compiled module, so the module is loaded before free memory is read)
+    C_lib = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    cur = torch.cuda.current_stream().cuda_stream
+    g.gemm_f16_nt(M, N, K, dA.data_ptr(), dB.data_ptr(), C_lib.data_ptr(), cur)
+    g.gemm_check_device_status(cur)
+    lib_out = C_lib.cpu().numpy().astype(np.float64)
+    check_f16(lib_out, C_ref, S, what="gemm_f16_nt")
 
-    for call in range(2):
-        C = torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda")
-        assert g.gemm_f16_nt_stream_k_noalloc(M, N, K, dA.data_ptr(), dB.data_ptr(),
-                                              C.data_ptr(), stream) == g.GEMM_OK
-        g.gemm_check_device_status(stream)
+    outs = [torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda") for _ in range(2)]
+    stream = torch.cuda.Stream()            # a stream no call has used yet
+    torch.cuda.synchronize()
+    free_before, _ = torch.cuda.mem_get_info()
+    for call, C in enumerate(outs):
+        assert g.gemm_f16_nt_stream_k_noalloc(M, N, K, dA.data_ptr(), dB.data_ptr(), C.data_ptr(),
+                                              stream.cuda_stream) == g.GEMM_OK
+        rec = g.gemm_debug_last_pair_launch()
+        assert rec is not None
+        pairs, whole, shared, kind = rec
+        assert kind == SCRATCH_STATIC and shared > 0, \
+            f"call {call}: the static-scratch split was not taken (launch record {rec})"
+        assert whole + shared // ((K + 63) // 64) == (M // 256) * (N // 256)
+        g.gemm_check_device_status(stream.cuda_stream)
+    free_after, _ = torch.cuda.mem_get_info()
+    assert free_after == free_before, \
+        f"device free memory moved by {free_before - free_after} bytes across the calls"
+
+    for call, C in enumerate(outs):
         got = C.cpu().numpy().astype(np.float64)
-        assert np.all(np.isfinite(got)), f"call {call}: unwritten or non-finite outputs"
-        err = np.abs(got - ref)
+        check_f16(got, C_ref, S, what=f"no-alloc call {call} against the oracle")
+        err = np.abs(got - lib_out)
         assert np.all(err <= bound), \
             f"call {call}: {(err > bound).sum()} outputs differ from gemm_f16_nt beyond tolerance"
