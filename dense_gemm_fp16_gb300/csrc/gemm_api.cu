@@ -72,9 +72,11 @@ int f16_default_grid(int variant, int M, int N, int K, int sm_count) {
     switch (variant) {
         case GEMM_F16_128x256: tiles = ceil_div(M, 128) * ceil_div(N, 256); break;
         case GEMM_F16_256x256_PAIR: tiles = 2 * ceil_div(M, 256) * ceil_div(N, 256); break;
+        case GEMM_F16_256x256_QUAD: tiles = 4 * ceil_div(M, 512) * ceil_div(N, 256); break;
         default: tiles = ceil_div(M, 128) * ceil_div(N, 128); break;
     }
     long long cap = sm_count;
+    if (variant == GEMM_F16_256x256_QUAD) cap = sm_count & ~3;
     if (variant == GEMM_F16_256x256_PAIR) {
         cap = sm_count & ~1;
         // Split-K spreads few tiles over all the pairs.
@@ -102,8 +104,10 @@ static int f16_default_raster(int variant, int M, int N, int K) {
     const double operand_bytes = 2.0 * (static_cast<double>(M) + N) * K;
     if (variant == GEMM_F16_GEMV || variant == GEMM_F16_SKINNY || operand_bytes <= 96.0 * 1024 * 1024)
         return 1 << 30;
-    return variant == GEMM_F16_256x256_PAIR ? 8 : 16;
+    return variant == GEMM_F16_256x256_PAIR || variant == GEMM_F16_256x256_QUAD ? 8 : 16;
 }
+
+
 
 int gemm_f16_select(int M, int N, int K, int sm_count, gemm_f16_config *cfg) {
     if (!cfg) return fail(GEMM_ERR_INVALID_ARG, "gemm_f16_select: cfg is NULL");
@@ -153,6 +157,18 @@ int gemm_f16_select(int M, int N, int K, int sm_count, gemm_f16_config *cfg) {
             best = w256;
         }
         if (wpair < best) variant = GEMM_F16_256x256_PAIR;
+        // Rows of A and B that are not a whole number of 128-byte lines (K not
+        // a multiple of 64) make every 128-byte TMA row span two L2 lines:
+        // the L2 requests per byte loaded more than double and bound the pair
+        // kernel (5000 x 5376 x 2040: 2.6x the requests of 5376^2 x 2048, the
+        // tensor pipe 63 % busy instead of 86 %).  Two pairs sharing B through
+        // multicast cut a quarter of them, which measured faster on every such
+        // shape tried, even where their 36 clusters need more waves than 76
+        // pairs (us, pair / two pairs: 5000 x 5376 x 2040 94 / 76, 5376^2 x 2040
+        // 95 / 87, 4096^2 x 4088 116 / 93, 8192^2 x 8184 803 / 713); on rows of
+        // whole lines the pair stays ahead (5376^2 x 2048 78 / 88).  With one
+        // row of pair tiles (M <= 256) the second pair would have no tiles.
+        if (variant == GEMM_F16_256x256_PAIR && K % 64 != 0 && M > 256) variant = GEMM_F16_256x256_QUAD;
     }
     cfg->variant = variant;
     cfg->grid = f16_default_grid(variant, M, N, K, sm_count);

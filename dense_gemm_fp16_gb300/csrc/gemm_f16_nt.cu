@@ -681,13 +681,25 @@ struct PairCfg {
 
 // RES: the fused epilogue's residual comes through per-warp TMA rings
 // (kResBufs staging buffers per epilogue warp; 4 epilogue warps).
-template <int STAGES, int EPI, int ACT, bool RES>
+//
+// CL = 4 (two pairs per cluster): the pairs of a cluster compute the two
+// vertically adjacent 256 x 256 tiles (2q, n) and (2q + 1, n) of quad tile
+// (q, n), which need the same 256 rows of B.  CTA r of pair p loads rows
+// 64p .. 64p+63 of its 128-row half of B and multicasts them to CTA r of both
+// pairs, so each B byte leaves L2 once for two tiles: a quarter fewer L2 reads
+// and requests per k-block (A is not shared).  The multicast bytes are counted
+// on the full barrier of each receiving pair's even CTA, which arms it for its
+// pair's 64 KB as before.  A stage can be refilled only when both pairs' MMAs
+// have read it, so empty[s] takes one commit from each pair's MMA issuer,
+// multicast to all four CTAs.
+template <int STAGES, int EPI, int ACT, bool RES, int CL = 2>
 __global__ void __launch_bounds__((2 + EPI) * 32, 1)
     gemm_f16_nt_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                             const __grid_constant__ CUtensorMap tmB,
                             const __grid_constant__ CUtensorMap tmC,
                             const __grid_constant__ CUtensorMap tmR, const F16Args args) {
     static_assert(!RES || EPI == 4, "residual rings are laid out for 4 epilogue warps");
+    static_assert(CL == 2 || CL == 4, "a CTA pair, or two pairs sharing B");
     constexpr int kBufs = RES ? kResBufs : 8 / EPI;
     using T = PairCfg<STAGES, EPI * kBufs * kEpiBufBytes, RES ? EPI * kResBufs : 0>;
     constexpr int BN = T::kBN;
@@ -710,10 +722,16 @@ __global__ void __launch_bounds__((2 + EPI) * 32, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t rank = cluster_ctarank();  // 0 (leader) or 1
+    const uint32_t crank = cluster_ctarank();
+    const uint32_t rank = crank & 1u;          // 0 (leader) or 1 within the pair
+    const uint32_t pic = crank >> 1;           // which pair of the cluster (CL = 4)
+    const uint32_t lead = crank & ~1u;         // this pair's even CTA
     const bool leader = rank == 0;
-    const int pair = blockIdx.x >> 1;
-    const int num_pairs = gridDim.x >> 1;
+    // the persistent work unit: a pair (CL = 2) or a two-pair cluster (CL = 4)
+    const int pair = static_cast<int>(blockIdx.x) / CL;
+    const int num_pairs = static_cast<int>(gridDim.x) / CL;
+    // tile row of this pair for work-list tile row mt (quad rows hold two)
+    auto pair_row = [&](int mt) { return CL == 2 ? mt : 2 * mt + static_cast<int>(pic); };
 
     if (threadIdx.x == 0) {
         tma_prefetch_desc(&tmA);
@@ -722,7 +740,7 @@ __global__ void __launch_bounds__((2 + EPI) * 32, 1)
         if (RES) tma_prefetch_desc(&tmR);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), 1);
+            mbar_init(empty_bar(s), CL / 2);  // one MMA commit per pair
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(accf_bar(b), 1);
@@ -760,8 +778,9 @@ __global__ void __launch_bounds__((2 + EPI) * 32, 1)
             while (ok && work.next(tile, kb0, kb1)) {
                 int mt, nt;
                 tile_mn(tile, args, mt, nt);
+                mt = pair_row(mt);
                 const int a_row = mt * 256 + static_cast<int>(rank) * 128;
-                const int b_row = nt * BN + static_cast<int>(rank) * 128;
+                const int b_row = nt * BN + static_cast<int>(rank) * 128 + (CL == 4 ? 64 * static_cast<int>(pic) : 0);
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait_cluster(empty_bar(stage), phase ^ 1u, args.timeout_ns, abort_flag)) {
                         ok = false;
@@ -770,14 +789,21 @@ __global__ void __launch_bounds__((2 + EPI) * 32, 1)
                     const bool skip = first_tile && kb == args.debug_skip_kblock && leader;
                     if (!skip) {
                         const uint32_t sa = sbase + stage * T::kStageBytes;
-                        const uint32_t full_leader = mapa_shared(full_bar(stage), 0);
+                        const uint32_t full_leader = mapa_shared(full_bar(stage), lead);
                         if (leader) {
                             mbar_arrive_expect_tx(full_bar(stage), 2 * T::kStageBytes);
                             armed |= 1u << stage;
                             arm_parity ^= 1u << stage;
                         }
                         tma_load_2d_pair(sa, &tmA, full_leader, kb * kBK, a_row);
-                        tma_load_2d_pair(sa + T::kABytes, &tmB, full_leader, kb * kBK, b_row);
+                        if constexpr (CL == 2) {
+                            tma_load_2d_pair(sa + T::kABytes, &tmB, full_leader, kb * kBK, b_row);
+                        } else {
+                            // rows 64 pic .. of this CTA's B half, to CTA `rank` of both pairs
+                            tma_load_2d_pair_multicast(sa + T::kABytes + pic * (T::kBBytes / 2), &tmB,
+                                                       full_leader, kb * kBK, b_row,
+                                                       static_cast<uint16_t>(0x5u << rank));
+                        }
                     }
                     if (++stage == STAGES) {
                         stage = 0;
@@ -823,14 +849,14 @@ __global__ void __launch_bounds__((2 + EPI) * 32, 1)
                     for (int k = 0; k < kBK / kUmmaK; ++k)
                         mma_f16_ss_pair(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc,
                                         (kb > kb0 || k > 0) ? 1u : 0u);
-                    mma_commit_pair_multicast(empty_bar(stage), 0x3);
+                    mma_commit_pair_multicast(empty_bar(stage), CL == 2 ? 0x3 : 0xF);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                mma_commit_pair_multicast(accf_bar(b), 0x3);
+                mma_commit_pair_multicast(accf_bar(b), static_cast<uint16_t>(0x3u << lead));
             }
             if (!ok) {
                 if (!*abort_flag) record_timeout(2);
@@ -857,6 +883,7 @@ __global__ void __launch_bounds__((2 + EPI) * 32, 1)
             const uint32_t ap = (i >> 1) & 1;
             int tm, tn;
             tile_mn(tile, args, tm, tn);
+            tm = pair_row(tm);
             const int row0 = tm * 256 + static_cast<int>(rank) * 128 + quarter * 32;
             const int n_base = tn * BN + col0;
             if constexpr (RES) {
@@ -875,6 +902,7 @@ __global__ void __launch_bounds__((2 + EPI) * 32, 1)
                 auto prefetch = [&](int t) {
                     int pm, pn;
                     tile_mn(t, args, pm, pn);
+                    pm = pair_row(pm);
                     epi_prefetch_res(args.epi, pm * 256 + static_cast<int>(rank) * 128 + quarter * 32 + lane,
                                      pn * BN + col0, kCols, args.M, args.N);
                 };
@@ -946,7 +974,7 @@ __global__ void __launch_bounds__((2 + EPI) * 32, 1)
             }
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(mapa_shared(acce_bar(b), 0));
+            if (lane == 0) mbar_arrive_cluster(mapa_shared(acce_bar(b), lead));
         }
         if constexpr (RES) {
             // Residual loads still in flight (only after an abort) land before
@@ -1248,11 +1276,13 @@ int noalloc_scratch(cudaStream_t stream, float **ws, uint32_t **flags, uint32_t 
 
 thread_local PairLaunchRecord t_last_pair;
 
-template <int STAGES, int EPI, int ACT, bool RES>
+// CL = 2: one CTA pair per 256 x 256 tile; CL = 4: two pairs per cluster
+// sharing B (vertically adjacent tiles), no split.
+template <int STAGES, int EPI, int ACT, bool RES, int CL = 2>
 int launch_pair(const F16Launch &L, std::string &err) {
     constexpr int kBufs = RES ? kResBufs : 8 / EPI;
     using T = PairCfg<STAGES, EPI * kBufs * kEpiBufBytes, RES ? EPI * kResBufs : 0>;
-    auto kernel = gemm_f16_nt_pair_kernel<STAGES, EPI, ACT, RES>;
+    auto kernel = gemm_f16_nt_pair_kernel<STAGES, EPI, ACT, RES, CL>;
     static int max_clusters[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -1271,7 +1301,7 @@ int launch_pair(const F16Launch &L, std::string &err) {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = CL;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1283,8 +1313,8 @@ int launch_pair(const F16Launch &L, std::string &err) {
     cfg.numAttrs = 1;
     int clusters = cached ? max_clusters[dev] : 0;
     if (!cached) {
-        // How many CTA pairs can be resident at once: the persistent grid size.
-        cfg.gridDim = dim3(2);
+        // How many clusters can be resident at once: the persistent grid size.
+        cfg.gridDim = dim3(CL);
         e = cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg);
         if (e != cudaSuccess || clusters <= 0) {
             err = std::string("cudaOccupancyMaxActiveClusters: ") + cudaGetErrorString(e);
@@ -1294,15 +1324,17 @@ int launch_pair(const F16Launch &L, std::string &err) {
     }
     CUtensorMap tmA, tmB;
     if (!encode_half_map(&tmA, L.A, L.M, L.K, kBM, kBK, err)) return GEMM_ERR_CUDA;
-    if (!encode_half_map(&tmB, L.B, L.N, L.K, 128, kBK, err)) return GEMM_ERR_CUDA;
+    // (two pairs sharing B each load 64 of a CTA's 128 rows of it)
+    if (!encode_half_map(&tmB, L.B, L.N, L.K, CL == 2 ? 128 : 64, kBK, err)) return GEMM_ERR_CUDA;
 
     F16Args args;
     args.C = static_cast<__half *>(L.C);
     args.M = L.M;
     args.N = L.N;
     args.K = L.K;
-    args.m_tiles = (L.M + 255) / 256;
-    args.raster = L.raster > 0 ? L.raster : (1 << 30);
+    // work-list tile rows: 256 output rows per pair, 512 per two-pair cluster
+    args.m_tiles = (L.M + 128 * CL - 1) / (128 * CL);
+    args.raster = L.raster > 0 ? (CL == 2 ? L.raster : (L.raster + 1) / 2) : (1 << 30);
     args.n_tiles = (L.N + 255) / 256;
     args.num_kb = (L.K + kBK - 1) / kBK;
     args.vec_store = (L.N % 8 == 0) && ((reinterpret_cast<uintptr_t>(L.C) & 15u) == 0);
@@ -1317,7 +1349,8 @@ int launch_pair(const F16Launch &L, std::string &err) {
     if (args.tma_store && !encode_half_map(&tmC, L.C, L.M, L.N, 32, 64, err)) return GEMM_ERR_CUDA;
     if (RES && !encode_half_map(&tmR, L.epi.res, L.M, L.N, 32, 64, err)) return GEMM_ERR_CUDA;
     const int tiles = args.m_tiles * args.n_tiles;
-    int pairs = L.grid / 2;
+    // `pairs` counts the persistent clusters (CTA pairs, or two-pair clusters)
+    int pairs = L.grid / CL;
     if (pairs < 1) pairs = 1;
     if (pairs > clusters) pairs = clusters;
     // The allocation-free entry point's static array has partial slots for
@@ -1339,15 +1372,15 @@ int launch_pair(const F16Launch &L, std::string &err) {
     args.sk_ws = nullptr;
     args.sk_flags = nullptr;
     args.seq = 0;
-    const int split_pairs = args.tma_store ? pair_split_pairs(tiles, args.num_kb, pairs) : 0;
+    const int split_pairs = CL == 2 && args.tma_store ? pair_split_pairs(tiles, args.num_kb, pairs) : 0;
     int rem = 0;  // tiles of the shared round
     if (split_pairs > 0) {
         rem = tiles;
     } else {
         if (pairs > tiles) pairs = tiles;
         const int r = tiles % pairs;
-        if (L.allow_stream_k && args.tma_store && tiles > pairs && r != 0 && 10 * r < 9 * pairs &&
-            static_cast<long long>(r) * args.num_kb >= pairs)
+        if (CL == 2 && L.allow_stream_k && args.tma_store && tiles > pairs && r != 0 &&
+            10 * r < 9 * pairs && static_cast<long long>(r) * args.num_kb >= pairs)
             rem = r;
     }
     if (rem > 0) {
@@ -1380,7 +1413,7 @@ int launch_pair(const F16Launch &L, std::string &err) {
             args.seq = seq;
         }
     }
-    cfg.gridDim = dim3(2 * pairs);
+    cfg.gridDim = dim3(CL * pairs);
     cfg.numAttrs = 2;  // cluster shape + programmatic dependent launch
     e = cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, tmC, tmR, args);
     if (e != cudaSuccess) {
@@ -1388,7 +1421,7 @@ int launch_pair(const F16Launch &L, std::string &err) {
         return GEMM_ERR_CUDA;
     }
     t_last_pair.valid = true;
-    t_last_pair.pairs = pairs;
+    t_last_pair.pairs = pairs * (CL / 2);
     t_last_pair.whole_tiles = args.dp_tiles;
     t_last_pair.shared_units = args.sk_units;
     t_last_pair.scratch_kind = args.sk_units == 0 ? 0 : (L.static_scratch ? 2 : 1);
@@ -1454,6 +1487,8 @@ int f16_launch(const F16Launch &L, std::string &err) {
         case GEMM_F16_128x256: return launch_variant_epi<256, 4>(L, err);
         case GEMM_F16_128x128: return launch_variant_epi<128, 6>(L, err);
         case GEMM_F16_256x256_PAIR: return launch_pair_epi(L, err);
+        // two pairs sharing B: the plain product (a fused epilogue runs on the pair variant)
+        case GEMM_F16_256x256_QUAD: return L.epi.on ? launch_pair_epi(L, err) : launch_pair<6, 4, -1, false, 4>(L, err);
         case GEMM_F16_GEMV: {
             GemvLaunch G{L.M, L.N, L.K, L.A, L.B, L.C, L.stream, L.sm_count, 4, L.epi};
             return gemv_launch(G, err);

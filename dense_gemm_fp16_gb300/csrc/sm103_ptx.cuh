@@ -239,6 +239,19 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void *desc,
         : "memory");
 }
 
+// The same, multicast: the box lands at offset `dst` in every CTA of
+// `cta_mask`, and each receiving CTA's bytes are counted on the barrier at
+// the offset of `bar_cluster` in the even CTA of that CTA's pair.
+__device__ __forceinline__ void tma_load_2d_pair_multicast(uint32_t dst, const void *desc,
+                                                           uint32_t bar_cluster, int c0, int c1,
+                                                           uint16_t cta_mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".multicast::cluster.cta_group::2 [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(desc)), "r"(bar_cluster), "r"(c0), "r"(c1), "h"(cta_mask)
+        : "memory");
+}
+
 // One warp in each CTA of the pair allocates the same TMEM columns in both.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst),

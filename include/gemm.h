@@ -187,7 +187,13 @@ enum {
                                 /* tile kernels' numerics).  Chosen for 2 <= M <=  */
                                 /* 64, and for any M whose tiles it splits in two  */
                                 /* shares of 16+ k-blocks or in four or more       */
-    GEMM_F16_NUM_VARIANTS = 6
+    GEMM_F16_256x256_QUAD = 6,  /* a 4-CTA cluster of two CTA pairs computing two  */
+                                /* vertically adjacent 256 x 256 tiles; each B     */
+                                /* byte is loaded once for both (TMA multicast),   */
+                                /* a quarter fewer L2 reads and requests; plain     */
+                                /* product only (with a fused epilogue the pair    */
+                                /* variant runs)                                    */
+    GEMM_F16_NUM_VARIANTS = 7
 };
 
 /*
@@ -198,8 +204,11 @@ enum {
  * least 16 k-blocks or into 4 or more; other M <= 128 take GEMM_F16_128x128;
  * larger M take the tile (128 x 128, 128 x 256 or the CTA pair) whose waves
  * over the SMs cost least, a wave of the wider tiles counting 1.15 / 1.1
- * waves of 128 x 128 tiles (1.5 / 1.5 when K <= 512).  Fills *cfg and
- * returns GEMM_OK, or GEMM_ERR_INVALID_ARG.
+ * waves of 128 x 128 tiles (1.5 / 1.5 when K <= 512).  When that is the pair
+ * and K % 64 != 0 (rows of A and B not a whole number of 128-byte lines, so
+ * every TMA row spans two L2 lines) with M > 256, GEMM_F16_256x256_QUAD
+ * replaces it.
+ * Fills *cfg and returns GEMM_OK, or GEMM_ERR_INVALID_ARG.
  */
 int gemm_f16_select(int M, int N, int K, int sm_count, gemm_f16_config *cfg);
 

@@ -158,7 +158,12 @@ def test_nvfp4_arguments_are_checked_on_the_host(lib):
 def test_f16_selector(lib):
     # the two fp16 workloads: CTA-pair 256 x 256 tiles, one CTA per SM
     assert g.gemm_f16_select(5376, 5376, 2048, 152)[:2] == (g.GEMM_F16_256x256_PAIR, 152)
-    assert g.gemm_f16_select(5000, 5376, 2040, 152)[:2] == (g.GEMM_F16_256x256_PAIR, 152)
+    # rows of 4080 bytes (K = 2040), off the 128-byte grid: two pairs sharing B
+    assert g.gemm_f16_select(5000, 5376, 2040, 152)[:2] == (g.GEMM_F16_256x256_QUAD, 152)
+    assert g.gemm_f16_select(5376, 5376, 2040, 152)[0] == g.GEMM_F16_256x256_QUAD
+    assert g.gemm_f16_select(8192, 8192, 8184, 152)[0] == g.GEMM_F16_256x256_QUAD
+    assert g.gemm_f16_select(2048, 2048, 1016, 152)[:2] == (g.GEMM_F16_256x256_QUAD, 128)
+    assert g.gemm_f16_select(5376, 5376, 2048, 152)[0] == g.GEMM_F16_256x256_PAIR   # whole lines
     assert g.gemm_f16_select(5376, 5376, 2048, 151)[:2] == (g.GEMM_F16_256x256_PAIR, 150)
     assert g.gemm_f16_select(8192, 8192, 8192, 152)[:2] == (g.GEMM_F16_256x256_PAIR, 152)
     # one row of A: the HBM-bound matrix-vector kernel, planned per SM
@@ -221,6 +226,14 @@ def test_f16_selector_rule_over_a_shape_grid(lib):
                         w = {g.GEMM_F16_128x128: cdiv(cdiv(M, 128) * cdiv(N, 128), sm),
                              g.GEMM_F16_128x256: (1.5 if short else 1.15) * cdiv(cdiv(M, 128) * cdiv(N, 256), sm),
                              g.GEMM_F16_256x256_PAIR: (1.5 if short else 1.1) * cdiv(cdiv(M, 256) * cdiv(N, 256), sm // 2)}
+                        quad = K % 64 != 0 and M > 256
+                        if v == g.GEMM_F16_256x256_QUAD:
+                            # the pair's waves were cheapest and the rows are
+                            # off the 128-byte grid
+                            assert quad
+                            v = g.GEMM_F16_256x256_PAIR
+                        else:
+                            assert not (v == g.GEMM_F16_256x256_PAIR and quad)
                         assert v in w and w[v] == min(w.values()), (M, N, K, sm, v, w)
                         assert 1 <= grid <= sm
 

@@ -87,6 +87,49 @@ def test_f16_nt_persistent_many_tiles_per_cta(variant, grid):
     check_f16(C, Cref, S, what=f"grid={grid} v{variant}")
 
 
+# Two CTA pairs sharing B (a 4-CTA cluster, B multicast to both pairs): each
+# tile is computed with the very MMAs of the pair kernel, so the two variants
+# must agree bit for bit, and both with the oracle.  Shapes: rows of A and B
+# off the 128-byte grid (K % 64 != 0), a cluster whose second pair falls
+# wholly past the last row (M = 600: its tile rows 768.. are empty), aligned
+# K, several tiles per cluster (grid of 2 or 3 clusters), a ragged N.
+@pytest.mark.parametrize("M,N,K,grid", [(600, 520, 136, 0), (1024, 768, 1000, 0),
+                                        (300, 300, 64, 0), (1536, 1280, 520, 8),
+                                        (1100, 700, 392, 12), (2048, 2048, 1016, 0)])
+def test_f16_nt_two_pairs_sharing_b_match_the_pair_kernel(M, N, K, grid):
+    A = wl.draw_f16((M, K), seed=M + 5, dist="normal")
+    B = wl.draw_f16((N, K), seed=N + 6, dist="normal")
+    C = _run(A, B, g.GEMM_F16_256x256_QUAD, grid)
+    Cref, S = oracle.gemm_f16_nt(A, B)
+    check_f16(C, Cref, S, what=f"quad {M}x{N}x{K} grid {grid}")
+    Cpair = _run(A, B, g.GEMM_F16_256x256_PAIR)
+    assert np.array_equal(C.view(np.uint16), Cpair.view(np.uint16)), \
+        "two pairs sharing B differ from the pair kernel"
+
+
+def test_f16_nt_two_pairs_sharing_b_repeatable():
+    # the same launch many times on one stream: every run bit-identical (a
+    # stage refilled before both pairs have read it would show as a change)
+    M, N, K = 2048, 2048, 2040
+    A = wl.draw_f16((M, K), seed=61, dist="normal")
+    B = wl.draw_f16((N, K), seed=62, dist="normal")
+    dA, dB = A.cuda(), B.cuda()
+    stream = torch.cuda.current_stream().cuda_stream
+    outs = []
+    for _ in range(20):
+        C = torch.empty((M, N), dtype=torch.float16, device="cuda")
+        g.gemm_f16_nt_ex(M, N, K, dA.data_ptr(), dB.data_ptr(), C.data_ptr(), stream,
+                         g.GEMM_F16_256x256_QUAD)
+        outs.append(C)
+    g.gemm_check_device_status(stream)
+    first = outs[0].cpu().numpy()
+    for i, C in enumerate(outs[1:]):
+        assert np.array_equal(C.cpu().numpy().view(np.uint16), first.view(np.uint16)), f"run {i + 1}"
+    rows, cols = wl.sample_positions(M, N, 65536, seed=63)
+    Cref, S = oracle.gemm_f16_nt_sampled(A, B, rows, cols)
+    check_f16(first[rows, cols], Cref, S, what="quad repeated")
+
+
 def test_f16_nt_small_integers_bit_exact():
     # entries in {-1, 0, 1}, K = 1024: every partial sum is an integer below
     # 2^11, exact in fp32 and in half, so the output must match bit for bit.

@@ -23,12 +23,14 @@ def _lib():
 
 
 # The first two shapes run the 1-CTA 128 x 128 kernel, the third the CTA-pair
-# kernel (enough 256 x 256 tiles for every SM pair), the last two the skinny
+# kernel (enough 256 x 256 tiles for every SM pair), the next two the skinny
 # kernel: one CTA per tile, and clusters of 8 CTAs splitting K (every CTA of
-# the cluster gives up, and they still meet at the cluster barriers).
+# the cluster gives up, and they still meet at the cluster barriers); the
+# last two CTA pairs sharing B (K = 1016: rows off the 128-byte grid), whose
+# stages also wait for the other pair's multicast.
 @pytest.mark.parametrize("M,N,K,skip", [(256, 512, 256, 0), (600, 700, 392, 3),
                                         (2560, 2560, 256, 1), (8, 77, 72, 1),
-                                        (8, 1000, 4096, 1)])
+                                        (8, 1000, 4096, 1), (2048, 2048, 1016, 1)])
 def test_missing_load_times_out_and_context_survives(M, N, K, skip):
     A = wl.draw_f16((M, K), seed=1)
     B = wl.draw_f16((N, K), seed=2)
