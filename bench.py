@@ -24,8 +24,13 @@ ranks is taken and rank 0 prints one JSON line.
 * ``cublas``: torch.matmul(A, Bᵀ) (cuBLAS, fp32 accumulation) timed the same
   way (after the same soak), plus its burst figure right after warm-up, as a
   reference line only.
-* ``sgemm``: the fp32 SGEMM at 4096³ (alpha 1, beta 0.5), a second line
-  against the FP32 FFMA peak.
+* ``configs``: one row per workload config -- the SGEMMs at 256³, 1024³ and
+  4096³ (alpha 1, beta 0.5) and the two fp16 shapes (5376 × 5376 × 2048 and
+  the tail shape 5000 × 5376 × 2040) -- each with its time, TFLOP/s, a
+  roofline against its peak (FP32 FFMA at the maximum and at the sampled
+  clock, or the bf16 tensor peak), the sampled clocks, the same-run cuBLAS
+  line (TF32 off for SGEMM) and the oracle's time on a row sample (for the
+  1024³ SGEMM also on one thread), with the host CPU model.
 * ``gemv``: the M = 1 matrix-vector product 1 × 16384 × 8192 against the
   measured HBM copy bandwidth.
 * ``skinny``: the same B against 16 rows of A (16 × 16384 × 8192, the skinny
@@ -40,7 +45,9 @@ ranks is taken and rank 0 prints one JSON line.
 
 N > 1 runs N independent replicas (one per GPU; the product has no exchange
 step), ``scaling: weak``.  ``--impl reference`` times the float64 oracle on
-the host cores instead (rank 0 only).
+the host cores instead (rank 0 only).  ``--case NAME [--calls C] [--variant V]
+[--cublas]`` launches one named workload C times and exits: the command the
+committed ncu summaries profile.
 """
 from __future__ import annotations
 

@@ -46,6 +46,7 @@ from ._binding import (  # noqa: F401
     GEMM_MXFP8_AUTO,
     GEMM_OK,
     GEMM_SGEMM_64x64,
+    GEMM_SGEMM_128x64,
     GEMM_SGEMM_128x128,
     GEMM_SGEMM_AUTO,
     LIB_PATH,

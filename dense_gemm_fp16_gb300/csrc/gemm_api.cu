@@ -180,15 +180,30 @@ int gemm_f16_select(int M, int N, int K, int sm_count, gemm_f16_config *cfg) {
 // Predicted time in microseconds of one SGEMM launch with a given tile and
 // split count.  The CTAs spread over the SMs, so the busiest SM runs
 // ceil(ctas / sms) of them, each over its K share; one 128 x 128 CTA costs
-// about 0.094 us per K element and one 64 x 64 CTA 0.041 us (13% less each
-// when two share an SM); a split adds the partial-slot writes, the fence and
-// the last CTA's pass over the slots.  The constants are GB300 measurements;
-// the model only has to rank the candidates.
+// about 0.094 us per K element, one 64 x 64 CTA 0.041 us (13% less each when
+// two share an SM) and one 128 x 64 CTA 0.062 us (20% less each when two
+// share an SM); a split adds the partial-slot writes, the fence and the last
+// CTA's pass over the slots.  The constants are GB300 measurements (the
+// 128 x 64 ones fitted to a 16-shape sweep of every tile at 1, 2, 4 and 8
+// shares: the picks land 0.3 % from the best measured on average, worst
+// 2.9 %, against 2.1 % and 13 % without that tile); the model only has to
+// rank the candidates.
+static void sgemm_tile(int variant, int *bm, int *bn) {
+    *bm = variant == GEMM_SGEMM_64x64 ? 64 : 128;
+    *bn = variant == GEMM_SGEMM_128x128 ? 128 : 64;
+}
+
 static double sgemm_cost(int variant, int M, int N, int sms, int splits, int chunk) {
     const bool big = variant == GEMM_SGEMM_128x128;
-    const int bm = big ? 128 : 64;
-    const double tiles = static_cast<double>(ceil_div(M, bm)) * static_cast<double>(ceil_div(N, bm));
+    int bm, bn;
+    sgemm_tile(variant, &bm, &bn);
+    const double tiles = static_cast<double>(ceil_div(M, bm)) * static_cast<double>(ceil_div(N, bn));
     const double per_sm = std::ceil(tiles * splits / sms);
+    if (variant == GEMM_SGEMM_128x64) {
+        double cost = per_sm * chunk * 0.062 * (per_sm >= 2 ? 0.8 : 1.0);
+        if (splits > 1) cost += 1.0 + 1.0 * splits;
+        return cost;
+    }
     const double share = (!big && per_sm >= 2) ? 0.87 : 1.0;
     double cost = per_sm * chunk * (big ? 0.094 : 0.041) * share;
     if (splits > 1) cost += big ? 2.0 + 1.0 * splits : 1.0 + 0.4 * splits;
@@ -207,8 +222,9 @@ static void sgemm_plan(int M, int N, int K, int sms, int fix_variant, int fix_sp
     *splits = 1;
     for (int v = GEMM_SGEMM_128x128; v < GEMM_SGEMM_NUM_VARIANTS; ++v) {
         if (fix_variant && v != fix_variant) continue;
-        const int bm = v == GEMM_SGEMM_128x128 ? 128 : 64;
-        const long long tiles = ceil_div(M, bm) * ceil_div(N, bm);
+        int bm, bn;
+        sgemm_tile(v, &bm, &bn);
+        const long long tiles = ceil_div(M, bm) * ceil_div(N, bn);
         const int smax = (K > 0 && tiles <= 2LL * sms) ? gb300::kSgemmMaxSplits : 1;
         const int s_lo = fix_splits ? fix_splits : 1, s_hi = fix_splits ? fix_splits : smax;
         for (int s = s_lo; s <= s_hi; ++s) {

@@ -163,7 +163,7 @@ struct SgemmLaunch {
     const float *B;
     float *C;
     cudaStream_t stream;
-    int variant;   // GEMM_SGEMM_128x128 or GEMM_SGEMM_64x64
+    int variant;   // GEMM_SGEMM_128x128, GEMM_SGEMM_64x64 or GEMM_SGEMM_128x64
     int splits;    // split-K depth, 1 = none (sgemm_split_chunk gives the shares)
 };
 

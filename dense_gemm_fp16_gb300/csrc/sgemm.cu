@@ -431,6 +431,7 @@ int sgemm_launch(const SgemmLaunch &L, std::string &err) {
     switch (L.variant) {
         case GEMM_SGEMM_128x128: return launch_pipe<128, 128, 16, 8, 16, 3, 2, false>(L, err);
         case GEMM_SGEMM_64x64: return launch_pipe<64, 64, 16, 4, 4, 3, 2, true>(L, err);
+        case GEMM_SGEMM_128x64: return launch_pipe<128, 64, 16, 8, 8, 3, 2, false>(L, err);
         default: err = "unknown sgemm variant"; return GEMM_ERR_INVALID_ARG;
     }
 }

@@ -412,13 +412,14 @@ enum {
     GEMM_SGEMM_AUTO = 0,
     GEMM_SGEMM_128x128 = 1,     /* 128 x 128 CTA tile, 8 x 16 per thread, BK 16, 3 stages */
     GEMM_SGEMM_64x64 = 2,       /* 64 x 64 CTA tile, 4 x 4 per thread, BK 16, 3 stages   */
-    GEMM_SGEMM_NUM_VARIANTS = 3
+    GEMM_SGEMM_128x64 = 3,      /* 128 x 64 CTA tile, 8 x 8 per thread, BK 16, 3 stages  */
+    GEMM_SGEMM_NUM_VARIANTS = 4
 };
 
-/* Shape-keyed choice of the SGEMM tile and split count (host logic only):
- * the pair with the lowest predicted time, where a launch takes as long as
- * its busiest SM (ceil(CTAs / sm_count) CTAs, each over its K share) plus the
- * cost of adding the split partials.  Splits are only considered when the
+/* Shape-keyed choice of the SGEMM tile (128 x 128, 64 x 64 or 128 x 64) and
+ * split count (host logic only): the pair with the lowest predicted time,
+ * where a launch takes as long as its busiest SM (ceil(CTAs / sm_count) CTAs,
+ * each over its K share) plus the cost of adding the split partials.  Splits are only considered when the
  * tiles number at most 2 * sm_count.  Fills cfg->variant and cfg->splits
  * (>= 1). */
 int gemm_sgemm_select(int M, int N, int K, int sm_count, gemm_sgemm_config *cfg);

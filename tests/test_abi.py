@@ -326,6 +326,9 @@ def test_sgemm_selector(lib):
     assert sel(512, 512, 8192, 152) == (g.GEMM_SGEMM_128x128, 8)
     assert sel(256, 256, 4096, 152) == (g.GEMM_SGEMM_64x64, 8)
     assert sel(1536, 1536, 1536, 152)[1] == 1                       # 144 tiles: one wave already
+    # the 128 x 64 tile where its splits fill the SMs better (measured 4-12 % faster)
+    assert sel(768, 768, 768, 152) == (g.GEMM_SGEMM_128x64, 4)
+    assert sel(8192, 64, 1024, 152) == (g.GEMM_SGEMM_128x64, 4)
     # no K: nothing to split
     assert sel(4096, 4096, 0, 152)[1] == 1
     assert sel(16, 16, 16, 152)[1] == 1
@@ -336,12 +339,13 @@ def test_sgemm_selector(lib):
 @pytest.mark.parametrize("sms", [1, 148, 152])
 def test_sgemm_selector_plans_are_valid(lib, M, N, K, sms):
     variant, splits = g.gemm_sgemm_select(M, N, K, sms)
-    assert variant in (g.GEMM_SGEMM_128x128, g.GEMM_SGEMM_64x64)
+    assert variant in (g.GEMM_SGEMM_128x128, g.GEMM_SGEMM_64x64, g.GEMM_SGEMM_128x64)
     assert 1 <= splits <= 8
     # each share of K is at least 64 deep, and splits only come with few tiles
     assert splits == 1 or splits <= -(-K // 64)
-    bm = 128 if variant == g.GEMM_SGEMM_128x128 else 64
-    assert splits == 1 or -(-M // bm) * -(-N // bm) <= 2 * sms
+    bm = 64 if variant == g.GEMM_SGEMM_64x64 else 128
+    bn = 128 if variant == g.GEMM_SGEMM_128x128 else 64
+    assert splits == 1 or -(-M // bm) * -(-N // bn) <= 2 * sms
 
 
 def test_product_path_never_imports_the_oracle():

@@ -57,7 +57,7 @@ def test_sgemm_4096_alpha_beta_sampled():
     check_sgemm(C[rows, cols], Cref, S, what="sgemm_4096")
 
 
-@pytest.mark.parametrize("variant", [g.GEMM_SGEMM_128x128, g.GEMM_SGEMM_64x64])
+@pytest.mark.parametrize("variant", [g.GEMM_SGEMM_128x128, g.GEMM_SGEMM_64x64, g.GEMM_SGEMM_128x64])
 @pytest.mark.parametrize("M,N,K,alpha,beta", [
     (100, 70, 33, 1.0, 0.0),       # ragged everything, scalar loads (K, N odd-ish)
     (257, 129, 17, -1.5, 0.25),    # one past the tile edges
@@ -127,7 +127,7 @@ def test_sgemm_tensor_wrapper():
     check_sgemm(C.cpu().numpy(), Cref, S, what="wrapper")
 
 
-V1, V2 = g.GEMM_SGEMM_128x128, g.GEMM_SGEMM_64x64
+V1, V2, V3 = g.GEMM_SGEMM_128x128, g.GEMM_SGEMM_64x64, g.GEMM_SGEMM_128x64
 
 
 @pytest.mark.parametrize("M,N,K,alpha,beta,variant,splits", [
@@ -140,6 +140,9 @@ V1, V2 = g.GEMM_SGEMM_128x128, g.GEMM_SGEMM_64x64
     (64, 1024, 4096, 1.5, 0.0, V2, 7),      # skinny M
     (96, 80, 150, 1.0, 1.0, V1, 8),         # short K: 8 requested, 3 shares of >= 64
     (256, 256, 4096, 1.0, 0.0, 0, 0),
+    (1024, 1024, 1024, 1.0, 0.5, V3, 1),    # the 128 x 64 tile over the whole K
+    (300, 200, 1000, -2.0, 0.25, V3, 4),    # ... split, ragged
+    (130, 70, 4099, 0.5, 0.0, V3, 3),       # ... element-wise loads, a partial tile column
 ])
 def test_sgemm_split_k(M, N, K, alpha, beta, variant, splits):
     # Each tile's K is shared over several CTAs; the last to finish adds the
@@ -161,7 +164,7 @@ def test_sgemm_split_k_matches_unsplit_within_rounding():
     A = wl.draw_f32((M, K), seed=41)
     B = wl.draw_f32((K, N), seed=42)
     Cref, S = oracle.sgemm(A, B, 1.0, 0.0, None)
-    for v in (V1, V2):
+    for v in (V1, V2, V3):
         plain = _run(A, B, None, 1.0, 0.0, v, splits=1)
         for sp in range(1, 9):
             C = _run(A, B, None, 1.0, 0.0, v, splits=sp)
