@@ -107,6 +107,17 @@ def test_f16_nt_two_pairs_sharing_b_match_the_pair_kernel(M, N, K, grid):
         "two pairs sharing B differ from the pair kernel"
 
 
+def test_f16_nt_two_pairs_sharing_b_scalar_store_paths():
+    # N % 8 != 0 and a C offset by one element take the per-element epilogue
+    # (no TMA store) in both pairs of the cluster.
+    for (M, N, K), pad in [((700, 250, 136), 64), ((530, 264, 200), 1)]:
+        A = wl.draw_f16((M, K), seed=M + 7, dist="normal")
+        B = wl.draw_f16((N, K), seed=N + 8, dist="normal")
+        C = _run(A, B, g.GEMM_F16_256x256_QUAD, pad=pad)
+        Cref, S = oracle.gemm_f16_nt(A, B)
+        check_f16(C, Cref, S, what=f"quad scalar {M}x{N}x{K} pad={pad}")
+
+
 def test_f16_nt_two_pairs_sharing_b_repeatable():
     # the same launch many times on one stream: every run bit-identical (a
     # stage refilled before both pairs have read it would show as a change)
