@@ -56,6 +56,7 @@ from ._binding import (  # noqa: F401
     gemm_check_device_status,
     gemm_debug_f16_nt_skip_load,
     gemm_debug_skinny_plan,
+    gemm_debug_skinny_parts,
     gemm_debug_last_pair_launch,
     gemm_debug_blockscaled_skip_load,
     gemm_debug_f16_nt_stream_k_skip_publish,

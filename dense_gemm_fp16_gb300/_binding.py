@@ -121,6 +121,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gemm_debug_skinny_plan.argtypes = [i, i, i, i, ctypes.POINTER(i), ctypes.POINTER(i),
                                                ctypes.POINTER(i)]
         lib.gemm_debug_skinny_plan.restype = i
+        lib.gemm_debug_skinny_parts.argtypes = [i, i, i, i]
+        lib.gemm_debug_skinny_parts.restype = i
         lib.gemm_debug_last_pair_launch.argtypes = [ctypes.POINTER(i)] * 4
         lib.gemm_debug_last_pair_launch.restype = i
         lib.gemm_debug_blockscaled_skip_load.argtypes = [i, i, i, i, vp, vp, vp, vp, vp, vp,
@@ -272,6 +274,14 @@ def gemm_debug_last_pair_launch():
     if load_library().gemm_debug_last_pair_launch(*[ctypes.byref(v) for v in vals]) != 0:
         return None
     return tuple(v.value for v in vals)
+
+
+def gemm_debug_skinny_parts(M, N, K, ctas):
+    """Clusters per tile the skinny variant plans (host logic only)."""
+    parts = load_library().gemm_debug_skinny_parts(M, N, K, ctas)
+    if parts < 0:
+        raise ValueError(f"bad plan arguments M={M} N={N} K={K} ctas={ctas}")
+    return parts
 
 
 def gemm_debug_skinny_plan(M, N, K, ctas):

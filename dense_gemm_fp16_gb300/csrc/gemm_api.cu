@@ -384,6 +384,14 @@ int gemm_debug_skinny_plan(int M, int N, int K, int ctas, int *rows, int *groups
     return p.splits;
 }
 
+// Test hook declared in gemm_testing.h: clusters per tile of the same plan.
+int gemm_debug_skinny_parts(int M, int N, int K, int ctas) {
+    if (M < 1 || N < 1 || K < 0 || ctas < 1) return -1;
+    gb300::SkinnyPlan p;
+    gb300::skinny_plan(M, N, K, ctas, nullptr, &p);
+    return p.parts;
+}
+
 // ---------------------------------------------------------------------------
 // Block-scaled FP8 (MXFP8)
 // ---------------------------------------------------------------------------

@@ -138,11 +138,12 @@ int skinny_ctas_per_sm();
 // tile's K range in `splits` shares of `kb_per_split` 64-deep k-blocks (the
 // last may be shorter), one CTA per share, a tile's shares one cluster.
 struct SkinnyPlan {
-    int splits;        // 1, 2, 4 or 8
+    int splits;        // 1, 2, 4 or 8: CTAs of a cluster sharing a tile's K range
     int rows;          // a multiple of 8, at most 128
     int groups;        // ceil(N / rows)
-    int kb_per_split;
+    int kb_per_split;  // k-blocks per share (a share is one CTA)
     int mtiles;        // 1 for M <= 128, else ceil(M / 128)
+    int parts = 1;     // clusters per tile: its K range in parts x splits shares
 };
 
 // The plan for an M x N product of depth K on `ctas` CTA slots; cap[l] is

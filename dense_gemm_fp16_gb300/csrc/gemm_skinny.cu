@@ -25,6 +25,12 @@
 // ("异步拷贝与 Hopper/Blackwell 新特性", section "线程块集群与分布式共享内存
 // sm_90+": CTAs of a cluster synchronise and read one another's shared
 // memory), so results do not depend on timing and no share goes through HBM.
+// When even 8-CTA clusters leave most SMs idle (a few tiles over a very long
+// K), each tile's K range goes to several clusters ("parts"): every cluster
+// sums its own shares as above and writes that fp32 partial to a workspace,
+// and the cluster that finishes the tile last (a per-slice counter tagged
+// with the launch's sequence number, so nothing is reset between launches)
+// adds the parts in order and stores.  Nothing waits on another cluster.
 // Every wait is bounded as in the other kernels.
 #include <cuda.h>
 #include <cuda_fp16.h>
@@ -84,7 +90,34 @@ struct SkArgs {
     uint64_t timeout_ns;
     Epi epi;           // fused epilogue, applied where the fp32 sum is rounded
     int debug_skip_kblock;  // test hook: every CTA leaves out this k-block of its share (-1: none)
+    // Clusters per tile (1: none): cluster p of a tile writes slice r of its
+    // sum to ws[((tile * splits + r) * parts + p) * slice4 + i] (float4 i of
+    // the slice) and bumps ctr[tile * splits + r], whose high 32 bits hold
+    // the launch's `seq` and low 32 bits the parts counted so far.
+    int parts;
+    int slice4;                // float4 of a CTA's slice of the tile
+    float4 *ws;
+    unsigned long long *ctr;
+    uint32_t seq;              // never 0
 };
+
+// Count one more part of this launch on a tagged counter; returns how many
+// parts, this one included, have arrived (a stale count from an earlier
+// launch counts as none).  Other parts of the same launch are the only
+// contenders, so the loop ends after at most `parts` rounds; the bound is a
+// guard.
+__device__ __forceinline__ int count_part(unsigned long long *ctr, uint32_t seq) {
+    unsigned long long cur = atomicAdd(ctr, 0ull);
+    for (int i = 0; i < 1 << 16; ++i) {
+        const unsigned long long want = (static_cast<uint32_t>(cur >> 32) == seq)
+                                            ? cur + 1ull
+                                            : ((static_cast<unsigned long long>(seq) << 32) | 1ull);
+        const unsigned long long prev = atomicCAS(ctr, cur, want);
+        if (prev == cur) return static_cast<int>(want & 0xffffffffull);
+        cur = prev;
+    }
+    return 0;
+}
 
 // One output through the epilogue and rounded to half.
 __device__ __forceinline__ __half skinny_out(const Epi &e, float x, int m, int n, int N) {
@@ -145,10 +178,12 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     // the B box is `rows` rows tall; the stage's rows past it keep stale data,
     // which only reaches TMEM lanes the epilogue never reads
     const uint32_t stage_tx = static_cast<uint32_t>(args.rows + MN) * (kSkBK * 2);
-    const int split = blockIdx.y;  // share of K
+    const int share = blockIdx.y;                // share of K (parts x splits of them per tile)
+    const int split = share % args.splits;        // this CTA's rank in its cluster
+    const int part = share / args.splits;         // which cluster of the tile
     const int m0 = static_cast<int>(blockIdx.z) * MN;  // first row of A (and of C) of this tile
     const int mt = args.M - m0 < MN ? args.M - m0 : MN;  // its rows of A
-    const int kb0 = split * args.kb_per_split;
+    const int kb0 = share * args.kb_per_split;
     const int kb1 = kb0 + args.kb_per_split < args.num_kb ? kb0 + args.kb_per_split : args.num_kb;
 
     if (threadIdx.x == 0) {
@@ -315,15 +350,55 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         const int g0 = split * per;
         const int g1 = g0 + per < groups ? g0 + per : groups;
         const bool vec = (args.N & 3) == 0 && (reinterpret_cast<uintptr_t>(args.C) & 7u) == 0;
-        for (int gi = g0 + static_cast<int>(threadIdx.x); gi < g1; gi += kSkThreads) {
-            const uint32_t at = sbase + static_cast<uint32_t>(gi) * 16u;
-            float4 sum = ld_dsmem_f4(mapa_shared(at, 0));
-            for (int sp = 1; sp < args.splits; ++sp) {
-                const float4 x = ld_dsmem_f4(mapa_shared(at, static_cast<uint32_t>(sp)));
-                sum.x += x.x;
-                sum.y += x.y;
-                sum.z += x.z;
-                sum.w += x.w;
+        const int tile_slice = (static_cast<int>(blockIdx.z) * static_cast<int>(gridDim.x) + tile) * args.splits + split;
+        float4 *slices = args.parts > 1 ? args.ws + static_cast<size_t>(tile_slice) * args.parts * args.slice4
+                                        : nullptr;
+        bool store = args.parts == 1;
+        if (args.parts > 1) {
+            // this cluster's part of the slice to the workspace, then count it
+            for (int gi = g0 + static_cast<int>(threadIdx.x); gi < g1; gi += kSkThreads) {
+                const uint32_t at = sbase + static_cast<uint32_t>(gi) * 16u;
+                float4 sum = ld_dsmem_f4(mapa_shared(at, 0));
+                for (int sp = 1; sp < args.splits; ++sp) {
+                    const float4 x = ld_dsmem_f4(mapa_shared(at, static_cast<uint32_t>(sp)));
+                    sum.x += x.x;
+                    sum.y += x.y;
+                    sum.z += x.z;
+                    sum.w += x.w;
+                }
+                slices[static_cast<size_t>(part) * args.slice4 + (gi - g0)] = sum;
+            }
+            __threadfence();
+            __syncthreads();
+            __shared__ int last;
+            if (threadIdx.x == 0) last = count_part(args.ctr + tile_slice, args.seq) == args.parts;
+            __syncthreads();
+            store = last != 0;
+            if (store) __threadfence();  // every part's slice is visible to this CTA
+        }
+        for (int gi = g0 + static_cast<int>(threadIdx.x); store && gi < g1; gi += kSkThreads) {
+            float4 sum;
+            if (args.parts > 1) {
+                // the parts in order p = 0, 1, ...: the sum does not depend on
+                // which cluster finished last
+                sum = __ldcg(&slices[gi - g0]);
+                for (int p = 1; p < args.parts; ++p) {
+                    const float4 x = __ldcg(&slices[static_cast<size_t>(p) * args.slice4 + (gi - g0)]);
+                    sum.x += x.x;
+                    sum.y += x.y;
+                    sum.z += x.z;
+                    sum.w += x.w;
+                }
+            } else {
+                const uint32_t at = sbase + static_cast<uint32_t>(gi) * 16u;
+                sum = ld_dsmem_f4(mapa_shared(at, 0));
+                for (int sp = 1; sp < args.splits; ++sp) {
+                    const float4 x = ld_dsmem_f4(mapa_shared(at, static_cast<uint32_t>(sp)));
+                    sum.x += x.x;
+                    sum.y += x.y;
+                    sum.z += x.z;
+                    sum.w += x.w;
+                }
             }
             const int m = m0 + gi / (kSkBM / 4);
             const int n = row0 + (gi % (kSkBM / 4)) * 4;
@@ -387,6 +462,59 @@ int max_clusters(int size, std::string &err) {
     return n;
 }
 
+// Workspace of the multi-cluster split, per (device, stream): partial slices
+// and tagged counters, grown on demand, with the stream's launch sequence
+// number (counters are cleared only when it wraps).  Calls on one stream run
+// in order, so a stream has one user at a time.
+struct SkWs {
+    float4 *ws = nullptr;
+    unsigned long long *ctr = nullptr;
+    size_t ws_bytes = 0;
+    int counters = 0;
+    uint32_t seq = 0;
+};
+
+int skinny_workspace(cudaStream_t stream, size_t ws_bytes, int counters, SkWs **out, std::string &err) {
+    static std::mutex mu;
+    static std::map<std::pair<int, cudaStream_t>, SkWs> cache;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        err = std::string("cudaGetDevice: ") + cudaGetErrorString(e);
+        return GEMM_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    SkWs &w = cache[{dev, stream}];
+    if (w.ws_bytes < ws_bytes || w.counters < counters) {
+        // the stream may still be running a launch that uses the old buffers
+        e = cudaStreamSynchronize(stream);
+        if (e == cudaSuccess && w.ws) e = cudaFree(w.ws);
+        if (e == cudaSuccess && w.ctr) e = cudaFree(w.ctr);
+        w = SkWs{};
+        if (e == cudaSuccess) e = cudaMalloc(&w.ws, ws_bytes);
+        if (e == cudaSuccess) e = cudaMalloc(&w.ctr, static_cast<size_t>(counters) * sizeof(unsigned long long));
+        if (e == cudaSuccess)
+            e = cudaMemsetAsync(w.ctr, 0, static_cast<size_t>(counters) * sizeof(unsigned long long), stream);
+        if (e != cudaSuccess) {
+            err = std::string("skinny split workspace: ") + cudaGetErrorString(e);
+            w = SkWs{};
+            return GEMM_ERR_CUDA;
+        }
+        w.ws_bytes = ws_bytes;
+        w.counters = counters;
+    }
+    if (++w.seq == 0) {  // the sequence number wrapped: no counter may hold a live tag
+        e = cudaMemsetAsync(w.ctr, 0, static_cast<size_t>(w.counters) * sizeof(unsigned long long), stream);
+        if (e != cudaSuccess) {
+            err = std::string("skinny split counter reset: ") + cudaGetErrorString(e);
+            return GEMM_ERR_CUDA;
+        }
+        w.seq = 1;
+    }
+    *out = &w;
+    return GEMM_OK;
+}
+
 template <int MN>
 int launch_mn(const SkinnyLaunch &L, std::string &err) {
     constexpr int S = sk_stages<MN>();
@@ -417,8 +545,37 @@ int launch_mn(const SkinnyLaunch &L, std::string &err) {
     skinny_plan(L.M, L.N, L.K, L.ctas, cap, &plan);
     const int num_kb = (L.K + kSkBK - 1) / kSkBK;
     const int splits = plan.splits;
+    // Several clusters per tile need the workspace; under stream capture (a
+    // replayed graph would reuse this launch's sequence number) the tile
+    // stays with one cluster.
+    float4 *ws = nullptr;
+    unsigned long long *ctr = nullptr;
+    uint32_t seq = 0;
+    const int slice4 = (MN * (kSkBM / 4) + splits - 1) / splits;
+    if (plan.parts > 1) {
+        cudaStreamCaptureStatus cap_status = cudaStreamCaptureStatusNone;
+        e = cudaStreamIsCapturing(L.stream, &cap_status);
+        if (e != cudaSuccess) {
+            err = std::string("cudaStreamIsCapturing: ") + cudaGetErrorString(e);
+            return GEMM_ERR_CUDA;
+        }
+        if (cap_status != cudaStreamCaptureStatusNone) {
+            plan.parts = 1;
+            plan.kb_per_split = (num_kb + splits - 1) / splits;
+        } else {
+            const int slices = plan.groups * plan.mtiles * splits;
+            SkWs *w = nullptr;
+            const int st = skinny_workspace(
+                L.stream, static_cast<size_t>(slices) * plan.parts * slice4 * sizeof(float4), slices, &w, err);
+            if (st != GEMM_OK) return st;
+            ws = w->ws;
+            ctr = w->ctr;
+            seq = w->seq;
+        }
+    }
     const SkArgs args{static_cast<__half *>(L.C), L.M, L.N, L.K, num_kb, plan.kb_per_split, splits, plan.rows,
-                      L.timeout_ns, make_epi(L.epi, L.N), L.debug_skip_kblock};
+                      L.timeout_ns, make_epi(L.epi, L.N), L.debug_skip_kblock, plan.parts, slice4, ws, ctr,
+                      seq};
     CUtensorMap tmB, tmA;
     if (!encode_map(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, L.B, L.N, L.K, plan.rows, kSkBK, err) ||
         !encode_map(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, L.A, L.M, L.K, MN, kSkBK, err))
@@ -431,7 +588,7 @@ int launch_mn(const SkinnyLaunch &L, std::string &err) {
     attr[1].val.clusterDim.x = 1;
     attr[1].val.clusterDim.y = splits;
     attr[1].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(plan.groups, splits, plan.mtiles);
+    cfg.gridDim = dim3(plan.groups, splits * plan.parts, plan.mtiles);
     cfg.blockDim = dim3(kSkThreads);
     cfg.dynamicSmemBytes = T::kSmemBytes;
     cfg.stream = L.stream;
@@ -476,8 +633,20 @@ void skinny_plan(int M, int N, int K, int ctas, const int *cap, SkinnyPlan *plan
         rows = static_cast<int>((N + slots - 1) / slots);
         rows = (rows + 7) & ~7;
     }
-    const int kbs = (num_kb + s - 1) / s;
-    *plan = SkinnyPlan{s, rows, (N + rows - 1) / rows, kbs > 0 ? kbs : 1, mtiles};
+    // Still most SMs idle with the largest cluster (a few tiles over a very
+    // long K): give each tile several clusters, as many as fill the SMs at
+    // once (at most 8), each share still at least 8 k-blocks.
+    int parts = 1;
+    if (s == 8) {
+        int fit = ctas / 8;
+        if (cap && cap[3] < fit) fit = cap[3];
+        long long p = tiles > 0 ? fit / tiles : 1;
+        if (p > 8) p = 8;
+        if (p > num_kb / (8 * s)) p = num_kb / (8 * s);
+        if (p >= 2) parts = static_cast<int>(p);
+    }
+    const int kbs = (num_kb + s * parts - 1) / (s * parts);
+    *plan = SkinnyPlan{s, rows, (N + rows - 1) / rows, kbs > 0 ? kbs : 1, mtiles, parts};
 }
 
 int skinny_launch(const SkinnyLaunch &L, std::string &err) {

@@ -44,6 +44,17 @@ int gemm_debug_f16_nt_skip_load(int M, int N, int K, const void *A, const void *
 int gemm_debug_skinny_plan(int M, int N, int K, int ctas, int *rows, int *groups, int *kb_per_split);
 
 /*
+ * How many clusters the same plan gives each tile: when even 8-CTA clusters
+ * leave most slots idle, each tile's K range goes to several clusters
+ * (parts), as many as the slots hold at once, at most 8, each share still at
+ * least 8 k-blocks; *kb_per_split above is then per share of parts x 8.  The
+ * parts' fp32 sums meet in a workspace the library allocates per device and
+ * stream (skipped under stream capture, where each tile keeps one cluster).
+ * Returns the parts (1 = one cluster per tile), or -1 for bad arguments.
+ */
+int gemm_debug_skinny_parts(int M, int N, int K, int ctas);
+
+/*
  * A block-scaled product (fmt 0: gemm_mxfp8_nt_ex, 1: gemm_nvfp4_nt_ex with
  * alpha = 1) with one k-block deliberately never loaded: each CTA (the even
  * CTA of each pair, for the pair variants) neither arms nor loads k-block

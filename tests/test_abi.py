@@ -243,7 +243,8 @@ def test_skinny_plan(lib):
     assert g.gemm_debug_skinny_plan(1, 8192, 8192, 152) == (2, 128, 64, 64)
     assert g.gemm_debug_skinny_plan(1, 16384, 8192, 152) == (1, 128, 128, 128)  # no room to split
     assert g.gemm_debug_skinny_plan(1, 4096, 4096, 152) == (4, 128, 32, 16)
-    assert g.gemm_debug_skinny_plan(1, 1000, 12008, 152) == (8, 128, 8, 24)     # 188 k-blocks
+    assert g.gemm_debug_skinny_plan(1, 1000, 12008, 152) == (8, 128, 8, 12)     # 188 k-blocks, 2 parts
+    assert g.gemm_debug_skinny_parts(1, 1000, 12008, 152) == 2
     assert g.gemm_debug_skinny_plan(1, 4000, 2056, 152) == (4, 128, 32, 9)      # 33 k-blocks: ragged
     assert g.gemm_debug_skinny_plan(1, 19456, 1024, 152) == (1, 128, 152, 16)   # exactly one wave
     assert g.gemm_debug_skinny_plan(1, 28672, 8192, 152) == (1, 96, 299, 128)   # two even waves
@@ -254,6 +255,12 @@ def test_skinny_plan(lib):
     assert g.gemm_debug_skinny_plan(512, 512, 32768, 152) == (8, 128, 4, 64)    # 4 x 4 tiles
     assert g.gemm_debug_skinny_plan(2048, 2048, 8192, 152) == (1, 128, 16, 128)  # 256 tiles
     assert g.gemm_debug_skinny_plan(300, 20000, 64, 152)[1] == 128             # no wave evening
+    # a few tiles over a very long K: several 8-CTA clusters per tile
+    assert g.gemm_debug_skinny_plan(256, 256, 65536, 152) == (8, 128, 2, 32)    # 4 tiles x 4 parts
+    assert g.gemm_debug_skinny_parts(256, 256, 65536, 152) == 4
+    assert g.gemm_debug_skinny_parts(128, 128, 65536, 152) == 8                 # 1 tile, at most 8
+    assert g.gemm_debug_skinny_parts(512, 512, 32768, 152) == 1                 # 16 tiles: no room
+    assert g.gemm_debug_skinny_parts(1, 4096, 4096, 152) == 1                   # 4 shares: no parts
     with pytest.raises(ValueError):
         g.gemm_debug_skinny_plan(1, 0, 64, 152)
 
@@ -268,6 +275,7 @@ def test_skinny_plan_properties(lib):
         for K in (0, 8, 64, 512, 520, 4096, 12008, 65536):
             for ctas in (1, 19, 152, 304):
                 s, rows, groups, kb = g.gemm_debug_skinny_plan(1, N, K, ctas)
+                parts = g.gemm_debug_skinny_parts(1, N, K, ctas)
                 tiles, nkb = -(-N // 128), -(-K // 64)
                 assert s in (1, 2, 4, 8)
                 if s > 1:
@@ -280,7 +288,14 @@ def test_skinny_plan_properties(lib):
                     assert rows % 8 == 0 and rows <= 128 and rows * waves * ctas >= N
                     assert rows - 8 < -(-N // (waves * ctas))
                 assert groups == -(-N // rows) and (groups - 1) * rows < N
-                assert kb == max(1, -(-nkb // s)) and kb * s >= nkb
+                # parts: only with 8-CTA clusters, all resident, shares of 8+
+                # k-blocks, at most 8, and one more would break one of these
+                assert 1 <= parts <= 8 and (parts == 1 or s == 8)
+                if parts > 1:
+                    assert tiles * 8 * parts <= ctas and nkb // (8 * parts) >= 8
+                if s == 8:
+                    assert parts == 8 or tiles * 8 * (parts + 1) > ctas or nkb // (8 * (parts + 1)) < 8
+                assert kb == max(1, -(-nkb // (s * parts))) and kb * s * parts >= nkb
 
 
 def test_f16_selector_raster(lib):

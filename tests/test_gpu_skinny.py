@@ -184,3 +184,50 @@ def test_skinny_several_row_tiles_of_a(M, N, K):
     B = wl.draw_f16((N, K), seed=N + 7, dist="normal")
     Cref, S = oracle.gemm_f16_nt(A, B)
     check_f16(_run(A, B), Cref, S, what=f"skinny {M}x{N}x{K}")
+
+
+# A few tiles over a very long K: each tile's K range goes to several 8-CTA
+# clusters (parts), whose fp32 sums meet in a workspace; the last cluster of
+# a tile adds them in part order.  (M, N, K) -> parts on 152 SMs: 4 tiles x 4,
+# one tile x 8, 4 tiles of 8 rows x 4.
+PARTS_SHAPES = [(256, 256, 65536), (128, 128, 65536), (8, 512, 32768)]
+
+
+@pytest.mark.parametrize("M,N,K", PARTS_SHAPES)
+def test_skinny_several_clusters_per_tile(M, N, K):
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert g.gemm_debug_skinny_parts(M, N, K, sms) > 1
+    A = wl.draw_f16((M, K), seed=M + 71, dist="normal")
+    B = wl.draw_f16((N, K), seed=N + 72, dist="normal")
+    Cref, S = oracle.gemm_f16_nt(A, B)
+    first = _run(A, B)
+    check_f16(first, Cref, S, what=f"skinny parts {M}x{N}x{K}")
+    for rep in range(3):   # the parts add in a fixed order: the same bits every time
+        assert np.array_equal(_run(A, B).view(np.uint16), first.view(np.uint16)), f"rep {rep}"
+
+
+def test_skinny_several_clusters_per_tile_fused_and_captured():
+    M, N, K = 256, 256, 65536
+    A = wl.draw_f16((M, K), seed=81, dist="normal")
+    B = wl.draw_f16((N, K), seed=82, dist="normal")
+    bias = wl.draw_f16((N,), seed=83, dist="normal")
+    R = wl.draw_f16((M, N), seed=84, dist="normal")
+    dA, dB, dbias, dR = A.cuda(), B.cuda(), bias.cuda(), R.cuda()
+    buf, C = _guarded(M, N)
+    stream = torch.cuda.current_stream().cuda_stream
+    g.gemm_f16_nt_fused(M, N, K, dA.data_ptr(), dB.data_ptr(), C.data_ptr(), 0.5, 1.0,
+                        dbias.data_ptr(), dR.data_ptr(), g.ACTIVATIONS["silu"], stream, g.GEMM_F16_SKINNY)
+    g.gemm_check_device_status(stream)
+    Y, S = oracle.gemm_f16_nt_epilogue(A, B, alpha=0.5, bias=bias, beta=1.0, R=R, act="silu")
+    check_f16_epilogue(_unguard(buf, M, N), Y, S, what="skinny parts fused")
+    # under stream capture the tile keeps one cluster (no workspace use)
+    Cg = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    with torch.cuda.graph(graph, stream=side):
+        g.gemm_f16_nt_ex(M, N, K, dA.data_ptr(), dB.data_ptr(), Cg.data_ptr(), side.cuda_stream,
+                         g.GEMM_F16_SKINNY)
+    graph.replay()
+    torch.cuda.synchronize()
+    Cref, S = oracle.gemm_f16_nt(A, B)
+    check_f16(Cg.cpu().numpy(), Cref, S, what="skinny parts captured")

@@ -26,11 +26,14 @@ def _lib():
 # kernel (enough 256 x 256 tiles for every SM pair), the next two the skinny
 # kernel: one CTA per tile, and clusters of 8 CTAs splitting K (every CTA of
 # the cluster gives up, and they still meet at the cluster barriers); the
-# last two CTA pairs sharing B (K = 1016: rows off the 128-byte grid), whose
-# stages also wait for the other pair's multicast.
+# sixth two CTA pairs sharing B (K = 1016: rows off the 128-byte grid), whose
+# stages also wait for the other pair's multicast; the last the skinny kernel
+# with 4 clusters per tile, whose parts still meet in the workspace after the
+# timeout, and whose tagged counters must not mislead the next call.
 @pytest.mark.parametrize("M,N,K,skip", [(256, 512, 256, 0), (600, 700, 392, 3),
                                         (2560, 2560, 256, 1), (8, 77, 72, 1),
-                                        (8, 1000, 4096, 1), (2048, 2048, 1016, 1)])
+                                        (8, 1000, 4096, 1), (2048, 2048, 1016, 1),
+                                        (8, 512, 32768, 1)])
 def test_missing_load_times_out_and_context_survives(M, N, K, skip):
     A = wl.draw_f16((M, K), seed=1)
     B = wl.draw_f16((N, K), seed=2)
