@@ -28,6 +28,9 @@
  *    of about 256 KB per CTA pair (19 MiB on a 152-SM GB300), allocated once
  *    per device and stream by the first call that splits and kept for the
  *    life of the process; gemm_f16_nt_stream_k_noalloc never allocates.
+ *    Likewise the skinny variant's split over several clusters per tile
+ *    (GEMM_F16_SKINNY) keeps its fp32 partial sums in a workspace allocated
+ *    once per device and stream (a few hundred KB; not under stream capture).
  *    C must not overlap A or B.
  *  - Asynchrony: work is enqueued on `stream` (a cudaStream_t; NULL means
  *    the legacy default stream) on the calling thread's current device.  The
@@ -186,7 +189,10 @@ enum {
                                 /* distributed shared memory (no workspace; the    */
                                 /* tile kernels' numerics).  Chosen for 2 <= M <=  */
                                 /* 64, and for any M whose tiles it splits in two  */
-                                /* shares of 16+ k-blocks or in four or more       */
+                                /* shares of 16+ k-blocks or in four or more.  A   */
+                                /* few tiles over a very long K get several 8-CTA  */
+                                /* clusters each, their sums added in a fixed      */
+                                /* order by the last to finish (a workspace)       */
     GEMM_F16_256x256_QUAD = 6,  /* a 4-CTA cluster of two CTA pairs computing two  */
                                 /* vertically adjacent 256 x 256 tiles; each B     */
                                 /* byte is loaded once for both (TMA multicast),   */
