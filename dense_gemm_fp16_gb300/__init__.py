@@ -58,6 +58,7 @@ from ._binding import (  # noqa: F401
     gemm_debug_skinny_plan,
     gemm_debug_skinny_parts,
     gemm_debug_last_pair_launch,
+    gemm_debug_sm_clocks,
     gemm_debug_blockscaled_skip_load,
     gemm_debug_f16_nt_stream_k_skip_publish,
     gemm_f16_nt,

@@ -124,6 +124,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gemm_debug_skinny_parts.argtypes = [i, i, i, i]
         lib.gemm_debug_skinny_parts.restype = i
         lib.gemm_debug_last_pair_launch.argtypes = [ctypes.POINTER(i)] * 4
+        lib.gemm_debug_sm_clocks.restype = i
+        lib.gemm_debug_sm_clocks.argtypes = [vp, i, vp]
         lib.gemm_debug_last_pair_launch.restype = i
         lib.gemm_debug_blockscaled_skip_load.argtypes = [i, i, i, i, vp, vp, vp, vp, vp, vp,
                                                          ctypes.POINTER(_MxConfig), i,
@@ -274,6 +276,12 @@ def gemm_debug_last_pair_launch():
     if load_library().gemm_debug_last_pair_launch(*[ctypes.byref(v) for v in vals]) != 0:
         return None
     return tuple(v.value for v in vals)
+
+
+def gemm_debug_sm_clocks(out, ctas, stream) -> None:
+    """Enqueue one clock sample per CTA into device words out[3 * ctas]:
+    (SM id, SM cycle counter, global timer in ns) for each CTA."""
+    _check(load_library().gemm_debug_sm_clocks(out, ctas, stream or None))
 
 
 def gemm_debug_skinny_parts(M, N, K, ctas):

@@ -86,6 +86,20 @@ int f16_default_grid(int variant, int M, int N, int K, int sm_count) {
     return static_cast<int>(g > 0 ? g : 1);
 }
 
+// Thread 0 of each CTA records the SM it runs on, that SM's cycle counter
+// and the global nanosecond timer, read back to back.
+__global__ void sm_clock_sample_kernel(unsigned long long *out) {
+    if (threadIdx.x != 0) return;
+    unsigned smid;
+    unsigned long long ns;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    const long long cycles = clock64();
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(ns));
+    out[3 * blockIdx.x + 0] = smid;
+    out[3 * blockIdx.x + 1] = static_cast<unsigned long long>(cycles);
+    out[3 * blockIdx.x + 2] = ns;
+}
+
 }  // namespace
 
 extern "C" {
@@ -180,13 +194,12 @@ int gemm_f16_select(int M, int N, int K, int sm_count, gemm_f16_config *cfg) {
 // Predicted time in microseconds of one SGEMM launch with a given tile and
 // split count.  The CTAs spread over the SMs, so the busiest SM runs
 // ceil(ctas / sms) of them, each over its K share; one 128 x 128 CTA costs
-// about 0.094 us per K element, one 64 x 64 CTA 0.041 us (13% less each when
-// two share an SM) and one 128 x 64 CTA 0.062 us (20% less each when two
+// about 0.090 us per K element, one 64 x 64 CTA 0.041 us (13% less each when
+// two share an SM) and one 128 x 64 CTA 0.054 us (10% less each when two
 // share an SM); a split adds the partial-slot writes, the fence and the last
-// CTA's pass over the slots.  The constants are GB300 measurements (the
-// 128 x 64 ones fitted to a 16-shape sweep of every tile at 1, 2, 4 and 8
-// shares: the picks land 0.3 % from the best measured on average, worst
-// 2.9 %, against 2.1 % and 13 % without that tile); the model only has to
+// CTA's pass over the slots.  The constants are GB300 measurements, fitted
+// to a 16-shape sweep of every tile at 1 to 8 shares: the picks land 0.3 %
+// from the best measured on average, worst 2.8 %; the model only has to
 // rank the candidates.
 static void sgemm_tile(int variant, int *bm, int *bn) {
     *bm = variant == GEMM_SGEMM_64x64 ? 64 : 128;
@@ -200,12 +213,12 @@ static double sgemm_cost(int variant, int M, int N, int sms, int splits, int chu
     const double tiles = static_cast<double>(ceil_div(M, bm)) * static_cast<double>(ceil_div(N, bn));
     const double per_sm = std::ceil(tiles * splits / sms);
     if (variant == GEMM_SGEMM_128x64) {
-        double cost = per_sm * chunk * 0.062 * (per_sm >= 2 ? 0.8 : 1.0);
-        if (splits > 1) cost += 1.0 + 1.0 * splits;
+        double cost = per_sm * chunk * 0.054 * (per_sm >= 2 ? 0.9 : 1.0);
+        if (splits > 1) cost += 1.0 + 0.2 * splits;
         return cost;
     }
     const double share = (!big && per_sm >= 2) ? 0.87 : 1.0;
-    double cost = per_sm * chunk * (big ? 0.094 : 0.041) * share;
+    double cost = per_sm * chunk * (big ? 0.090 : 0.041) * share;
     if (splits > 1) cost += big ? 2.0 + 1.0 * splits : 1.0 + 0.4 * splits;
     return cost;
 }
@@ -371,6 +384,18 @@ int gemm_debug_last_pair_launch(int *pairs, int *whole_tiles, int *shared_units,
     *shared_units = r.shared_units;
     *scratch_kind = r.scratch_kind;
     return 0;
+}
+
+// Measurement hook declared in gemm_testing.h: one clock sample per CTA.
+int gemm_debug_sm_clocks(unsigned long long *out, int ctas, gemm_stream_t stream) {
+    if (ctas < 1 || ctas > 65535)
+        return fail(GEMM_ERR_INVALID_ARG, "gemm_debug_sm_clocks: ctas=%d outside 1..65535", ctas);
+    if (!out || reinterpret_cast<uintptr_t>(out) % 8 != 0)
+        return fail(GEMM_ERR_INVALID_ARG, "gemm_debug_sm_clocks: out is NULL or not 8-byte aligned");
+    sm_clock_sample_kernel<<<ctas, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(out);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "gemm_debug_sm_clocks: launch: %s", cudaGetErrorString(e));
+    return GEMM_OK;
 }
 
 // Test hook declared in gemm_testing.h: the skinny variant's plan.

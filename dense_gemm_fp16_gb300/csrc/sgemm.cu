@@ -82,7 +82,7 @@ struct SplitK {
     unsigned *counters; // [tiles], zero between launches
 };
 
-template <int BM, int BN, int BK, int TM, int TN, int STAGES, int MINB, bool VEC, bool PADA>
+template <int BM, int BN, int BK, int TM, int TN, int STAGES, int MINB, bool VEC, bool PADA, bool PIPE>
 __global__ void __launch_bounds__(sgemm_threads<BM, BN, TM, TN>(), MINB)
     sgemm_pipe_kernel(int M, int N, int K, float alpha, const float *__restrict__ A,
                       const float *__restrict__ B, float beta, float *__restrict__ C, const SplitK sk) {
@@ -167,38 +167,95 @@ __global__ void __launch_bounds__(sgemm_threads<BM, BN, TM, TN>(), MINB)
         if (s < KT) load_slice(s, kbeg + s * BK);
         cp_async_commit();  // one group per slice, empty ones included
     }
-    for (int kt = 0; kt < KT; ++kt) {
-        cp_async_wait<STAGES - 2>();  // slice kt has landed (this thread's part)
-        __syncthreads();              // ... everyone's part; slice kt-1 is no longer read
-        const int next = kt + STAGES - 1;
-        if (next < KT) load_slice(next % STAGES, kbeg + next * BK);
-        cp_async_commit();
-        const int buf = kt % STAGES;
+    // One k step of the outer product: the broadcast pairs (a, a) of the
+    // TM rows first, then the TM x TN/2 packed FMAs.
+    auto fma_step = [&](const float4(&av)[TM], int kk, const float4(&bv)[RN]) {
+        float2 bp[TN / 2];
 #pragma unroll
-        for (int kq = 0; kq < BK / 4; ++kq) {
-            float4 av[TM];
+        for (int g = 0; g < RN; ++g) {
+            bp[g * 2 + 0] = make_float2(bv[g].x, bv[g].y);
+            bp[g * 2 + 1] = make_float2(bv[g].z, bv[g].w);
+        }
+        float2 aa[TM];
 #pragma unroll
-            for (int g = 0; g < RM; ++g)
+        for (int i = 0; i < TM; ++i) {
+            const float a = kk == 0 ? av[i].x : kk == 1 ? av[i].y : kk == 2 ? av[i].z : av[i].w;
+            aa[i] = make_float2(a, a);
+        }
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    av[g * 4 + i] = *reinterpret_cast<const float4 *>(
-                        &As[buf][trow(g, i)][achunk(trow(g, i), kq) * 4]);
+        for (int i = 0; i < TM; ++i)
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                float2 bp[TN / 2];
+            for (int j = 0; j < TN / 2; ++j) accp[i][j] = __ffma2_rn(aa[i], bp[j], accp[i][j]);
+    };
+    auto read_a = [&](float4(&dst)[TM], int buf, int kq) {
 #pragma unroll
-                for (int g = 0; g < RN; ++g) {
-                    const float4 v = *reinterpret_cast<const float4 *>(
-                        &Bs[buf][kq * 4 + kk][g * (BN / RN) + tx * 4]);
-                    bp[g * 2 + 0] = make_float2(v.x, v.y);
-                    bp[g * 2 + 1] = make_float2(v.z, v.w);
+        for (int g = 0; g < RM; ++g)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                dst[g * 4 + i] = *reinterpret_cast<const float4 *>(
+                    &As[buf][trow(g, i)][achunk(trow(g, i), kq) * 4]);
+    };
+    auto read_b = [&](float4(&dst)[RN], int buf, int k) {
+#pragma unroll
+        for (int g = 0; g < RN; ++g)
+            dst[g] = *reinterpret_cast<const float4 *>(&Bs[buf][k][g * (BN / RN) + tx * 4]);
+    };
+    if constexpr (PIPE) {
+        // Register fragments read from shared memory one k step before their
+        // FMAs, in double buffers.  A slice's barrier sits in its last k
+        // step: after it the next slice's first fragments are read while that
+        // step's FMAs run, so no step waits for a shared-memory read.  The
+        // next slice's copy is then issued one slice later than in the loop
+        // below, so this form wants a ring one stage deeper.
+        static_assert(STAGES >= 3 && BK % 8 == 0, "fragment double buffers alternate within a slice");
+        cp_async_wait<STAGES - 2>();  // slice 0 has landed (this thread's part)
+        __syncthreads();              // ... everyone's part
+        float4 afr[2][TM];
+        float4 bfr[2][RN];
+        read_a(afr[0], 0, 0);
+        read_b(bfr[0], 0, 0);
+        for (int kt = 0; kt < KT; ++kt) {
+            const int buf = kt % STAGES;
+#pragma unroll
+            for (int k = 0; k < BK; ++k) {
+                const int kq = k / 4, kk = k % 4, ca = kq & 1, cb = k & 1;
+                if (k + 1 < BK) {
+                    read_b(bfr[cb ^ 1], buf, k + 1);
+                    if (kk == 3) read_a(afr[ca ^ 1], buf, kq + 1);
+                } else {
+                    cp_async_wait<STAGES - 3>();  // slice kt+1 has landed (this thread's part)
+                    __syncthreads();              // ... everyone's; slice kt-1's buffer is free
+                    const int next = kt + STAGES - 1;
+                    if (next < KT) load_slice(next % STAGES, kbeg + next * BK);
+                    cp_async_commit();
+                    if (kt + 1 < KT) {
+                        read_b(bfr[cb ^ 1], (kt + 1) % STAGES, 0);
+                        read_a(afr[ca ^ 1], (kt + 1) % STAGES, 0);
+                    }
                 }
+                fma_step(afr[ca], kk, bfr[cb]);
+            }
+        }
+    } else {
+        // One barrier at the top of each slice, then its fragments read as
+        // they are used (the register file holds no second set next to the
+        // 8 x 16 micro-tile's 128 accumulators).
+        for (int kt = 0; kt < KT; ++kt) {
+            cp_async_wait<STAGES - 2>();  // slice kt has landed (this thread's part)
+            __syncthreads();              // ... everyone's part; slice kt-1 is no longer read
+            const int next = kt + STAGES - 1;
+            if (next < KT) load_slice(next % STAGES, kbeg + next * BK);
+            cp_async_commit();
+            const int buf = kt % STAGES;
 #pragma unroll
-                for (int i = 0; i < TM; ++i) {
-                    const float a = kk == 0 ? av[i].x : kk == 1 ? av[i].y : kk == 2 ? av[i].z : av[i].w;
-                    const float2 aa = make_float2(a, a);
+            for (int kq = 0; kq < BK / 4; ++kq) {
+                float4 av[TM];
+                read_a(av, buf, kq);
 #pragma unroll
-                    for (int j = 0; j < TN / 2; ++j) accp[i][j] = __ffma2_rn(aa, bp[j], accp[i][j]);
+                for (int kk = 0; kk < 4; ++kk) {
+                    float4 bv[RN];
+                    read_b(bv, buf, kq * 4 + kk);
+                    fma_step(av, kk, bv);
                 }
             }
         }
@@ -221,10 +278,9 @@ __global__ void __launch_bounds__(sgemm_threads<BM, BN, TM, TN>(), MINB)
         }
         __threadfence();
         __syncthreads();
-        __shared__ int last;
-        if (tid == 0) last = atomicAdd(&sk.counters[tile], 1u) == static_cast<unsigned>(sk.splits - 1);
-        __syncthreads();
-        if (!last) return;
+        int arrived_last = 0;
+        if (tid == 0) arrived_last = atomicAdd(&sk.counters[tile], 1u) == static_cast<unsigned>(sk.splits - 1);
+        if (!__syncthreads_or(arrived_last)) return;
         __threadfence();  // every split's partial is visible to this CTA
         if (tid == 0) sk.counters[tile] = 0u;
         // Sum the slots in split order, QC float4 of each slot in flight at
@@ -371,7 +427,7 @@ int sg_workspace(cudaStream_t stream, size_t ws_bytes, int tiles, bool capturing
     return GEMM_OK;
 }
 
-template <int BM, int BN, int BK, int TM, int TN, int STAGES, int MINB, bool PADA>
+template <int BM, int BN, int BK, int TM, int TN, int STAGES, int MINB, bool PADA, bool PIPE>
 int launch_pipe(const SgemmLaunch &L, std::string &err) {
     dim3 grid((L.N + BN - 1) / BN, (L.M + BM - 1) / BM);
     // Split-K as planned by the caller: blockIdx.z picks a K share.
@@ -400,8 +456,8 @@ int launch_pipe(const SgemmLaunch &L, std::string &err) {
                      ((reinterpret_cast<uintptr_t>(L.A) | reinterpret_cast<uintptr_t>(L.B) |
                        reinterpret_cast<uintptr_t>(L.C)) & 15u) == 0;
     constexpr int threads = sgemm_threads<BM, BN, TM, TN>();
-    auto kvec = sgemm_pipe_kernel<BM, BN, BK, TM, TN, STAGES, MINB, true, PADA>;
-    auto kscalar = sgemm_pipe_kernel<BM, BN, BK, TM, TN, STAGES, MINB, false, PADA>;
+    auto kvec = sgemm_pipe_kernel<BM, BN, BK, TM, TN, STAGES, MINB, true, PADA, PIPE>;
+    auto kscalar = sgemm_pipe_kernel<BM, BN, BK, TM, TN, STAGES, MINB, false, PADA, PIPE>;
     if (vec)
         kvec<<<grid, threads, 0, L.stream>>>(L.M, L.N, L.K, L.alpha, L.A, L.B, L.beta, L.C, sk);
     else
@@ -429,9 +485,9 @@ int sgemm_launch(const SgemmLaunch &L, std::string &err) {
         return GEMM_OK;
     }
     switch (L.variant) {
-        case GEMM_SGEMM_128x128: return launch_pipe<128, 128, 16, 8, 16, 3, 2, false>(L, err);
-        case GEMM_SGEMM_64x64: return launch_pipe<64, 64, 16, 4, 4, 3, 2, true>(L, err);
-        case GEMM_SGEMM_128x64: return launch_pipe<128, 64, 16, 8, 8, 3, 2, false>(L, err);
+        case GEMM_SGEMM_128x128: return launch_pipe<128, 128, 16, 8, 16, 3, 2, false, false>(L, err);
+        case GEMM_SGEMM_64x64: return launch_pipe<64, 64, 16, 4, 4, 3, 2, true, false>(L, err);
+        case GEMM_SGEMM_128x64: return launch_pipe<128, 64, 16, 8, 8, 4, 2, false, true>(L, err);
         default: err = "unknown sgemm variant"; return GEMM_ERR_INVALID_ARG;
     }
 }

@@ -96,6 +96,21 @@ int gemm_debug_f16_nt_stream_k_skip_publish(int M, int N, int K, const void *A, 
  */
 int gemm_debug_last_pair_launch(int *pairs, int *whole_tiles, int *shared_units, int *scratch_kind);
 
+/*
+ * A clock sample for measurement: launches `ctas` CTAs of 32 threads on
+ * `stream`; thread 0 of CTA b writes out[3b] = the SM it ran on (%smid),
+ * out[3b + 1] = that SM's cycle counter (clock64) and out[3b + 2] = the
+ * global nanosecond timer (%globaltimer), read back to back.  Two samples
+ * enqueued around a stretch of work give each SM seen in both its mean clock
+ * over that stretch: the cycle difference over the nanosecond difference.
+ * Which SMs the CTAs land on is up to the hardware; twice the SM count of
+ * CTAs usually reaches every SM.  `out`: caller-owned device memory of
+ * 3 * ctas 64-bit words, 8-byte aligned.  Returns GEMM_OK,
+ * GEMM_ERR_INVALID_ARG (ctas outside 1..65535, out NULL or misaligned;
+ * nothing enqueued) or GEMM_ERR_CUDA (the launch failed).
+ */
+int gemm_debug_sm_clocks(unsigned long long *out, int ctas, gemm_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -38,7 +38,7 @@ def test_headers_declare_the_boundary():
               "gemm_f16_nt_fused", "gemm_f16_nt_stream_k_noalloc",
               "gemm_mxfp8_nt", "gemm_mxfp8_scale_bytes", "gemm_mxfp8_pack_scales",
               "gemm_nvfp4_nt", "gemm_nvfp4_nt_ex", "gemm_nvfp4_scale_bytes", "gemm_nvfp4_pack_scales",
-              "gemm_debug_last_pair_launch"]:
+              "gemm_debug_last_pair_launch", "gemm_debug_sm_clocks"]:
         assert n in names
 
 
@@ -60,6 +60,15 @@ def test_negative_sizes_are_rejected_on_the_host(lib):
 def test_pair_launch_record_is_empty_before_any_launch(lib):
     # host-side state of the test hook: nothing launched in this process yet
     assert g.gemm_debug_last_pair_launch() is None
+
+
+def test_clock_sample_rejects_bad_arguments_on_the_host(lib):
+    # checked before any CUDA call: nothing is enqueued
+    for out, ctas in [(0, 4), (4096, 0), (4096, 65536), (4100, 4)]:
+        with pytest.raises(g.GemmError) as e:
+            g.gemm_debug_sm_clocks(out, ctas, 0)
+        assert e.value.status == g.GEMM_ERR_INVALID_ARG
+    assert "gemm_debug_sm_clocks" in g.gemm_last_error()
 
 
 def test_empty_problems_are_no_ops(lib):
@@ -338,12 +347,13 @@ def test_sgemm_selector(lib):
     assert sel(3000, 3000, 3000, 152) == (g.GEMM_SGEMM_128x128, 1)
     # shapes where the GB300 sweep of every (tile, splits) pair had a clear winner
     assert sel(2048, 2048, 2048, 152) == (g.GEMM_SGEMM_128x128, 4)   # 256 tiles: 4 splits even the waves
-    assert sel(512, 512, 8192, 152) == (g.GEMM_SGEMM_128x128, 8)
     assert sel(256, 256, 4096, 152) == (g.GEMM_SGEMM_64x64, 8)
     assert sel(1536, 1536, 1536, 152)[1] == 1                       # 144 tiles: one wave already
-    # the 128 x 64 tile where its splits fill the SMs better (measured 4-12 % faster)
+    # the 128 x 64 tile where its splits fill the SMs better (measured 2-12 % faster)
+    assert sel(512, 512, 8192, 152) == (g.GEMM_SGEMM_128x64, 8)
     assert sel(768, 768, 768, 152) == (g.GEMM_SGEMM_128x64, 4)
-    assert sel(8192, 64, 1024, 152) == (g.GEMM_SGEMM_128x64, 4)
+    assert sel(1024, 1024, 1024, 152) == (g.GEMM_SGEMM_128x64, 8)
+    assert sel(8192, 64, 1024, 152) == (g.GEMM_SGEMM_128x64, 7)
     # no K: nothing to split
     assert sel(4096, 4096, 0, 152)[1] == 1
     assert sel(16, 16, 16, 152)[1] == 1

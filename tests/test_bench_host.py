@@ -34,6 +34,18 @@ def test_clock_summary_single_gpu_without_bus_match():
     assert bench.summarize_clock_samples([], None)["reasons"] == ["no samples"]
 
 
+def test_sm_clock_from_two_device_samples():
+    # (SM id, cycles, ns) triples: SM 3 ran 2e6 cycles in 1e6 ns = 2000 MHz,
+    # SM 5 1.5e6 in 1e6 = 1500 MHz (its second record in a sample is ignored),
+    # SM 9 appears only once and does not count.
+    before = [3, 1000, 10_000, 5, 0, 10_000, 5, 777, 10_500, 9, 0, 0]
+    after = [5, 1_500_000, 1_010_000, 3, 2_001_000, 1_010_000]
+    mhz, sms = bench.sm_clock_mhz(before, after)
+    assert sms == 2 and abs(mhz - 1750.0) < 1e-9
+    assert bench.sm_clock_mhz([1, 5, 5], [2, 9, 9]) == (None, 0)
+    assert bench.sm_clock_mhz([1, 5, 5], [1, 9, 5]) == (None, 0)     # no time elapsed
+
+
 def test_traffic_is_null_unless_the_kernel_hash_matches(tmp_path, monkeypatch):
     f = tmp_path / "t.txt"
     f.write_text("kernel_source_sha256_16: deadbeef\ndram_bytes_per_launch: 123\n")
