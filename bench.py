@@ -735,13 +735,17 @@ def run_ours(args):
     with torch.cuda.stream(stream):
         region_time(cublas_step, stream, args.warmup + 2)  # handle set-up, heuristics
         time.sleep(args.idle_s)
-        region_time(cublas_step, stream, args.warmup)
-        cb = region_time(cublas_step, stream, args.steps) / args.steps
+        with ClockSampler(local) as cclocks:
+            region_time(cublas_step, stream, args.warmup)
+            probe.sample(0)
+            cb = region_time(cublas_step, stream, args.steps) / args.steps
+            probe.sample(1)
+        cb_clk = region_clocks(probe, cclocks, "0.3 s idle, the warm-up, the timed region, 0.2 s idle")
 
     # ---- sustained: the same K calls after a soak of the same launches, at
     # the power-capped clocks of a long run, against the sustained peak; the
     # nvidia-smi sampler runs over the soaks before and after the region.
-    soak = max(1, int(args.soak_s / max(1e-4, avg_launch_ms)))
+    soak = max(1, int(args.soak_s / max(1e-7, 1e-3 * avg_launch_ms)))
     with ClockSampler(local) as sclocks:
         region_time(step, stream, soak)
         probe.sample(0)
@@ -751,8 +755,12 @@ def run_ours(args):
     g.gemm_check_device_status(sh)
     sus_clk = region_clocks(probe, sclocks, f"{args.soak_s} s soaks before and after the region")
     with torch.cuda.stream(stream):
-        region_time(cublas_step, stream, soak)
-        cb_sus = region_time(cublas_step, stream, args.steps) / args.steps
+        with ClockSampler(local) as csclocks:
+            region_time(cublas_step, stream, soak)
+            probe.sample(0)
+            cb_sus = region_time(cublas_step, stream, args.steps) / args.steps
+            probe.sample(1)
+        cbs_clk = region_clocks(probe, csclocks, f"a {args.soak_s} s soak and the region")
     sval = w.flop / (t_sus * 1e-3) / 1e12
     line["sustained"] = {
         "value": sval, "unit": "TFLOP/s", "us_per_call": 1e3 * t_sus,
@@ -761,9 +769,10 @@ def run_ours(args):
                      "frac": sval / peak_sus, "peak_source": sustained_note},
         "clocks": sus_clk,
         "cublas": {"value": w.flop / (cb_sus * 1e-3) / 1e12, "unit": "TFLOP/s",
-                   "us_per_call": 1e3 * cb_sus, "what": "torch.matmul after the same soak"}}
+                   "us_per_call": 1e3 * cb_sus, "clocks": cbs_clk,
+                   "what": "torch.matmul after the same soak"}}
     line["cublas"] = {"value": w.flop / (cb * 1e-3) / 1e12, "unit": "TFLOP/s",
-                      "us_per_call": 1e3 * cb,
+                      "us_per_call": 1e3 * cb, "clocks": cb_clk,
                       "sustained_value": w.flop / (cb_sus * 1e-3) / 1e12,
                       "what": "torch.matmul(A, B.t()) fp16, fp32 accumulation, timed like value "
                               "(idle pause, warm-up, K calls); sustained_value: like the sustained "
@@ -813,12 +822,14 @@ def run_ours(args):
 
             n = calls_for(sg, stream, target_ms=20.0)
             with ClockSampler(local) as ck:
+                probe.sample(0)
                 t_sg, trials = timed_trials(sg, stream, n)
+                probe.sample(1)
             g.gemm_check_device_status(sh)
             with torch.cuda.stream(stream):
                 region_time(sg_cublas, stream, 3)
                 t_cb, _ = timed_trials(sg_cublas, stream, n)
-            clk = ck.summary()
+            clk = region_clocks(probe, ck, "0.3 s idle, the timed regions, 0.2 s idle")
             sval = sw.flop / (t_sg * 1e-3) / 1e12
             at_clock = (fp32_nominal * clk["sm_mhz"] / max_mhz) if clk.get("sm_mhz") else None
             variant, splits = g.gemm_sgemm_select(sw.M, sw.N, sw.K, sm_count)
@@ -942,7 +953,9 @@ def run_ours(args):
         region_time(gv, stream, 5)
         n_gv = 50
         with ClockSampler(local) as ck:
+            probe.sample(0)
             t_gv, trials = timed_trials(gv, stream, n_gv)
+            probe.sample(1)
         gbytes = 2 * (gw.N * gw.K + gw.M * gw.K + gw.M * gw.N)
         achieved_gbs = gbytes / (t_gv * 1e-3) / 1e9
         line["gemv"] = {"workload": gw.name, "value": gw.flop / (t_gv * 1e-3) / 1e12,
@@ -953,7 +966,7 @@ def run_ours(args):
                                      "unit": "GB/s", "frac": achieved_gbs / hbm,
                                      "bytes_per_call": gbytes,
                                      "peak_source": f"{peak_kind} HBM copy bandwidth"},
-                        "clocks": ck.summary()}
+                        "clocks": region_clocks(probe, ck, "0.3 s idle, the timed regions, 0.2 s idle")}
         g.gemm_check_device_status(sh)
 
         # ---- 16 rows of A against the same B: the skinny tensor-core kernel
@@ -971,7 +984,9 @@ def run_ours(args):
             g.gemm_f16_nt(kw.M, kw.N, kw.K, dka.data_ptr(), dgb.data_ptr(), dkc.data_ptr(), sh)
         region_time(sk, stream, 5)
         with ClockSampler(local) as ck:
+            probe.sample(0)
             t_sk, trials = timed_trials(sk, stream, n_gv)
+            probe.sample(1)
         kbytes = 2 * (kw.N * kw.K + kw.M * kw.K + kw.M * kw.N)
         k_gbs = kbytes / (t_sk * 1e-3) / 1e9
         line["skinny"] = {"workload": kw.name, "value": kw.flop / (t_sk * 1e-3) / 1e12,
@@ -981,7 +996,7 @@ def run_ours(args):
                                        "unit": "GB/s", "frac": k_gbs / hbm,
                                        "bytes_per_call": kbytes,
                                        "peak_source": f"{peak_kind} HBM copy bandwidth"},
-                          "clocks": ck.summary()}
+                          "clocks": region_clocks(probe, ck, "0.3 s idle, the timed regions, 0.2 s idle")}
         g.gemm_check_device_status(sh)
         del dka, dkc
 
@@ -1012,8 +1027,12 @@ def run_ours(args):
             region_time(fused, stream, 5)
             region_time(unfused, stream, 3)
             time.sleep(args.idle_s)
-            t_plain = region_time(step, stream, n_ep) / n_ep
-            t_fused = region_time(fused, stream, n_ep) / n_ep
+            with ClockSampler(local) as fck:
+                t_plain = region_time(step, stream, n_ep) / n_ep
+                probe.sample(0)
+                t_fused = region_time(fused, stream, n_ep) / n_ep
+                probe.sample(1)
+            f_clk = region_clocks(probe, fck, "0.3 s idle, the plain and fused regions, 0.2 s idle")
             t_unfused = region_time(unfused, stream, n_ep) / n_ep
         g.gemm_check_device_status(sh)
         fval = w.flop / (t_fused * 1e-3) / 1e12
@@ -1026,7 +1045,8 @@ def run_ours(args):
             "extra_bytes_per_call": 2 * N + 2 * M * N,
             "roofline": {"bound": "tensor", "achieved": fval, "peak": burst, "unit": "TFLOP/s",
                          "frac": fval / burst, "peak_source": burst_note,
-                         "frac_of_sustained_peak": fval / peak_sus}}
+                         "frac_of_sustained_peak": fval / peak_sus},
+            "clocks": f_clk}
 
     # ---- block-scaled FP8 (MXFP8) at the headline shape against the fp8
     # dense peak (the measured bf16 peak x the nominal fp8/bf16 ratio of 2)
@@ -1049,7 +1069,11 @@ def run_ours(args):
             region_time(mxs, stream, 5)
             time.sleep(args.idle_s)
             n_mx = 50
-            t_mx = region_time(mxs, stream, n_mx) / n_mx
+            with ClockSampler(local) as mck:
+                probe.sample(0)
+                t_mx = region_time(mxs, stream, n_mx) / n_mx
+                probe.sample(1)
+            m_clk = region_clocks(probe, mck, "0.3 s idle, the timed region, 0.2 s idle")
         g.gemm_check_device_status(sh)
         fp8_peak = 2.0 * burst
         mval = w.flop / (t_mx * 1e-3) / 1e12
@@ -1059,7 +1083,8 @@ def run_ours(args):
             "roofline": {"bound": "tensor", "achieved": mval, "peak": fp8_peak, "unit": "TFLOP/s",
                          "frac": mval / fp8_peak,
                          "peak_source": burst_note + " x 2 (nominal fp8/bf16 ratio)",
-                         "frac_of_sustained_peak": mval / (2.0 * peak_sus)}}
+                         "frac_of_sustained_peak": mval / (2.0 * peak_sus)},
+            "clocks": m_clk}
 
     # ---- block-scaled FP4 (NVFP4) at the headline shape against the fp4
     # dense peak (the measured bf16 peak x the nominal fp4/bf16 ratio of 6)
@@ -1082,7 +1107,11 @@ def run_ours(args):
             region_time(nvs, stream, 5)
             time.sleep(args.idle_s)
             n_nv = 50
-            t_nv = region_time(nvs, stream, n_nv) / n_nv
+            with ClockSampler(local) as nck:
+                probe.sample(0)
+                t_nv = region_time(nvs, stream, n_nv) / n_nv
+                probe.sample(1)
+            n_clk = region_clocks(probe, nck, "0.3 s idle, the timed region, 0.2 s idle")
         g.gemm_check_device_status(sh)
         fp4_peak = 6.0 * burst
         nval = w.flop / (t_nv * 1e-3) / 1e12
@@ -1092,7 +1121,8 @@ def run_ours(args):
             "roofline": {"bound": "tensor", "achieved": nval, "peak": fp4_peak, "unit": "TFLOP/s",
                          "frac": nval / fp4_peak,
                          "peak_source": burst_note + " x 6 (nominal fp4/bf16 ratio)",
-                         "frac_of_sustained_peak": nval / (6.0 * peak_sus)}}
+                         "frac_of_sustained_peak": nval / (6.0 * peak_sus)},
+            "clocks": n_clk}
 
     if rank == 0 and not args.skip_cpu_baseline:
         model = cpu_model()
@@ -1124,7 +1154,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--soak-s", type=float, default=0.6,
+    ap.add_argument("--soak-s", type=float, default=1.5,
                     help="seconds of launches before and after the sustained regions")
     ap.add_argument("--idle-s", type=float, default=3.0,
                     help="idle pause before each region timed at burst clocks")
