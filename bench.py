@@ -514,6 +514,9 @@ def f16_kernel_names(g):
             g.GEMM_F16_SKINNY: "gemm_skinny_kernel (swapped tcgen05 product, K split over a cluster)"}
 
 
+EXTRA_CASES = ("f16_nt_fused_gelu_5376x5376x2048", "mxfp8_nt_5376x5376x2048", "nvfp4_nt_5376x5376x2048")
+
+
 def run_case(args):
     """One workload, `--calls` back-to-back launches of our kernel (or, with
     --cublas, of the cuBLAS reference), nothing timed: the command that the
@@ -527,10 +530,42 @@ def run_case(args):
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
     build.build()
     g.load_library()
-    w = wl.WORKLOADS[args.case]
-    A, B, C0 = wl.make_inputs(w)
     stream = torch.cuda.current_stream()
     sh = stream.cuda_stream
+    if args.case in EXTRA_CASES:
+        # the bench line's extra objects at the headline shape: the fused
+        # epilogue, MXFP8 and NVFP4 (their inputs drawn as the bench draws them)
+        w = wl.WORKLOADS[wl.HEADLINE]
+        M, N, K = w.M, w.N, w.K
+        C = torch.empty((M, N), dtype=torch.float16, device="cuda")
+        if args.case.startswith("f16_nt_fused"):
+            A, B, _ = wl.make_inputs(w)
+            dA, dB = A.cuda(), B.cuda()
+            bias, R = wl.draw_f16((N,), seed=91).cuda(), wl.draw_f16((M, N), seed=95).cuda()
+            fn = lambda: g.gemm_f16_nt_fused(M, N, K, dA.data_ptr(), dB.data_ptr(), C.data_ptr(), 1.0, 1.0,
+                                             bias.data_ptr(), R.data_ptr(), g.GEMM_ACT_GELU_TANH, sh)
+        elif args.case.startswith("mxfp8"):
+            xa, xsa = wl.draw_mxfp8(M, K, seed=31)
+            xb, xsb = wl.draw_mxfp8(N, K, seed=41)
+            dA, dB = xa.cuda(), xb.cuda()
+            pa, pb = g.mxfp8_pack_scales(xsa.cuda(), stream), g.mxfp8_pack_scales(xsb.cuda(), stream)
+            fn = lambda: g.gemm_mxfp8_nt(M, N, K, dA.data_ptr(), pa.data_ptr(), dB.data_ptr(), pb.data_ptr(),
+                                         C.data_ptr(), sh)
+        else:
+            xa, xsa = wl.draw_nvfp4(M, K, seed=51)
+            xb, xsb = wl.draw_nvfp4(N, K, seed=61)
+            dA, dB = xa.cuda(), xb.cuda()
+            pa, pb = g.nvfp4_pack_scales(xsa.cuda(), stream), g.nvfp4_pack_scales(xsb.cuda(), stream)
+            fn = lambda: g.gemm_nvfp4_nt(M, N, K, dA.data_ptr(), pa.data_ptr(), dB.data_ptr(), pb.data_ptr(),
+                                         1.0, C.data_ptr(), sh)
+        for _ in range(args.calls):
+            fn()
+        torch.cuda.synchronize()
+        g.gemm_check_device_status(sh)
+        print(json.dumps({"case": args.case, "calls": args.calls, "impl": "ours"}), flush=True)
+        return 0
+    w = wl.WORKLOADS[args.case]
+    A, B, C0 = wl.make_inputs(w)
     dA, dB = A.cuda(), B.cuda()
     if w.form == "f16_nt":
         C = torch.empty((w.M, w.N), dtype=torch.float16, device="cuda")
@@ -1165,7 +1200,8 @@ def main():
     ap.add_argument("--skip-extras", "--skip-sgemm", dest="skip_sgemm", action="store_true",
                     help="only the headline line: no sgemm, gemv, fused_epilogue, mxfp8 or nvfp4 objects")
     ap.add_argument("--case", default=None,
-                    help="profiling mode: launch one named workload --calls times and exit")
+                    help="profiling mode: launch one named workload --calls times and exit (a workload "
+                         "name, or " + ", ".join(EXTRA_CASES) + ")")
     ap.add_argument("--calls", type=int, default=3)
     ap.add_argument("--variant", type=int, default=0,
                     help="profiling mode: the kernel variant (gemm.h GEMM_F16_* / GEMM_SGEMM_*; 0 = auto)")
