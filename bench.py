@@ -18,10 +18,11 @@ ranks is taken and rank 0 prints one JSON line.
 * ``roofline``: the GEMM kernel's average launch duration from CUDA events on
   its own stream, against the measured dense bf16/fp16 tensor peak of a
   kernel timed alone (the burst figure).
-* ``clocks``: the region's mean SM clock from device samples of each SM's
-  cycle counter and the global timer right before and after it
-  (``gemm_debug_sm_clocks``); the maximum clock and the throttle reasons from
-  nvidia-smi sampled across it.
+* ``clocks``: nvidia-smi's SM clock, maximum clock and throttle reasons
+  sampled across the region, and ``sm_mhz_device``, the region's mean SM
+  clock from device samples of each SM's cycle counter and the global timer
+  right before and after it (``gemm_debug_sm_clocks``): nvidia-smi updates
+  every 100 ms, too coarse for a region of a few milliseconds.
 * ``sustained``: the same K calls after a soak of the same launches
   (``--soak-s``), at the power-capped clocks of a long run, against the
   sustained peak, with its clocks and the same-run cuBLAS figure.
@@ -298,17 +299,19 @@ class SmClockProbe:
 
 
 def region_clocks(probe, sampler, window):
-    """The `clocks` record of one timed region: the SM clock from the device
-    samples around it, the maximum clock and throttle reasons from nvidia-smi
-    over `window` (what the sampler ran across), and nvidia-smi's own summary."""
+    """The `clocks` record of one timed region: nvidia-smi's median SM clock
+    under load, maximum clock and throttle reasons over `window` (what the
+    sampler ran across), and beside them the region's mean SM clock from the
+    device samples around it, which nvidia-smi's 100 ms updates cannot
+    resolve for a region of a few milliseconds."""
     mhz, sms = probe.mhz()
     smi = sampler.summary()
-    out = {"sm_mhz": mhz if mhz is not None else smi.get("sm_mhz"),
-           "sm_max_mhz": smi.get("sm_max_mhz"), "reasons": smi.get("reasons")}
-    out["sm_mhz_source"] = (f"mean SM clock over the timed region on {sms} SMs (cycle counter over "
-                            f"global timer, sampled on the device right before and after it)"
-                            if mhz is not None else "nvidia-smi median under load")
-    out["nvidia_smi"] = dict(smi, window=window)
+    out = {"sm_mhz": smi.get("sm_mhz"), "sm_max_mhz": smi.get("sm_max_mhz"),
+           "reasons": smi.get("reasons"), "samples": smi.get("samples"), "window": window,
+           "sm_mhz_device": mhz}
+    if mhz is not None:
+        out["sm_mhz_device_source"] = (f"mean SM clock over the timed region on {sms} SMs: cycle counter "
+                                       f"over global timer, sampled on the device right before and after it")
     return out
 
 
@@ -866,7 +869,9 @@ def run_ours(args):
                 t_cb, _ = timed_trials(sg_cublas, stream, n)
             clk = region_clocks(probe, ck, "0.3 s idle, the timed regions, 0.2 s idle")
             sval = sw.flop / (t_sg * 1e-3) / 1e12
-            at_clock = (fp32_nominal * clk["sm_mhz"] / max_mhz) if clk.get("sm_mhz") else None
+            # the FP32 peak at the region's clock: the device-sampled mean, else nvidia-smi's
+            run_mhz = clk.get("sm_mhz_device") or clk.get("sm_mhz")
+            at_clock = (fp32_nominal * run_mhz / max_mhz) if run_mhz else None
             variant, splits = g.gemm_sgemm_select(sw.M, sw.N, sw.K, sm_count)
             line["configs"][name] = {
                 "form": "sgemm", "M": sw.M, "N": sw.N, "K": sw.K, "alpha": sw.alpha,
