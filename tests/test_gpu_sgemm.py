@@ -206,3 +206,24 @@ def test_sgemm_split_k_under_graph_capture():
     graph.replay()
     torch.cuda.synchronize()
     check_sgemm(C.cpu().numpy(), Cref, S, what="captured")
+
+
+def test_sgemm_split_k_on_two_streams_at_once():
+    # Split-K slots and tile counters are per stream: two streams whose split
+    # products overlap on the GPU must not mix their partials.
+    M, N, K = 512, 512, 8192
+    ins = [(wl.draw_f32((M, K), seed=41 + j), wl.draw_f32((K, N), seed=43 + j)) for j in range(2)]
+    devs = [(A.cuda(), B.cuda()) for A, B in ins]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = [torch.zeros((M, N), device="cuda") for _ in range(2)]
+    torch.cuda.synchronize()
+    for rep in range(4):
+        for j in range(2):
+            dA, dB = devs[j]
+            g.sgemm_ex(M, N, K, 1.0, dA.data_ptr(), dB.data_ptr(), 0.0, outs[j].data_ptr(), streams[j].cuda_stream,
+                       g.GEMM_SGEMM_128x64, 8)
+    for s in streams:
+        s.synchronize()
+    for j in range(2):
+        Cref, S = oracle.sgemm(*ins[j], 1.0, 0.0, None)
+        check_sgemm(outs[j].cpu().numpy(), Cref, S, what=f"split-K, stream {j}")

@@ -231,3 +231,28 @@ def test_skinny_several_clusters_per_tile_fused_and_captured():
     torch.cuda.synchronize()
     Cref, S = oracle.gemm_f16_nt(A, B)
     check_f16(Cg.cpu().numpy(), Cref, S, what="skinny parts captured")
+
+
+def test_skinny_several_clusters_per_tile_on_two_streams_at_once():
+    # Each stream has its own workspace and counters: two streams whose
+    # multi-cluster products overlap on the GPU must not mix their parts.
+    M, N, K = 256, 256, 65536
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert g.gemm_debug_skinny_parts(M, N, K, sms) > 1
+    ins = [(wl.draw_f16((M, K), seed=91 + j, dist="normal"), wl.draw_f16((N, K), seed=93 + j, dist="normal"))
+           for j in range(2)]
+    devs = [(A.cuda(), B.cuda()) for A, B in ins]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = [torch.empty((M, N), dtype=torch.float16, device="cuda") for _ in range(2)]
+    torch.cuda.synchronize()
+    for rep in range(4):
+        for j in range(2):
+            dA, dB = devs[j]
+            g.gemm_f16_nt_ex(M, N, K, dA.data_ptr(), dB.data_ptr(), outs[j].data_ptr(), streams[j].cuda_stream,
+                             g.GEMM_F16_SKINNY)
+    for s in streams:
+        s.synchronize()
+    g.gemm_check_device_status(0)
+    for j in range(2):
+        Cref, S = oracle.gemm_f16_nt(*ins[j])
+        check_f16(outs[j].cpu().numpy(), Cref, S, what=f"skinny parts, stream {j}")
