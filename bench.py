@@ -513,6 +513,7 @@ def f16_kernel_names(g):
             g.GEMM_F16_128x128: "gemm_f16_nt_tc_kernel<128,6> (1-CTA 128x128)",
             g.GEMM_F16_256x256_PAIR: "gemm_f16_nt_pair_kernel<6> (CTA pair 256x256)",
             g.GEMM_F16_256x256_QUAD: "gemm_f16_nt_pair_kernel<6,...,4> (two CTA pairs sharing B, 512x256)",
+            g.GEMM_F16_256x256_KSPLIT: "gemm_f16_nt_pair_kernel<6,...,4,true> (two CTA pairs splitting K, 256x256)",
             g.GEMM_F16_GEMV: "gemv_rows_kernel (CUDA cores)",
             g.GEMM_F16_SKINNY: "gemm_skinny_kernel (swapped tcgen05 product, K split over a cluster)"}
 

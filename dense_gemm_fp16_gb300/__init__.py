@@ -33,6 +33,7 @@ from ._binding import (  # noqa: F401
     GEMM_F16_128x256,
     GEMM_F16_256x256_PAIR,
     GEMM_F16_256x256_QUAD,
+    GEMM_F16_256x256_KSPLIT,
     GEMM_F16_AUTO,
     GEMM_F16_FLAG_STREAM_K,
     GEMM_F16_GEMV,

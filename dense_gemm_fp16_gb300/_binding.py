@@ -20,7 +20,7 @@ GEMM_ERR_CUDA = -4
 GEMM_ERR_DEVICE_TIMEOUT = -5
 
 GEMM_F16_AUTO, GEMM_F16_128x256, GEMM_F16_128x128, GEMM_F16_256x256_PAIR, GEMM_F16_GEMV = 0, 1, 2, 3, 4
-GEMM_F16_SKINNY, GEMM_F16_256x256_QUAD, GEMM_F16_NUM_VARIANTS = 5, 6, 7
+GEMM_F16_SKINNY, GEMM_F16_256x256_QUAD, GEMM_F16_256x256_KSPLIT, GEMM_F16_NUM_VARIANTS = 5, 6, 7, 8
 GEMM_SGEMM_AUTO, GEMM_SGEMM_128x128, GEMM_SGEMM_64x64, GEMM_SGEMM_128x64 = 0, 1, 2, 3
 GEMM_F16_FLAG_STREAM_K = 1
 GEMM_MXFP8_AUTO, GEMM_MXFP8_128x128, GEMM_MXFP8_256x128_PAIR, GEMM_MXFP8_128x256 = 0, 1, 2, 3

@@ -73,6 +73,7 @@ int f16_default_grid(int variant, int M, int N, int K, int sm_count) {
         case GEMM_F16_128x256: tiles = ceil_div(M, 128) * ceil_div(N, 256); break;
         case GEMM_F16_256x256_PAIR: tiles = 2 * ceil_div(M, 256) * ceil_div(N, 256); break;
         case GEMM_F16_256x256_QUAD: tiles = 4 * ceil_div(M, 512) * ceil_div(N, 256); break;
+        case GEMM_F16_256x256_KSPLIT: return static_cast<int>(4 * ceil_div(M, 256) * ceil_div(N, 256));
         default: tiles = ceil_div(M, 128) * ceil_div(N, 128); break;
     }
     long long cap = sm_count;
@@ -183,6 +184,17 @@ int gemm_f16_select(int M, int N, int K, int sm_count, gemm_f16_config *cfg) {
         // whole lines the pair stays ahead (5376^2 x 2048 78 / 88).  With one
         // row of pair tiles (M <= 256) the second pair would have no tiles.
         if (variant == GEMM_F16_256x256_PAIR && K % 64 != 0 && M > 256) variant = GEMM_F16_256x256_QUAD;
+        // Few pair tiles over a long K: two pairs per cluster split each
+        // tile's K, their sums added through distributed shared memory, when
+        // the tiles fill at least half of the 4-CTA clusters that fit at once
+        // (36 on 152 SMs) and each half keeps 64+ k-blocks.  Measured (us,
+        // that / the tile pick / cuBLAS): 1024 x 2048 x 8192 28.3 / 30.8 /
+        // 23.0, 256 x 8192 x 8192 34.9 / 37.1 / 28.5, 512 x 4096 x 14336
+        // 45.1 / 54.0 / 41.0; with 32 k-blocks per half it lost (1024 x 2048 x
+        // 2048 14.9 / 10.6), and with more tiles than clusters too.
+        const long long ks_clusters = sm_count / 4 - 2;
+        if (M >= 256 && K % 64 == 0 && ceil_div(K, 64) >= 128 && 2 * tpair > ks_clusters && tpair <= ks_clusters)
+            variant = GEMM_F16_256x256_KSPLIT;
     }
     cfg->variant = variant;
     cfg->grid = f16_default_grid(variant, M, N, K, sm_count);

@@ -205,12 +205,30 @@ struct Partials {
     int first_slot;      // slots first_slot, first_slot - 2, ... (pairs below this one)
     int region;          // float offset of this warp's region in a slot
     int lane;
+    uint32_t dsmem = 0;  // or: this warp's region of the partner pair's share (shared::cluster); 0: none
 };
 
 constexpr size_t kSkSlotFloatsDev = 128 * 256;
 
 __device__ __forceinline__ void add_partial_slab(const Partials &pp, int c, uint32_t (&lo)[32],
                                                  uint32_t (&hi)[32]) {
+    if (pp.dsmem) {
+        // the partner pair's share of the same rows and columns, from its
+        // shared memory (the layout epilogue_warp_share writes)
+        float4 x[16];
+#pragma unroll
+        for (int v = 0; v < 16; ++v)
+            x[v] = ld_dsmem_f4(pp.dsmem + static_cast<uint32_t>(((c * 16 + v) * 32 + pp.lane) * 16));
+#pragma unroll
+        for (int v = 0; v < 16; ++v) {
+            uint32_t *d = v < 8 ? &lo[v * 4] : &hi[(v - 8) * 4];
+            d[0] = __float_as_uint(__uint_as_float(d[0]) + x[v].x);
+            d[1] = __float_as_uint(__uint_as_float(d[1]) + x[v].y);
+            d[2] = __float_as_uint(__uint_as_float(d[2]) + x[v].z);
+            d[3] = __float_as_uint(__uint_as_float(d[3]) + x[v].w);
+        }
+        return;
+    }
 #pragma unroll 1
     for (int q = 0; q < pp.count; ++q) {
         const float4 *src = reinterpret_cast<const float4 *>(
@@ -227,6 +245,25 @@ __device__ __forceinline__ void add_partial_slab(const Partials &pp, int c, uint
             d[1] = __float_as_uint(__uint_as_float(d[1]) + x[v].y);
             d[2] = __float_as_uint(__uint_as_float(d[2]) + x[v].z);
             d[3] = __float_as_uint(__uint_as_float(d[3]) + x[v].w);
+        }
+    }
+}
+
+// This warp's rows of the accumulator, unrounded, into shared memory at
+// `dst` for the partner pair of a K-split cluster: float4 v of slab c of lane
+// l at ((c * 16 + v) * 32 + l) * 16 bytes, so a warp's store covers 512
+// contiguous bytes (no bank conflicts), as add_partial_slab reads it back.
+template <int NCOLS>
+__device__ __forceinline__ void epilogue_warp_share(uint32_t dst, uint32_t taddr, int lane) {
+#pragma unroll 1
+    for (int c = 0; c < NCOLS / 64; ++c) {
+        uint32_t lo[32], hi[32];
+        tmem_load_32cols(taddr + static_cast<uint32_t>(c * 64), lo);
+        tmem_load_32cols(taddr + static_cast<uint32_t>(c * 64 + 32), hi);
+#pragma unroll
+        for (int v = 0; v < 16; ++v) {
+            const uint32_t *s = v < 8 ? &lo[v * 4] : &hi[(v - 8) * 4];
+            st_shared_v4(dst + static_cast<uint32_t>(((c * 16 + v) * 32 + lane) * 16), s[0], s[1], s[2], s[3]);
         }
     }
 }
@@ -357,7 +394,7 @@ __device__ __forceinline__ bool epilogue_warp_tile(const F16Args &args, const CU
             uint32_t lo[32], hi[32];
             tmem_load_32cols(taddr + static_cast<uint32_t>(c * 64), lo);
             tmem_load_32cols(taddr + static_cast<uint32_t>(c * 64 + 32), hi);
-            if (pp.count) add_partial_slab(pp, c, lo, hi);
+            if (pp.count || pp.dsmem) add_partial_slab(pp, c, lo, hi);
             if constexpr (ACT >= 0) {
 #pragma unroll
                 for (int q = 0; q < 8; ++q)
@@ -414,6 +451,22 @@ __device__ __forceinline__ bool epilogue_warp_tile(const F16Args &args, const CU
             }
             uint32_t r[32];
             tmem_load_32cols(taddr + static_cast<uint32_t>(c * 32), r);
+            if (pp.dsmem) {
+                // the partner pair's share of these 32 columns: half h of
+                // 64-column slab c / 2 in epilogue_warp_share's layout
+                float4 x[8];
+#pragma unroll
+                for (int v = 0; v < 8; ++v)
+                    x[v] = ld_dsmem_f4(pp.dsmem + static_cast<uint32_t>(
+                                                      (((c >> 1) * 16 + (c & 1) * 8 + v) * 32 + lane) * 16));
+#pragma unroll
+                for (int v = 0; v < 8; ++v) {
+                    r[v * 4 + 0] = __float_as_uint(__uint_as_float(r[v * 4 + 0]) + x[v].x);
+                    r[v * 4 + 1] = __float_as_uint(__uint_as_float(r[v * 4 + 1]) + x[v].y);
+                    r[v * 4 + 2] = __float_as_uint(__uint_as_float(r[v * 4 + 2]) + x[v].z);
+                    r[v * 4 + 3] = __float_as_uint(__uint_as_float(r[v * 4 + 3]) + x[v].w);
+                }
+            }
             if constexpr (ACT >= 0) {
 #pragma unroll
                 for (int q = 0; q < 4; ++q) epi_apply8<ACT>(args.epi, &r[q * 8], shfl_u4(bias_l, q), res8[q]);
@@ -692,7 +745,14 @@ struct PairCfg {
 // pair's 64 KB as before.  A stage can be refilled only when both pairs' MMAs
 // have read it, so empty[s] takes one commit from each pair's MMA issuer,
 // multicast to all four CTAs.
-template <int STAGES, int EPI, int ACT, bool RES, int CL = 2>
+//
+// KS (with CL = 4): the two pairs of a cluster compute the same 256 x 256
+// tile over the two halves of its K range instead, each pair loading its own
+// A and B boxes.  Pair 1's epilogue warps write their fp32 accumulator rows
+// into their own CTA's (idle) ring; pair 0's warps wait on a barrier those
+// writes arrive on, add them through distributed shared memory, and store.
+// One tile per cluster: the ring holds the share, so no next tile may load.
+template <int STAGES, int EPI, int ACT, bool RES, int CL = 2, bool KS = false>
 __global__ void __launch_bounds__((2 + EPI) * 32, 1)
     gemm_f16_nt_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                             const __grid_constant__ CUtensorMap tmB,
@@ -700,8 +760,11 @@ __global__ void __launch_bounds__((2 + EPI) * 32, 1)
                             const __grid_constant__ CUtensorMap tmR, const F16Args args) {
     static_assert(!RES || EPI == 4, "residual rings are laid out for 4 epilogue warps");
     static_assert(CL == 2 || CL == 4, "a CTA pair, or two pairs sharing B");
+    static_assert(!KS || CL == 4, "the K split puts two pairs in one cluster");
     constexpr int kBufs = RES ? kResBufs : 8 / EPI;
-    using T = PairCfg<STAGES, EPI * kBufs * kEpiBufBytes, RES ? EPI * kResBufs : 0>;
+    constexpr int kResBars = RES ? EPI * kResBufs : 0;
+    using T = PairCfg<STAGES, EPI * kBufs * kEpiBufBytes, kResBars + (KS ? EPI : 0)>;
+    static_assert(!KS || STAGES * T::kStageBytes >= 256 * 128 * 4, "the ring holds a CTA's share");
     constexpr int BN = T::kBN;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
@@ -716,6 +779,8 @@ __global__ void __launch_bounds__((2 + EPI) * 32, 1)
     auto acce_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
     const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
     const uint32_t res_bar0 = bar0 + 8u * (2 * STAGES + 5);  // RES: kResBufs per epilogue warp
+    // KS: per epilogue warp of pair 0, the partner warp's share is in place
+    auto xready_bar = [&](int w) { return bar0 + 8u * (2 * STAGES + 5 + kResBars + w); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + T::kNumBars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     __shared__ int never_abort;
@@ -731,7 +796,14 @@ __global__ void __launch_bounds__((2 + EPI) * 32, 1)
     const int pair = static_cast<int>(blockIdx.x) / CL;
     const int num_pairs = static_cast<int>(gridDim.x) / CL;
     // tile row of this pair for work-list tile row mt (quad rows hold two)
-    auto pair_row = [&](int mt) { return CL == 2 ? mt : 2 * mt + static_cast<int>(pic); };
+    auto pair_row = [&](int mt) { return CL == 2 || KS ? mt : 2 * mt + static_cast<int>(pic); };
+    // KS: this pair's half of a tile's k-blocks [kb0, kb1)
+    auto k_half = [&](int &kb0, int &kb1) {
+        if constexpr (KS) {
+            const int h = (kb1 - kb0 + 1) / 2;
+            if (pic) kb0 += h; else kb1 = kb0 + h;
+        }
+    };
 
     if (threadIdx.x == 0) {
         tma_prefetch_desc(&tmA);
@@ -740,7 +812,7 @@ __global__ void __launch_bounds__((2 + EPI) * 32, 1)
         if (RES) tma_prefetch_desc(&tmR);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), CL / 2);  // one MMA commit per pair
+            mbar_init(empty_bar(s), KS ? 1 : CL / 2);  // one MMA commit per pair reading the stage
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(accf_bar(b), 1);
@@ -748,6 +820,8 @@ __global__ void __launch_bounds__((2 + EPI) * 32, 1)
         }
         if (RES)
             for (int j = 0; j < EPI * kResBufs; ++j) mbar_init(res_bar0 + 8u * j, 1);
+        if (KS)
+            for (int w = 0; w < EPI; ++w) mbar_init(xready_bar(w), 32);  // every lane of the partner warp
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
         never_abort = 0;
@@ -776,11 +850,13 @@ __global__ void __launch_bounds__((2 + EPI) * 32, 1)
             PairWork work(args, pair, num_pairs);
             int tile, kb0, kb1;
             while (ok && work.next(tile, kb0, kb1)) {
+                k_half(kb0, kb1);
                 int mt, nt;
                 tile_mn(tile, args, mt, nt);
                 mt = pair_row(mt);
                 const int a_row = mt * 256 + static_cast<int>(rank) * 128;
-                const int b_row = nt * BN + static_cast<int>(rank) * 128 + (CL == 4 ? 64 * static_cast<int>(pic) : 0);
+                const int b_row = nt * BN + static_cast<int>(rank) * 128 +
+                                  (CL == 4 && !KS ? 64 * static_cast<int>(pic) : 0);
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait_cluster(empty_bar(stage), phase ^ 1u, args.timeout_ns, abort_flag)) {
                         ok = false;
@@ -796,7 +872,7 @@ __global__ void __launch_bounds__((2 + EPI) * 32, 1)
                             arm_parity ^= 1u << stage;
                         }
                         tma_load_2d_pair(sa, &tmA, full_leader, kb * kBK, a_row);
-                        if constexpr (CL == 2) {
+                        if constexpr (CL == 2 || KS) {
                             tma_load_2d_pair(sa + T::kABytes, &tmB, full_leader, kb * kBK, b_row);
                         } else {
                             // rows 64 pic .. of this CTA's B half, to CTA `rank` of both pairs
@@ -828,6 +904,7 @@ __global__ void __launch_bounds__((2 + EPI) * 32, 1)
             PairWork work(args, pair, num_pairs);
             int tile, kb0, kb1;
             for (int i = 0; work.next(tile, kb0, kb1); ++i) {
+                k_half(kb0, kb1);
                 const int b = i & 1;
                 const uint32_t ap = (i >> 1) & 1;
                 if (!mbar_wait_cluster(acce_bar(b), ap ^ 1u, args.timeout_ns, abort_flag)) {
@@ -849,7 +926,10 @@ __global__ void __launch_bounds__((2 + EPI) * 32, 1)
                     for (int k = 0; k < kBK / kUmmaK; ++k)
                         mma_f16_ss_pair(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc,
                                         (kb > kb0 || k > 0) ? 1u : 0u);
-                    mma_commit_pair_multicast(empty_bar(stage), CL == 2 ? 0x3 : 0xF);
+                    // the stage is free once every pair reading it is done: this
+                    // pair, or (B shared) both pairs of the cluster
+                    mma_commit_pair_multicast(empty_bar(stage),
+                                              KS ? static_cast<uint16_t>(0x3u << lead) : (CL == 2 ? 0x3 : 0xF));
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -925,7 +1005,14 @@ __global__ void __launch_bounds__((2 + EPI) * 32, 1)
             tc_fence_after_sync();
             const uint32_t taddr = tmem_base + lane_field + static_cast<uint32_t>(b * BN + col0);
             const int region = ew * kCols * 32;    // this warp's part of a partial slot
-            if (kb0 > 0) {
+            if (KS && pic == 1) {
+                // K-split partner: this warp's rows of the accumulator into
+                // its own ring (idle: the pair's k-blocks are all consumed),
+                // then every lane arrives, with cluster-scope release, on the
+                // barrier of pair 0's matching warp (CTA `rank` of the cluster).
+                epilogue_warp_share<kCols>(sbase + static_cast<uint32_t>(region) * 4u, taddr, lane);
+                mbar_arrive_cluster(mapa_shared(xready_bar(ew), rank));
+            } else if (kb0 > 0) {
                 // Stream-K contributor: this warp publishes its rows of the
                 // unrounded partial, then its own flag (no barrier between warps).
                 float *slot = args.sk_ws + static_cast<size_t>(pair * 2 + rank) * kSkSlotFloatsDev;
@@ -936,6 +1023,24 @@ __global__ void __launch_bounds__((2 + EPI) * 32, 1)
                     st_release_gpu(args.sk_flags + (pair * 2 + rank) * 8 + ew, args.seq);
             } else {
                 Partials pp{args.sk_ws, 0, 0, region, lane};
+                if constexpr (KS) {
+                    // K-split owner: wait (bounded) for the partner warp's
+                    // share, then every lane acquires it before reading it
+                    // through distributed shared memory.
+                    const uint32_t xp = static_cast<uint32_t>(i & 1);
+                    int got = 1;
+                    if (lane == 0) got = mbar_wait_cluster(xready_bar(ew), xp, args.timeout_ns, abort_flag) ? 1 : 0;
+                    got = __shfl_sync(0xffffffffu, got, 0);
+                    if (!got) {
+                        if (lane == 0) {
+                            if (!*abort_flag) record_timeout(3);
+                            *abort_flag = 1;
+                        }
+                        break;
+                    }
+                    (void)mbar_try_wait_cluster(xready_bar(ew), xp);
+                    pp.dsmem = mapa_shared(sbase + static_cast<uint32_t>(region) * 4u, crank + 2u);
+                }
                 if (kb1 < args.num_kb) {
                     // Owner of a split tile: the following share ranks (pairs
                     // pair-1, pair-2, ...), whose shares begin inside this tile,
@@ -1277,12 +1382,13 @@ int noalloc_scratch(cudaStream_t stream, float **ws, uint32_t **flags, uint32_t 
 thread_local PairLaunchRecord t_last_pair;
 
 // CL = 2: one CTA pair per 256 x 256 tile; CL = 4: two pairs per cluster
-// sharing B (vertically adjacent tiles), no split.
-template <int STAGES, int EPI, int ACT, bool RES, int CL = 2>
+// sharing B (vertically adjacent tiles), no split; CL = 4 with KS: two pairs
+// per cluster splitting one tile's K range, one tile per cluster.
+template <int STAGES, int EPI, int ACT, bool RES, int CL = 2, bool KS = false>
 int launch_pair(const F16Launch &L, std::string &err) {
     constexpr int kBufs = RES ? kResBufs : 8 / EPI;
-    using T = PairCfg<STAGES, EPI * kBufs * kEpiBufBytes, RES ? EPI * kResBufs : 0>;
-    auto kernel = gemm_f16_nt_pair_kernel<STAGES, EPI, ACT, RES, CL>;
+    using T = PairCfg<STAGES, EPI * kBufs * kEpiBufBytes, (RES ? EPI * kResBufs : 0) + (KS ? EPI : 0)>;
+    auto kernel = gemm_f16_nt_pair_kernel<STAGES, EPI, ACT, RES, CL, KS>;
     static int max_clusters[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -1325,16 +1431,18 @@ int launch_pair(const F16Launch &L, std::string &err) {
     CUtensorMap tmA, tmB;
     if (!encode_half_map(&tmA, L.A, L.M, L.K, kBM, kBK, err)) return GEMM_ERR_CUDA;
     // (two pairs sharing B each load 64 of a CTA's 128 rows of it)
-    if (!encode_half_map(&tmB, L.B, L.N, L.K, CL == 2 ? 128 : 64, kBK, err)) return GEMM_ERR_CUDA;
+    if (!encode_half_map(&tmB, L.B, L.N, L.K, CL == 2 || KS ? 128 : 64, kBK, err)) return GEMM_ERR_CUDA;
 
     F16Args args;
     args.C = static_cast<__half *>(L.C);
     args.M = L.M;
     args.N = L.N;
     args.K = L.K;
-    // work-list tile rows: 256 output rows per pair, 512 per two-pair cluster
-    args.m_tiles = (L.M + 128 * CL - 1) / (128 * CL);
-    args.raster = L.raster > 0 ? (CL == 2 ? L.raster : (L.raster + 1) / 2) : (1 << 30);
+    // work-list tile rows: 256 output rows per pair (or per K-split cluster),
+    // 512 per two-pair cluster sharing B
+    constexpr int kRowsPerUnit = CL == 2 || KS ? 256 : 512;
+    args.m_tiles = (L.M + kRowsPerUnit - 1) / kRowsPerUnit;
+    args.raster = L.raster > 0 ? (kRowsPerUnit == 256 ? L.raster : (L.raster + 1) / 2) : (1 << 30);
     args.n_tiles = (L.N + 255) / 256;
     args.num_kb = (L.K + kBK - 1) / kBK;
     args.vec_store = (L.N % 8 == 0) && ((reinterpret_cast<uintptr_t>(L.C) & 15u) == 0);
@@ -1356,6 +1464,10 @@ int launch_pair(const F16Launch &L, std::string &err) {
     // The allocation-free entry point's static array has partial slots for
     // kNoAllocMaxPairs pairs: a larger device runs that many persistent pairs.
     if (L.static_scratch && pairs > kNoAllocMaxPairs) pairs = kNoAllocMaxPairs;
+    // K split: one tile per cluster, since the partner pair's share occupies
+    // its ring.  No cluster waits on another, so clusters beyond those that
+    // fit at once simply start later.
+    if (KS) pairs = tiles;
 
     // The k-blocks of some tiles shared out over several pairs (stream-K),
     // whose fp32 partials the pair holding k-block 0 adds before rounding:
@@ -1489,6 +1601,9 @@ int f16_launch(const F16Launch &L, std::string &err) {
         case GEMM_F16_256x256_PAIR: return launch_pair_epi(L, err);
         // two pairs sharing B: the plain product (a fused epilogue runs on the pair variant)
         case GEMM_F16_256x256_QUAD: return L.epi.on ? launch_pair_epi(L, err) : launch_pair<6, 4, -1, false, 4>(L, err);
+        // two pairs splitting one tile's K: the plain product over at least two k-blocks
+        case GEMM_F16_256x256_KSPLIT:
+            return L.epi.on || L.K <= kBK ? launch_pair_epi(L, err) : launch_pair<6, 4, -1, false, 4, true>(L, err);
         case GEMM_F16_GEMV: {
             GemvLaunch G{L.M, L.N, L.K, L.A, L.B, L.C, L.stream, L.sm_count, 4, L.epi};
             return gemv_launch(G, err);

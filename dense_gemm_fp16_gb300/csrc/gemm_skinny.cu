@@ -129,15 +129,6 @@ __device__ __forceinline__ __half skinny_out(const Epi &e, float x, int m, int n
     return __float2half_rn(x);
 }
 
-// Four fp32 values at a shared::cluster address (another CTA's shared memory).
-__device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(addr));
-    return v;
-}
-
 // Whole warp: 16 consecutive 32-bit TMEM columns of this warp's 32 lanes.
 __device__ __forceinline__ void tmem_load_16cols(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(

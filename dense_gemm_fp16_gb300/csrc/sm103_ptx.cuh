@@ -187,6 +187,15 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
     return r;
 }
 
+// Four fp32 values at a shared::cluster address (another CTA's shared memory).
+__device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
 // All threads of every CTA in the cluster.
 __device__ __forceinline__ void cluster_sync() {
     asm volatile(

@@ -199,7 +199,16 @@ enum {
                                 /* a quarter fewer L2 reads and requests; plain     */
                                 /* product only (with a fused epilogue the pair    */
                                 /* variant runs)                                    */
-    GEMM_F16_NUM_VARIANTS = 7
+    GEMM_F16_256x256_KSPLIT = 7,/* a 4-CTA cluster of two CTA pairs computing one  */
+                                /* 256 x 256 tile over the two halves of K, the    */
+                                /* second pair's fp32 sum added by the first       */
+                                /* through distributed shared memory (no           */
+                                /* workspace; the sum of the two halves, each in   */
+                                /* the pair kernel's order); one tile per cluster. */
+                                /* For few tiles over a long K.  Plain product     */
+                                /* with K > 64 only: otherwise the pair variant    */
+                                /* runs                                             */
+    GEMM_F16_NUM_VARIANTS = 8
 };
 
 /*
@@ -213,7 +222,10 @@ enum {
  * waves of 128 x 128 tiles (1.5 / 1.5 when K <= 512).  When that is the pair
  * and K % 64 != 0 (rows of A and B not a whole number of 128-byte lines, so
  * every TMA row spans two L2 lines) with M > 256, GEMM_F16_256x256_QUAD
- * replaces it.
+ * replaces it.  From 256 rows, when K % 64 == 0, K >= 8192 and the 256 x 256
+ * tiles number more than half and at most all of the 4-CTA clusters that fit
+ * at once (sm_count / 4 - 2 of them), GEMM_F16_256x256_KSPLIT takes the
+ * product instead.
  * Fills *cfg and returns GEMM_OK, or GEMM_ERR_INVALID_ARG.
  */
 int gemm_f16_select(int M, int N, int K, int sm_count, gemm_f16_config *cfg);

@@ -168,6 +168,12 @@ def test_f16_selector(lib):
     # the two fp16 workloads: CTA-pair 256 x 256 tiles, one CTA per SM
     assert g.gemm_f16_select(5376, 5376, 2048, 152)[:2] == (g.GEMM_F16_256x256_PAIR, 152)
     # rows of 4080 bytes (K = 2040), off the 128-byte grid: two pairs sharing B
+    # few pair tiles over a long K: two pairs per cluster split each tile's K
+    assert g.gemm_f16_select(1024, 2048, 8192, 152)[:2] == (g.GEMM_F16_256x256_KSPLIT, 128)
+    assert g.gemm_f16_select(512, 4096, 14336, 152)[0] == g.GEMM_F16_256x256_KSPLIT
+    assert g.gemm_f16_select(1024, 2048, 2048, 152)[0] != g.GEMM_F16_256x256_KSPLIT   # halves too short
+    assert g.gemm_f16_select(768, 4096, 8192, 152)[0] != g.GEMM_F16_256x256_KSPLIT    # 48 tiles > 36 clusters
+    assert g.gemm_f16_select(1024, 1024, 8192, 152)[0] == g.GEMM_F16_SKINNY           # 16 tiles: the skinny split
     assert g.gemm_f16_select(5000, 5376, 2040, 152)[:2] == (g.GEMM_F16_256x256_QUAD, 152)
     assert g.gemm_f16_select(5376, 5376, 2040, 152)[0] == g.GEMM_F16_256x256_QUAD
     assert g.gemm_f16_select(8192, 8192, 8184, 152)[0] == g.GEMM_F16_256x256_QUAD
@@ -236,6 +242,13 @@ def test_f16_selector_rule_over_a_shape_grid(lib):
                              g.GEMM_F16_128x256: (1.5 if short else 1.15) * cdiv(cdiv(M, 128) * cdiv(N, 256), sm),
                              g.GEMM_F16_256x256_PAIR: (1.5 if short else 1.1) * cdiv(cdiv(M, 256) * cdiv(N, 256), sm // 2)}
                         quad = K % 64 != 0 and M > 256
+                        tpair = cdiv(M, 256) * cdiv(N, 256)
+                        ks = (M >= 256 and K % 64 == 0 and cdiv(K, 64) >= 128 and
+                              2 * tpair > sm // 4 - 2 and tpair <= sm // 4 - 2)
+                        assert (v == g.GEMM_F16_256x256_KSPLIT) == ks, (M, N, K, sm, v)
+                        if ks:
+                            assert grid == 4 * tpair
+                            continue
                         if v == g.GEMM_F16_256x256_QUAD:
                             # the pair's waves were cheapest and the rows are
                             # off the 128-byte grid

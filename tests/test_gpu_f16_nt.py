@@ -141,6 +141,46 @@ def test_f16_nt_two_pairs_sharing_b_repeatable():
     check_f16(first[rows, cols], Cref, S, what="quad repeated")
 
 
+# Two CTA pairs of a 4-CTA cluster splitting one tile's K range: the second
+# pair's fp32 sum reaches the first through distributed shared memory.
+# Shapes: one tile, ragged M, N and K (a partial last k-block), the fewest
+# k-blocks the split takes (2 and 3), tiles past the clusters that fit at
+# once (80 tiles: clusters start later), a long K, and K = 64 (a single
+# k-block: the pair variant runs instead).
+@pytest.mark.parametrize("M,N,K", [(256, 256, 128), (300, 700, 520), (200, 600, 136), (512, 384, 4104),
+                                   (2560, 2048, 256), (1024, 1024, 8192), (256, 512, 64)])
+def test_f16_nt_k_split_cluster(M, N, K):
+    A = wl.draw_f16((M, K), seed=M + 21, dist="normal")
+    B = wl.draw_f16((N, K), seed=N + 22, dist="normal")
+    C = _run(A, B, g.GEMM_F16_256x256_KSPLIT)
+    Cref, S = oracle.gemm_f16_nt(A, B)
+    check_f16(C, Cref, S, what=f"k-split {M}x{N}x{K}")
+
+
+def test_f16_nt_k_split_cluster_repeatable_and_exact():
+    # small integers: every partial sum is an exact integer, so the result
+    # must equal the exact product bit for bit; and repeated runs agree
+    M, N, K = 768, 1024, 2048
+    rng = np.random.default_rng(5)
+    A = torch.from_numpy(rng.integers(-1, 2, (M, K)).astype(np.float16))
+    B = torch.from_numpy(rng.integers(-1, 2, (N, K)).astype(np.float16))
+    exact = (A.double() @ B.double().t()).numpy()
+    first = _run(A, B, g.GEMM_F16_256x256_KSPLIT)
+    assert np.array_equal(first.astype(np.float64), exact)
+    for _ in range(3):
+        assert np.array_equal(_run(A, B, g.GEMM_F16_256x256_KSPLIT).view(np.uint16), first.view(np.uint16))
+
+
+def test_f16_nt_k_split_cluster_sampled_large():
+    M, N, K = 1024, 2048, 8192
+    A = wl.draw_f16((M, K), seed=31, dist="normal")
+    B = wl.draw_f16((N, K), seed=32, dist="normal")
+    C = _run(A, B, g.GEMM_F16_256x256_KSPLIT)
+    rows, cols = wl.sample_positions(M, N, 65536, seed=33)
+    Cref, S = oracle.gemm_f16_nt_sampled(A, B, rows, cols)
+    check_f16(C[rows, cols], Cref, S, what="k-split sampled")
+
+
 def test_f16_nt_small_integers_bit_exact():
     # entries in {-1, 0, 1}, K = 1024: every partial sum is an integer below
     # 2^11, exact in fp32 and in half, so the output must match bit for bit.
