@@ -64,6 +64,9 @@ WORKLOADS = {
         # The same B against 16 rows of A (a small decode batch): the skinny
         # tensor-core path, also bound by reading B once.
         Workload("f16_skinny_16x16384x8192", "f16_nt", 16, 16384, 8192, "uniform", 8, 7),
+        # Few 256 x 256 tiles over a long K (32 tiles, 128 k-blocks): the
+        # shape class the K split over two CTA pairs per cluster serves.
+        Workload("f16_ksplit_1024x2048x8192", "f16_nt", 1024, 2048, 8192, "uniform", 10, 11),
     ]
 }
 
