@@ -29,12 +29,18 @@ def _lib():
 # sixth two CTA pairs sharing B (K = 1016: rows off the 128-byte grid), whose
 # stages also wait for the other pair's multicast; the last the skinny kernel
 # with 4 clusters per tile, whose parts still meet in the workspace after the
-# timeout, and whose tagged counters must not mislead the next call.
+# timeout, and whose tagged counters must not mislead the next call; and two
+# CTA pairs splitting one tile's K (1024 x 2048 x 8192), where pair 0 gives
+# up while pair 1 finishes and publishes its share, and both still meet at
+# the cluster's closing barrier.
 @pytest.mark.parametrize("M,N,K,skip", [(256, 512, 256, 0), (600, 700, 392, 3),
                                         (2560, 2560, 256, 1), (8, 77, 72, 1),
                                         (8, 1000, 4096, 1), (2048, 2048, 1016, 1),
-                                        (8, 512, 32768, 1)])
+                                        (8, 512, 32768, 1), (1024, 2048, 8192, 1)])
 def test_missing_load_times_out_and_context_survives(M, N, K, skip):
+    if (M, N, K) == (1024, 2048, 8192):
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        assert g.gemm_f16_select(M, N, K, sms)[0] == g.GEMM_F16_256x256_KSPLIT
     A = wl.draw_f16((M, K), seed=1)
     B = wl.draw_f16((N, K), seed=2)
     dA, dB = A.cuda(), B.cuda()
