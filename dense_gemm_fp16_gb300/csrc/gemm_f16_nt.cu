@@ -115,9 +115,9 @@ struct PairWork {
     __device__ PairWork(const F16Args &a, int pair, int pairs)
         : num_pairs(pairs), dp_tiles(a.dp_tiles), num_kb(a.num_kb), sk_units(a.sk_units),
           next_dp(pair), u(sk_begin(pairs - 1 - pair)), u_end(sk_begin(pairs - pair)) {}
-    // first stream-K k-block of share rank r
+    // first stream-K k-block of share rank r (no 64-bit division without stream-K work)
     __device__ int sk_begin(int r) const {
-        return static_cast<int>((static_cast<long long>(r) * sk_units) / num_pairs);
+        return sk_units ? static_cast<int>((static_cast<long long>(r) * sk_units) / num_pairs) : 0;
     }
     __device__ bool next(int &tile, int &kb0, int &kb1) {
         if (next_dp < dp_tiles) {
@@ -831,8 +831,11 @@ __global__ void __launch_bounds__((2 + EPI) * 32, 1)
         tmem_alloc_pair(smem_addr(tmem_slot), T::kTmemCols);
         tmem_relinquish_alloc_permit_pair();
     }
+    // This CTA's TMEM address and flags, then both CTAs' barriers initialised
+    // (released by fence.mbarrier_init) and TMEM allocated in both.
     tc_fence_before_sync();
-    cluster_sync();  // barriers of both CTAs initialised, TMEM allocated in both
+    __syncthreads();
+    cluster_sync_relaxed();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
     pdl_launch_dependents();
@@ -847,6 +850,7 @@ __global__ void __launch_bounds__((2 + EPI) * 32, 1)
             uint32_t phase = 0;
             bool ok = true;
             bool first_tile = true;
+            int filled = 0;  // every slot starts free: the first STAGES loads need no wait
             PairWork work(args, pair, num_pairs);
             int tile, kb0, kb1;
             while (ok && work.next(tile, kb0, kb1)) {
@@ -858,7 +862,9 @@ __global__ void __launch_bounds__((2 + EPI) * 32, 1)
                 const int b_row = nt * BN + static_cast<int>(rank) * 128 +
                                   (CL == 4 && !KS ? 64 * static_cast<int>(pic) : 0);
                 for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!mbar_wait_cluster(empty_bar(stage), phase ^ 1u, args.timeout_ns, abort_flag)) {
+                    if (filled < STAGES) {
+                        ++filled;
+                    } else if (!mbar_wait_cluster(empty_bar(stage), phase ^ 1u, args.timeout_ns, abort_flag)) {
                         ok = false;
                         break;
                     }
@@ -1079,7 +1085,12 @@ __global__ void __launch_bounds__((2 + EPI) * 32, 1)
             }
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(mapa_shared(acce_bar(b), lead));
+            // The MMA issuer waits for this buffer only before a later tile:
+            // after the last one nothing is sent, so no arrival on the even
+            // CTA can still be in flight when the pair leaves.
+            PairWork more = work;
+            int t2, k0, k1;
+            if (lane == 0 && more.next(t2, k0, k1)) mbar_arrive_cluster(mapa_shared(acce_bar(b), lead));
         }
         if constexpr (RES) {
             // Residual loads still in flight (only after an abort) land before
@@ -1095,7 +1106,8 @@ __global__ void __launch_bounds__((2 + EPI) * 32, 1)
 
     tc_fence_before_sync();
     __syncthreads();
-    if (*abort_flag) {
+    const bool aborted = *abort_flag != 0;
+    if (aborted) {
         // The even CTA waits for the last phase armed on each stage (it counts
         // both CTAs' bytes) and for every MMA it issued; the odd CTA's copies
         // complete on those same barriers.
@@ -1114,8 +1126,16 @@ __global__ void __launch_bounds__((2 + EPI) * 32, 1)
         __syncthreads();
     }
     // Neither CTA may leave while the other can still touch its shared memory
-    // (remote arrivals, pair TMA completions, pair MMA operand reads).
-    cluster_sync();
+    // (remote arrivals, pair TMA completions, pair MMA operand reads).  On the
+    // normal path every such operation has completed on an mbarrier the other
+    // CTA waited on (the last tile sends no drained-accumulator arrival; the
+    // K-split partner's share was acquired and read), so the barrier only
+    // orders execution.  After an abort an arrival may still be in flight, and
+    // the releasing form orders it first.
+    if (aborted)
+        cluster_sync();
+    else
+        cluster_sync_relaxed();
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc_pair(tmem_base, T::kTmemCols);

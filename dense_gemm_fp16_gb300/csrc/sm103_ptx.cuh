@@ -203,6 +203,17 @@ __device__ __forceinline__ void cluster_sync() {
         "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// The same barrier, ordering execution only: the arrive releases nothing, so
+// whatever another CTA must see has to be released before it (barrier
+// initialisation by fence.mbarrier_init.release.cluster) or be carried by an
+// mbarrier that CTA has already waited on.  Measured ~0.5 us cheaper than the
+// releasing form at kernel start and ~0.4 us at kernel end.
+__device__ __forceinline__ void cluster_sync_relaxed() {
+    asm volatile(
+        "barrier.cluster.arrive.relaxed.aligned;\n\t"
+        "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // try_wait with cluster-scope acquire: for barriers that threads or the
 // tensor core of the peer CTA arrive on.
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
