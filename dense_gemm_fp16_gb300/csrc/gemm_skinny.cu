@@ -410,7 +410,10 @@ __global__ void __launch_bounds__(kSkThreads, 1)
                     if (n + j < nend) out[j] = skinny_out(args.epi, s4[j], m, n + j, args.N);
             }
         }
-        cluster_sync();  // no CTA leaves while another still reads its share
+        // No CTA leaves while another still reads its share.  Those reads have
+        // returned their values (they feed the stores above) before a CTA
+        // arrives, so the barrier only has to order execution.
+        cluster_sync_relaxed();
     }
     if (warp == 1) {
         tc_fence_after_sync();
