@@ -804,6 +804,31 @@ __global__ void __launch_bounds__((2 + EPI) * 32, 1)
             if (pic) kb0 += h; else kb1 = kb0 + h;
         }
     };
+    // The boxes of this CTA's first ring fill are asked of L2 before the
+    // set-up and the dependent-launch wait, one per lane of warp 3, so that the
+    // first loads find them there instead of waiting on DRAM (-0.9 us per
+    // launch at 5376 x 5376 x 2048).  A prefetch only fills L2, which is where
+    // a previous kernel's writes land too, so it cannot make a later load see
+    // stale data.
+    if (warp == 3 && lane < 2 * STAGES) {
+        PairWork first(args, pair, num_pairs);
+        int tile, kb0, kb1;
+        if (first.next(tile, kb0, kb1)) {
+            k_half(kb0, kb1);
+            const int kb = kb0 + (lane >> 1);
+            if (kb < kb1) {
+                int mt, nt;
+                tile_mn(tile, args, mt, nt);
+                mt = pair_row(mt);
+                if (lane & 1)
+                    tma_prefetch_l2_2d(&tmB, kb * kBK,
+                                       nt * BN + static_cast<int>(rank) * 128 +
+                                           (CL == 4 && !KS ? 64 * static_cast<int>(pic) : 0));
+                else
+                    tma_prefetch_l2_2d(&tmA, kb * kBK, mt * 256 + static_cast<int>(rank) * 128);
+            }
+        }
+    }
 
     if (threadIdx.x == 0) {
         tma_prefetch_desc(&tmA);

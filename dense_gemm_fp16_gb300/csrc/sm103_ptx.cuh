@@ -91,6 +91,15 @@ __device__ __forceinline__ void tma_prefetch_desc(const void *desc) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(desc)) : "memory");
 }
 
+// Ask L2 for the box at coordinates (c0 innermost, c1): a hint that fills L2
+// and writes nothing else, so values read later are never affected by it.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const void *desc, int c0, int c1) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(desc)),
+                 "r"(c0), "r"(c1)
+                 : "memory");
+}
+
 // Load the box at coordinates (c0 innermost, c1) into shared memory `dst`.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *desc, uint32_t bar, int c0,
                                             int c1) {
