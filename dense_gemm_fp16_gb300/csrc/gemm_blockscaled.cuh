@@ -169,6 +169,19 @@ __global__ void __launch_bounds__((2 + EW) * 32, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
+    // The A and B boxes of this CTA's first ring fill are asked of L2 before
+    // the set-up and the dependent-launch wait, one per lane of warp 2.  A
+    // prefetch only fills L2, where a previous kernel's writes land too.
+    if (args.prefetch_first && warp == 2 && lane < 2 * STAGES && lane / 2 < args.num_kb &&
+        static_cast<int>(blockIdx.x) < args.m_tiles * args.n_tiles) {
+        const int mt = static_cast<int>(blockIdx.x) % args.m_tiles;
+        const int nt = static_cast<int>(blockIdx.x) / args.m_tiles;
+        if (lane & 1)
+            tma_prefetch_l2_2d(&tmB, (lane >> 1) * kMxBK, nt * BN);
+        else
+            tma_prefetch_l2_2d(&tmA, (lane >> 1) * kMxBK, mt * kBM);
+    }
+
     if (threadIdx.x == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
@@ -753,6 +766,8 @@ inline F16Args mx_args(const MxLaunch &L, int tile_rows, int BN, int num_kb) {
     args.m_tiles = (L.M + tile_rows - 1) / tile_rows;
     args.n_tiles = (L.N + BN - 1) / BN;
     args.num_kb = num_kb;
+    // operand bytes: one per E4M3 element, one per E2M1 pair
+    args.prefetch_first = (static_cast<size_t>(L.M) + L.N) * static_cast<size_t>(L.K) / (L.fmt == kFmtNv4 ? 2 : 1) >= kPrefetchMinBytes;
     args.vec_store = (L.N % 8 == 0) && ((reinterpret_cast<uintptr_t>(L.C) & 15u) == 0);
     args.tma_store = args.vec_store;
     EpiSpec scale;

@@ -177,6 +177,12 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     const int kb0 = share * args.kb_per_split;
     const int kb1 = kb0 + args.kb_per_split < args.num_kb ? kb0 + args.kb_per_split : args.num_kb;
 
+    // The B boxes of this CTA's first ring fill are asked of L2 before the
+    // set-up and the dependent-launch wait, one per lane of warp 2, so the
+    // stream from DRAM starts earlier.  A prefetch only fills L2, where a
+    // previous kernel's writes land too.
+    if (warp == 2 && lane < STAGES && kb0 + lane < kb1) tma_prefetch_l2_2d(&tmB, (kb0 + lane) * kSkBK, row0);
+
     if (threadIdx.x == 0) {
         tma_prefetch_desc(&tmB);
         tma_prefetch_desc(&tmA);
