@@ -34,7 +34,12 @@
  *    C must not overlap A or B.
  *  - Asynchrony: work is enqueued on `stream` (a cudaStream_t; NULL means
  *    the legacy default stream) on the calling thread's current device.  The
- *    call returns once the work is enqueued; it does not synchronise.
+ *    call returns once the work is enqueued; it does not synchronise.  Stream
+ *    order holds: the fp16, matrix-vector and block-scaled kernels are
+ *    launched as programmatic dependents, so their set-up (and an L2
+ *    prefetch of their first operand boxes, which changes no value) may
+ *    overlap the end of the previous kernel on the stream, but they read A
+ *    and B and write C only after that kernel has completed.
  *  - Errors: the return value is a gemm_status.  On any non-OK status nothing
  *    was enqueued, and gemm_last_error() gives a message.  Faults found on
  *    the device (a bounded wait inside a kernel that ran out) are reported by
