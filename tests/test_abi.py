@@ -263,7 +263,7 @@ def test_f16_selector_rule_over_a_shape_grid(lib):
 def test_skinny_plan(lib):
     # Worked cases on 152 SMs: (shares, rows per group, groups, k-blocks a share).
     assert g.gemm_debug_skinny_plan(1, 8192, 8192, 152) == (2, 128, 64, 64)
-    assert g.gemm_debug_skinny_plan(1, 16384, 8192, 152) == (1, 128, 128, 128)  # no room to split
+    assert g.gemm_debug_skinny_plan(1, 16384, 8192, 152) == (1, 112, 147, 128)  # no room to split: rows spread
     assert g.gemm_debug_skinny_plan(1, 4096, 4096, 152) == (4, 128, 32, 16)
     assert g.gemm_debug_skinny_plan(1, 1000, 12008, 152) == (8, 128, 8, 12)     # 188 k-blocks, 2 parts
     assert g.gemm_debug_skinny_parts(1, 1000, 12008, 152) == 2
@@ -291,8 +291,9 @@ def test_skinny_plan_properties(lib):
     # Against the rule itself, over a grid of shapes: the shares a power of
     # two up to 8, each at least 8 k-blocks, their CTAs within the slots, and
     # the next power of two breaking one of these; groups of 128 rows unless
-    # 128-row groups need several waves, then the multiple of 8 that fills
-    # that many waves; groups and k-blocks covering N and K.
+    # 128-row groups need several waves (then the multiple of 8 that fills
+    # that many waves) or fill more than half but not all of the slots (then
+    # the multiple of 8 that fills them); groups and k-blocks covering N and K.
     for N in (1, 127, 128, 129, 1000, 4096, 8192, 16384, 19456, 19457, 28672):
         for K in (0, 8, 64, 512, 520, 4096, 12008, 65536):
             for ctas in (1, 19, 152, 304):
@@ -303,8 +304,12 @@ def test_skinny_plan_properties(lib):
                 if s > 1:
                     assert tiles * s <= ctas and nkb // s >= 8
                 assert 2 * s > 8 or tiles * 2 * s > ctas or nkb // (2 * s) < 8
-                if s > 1 or tiles <= ctas:
+                if s > 1 or tiles == ctas or 2 * tiles <= ctas:
                     assert rows == 128
+                elif tiles < ctas:
+                    # fewer groups than slots, more than half: rows spread over the slots
+                    assert rows % 8 == 0 and rows <= 128 and rows * ctas >= N
+                    assert rows - 8 < -(-N // ctas)
                 else:
                     waves = -(-tiles // ctas)
                     assert rows % 8 == 0 and rows <= 128 and rows * waves * ctas >= N
